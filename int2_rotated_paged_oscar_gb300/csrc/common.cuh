@@ -1,0 +1,201 @@
+// Device helpers shared by the OSCAR kernels (sm_103a).
+//
+// Everything here is hand-written inline PTX or plain CUDA: mbarrier phase
+// waits (always bounded by %globaltimer so a lost copy can never hang the GPU),
+// non-multicast bulk global->shared copies, warp-level f16 MMA, and the
+// magic-number unpack of 2-bit codes into f16 pairs.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "oscar_internal.h"
+
+namespace oscar {
+
+__device__ __forceinline__ void flag_error(int* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, giving up after
+// kWaitLimitNs.  On give-up the status word gets OSCAR_DEV_TIMEOUT and false
+// is returned; callers then stop issuing work and drain.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      flag_error(status, kDevTimeout);
+      return false;
+    }
+  }
+}
+
+// Non-multicast bulk copy global -> this CTA's shared memory, completion
+// signalled on an mbarrier (complete_tx).  Both addresses 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ------------------------------------------------------------------ PDL
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ MMA
+// D = A(16x16, row) * B(16x8, col) + D, f16 inputs, f32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------ code unpack
+// A 32-bit word holds 8 slot pairs: slot x has one code at bits 2x and one at
+// bits 16+2x.  Slots 0..4 are read in place (positions 0,2,4,6,8), slots 5..7
+// after a right shift by 6 (positions 4,6,8).  OR-ing a code c sitting at
+// mantissa bits [pos, pos+2) into the f16 pattern of 1.0 gives 1 + c*2^(pos-10)
+// exactly; subtracting 1.0 leaves c * 2^(pos-10), also exact.  The 2^(10-pos)
+// factor is folded into the other MMA operand (query side) or into the final
+// per-channel scaling (value side).
+__host__ __device__ constexpr int slot_pos(int x) { return x < 5 ? 2 * x : 2 * x - 6; }
+
+__device__ __forceinline__ uint32_t hsub2_one(uint32_t v) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x3C003C00u));
+  return r;
+}
+
+template <int X>
+__device__ __forceinline__ uint32_t unpack_slot(uint32_t w, uint32_t w6) {
+  constexpr int pos = slot_pos(X);
+  constexpr uint32_t mask = (3u << pos) | (3u << (16 + pos));
+  const uint32_t src = X < 5 ? w : w6;
+  return hsub2_one((src & mask) | 0x3C003C00u);
+}
+
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t (&o)[8]) {
+  const uint32_t w6 = w >> 6;
+  o[0] = unpack_slot<0>(w, w6);
+  o[1] = unpack_slot<1>(w, w6);
+  o[2] = unpack_slot<2>(w, w6);
+  o[3] = unpack_slot<3>(w, w6);
+  o[4] = unpack_slot<4>(w, w6);
+  o[5] = unpack_slot<5>(w, w6);
+  o[6] = unpack_slot<6>(w, w6);
+  o[7] = unpack_slot<7>(w, w6);
+}
+
+// BF16 variant: bfloat16 keeps 7 stored mantissa bits, so codes are read at
+// positions 0, 2, 4 only: slots 0..2 in place, 3..5 after >> 6, 6..7 after
+// >> 12.  (1.0 | c << pos) - 1.0 = c * 2^(pos-7), exact in bfloat16.
+__host__ __device__ constexpr int slot_pos_bf16(int x) { return x < 3 ? 2 * x : (x < 6 ? 2 * (x - 3) : 2 * (x - 6)); }
+
+__device__ __forceinline__ uint32_t bsub2_one(uint32_t v) {
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x3F803F80u));
+  return r;
+}
+
+template <int X>
+__device__ __forceinline__ uint32_t unpack_slot_bf16(uint32_t w, uint32_t w6, uint32_t w12) {
+  constexpr int pos = slot_pos_bf16(X);
+  constexpr uint32_t mask = (3u << pos) | (3u << (16 + pos));
+  const uint32_t src = X < 3 ? w : (X < 6 ? w6 : w12);
+  return bsub2_one((src & mask) | 0x3F803F80u);
+}
+
+__device__ __forceinline__ void unpack_word_bf16(uint32_t w, uint32_t (&o)[8]) {
+  const uint32_t w6 = w >> 6, w12 = w >> 12;
+  o[0] = unpack_slot_bf16<0>(w, w6, w12);
+  o[1] = unpack_slot_bf16<1>(w, w6, w12);
+  o[2] = unpack_slot_bf16<2>(w, w6, w12);
+  o[3] = unpack_slot_bf16<3>(w, w6, w12);
+  o[4] = unpack_slot_bf16<4>(w, w6, w12);
+  o[5] = unpack_slot_bf16<5>(w, w6, w12);
+  o[6] = unpack_slot_bf16<6>(w, w6, w12);
+  o[7] = unpack_slot_bf16<7>(w, w6, w12);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo_elem, float hi_elem) {
+  __half2 h = __floats2half2_rn(lo_elem, hi_elem);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float lo_elem, float hi_elem) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo_elem, hi_elem);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float ex2(float x) { return exp2f(x); }
+
+__device__ __forceinline__ float warp_max_xor(float v, int lane_mask) {
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, lane_mask));
+}
+
+}  // namespace oscar

@@ -1,0 +1,688 @@
+// Host runtime and C ABI of the OSCAR INT2 paged KV cache (see include/oscar.h).
+//
+// Owns: configuration validation, the page allocator (refcounts, free list,
+// branch-point prefix forks with copy-on-write of the partial page), decode
+// planning (split sizes, workspace carve-up), the device status word, optional
+// per-kernel event timing, and the kernel launches on the caller's stream.
+// No exception crosses the ABI; errors are status codes plus a thread-local
+// message.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/oscar.h"
+#include "oscar_internal.h"
+
+using oscar::DecodeArgs;
+using oscar::DecodeWs;
+using oscar::Geom;
+using oscar::WriteArgs;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+oscar_status fail(oscar_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+oscar_status cuda_fail(int err, const char* what) {
+  return fail(OSCAR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(static_cast<cudaError_t>(err)));
+}
+
+struct Timing {
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending;
+  double ms = 0.0;
+  int launches = 0;
+};
+
+}  // namespace
+
+struct oscar_ctx {
+  Geom g{};
+  uint8_t* pool = nullptr;
+  uint16_t* slab = nullptr;
+  int* d_status = nullptr;
+  std::mutex mu;
+  std::vector<int32_t> refcount;
+  std::vector<int32_t> free_stack;  // top = back
+  long long alloc_fail_after = -1;  // fault injection (OSCAR_FAULT_ALLOC_FAIL_AFTER)
+  long long allocs_done = 0;
+  bool timing = false;
+  std::map<std::string, Timing> timers;
+  std::vector<cudaEvent_t> event_pool;
+  long long launches = 0;
+};
+
+namespace {
+
+bool is_pow2_in(int v, std::initializer_list<int> allowed) {
+  for (int a : allowed)
+    if (v == a) return true;
+  return false;
+}
+
+oscar_status validate(const oscar_config* c, Geom* out) {
+  if (!c) return fail(OSCAR_ERR_INVALID, "config is null");
+  if (c->num_layers < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 || c->max_requests < 1 ||
+      c->max_pages_per_req < 1 || c->num_pages < 1 || c->sink < 0 || c->recent < 1)
+    return fail(OSCAR_ERR_INVALID, "config has a non-positive size");
+  if (c->n_q_heads % c->n_kv_heads)
+    return fail(OSCAR_ERR_UNSUPPORTED, "n_q_heads (%d) is not a multiple of n_kv_heads (%d)", c->n_q_heads,
+                c->n_kv_heads);
+  const int gq = c->n_q_heads / c->n_kv_heads;
+  if (!is_pow2_in(gq, {1, 2, 4, 8})) return fail(OSCAR_ERR_UNSUPPORTED, "GQA ratio %d not in {1,2,4,8}", gq);
+  if (!is_pow2_in(c->head_dim, {64, 128})) return fail(OSCAR_ERR_UNSUPPORTED, "head_dim %d not in {64,128}", c->head_dim);
+  if (!is_pow2_in(c->page_size, {16, 32, 64}))
+    return fail(OSCAR_ERR_UNSUPPORTED, "page_size %d not in {16,32,64}", c->page_size);
+  if (c->group_size != 32) return fail(OSCAR_ERR_UNSUPPORTED, "group_size %d is not 32", c->group_size);
+  if ((long long)c->max_pages_per_req * c->page_size > (1LL << 30))
+    return fail(OSCAR_ERR_INVALID, "max_pages_per_req * page_size too large");
+  Geom g;
+  g.L = c->num_layers;
+  g.Hq = c->n_q_heads;
+  g.Hkv = c->n_kv_heads;
+  g.D = c->head_dim;
+  g.P = c->page_size;
+  g.G = c->group_size;
+  g.S = c->sink;
+  g.W = c->recent;
+  g.max_req = c->max_requests;
+  g.max_pages_per_req = c->max_pages_per_req;
+  g.num_pages = c->num_pages;
+  *out = g;
+  return OSCAR_OK;
+}
+
+// --------------------------------------------------------------- tracing
+cudaEvent_t take_event(oscar_ctx* ctx) {
+  if (!ctx->event_pool.empty()) {
+    cudaEvent_t e = ctx->event_pool.back();
+    ctx->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+struct LaunchScope {
+  oscar_ctx* ctx;
+  const char* name;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr, b = nullptr;
+  LaunchScope(oscar_ctx* c, const char* n, void* stream) : ctx(c), name(n), s(static_cast<cudaStream_t>(stream)) {
+    if (ctx->timing) {
+      a = take_event(ctx);
+      b = take_event(ctx);
+      if (a) cudaEventRecord(a, s);
+    }
+  }
+  void done(int err) {
+    if (err == 0) ctx->launches++;
+    if (ctx->timing && a && b) {
+      cudaEventRecord(b, s);
+      ctx->timers[name].pending.push_back({a, b});
+    }
+  }
+};
+
+oscar_status need_device(oscar_ctx* ctx) {
+  if (!ctx) return fail(OSCAR_ERR_INVALID, "context is null");
+  if (!ctx->pool || !ctx->slab || !ctx->d_status)
+    return fail(OSCAR_ERR_INVALID, "context was created without device buffers");
+  return OSCAR_OK;
+}
+
+oscar_status check_layer(const oscar_ctx* ctx, int32_t layer) {
+  if (layer < 0 || layer >= ctx->g.L) return fail(OSCAR_ERR_INVALID, "layer %d out of [0, %d)", layer, ctx->g.L);
+  return OSCAR_OK;
+}
+
+}  // namespace
+
+// ====================================================================== planning
+namespace oscar {
+
+DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
+  DecodeWs w{};
+  const int gq = g.Hq / g.Hkv;
+  w.nt = gq == 8 ? 2 : 1;
+  const int stage_pages = bf16_pool ? 1 : 64 / g.P;
+  long long max_pages;
+  if (bf16_pool) max_pages = max_seq > 0 ? (max_seq - 1) / g.P + 1 : 0;
+  else max_pages = (max_seq - g.W > g.S) ? (long long)(max_seq - g.W - 1) / g.P + 1 : 0;
+  const long long target_ctas = 152LL * 4;
+  const long long total = (long long)batch * g.Hkv * max_pages;
+  long long pps = (total + target_ctas - 1) / target_ctas;
+  if (pps < stage_pages) pps = stage_pages;
+  pps = (pps + stage_pages - 1) / stage_pages * stage_pages;
+  long long splits = max_pages > 0 ? (max_pages + pps - 1) / pps : 0;
+  while (splits > 1023) {
+    pps += stage_pages;
+    splits = (max_pages + pps - 1) / pps;
+  }
+  w.pages_per_split = static_cast<int>(pps);
+  w.max_splits = static_cast<int>(splits);
+  auto align = [](size_t x) { return (x + 255) & ~size_t(255); };
+  size_t off = 0;
+  w.qfrag_off = off;
+  off = align(off + (size_t)batch * g.Hkv * w.nt * (g.D / 16) * 32 * 8);
+  w.qaux_off = off;
+  off = align(off + (size_t)batch * g.Hq * 8 * sizeof(float));
+  w.qplain_off = off;
+  off = align(off + (size_t)batch * g.Hq * g.D * sizeof(float));
+  w.part_off = off;
+  const size_t slots = bf16_pool ? (size_t)w.max_splits : (size_t)w.max_splits + 1;
+  off = align(off + (size_t)batch * g.Hq * slots * (g.D + 4) * sizeof(float));
+  w.total = off;
+  return w;
+}
+
+}  // namespace oscar
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* oscar_last_error(void) { return g_last_error.c_str(); }
+
+const char* oscar_version(void) { return "oscar-gb300 0.1 (sm_103a)"; }
+
+size_t oscar_int2_pool_bytes(const oscar_config* cfg) {
+  Geom g;
+  if (validate(cfg, &g) != OSCAR_OK) return 0;
+  return g.pool_bytes();
+}
+
+size_t oscar_window_slab_bytes(const oscar_config* cfg) {
+  Geom g;
+  if (validate(cfg, &g) != OSCAR_OK) return 0;
+  return g.slab_bytes();
+}
+
+size_t oscar_page_block_bytes(const oscar_config* cfg) {
+  Geom g;
+  if (validate(cfg, &g) != OSCAR_OK) return 0;
+  return g.block_bytes();
+}
+
+oscar_status oscar_create(const oscar_config* cfg, void* int2_pool, void* window_slab, oscar_ctx** out) {
+  if (!out) return fail(OSCAR_ERR_INVALID, "out is null");
+  *out = nullptr;
+  Geom g;
+  oscar_status st = validate(cfg, &g);
+  if (st != OSCAR_OK) return st;
+  if ((int2_pool == nullptr) != (window_slab == nullptr))
+    return fail(OSCAR_ERR_INVALID, "pass both device buffers or neither");
+  if (int2_pool && (reinterpret_cast<uintptr_t>(int2_pool) & 15))
+    return fail(OSCAR_ERR_INVALID, "int2_pool must be 16-byte aligned");
+  oscar_ctx* ctx = new (std::nothrow) oscar_ctx();
+  if (!ctx) return fail(OSCAR_ERR_OOM, "host allocation failed");
+  ctx->g = g;
+  ctx->pool = static_cast<uint8_t*>(int2_pool);
+  ctx->slab = static_cast<uint16_t*>(window_slab);
+  ctx->refcount.assign(g.num_pages, 0);
+  ctx->free_stack.reserve(g.num_pages);
+  for (int i = g.num_pages - 1; i >= 0; --i) ctx->free_stack.push_back(i);  // lowest id first
+  if (const char* f = std::getenv("OSCAR_FAULT_ALLOC_FAIL_AFTER")) ctx->alloc_fail_after = std::atoll(f);
+  if (int2_pool) {
+    cudaError_t e = cudaMalloc(&ctx->d_status, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(ctx->d_status, 0, sizeof(int));
+    if (e != cudaSuccess) {
+      if (ctx->d_status) cudaFree(ctx->d_status);
+      delete ctx;
+      return cuda_fail(e, "status word");
+    }
+  }
+  *out = ctx;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_destroy(oscar_ctx* ctx) {
+  if (!ctx) return OSCAR_OK;
+  for (auto& kv : ctx->timers)
+    for (auto& p : kv.second.pending) {
+      cudaEventDestroy(p.first);
+      cudaEventDestroy(p.second);
+    }
+  for (auto e : ctx->event_pool) cudaEventDestroy(e);
+  if (ctx->d_status) cudaFree(ctx->d_status);
+  delete ctx;
+  return OSCAR_OK;
+}
+
+// ---------------------------------------------------------------- allocator
+oscar_status oscar_alloc_pages(oscar_ctx* ctx, int32_t n, int32_t* out_ids) {
+  if (!ctx || (n > 0 && !out_ids) || n < 0) return fail(OSCAR_ERR_INVALID, "bad arguments to oscar_alloc_pages");
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  if ((size_t)n > ctx->free_stack.size())
+    return fail(OSCAR_ERR_OOM, "page pool exhausted: %d requested, %zu free", n, ctx->free_stack.size());
+  if (ctx->alloc_fail_after >= 0 && ctx->allocs_done + n > ctx->alloc_fail_after)
+    return fail(OSCAR_ERR_OOM, "page allocation failed (fault injection after %lld pages)", ctx->alloc_fail_after);
+  for (int i = 0; i < n; ++i) {
+    const int32_t id = ctx->free_stack.back();
+    ctx->free_stack.pop_back();
+    ctx->refcount[id] = 1;
+    out_ids[i] = id;
+  }
+  ctx->allocs_done += n;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_ref_pages(oscar_ctx* ctx, const int32_t* ids, int32_t n) {
+  if (!ctx || (n > 0 && !ids) || n < 0) return fail(OSCAR_ERR_INVALID, "bad arguments to oscar_ref_pages");
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  for (int i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= ctx->g.num_pages || ctx->refcount[ids[i]] <= 0)
+      return fail(OSCAR_ERR_INVALID, "page %d is not allocated", ids[i]);
+  for (int i = 0; i < n; ++i) ctx->refcount[ids[i]]++;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_unref_pages(oscar_ctx* ctx, const int32_t* ids, int32_t n) {
+  if (!ctx || (n > 0 && !ids) || n < 0) return fail(OSCAR_ERR_INVALID, "bad arguments to oscar_unref_pages");
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  std::map<int32_t, int> dec;
+  for (int i = 0; i < n; ++i) {
+    if (ids[i] < 0 || ids[i] >= ctx->g.num_pages) return fail(OSCAR_ERR_INVALID, "page %d out of range", ids[i]);
+    dec[ids[i]]++;
+  }
+  for (auto& kv : dec)
+    if (ctx->refcount[kv.first] < kv.second)
+      return fail(OSCAR_ERR_INVALID, "page %d released more often than referenced", kv.first);
+  for (auto& kv : dec) {
+    ctx->refcount[kv.first] -= kv.second;
+    if (ctx->refcount[kv.first] == 0) ctx->free_stack.push_back(kv.first);
+  }
+  return OSCAR_OK;
+}
+
+oscar_status oscar_page_refcount(oscar_ctx* ctx, int32_t id, int32_t* out_refcount) {
+  if (!ctx || !out_refcount || id < 0 || id >= ctx->g.num_pages)
+    return fail(OSCAR_ERR_INVALID, "bad arguments to oscar_page_refcount");
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  *out_refcount = ctx->refcount[id];
+  return OSCAR_OK;
+}
+
+oscar_status oscar_free_page_count(oscar_ctx* ctx, int32_t* out_n) {
+  if (!ctx || !out_n) return fail(OSCAR_ERR_INVALID, "bad arguments to oscar_free_page_count");
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  *out_n = static_cast<int32_t>(ctx->free_stack.size());
+  return OSCAR_OK;
+}
+
+int32_t oscar_pages_needed(const oscar_config* cfg, int32_t seq_len) {
+  Geom g;
+  if (validate(cfg, &g) != OSCAR_OK || seq_len < 0) return -1;
+  const int h_end = seq_len - g.W;
+  if (h_end <= g.S) return 0;
+  return (h_end - 1) / g.P + 1;
+}
+
+oscar_status oscar_fork_prefix(oscar_ctx* ctx, const int32_t* src_bt, int32_t* dst_bt, int32_t n, int32_t src_slot,
+                               int32_t dst_slot, void* stream) {
+  if (!ctx || !src_bt || !dst_bt) return fail(OSCAR_ERR_INVALID, "bad arguments to oscar_fork_prefix");
+  const Geom& g = ctx->g;
+  if (n < 0 || (long long)n > (long long)g.max_pages_per_req * g.P)
+    return fail(OSCAR_ERR_INVALID, "prefix length %d out of range", n);
+  if (src_slot < 0 || src_slot >= g.max_req || dst_slot < 0 || dst_slot >= g.max_req || src_slot == dst_slot)
+    return fail(OSCAR_ERR_INVALID, "bad request slots %d -> %d", src_slot, dst_slot);
+  const int h_end = n - g.W > g.S ? n - g.W : 0;  // history covers [S, h_end)
+  const int full = h_end / g.P;
+  const bool partial = h_end % g.P != 0;
+  for (int i = 0; i < full + (partial ? 1 : 0); ++i)
+    if (src_bt[i] < 0 || src_bt[i] >= g.num_pages) return fail(OSCAR_ERR_INVALID, "source page %d unmapped", i);
+  int32_t fresh = -1;
+  if (partial) {
+    oscar_status st = oscar_alloc_pages(ctx, 1, &fresh);
+    if (st != OSCAR_OK) return st;
+  }
+  if (full > 0) {
+    oscar_status st = oscar_ref_pages(ctx, src_bt, full);
+    if (st != OSCAR_OK) {
+      if (partial) oscar_unref_pages(ctx, &fresh, 1);
+      return st;
+    }
+  }
+  for (int i = 0; i < g.max_pages_per_req; ++i) dst_bt[i] = -1;
+  for (int i = 0; i < full; ++i) dst_bt[i] = src_bt[i];
+  if (partial) dst_bt[full] = fresh;
+  if (ctx->pool) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t blk = (size_t)g.Hkv * g.block_bytes();
+    for (int l = 0; l < g.L; ++l) {
+      cudaError_t e = cudaSuccess;
+      if (partial)
+        e = cudaMemcpyAsync(ctx->pool + l * g.layer_pool_bytes() + (size_t)fresh * blk,
+                            ctx->pool + l * g.layer_pool_bytes() + (size_t)src_bt[full] * blk, blk,
+                            cudaMemcpyDeviceToDevice, s);
+      if (e == cudaSuccess) {
+        const size_t req = g.slab_req_elems();
+        e = cudaMemcpyAsync(ctx->slab + ((size_t)l * g.max_req + dst_slot) * req,
+                            ctx->slab + ((size_t)l * g.max_req + src_slot) * req, req * 2, cudaMemcpyDeviceToDevice, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "fork copy");
+    }
+  }
+  return OSCAR_OK;
+}
+
+// ---------------------------------------------------------------- write path
+static oscar_status write_common(oscar_ctx* ctx, int32_t layer, const void* K, const void* V, int32_t dtype,
+                                 const int32_t* cu_seqlens, const int32_t* start_pos, int32_t batch,
+                                 int32_t total_tokens, const float* R_K, const float* R_V, float clip_K,
+                                 float clip_V, const int32_t* block_table, int32_t bt_stride, const int32_t* req_slot,
+                                 void* stream, int hadamard) {
+  oscar_status st = need_device(ctx);
+  if (st != OSCAR_OK) return st;
+  if ((st = check_layer(ctx, layer)) != OSCAR_OK) return st;
+  if (batch < 0 || total_tokens < 0 || bt_stride < 1) return fail(OSCAR_ERR_INVALID, "bad batch/total/bt_stride");
+  if (batch == 0) return OSCAR_OK;
+  if (!cu_seqlens || !start_pos || !block_table || !req_slot || (total_tokens > 0 && (!K || !V)))
+    return fail(OSCAR_ERR_INVALID, "null tensor argument");
+  if (!hadamard && (!R_K || !R_V)) return fail(OSCAR_ERR_INVALID, "R_K / R_V are null");
+  if (dtype != OSCAR_DTYPE_BF16 && dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad dtype %d", dtype);
+  if (!(clip_K > 0.f) || !(clip_V > 0.f)) return fail(OSCAR_ERR_INVALID, "clip thresholds must be positive");
+  WriteArgs a{};
+  a.g = ctx->g;
+  a.layer = layer;
+  a.K = K;
+  a.V = V;
+  a.dtype = dtype;
+  a.cu_seqlens = cu_seqlens;
+  a.start_pos = start_pos;
+  a.batch = batch;
+  a.total_tokens = total_tokens;
+  a.R_K = R_K;
+  a.R_V = R_V;
+  a.clip_K = clip_K;
+  a.clip_V = clip_V;
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.req_slot = req_slot;
+  a.pool = ctx->pool;
+  a.slab = ctx->slab;
+  a.status = ctx->d_status;
+  a.hadamard = hadamard;
+  {
+    LaunchScope ls(ctx, "evict", stream);
+    int e = oscar::launch_evict(a, stream);
+    ls.done(e);
+    if (e) return cuda_fail(e, "evict launch");
+  }
+  LaunchScope ls(ctx, "write", stream);
+  int e = oscar::launch_write(a, stream);
+  ls.done(e);
+  if (e) return cuda_fail(e, "write launch");
+  return OSCAR_OK;
+}
+
+oscar_status oscar_write_kv(oscar_ctx* ctx, int32_t layer, const void* K, const void* V, int32_t dtype,
+                            const int32_t* cu_seqlens, const int32_t* start_pos, int32_t batch, int32_t total_tokens,
+                            const float* R_K, const float* R_V, float clip_K, float clip_V,
+                            const int32_t* block_table, int32_t bt_stride, const int32_t* req_slot, void* stream) {
+  return write_common(ctx, layer, K, V, dtype, cu_seqlens, start_pos, batch, total_tokens, R_K, R_V, clip_K, clip_V,
+                      block_table, bt_stride, req_slot, stream, 0);
+}
+
+oscar_status oscar_write_kv_hadamard(oscar_ctx* ctx, int32_t layer, const void* K, const void* V, int32_t dtype,
+                                     const int32_t* cu_seqlens, const int32_t* start_pos, int32_t batch,
+                                     int32_t total_tokens, float clip_K, float clip_V, const int32_t* block_table,
+                                     int32_t bt_stride, const int32_t* req_slot, void* stream) {
+  return write_common(ctx, layer, K, V, dtype, cu_seqlens, start_pos, batch, total_tokens, nullptr, nullptr, clip_K,
+                      clip_V, block_table, bt_stride, req_slot, stream, 1);
+}
+
+oscar_status oscar_append_step(oscar_ctx* ctx, int32_t layer, const void* K_new, const void* V_new, int32_t dtype,
+                               const int32_t* seq_lens_before, int32_t batch, const float* R_K, const float* R_V,
+                               float clip_K, float clip_V, const int32_t* block_table, int32_t bt_stride,
+                               const int32_t* req_slot, void* stream) {
+  oscar_status st = need_device(ctx);
+  if (st != OSCAR_OK) return st;
+  if ((st = check_layer(ctx, layer)) != OSCAR_OK) return st;
+  if (batch < 0 || bt_stride < 1) return fail(OSCAR_ERR_INVALID, "bad batch/bt_stride");
+  if (batch == 0) return OSCAR_OK;
+  if (!K_new || !V_new || !seq_lens_before || !R_K || !R_V || !block_table || !req_slot)
+    return fail(OSCAR_ERR_INVALID, "null tensor argument");
+  if (dtype != OSCAR_DTYPE_BF16 && dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad dtype %d", dtype);
+  if (!(clip_K > 0.f) || !(clip_V > 0.f)) return fail(OSCAR_ERR_INVALID, "clip thresholds must be positive");
+  WriteArgs a{};
+  a.g = ctx->g;
+  a.layer = layer;
+  a.K = K_new;
+  a.V = V_new;
+  a.dtype = dtype;
+  a.start_pos = seq_lens_before;
+  a.batch = batch;
+  a.R_K = R_K;
+  a.R_V = R_V;
+  a.clip_K = clip_K;
+  a.clip_V = clip_V;
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.req_slot = req_slot;
+  a.pool = ctx->pool;
+  a.slab = ctx->slab;
+  a.status = ctx->d_status;
+  LaunchScope ls(ctx, "append", stream);
+  int e = oscar::launch_append(a, stream);
+  ls.done(e);
+  if (e) return cuda_fail(e, "append launch");
+  return OSCAR_OK;
+}
+
+// ---------------------------------------------------------------- decode
+oscar_status oscar_decode_workspace_size(const oscar_config* cfg, int32_t batch, int32_t max_seq, size_t* bytes) {
+  Geom g;
+  oscar_status st = validate(cfg, &g);
+  if (st != OSCAR_OK) return st;
+  if (!bytes || batch < 0 || max_seq < 0) return fail(OSCAR_ERR_INVALID, "bad arguments to workspace size");
+  *bytes = oscar::plan_decode(g, batch, max_seq, false).total;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_bf16_decode_workspace_size(const oscar_config* cfg, int32_t batch, int32_t max_seq,
+                                              size_t* bytes) {
+  Geom g;
+  oscar_status st = validate(cfg, &g);
+  if (st != OSCAR_OK) return st;
+  if (!bytes || batch < 0 || max_seq < 0) return fail(OSCAR_ERR_INVALID, "bad arguments to workspace size");
+  *bytes = oscar::plan_decode(g, batch, max_seq, true).total;
+  return OSCAR_OK;
+}
+
+static oscar_status decode_common_checks(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
+                                         int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
+                                         const int32_t* seq_lens, int32_t batch, int32_t max_seq, void* workspace) {
+  oscar_status st = need_device(ctx);
+  if (st != OSCAR_OK) return st;
+  if ((st = check_layer(ctx, layer)) != OSCAR_OK) return st;
+  if (batch < 0 || bt_stride < 1 || max_seq < 0) return fail(OSCAR_ERR_INVALID, "bad batch/bt_stride/max_seq");
+  if ((long long)max_seq > (long long)ctx->g.max_pages_per_req * ctx->g.P)
+    return fail(OSCAR_ERR_INVALID, "max_seq %d exceeds max_pages_per_req * page_size", max_seq);
+  if (batch == 0) return OSCAR_OK;
+  if (!q || !out || !block_table || !seq_lens || !workspace) return fail(OSCAR_ERR_INVALID, "null tensor argument");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(OSCAR_ERR_INVALID, "workspace must be 256-byte aligned");
+  if (q_dtype != OSCAR_DTYPE_BF16 && q_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad q dtype");
+  if (out_dtype != OSCAR_DTYPE_BF16 && out_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad out dtype");
+  return OSCAR_OK;
+}
+
+oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
+                               int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
+                               const int32_t* seq_lens, const int32_t* req_slot, int32_t batch, int32_t max_seq,
+                               int32_t sink, int32_t recent, const float* R_K, const float* R_V, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  oscar_status st = decode_common_checks(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens,
+                                         batch, max_seq, workspace);
+  if (st != OSCAR_OK || batch == 0) return st;
+  if (sink != ctx->g.S || recent != ctx->g.W)
+    return fail(OSCAR_ERR_INVALID, "sink/recent (%d, %d) differ from the cache configuration (%d, %d)", sink, recent,
+                ctx->g.S, ctx->g.W);
+  if (!req_slot || !R_K || !R_V) return fail(OSCAR_ERR_INVALID, "null tensor argument");
+  DecodeArgs a{};
+  a.g = ctx->g;
+  a.layer = layer;
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.seq_lens = seq_lens;
+  a.req_slot = req_slot;
+  a.batch = batch;
+  a.max_seq = max_seq;
+  a.R_K = R_K;
+  a.R_V = R_V;
+  a.pool = ctx->pool;
+  a.slab = ctx->slab;
+  a.status = ctx->d_status;
+  a.ws = static_cast<uint8_t*>(workspace);
+  a.wl = oscar::plan_decode(ctx->g, batch, max_seq, false);
+  if (ws_bytes < a.wl.total)
+    return fail(OSCAR_ERR_INVALID, "workspace too small: %zu < %zu bytes", ws_bytes, a.wl.total);
+  const bool pdl = !ctx->timing;  // timing events between launches would break the programmatic overlap
+  {
+    LaunchScope ls(ctx, "q_rotate", stream);
+    int e = oscar::launch_q_rotate(a, stream);
+    ls.done(e);
+    if (e) return cuda_fail(e, "q_rotate launch");
+  }
+  {
+    LaunchScope ls(ctx, "decode_splitk", stream);
+    int e = oscar::launch_decode_splitk(a, stream, pdl);
+    ls.done(e);
+    if (e) return cuda_fail(e, "decode_splitk launch");
+  }
+  LaunchScope ls(ctx, "decode_combine", stream);
+  int e = oscar::launch_decode_combine(a, stream, pdl);
+  ls.done(e);
+  if (e) return cuda_fail(e, "decode_combine launch");
+  return OSCAR_OK;
+}
+
+oscar_status oscar_bf16_decode_attn(oscar_ctx* ctx, int32_t layer, const void* bf16_pool, const void* q,
+                                    int32_t q_dtype, void* out, int32_t out_dtype, const int32_t* block_table,
+                                    int32_t bt_stride, const int32_t* seq_lens, int32_t batch, int32_t max_seq,
+                                    void* workspace, size_t ws_bytes, void* stream) {
+  oscar_status st = decode_common_checks(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens,
+                                         batch, max_seq, workspace);
+  if (st != OSCAR_OK || batch == 0) return st;
+  if (!bf16_pool) return fail(OSCAR_ERR_INVALID, "bf16_pool is null");
+  if (reinterpret_cast<uintptr_t>(bf16_pool) & 15) return fail(OSCAR_ERR_INVALID, "bf16_pool must be 16-byte aligned");
+  if (ctx->g.P != 64) return fail(OSCAR_ERR_UNSUPPORTED, "the BF16 comparison kernel needs page_size 64");
+  DecodeArgs a{};
+  a.g = ctx->g;
+  a.layer = layer;
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.max_seq = max_seq;
+  a.bf16_pool = static_cast<const uint8_t*>(bf16_pool);
+  a.status = ctx->d_status;
+  a.ws = static_cast<uint8_t*>(workspace);
+  a.wl = oscar::plan_decode(ctx->g, batch, max_seq, true);
+  if (ws_bytes < a.wl.total)
+    return fail(OSCAR_ERR_INVALID, "workspace too small: %zu < %zu bytes", ws_bytes, a.wl.total);
+  const bool pdl = !ctx->timing;
+  {
+    LaunchScope ls(ctx, "bf16_prepare", stream);
+    int e = oscar::launch_bf16_prepare(a, stream);
+    ls.done(e);
+    if (e) return cuda_fail(e, "bf16_prepare launch");
+  }
+  {
+    LaunchScope ls(ctx, "bf16_decode", stream);
+    int e = oscar::launch_bf16_decode(a, stream, pdl);
+    ls.done(e);
+    if (e) return cuda_fail(e, "bf16_decode launch");
+  }
+  LaunchScope ls(ctx, "bf16_combine", stream);
+  int e = oscar::launch_bf16_combine(a, stream, pdl);
+  ls.done(e);
+  if (e) return cuda_fail(e, "bf16_combine launch");
+  return OSCAR_OK;
+}
+
+// ---------------------------------------------------------------- status, tracing
+oscar_status oscar_check_status(oscar_ctx* ctx, void* stream, int32_t* out_bits) {
+  oscar_status st = need_device(ctx);
+  if (st != OSCAR_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int bits = 0;
+  e = cudaMemcpy(&bits, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (out_bits) *out_bits = bits;
+  if (bits) {
+    cudaMemset(ctx->d_status, 0, sizeof(int));
+    return fail(OSCAR_ERR_DEVICE, "device status 0x%x (%s%s%s)", bits, (bits & oscar::kDevBadPage) ? "bad page " : "",
+                (bits & oscar::kDevTimeout) ? "wait timeout " : "", (bits & oscar::kDevBadLen) ? "bad length " : "");
+  }
+  return OSCAR_OK;
+}
+
+oscar_status oscar_set_timing(oscar_ctx* ctx, int32_t enable) {
+  if (!ctx) return fail(OSCAR_ERR_INVALID, "context is null");
+  ctx->timing = enable != 0;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_kernel_time(oscar_ctx* ctx, const char* name, double* out_ms, int32_t* out_launches) {
+  if (!ctx || !name || !out_ms || !out_launches) return fail(OSCAR_ERR_INVALID, "bad arguments to oscar_kernel_time");
+  Timing& t = ctx->timers[name];
+  for (auto& p : t.pending) {
+    cudaError_t e = cudaEventSynchronize(p.second);
+    if (e != cudaSuccess) return cuda_fail(e, "event synchronize");
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, p.first, p.second);
+    t.ms += ms;
+    t.launches++;
+    ctx->event_pool.push_back(p.first);
+    ctx->event_pool.push_back(p.second);
+  }
+  t.pending.clear();
+  *out_ms = t.ms;
+  *out_launches = t.launches;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_reset_timing(oscar_ctx* ctx) {
+  if (!ctx) return fail(OSCAR_ERR_INVALID, "context is null");
+  for (auto& kv : ctx->timers) {
+    for (auto& p : kv.second.pending) {
+      cudaEventSynchronize(p.second);
+      ctx->event_pool.push_back(p.first);
+      ctx->event_pool.push_back(p.second);
+    }
+    kv.second.pending.clear();
+    kv.second.ms = 0.0;
+    kv.second.launches = 0;
+  }
+  return OSCAR_OK;
+}
+
+int64_t oscar_launch_count(oscar_ctx* ctx) { return ctx ? ctx->launches : 0; }
+
+}  // extern "C"

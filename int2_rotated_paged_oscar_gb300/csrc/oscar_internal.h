@@ -1,0 +1,111 @@
+// Internal declarations shared by the host runtime and the CUDA kernels.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define OSCAR_HD __host__ __device__
+#else
+#define OSCAR_HD
+#endif
+
+namespace oscar {
+
+constexpr int kDevBadPage = 1;
+constexpr int kDevTimeout = 2;
+constexpr int kDevBadLen = 4;
+constexpr int kDevBadSlot = 8;
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;  // 200 ms per barrier wait
+
+constexpr int kDtypeF32 = 0;
+constexpr int kDtypeBF16 = 1;
+
+// Cache geometry (validated copy of oscar_config).
+struct Geom {
+  int L, Hq, Hkv, D, P, G, S, W, max_req, max_pages_per_req, num_pages;
+  OSCAR_HD int gq() const { return Hq / Hkv; }
+  OSCAR_HD size_t row_bytes() const { return (size_t)D / 4; }
+  OSCAR_HD size_t sz_bytes() const { return 4 * (size_t)(D / G); }
+  OSCAR_HD size_t k_sz_off() const { return (size_t)P * row_bytes(); }
+  OSCAR_HD size_t v_codes_off() const { return k_sz_off() + (size_t)P * sz_bytes(); }
+  OSCAR_HD size_t v_sz_off() const { return v_codes_off() + (size_t)P * row_bytes(); }
+  OSCAR_HD size_t block_bytes() const { return v_sz_off() + (size_t)P * sz_bytes(); }
+  OSCAR_HD size_t layer_pool_bytes() const { return (size_t)num_pages * Hkv * block_bytes(); }
+  OSCAR_HD size_t pool_bytes() const { return (size_t)L * layer_pool_bytes(); }
+  OSCAR_HD int window() const { return S + W; }
+  // bf16 elements of one (layer, request slot) window region: [Hkv][2][S+W][D]
+  OSCAR_HD size_t slab_req_elems() const { return (size_t)Hkv * 2 * window() * D; }
+  OSCAR_HD size_t slab_bytes() const { return (size_t)L * max_req * slab_req_elems() * 2; }
+};
+
+// Arguments of the write family (prefill / extend, eviction, append).
+struct WriteArgs {
+  Geom g;
+  int layer;
+  const void* K;
+  const void* V;
+  int dtype;
+  const int* cu_seqlens;   // [batch+1] (write) or null (append)
+  const int* start_pos;    // [batch] (write) / seq_lens_before (append)
+  int batch;
+  int total_tokens;
+  const float* R_K;
+  const float* R_V;
+  float clip_K, clip_V;
+  const int* block_table;
+  int bt_stride;
+  const int* req_slot;
+  uint8_t* pool;
+  uint16_t* slab;
+  int* status;
+  int hadamard;            // 1: rotation is H_Had . P_br computed by a fast Walsh-Hadamard transform
+};
+
+// Decode workspace carve-up (offsets in bytes from the workspace base).
+struct DecodeWs {
+  size_t qfrag_off, qaux_off, qplain_off, part_off, total;
+  int max_splits;        // INT2 splits per (request, kv head); grid.x = max_splits + 1 (x = 0 is the window)
+  int pages_per_split;   // multiple of 64 / page_size
+  int nt;                // query n-tiles (max(1, 2*gq/8))
+};
+
+struct DecodeArgs {
+  Geom g;
+  int layer;
+  const void* q;
+  int q_dtype;
+  void* out;
+  int out_dtype;
+  const int* block_table;
+  int bt_stride;
+  const int* seq_lens;
+  const int* req_slot;
+  int batch;
+  int max_seq;
+  const float* R_K;
+  const float* R_V;
+  const uint8_t* pool;       // whole pool (all layers)
+  const uint16_t* slab;      // whole slab (all layers)
+  const uint8_t* bf16_pool;  // comparison kernel: whole BF16 pool
+  int* status;
+  uint8_t* ws;
+  DecodeWs wl;
+  int v_prescale_exp;        // softmax weights times 2^v_prescale_exp before the f16 split
+};
+
+// Host-side planning (pure functions, no CUDA).
+DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool);
+int v_prescale_exponent_for_clip(float clip_v);
+
+// Kernel launchers (return cudaError_t as int).  Each launches on `stream`.
+int launch_write(const WriteArgs& a, void* stream);
+int launch_evict(const WriteArgs& a, void* stream);
+int launch_append(const WriteArgs& a, void* stream);
+int launch_q_rotate(const DecodeArgs& a, void* stream);
+int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl);
+int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl);
+int launch_bf16_prepare(const DecodeArgs& a, void* stream);
+int launch_bf16_decode(const DecodeArgs& a, void* stream, bool pdl);
+int launch_bf16_combine(const DecodeArgs& a, void* stream, bool pdl);
+
+}  // namespace oscar

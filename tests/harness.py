@@ -1,0 +1,199 @@
+"""Test helpers: drive the CUDA path through the C ABI and compare with the oracle.
+
+Only tests import this module.  Oracle outputs may feed the CUDA path (for
+example an oracle-built cache image uploaded for decode parity); nothing from
+the CUDA path ever feeds the oracle.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+import synthetic as syn
+from oracle import attention, cache, quant, rotation
+
+# decode tolerance on unit-scale outputs (errors divided by the RMS of the oracle output)
+DECODE_MAX_ABS = 2e-3
+DECODE_MEAN_ABS = 2e-4
+# near-boundary rule for packed codes
+BOUNDARY_REL = 1e-6
+EXEMPT_FRACTION = 1e-4
+
+
+def torch_mod():
+    import torch
+    return torch
+
+
+def geometry(shape: syn.Shape, num_pages: int, max_requests: int, num_layers: int = 1) -> cache.Geometry:
+    return cache.Geometry(num_layers, shape.n_kv_heads, shape.head_dim, shape.page_size, shape.group_size,
+                          shape.sink, shape.recent, num_pages, max_requests)
+
+
+def fixture(wl: syn.Workload, layer: int = 0, n_cal: int = 256, u_identity: bool = False) -> dict:
+    q = syn.queries(wl, layer, n_cal, calib=True)
+    k, v = syn.kv_tokens(wl, layer, n_cal, calib=True)
+    return rotation.layer_fixture(q, k, v, u_identity=u_identity)
+
+
+@dataclass
+class GpuCache:
+    """Device buffers + context for one cache geometry."""
+    cfg: object
+    ctx: int
+    pool: object
+    slab: object
+    geom: cache.Geometry
+
+    def close(self):
+        import int2_rotated_paged_oscar_gb300 as osc
+        osc.oscar_destroy(self.ctx)
+
+    def pool_np(self) -> np.ndarray:
+        g = self.geom
+        return self.pool.cpu().numpy().reshape(g.num_layers, g.num_pages, g.n_kv_heads, g.block_bytes)
+
+    def slab_np(self) -> np.ndarray:
+        g = self.geom
+        return self.slab.cpu().numpy().view(np.uint16).reshape(
+            g.num_layers, g.max_requests, g.n_kv_heads, 2, g.window, g.head_dim)
+
+    def upload(self, img: cache.CacheImage):
+        torch = torch_mod()
+        self.pool.copy_(torch.from_numpy(img.pool.reshape(-1)))
+        self.slab.copy_(torch.from_numpy(img.slab.reshape(-1).view(np.int16)))
+
+
+def make_gpu_cache(geom: cache.Geometry, n_q_heads: int, max_pages_per_req: int, fill: int = 0) -> GpuCache:
+    torch = torch_mod()
+    import int2_rotated_paged_oscar_gb300 as osc
+    cfg = osc.make_config(num_layers=geom.num_layers, n_q_heads=n_q_heads, n_kv_heads=geom.n_kv_heads,
+                          head_dim=geom.head_dim, page_size=geom.page_size, group_size=geom.group_size,
+                          sink=geom.sink, recent=geom.recent, max_requests=geom.max_requests,
+                          max_pages_per_req=max_pages_per_req, num_pages=geom.num_pages)
+    nbytes = osc.oscar_int2_pool_bytes(cfg)
+    assert nbytes == geom.num_layers * geom.num_pages * geom.n_kv_heads * geom.block_bytes
+    pool = torch.full((nbytes,), fill, dtype=torch.uint8, device="cuda")
+    slab = torch.zeros((osc.oscar_window_slab_bytes(cfg) // 2,), dtype=torch.int16, device="cuda")
+    ctx = osc.oscar_create(cfg, pool, slab)
+    return GpuCache(cfg, ctx, pool, slab, geom)
+
+
+def dev(x, dtype=None):
+    torch = torch_mod()
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def dev_input(x: np.ndarray, dtype: str):
+    """Upload float32 input values in their storage type (bf16 bit patterns or float32)."""
+    torch = torch_mod()
+    if dtype == "bf16":
+        bits = syn.to_bf16_bits(x)
+        return torch.from_numpy(bits.view(np.int16)).cuda()
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+
+
+def dtype_code(dtype: str) -> int:
+    import int2_rotated_paged_oscar_gb300 as osc
+    return osc.DTYPE_BF16 if dtype == "bf16" else osc.DTYPE_F32
+
+
+# ------------------------------------------------------------------ write parity with the near-boundary rule
+def _near_bf16_boundary(x: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """True where x lies within 1e-6 * max(|x|, ref) of a BF16 rounding boundary.
+
+    ref is the group's scale: a rotated value carries an absolute error set by the
+    magnitude of the group's values, so a group minimum close to zero is judged on
+    the scale of its group, the same reference the per-element rule uses.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    w = BOUNDARY_REL * np.maximum(np.abs(x), np.asarray(ref, dtype=np.float64))
+    return quant.bf16_round(x + w) != quant.bf16_round(x - w)
+
+
+def _near_code_boundary(y: np.ndarray, scale: np.ndarray, zero: np.ndarray, group: int) -> np.ndarray:
+    d = y.shape[-1]
+    yg = y.reshape(y.shape[:-1] + (d // group, group))
+    s = scale[..., None]
+    z = zero[..., None]
+    near = np.zeros(yg.shape, dtype=bool)
+    for k in range(3):
+        yb = z + (k + 0.5) * s
+        near |= np.abs(yg - yb) <= BOUNDARY_REL * np.maximum(np.abs(yb), s)
+    return near.reshape(y.shape)
+
+
+def compare_history(gpu_pool: np.ndarray, geom: cache.Geometry, layer: int, diag: dict) -> dict:
+    """Check GPU history rows against the oracle write diagnostics; returns counts, raises on violation."""
+    if "k" not in diag:
+        return {"elements": 0, "exempt": 0}
+    gimg = cache.CacheImage(geom)
+    gimg.pool = gpu_pool
+    ck, sk, zk, cv, sv, zv = gimg.read_history(layer, diag["pages"], diag["slots"])
+    total, exempt_list = 0, []
+    for name, qd, gc, gs, gz in (("K", diag["k"], ck, sk, zk), ("V", diag["v"], cv, sv, zv)):
+        y = qd["y"]
+        same_sz = (gs == qd["scale"]) & (gz == qd["zero"])
+        group_exempt = _near_bf16_boundary(qd["mn"], qd["rng3"]) | _near_bf16_boundary(qd["rng3"], qd["rng3"])
+        bad_groups = ~same_sz & ~group_exempt
+        if bad_groups.any():
+            idx = np.argwhere(bad_groups)[:5]
+            raise AssertionError(f"{name}: scale/zero differ outside the boundary rule at {idx.tolist()}")
+        # expected codes: oracle codes where (s, z) agree, else re-quantised with the GPU's own (s, z)
+        want = np.where(np.repeat(same_sz, geom.group_size, axis=-1), qd["codes"],
+                        quant.quantize_with(y, gs, gz, geom.group_size))
+        near = _near_code_boundary(y, gs, gz, geom.group_size)
+        diff = gc != want
+        bad = diff & ~near
+        if bad.any():
+            idx = np.argwhere(bad)[:5]
+            raise AssertionError(f"{name}: {int(bad.sum())} codes differ away from a rounding boundary, e.g. "
+                                 f"{idx.tolist()}")
+        total += gc.size
+        for i in np.argwhere(diff & near):
+            exempt_list.append((name, int(diag["b"][i[0]]), int(diag["t"][i[0]]), int(i[1]), int(i[2])))
+        for i in np.argwhere(~same_sz):
+            exempt_list.append((name + "-group", int(diag["b"][i[0]]), int(diag["t"][i[0]]), int(i[1]), int(i[2])))
+    assert len(exempt_list) <= EXEMPT_FRACTION * max(total, 1) + 1, f"too many exemptions: {len(exempt_list)}"
+    return {"elements": total, "exempt": len(exempt_list), "list": exempt_list}
+
+
+def compare_window(gpu_slab: np.ndarray, oracle_slab: np.ndarray, layer: int, slots):
+    for s in slots:
+        assert np.array_equal(gpu_slab[layer, s], oracle_slab[layer, s]), f"window slab of request slot {s} differs"
+
+
+def decode_errors(got: np.ndarray, want: np.ndarray):
+    rms = float(np.sqrt(np.mean(np.square(want))))
+    e = np.abs(np.asarray(got, dtype=np.float64) - want) / max(rms, 1e-30)
+    return float(e.max()), float(e.mean())
+
+
+def assert_decode_close(got, want, max_abs=DECODE_MAX_ABS, mean_abs=DECODE_MEAN_ABS):
+    assert np.all(np.isfinite(got)), "non-finite decode output"
+    mx, mn = decode_errors(got, want)
+    assert mx <= max_abs and mn <= mean_abs, f"decode error max {mx:.3e} (<= {max_abs}), mean {mn:.3e} (<= {mean_abs})"
+    return mx, mn
+
+
+def run_decode(gc: GpuCache, layer, q: np.ndarray, q_dtype: str, bt: np.ndarray, seq_lens, req_slot, fx,
+               max_seq=None, out_bf16=False):
+    torch = torch_mod()
+    import int2_rotated_paged_oscar_gb300 as osc
+    b = q.shape[0]
+    max_seq = int(max(seq_lens)) if max_seq is None else max_seq
+    ws_bytes = osc.oscar_decode_workspace_size(gc.cfg, b, max_seq)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    qd = dev_input(q, q_dtype)
+    out = torch.empty((b, q.shape[1], q.shape[2]), dtype=torch.bfloat16 if out_bf16 else torch.float32, device="cuda")
+    bt_d = dev(bt.astype(np.int32))
+    osc.oscar_decode_attn(gc.ctx, layer, qd, dtype_code(q_dtype), out, osc.DTYPE_BF16 if out_bf16 else osc.DTYPE_F32,
+                          bt_d, bt.shape[1], dev(np.asarray(seq_lens, np.int32)), dev(np.asarray(req_slot, np.int32)),
+                          b, max_seq, gc.geom.sink, gc.geom.recent, dev(fx["R_K"]), dev(fx["R_V"]), ws, ws_bytes)
+    status = osc.oscar_check_status(gc.ctx)
+    assert status == 0, f"device status {status}"
+    return out.float().cpu().numpy().astype(np.float64)

@@ -1,0 +1,379 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the same seeded inputs.
+
+Write path: packed codes, scales and zeros bit-exact except elements within
+1e-6 relative of a rounding boundary (at most 1e-4 of the elements, listed);
+window slab bit-exact.  Decode: max abs error <= 2e-3 and mean abs error <=
+2e-4 on unit-scale outputs, given identical packed caches (the oracle's cache
+image is uploaded as the GPU cache).
+"""
+import numpy as np
+import pytest
+
+import synthetic as syn
+from oracle import attention, cache, quant
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def osc():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA GPU is required for -m gpu tests")
+    from int2_rotated_paged_oscar_gb300 import build
+    build.build()
+    import int2_rotated_paged_oscar_gb300 as m
+    m.load()
+    return m
+
+
+def _contiguous_bt(batch, pages_per_req, offset=0):
+    return (offset + np.arange(batch * pages_per_req, dtype=np.int32)).reshape(batch, pages_per_req)
+
+
+def _prefill_both(osc, wl, fx, lens, bt, num_pages, max_requests=None, start=None, fill=0):
+    """Prefill requests with lengths `lens` on both sides; returns (gpu cache, oracle image, diag, k, v)."""
+    s = wl.shape
+    b = len(lens)
+    geom = H.geometry(s, num_pages, max_requests or b)
+    img = cache.CacheImage(geom, fill=fill)
+    gc = H.make_gpu_cache(geom, s.n_q_heads, bt.shape[1], fill=fill)
+    ks, vs = [], []
+    for i, n in enumerate(lens):
+        k, v = syn.kv_tokens(wl, 0, n, sub=i)
+        ks.append(k)
+        vs.append(v)
+    k = np.concatenate(ks)
+    v = np.concatenate(vs)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    sp = np.zeros(b, np.int32) if start is None else np.asarray(start, np.int32)
+    slots = np.arange(b, dtype=np.int32)
+    diag = cache.write_kv(img, 0, k, v, cu, sp, fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"], bt, slots)
+    osc.oscar_write_kv(gc.ctx, 0, H.dev_input(k, wl.dtype), H.dev_input(v, wl.dtype), H.dtype_code(wl.dtype),
+                       H.dev(cu), H.dev(sp), b, int(cu[-1]), H.dev(fx["R_K"]), H.dev(fx["R_V"]), fx["clip_K"],
+                       fx["clip_V"], H.dev(bt), bt.shape[1], H.dev(slots))
+    assert osc.oscar_check_status(gc.ctx) == 0
+    return gc, img, diag, k, v
+
+
+# ---------------------------------------------------------------------------------------------- write path
+@pytest.mark.parametrize("wl,lens", [
+    (syn.tiny(), [512]),
+    (syn.Workload("d128_ragged", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=1), [1000, 4133, 131, 70]),
+    (syn.Workload("d64_p32_bf16", syn.Shape(8, 2, 64, 32, 32, 4, 16, 1), [0], seed=6), [300, 77]),
+], ids=["tiny_f32", "d128_ragged_bf16", "d64_p32"])
+def test_write_parity(osc, wl, lens):
+    fx = H.fixture(wl)
+    s = wl.shape
+    ppr = max(syn.pages_for(n, s.page_size) for n in lens) + 1
+    bt = _contiguous_bt(len(lens), ppr)
+    gc, img, diag, _, _ = _prefill_both(osc, wl, fx, lens, bt, len(lens) * ppr)
+    try:
+        res = H.compare_history(gc.pool_np(), img.g, 0, diag)
+        H.compare_window(gc.slab_np(), img.slab, 0, range(len(lens)))
+        assert res["elements"] > 0
+    finally:
+        gc.close()
+
+
+def test_write_hadamard_only_parity(osc):
+    """Data-oblivious rotation R = H P (U = I): the FWHT path against the oracle's dense fp32 R."""
+    wl = syn.Workload("had", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=7)
+    fx = H.fixture(wl, u_identity=True)
+    lens = [700, 300]
+    s = wl.shape
+    ppr = 12
+    bt = _contiguous_bt(2, ppr)
+    geom = H.geometry(s, 2 * ppr, 2)
+    img = cache.CacheImage(geom)
+    gc = H.make_gpu_cache(geom, s.n_q_heads, ppr)
+    try:
+        k = np.concatenate([syn.kv_tokens(wl, 0, n, sub=i)[0] for i, n in enumerate(lens)])
+        v = np.concatenate([syn.kv_tokens(wl, 0, n, sub=i)[1] for i, n in enumerate(lens)])
+        cu = np.array([0, lens[0], sum(lens)], np.int32)
+        sp = np.zeros(2, np.int32)
+        slots = np.arange(2, dtype=np.int32)
+        diag = cache.write_kv(img, 0, k, v, cu, sp, fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"], bt, slots)
+        osc.oscar_write_kv_hadamard(gc.ctx, 0, H.dev_input(k, "bf16"), H.dev_input(v, "bf16"), osc.DTYPE_BF16,
+                                    H.dev(cu), H.dev(sp), 2, int(cu[-1]), fx["clip_K"], fx["clip_V"], H.dev(bt), ppr,
+                                    H.dev(slots))
+        assert osc.oscar_check_status(gc.ctx) == 0
+        H.compare_history(gc.pool_np(), geom, 0, diag)
+        H.compare_window(gc.slab_np(), img.slab, 0, range(2))
+    finally:
+        gc.close()
+
+
+def test_append_and_extend_parity(osc):
+    """Prefill, then an extend (evicting ring tokens), then single-token appends, on both sides."""
+    wl = syn.Workload("app", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=8)
+    fx = H.fixture(wl)
+    s = wl.shape
+    ppr = 20
+    lens0 = [300, 140]
+    bt = _contiguous_bt(2, ppr)
+    gc, img, diag0, _, _ = _prefill_both(osc, wl, fx, lens0, bt, 2 * ppr)
+    try:
+        H.compare_history(gc.pool_np(), img.g, 0, diag0)
+        # extend by 90 and 200 tokens
+        ext = [90, 200]
+        k = np.concatenate([syn.kv_tokens(wl, 0, n, sub=10 + i)[0] for i, n in enumerate(ext)])
+        v = np.concatenate([syn.kv_tokens(wl, 0, n, sub=10 + i)[1] for i, n in enumerate(ext)])
+        cu = np.array([0, ext[0], sum(ext)], np.int32)
+        sp = np.array(lens0, np.int32)
+        slots = np.arange(2, dtype=np.int32)
+        diag1 = cache.write_kv(img, 0, k, v, cu, sp, fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"], bt, slots)
+        osc.oscar_write_kv(gc.ctx, 0, H.dev_input(k, "bf16"), H.dev_input(v, "bf16"), osc.DTYPE_BF16, H.dev(cu),
+                           H.dev(sp), 2, int(cu[-1]), H.dev(fx["R_K"]), H.dev(fx["R_V"]), fx["clip_K"], fx["clip_V"],
+                           H.dev(bt), ppr, H.dev(slots))
+        assert osc.oscar_check_status(gc.ctx) == 0
+        H.compare_history(gc.pool_np(), img.g, 0, diag1)
+        H.compare_window(gc.slab_np(), img.slab, 0, range(2))
+        # 40 appends
+        lens = [lens0[0] + ext[0], lens0[1] + ext[1]]
+        for step in range(40):
+            kn, vn = syn.kv_tokens(wl, 0, 2, sub=100 + step)
+            sl = np.array(lens, np.int32)
+            diag = cache.append_step(img, 0, kn, vn, sl, fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"], bt,
+                                     slots)
+            osc.oscar_append_step(gc.ctx, 0, H.dev_input(kn, "bf16"), H.dev_input(vn, "bf16"), osc.DTYPE_BF16,
+                                  H.dev(sl), 2, H.dev(fx["R_K"]), H.dev(fx["R_V"]), fx["clip_K"], fx["clip_V"],
+                                  H.dev(bt), ppr, H.dev(slots))
+            if step % 13 == 0 or step == 39:
+                assert osc.oscar_check_status(gc.ctx) == 0
+                H.compare_history(gc.pool_np(), img.g, 0, diag)
+            lens = [n + 1 for n in lens]
+        assert osc.oscar_check_status(gc.ctx) == 0
+        H.compare_window(gc.slab_np(), img.slab, 0, range(2))
+        # decode after the appends on the GPU's own cache, against the oracle on its own cache
+        q = syn.queries(wl, 0, 2)
+        want = attention.decode(img, 0, q, bt, lens, slots, fx["R_K"], fx["R_V"])
+        got = H.run_decode(gc, 0, q, "bf16", bt, lens, slots, fx)
+        H.assert_decode_close(got, want)
+    finally:
+        gc.close()
+
+
+def test_prefill_plus_appends_equals_direct_prefill_on_gpu(osc):
+    wl = syn.Workload("chain", syn.Shape(16, 8, 128, 64, 32, 4, 128, 1), [0], seed=9)
+    fx = H.fixture(wl)
+    n0, extra = 400, 70
+    ppr = 10
+    bt = _contiguous_bt(1, ppr)
+    k, v = syn.kv_tokens(wl, 0, n0 + extra)
+    geom = H.geometry(wl.shape, ppr, 1)
+    a = H.make_gpu_cache(geom, 16, ppr)
+    b = H.make_gpu_cache(geom, 16, ppr)
+    try:
+        args = (H.dev(fx["R_K"]), H.dev(fx["R_V"]), fx["clip_K"], fx["clip_V"], H.dev(bt), ppr, H.dev(np.zeros(1, np.int32)))
+        osc.oscar_write_kv(a.ctx, 0, H.dev_input(k[:n0], "bf16"), H.dev_input(v[:n0], "bf16"), osc.DTYPE_BF16,
+                           H.dev(np.array([0, n0], np.int32)), H.dev(np.zeros(1, np.int32)), 1, n0, *args)
+        for i in range(extra):
+            osc.oscar_append_step(a.ctx, 0, H.dev_input(k[n0 + i][None], "bf16"), H.dev_input(v[n0 + i][None], "bf16"),
+                                  osc.DTYPE_BF16, H.dev(np.array([n0 + i], np.int32)), 1, *args)
+        osc.oscar_write_kv(b.ctx, 0, H.dev_input(k, "bf16"), H.dev_input(v, "bf16"), osc.DTYPE_BF16,
+                           H.dev(np.array([0, n0 + extra], np.int32)), H.dev(np.zeros(1, np.int32)), 1, n0 + extra,
+                           *args)
+        assert osc.oscar_check_status(a.ctx) == 0 and osc.oscar_check_status(b.ctx) == 0
+        assert np.array_equal(a.pool_np(), b.pool_np())
+        assert np.array_equal(a.slab_np(), b.slab_np())
+    finally:
+        a.close()
+        b.close()
+
+
+# ---------------------------------------------------------------------------------------------- decode
+def _decode_case(osc, wl, lens, q_scale=1.0, shuffle=False, fill=0xFF):
+    """Oracle-built cache uploaded to the GPU; GPU decode vs oracle decode."""
+    fx = H.fixture(wl)
+    s = wl.shape
+    b = len(lens)
+    ppr = max(syn.pages_for(n, s.page_size) for n in lens) + 1
+    num_pages = b * ppr
+    order = syn.page_permutation(wl.seed, num_pages, shuffle=shuffle)
+    bt = order.reshape(b, ppr).astype(np.int32)
+    geom = H.geometry(s, num_pages, b)
+    img = cache.CacheImage(geom, fill=fill)
+    for i, n in enumerate(lens):
+        k, v = syn.kv_tokens(wl, 0, n, sub=i)
+        cache.write_kv(img, 0, k, v, [0, n], [0], fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"], bt[i:i + 1], [i])
+    q = syn.queries(wl, 0, b, scale=q_scale)
+    want = attention.decode(img, 0, q, bt, lens, np.arange(b), fx["R_K"], fx["R_V"])
+    gc = H.make_gpu_cache(geom, s.n_q_heads, ppr)
+    try:
+        gc.upload(img)
+        got = H.run_decode(gc, 0, q, wl.dtype, bt, lens, np.arange(b), fx)
+        return got, want
+    finally:
+        gc.close()
+
+
+@pytest.mark.parametrize("q_scale", [1.0, 0.25])
+def test_decode_parity_tiny(osc, q_scale):
+    got, want = _decode_case(osc, syn.tiny(), [512], q_scale)
+    H.assert_decode_close(got, want)
+
+
+@pytest.mark.parametrize("q_scale", [1.0, 0.25])
+def test_decode_parity_batch1_gq4(osc, q_scale):
+    wl = syn.Workload("b1", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=1)
+    got, want = _decode_case(osc, wl, [6000], q_scale)
+    H.assert_decode_close(got, want)
+
+
+def test_decode_parity_gq8_ragged_shuffled(osc):
+    wl = syn.Workload("b4", syn.Shape(64, 8, 128, 64, 32, 4, 128, 1), [0], seed=2)
+    got, want = _decode_case(osc, wl, [3000, 133, 1029, 64 * 9 + 132], shuffle=True)
+    H.assert_decode_close(got, want)
+
+
+@pytest.mark.parametrize("lens", [[1], [4], [100], [132], [133], [134], [197], [4 + 128 + 64]])
+def test_decode_edge_lengths(osc, lens):
+    """No history, a single history token, history ending exactly at a page boundary."""
+    wl = syn.Workload("edge", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=3)
+    got, want = _decode_case(osc, wl, lens)
+    H.assert_decode_close(got, want)
+
+
+def test_decode_gq1_gq2_d64(osc):
+    for shape in (syn.Shape(4, 4, 64, 16, 32, 4, 32, 1), syn.Shape(8, 4, 64, 32, 32, 2, 20, 1)):
+        wl = syn.Workload("small", shape, [0], seed=4, dtype="f32")
+        got, want = _decode_case(osc, wl, [700, 333])
+        H.assert_decode_close(got, want)
+
+
+def test_decode_independent_of_split_count(osc):
+    """A larger max_seq changes the split plan but not the result (beyond summation order)."""
+    wl = syn.Workload("split", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=5)
+    fx = H.fixture(wl)
+    n = 5000
+    ppr = 200
+    bt = _contiguous_bt(1, ppr)
+    geom = H.geometry(wl.shape, ppr, 1)
+    img = cache.CacheImage(geom)
+    k, v = syn.kv_tokens(wl, 0, n)
+    cache.write_kv(img, 0, k, v, [0, n], [0], fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"], bt, [0])
+    q = syn.queries(wl, 0, 1)
+    gc = H.make_gpu_cache(geom, 32, ppr)
+    try:
+        gc.upload(img)
+        a = H.run_decode(gc, 0, q, "bf16", bt, [n], [0], fx, max_seq=n)
+        b = H.run_decode(gc, 0, q, "bf16", bt, [n], [0], fx, max_seq=ppr * 64)
+        rms = np.sqrt(np.mean(a ** 2))
+        assert np.abs(a - b).max() / rms < 2e-5
+    finally:
+        gc.close()
+
+
+def test_bad_page_sets_status_without_fault(osc):
+    wl = syn.Workload("bad", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=6)
+    fx = H.fixture(wl)
+    geom = H.geometry(wl.shape, 8, 1)
+    gc = H.make_gpu_cache(geom, 32, 8)
+    try:
+        bt = np.array([[0, 1, 2, 99, 4, 5, 6, 7]], np.int32)   # page 99 does not exist
+        import torch
+        ws_bytes = osc.oscar_decode_workspace_size(gc.cfg, 1, 500)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        out = torch.empty((1, 32, 128), dtype=torch.float32, device="cuda")
+        q = H.dev_input(syn.queries(wl, 0, 1), "bf16")
+        osc.oscar_decode_attn(gc.ctx, 0, q, osc.DTYPE_BF16, out, osc.DTYPE_F32, H.dev(bt), 8,
+                              H.dev(np.array([500], np.int32)), H.dev(np.zeros(1, np.int32)), 1, 500, 4, 128,
+                              H.dev(fx["R_K"]), H.dev(fx["R_V"]), ws, ws_bytes)
+        bits = osc.oscar_check_status(gc.ctx)
+        assert bits & osc.DEV_BAD_PAGE
+        assert osc.oscar_check_status(gc.ctx) == 0    # cleared after reading
+        # a sequence length beyond max_seq is flagged, not read
+        osc.oscar_decode_attn(gc.ctx, 0, q, osc.DTYPE_BF16, out, osc.DTYPE_F32, H.dev(bt), 8,
+                              H.dev(np.array([600], np.int32)), H.dev(np.zeros(1, np.int32)), 1, 500, 4, 128,
+                              H.dev(fx["R_K"]), H.dev(fx["R_V"]), ws, ws_bytes)
+        assert osc.oscar_check_status(gc.ctx) & osc.DEV_BAD_LEN
+        with pytest.raises(osc.OscarError):   # sink/recent must match the cache
+            osc.oscar_decode_attn(gc.ctx, 0, q, osc.DTYPE_BF16, out, osc.DTYPE_F32, H.dev(bt), 8,
+                                  H.dev(np.array([500], np.int32)), H.dev(np.zeros(1, np.int32)), 1, 500, 4, 64,
+                                  H.dev(fx["R_K"]), H.dev(fx["R_V"]), ws, ws_bytes)
+    finally:
+        gc.close()
+
+
+# ---------------------------------------------------------------------------------------------- prefix fork
+def test_fork_prefix_then_diverge(osc):
+    wl = syn.Workload("fork", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=7)
+    fx = H.fixture(wl)
+    n_pre, n = 1000, 1700
+    ppr = 30
+    geom = H.geometry(wl.shape, 80, 2)
+    gc = H.make_gpu_cache(geom, 32, ppr)
+    img = cache.CacheImage(geom)
+    try:
+        ids = osc.oscar_alloc_pages(gc.ctx, syn.pages_for(n, 64))
+        bt0 = np.full(ppr, -1, np.int32)
+        bt0[:len(ids)] = ids
+        k, v = syn.kv_tokens(wl, 0, n)
+        k2, v2 = syn.kv_tokens(wl, 0, n, sub=1)
+        args = (H.dev(fx["R_K"]), H.dev(fx["R_V"]), fx["clip_K"], fx["clip_V"])
+        osc.oscar_write_kv(gc.ctx, 0, H.dev_input(k[:n_pre], "bf16"), H.dev_input(v[:n_pre], "bf16"), osc.DTYPE_BF16,
+                           H.dev(np.array([0, n_pre], np.int32)), H.dev(np.zeros(1, np.int32)), 1, n_pre, *args,
+                           H.dev(bt0[None]), ppr, H.dev(np.array([0], np.int32)))
+        import torch
+        torch.cuda.synchronize()
+        bt1 = np.array(osc.oscar_fork_prefix(gc.ctx, bt0, n_pre, 0, 1, ppr, stream=None), np.int32)
+        need = syn.pages_for(n, 64)
+        have = int((bt1 >= 0).sum())
+        bt1[have:need] = osc.oscar_alloc_pages(gc.ctx, need - have)
+        bt = np.stack([bt0, bt1])
+        for i, (kk, vv) in enumerate(((k, v), (k2, v2))):
+            osc.oscar_write_kv(gc.ctx, 0, H.dev_input(kk[n_pre:], "bf16"), H.dev_input(vv[n_pre:], "bf16"),
+                               osc.DTYPE_BF16, H.dev(np.array([0, n - n_pre], np.int32)),
+                               H.dev(np.array([n_pre], np.int32)), 1, n - n_pre, *args, H.dev(bt[i:i + 1]), ppr,
+                               H.dev(np.array([i], np.int32)))
+        assert osc.oscar_check_status(gc.ctx) == 0
+        # oracle: both requests written from scratch (request 1 = shared prefix + its own suffix)
+        k2[:n_pre], v2[:n_pre] = k[:n_pre], v[:n_pre]
+        bt_o = np.stack([np.arange(ppr), ppr + np.arange(ppr)]).astype(np.int32)
+        geom2 = H.geometry(wl.shape, 2 * ppr, 2)
+        img = cache.CacheImage(geom2)
+        for i, (kk, vv) in enumerate(((k, v), (k2, v2))):
+            cache.write_kv(img, 0, kk, vv, [0, n], [0], fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"],
+                           bt_o[i:i + 1], [i])
+        q = syn.queries(wl, 0, 2)
+        want = attention.decode(img, 0, q, bt_o, [n, n], [0, 1], fx["R_K"], fx["R_V"])
+        got = H.run_decode(gc, 0, q, "bf16", bt, [n, n], [0, 1], fx)
+        H.assert_decode_close(got, want)
+    finally:
+        gc.close()
+
+
+# ---------------------------------------------------------------------------------------------- BF16 comparison kernel
+@pytest.mark.parametrize("hq,lens", [(32, [3000]), (64, [700, 64, 1, 1500])])
+def test_bf16_paged_decode_parity(osc, hq, lens):
+    import torch
+    rng = np.random.default_rng(11)
+    hkv, d, p = 8, 128, 64
+    b = len(lens)
+    ppr = max(syn.pages_for(n, p) for n in lens)
+    num_pages = b * ppr + 3
+    wl = syn.Workload("bf", syn.Shape(hq, hkv, d, p, 32, 4, 128, 1), [0], seed=12)
+    pool = np.zeros((1, num_pages, hkv, 2, p, d), np.uint16)
+    bt = (3 + rng.permutation(b * ppr)).astype(np.int32).reshape(b, ppr)
+    for i, n in enumerate(lens):
+        k, v = syn.kv_tokens(wl, 0, n, sub=i)
+        t = np.arange(n)
+        pool[0, bt[i, t // p], :, 0, t % p] = syn.to_bf16_bits(k)
+        pool[0, bt[i, t // p], :, 1, t % p] = syn.to_bf16_bits(v)
+    q = syn.queries(wl, 0, b)
+    want = attention.bf16_paged_decode(pool, 0, q, bt, lens, p)
+    geom = H.geometry(wl.shape, num_pages, b)
+    gc = H.make_gpu_cache(geom, hq, ppr)
+    try:
+        ws_bytes = osc.oscar_bf16_decode_workspace_size(gc.cfg, b, max(lens))
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        out = torch.empty((b, hq, d), dtype=torch.float32, device="cuda")
+        pool_d = torch.from_numpy(pool.reshape(-1).view(np.int16)).cuda()
+        osc.oscar_bf16_decode_attn(gc.ctx, 0, pool_d, H.dev_input(q, "bf16"), osc.DTYPE_BF16, out, osc.DTYPE_F32,
+                                   H.dev(bt), ppr, H.dev(np.asarray(lens, np.int32)), b, max(lens), ws, ws_bytes)
+        assert osc.oscar_check_status(gc.ctx) == 0
+        H.assert_decode_close(out.cpu().numpy().astype(np.float64), want)
+    finally:
+        gc.close()
