@@ -1,0 +1,513 @@
+#!/usr/bin/env python3
+"""Benchmark of the OSCAR INT2 paged decode hot path on GB300.
+
+Workload (N=1): batch-1 decode at 32K context of a Qwen3-8B-shaped attention
+stack: 36 layers x (32 q heads, 8 kv heads, head_dim 128), context 32,768 =
+4 sink + 128 recent BF16 + INT2 history, page 64, group 32.  One step is one
+decode step through all 36 layers: per layer the append (evict the oldest
+recent token into INT2, write the new token) and the fused decode attention
+(q rotation, split-K INT2 + BF16 window attention, combine with R_V^T).  The
+36-layer cache (~1 GB) is larger than L2, so consecutive layers and steps read
+HBM.  Synthetic seeded inputs (see synthetic/), per-layer rotations from the
+offline calibration on synthetic calibration activations.
+
+Printed JSON line: metric / value = effective KV GB/s of the step (bytes the
+step touches: INT2 codes + scales/zeros, BF16 window, q, o and the append's
+reads and writes, divided by the device time), plus decode-only steps/s, the
+in-house BF16 paged decode on the same shapes, the dominant kernel's roofline
+(measured live with CUDA events), the end-to-end figure through the C ABI with
+host buffers, clocks sampled during the timed region, and the CPU oracle
+baseline.  ``--impl reference`` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic as syn  # noqa: E402
+
+METRIC = "INT2 paged decode: effective KV GB/s & % of HBM roofline; decode steps/s vs BF16"
+LAYERS = 36
+N_CTX = 32768
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true")
+    return ap.parse_args()
+
+
+def workload_config(layers):
+    return {"workload": f"batch1_decode_32k_qwen3_8b_attention_x{layers}_layers", "batch": 1, "context": N_CTX,
+            "n_q_heads": 32, "n_kv_heads": 8, "head_dim": 128, "sink": 4, "recent": 128, "page_size": 64,
+            "group_size": 32, "layers_per_step": layers,
+            "l2": f"inputs larger than L2: {layers}-layer INT2 cache read once per step"}
+
+
+# ------------------------------------------------------------------ byte accounting
+def decode_bytes(n, hq=32, hkv=8, d=128, s=4, w=128, out_bytes=4):
+    hist = max(0, n - w - s)
+    window = min(n, s + w)
+    return {"int2": hist * hkv * 2 * (d // 4 + d // 8), "window": window * hkv * 2 * d * 2,
+            "q": hq * d * 2, "o": hq * d * out_bytes}
+
+
+def append_bytes(hkv=8, d=128):
+    # read the evicted BF16 ring token, write its INT2 row, write the new BF16 token, read K_new/V_new
+    return 2 * hkv * (d * 2 + (d // 4 + d // 8) + d * 2 + d * 2)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed (replicas)
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
+class OracleLayer:
+    """One layer of the workload as a CPU oracle cache image (built once, decoded many times)."""
+
+    def __init__(self):
+        from oracle import cache, rotation
+        wl = syn.batch1_32k()
+        s = wl.shape
+        self.n = N_CTX
+        q_cal = syn.queries(wl, 0, 256, calib=True)
+        k_cal, v_cal = syn.kv_tokens(wl, 0, 256, calib=True)
+        self.fx = rotation.layer_fixture(q_cal, k_cal, v_cal)
+        ppr = syn.pages_for(self.n, s.page_size)
+        geom = cache.Geometry(1, s.n_kv_heads, s.head_dim, s.page_size, 32, s.sink, s.recent, ppr, 1)
+        self.img = cache.CacheImage(geom)
+        k, v = syn.kv_tokens(wl, 0, self.n)
+        self.bt = np.arange(ppr, dtype=np.int32)[None]
+        fx = self.fx
+        cache.write_kv(self.img, 0, k, v, [0, self.n], [0], fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"],
+                       self.bt, [0])
+        self.q = syn.queries(wl, 0, 1)
+
+    def decode(self):
+        from oracle import attention
+        return attention.decode(self.img, 0, self.q, self.bt, [self.n], [0], self.fx["R_K"], self.fx["R_V"])
+
+
+def oracle_decode_sample(target_s=15.0, max_reps=50):
+    """Time the CPU oracle's decode of one layer of the workload (a bounded sample)."""
+    layer = OracleLayer()
+    n = layer.n
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        layer.decode()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or reps >= max_reps:
+            break
+    per = el / reps
+    b = sum(decode_bytes(n).values())
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"seconds_per_layer": per, "gbs": b / per / 1e9, "reps": reps, "cores": cores,
+            "sample": f"oracle float64 decode of 1 layer (batch 1, n={n}, 32q/8kv heads, d=128), {reps} reps"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    layer = OracleLayer()
+    for _ in range(args.warmup):
+        layer.decode()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        layer.decode()
+    sec = time.perf_counter() - t0
+    b = sum(decode_bytes(N_CTX).values()) * args.steps
+    value = b / sec / 1e9
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"oracle float64 decode of 1 of the {args.layers} layers (batch 1, n={N_CTX}, 32q/8kv heads, d=128) "
+              "per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000 * sec / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(args.layers),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, world, rank, local):
+    import torch
+    from int2_rotated_paged_oscar_gb300 import build as bld
+    bld.build()
+    import int2_rotated_paged_oscar_gb300 as osc
+    from int2_rotated_paged_oscar_gb300 import calibrate
+
+    torch.cuda.set_device(local)
+    L = args.layers
+    wl = syn.batch1_32k(num_layers=L)
+    s = wl.shape
+    hq, hkv, d, P = s.n_q_heads, s.n_kv_heads, s.head_dim, s.page_size
+    total_steps = args.warmup + args.steps
+    n0 = N_CTX
+    n_final = n0 + 3 * total_steps + 8
+    ppr = syn.pages_for(n_final, P)
+    cfg = osc.make_config(num_layers=L, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, page_size=P, sink=s.sink,
+                          recent=s.recent, max_requests=1, max_pages_per_req=ppr, num_pages=ppr)
+    pool = torch.empty(osc.oscar_int2_pool_bytes(cfg), dtype=torch.uint8, device="cuda")
+    slab = torch.zeros(osc.oscar_window_slab_bytes(cfg) // 2, dtype=torch.int16, device="cuda")
+    ctx = osc.oscar_create(cfg, pool, slab)
+    stream = torch.cuda.current_stream()
+    ids = osc.oscar_alloc_pages(ctx, ppr)
+    bt = torch.tensor([ids], dtype=torch.int32, device="cuda")
+    slot0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    # per-layer calibration (offline) and the prefill of every layer through the write kernel
+    rk, rv, ck, cv = [], [], [], []
+    k_host, v_host = syn.kv_tokens(wl, 0, n0)
+    k_dev = torch.from_numpy(syn.to_bf16_bits(k_host).view(np.int16)).cuda()
+    v_dev = torch.from_numpy(syn.to_bf16_bits(v_host).view(np.int16)).cuda()
+    cu = torch.tensor([0, n0], dtype=torch.int32, device="cuda")
+    for layer in range(L):
+        fx = calibrate.calibrate_layer(syn.queries(wl, layer, 128, calib=True),
+                                       *syn.kv_tokens(wl, layer, 128, calib=True))
+        rk.append(torch.from_numpy(fx["R_K"]).cuda())
+        rv.append(torch.from_numpy(fx["R_V"]).cuda())
+        ck.append(fx["clip_K"])
+        cv.append(fx["clip_V"])
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for layer in range(L):
+        osc.oscar_write_kv(ctx, layer, k_dev, v_dev, osc.DTYPE_BF16, cu, slot0, 1, n0, rk[layer], rv[layer],
+                           ck[layer], cv[layer], bt, ppr, slot0)
+    ev1.record()
+    torch.cuda.synchronize()
+    write_ms = ev0.elapsed_time(ev1)
+    assert osc.oscar_check_status(ctx) == 0
+
+    # per-step inputs: a few distinct q / new-token sets cycled; seq lens per step precomputed
+    nvar = 4
+    qs = [torch.from_numpy(syn.to_bf16_bits(syn.queries(wl, i, L)).view(np.int16)).cuda() for i in range(nvar)]
+    kn = [torch.from_numpy(syn.to_bf16_bits(syn.kv_tokens(wl, i, L, sub=77)[0]).view(np.int16)).cuda()
+          for i in range(nvar)]
+    vn = [torch.from_numpy(syn.to_bf16_bits(syn.kv_tokens(wl, i, L, sub=77)[1]).view(np.int16)).cuda()
+          for i in range(nvar)]
+    lens_dev = torch.arange(n0, n0 + 3 * total_steps + 4, dtype=torch.int32, device="cuda")
+    max_seq = n_final
+    ws_bytes = osc.oscar_decode_workspace_size(cfg, 1, max_seq)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((L, 1, hq, d), dtype=torch.float32, device="cuda")
+    qsz = hq * d * 2
+    kvsz = hkv * d * 2
+    state = {"n": n0}
+
+    def step_ptr(t, row, nbytes):
+        return t.data_ptr() + row * nbytes
+
+    def decode_step(i, append=True):
+        n = state["n"]
+        lb = lens_dev.data_ptr() + 4 * (n - n0)          # seq_lens_before = n
+        la = lb + 4                                       # seq_lens after the append = n + 1
+        qv, kv_, vv = qs[i % nvar], kn[i % nvar], vn[i % nvar]
+        for layer in range(L):
+            if append:
+                osc.oscar_append_step(ctx, layer, step_ptr(kv_, layer, kvsz), step_ptr(vv, layer, kvsz),
+                                      osc.DTYPE_BF16, lb, 1, rk[layer], rv[layer], ck[layer], cv[layer], bt, ppr,
+                                      slot0)
+            osc.oscar_decode_attn(ctx, layer, step_ptr(qv, layer, qsz), osc.DTYPE_BF16, out[layer], osc.DTYPE_F32,
+                                  bt, ppr, la if append else lb, slot0, 1, max_seq, s.sink, s.recent, rk[layer],
+                                  rv[layer], ws, ws_bytes)
+        if append:
+            state["n"] = n + 1
+
+    # ---------------- main timed loop: append + decode through all layers
+    for i in range(args.warmup):
+        decode_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    launches0 = osc.oscar_launch_count(ctx)
+    n_start = state["n"]
+    ev0.record()
+    for i in range(args.steps):
+        decode_step(i)
+    ev1.record()
+    torch.cuda.synchronize()
+    launches = osc.oscar_launch_count(ctx) - launches0
+    barrier(world)
+    step_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    clk = clocks.stop()
+    st = osc.oscar_check_status(ctx)
+    assert st == 0, f"device status {st}"
+    n_mid = n_start + args.steps // 2 + 1
+    db = decode_bytes(n_mid)
+    bytes_step = L * (sum(db.values()) + append_bytes())
+    value_rank = bytes_step / (step_ms * 1e-3) / 1e9
+    # ---------------- decode-only (no append) for the BF16 comparison, and the per-kernel roofline
+    for i in range(3):
+        decode_step(i, append=False)
+    torch.cuda.synchronize()
+    ev0.record()
+    for i in range(args.steps):
+        decode_step(i, append=False)
+    ev1.record()
+    torch.cuda.synchronize()
+    dec_only_ms = ev0.elapsed_time(ev1) / args.steps
+    osc.oscar_set_timing(ctx, True)
+    osc.oscar_reset_timing(ctx)
+    for i in range(args.steps):
+        decode_step(i, append=False)
+    torch.cuda.synchronize()
+    kms, kl = osc.oscar_kernel_time(ctx, "decode_splitk")
+    qms, _ = osc.oscar_kernel_time(ctx, "q_rotate")
+    cms, _ = osc.oscar_kernel_time(ctx, "decode_combine")
+    osc.oscar_set_timing(ctx, False)
+    kern_avg_ms = kms / max(kl, 1)
+    dbk = decode_bytes(state["n"])
+    kern_bytes = dbk["int2"] + dbk["window"] + dbk["q"]
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    achieved = kern_bytes / (kern_avg_ms * 1e-3) / 1e9
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "decode_splitk_traffic.json")
+    if os.path.exists(tr_path):
+        tr = json.load(open(tr_path))
+        if tr.get("kernel_version") == osc.oscar_version():
+            traffic = tr.get("bytes_per_launch")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "traffic": traffic, "kernel": "decode_splitk", "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": kern_bytes, "avg_launch_us": kern_avg_ms * 1e3,
+                "q_rotate_avg_us": qms / max(kl, 1) * 1e3, "combine_avg_us": cms / max(kl, 1) * 1e3}
+
+    # ---------------- in-house BF16 paged decode on the same shapes (decode only)
+    bf16_info = None
+    if not args.no_bf16:
+        bpages = syn.pages_for(state["n"] + 8, P)
+        bpool = torch.zeros((L, bpages, hkv, 2, P, d), dtype=torch.int16, device="cuda")
+        tok = state["n"]
+        kk = k_dev.view(n0, hkv, d)
+        vv = v_dev.view(n0, hkv, d)
+        full = (n0 // P) * P
+        for layer in range(L):
+            bpool[layer, : full // P, :, 0] = kk[:full].view(full // P, P, hkv, d).permute(0, 2, 1, 3)
+            bpool[layer, : full // P, :, 1] = vv[:full].view(full // P, P, hkv, d).permute(0, 2, 1, 3)
+        bbt = torch.arange(bpages, dtype=torch.int32, device="cuda")[None]
+        bws_bytes = osc.oscar_bf16_decode_workspace_size(cfg, 1, tok)
+        bws = torch.empty(bws_bytes, dtype=torch.uint8, device="cuda")
+        bcfg = osc.make_config(num_layers=L, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, page_size=P, sink=s.sink,
+                               recent=s.recent, max_requests=1, max_pages_per_req=bpages, num_pages=bpages)
+        bctx = osc.oscar_create(bcfg, pool, slab)   # geometry for the BF16 pool (INT2 buffers unused here)
+        blen = torch.tensor([tok], dtype=torch.int32, device="cuda")
+
+        def bf16_step(i):
+            for layer in range(L):
+                osc.oscar_bf16_decode_attn(bctx, layer, bpool, step_ptr(qs[i % nvar], layer, qsz), osc.DTYPE_BF16,
+                                           out[layer], osc.DTYPE_F32, bbt, bpages, blen, 1, tok, bws, bws_bytes)
+        for i in range(3):
+            bf16_step(i)
+        torch.cuda.synchronize()
+        ev0.record()
+        for i in range(args.steps):
+            bf16_step(i)
+        ev1.record()
+        torch.cuda.synchronize()
+        bf16_ms = ev0.elapsed_time(ev1) / args.steps
+        assert osc.oscar_check_status(bctx) == 0
+        osc.oscar_destroy(bctx)
+        bf16_bytes = L * (tok * hkv * 2 * d * 2 + hq * d * 2 + hq * d * 4)
+        bf16_info = {"steps_per_s": 1000.0 / bf16_ms, "ms_per_step": bf16_ms,
+                     "effective_gbs": bf16_bytes / (bf16_ms * 1e-3) / 1e9,
+                     "int2_decode_only_ms_per_step": dec_only_ms,
+                     "int2_decode_only_steps_per_s": 1000.0 / dec_only_ms,
+                     "int2_speedup_vs_bf16": bf16_ms / dec_only_ms}
+        del bpool
+
+    # ---------------- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    hq_host = [torch.empty_like(q, device="cpu").pin_memory() for q in qs]
+    hk_host = [torch.empty_like(k, device="cpu").pin_memory() for k in kn]
+    hv_host = [torch.empty_like(v, device="cpu").pin_memory() for v in vn]
+    for a, b in zip(hq_host + hk_host + hv_host, qs + kn + vn):
+        a.copy_(b)
+    out_host = torch.empty_like(out, device="cpu").pin_memory()
+    q_in = torch.empty_like(qs[0])
+    k_in = torch.empty_like(kn[0])
+    v_in = torch.empty_like(vn[0])
+    n_base = state["n"]
+    lens_host = torch.arange(n_base, n_base + total_steps + 4, dtype=torch.int32).pin_memory()
+    lens_in = torch.empty(2, dtype=torch.int32, device="cuda")
+
+    def e2e_step(i):
+        n = state["n"]
+        q_in.copy_(hq_host[i % nvar], non_blocking=True)
+        k_in.copy_(hk_host[i % nvar], non_blocking=True)
+        v_in.copy_(hv_host[i % nvar], non_blocking=True)
+        lens_in.copy_(lens_host[n - n_base: n - n_base + 2], non_blocking=True)
+        for layer in range(L):
+            osc.oscar_append_step(ctx, layer, step_ptr(k_in, layer, kvsz), step_ptr(v_in, layer, kvsz),
+                                  osc.DTYPE_BF16, lens_in, 1, rk[layer], rv[layer], ck[layer], cv[layer], bt, ppr,
+                                  slot0)
+            osc.oscar_decode_attn(ctx, layer, step_ptr(q_in, layer, qsz), osc.DTYPE_BF16, out[layer],
+                                  osc.DTYPE_F32, bt, ppr, lens_in.data_ptr() + 4, slot0, 1, max_seq, s.sink,
+                                  s.recent, rk[layer], rv[layer], ws, ws_bytes)
+        out_host.copy_(out, non_blocking=True)
+        state["n"] = n + 1
+
+    e2e_steps = min(args.steps, total_steps)
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    ev0.record()
+    for i in range(e2e_steps - 2):
+        e2e_step(i)
+    ev1.record()
+    torch.cuda.synchronize()
+    e2e_wall_ms = (time.perf_counter() - t0) * 1000 / max(e2e_steps - 2, 1)
+    e2e_ms = max_over_ranks(max(ev0.elapsed_time(ev1) / max(e2e_steps - 2, 1), e2e_wall_ms), world)
+    h2d = qs[0].numel() * 2 + kn[0].numel() * 2 * 2 + 8
+    d2h = out.numel() * 4
+    e2e_value = sum_over_ranks(bytes_step / (e2e_ms * 1e-3) / 1e9, world)
+    assert osc.oscar_check_status(ctx) == 0
+
+    value = sum_over_ranks(value_rank, world)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        r = oracle_decode_sample(target_s=15.0)
+        cpu = {"value": r["gbs"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
+    osc.oscar_destroy(ctx)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "int2 codes, f16/bf16 MMA, f32 accumulate", "data": "synthetic",
+                "config": workload_config(L),
+                "decode_steps_per_s": 1000.0 / step_ms,
+                "bytes_per_step": bytes_step,
+                "hbm_roofline_frac_of_step": value_rank / hbm_peak,
+                "roofline": roofline, "bf16_comparison": bf16_info,
+                "write": {"tokens_per_s": L * n0 / (write_ms * 1e-3), "ms": write_ms,
+                          "what": f"prefill write of {L} layers x {n0} tokens x {hkv} kv heads (K and V)"},
+                "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                        "ms_per_step": e2e_ms},
+                "gpu_launches": int(launches), "clocks": clk, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        rc = run_reference(args, world, rank)
+    else:
+        rc = run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())
