@@ -207,6 +207,33 @@ oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
                                int32_t sink, int32_t recent, const float* R_K, const float* R_V,
                                void* workspace, size_t ws_bytes, void* stream);
 
+/* Allocation-free variant of oscar_decode_attn (no counterpart in the OSCAR
+ * paper; it exists for callers that cannot allocate device memory).
+ *
+ * Some callers cannot hand over a workspace: an engine whose device memory is
+ * all owned and budgeted by its own allocator, a plugin that must not call
+ * cudaMalloc (which can synchronise the device and stall other work), or a
+ * serving loop that is forbidden from allocating after start-up.  This call
+ * takes the same arguments as oscar_decode_attn minus workspace/ws_bytes and
+ * uses scratch in a file-scope device array of 8 MiB that the library keeps on
+ * every GPU that loads it, until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *  - Limit: the scratch oscar_decode_workspace_size would report for
+ *    (batch, max_seq) must be at most 8 MiB (for example batch 1 up to 128K
+ *    tokens at 32 q heads); larger calls return OSCAR_ERR_INVALID with a
+ *    message and launch nothing.
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current); make that first call before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents
+ *    (nothing in it needs to start at zero).  Calls whose kernels overlap on
+ *    the GPU (different streams, or different host threads) race on it:
+ *    serialise them. */
+oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
+                                       int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
+                                       const int32_t* seq_lens, const int32_t* req_slot, int32_t batch,
+                                       int32_t max_seq, int32_t sink, int32_t recent, const float* R_K,
+                                       const float* R_V, void* stream);
+
 /* In-house comparison: standard split-K paged decode over an all-BF16 cache
  * (layout above), same grid and staging as the INT2 kernel.  bf16_pool points
  * at the whole [num_layers][num_pages]... pool; workspace from

@@ -76,6 +76,8 @@ _SIGS = {
     "oscar_decode_workspace_size": (_i32, [_cfgp, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)]),
     "oscar_decode_attn": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
                                  _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "oscar_decode_attn_noalloc": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32,
+                                         _i32, _vp, _vp, _vp]),
     "oscar_bf16_decode_workspace_size": (_i32, [_cfgp, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)]),
     "oscar_bf16_decode_attn": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _vp,
                                       ctypes.c_size_t, _vp]),
@@ -236,6 +238,14 @@ def oscar_decode_attn(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_st
     _check(load().oscar_decode_attn(ctx, layer, ptr(q), q_dtype, ptr(out), out_dtype, ptr(block_table), bt_stride,
                                     ptr(seq_lens), ptr(req_slot), batch, max_seq, sink, recent, ptr(R_K), ptr(R_V),
                                     ptr(workspace), ws_bytes, stream_ptr(stream)))
+
+
+def oscar_decode_attn_noalloc(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens, req_slot,
+                              batch, max_seq, sink, recent, R_K, R_V, stream=None) -> None:
+    """oscar_decode_attn without a workspace: scratch is the library's own 8 MiB device array (see oscar.h)."""
+    _check(load().oscar_decode_attn_noalloc(ctx, layer, ptr(q), q_dtype, ptr(out), out_dtype, ptr(block_table),
+                                            bt_stride, ptr(seq_lens), ptr(req_slot), batch, max_seq, sink, recent,
+                                            ptr(R_K), ptr(R_V), stream_ptr(stream)))
 
 
 def oscar_bf16_decode_attn(ctx, layer, bf16_pool, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens,

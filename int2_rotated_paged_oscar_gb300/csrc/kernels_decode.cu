@@ -40,10 +40,20 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "oscar_internal.h"
 
 namespace oscar {
+
+// Scratch of the allocation-free decode entry point (oscar_decode_attn_noalloc):
+// a file-scope device array of kStaticScratchBytes.  Every GPU that loads the
+// library holds it until the process exits.  Host code never uses the symbol
+// as an address; it asks the runtime for the device address once per device
+// (static_decode_scratch below).
+static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
+
 namespace {
 
 constexpr int kThreads = 128;  // 4 warps
@@ -746,6 +756,26 @@ int launch_splitk_p(const DecodeArgs& a, cudaStream_t s, bool pdl) {
 }
 
 }  // namespace
+
+int static_decode_scratch(void** out, size_t* capacity) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* ptrs[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);  // with this device current
+    if (e != cudaSuccess) return (int)e;
+    ptrs[dev] = p;
+  }
+  *out = ptrs[dev];
+  *capacity = kStaticScratchBytes;
+  return 0;
+}
 
 int launch_q_rotate(const DecodeArgs& a, void* stream) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -576,6 +576,66 @@ oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
   return OSCAR_OK;
 }
 
+oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
+                                       int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
+                                       const int32_t* seq_lens, const int32_t* req_slot, int32_t batch,
+                                       int32_t max_seq, int32_t sink, int32_t recent, const float* R_K,
+                                       const float* R_V, void* stream) {
+  // Scratch comes from the library's file-scope device array: nothing here
+  // allocates (no cudaMalloc / cudaFree, no events, no torch).
+  oscar_status st = need_device(ctx);
+  if (st != OSCAR_OK) return st;
+  if ((st = check_layer(ctx, layer)) != OSCAR_OK) return st;
+  if (batch < 0 || bt_stride < 1 || max_seq < 0) return fail(OSCAR_ERR_INVALID, "bad batch/bt_stride/max_seq");
+  if ((long long)max_seq > (long long)ctx->g.max_pages_per_req * ctx->g.P)
+    return fail(OSCAR_ERR_INVALID, "max_seq %d exceeds max_pages_per_req * page_size", max_seq);
+  if (batch == 0) return OSCAR_OK;
+  if (!q || !out || !block_table || !seq_lens || !req_slot || !R_K || !R_V)
+    return fail(OSCAR_ERR_INVALID, "null tensor argument");
+  if (q_dtype != OSCAR_DTYPE_BF16 && q_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad q dtype");
+  if (out_dtype != OSCAR_DTYPE_BF16 && out_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad out dtype");
+  if (sink != ctx->g.S || recent != ctx->g.W)
+    return fail(OSCAR_ERR_INVALID, "sink/recent (%d, %d) differ from the cache configuration (%d, %d)", sink, recent,
+                ctx->g.S, ctx->g.W);
+  const DecodeWs plan = oscar::plan_decode(ctx->g, batch, max_seq, false);
+  if (plan.total > oscar::kStaticScratchBytes)
+    return fail(OSCAR_ERR_INVALID,
+                "decode needs %zu bytes of scratch for batch %d, max_seq %d; the allocation-free entry point has "
+                "%zu (use oscar_decode_attn with a caller workspace)",
+                plan.total, batch, max_seq, oscar::kStaticScratchBytes);
+  void* scratch = nullptr;
+  size_t cap = 0;
+  int e = oscar::static_decode_scratch(&scratch, &cap);
+  if (e) return cuda_fail(e, "static scratch address");
+  DecodeArgs a{};
+  a.g = ctx->g;
+  a.layer = layer;
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.seq_lens = seq_lens;
+  a.req_slot = req_slot;
+  a.batch = batch;
+  a.max_seq = max_seq;
+  a.R_K = R_K;
+  a.R_V = R_V;
+  a.pool = ctx->pool;
+  a.slab = ctx->slab;
+  a.status = ctx->d_status;
+  a.ws = static_cast<uint8_t*>(scratch);
+  a.wl = plan;
+  if ((e = oscar::launch_q_rotate(a, stream))) return cuda_fail(e, "q_rotate launch");
+  ctx->launches++;
+  if ((e = oscar::launch_decode_splitk(a, stream, true))) return cuda_fail(e, "decode_splitk launch");
+  ctx->launches++;
+  if ((e = oscar::launch_decode_combine(a, stream, true))) return cuda_fail(e, "decode_combine launch");
+  ctx->launches++;
+  return OSCAR_OK;
+}
+
 oscar_status oscar_bf16_decode_attn(oscar_ctx* ctx, int32_t layer, const void* bf16_pool, const void* q,
                                     int32_t q_dtype, void* out, int32_t out_dtype, const int32_t* block_table,
                                     int32_t bt_stride, const int32_t* seq_lens, int32_t batch, int32_t max_seq,

@@ -17,6 +17,9 @@ constexpr int kDevBadLen = 4;
 constexpr int kDevBadSlot = 8;
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;  // 200 ms per barrier wait
 
+// Size of the file-scope scratch used by the allocation-free decode entry point.
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+
 constexpr int kDtypeF32 = 0;
 constexpr int kDtypeBF16 = 1;
 
@@ -105,6 +108,10 @@ int launch_q_rotate(const DecodeArgs& a, void* stream);
 int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl);
 int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl);
 int launch_bf16_prepare(const DecodeArgs& a, void* stream);
+// Device address (for the current device) and size of the file-scope decode
+// scratch; the first call on a device looks the address up (not during stream
+// capture).
+int static_decode_scratch(void** out, size_t* capacity);
 int launch_bf16_decode(const DecodeArgs& a, void* stream, bool pdl);
 int launch_bf16_combine(const DecodeArgs& a, void* stream, bool pdl);
 
