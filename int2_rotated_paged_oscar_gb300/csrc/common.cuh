@@ -10,9 +10,38 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "oscar_internal.h"
 
 namespace oscar {
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device) (the
+// first launch on a device), so that later launches, including ones recorded
+// into a CUDA graph, issue nothing but the launch itself.
+inline cudaError_t ensure_smem_limit_ptr(const void* kern, size_t bytes) {
+  struct Entry { const void* k; int dev; size_t bytes; };
+  static std::mutex mu;
+  static Entry table[256];
+  static int used = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < used; ++i)
+    if (table[i].k == kern && table[i].dev == dev && table[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < used; ++i)
+    if (table[i].k == kern && table[i].dev == dev) { table[i].bytes = bytes; return cudaSuccess; }
+  if (used < 256) table[used++] = Entry{kern, dev, bytes};
+  return cudaSuccess;
+}
+
+template <typename Kernel>
+inline cudaError_t ensure_smem_limit(Kernel kern, size_t bytes) {
+  return ensure_smem_limit_ptr(reinterpret_cast<const void*>(kern), bytes);
+}
 
 __device__ __forceinline__ void flag_error(int* status, int bits) {
   if (status) atomicOr(status, bits);

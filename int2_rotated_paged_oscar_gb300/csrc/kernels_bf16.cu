@@ -389,7 +389,7 @@ int launch_bf16_t(const DecodeArgs& a, cudaStream_t s, bool pdl) {
   if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
   const size_t smem = kStages * STAGE + 1024 + kStages * 8;
   auto kern = bf16_decode_kernel<D, NT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem_limit(kern, smem);
   if (e != cudaSuccess) return (int)e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.wl.max_splits, a.g.Hkv, a.batch);

@@ -61,13 +61,16 @@ constexpr int kStages = 4;
 constexpr int kStageTokens = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSplits = 1023;  // the host plan never asks for more
+constexpr int kWinChunk = 16;     // window slots per window CTA
+constexpr int kMaxWinChunks = 32;
+constexpr float kRescaleLog2 = 8.f;
 
 // ------------------------------------------------------------------ workspace views
 struct WsView {
   uint2* qfrag;   // [B][Hkv][NT][D/16][32]
   float* qaux;    // [B][Hq][8]: [0] = 2^-e_h, [1 + g] = Q_g
   float* qplain;  // [B][Hq][D]
-  float* part;    // [B][Hq][max_splits + 1][D + 4]: [0] m (log2 domain), [1] l, [4..] acc
+  float* part;    // [B][Hq][win_chunks + max_splits][D + 4]: [0] m (log2 domain), [1] l, [4..] acc
 };
 
 __device__ __forceinline__ WsView ws_view(const DecodeArgs& a) {
@@ -100,149 +103,209 @@ __device__ __forceinline__ bool seq_len_ok(const DecodeArgs& a, int n) {
 }
 
 // ------------------------------------------------------------------ q rotate
-// grid (Hq, B), block 128.  Thread j < D computes q'_j = sum_i q_i R_K[i][j].
+// grid (Hkv, B), block 128, dynamic shared memory: R_K (D*D floats) + q and q'
+// of the group's gq heads.  R_K is read once per (request, kv head); thread
+// j < D computes q'_j = sum_i q_i R_K[i][j] for every head of the group.
 template <int D>
 __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
   pdl_launch_dependents();
+  extern __shared__ __align__(16) float qsm_dyn[];
+  float* Rs = qsm_dyn;        // [D][D]
+  float* qs = Rs + D * D;     // [8][D]
+  float* qr = qs + 8 * D;     // [8][D]
+  __shared__ float red[kThreads / 32][8];
   const Geom& g = a.g;
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int j = threadIdx.x;
+  const int kvh = blockIdx.x, b = blockIdx.y;
+  const int j = threadIdx.x, warp = j >> 5, lane = j & 31;
   const int gq = g.gq();
-  const int kvh = h / gq, hh = h % gq;
-  const int nt = hh >> 2;
-  __shared__ float qs[D];
-  __shared__ float qr[D];
-  __shared__ float red[kThreads / 32];
   WsView ws = ws_view(a);
-  const size_t qbase = ((size_t)b * g.Hq + h) * D;
-  if (j < D) {
-    qs[j] = load_q(a, qbase + j);
-    ws.qplain[qbase + j] = qs[j];
+  {
+    const float4* Rg = reinterpret_cast<const float4*>(a.R_K);
+    float4* R4 = reinterpret_cast<float4*>(Rs);
+    for (int i = j; i < D * D / 4; i += kThreads) R4[i] = Rg[i];
+  }
+  const size_t qbase = ((size_t)b * g.Hq + (size_t)kvh * gq) * D;
+  for (int i = j; i < gq * D; i += kThreads) {
+    const float v = load_q(a, qbase + i);
+    qs[i] = v;
+    ws.qplain[qbase + i] = v;
   }
   __syncthreads();
-  float acc = 0.f;
+  float acc[8];
+#pragma unroll
+  for (int hh = 0; hh < 8; ++hh) acc[hh] = 0.f;
   if (j < D) {
-    for (int i = 0; i < D; ++i) acc = fmaf(qs[i], a.R_K[(size_t)i * D + j], acc);
-    qr[j] = acc;
-  }
-  float m = j < D ? fabsf(acc) : 0.f;
+#pragma unroll 4
+    for (int i = 0; i < D; ++i) {
+      const float r = Rs[i * D + j];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  // group sums: group gi = channels [32 gi, 32 gi + 32) = warp gi
-  float gs = j < D ? acc : 0.f;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-  if ((j & 31) == 0) red[j >> 5] = m;
-  __syncthreads();
-  float mx = 0.f;
-#pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) mx = fmaxf(mx, red[w]);
-  int e = 0;
-  if (mx > 0.f) {
-    int E;
-    frexpf(mx, &E);  // mx = f * 2^E, f in [0.5, 1)
-    e = 5 - E;       // mx * 2^e in [16, 32): times 2^(10-pos) <= 1024 stays below the f16 maximum
-  }
-  float* aux = ws.qaux + ((size_t)b * g.Hq + h) * 8;
-  if (j == 0) aux[0] = ldexpf(1.f, -e);
-  if ((j & 31) == 0 && (j >> 5) < D / 32) aux[1 + (j >> 5)] = gs;
-  // query-side fragments of the QK MMA: this head owns columns 2*(hh%4) + {hi, lo}
-  if (j < (D / 16) * 8) {
-    const int kk = j >> 3;  // k-tile = (group, kt)
-    const int sub = j & 7;
-    const int hl = sub >> 2, tig = sub & 3;
-    const int gid = 2 * (hh & 3) + hl;
-    const int lane = gid * 4 + tig;
-    const int gi = kk >> 1, kt = kk & 1;
-    const int p8 = 4 * gi + 2 * kt;
-    uint32_t regs[2];
-#pragma unroll
-    for (int hpair = 0; hpair < 2; ++hpair) {
-      const int ch = 32 * gi + 16 * kt + 8 * hpair + 2 * tig;
-      const int pos = slot_pos((p8 + hpair) & 7);
-      float v[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const float x = ldexpf(qr[ch + u], e + 10 - pos);
-        const __half hi = __float2half_rn(x);
-        const float lo = x - __half2float(hi);
-        v[u] = hl ? lo : __half2float(hi);
-      }
-      regs[hpair] = pack_half2(v[0], v[1]);
+      for (int hh = 0; hh < 8; ++hh)
+        if (hh < gq) acc[hh] = fmaf(qs[hh * D + i], r, acc[hh]);
     }
-    const size_t fidx = ((((size_t)b * g.Hkv + kvh) * a.wl.nt + nt) * (D / 16) + kk) * 32 + lane;
-    ws.qfrag[fidx] = make_uint2(regs[0], regs[1]);
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh)
+      if (hh < gq) qr[hh * D + j] = acc[hh];
+  }
+  // per-head max |q'| (for the power-of-two normalisation) and group sums Q_g
+#pragma unroll
+  for (int hh = 0; hh < 8; ++hh) {
+    if (hh >= gq) break;
+    float m = j < D ? fabsf(acc[hh]) : 0.f;
+    float sg = j < D ? acc[hh] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      sg += __shfl_xor_sync(0xffffffffu, sg, o);
+    }
+    if (lane == 0) {
+      red[warp][hh] = m;
+      if (warp < D / 32) ws.qaux[((size_t)b * g.Hq + (size_t)kvh * gq + hh) * 8 + 1 + warp] = sg;  // group = warp
+    }
+  }
+  __syncthreads();
+  for (int hh = 0; hh < gq; ++hh) {
+    float mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) mx = fmaxf(mx, red[w][hh]);
+    int e = 0;
+    if (mx > 0.f) {
+      int E;
+      frexpf(mx, &E);  // mx = f * 2^E, f in [0.5, 1)
+      e = 5 - E;       // mx * 2^e in [16, 32): times 2^(10-pos) <= 1024 stays below the f16 maximum
+    }
+    if (j == 0) ws.qaux[((size_t)b * g.Hq + (size_t)kvh * gq + hh) * 8] = ldexpf(1.f, -e);
+    // query-side fragments of the QK MMA: head hh owns columns 2*(hh%4) + {hi, lo} of n-tile hh/4
+    if (j < (D / 16) * 8) {
+      const int kk = j >> 3;  // k-tile = (group, kt)
+      const int sub = j & 7;
+      const int hl = sub >> 2, tig = sub & 3;
+      const int gid = 2 * (hh & 3) + hl;
+      const int ln = gid * 4 + tig;
+      const int gi = kk >> 1, kt = kk & 1;
+      const int p8 = 4 * gi + 2 * kt;
+      uint32_t regs[2];
+#pragma unroll
+      for (int hpair = 0; hpair < 2; ++hpair) {
+        const int ch = 32 * gi + 16 * kt + 8 * hpair + 2 * tig;
+        const int pos = slot_pos((p8 + hpair) & 7);
+        float v[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float x = ldexpf(qr[hh * D + ch + u], e + 10 - pos);
+          const __half hi = __float2half_rn(x);
+          const float lo = x - __half2float(hi);
+          v[u] = hl ? lo : __half2float(hi);
+        }
+        regs[hpair] = pack_half2(v[0], v[1]);
+      }
+      const size_t fidx = ((((size_t)b * g.Hkv + kvh) * a.wl.nt + (hh >> 2)) * (D / 16) + kk) * 32 + ln;
+      ws.qfrag[fidx] = make_uint2(regs[0], regs[1]);
+    }
   }
 }
 
-// ------------------------------------------------------------------ window split (BF16, float32 math)
-template <int D, int NT>
-__device__ void window_split(const DecodeArgs& a, int b, int kvh, float* smem_f) {
+// ------------------------------------------------------------------ window chunks (BF16, float32 math)
+// The S + W window slots of a (request, kv head) are split into chunks of
+// kWinChunk = 16 slots, one CTA each (grid.x < win_chunks).  The chunk's K and
+// V rows are staged in shared memory; warp w handles query heads w, w + 4.
+// Lane l owns channels [l*D/32, (l+1)*D/32): per token it forms a partial dot
+// product, and a 31-shuffle reduction leaves the score of slot l in lane l
+// (lanes 16..31 hold copies and are masked out).  Output: one partial (m, l, acc) per (query head, chunk) in the plain
+// basis.
+template <int D>
+__device__ void window_chunk(const DecodeArgs& a, int b, int kvh, int chunk, uint8_t* smem) {
+  constexpr int C = D / 32;
   const Geom& g = a.g;
   const int gq = g.gq();
   const int n = a.seq_lens[b];
   const int win = g.window();
-  float* qsm = smem_f;                 // [gq][D]
-  float* sc = qsm + 8 * D;             // [win][8]
-  float* red = sc + win * 8;           // [4][8]
-  WsView ws = ws_view(a);
-  const int tid = threadIdx.x;
-  for (int i = tid; i < gq * D; i += kThreads)
-    qsm[i] = ws.qplain[((size_t)b * g.Hq + kvh * gq) * D + i];
-  __syncthreads();
+  const int t0 = chunk * kWinChunk;
+  const int cnt = min(kWinChunk, win - t0);
+  uint16_t* ks = reinterpret_cast<uint16_t*>(smem);            // [kWinChunk][D]
+  uint16_t* vs = ks + kWinChunk * D;                            // [kWinChunk][D]
+  float* qsm = reinterpret_cast<float*>(vs + kWinChunk * D);    // [gq][D]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const size_t sbase = ((size_t)a.layer * g.max_req + a.req_slot[b]) * g.slab_req_elems();
-  const uint16_t* kwin = a.slab + sbase + ((size_t)kvh * 2 + 0) * win * D;
-  const uint16_t* vwin = a.slab + sbase + ((size_t)kvh * 2 + 1) * win * D;
+  const uint16_t* kwin = a.slab + sbase + ((size_t)kvh * 2 + 0) * win * D + (size_t)t0 * D;
+  const uint16_t* vwin = a.slab + sbase + ((size_t)kvh * 2 + 1) * win * D + (size_t)t0 * D;
+  const int nvec = cnt * D / 8;  // 16-byte vectors of 8 bf16
+  for (int i = tid; i < nvec; i += kThreads) {
+    reinterpret_cast<uint4*>(ks)[i] = reinterpret_cast<const uint4*>(kwin)[i];
+    reinterpret_cast<uint4*>(vs)[i] = reinterpret_cast<const uint4*>(vwin)[i];
+  }
+  WsView ws = ws_view(a);
+  for (int i = tid; i < gq * D; i += kThreads) qsm[i] = ws.qplain[((size_t)b * g.Hq + (size_t)kvh * gq) * D + i];
+  __syncthreads();
   const int n_recent = n > g.S ? min(n - g.S, g.W) : 0;
+  const int slot = t0 + lane;
+  const bool valid = lane < cnt && (slot < g.S ? slot < n : (slot - g.S) < n_recent);
   const float sm = kLog2e * rsqrtf((float)D);
-  for (int i = tid; i < win; i += kThreads) {
-    const bool valid = i < g.S ? (i < n) : (i - g.S < n_recent);
-    float acc[8];
+  const int stride = a.wl.win_chunks + a.wl.max_splits;
+  for (int hh = warp; hh < gq; hh += kThreads / 32) {
+    float qv[C];
 #pragma unroll
-    for (int hh = 0; hh < 8; ++hh) acc[hh] = 0.f;
-    if (valid) {
-      const uint32_t* kr = reinterpret_cast<const uint32_t*>(kwin + (size_t)i * D);
-      for (int c2 = 0; c2 < D / 2; ++c2) {
-        const uint32_t w = kr[c2];
-        const float k0 = bf16_lo(w), k1 = bf16_hi(w);
+    for (int c = 0; c < C; ++c) qv[c] = qsm[hh * D + lane * C + c];
+    float part[kWinChunk];
 #pragma unroll
-        for (int hh = 0; hh < 8; ++hh)
-          if (hh < gq) acc[hh] = fmaf(qsm[hh * D + 2 * c2 + 1], k1, fmaf(qsm[hh * D + 2 * c2], k0, acc[hh]));
+    for (int t = 0; t < kWinChunk; ++t) {
+      float dot = 0.f;
+      if (t < cnt) {
+        const uint16_t* kr = ks + t * D + lane * C;
+        if constexpr (C == 4) {
+          const uint2 w = *reinterpret_cast<const uint2*>(kr);
+          dot = fmaf(qv[0], bf16_lo(w.x), dot);
+          dot = fmaf(qv[1], bf16_hi(w.x), dot);
+          dot = fmaf(qv[2], bf16_lo(w.y), dot);
+          dot = fmaf(qv[3], bf16_hi(w.y), dot);
+        } else {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(kr);
+          dot = fmaf(qv[0], bf16_lo(w), dot);
+          dot = fmaf(qv[1], bf16_hi(w), dot);
+        }
+      }
+      part[t] = dot;
+    }
+    // fold the two half-warps, then a transpose-reduction: after the step with
+    // offset o a lane keeps the o values of its half; finally part[0] of lane l
+    // (and of lane l + 16) is the full dot product of slot l
+#pragma unroll
+    for (int t = 0; t < kWinChunk; ++t) part[t] += __shfl_xor_sync(0xffffffffu, part[t], 16);
+#pragma unroll
+    for (int o = kWinChunk / 2; o >= 1; o >>= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < o; ++i) {
+        const float send = upper ? part[i] : part[i + o];
+        const float keep = upper ? part[i + o] : part[i];
+        part[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
       }
     }
+    const float sc = valid ? part[0] * sm : -INFINITY;
+    float m = sc;
 #pragma unroll
-    for (int hh = 0; hh < 8; ++hh) sc[i * 8 + hh] = valid ? acc[hh] * sm : -INFINITY;
-  }
-  __syncthreads();
-  // per-head max and sum (thread hh < gq scans the window; the window is small)
-  if (tid < gq) {
-    float m = -INFINITY;
-    for (int i = 0; i < win; ++i) m = fmaxf(m, sc[i * 8 + tid]);
-    float l = 0.f;
-    for (int i = 0; i < win; ++i) {
-      const float s = sc[i * 8 + tid];
-      const float p = s == -INFINITY ? 0.f : ex2(s - m);
-      sc[i * 8 + tid] = p;
-      l += p;
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float p = (sc == -INFINITY) ? 0.f : ex2(sc - m);
+    float l = p;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    float acc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] = 0.f;
+    for (int t = 0; t < cnt; ++t) {
+      const float pt = __shfl_sync(0xffffffffu, p, t);
+      if (pt != 0.f) {  // warp-uniform
+        const uint16_t* vr = vs + t * D + lane * C;
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+          acc[c] = fmaf(pt, __uint_as_float(static_cast<uint32_t>(vr[c]) << 16), acc[c]);
+      }
     }
-    red[tid] = m;
-    red[8 + tid] = l;
-  }
-  __syncthreads();
-  float* part = ws.part;
-  const int stride = a.wl.max_splits + 1;
-  for (int idx = tid; idx < gq * D; idx += kThreads) {
-    const int hh = idx / D, ch = idx % D;
-    float acc = 0.f;
-    for (int i = 0; i < win; ++i) {
-      const float p = sc[i * 8 + hh];
-      if (p != 0.f) acc = fmaf(p, __uint_as_float(static_cast<uint32_t>(vwin[(size_t)i * D + ch]) << 16), acc);
-    }
-    float* pp = part + (((size_t)b * g.Hq + kvh * gq + hh) * stride + 0) * (D + 4);
-    pp[4 + ch] = acc;
-    if (ch == 0) {
-      pp[0] = red[hh];
-      pp[1] = red[8 + hh];
+    float* pp = ws.part + (((size_t)b * g.Hq + (size_t)kvh * gq + hh) * stride + chunk) * (D + 4);
+#pragma unroll
+    for (int c = 0; c < C; ++c) pp[4 + lane * C + c] = acc[c];
+    if (lane == 0) {
+      pp[0] = m;
+      pp[1] = l;
     }
   }
 }
@@ -282,19 +345,19 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
     pdl_launch_dependents();
     return;
   }
-  if (blockIdx.x == 0) {
+  if ((int)blockIdx.x < a.wl.win_chunks) {
     const int req = a.req_slot[b];
     if (req < 0 || req >= g.max_req) {
-      if (tid == 0) flag_error(a.status, kDevBadSlot);
+      if (tid == 0 && blockIdx.x == 0) flag_error(a.status, kDevBadSlot);
       pdl_launch_dependents();
       return;
     }
     pdl_wait();
-    window_split<D, NT>(a, b, kvh, reinterpret_cast<float*>(smem));
+    window_chunk<D>(a, b, kvh, blockIdx.x, smem);
     pdl_launch_dependents();
     return;
   }
-  const int split = blockIdx.x - 1;
+  const int split = blockIdx.x - a.wl.win_chunks;
   const int h_end = n - g.W;
   if (h_end <= g.S) { pdl_launch_dependents(); return; }
   const int n_hist_pages = (h_end - 1) / P + 1;
@@ -464,9 +527,14 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
         }
       }
       const int ta = tb + ra, tbk = tb + rb;
+      // every row of the block is a history token on a mapped page (warp-uniform)
+      const bool full_block = page_ok && tb >= g.S && tb + 15 < h_end;
       const bool va = page_ok && ta >= g.S && ta < h_end;
       const bool vb = page_ok && tbk >= g.S && tbk < h_end;
-      // ---------------- online softmax (per head: lanes sharing tig)
+      // ---------------- online softmax (per head: lanes sharing tig).  The running
+      // reference m_run only moves when a block maximum exceeds it by more than
+      // 2^kRescaleLog2, so the accumulators are rescaled rarely; p stays below
+      // 2^kRescaleLog2, which float32 sums and bf16 operands absorb.
       float pa[NT], pb[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -476,18 +544,21 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
         mb = warp_max_xor(mb, 4);
         mb = warp_max_xor(mb, 8);
         mb = warp_max_xor(mb, 16);
-        const float m_new = fmaxf(m_run[nt], mb);
-        const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run[nt] - m_new);
-        pa[nt] = (s_a == -INFINITY) ? 0.f : ex2(s_a - m_new);
-        pb[nt] = (s_b == -INFINITY) ? 0.f : ex2(s_b - m_new);
-        m_run[nt] = m_new;
-        l_run[nt] = fmaf(l_run[nt], alpha, pa[nt] + pb[nt]);
+        const float m_ref = (mb > m_run[nt] + kRescaleLog2) ? mb : m_run[nt];
+        if (__any_sync(0xffffffffu, m_ref != m_run[nt])) {
+          const float alpha = (m_run[nt] == -INFINITY) ? 0.f : ex2(m_run[nt] - m_ref);
+          l_run[nt] *= alpha;
 #pragma unroll
-        for (int mt = 0; mt < Lay::MT; ++mt)
+          for (int mt = 0; mt < Lay::MT; ++mt)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) acc[nt][mt][r] *= alpha;
+            for (int r = 0; r < 4; ++r) acc[nt][mt][r] *= alpha;
 #pragma unroll
-        for (int gi = 0; gi < Lay::GROUPS; ++gi) zacc[nt][gi] *= alpha;
+          for (int gi = 0; gi < Lay::GROUPS; ++gi) zacc[nt][gi] *= alpha;
+          m_run[nt] = m_ref;
+        }
+        pa[nt] = (s_a == -INFINITY) ? 0.f : ex2(s_a - m_run[nt]);
+        pb[nt] = (s_b == -INFINITY) ? 0.f : ex2(s_b - m_run[nt]);
+        l_run[nt] += pa[nt] + pb[nt];
       }
       // ---------------- zero term of the values (rows ra, rb)
       {
@@ -499,8 +570,12 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
           const float z_b = bf16_hi(vszB[gi]);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            if (pa[nt] > 0.f) zacc[nt][gi] = fmaf(pa[nt], z_a, zacc[nt][gi]);
-            if (pb[nt] > 0.f) zacc[nt][gi] = fmaf(pb[nt], z_b, zacc[nt][gi]);
+            if (full_block) {
+              zacc[nt][gi] = fmaf(pb[nt], z_b, fmaf(pa[nt], z_a, zacc[nt][gi]));
+            } else {
+              if (pa[nt] > 0.f) zacc[nt][gi] = fmaf(pa[nt], z_a, zacc[nt][gi]);
+              if (pb[nt] > 0.f) zacc[nt][gi] = fmaf(pb[nt], z_b, zacc[nt][gi]);
+            }
           }
         }
       }
@@ -553,18 +628,21 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
           const float p9 = __shfl_sync(0xffffffffu, pb[nt], src1);
 #pragma unroll
           for (int gi = 0; gi < Lay::GROUPS; ++gi) {
-            float wv[4];
             const float pr[4] = {p0, p1, p8v, p9};
             const uint32_t szr[4] = {vs0[gi], vs1[gi], vs8[gi], vs9[gi]};
+            float w[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const float w = pr[u] > 0.f ? pr[u] * bf16_lo(szr[u]) : 0.f;
-              const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-              const float hif = __bfloat162float(hi);
-              wv[u] = lo_lane ? (w - hif) : hif;
+              w[u] = pr[u] * bf16_lo(szr[u]);
+              if (!full_block) w[u] = pr[u] > 0.f ? w[u] : 0.f;  // unwritten slots may hold NaN scales
             }
-            const uint32_t b0 = pack_bf162(wv[0], wv[1]);
-            const uint32_t b1 = pack_bf162(wv[2], wv[3]);
+            // bf16 hi/lo split: hi = bf16(w), lo = bf16(w - hi); lane parity picks the column
+            const uint32_t h01 = pack_bf162(w[0], w[1]);
+            const uint32_t h23 = pack_bf162(w[2], w[3]);
+            const uint32_t l01 = pack_bf162(w[0] - bf16_lo(h01), w[1] - bf16_hi(h01));
+            const uint32_t l23 = pack_bf162(w[2] - bf16_lo(h23), w[3] - bf16_hi(h23));
+            const uint32_t b0 = lo_lane ? l01 : h01;
+            const uint32_t b1 = lo_lane ? l23 : h23;
 #pragma unroll
             for (int mq = 0; mq < 2; ++mq) {
               const int mt = 2 * gi + mq;
@@ -632,7 +710,7 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
     }
   }
   __syncthreads();
-  const int stride = a.wl.max_splits + 1;
+  const int stride = a.wl.win_chunks + a.wl.max_splits;
   for (int idx = tid; idx < gq * D; idx += kThreads) {
     const int hh = idx / D, ch = idx % D;
     float M = -INFINITY;
@@ -656,30 +734,33 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
 }
 
 // ------------------------------------------------------------------ combine
-// grid (Hq, B), block 128.  Merges the window partial (plain basis) and the
+// grid (Hq, B), block 128.  Merges the window partials (plain basis) and the
 // INT2 partials (rotated basis), applies R_V^T once, divides by l.
 template <int D>
 __global__ void __launch_bounds__(kThreads) decode_combine_kernel(DecodeArgs a) {
+  constexpr int C = D / 32;
   pdl_wait();
   const Geom& g = a.g;
   const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __shared__ float rot[D];
   __shared__ float rotated_out[D];
-  __shared__ float wts[kMaxSplits + 1];
+  __shared__ float wts[kMaxSplits + kMaxWinChunks];
   __shared__ float s_l;
   WsView ws = ws_view(a);
   const int n = a.seq_lens[b];
+  const int wc = a.wl.win_chunks;
   const int nsp = seq_len_ok(a, n) ? min(splits_for(a, n), kMaxSplits) : 0;
-  const int stride = a.wl.max_splits + 1;
+  const int nslot = wc + nsp;
+  const int stride = wc + a.wl.max_splits;
   const float* base = ws.part + ((size_t)b * g.Hq + h) * stride * (D + 4);
   if (warp == 0) {
     float M = -INFINITY;
-    for (int i = lane; i <= nsp; i += 32) M = fmaxf(M, base[(size_t)i * (D + 4)]);
+    for (int i = lane; i < nslot; i += 32) M = fmaxf(M, base[(size_t)i * (D + 4)]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f;
-    for (int i = lane; i <= nsp; i += 32) {
+    for (int i = lane; i < nslot; i += 32) {
       const float mi = base[(size_t)i * (D + 4)];
       const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
       wts[i] = w;
@@ -692,19 +773,42 @@ __global__ void __launch_bounds__(kThreads) decode_combine_kernel(DecodeArgs a) 
   __syncthreads();
   float plain = 0.f;
   if (tid < D) {
+    for (int i = 0; i < wc; ++i) plain = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + tid], plain);
     float r = 0.f;
-    for (int i = 1; i <= nsp; ++i) r = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + tid], r);
+#pragma unroll 8
+    for (int i = wc; i < nslot; ++i) r = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + tid], r);
     rot[tid] = r;
-    plain = wts[0] * base[4 + tid];
   }
   __syncthreads();
-  // (rot R_V^T)_j = sum_k rot_k R_V[j][k]; warp w handles rows j = w, w + 4, ...
-  for (int j = warp; j < D; j += kThreads / 32) {
-    float s = 0.f;
-    for (int k = lane; k < D; k += 32) s = fmaf(rot[k], a.R_V[(size_t)j * D + k], s);
+  // (rot R_V^T)_j = sum_k rot_k R_V[j][k]: warp w handles rows [w*D/4, (w+1)*D/4) in batches of 8,
+  // lane l reads the contiguous slice [l*C, (l+1)*C) of each row
+  float rl[C];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) rotated_out[j] = s;
+  for (int c = 0; c < C; ++c) rl[c] = rot[lane * C + c];
+  for (int j0 = warp * (D / 4); j0 < (warp + 1) * (D / 4); j0 += 8) {
+    float sacc[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float* row = a.R_V + (size_t)(j0 + r) * D + lane * C;
+      float v[C];
+      if constexpr (C == 4) {
+        const float4 q4 = *reinterpret_cast<const float4*>(row);
+        v[0] = q4.x; v[1] = q4.y; v[2] = q4.z; v[3] = q4.w;
+      } else {
+        const float2 q2 = *reinterpret_cast<const float2*>(row);
+        v[0] = q2.x; v[1] = q2.y;
+      }
+      float t = 0.f;
+#pragma unroll
+      for (int c = 0; c < C; ++c) t = fmaf(rl[c], v[c], t);
+      sacc[r] = t;
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sacc[r] += __shfl_xor_sync(0xffffffffu, sacc[r], o);
+      if (lane == r) rotated_out[j0 + r] = sacc[r];
+    }
   }
   __syncthreads();
   if (tid < D) {
@@ -724,16 +828,16 @@ template <int D, int NT, int P>
 int launch_splitk_t(const DecodeArgs& a, cudaStream_t s, bool pdl) {
   using Lay = Int2Layout<D, NT, P>;
   size_t smem = kStages * Lay::STAGE + kStages * 8 + kStages * 4;
-  const size_t win_smem = (8 * D + a.g.window() * 8 + 64) * sizeof(float);
+  const size_t win_smem = 2 * kWinChunk * D * sizeof(uint16_t) + 8 * D * sizeof(float);
   const size_t merge_smem = (64 + 4 * 8 * D) * sizeof(float);
   if (win_smem > smem) smem = win_smem;
   if (merge_smem > smem) smem = merge_smem;
   smem = (smem + 127) & ~size_t(127);
   auto kern = decode_splitk_kernel<D, NT, P>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem_limit(kern, smem);
   if (e != cudaSuccess) return (int)e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.wl.max_splits + 1, a.g.Hkv, a.batch);
+  cfg.gridDim = dim3(a.wl.win_chunks + a.wl.max_splits, a.g.Hkv, a.batch);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -753,6 +857,15 @@ int launch_splitk_p(const DecodeArgs& a, cudaStream_t s, bool pdl) {
     case 32: return launch_splitk_t<D, NT, 32>(a, s, pdl);
     default: return launch_splitk_t<D, NT, 64>(a, s, pdl);
   }
+}
+
+template <int D>
+int launch_q_rotate_t(const DecodeArgs& a, cudaStream_t s) {
+  const size_t smem = sizeof(float) * (D * D + 16 * D);
+  cudaError_t e = ensure_smem_limit(q_rotate_kernel<D>, smem);
+  if (e != cudaSuccess) return (int)e;
+  q_rotate_kernel<D><<<dim3(a.g.Hkv, a.batch), kThreads, smem, s>>>(a);
+  return (int)cudaGetLastError();
 }
 
 }  // namespace
@@ -779,10 +892,7 @@ int static_decode_scratch(void** out, size_t* capacity) {
 
 int launch_q_rotate(const DecodeArgs& a, void* stream) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 grid(a.g.Hq, a.batch);
-  if (a.g.D == 128) q_rotate_kernel<128><<<grid, kThreads, 0, s>>>(a);
-  else q_rotate_kernel<64><<<grid, kThreads, 0, s>>>(a);
-  return (int)cudaGetLastError();
+  return a.g.D == 128 ? launch_q_rotate_t<128>(a, s) : launch_q_rotate_t<64>(a, s);
 }
 
 int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl) {

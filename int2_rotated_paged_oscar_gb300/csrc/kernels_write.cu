@@ -8,12 +8,15 @@
 // scale and zero, round-to-nearest-even codes clamped to [0, 3]) and the code
 // layouts are the ones documented in include/oscar.h.
 //
-// One warp handles one (token, kv head, K|V) row: lane l owns channels
-// [l*D/32, (l+1)*D/32).  The rotation y_j = sum_i x_i R[i][j] runs in float32
-// with one FMA per term in increasing i, the same order in every kernel of this
-// file, so the append, eviction and prefill paths produce identical codes for
-// the same BF16 input.  The Hadamard-only variant replaces the dense product by
-// a fast Walsh-Hadamard transform followed by the bit-reversal gather.
+// Lane l of a warp owns output channels [l*D/32, (l+1)*D/32) of a row.  The
+// rotation y_j = sum_i x_i R[i][j] runs in float32 in one canonical order used
+// by every kernel of this file: four partial sums over the input quarters
+// i in [kD/4, (k+1)D/4), each one FMA per term in increasing i starting from
+// zero, added as ((c0 + c1) + c2) + c3.  The prefill, eviction and append paths
+// therefore produce identical codes for the same BF16 input, whichever way
+// they spread the four chains over warps.  The Hadamard-only variant replaces
+// the dense product by a fast Walsh-Hadamard transform followed by the
+// bit-reversal gather.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -55,15 +58,24 @@ __device__ __forceinline__ void rotate_row(const float* xs, const float* R, int 
   constexpr int C = D / 32;
   const int lane = threadIdx.x & 31;
   if (!hadamard) {
+    float ch[4][C];
 #pragma unroll
-    for (int c = 0; c < C; ++c) y[c] = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < D; ++i) {
-      const float xi = xs[i];
-      const float* r = R + (size_t)i * D + lane * C;
+    for (int k = 0; k < 4; ++k)
 #pragma unroll
-      for (int c = 0; c < C; ++c) y[c] = fmaf(xi, r[c], y[c]);
+      for (int c = 0; c < C; ++c) ch[k][c] = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < D / 4; ++i) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int ii = k * (D / 4) + i;
+        const float xi = xs[ii];
+        const float* r = R + (size_t)ii * D + lane * C;
+#pragma unroll
+        for (int c = 0; c < C; ++c) ch[k][c] = fmaf(xi, r[c], ch[k][c]);
+      }
     }
+#pragma unroll
+    for (int c = 0; c < C; ++c) y[c] = ((ch[0][c] + ch[1][c]) + ch[2][c]) + ch[3][c];
     return;
   }
   // Fast Walsh-Hadamard transform in natural (Sylvester) order: lane holds
@@ -193,6 +205,19 @@ __device__ __forceinline__ uint16_t* window_row(const WriteArgs& a, int req, int
 
 __device__ __forceinline__ int window_slot(int t, int S, int W) { return t < S ? t : S + (t - S) % W; }
 
+// Page holding history token t of request b, or -1 (flagged) if unmapped.
+__device__ __forceinline__ int history_page(const WriteArgs& a, int b, int t) {
+  const Geom& g = a.g;
+  const int lp = t / g.P;
+  int page = -1;
+  if (lp < a.bt_stride && lp < g.max_pages_per_req) page = a.block_table[(size_t)b * a.bt_stride + lp];
+  if (page < 0 || page >= g.num_pages) {
+    if ((threadIdx.x & 31) == 0) flag_error(a.status, kDevBadPage);
+    return -1;
+  }
+  return page;
+}
+
 // Quantise the row held in xs (float32, D values) into history slot t of request b.
 template <int D>
 __device__ void store_history(const WriteArgs& a, int b, int t, int h, bool is_v, const float* xs, const float* R,
@@ -220,50 +245,132 @@ struct WarpSmem {
 };
 
 // ------------------------------------------------------------------ prefill / extend
-// grid.x covers total_tokens * Hkv rows for one of K (blockIdx.y = 0) or V (1).
+// grid (ctas, 2): blockIdx.y selects K (0) or V (1).  The CTA keeps R in shared
+// memory; each warp takes kRowsPerPass (token, kv head) rows at a time and
+// rotates them together so every R element read from shared memory feeds
+// kRowsPerPass FMAs.
+constexpr int kRowsPerPass = 4;
+
 template <int D>
-__global__ void __launch_bounds__(kWarpsPerCta * 32) write_kernel(WriteArgs a) {
-  __shared__ WarpSmem sm[kWarpsPerCta];
+struct WriteSmem {
+  float x[kWarpsPerCta][kRowsPerPass][D];
+  float scratch[kWarpsPerCta][D];  // FWHT gather buffer
+  int meta[kWarpsPerCta][kRowsPerPass][3];  // (request, token, kv head) of history rows
+  uint8_t codes[kWarpsPerCta][D];
+};
+
+template <int D>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, 2) write_kernel(WriteArgs a) {
+  constexpr int C = D / 32;
+  extern __shared__ __align__(16) float wsm[];
+  float* Rs = wsm;                                                  // [D][D]
+  WriteSmem<D>& sm = *reinterpret_cast<WriteSmem<D>*>(wsm + D * D);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_v = blockIdx.y == 1;
   const Geom& g = a.g;
   const void* src = is_v ? a.V : a.K;
-  const float* R = is_v ? a.R_V : a.R_K;
+  {
+    const float4* Rg = reinterpret_cast<const float4*>(is_v ? a.R_V : a.R_K);
+    float4* R4 = reinterpret_cast<float4*>(Rs);
+    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) R4[i] = Rg[i];
+  }
+  __syncthreads();
   const long long rows = (long long)a.total_tokens * g.Hkv;
-  for (long long item = (long long)blockIdx.x * kWarpsPerCta + warp; item < rows;
-       item += (long long)gridDim.x * kWarpsPerCta) {
-    const int row = static_cast<int>(item / g.Hkv);
-    const int h = static_cast<int>(item % g.Hkv);
-    // request of this row: largest b with cu_seqlens[b] <= row
-    int lo = 0, hi = a.batch - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (a.cu_seqlens[mid] <= row) lo = mid; else hi = mid - 1;
-    }
-    const int b = lo;
-    const int t0 = a.start_pos[b];
-    const int len = a.cu_seqlens[b + 1] - a.cu_seqlens[b];
-    const int t = t0 + (row - a.cu_seqlens[b]);
-    const int n1 = t0 + len;
-    if (t0 < 0 || n1 > g.max_pages_per_req * g.P) {
-      if (lane == 0) flag_error(a.status, kDevBadLen);
-      continue;
-    }
-    const size_t in_base = ((size_t)row * g.Hkv + h) * D;
-    if (t >= g.S && t < n1 - g.W) {
-      for (int i = lane; i < D; i += 32) sm[warp].x[i] = load_in(src, a.dtype, in_base + i);
-      __syncwarp();
-      store_history<D>(a, b, t, h, is_v, sm[warp].x, R, sm[warp].codes, sm[warp].f);
-      __syncwarp();
-    } else {
-      const int req = a.req_slot[b];
-      if (req < 0 || req >= g.max_req) {
-        if (lane == 0) flag_error(a.status, kDevBadSlot);
+  const long long stride = (long long)gridDim.x * kWarpsPerCta * kRowsPerPass;
+  for (long long base = ((long long)blockIdx.x * kWarpsPerCta + warp) * kRowsPerPass; base < rows; base += stride) {
+    unsigned hist = 0;  // bit r: row r goes to an INT2 page
+#pragma unroll 1
+    for (int r = 0; r < kRowsPerPass; ++r) {
+      const long long item = base + r;
+      if (item >= rows) continue;
+      const int row = static_cast<int>(item / g.Hkv);
+      const int h = static_cast<int>(item % g.Hkv);
+      int lo = 0, hi = a.batch - 1;  // request of this row: largest b with cu_seqlens[b] <= row
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.cu_seqlens[mid] <= row) lo = mid; else hi = mid - 1;
+      }
+      const int b = lo;
+      const int t0 = a.start_pos[b];
+      const int len = a.cu_seqlens[b + 1] - a.cu_seqlens[b];
+      const int t = t0 + (row - a.cu_seqlens[b]);
+      const int n1 = t0 + len;
+      if (t0 < 0 || n1 > g.max_pages_per_req * g.P) {
+        if (lane == 0) flag_error(a.status, kDevBadLen);
         continue;
       }
-      uint16_t* dst = window_row(a, req, h, is_v, window_slot(t, g.S, g.W));
-      for (int i = lane; i < D; i += 32) dst[i] = to_bf16_bits(load_in(src, a.dtype, in_base + i));
+      const size_t in_base = ((size_t)row * g.Hkv + h) * D;
+      if (t >= g.S && t < n1 - g.W) {
+        hist |= 1u << r;
+        if (lane == 0) {
+          sm.meta[warp][r][0] = b;
+          sm.meta[warp][r][1] = t;
+          sm.meta[warp][r][2] = h;
+        }
+        for (int i = lane; i < D; i += 32) sm.x[warp][r][i] = load_in(src, a.dtype, in_base + i);
+      } else {
+        const int req = a.req_slot[b];
+        if (req < 0 || req >= g.max_req) {
+          if (lane == 0) flag_error(a.status, kDevBadSlot);
+          continue;
+        }
+        uint16_t* dst = window_row(a, req, h, is_v, window_slot(t, g.S, g.W));
+        for (int i = lane; i < D; i += 32) dst[i] = to_bf16_bits(load_in(src, a.dtype, in_base + i));
+      }
     }
+    __syncwarp();
+    if (!hist) continue;
+    float y[kRowsPerPass][C];
+    if (a.hadamard) {
+#pragma unroll
+      for (int r = 0; r < kRowsPerPass; ++r)
+        if (hist >> r & 1) rotate_row<D>(sm.x[warp][r], nullptr, 1, y[r], sm.scratch[warp]);
+    } else {
+      float ch[kRowsPerPass][4][C];
+#pragma unroll
+      for (int r = 0; r < kRowsPerPass; ++r)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int c = 0; c < C; ++c) ch[r][k][c] = 0.f;
+#pragma unroll 2
+      for (int i = 0; i < D / 4; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int ii = k * (D / 4) + i;
+          float rv[C];
+          if constexpr (C == 4) {
+            const float4 q4 = *reinterpret_cast<const float4*>(Rs + ii * D + lane * 4);
+            rv[0] = q4.x; rv[1] = q4.y; rv[2] = q4.z; rv[3] = q4.w;
+          } else {
+            const float2 q2 = *reinterpret_cast<const float2*>(Rs + ii * D + lane * 2);
+            rv[0] = q2.x; rv[1] = q2.y;
+          }
+#pragma unroll
+          for (int r = 0; r < kRowsPerPass; ++r) {
+            const float xi = sm.x[warp][r][ii];
+#pragma unroll
+            for (int c = 0; c < C; ++c) ch[r][k][c] = fmaf(xi, rv[c], ch[r][k][c]);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kRowsPerPass; ++r)
+#pragma unroll
+        for (int c = 0; c < C; ++c) y[r][c] = ((ch[r][0][c] + ch[r][1][c]) + ch[r][2][c]) + ch[r][3][c];
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsPerPass; ++r) {
+      if (!(hist >> r & 1)) continue;
+      const int rb = sm.meta[warp][r][0], rt = sm.meta[warp][r][1], rh = sm.meta[warp][r][2];
+      const int page = history_page(a, rb, rt);
+      if (page < 0) continue;
+      uint8_t* codes;
+      uint32_t* sz;
+      history_row_ptrs<D>(a, page, rt % g.P, rh, is_v, &codes, &sz);
+      quant_pack_store<D>(y[r], is_v ? a.clip_V : a.clip_K, is_v, codes, sz, sm.codes[warp]);
+    }
+    __syncwarp();
   }
 }
 
@@ -304,57 +411,96 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) evict_kernel(WriteArgs a) {
 }
 
 // ------------------------------------------------------------------ decode append
-// grid = (batch, Hkv), block = 2 warps (K, V).
+// grid = (batch, Hkv), block = 8 warps: warp w works on K (w < 4) or V, and on
+// rotation chain k = w % 4 (input channels [kD/4, (k+1)D/4)), so each warp has
+// all of its R loads in flight at once.  The chain-0 warp of K and of V adds
+// the four chains in the canonical order, quantises and packs.
 template <int D>
-__global__ void __launch_bounds__(64) append_kernel(WriteArgs a) {
-  __shared__ WarpSmem sm[2];
+__global__ void __launch_bounds__(256) append_kernel(WriteArgs a) {
+  constexpr int C = D / 32;
+  __shared__ float xs[2][D];
+  __shared__ float part[2][4][D];
+  __shared__ uint8_t code_scratch[2][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geom& g = a.g;
   const int b = blockIdx.x, h = blockIdx.y;
-  const bool is_v = warp == 1;
-  const float* R = is_v ? a.R_V : a.R_K;
+  const int kv = warp >> 2, k = warp & 3;
+  const bool is_v = kv == 1;
   const int n0 = a.start_pos[b];
   if (n0 < 0 || n0 + 1 > g.max_pages_per_req * g.P) {
-    if (lane == 0) flag_error(a.status, kDevBadLen);
+    if (threadIdx.x == 0) flag_error(a.status, kDevBadLen);
     return;
   }
   const int req = a.req_slot[b];
   if (req < 0 || req >= g.max_req) {
-    if (lane == 0) flag_error(a.status, kDevBadSlot);
+    if (threadIdx.x == 0) flag_error(a.status, kDevBadSlot);
     return;
   }
   const int slot_new = window_slot(n0, g.S, g.W);
   uint16_t* ring = window_row(a, req, h, is_v, slot_new);
   const int e = n0 - g.W;
-  if (e >= g.S) {
-    // the evicted token occupies the slot the new token takes
-    for (int c = lane; c < D; c += 32) sm[warp].x[c] = __uint_as_float(static_cast<uint32_t>(ring[c]) << 16);
-    __syncwarp();
-    store_history<D>(a, b, e, h, is_v, sm[warp].x, R, sm[warp].codes, sm[warp].f);
-    __syncwarp();
+  const bool evict = e >= g.S;  // the evicted token occupies the slot the new token takes
+  if (evict) {
+    if (k == 0)
+      for (int c = lane; c < D; c += 32) xs[kv][c] = __uint_as_float(static_cast<uint32_t>(ring[c]) << 16);
+    __syncthreads();
+    const float* R = is_v ? a.R_V : a.R_K;
+    float acc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] = 0.f;
+#pragma unroll
+    for (int i = 0; i < D / 4; ++i) {
+      const int ii = k * (D / 4) + i;
+      const float xi = xs[kv][ii];
+      const float* r = R + (size_t)ii * D + lane * C;
+#pragma unroll
+      for (int c = 0; c < C; ++c) acc[c] = fmaf(xi, r[c], acc[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < C; ++c) part[kv][k][lane * C + c] = acc[c];
   }
-  const void* src = is_v ? a.V : a.K;
-  const size_t in_base = ((size_t)b * g.Hkv + h) * D;
-  for (int c = lane; c < D; c += 32) ring[c] = to_bf16_bits(load_in(src, a.dtype, in_base + c));
-}
-
-int grid_for_rows(long long rows) {
-  long long ctas = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
-  if (ctas > 152 * 16) ctas = 152 * 16;
-  if (ctas < 1) ctas = 1;
-  return static_cast<int>(ctas);
+  __syncthreads();
+  if (evict && k == 0) {
+    float y[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      const int j = lane * C + c;
+      y[c] = ((part[kv][0][j] + part[kv][1][j]) + part[kv][2][j]) + part[kv][3][j];
+    }
+    const int page = history_page(a, b, e);
+    if (page >= 0) {
+      uint8_t* codes;
+      uint32_t* sz;
+      history_row_ptrs<D>(a, page, e % g.P, h, is_v, &codes, &sz);
+      quant_pack_store<D>(y, is_v ? a.clip_V : a.clip_K, is_v, codes, sz, code_scratch[kv]);
+    }
+  }
+  if (k == 0) {
+    const void* src = is_v ? a.V : a.K;
+    const size_t in_base = ((size_t)b * g.Hkv + h) * D;
+    for (int c = lane; c < D; c += 32) ring[c] = to_bf16_bits(load_in(src, a.dtype, in_base + c));
+  }
 }
 
 }  // namespace
+
+template <int D>
+int launch_write_t(const WriteArgs& a, cudaStream_t s) {
+  const long long rows = (long long)a.total_tokens * a.g.Hkv;
+  long long ctas = (rows + kWarpsPerCta * kRowsPerPass - 1) / (kWarpsPerCta * kRowsPerPass);
+  if (ctas > 152 * 2) ctas = 152 * 2;  // two CTAs per SM fit (R + row buffers)
+  const size_t smem = sizeof(float) * D * D + sizeof(WriteSmem<D>);
+  cudaError_t e = ensure_smem_limit(write_kernel<D>, smem);
+  if (e != cudaSuccess) return (int)e;
+  write_kernel<D><<<dim3((unsigned)ctas, 2), kWarpsPerCta * 32, smem, s>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
 
 int launch_write(const WriteArgs& a, void* stream) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long rows = (long long)a.total_tokens * a.g.Hkv;
   if (rows == 0) return 0;
-  dim3 grid(grid_for_rows(rows), 2);
-  if (a.g.D == 128) write_kernel<128><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
-  else write_kernel<64><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  return a.g.D == 128 ? launch_write_t<128>(a, s) : launch_write_t<64>(a, s);
 }
 
 int launch_evict(const WriteArgs& a, void* stream) {
@@ -370,8 +516,8 @@ int launch_append(const WriteArgs& a, void* stream) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.batch == 0) return 0;
   dim3 grid(a.batch, a.g.Hkv);
-  if (a.g.D == 128) append_kernel<128><<<grid, 64, 0, s>>>(a);
-  else append_kernel<64><<<grid, 64, 0, s>>>(a);
+  if (a.g.D == 128) append_kernel<128><<<grid, 256, 0, s>>>(a);
+  else append_kernel<64><<<grid, 256, 0, s>>>(a);
   return static_cast<int>(cudaGetLastError());
 }
 

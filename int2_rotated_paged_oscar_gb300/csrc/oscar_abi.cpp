@@ -89,6 +89,8 @@ oscar_status validate(const oscar_config* c, Geom* out) {
   if (!is_pow2_in(c->page_size, {16, 32, 64}))
     return fail(OSCAR_ERR_UNSUPPORTED, "page_size %d not in {16,32,64}", c->page_size);
   if (c->group_size != 32) return fail(OSCAR_ERR_UNSUPPORTED, "group_size %d is not 32", c->group_size);
+  if (c->sink + c->recent > 512)
+    return fail(OSCAR_ERR_UNSUPPORTED, "sink + recent = %d exceeds 512", c->sink + c->recent);
   if ((long long)c->max_pages_per_req * c->page_size > (1LL << 30))
     return fail(OSCAR_ERR_INVALID, "max_pages_per_req * page_size too large");
   Geom g;
@@ -177,6 +179,7 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   }
   w.pages_per_split = static_cast<int>(pps);
   w.max_splits = static_cast<int>(splits);
+  w.win_chunks = bf16_pool ? 0 : (g.S + g.W + 15) / 16;
   auto align = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
   w.qfrag_off = off;
@@ -186,7 +189,7 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   w.qplain_off = off;
   off = align(off + (size_t)batch * g.Hq * g.D * sizeof(float));
   w.part_off = off;
-  const size_t slots = bf16_pool ? (size_t)w.max_splits : (size_t)w.max_splits + 1;
+  const size_t slots = (size_t)w.max_splits + (size_t)w.win_chunks;
   off = align(off + (size_t)batch * g.Hq * slots * (g.D + 4) * sizeof(float));
   w.total = off;
   return w;

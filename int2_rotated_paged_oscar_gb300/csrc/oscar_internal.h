@@ -67,9 +67,10 @@ struct WriteArgs {
 // Decode workspace carve-up (offsets in bytes from the workspace base).
 struct DecodeWs {
   size_t qfrag_off, qaux_off, qplain_off, part_off, total;
-  int max_splits;        // INT2 splits per (request, kv head); grid.x = max_splits + 1 (x = 0 is the window)
+  int max_splits;        // INT2 splits per (request, kv head)
   int pages_per_split;   // multiple of 64 / page_size
   int nt;                // query n-tiles (max(1, 2*gq/8))
+  int win_chunks;        // BF16 window CTAs per (request, kv head): grid.x = win_chunks + max_splits
 };
 
 struct DecodeArgs {
