@@ -174,12 +174,16 @@ __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
       e = 5 - E;       // mx * 2^e in [16, 32): times 2^(10-pos) <= 1024 stays below the f16 maximum
     }
     if (j == 0) ws.qaux[((size_t)b * g.Hq + (size_t)kvh * gq + hh) * 8] = ldexpf(1.f, -e);
-    // query-side fragments of the QK MMA: head hh owns columns 2*(hh%4) + {hi, lo} of n-tile hh/4
+    // query-side fragments of the QK MMA.  Up to 4 heads: head hh owns columns
+    // 2*hh + {hi, lo} of one operand.  8 heads: column hh of two operand planes
+    // (plane 0 = hi, plane 1 = lo) that accumulate into the same registers.
     if (j < (D / 16) * 8) {
       const int kk = j >> 3;  // k-tile = (group, kt)
       const int sub = j & 7;
       const int hl = sub >> 2, tig = sub & 3;
-      const int gid = 2 * (hh & 3) + hl;
+      const bool g8 = gq == 8;
+      const int gid = g8 ? hh : 2 * (hh & 3) + hl;
+      const int plane = g8 ? hl : 0;
       const int ln = gid * 4 + tig;
       const int gi = kk >> 1, kt = kk & 1;
       const int p8 = 4 * gi + 2 * kt;
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
         }
         regs[hpair] = pack_half2(v[0], v[1]);
       }
-      const size_t fidx = ((((size_t)b * g.Hkv + kvh) * a.wl.nt + (hh >> 2)) * (D / 16) + kk) * 32 + ln;
+      const size_t fidx = ((((size_t)b * g.Hkv + kvh) * a.wl.nt + plane) * (D / 16) + kk) * 32 + ln;
       ws.qfrag[fidx] = make_uint2(regs[0], regs[1]);
     }
   }
@@ -413,40 +417,52 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
   // query side (written by q_rotate): wait for the previous grid
   pdl_wait();
   WsView ws = ws_view(a);
+  // Column layout of the MMAs (see q_rotate):
+  //  G8 (8 query heads per kv head): columns are heads; the f16 (QK) / bf16 (PV)
+  //     hi and lo parts are separate operand planes accumulated into the same
+  //     registers.  A lane owns heads 2*tig and 2*tig + 1.
+  //  otherwise (<= 4 heads): QK columns are (head, hi|lo) = 2*head + part; PV
+  //     columns are (head, group parity) = 2*head + (g & 1) with hi and lo as two
+  //     MMAs.  A lane owns head tig.
+  constexpr bool G8 = NT == 2;
+  constexpr int NH = G8 ? 2 : 1;  // heads per lane
   uint32_t qb[NT][Lay::KT][2];
-  float qscale[NT];
-  float qg[NT][Lay::GROUPS];
+  float qscale[NH];
+  float qg[NH][Lay::GROUPS];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const bool col_ok = (nt * 4 + (gid >> 1)) < gq;
+    const bool col_ok = G8 || (gid >> 1) < gq;
 #pragma unroll
     for (int kk = 0; kk < Lay::KT; ++kk) {
       const uint2 f = ws.qfrag[((((size_t)b * g.Hkv + kvh) * NT + nt) * Lay::KT + kk) * 32 + lane];
       qb[nt][kk][0] = col_ok ? f.x : 0u;
       qb[nt][kk][1] = col_ok ? f.y : 0u;
     }
-    const int hh = nt * 4 + tig;
-    const float* aux = ws.qaux + ((size_t)b * g.Hq + kvh * gq + min(hh, gq - 1)) * 8;
-    qscale[nt] = hh < gq ? aux[0] : 0.f;
+  }
 #pragma unroll
-    for (int gi = 0; gi < Lay::GROUPS; ++gi) qg[nt][gi] = hh < gq ? aux[1 + gi] : 0.f;
+  for (int j = 0; j < NH; ++j) {
+    const int hh = G8 ? 2 * tig + j : tig;
+    const float* aux = ws.qaux + ((size_t)b * g.Hq + kvh * gq + min(hh, gq - 1)) * 8;
+    qscale[j] = hh < gq ? aux[0] : 0.f;
+#pragma unroll
+    for (int gi = 0; gi < Lay::GROUPS; ++gi) qg[j][gi] = hh < gq ? aux[1 + gi] : 0.f;
   }
 
   const float sm_log2 = kLog2e * rsqrtf((float)D);
-  float m_run[NT], l_run[NT];
-  float acc[NT][Lay::MT][4];
-  float zacc[NT][Lay::GROUPS];
+  float m_run[NH], l_run[NH];
+  float acc[Lay::MT][4];
+  float zacc[NH][Lay::GROUPS];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m_run[nt] = -INFINITY;
-    l_run[nt] = 0.f;
+  for (int j = 0; j < NH; ++j) {
+    m_run[j] = -INFINITY;
+    l_run[j] = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < Lay::MT; ++mt)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc[nt][mt][r] = 0.f;
-#pragma unroll
-    for (int gi = 0; gi < Lay::GROUPS; ++gi) zacc[nt][gi] = 0.f;
+    for (int gi = 0; gi < Lay::GROUPS; ++gi) zacc[j][gi] = 0.f;
   }
+#pragma unroll
+  for (int mt = 0; mt < Lay::MT; ++mt)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
 
   // rows of this lane inside a 16-token block (token order sigma(k) = k/2 + 8*(k%2))
   const int ra = (gid >> 1) + 8 * (gid & 1);      // sigma(gid)
@@ -465,7 +481,7 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
       const int tb = (pg0 + it * Lay::PPS) * P + w_off;  // absolute token of row 0 of the block
       const uint8_t* buf = stage_buf + s * Lay::STAGE + pi * Lay::BLOCK;
       // ---------------- QK
-      uint32_t ua[2 * Lay::GROUPS * 2], ub[2 * Lay::GROUPS * 2];  // D/8 pairs per row
+      uint32_t ua[D / 8], ub[D / 8];  // f16 code pairs of rows ra and rb
       {
         const uint8_t* kc = buf;
         if constexpr (D == 128) {
@@ -487,43 +503,58 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
         } else {
           const uint32_t wa = *reinterpret_cast<const uint32_t*>(kc + (slot0 + ra) * Lay::ROW + tig * 4);
           const uint32_t wb = *reinterpret_cast<const uint32_t*>(kc + (slot0 + rb) * Lay::ROW + tig * 4);
-          uint32_t t8[8];
-          unpack_word(wa, t8);
-#pragma unroll
-          for (int x = 0; x < 8; ++x) ua[x] = t8[x];
-          unpack_word(wb, t8);
-#pragma unroll
-          for (int x = 0; x < 8; ++x) ub[x] = t8[x];
+          unpack_word(wa, ua);
+          unpack_word(wb, ub);
         }
       }
-      float sca[NT], scb[NT];
+      float sc[NH][2];  // scores (log2 domain) of this lane's heads for rows ra, rb
       {
-        const uint32_t* kszA = reinterpret_cast<const uint32_t*>(buf + Lay::KSZ + (slot0 + ra) * Lay::SZ);
-        const uint32_t* kszB = reinterpret_cast<const uint32_t*>(buf + Lay::KSZ + (slot0 + rb) * Lay::SZ);
         uint32_t sza[Lay::GROUPS], szb[Lay::GROUPS];
+        if constexpr (Lay::GROUPS == 4) {
+          const uint4 A4 = *reinterpret_cast<const uint4*>(buf + Lay::KSZ + (slot0 + ra) * Lay::SZ);
+          const uint4 B4 = *reinterpret_cast<const uint4*>(buf + Lay::KSZ + (slot0 + rb) * Lay::SZ);
+          sza[0] = A4.x; sza[1] = A4.y; sza[2] = A4.z; sza[3] = A4.w;
+          szb[0] = B4.x; szb[1] = B4.y; szb[2] = B4.z; szb[3] = B4.w;
+        } else {
+          const uint2 A2 = *reinterpret_cast<const uint2*>(buf + Lay::KSZ + (slot0 + ra) * Lay::SZ);
+          const uint2 B2 = *reinterpret_cast<const uint2*>(buf + Lay::KSZ + (slot0 + rb) * Lay::SZ);
+          sza[0] = A2.x; sza[1] = A2.y;
+          szb[0] = B2.x; szb[1] = B2.y;
+        }
+        float dsum[NH][2], zsum[NH][2];
+#pragma unroll
+        for (int j = 0; j < NH; ++j) dsum[j][0] = dsum[j][1] = zsum[j][0] = zsum[j][1] = 0.f;
 #pragma unroll
         for (int gi = 0; gi < Lay::GROUPS; ++gi) {
-          sza[gi] = kszA[gi];
-          szb[gi] = kszB[gi];
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kt = 0; kt < 2; ++kt) {
+            const int p8 = 4 * gi + 2 * kt;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_f16(c, ua[p8], ub[p8], ua[p8 + 1], ub[p8 + 1], qb[nt][2 * gi + kt][0], qb[nt][2 * gi + kt][1]);
+          }
+          const float s_a = bf16_lo(sza[gi]), s_b = bf16_lo(szb[gi]);
+          const float z_a = bf16_hi(sza[gi]), z_b = bf16_hi(szb[gi]);
+          if constexpr (G8) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              dsum[j][0] = fmaf(s_a, c[j], dsum[j][0]);
+              dsum[j][1] = fmaf(s_b, c[2 + j], dsum[j][1]);
+              zsum[j][0] = fmaf(z_a, qg[j][gi], zsum[j][0]);
+              zsum[j][1] = fmaf(z_b, qg[j][gi], zsum[j][1]);
+            }
+          } else {
+            dsum[0][0] = fmaf(s_a, c[0] + c[1], dsum[0][0]);
+            dsum[0][1] = fmaf(s_b, c[2] + c[3], dsum[0][1]);
+            zsum[0][0] = fmaf(z_a, qg[0][gi], zsum[0][0]);
+            zsum[0][1] = fmaf(z_b, qg[0][gi], zsum[0][1]);
+          }
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float da = 0.f, db = 0.f, za = 0.f, zb = 0.f;
-#pragma unroll
-          for (int gi = 0; gi < Lay::GROUPS; ++gi) {
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-              const int p8 = 4 * gi + 2 * kt;
-              mma_f16(c, ua[p8], ub[p8], ua[p8 + 1], ub[p8 + 1], qb[nt][2 * gi + kt][0], qb[nt][2 * gi + kt][1]);
-            }
-            da = fmaf(bf16_lo(sza[gi]), c[0] + c[1], da);
-            db = fmaf(bf16_lo(szb[gi]), c[2] + c[3], db);
-            za = fmaf(bf16_hi(sza[gi]), qg[nt][gi], za);
-            zb = fmaf(bf16_hi(szb[gi]), qg[nt][gi], zb);
-          }
-          sca[nt] = fmaf(da, qscale[nt], za) * sm_log2;
-          scb[nt] = fmaf(db, qscale[nt], zb) * sm_log2;
+        for (int j = 0; j < NH; ++j) {
+          sc[j][0] = fmaf(dsum[j][0], qscale[j], zsum[j][0]) * sm_log2;
+          sc[j][1] = fmaf(dsum[j][1], qscale[j], zsum[j][1]) * sm_log2;
         }
       }
       const int ta = tb + ra, tbk = tb + rb;
@@ -535,31 +566,49 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
       // reference m_run only moves when a block maximum exceeds it by more than
       // 2^kRescaleLog2, so the accumulators are rescaled rarely; p stays below
       // 2^kRescaleLog2, which float32 sums and bf16 operands absorb.
-      float pa[NT], pb[NT];
+      float pa[NH], pb[NH];
+      float alpha[NH];
+      bool rescale = false;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float s_a = va ? sca[nt] : -INFINITY;
-        const float s_b = vb ? scb[nt] : -INFINITY;
+      for (int j = 0; j < NH; ++j) {
+        const float s_a = va ? sc[j][0] : -INFINITY;
+        const float s_b = vb ? sc[j][1] : -INFINITY;
         float mb = fmaxf(s_a, s_b);
         mb = warp_max_xor(mb, 4);
         mb = warp_max_xor(mb, 8);
         mb = warp_max_xor(mb, 16);
-        const float m_ref = (mb > m_run[nt] + kRescaleLog2) ? mb : m_run[nt];
-        if (__any_sync(0xffffffffu, m_ref != m_run[nt])) {
-          const float alpha = (m_run[nt] == -INFINITY) ? 0.f : ex2(m_run[nt] - m_ref);
-          l_run[nt] *= alpha;
-#pragma unroll
-          for (int mt = 0; mt < Lay::MT; ++mt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[nt][mt][r] *= alpha;
-#pragma unroll
-          for (int gi = 0; gi < Lay::GROUPS; ++gi) zacc[nt][gi] *= alpha;
-          m_run[nt] = m_ref;
+        const float m_ref = (mb > m_run[j] + kRescaleLog2) ? mb : m_run[j];
+        alpha[j] = 1.f;
+        if (m_ref != m_run[j]) {
+          alpha[j] = (m_run[j] == -INFINITY) ? 0.f : ex2(m_run[j] - m_ref);
+          rescale = true;
+          m_run[j] = m_ref;
         }
-        pa[nt] = (s_a == -INFINITY) ? 0.f : ex2(s_a - m_run[nt]);
-        pb[nt] = (s_b == -INFINITY) ? 0.f : ex2(s_b - m_run[nt]);
-        l_run[nt] += pa[nt] + pb[nt];
+        pa[j] = (s_a == -INFINITY) ? 0.f : ex2(s_a - m_run[j]);
+        pb[j] = (s_b == -INFINITY) ? 0.f : ex2(s_b - m_run[j]);
       }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+          l_run[j] *= alpha[j];
+#pragma unroll
+          for (int gi = 0; gi < Lay::GROUPS; ++gi) zacc[j][gi] *= alpha[j];
+        }
+#pragma unroll
+        for (int mt = 0; mt < Lay::MT; ++mt) {
+          if constexpr (G8) {
+            acc[mt][0] *= alpha[0];
+            acc[mt][1] *= alpha[NH - 1];
+            acc[mt][2] *= alpha[0];
+            acc[mt][3] *= alpha[NH - 1];
+          } else {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[mt][r] *= alpha[0];
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NH; ++j) l_run[j] += pa[j] + pb[j];
       // ---------------- zero term of the values (rows ra, rb)
       {
         const uint32_t* vszA = reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + ra) * Lay::SZ);
@@ -569,12 +618,12 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
           const float z_a = bf16_hi(vszA[gi]);
           const float z_b = bf16_hi(vszB[gi]);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
+          for (int j = 0; j < NH; ++j) {
             if (full_block) {
-              zacc[nt][gi] = fmaf(pb[nt], z_b, fmaf(pa[nt], z_a, zacc[nt][gi]));
+              zacc[j][gi] = fmaf(pb[j], z_b, fmaf(pa[j], z_a, zacc[j][gi]));
             } else {
-              if (pa[nt] > 0.f) zacc[nt][gi] = fmaf(pa[nt], z_a, zacc[nt][gi]);
-              if (pb[nt] > 0.f) zacc[nt][gi] = fmaf(pb[nt], z_b, zacc[nt][gi]);
+              if (pa[j] > 0.f) zacc[j][gi] = fmaf(pa[j], z_a, zacc[j][gi]);
+              if (pb[j] > 0.f) zacc[j][gi] = fmaf(pb[j], z_b, zacc[j][gi]);
             }
           }
         }
@@ -613,40 +662,80 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
           unpack_word_bf16(prmt(w0, w1, sel), ux);
           unpack_word_bf16(prmt(w8, w9, sel), uy);
         }
-        const uint32_t* vs0 = reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig) * Lay::SZ);
-        const uint32_t* vs1 = reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig + 8) * Lay::SZ);
-        const uint32_t* vs8 = reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig + 4) * Lay::SZ);
-        const uint32_t* vs9 = reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig + 12) * Lay::SZ);
+        // scales of rows 2tig, 2tig+1, 2tig+8, 2tig+9 (tokens tig, tig+8, tig+4, tig+12)
+        const uint32_t* vsr[4] = {
+            reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig) * Lay::SZ),
+            reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig + 8) * Lay::SZ),
+            reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig + 4) * Lay::SZ),
+            reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig + 12) * Lay::SZ)};
+        // p of this lane's column head at rows 2tig, 2tig+1, 2tig+8, 2tig+9
         const int src0 = (2 * tig) * 4 + (gid >> 1);
         const int src1 = (2 * tig + 1) * 4 + (gid >> 1);
-        const bool lo_lane = (gid & 1) != 0;
+        float pr[4];
+        if constexpr (G8) {
+          // column head gid lives in lane group tig = gid >> 1 as its head j = gid & 1
+          const bool second = (gid & 1) != 0;
+          const float a0 = __shfl_sync(0xffffffffu, pa[0], src0), a1 = __shfl_sync(0xffffffffu, pa[NH - 1], src0);
+          const float b0 = __shfl_sync(0xffffffffu, pa[0], src1), b1 = __shfl_sync(0xffffffffu, pa[NH - 1], src1);
+          const float c0 = __shfl_sync(0xffffffffu, pb[0], src0), c1 = __shfl_sync(0xffffffffu, pb[NH - 1], src0);
+          const float d0 = __shfl_sync(0xffffffffu, pb[0], src1), d1 = __shfl_sync(0xffffffffu, pb[NH - 1], src1);
+          pr[0] = second ? a1 : a0;
+          pr[1] = second ? b1 : b0;
+          pr[2] = second ? c1 : c0;
+          pr[3] = second ? d1 : d0;
+        } else {
+          pr[0] = __shfl_sync(0xffffffffu, pa[0], src0);
+          pr[1] = __shfl_sync(0xffffffffu, pa[0], src1);
+          pr[2] = __shfl_sync(0xffffffffu, pb[0], src0);
+          pr[3] = __shfl_sync(0xffffffffu, pb[0], src1);
+        }
+        // B operands: weights w = p * scale_g, split as hi = bf16 truncation of w and
+        // lo = bf16(w - hi) (round to nearest); both go through the MMA into one accumulator
+        auto weights = [&](int gi, uint32_t& bh0, uint32_t& bh1, uint32_t& bl0, uint32_t& bl1) {
+          float w[4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const float p0 = __shfl_sync(0xffffffffu, pa[nt], src0);
-          const float p1 = __shfl_sync(0xffffffffu, pa[nt], src1);
-          const float p8v = __shfl_sync(0xffffffffu, pb[nt], src0);
-          const float p9 = __shfl_sync(0xffffffffu, pb[nt], src1);
+          for (int u = 0; u < 4; ++u) {
+            w[u] = pr[u] * bf16_lo(vsr[u][gi]);
+            if (!full_block) w[u] = pr[u] > 0.f ? w[u] : 0.f;  // unwritten slots may hold NaN scales
+          }
+          uint32_t hw[4];
+          float lo[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            hw[u] = __float_as_uint(w[u]) & 0xFFFF0000u;
+            lo[u] = w[u] - __uint_as_float(hw[u]);
+          }
+          bh0 = prmt(hw[0], hw[1], 0x7632);
+          bh1 = prmt(hw[2], hw[3], 0x7632);
+          bl0 = pack_bf162(lo[0], lo[1]);
+          bl1 = pack_bf162(lo[2], lo[3]);
+        };
+        if constexpr (G8) {
 #pragma unroll
           for (int gi = 0; gi < Lay::GROUPS; ++gi) {
-            const float pr[4] = {p0, p1, p8v, p9};
-            const uint32_t szr[4] = {vs0[gi], vs1[gi], vs8[gi], vs9[gi]};
-            float w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              w[u] = pr[u] * bf16_lo(szr[u]);
-              if (!full_block) w[u] = pr[u] > 0.f ? w[u] : 0.f;  // unwritten slots may hold NaN scales
-            }
-            // bf16 hi/lo split: hi = bf16(w), lo = bf16(w - hi); lane parity picks the column
-            const uint32_t h01 = pack_bf162(w[0], w[1]);
-            const uint32_t h23 = pack_bf162(w[2], w[3]);
-            const uint32_t l01 = pack_bf162(w[0] - bf16_lo(h01), w[1] - bf16_hi(h01));
-            const uint32_t l23 = pack_bf162(w[2] - bf16_lo(h23), w[3] - bf16_hi(h23));
-            const uint32_t b0 = lo_lane ? l01 : h01;
-            const uint32_t b1 = lo_lane ? l23 : h23;
+            uint32_t bh0, bh1, bl0, bl1;
+            weights(gi, bh0, bh1, bl0, bl1);
 #pragma unroll
             for (int mq = 0; mq < 2; ++mq) {
               const int mt = 2 * gi + mq;
-              mma_bf16(acc[nt][mt], ux[2 * mt], ux[2 * mt + 1], uy[2 * mt], uy[2 * mt + 1], b0, b1);
+              mma_bf16(acc[mt], ux[2 * mt], ux[2 * mt + 1], uy[2 * mt], uy[2 * mt + 1], bh0, bh1);
+              mma_bf16(acc[mt], ux[2 * mt], ux[2 * mt + 1], uy[2 * mt], uy[2 * mt + 1], bl0, bl1);
+            }
+          }
+        } else {
+          // column (head, parity): parity gid & 1 selects group 2*gp + parity of pair gp
+#pragma unroll
+          for (int gp = 0; gp < (Lay::GROUPS + 1) / 2; ++gp) {
+            const int gi = min(2 * gp + (gid & 1), Lay::GROUPS - 1);
+            uint32_t bh0, bh1, bl0, bl1;
+            weights(gi, bh0, bh1, bl0, bl1);
+#pragma unroll
+            for (int mq = 0; mq < 4; ++mq) {
+              const int mt = 4 * gp + mq;  // m-tiles of groups 2gp, 2gp+1
+              if (mt < Lay::MT) {
+                mma_bf16(acc[mt], ux[2 * mt], ux[2 * mt + 1], uy[2 * mt], uy[2 * mt + 1], bh0, bh1);
+                mma_bf16(acc[mt], ux[2 * mt], ux[2 * mt + 1], uy[2 * mt], uy[2 * mt + 1], bl0, bl1);
+              }
             }
           }
         }
@@ -674,15 +763,15 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
 
   // ---------------- per-warp finalisation
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], 4);
-    l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], 8);
-    l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], 16);
+  for (int j = 0; j < NH; ++j) {
+    l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
+    l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
+    l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
 #pragma unroll
     for (int gi = 0; gi < Lay::GROUPS; ++gi) {
-      zacc[nt][gi] += __shfl_xor_sync(0xffffffffu, zacc[nt][gi], 4);
-      zacc[nt][gi] += __shfl_xor_sync(0xffffffffu, zacc[nt][gi], 8);
-      zacc[nt][gi] += __shfl_xor_sync(0xffffffffu, zacc[nt][gi], 16);
+      zacc[j][gi] += __shfl_xor_sync(0xffffffffu, zacc[j][gi], 4);
+      zacc[j][gi] += __shfl_xor_sync(0xffffffffu, zacc[j][gi], 8);
+      zacc[j][gi] += __shfl_xor_sync(0xffffffffu, zacc[j][gi], 16);
     }
   }
   // cross-warp merge through shared memory (the stage ring is free now)
@@ -690,22 +779,25 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
   float* wl = wm + 32;                          // [4][8]
   float* wacc = wl + 32;                        // [4][8][D]
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int hh = nt * 4 + tig;
+  for (int j = 0; j < NH; ++j) {
+    const int hh = G8 ? 2 * tig + j : tig;
     if (hh < gq) {
       if (gid == 0) {
-        wm[warp * 8 + hh] = m_run[nt];
-        wl[warp * 8 + hh] = l_run[nt];
+        wm[warp * 8 + hh] = m_run[j];
+        wl[warp * 8 + hh] = l_run[j];
       }
 #pragma unroll
       for (int mt = 0; mt < Lay::MT; ++mt) {
         const int ch_a = 16 * mt + gid, ch_b = ch_a + 8;
+        // G8: registers (0, 2) hold head 2tig, (1, 3) head 2tig+1.  Otherwise the
+        // register of the group's parity holds the value (the other is a discarded column).
+        const int par = (mt >> 1) & 1;
+        const float ra_ = G8 ? acc[mt][j] : acc[mt][par];
+        const float rb_ = G8 ? acc[mt][2 + j] : acc[mt][2 + par];
         // channel ch of the V row sits in slot s = (ch mod 64) / 8 with bit position vpos(s)
         const int sa = (ch_a & 63) >> 3, sb = (ch_b & 63) >> 3;
-        const float va = ldexpf(acc[nt][mt][0] + acc[nt][mt][1], 7 - slot_pos_bf16(sa)) + zacc[nt][ch_a / 32];
-        const float vb = ldexpf(acc[nt][mt][2] + acc[nt][mt][3], 7 - slot_pos_bf16(sb)) + zacc[nt][ch_b / 32];
-        wacc[(warp * 8 + hh) * D + ch_a] = va;
-        wacc[(warp * 8 + hh) * D + ch_b] = vb;
+        wacc[(warp * 8 + hh) * D + ch_a] = ldexpf(ra_, 7 - slot_pos_bf16(sa)) + zacc[j][ch_a / 32];
+        wacc[(warp * 8 + hh) * D + ch_b] = ldexpf(rb_, 7 - slot_pos_bf16(sb)) + zacc[j][ch_b / 32];
       }
     }
   }

@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 2) write_kernel(WriteArgs a
   const bool is_v = blockIdx.y == 1;
   const Geom& g = a.g;
   const void* src = is_v ? a.V : a.K;
-  {
+  if (!a.hadamard) {  // the Hadamard-only rotation has no matrix (R_K, R_V are null)
     const float4* Rg = reinterpret_cast<const float4*>(is_v ? a.R_V : a.R_K);
     float4* R4 = reinterpret_cast<float4*>(Rs);
     for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) R4[i] = Rg[i];
