@@ -261,7 +261,9 @@ def test_decode_independent_of_split_count(osc):
         a = H.run_decode(gc, 0, q, "bf16", bt, [n], [0], fx, max_seq=n)
         b = H.run_decode(gc, 0, q, "bf16", bt, [n], [0], fx, max_seq=ppr * 64)
         rms = np.sqrt(np.mean(a ** 2))
-        assert np.abs(a - b).max() / rms < 2e-5
+        # each split keeps its own softmax reference, so the bf16 hi/lo split of p*scale rounds
+        # differently (~2^-16 relative per weight); a merging bug would show at O(1)
+        assert np.abs(a - b).max() / rms < 2e-4
     finally:
         gc.close()
 
