@@ -23,7 +23,7 @@
  *    bounded wait that timed out) set a status word read by
  *    oscar_check_status().
  *  - Row-vector convention: a rotated vector is y = x R, R is d x d float32
- *    row-major (R[i*d + j]).
+ *    row-major (R[i*d + j]), 16-byte aligned (OSCAR_ERR_INVALID otherwise).
  *  - bf16 tensors are uint16 bit patterns of bfloat16.
  *
  * Memory layout (all little-endian)

@@ -146,9 +146,9 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 __host__ __device__ constexpr int slot_pos(int x) { return x < 5 ? 2 * x : 2 * x - 6; }
 
 __device__ __forceinline__ uint32_t hsub2_one(uint32_t v) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x3C003C00u));
-  return r;
+  const __half2 x = *reinterpret_cast<const __half2*>(&v);
+  const __half2 r = __hsub2(x, __half2half2(__ushort_as_half(0x3C00)));
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 template <int X>
@@ -177,9 +177,9 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t (&o)[8]) {
 __host__ __device__ constexpr int slot_pos_bf16(int x) { return x < 3 ? 2 * x : (x < 6 ? 2 * (x - 3) : 2 * (x - 6)); }
 
 __device__ __forceinline__ uint32_t bsub2_one(uint32_t v) {
-  uint32_t r;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x3F803F80u));
-  return r;
+  const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&v);
+  const __nv_bfloat162 r = __hsub2(x, __bfloat162bfloat162(__ushort_as_bfloat16(0x3F80)));
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 template <int X>
@@ -202,11 +202,7 @@ __device__ __forceinline__ void unpack_word_bf16(uint32_t w, uint32_t (&o)[8]) {
   o[7] = unpack_slot_bf16<7>(w, w6, w12);
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo_elem, float hi_elem) {
   __half2 h = __floats2half2_rn(lo_elem, hi_elem);
@@ -221,7 +217,13 @@ __device__ __forceinline__ uint32_t pack_bf162(float lo_elem, float hi_elem) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ float ex2(float x) { return exp2f(x); }
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error ~2^-22,
+// ex2(-inf) = 0); used for softmax weights, which tolerate it.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ float warp_max_xor(float v, int lane_mask) {
   return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, lane_mask));

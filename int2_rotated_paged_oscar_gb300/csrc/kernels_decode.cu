@@ -118,11 +118,14 @@ __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int j = threadIdx.x, warp = j >> 5, lane = j & 31;
   const int gq = g.gq();
+  __shared__ __align__(8) uint64_t bar;
   WsView ws = ws_view(a);
-  {
-    const float4* Rg = reinterpret_cast<const float4*>(a.R_K);
-    float4* R4 = reinterpret_cast<float4*>(Rs);
-    for (int i = j; i < D * D / 4; i += kThreads) R4[i] = Rg[i];
+  // R_K (D*D floats) arrives by one bulk copy while the threads load q
+  if (j == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(&bar, D * D * sizeof(float));
+    bulk_g2s(Rs, a.R_K, D * D * sizeof(float), &bar);
   }
   const size_t qbase = ((size_t)b * g.Hq + (size_t)kvh * gq) * D;
   for (int i = j; i < gq * D; i += kThreads) {
@@ -131,6 +134,12 @@ __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
     ws.qplain[qbase + i] = v;
   }
   __syncthreads();
+  // every thread waits for the copy; a timeout flags the status word and the
+  // kernel still waits (bounded) once more so the copy is not in flight at exit
+  if (!mbar_wait_bounded(&bar, 0, a.status)) {
+    (void)mbar_wait_bounded(&bar, 0, nullptr);
+    return;
+  }
   float acc[8];
 #pragma unroll
   for (int hh = 0; hh < 8; ++hh) acc[hh] = 0.f;
@@ -826,93 +835,121 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
 }
 
 // ------------------------------------------------------------------ combine
-// grid (Hq, B), block 128.  Merges the window partials (plain basis) and the
-// INT2 partials (rotated basis), applies R_V^T once, divides by l.
+// grid (Hq / hpc, B), block 128.  One CTA handles hpc query heads of one
+// request: it merges the window partials (plain basis) and the INT2 partials
+// (rotated basis), applies R_V^T once per head, divides by l.  R_V and, when the
+// plan says they fit, the heads' partials are staged in shared memory by bulk
+// copies; otherwise the partials are read from global memory.
 template <int D>
 __global__ void __launch_bounds__(kThreads) decode_combine_kernel(DecodeArgs a) {
   constexpr int C = D / 32;
-  pdl_wait();
-  const Geom& g = a.g;
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  extern __shared__ __align__(16) float csm[];
+  float* Rs = csm;                 // [D][D]
+  float* parts = Rs + D * D;       // [hpc][stride][D + 4] when staged
   __shared__ float rot[D];
   __shared__ float rotated_out[D];
   __shared__ float wts[kMaxSplits + kMaxWinChunks];
   __shared__ float s_l;
+  __shared__ __align__(8) uint64_t bar;
+  const Geom& g = a.g;
+  const int hpc = a.wl.combine_hpc;
+  const int b = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   WsView ws = ws_view(a);
-  const int n = a.seq_lens[b];
   const int wc = a.wl.win_chunks;
+  const int stride = wc + a.wl.max_splits;
+  const size_t head_bytes = (size_t)stride * (D + 4) * sizeof(float);
+  const int h0 = blockIdx.x * hpc;
+  const float* gbase = ws.part + ((size_t)b * g.Hq + h0) * stride * (D + 4);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // R_V does not depend on the previous kernel: start its copy before waiting on it
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar, D * D * sizeof(float) + (a.wl.combine_part_smem ? hpc * head_bytes : 0));
+    bulk_g2s(Rs, a.R_V, D * D * sizeof(float), &bar);
+  }
+  pdl_wait();
+  if (tid == 0 && a.wl.combine_part_smem) bulk_g2s(parts, gbase, (uint32_t)(hpc * head_bytes), &bar);
+  const int n = a.seq_lens[b];
   const int nsp = seq_len_ok(a, n) ? min(splits_for(a, n), kMaxSplits) : 0;
   const int nslot = wc + nsp;
-  const int stride = wc + a.wl.max_splits;
-  const float* base = ws.part + ((size_t)b * g.Hq + h) * stride * (D + 4);
-  if (warp == 0) {
-    float M = -INFINITY;
-    for (int i = lane; i < nslot; i += 32) M = fmaxf(M, base[(size_t)i * (D + 4)]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
-    for (int i = lane; i < nslot; i += 32) {
-      const float mi = base[(size_t)i * (D + 4)];
-      const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
-      wts[i] = w;
-      L = fmaf(w, base[(size_t)i * (D + 4) + 1], L);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) s_l = L;
+  if (!mbar_wait_bounded(&bar, 0, a.status)) {
+    (void)mbar_wait_bounded(&bar, 0, nullptr);
+    return;
   }
-  __syncthreads();
-  float plain = 0.f;
-  if (tid < D) {
-    for (int i = 0; i < wc; ++i) plain = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + tid], plain);
-    float r = 0.f;
-#pragma unroll 8
-    for (int i = wc; i < nslot; ++i) r = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + tid], r);
-    rot[tid] = r;
-  }
-  __syncthreads();
-  // (rot R_V^T)_j = sum_k rot_k R_V[j][k]: warp w handles rows [w*D/4, (w+1)*D/4) in batches of 8,
-  // lane l reads the contiguous slice [l*C, (l+1)*C) of each row
-  float rl[C];
+  for (int hi = 0; hi < hpc; ++hi) {
+    const int h = h0 + hi;
+    const float* base = a.wl.combine_part_smem ? parts + (size_t)hi * stride * (D + 4)
+                                               : gbase + (size_t)hi * stride * (D + 4);
+    if (warp == 0) {
+      float M = -INFINITY;
+      for (int i = lane; i < nslot; i += 32) M = fmaxf(M, base[(size_t)i * (D + 4)]);
 #pragma unroll
-  for (int c = 0; c < C; ++c) rl[c] = rot[lane * C + c];
-  for (int j0 = warp * (D / 4); j0 < (warp + 1) * (D / 4); j0 += 8) {
-    float sacc[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const float* row = a.R_V + (size_t)(j0 + r) * D + lane * C;
-      float v[C];
-      if constexpr (C == 4) {
-        const float4 q4 = *reinterpret_cast<const float4*>(row);
-        v[0] = q4.x; v[1] = q4.y; v[2] = q4.z; v[3] = q4.w;
-      } else {
-        const float2 q2 = *reinterpret_cast<const float2*>(row);
-        v[0] = q2.x; v[1] = q2.y;
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float L = 0.f;
+      for (int i = lane; i < nslot; i += 32) {
+        const float mi = base[(size_t)i * (D + 4)];
+        const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
+        wts[i] = w;
+        L = fmaf(w, base[(size_t)i * (D + 4) + 1], L);
       }
-      float t = 0.f;
 #pragma unroll
-      for (int c = 0; c < C; ++c) t = fmaf(rl[c], v[c], t);
-      sacc[r] = t;
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      if (lane == 0) s_l = L;
     }
+    __syncthreads();
+    float plain = 0.f;
+    if (tid < D) {
+      for (int i = 0; i < wc; ++i) plain = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + tid], plain);
+      float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+      int i = wc;
+      for (; i + 3 < nslot; i += 4) {
+        r0 = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + tid], r0);
+        r1 = fmaf(wts[i + 1], base[(size_t)(i + 1) * (D + 4) + 4 + tid], r1);
+        r2 = fmaf(wts[i + 2], base[(size_t)(i + 2) * (D + 4) + 4 + tid], r2);
+        r3 = fmaf(wts[i + 3], base[(size_t)(i + 3) * (D + 4) + 4 + tid], r3);
+      }
+      for (; i < nslot; ++i) r0 = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + tid], r0);
+      rot[tid] = (r0 + r1) + (r2 + r3);
+    }
+    __syncthreads();
+    // (rot R_V^T)_j = sum_k rot_k R_V[j][k]: warp w handles rows [w*D/4, (w+1)*D/4) in batches of 8
+    float rl[C];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int c = 0; c < C; ++c) rl[c] = rot[lane * C + c];
+    for (int j0 = warp * (D / 4); j0 < (warp + 1) * (D / 4); j0 += 8) {
+      float sacc[8];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sacc[r] += __shfl_xor_sync(0xffffffffu, sacc[r], o);
-      if (lane == r) rotated_out[j0 + r] = sacc[r];
+      for (int r = 0; r < 8; ++r) {
+        const float* row = Rs + (j0 + r) * D + lane * C;
+        float t = 0.f;
+#pragma unroll
+        for (int c = 0; c < C; ++c) t = fmaf(rl[c], row[c], t);
+        sacc[r] = t;
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sacc[r] += __shfl_xor_sync(0xffffffffu, sacc[r], o);
+        if (lane == r) rotated_out[j0 + r] = sacc[r];
+      }
     }
-  }
-  __syncthreads();
-  if (tid < D) {
-    const float inv = s_l > 0.f ? 1.f / s_l : 0.f;
-    const float o = (plain + rotated_out[tid]) * inv;
-    const size_t oi = ((size_t)b * g.Hq + h) * D + tid;
-    if (a.out_dtype == kDtypeBF16) {
-      __nv_bfloat16 hb = __float2bfloat16_rn(o);
-      static_cast<uint16_t*>(a.out)[oi] = *reinterpret_cast<uint16_t*>(&hb);
-    } else {
-      static_cast<float*>(a.out)[oi] = o;
+    __syncthreads();
+    if (tid < D) {
+      const float inv = s_l > 0.f ? 1.f / s_l : 0.f;
+      const float o = (plain + rotated_out[tid]) * inv;
+      const size_t oi = ((size_t)b * g.Hq + h) * D + tid;
+      if (a.out_dtype == kDtypeBF16) {
+        __nv_bfloat16 hb = __float2bfloat16_rn(o);
+        static_cast<uint16_t*>(a.out)[oi] = *reinterpret_cast<uint16_t*>(&hb);
+      } else {
+        static_cast<float*>(a.out)[oi] = o;
+      }
     }
+    __syncthreads();
   }
 }
 
@@ -997,7 +1034,7 @@ int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl) {
 int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.g.Hq, a.batch);
+  cfg.gridDim = dim3(a.g.Hq / a.wl.combine_hpc, a.batch);
   cfg.blockDim = dim3(kThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1005,7 +1042,13 @@ int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (a.g.D == 128) return (int)cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, a);
+  cfg.dynamicSmemBytes = a.wl.combine_smem;
+  cudaError_t e;
+  if (a.g.D == 128) {
+    if ((e = ensure_smem_limit(decode_combine_kernel<128>, a.wl.combine_smem)) != cudaSuccess) return (int)e;
+    return (int)cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, a);
+  }
+  if ((e = ensure_smem_limit(decode_combine_kernel<64>, a.wl.combine_smem)) != cudaSuccess) return (int)e;
   return (int)cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, a);
 }
 

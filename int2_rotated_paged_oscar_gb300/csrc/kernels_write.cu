@@ -448,13 +448,24 @@ __global__ void __launch_bounds__(256) append_kernel(WriteArgs a) {
     float acc[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) acc[c] = 0.f;
+    // all of this chain's R rows are loaded before the FMAs (16-byte vectors)
+    float rv[D / 4][C];
 #pragma unroll
     for (int i = 0; i < D / 4; ++i) {
-      const int ii = k * (D / 4) + i;
-      const float xi = xs[kv][ii];
-      const float* r = R + (size_t)ii * D + lane * C;
+      const float* r = R + (size_t)(k * (D / 4) + i) * D + lane * C;
+      if constexpr (C == 4) {
+        const float4 q4 = __ldg(reinterpret_cast<const float4*>(r));
+        rv[i][0] = q4.x; rv[i][1] = q4.y; rv[i][2] = q4.z; rv[i][3] = q4.w;
+      } else {
+        const float2 q2 = __ldg(reinterpret_cast<const float2*>(r));
+        rv[i][0] = q2.x; rv[i][1] = q2.y;
+      }
+    }
 #pragma unroll
-      for (int c = 0; c < C; ++c) acc[c] = fmaf(xi, r[c], acc[c]);
+    for (int i = 0; i < D / 4; ++i) {
+      const float xi = xs[kv][k * (D / 4) + i];
+#pragma unroll
+      for (int c = 0; c < C; ++c) acc[c] = fmaf(xi, rv[i][c], acc[c]);
     }
 #pragma unroll
     for (int c = 0; c < C; ++c) part[kv][k][lane * C + c] = acc[c];

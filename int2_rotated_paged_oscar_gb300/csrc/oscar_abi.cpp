@@ -149,6 +149,13 @@ oscar_status need_device(oscar_ctx* ctx) {
   return OSCAR_OK;
 }
 
+// The kernels stage R with 16-byte vector loads and bulk copies.
+oscar_status check_r_align(const float* R_K, const float* R_V) {
+  if ((reinterpret_cast<uintptr_t>(R_K) | reinterpret_cast<uintptr_t>(R_V)) & 15)
+    return fail(OSCAR_ERR_INVALID, "R_K and R_V must be 16-byte aligned");
+  return OSCAR_OK;
+}
+
 oscar_status check_layer(const oscar_ctx* ctx, int32_t layer) {
   if (layer < 0 || layer >= ctx->g.L) return fail(OSCAR_ERR_INVALID, "layer %d out of [0, %d)", layer, ctx->g.L);
   return OSCAR_OK;
@@ -167,9 +174,16 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   long long max_pages;
   if (bf16_pool) max_pages = max_seq > 0 ? (max_seq - 1) / g.P + 1 : 0;
   else max_pages = (max_seq - g.W > g.S) ? (long long)(max_seq - g.W - 1) / g.P + 1 : 0;
-  const long long target_ctas = 152LL * 4;
-  const long long total = (long long)batch * g.Hkv * max_pages;
-  long long pps = (total + target_ctas - 1) / target_ctas;
+  // Size the INT2 splits so that window CTAs plus INT2 CTAs fill the resident
+  // CTA slots of one wave (152 SMs x CTAs per SM at the kernel's register use);
+  // more requests than that run in several full waves.
+  const int occ = bf16_pool ? 2 : (w.nt == 2 ? 3 : 5);
+  const long long win_ctas = bf16_pool ? 0 : (long long)batch * g.Hkv * ((g.S + g.W + 15) / 16);
+  long long free_slots = 152LL * occ - win_ctas;
+  if (free_slots < (long long)batch * g.Hkv) free_slots = (long long)batch * g.Hkv;
+  long long split_target = free_slots / ((long long)batch * g.Hkv > 0 ? (long long)batch * g.Hkv : 1);
+  if (split_target < 1) split_target = 1;
+  long long pps = max_pages > 0 ? (max_pages + split_target - 1) / split_target : stage_pages;
   if (pps < stage_pages) pps = stage_pages;
   pps = (pps + stage_pages - 1) / stage_pages * stage_pages;
   long long splits = max_pages > 0 ? (max_pages + pps - 1) / pps : 0;
@@ -192,6 +206,21 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   const size_t slots = (size_t)w.max_splits + (size_t)w.win_chunks;
   off = align(off + (size_t)batch * g.Hq * slots * (g.D + 4) * sizeof(float));
   w.total = off;
+  // combine: R_V (D*D floats) plus, if they fit, the split partials of hpc heads
+  // in shared memory; hpc is the largest power-of-two divisor of gq that fits
+  const size_t rv_bytes = (size_t)g.D * g.D * sizeof(float);
+  const size_t per_head = slots * (g.D + 4) * sizeof(float);
+  const size_t budget = 200 * 1024;
+  w.combine_hpc = 1;
+  w.combine_part_smem = 0;
+  for (int h = gq; h >= 1; h >>= 1) {
+    if (rv_bytes + (size_t)h * per_head <= budget) {
+      w.combine_hpc = h;
+      w.combine_part_smem = 1;
+      break;
+    }
+  }
+  w.combine_smem = rv_bytes + (w.combine_part_smem ? (size_t)w.combine_hpc * per_head : 0) + 64;
   return w;
 }
 
@@ -398,6 +427,7 @@ static oscar_status write_common(oscar_ctx* ctx, int32_t layer, const void* K, c
   if (!cu_seqlens || !start_pos || !block_table || !req_slot || (total_tokens > 0 && (!K || !V)))
     return fail(OSCAR_ERR_INVALID, "null tensor argument");
   if (!hadamard && (!R_K || !R_V)) return fail(OSCAR_ERR_INVALID, "R_K / R_V are null");
+  if (!hadamard && (st = check_r_align(R_K, R_V)) != OSCAR_OK) return st;
   if (dtype != OSCAR_DTYPE_BF16 && dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad dtype %d", dtype);
   if (!(clip_K > 0.f) || !(clip_V > 0.f)) return fail(OSCAR_ERR_INVALID, "clip thresholds must be positive");
   WriteArgs a{};
@@ -461,6 +491,7 @@ oscar_status oscar_append_step(oscar_ctx* ctx, int32_t layer, const void* K_new,
   if (batch == 0) return OSCAR_OK;
   if (!K_new || !V_new || !seq_lens_before || !R_K || !R_V || !block_table || !req_slot)
     return fail(OSCAR_ERR_INVALID, "null tensor argument");
+  if ((st = check_r_align(R_K, R_V)) != OSCAR_OK) return st;
   if (dtype != OSCAR_DTYPE_BF16 && dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad dtype %d", dtype);
   if (!(clip_K > 0.f) || !(clip_V > 0.f)) return fail(OSCAR_ERR_INVALID, "clip thresholds must be positive");
   WriteArgs a{};
@@ -537,6 +568,7 @@ oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
     return fail(OSCAR_ERR_INVALID, "sink/recent (%d, %d) differ from the cache configuration (%d, %d)", sink, recent,
                 ctx->g.S, ctx->g.W);
   if (!req_slot || !R_K || !R_V) return fail(OSCAR_ERR_INVALID, "null tensor argument");
+  if ((st = check_r_align(R_K, R_V)) != OSCAR_OK) return st;
   DecodeArgs a{};
   a.g = ctx->g;
   a.layer = layer;
@@ -595,6 +627,7 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
   if (batch == 0) return OSCAR_OK;
   if (!q || !out || !block_table || !seq_lens || !req_slot || !R_K || !R_V)
     return fail(OSCAR_ERR_INVALID, "null tensor argument");
+  if ((st = check_r_align(R_K, R_V)) != OSCAR_OK) return st;
   if (q_dtype != OSCAR_DTYPE_BF16 && q_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad q dtype");
   if (out_dtype != OSCAR_DTYPE_BF16 && out_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad out dtype");
   if (sink != ctx->g.S || recent != ctx->g.W)

@@ -71,6 +71,9 @@ struct DecodeWs {
   int pages_per_split;   // multiple of 64 / page_size
   int nt;                // query n-tiles (max(1, 2*gq/8))
   int win_chunks;        // BF16 window CTAs per (request, kv head): grid.x = win_chunks + max_splits
+  int combine_hpc;       // query heads per combine CTA (divides gq)
+  int combine_part_smem; // 1: the combine CTA stages its split partials in shared memory
+  size_t combine_smem;   // dynamic shared memory of the combine kernel
 };
 
 struct DecodeArgs {
