@@ -103,117 +103,102 @@ __device__ __forceinline__ bool seq_len_ok(const DecodeArgs& a, int n) {
 }
 
 // ------------------------------------------------------------------ q rotate
-// grid (Hkv, B), block 128, dynamic shared memory: R_K (D*D floats) + q and q'
-// of the group's gq heads.  R_K is read once per (request, kv head); thread
-// j < D computes q'_j = sum_i q_i R_K[i][j] for every head of the group.
+// grid (Hkv * D/32, B), block 128.  CTA (kvh, grp) computes the 32 rotated
+// channels of group grp, q'_j = sum_i q_i R_K[i][j] for j in [32 grp, 32 grp + 32),
+// for every query head of kv head kvh, and writes the group sum Q_g and the
+// query-side MMA fragments of its two k-tiles.  The power-of-two scale of head
+// h is set from ||q_h||_2, which bounds |q'_h|_inf (R_K is orthogonal), so the
+// CTAs of a head need not agree on a maximum.
 template <int D>
 __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
   pdl_launch_dependents();
-  extern __shared__ __align__(16) float qsm_dyn[];
-  float* Rs = qsm_dyn;        // [D][D]
-  float* qs = Rs + D * D;     // [8][D]
-  float* qr = qs + 8 * D;     // [8][D]
-  __shared__ float red[kThreads / 32][8];
+  __shared__ __align__(16) float Rs[D][33];   // R_K[:, 32 grp + c], padded
+  __shared__ float qs[8][D];
+  __shared__ float qr[8][32];
+  __shared__ float nrm[8];
   const Geom& g = a.g;
-  const int kvh = blockIdx.x, b = blockIdx.y;
-  const int j = threadIdx.x, warp = j >> 5, lane = j & 31;
+  const int grp = blockIdx.x % (D / 32), kvh = blockIdx.x / (D / 32), b = blockIdx.y;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int gq = g.gq();
-  __shared__ __align__(8) uint64_t bar;
   WsView ws = ws_view(a);
-  // R_K (D*D floats) arrives by one bulk copy while the threads load q
-  if (j == 0) {
-    mbar_init(&bar, 1);
-    fence_barrier_init();
-    mbar_arrive_expect_tx(&bar, D * D * sizeof(float));
-    bulk_g2s(Rs, a.R_K, D * D * sizeof(float), &bar);
+  // R_K column slice: D rows x 32 floats (8 float4 per row), 16-byte loads, all in flight
+  {
+    const float4* Rg = reinterpret_cast<const float4*>(a.R_K);
+    float4 v[D * 8 / kThreads];
+#pragma unroll
+    for (int u = 0; u < D * 8 / kThreads; ++u) {
+      const int idx = t + u * kThreads;  // row idx / 8, float4 idx % 8
+      v[u] = __ldg(Rg + (size_t)(idx >> 3) * (D / 4) + grp * 8 + (idx & 7));
+    }
+#pragma unroll
+    for (int u = 0; u < D * 8 / kThreads; ++u) {
+      const int idx = t + u * kThreads;
+      float* dst = &Rs[idx >> 3][(idx & 7) * 4];
+      dst[0] = v[u].x; dst[1] = v[u].y; dst[2] = v[u].z; dst[3] = v[u].w;
+    }
   }
   const size_t qbase = ((size_t)b * g.Hq + (size_t)kvh * gq) * D;
-  for (int i = j; i < gq * D; i += kThreads) {
-    const float v = load_q(a, qbase + i);
-    qs[i] = v;
-    ws.qplain[qbase + i] = v;
+  for (int i = t; i < gq * D; i += kThreads) {
+    const float x = load_q(a, qbase + i);
+    qs[i / D][i % D] = x;
+    if (grp == 0) ws.qplain[qbase + i] = x;
   }
   __syncthreads();
-  // every thread waits for the copy; a timeout flags the status word and the
-  // kernel still waits (bounded) once more so the copy is not in flight at exit
-  if (!mbar_wait_bounded(&bar, 0, a.status)) {
-    (void)mbar_wait_bounded(&bar, 0, nullptr);
-    return;
+  // squared norms: warp w sums heads w, w + 4
+  for (int hh = warp; hh < gq; hh += kThreads / 32) {
+    float ss = 0.f;
+    for (int i = lane; i < D; i += 32) ss = fmaf(qs[hh][i], qs[hh][i], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) nrm[hh] = sqrtf(ss);
   }
-  float acc[8];
+  // rotation: lane = channel 32 grp + lane, warp w handles heads w, w + 4
+  for (int hh = warp; hh < gq; hh += kThreads / 32) {
+    float acc = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < D; ++i) acc = fmaf(qs[hh][i], Rs[i][lane], acc);
+    qr[hh][lane] = acc;
+    float gs = acc;
 #pragma unroll
-  for (int hh = 0; hh < 8; ++hh) acc[hh] = 0.f;
-  if (j < D) {
-#pragma unroll 4
-    for (int i = 0; i < D; ++i) {
-      const float r = Rs[i * D + j];
-#pragma unroll
-      for (int hh = 0; hh < 8; ++hh)
-        if (hh < gq) acc[hh] = fmaf(qs[hh * D + i], r, acc[hh]);
-    }
-#pragma unroll
-    for (int hh = 0; hh < 8; ++hh)
-      if (hh < gq) qr[hh * D + j] = acc[hh];
-  }
-  // per-head max |q'| (for the power-of-two normalisation) and group sums Q_g
-#pragma unroll
-  for (int hh = 0; hh < 8; ++hh) {
-    if (hh >= gq) break;
-    float m = j < D ? fabsf(acc[hh]) : 0.f;
-    float sg = j < D ? acc[hh] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      sg += __shfl_xor_sync(0xffffffffu, sg, o);
-    }
-    if (lane == 0) {
-      red[warp][hh] = m;
-      if (warp < D / 32) ws.qaux[((size_t)b * g.Hq + (size_t)kvh * gq + hh) * 8 + 1 + warp] = sg;  // group = warp
-    }
+    for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+    if (lane == 0) ws.qaux[((size_t)b * g.Hq + (size_t)kvh * gq + hh) * 8 + 1 + grp] = gs;
   }
   __syncthreads();
-  for (int hh = 0; hh < gq; ++hh) {
-    float mx = 0.f;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) mx = fmaxf(mx, red[w][hh]);
+  // fragments of the two k-tiles of this group: 8 lanes x 2 k-tiles per head
+  for (int idx = t; idx < gq * 16; idx += kThreads) {
+    const int hh = idx >> 4, sub = idx & 15;
+    const int kt = sub >> 3, hl = (sub >> 2) & 1, tig = sub & 3;
     int e = 0;
+    const float mx = nrm[hh];
     if (mx > 0.f) {
       int E;
-      frexpf(mx, &E);  // mx = f * 2^E, f in [0.5, 1)
-      e = 5 - E;       // mx * 2^e in [16, 32): times 2^(10-pos) <= 1024 stays below the f16 maximum
+      frexpf(mx, &E);  // |q'|_inf <= ||q||_2 = mx * (1 + rounding) < 2^E
+      e = 5 - E;       // |q'| * 2^e < 32: times 2^(10-pos) <= 1024 stays below the f16 maximum
     }
-    if (j == 0) ws.qaux[((size_t)b * g.Hq + (size_t)kvh * gq + hh) * 8] = ldexpf(1.f, -e);
-    // query-side fragments of the QK MMA.  Up to 4 heads: head hh owns columns
-    // 2*hh + {hi, lo} of one operand.  8 heads: column hh of two operand planes
-    // (plane 0 = hi, plane 1 = lo) that accumulate into the same registers.
-    if (j < (D / 16) * 8) {
-      const int kk = j >> 3;  // k-tile = (group, kt)
-      const int sub = j & 7;
-      const int hl = sub >> 2, tig = sub & 3;
-      const bool g8 = gq == 8;
-      const int gid = g8 ? hh : 2 * (hh & 3) + hl;
-      const int plane = g8 ? hl : 0;
-      const int ln = gid * 4 + tig;
-      const int gi = kk >> 1, kt = kk & 1;
-      const int p8 = 4 * gi + 2 * kt;
-      uint32_t regs[2];
+    if (grp == 0 && sub == 0) ws.qaux[((size_t)b * g.Hq + (size_t)kvh * gq + hh) * 8] = ldexpf(1.f, -e);
+    const bool g8 = gq == 8;
+    const int gid = g8 ? hh : 2 * (hh & 3) + hl;
+    const int plane = g8 ? hl : 0;
+    const int ln = gid * 4 + tig;
+    const int kk = 2 * grp + kt;
+    const int p8 = 4 * grp + 2 * kt;
+    uint32_t regs[2];
 #pragma unroll
-      for (int hpair = 0; hpair < 2; ++hpair) {
-        const int ch = 32 * gi + 16 * kt + 8 * hpair + 2 * tig;
-        const int pos = slot_pos((p8 + hpair) & 7);
-        float v[2];
+    for (int hpair = 0; hpair < 2; ++hpair) {
+      const int ch = 16 * kt + 8 * hpair + 2 * tig;  // channel within the group
+      const int pos = slot_pos((p8 + hpair) & 7);
+      float v[2];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const float x = ldexpf(qr[hh * D + ch + u], e + 10 - pos);
-          const __half hi = __float2half_rn(x);
-          const float lo = x - __half2float(hi);
-          v[u] = hl ? lo : __half2float(hi);
-        }
-        regs[hpair] = pack_half2(v[0], v[1]);
+      for (int u = 0; u < 2; ++u) {
+        const float x = ldexpf(qr[hh][ch + u], e + 10 - pos);
+        const __half hi = __float2half_rn(x);
+        const float lo = x - __half2float(hi);
+        v[u] = hl ? lo : __half2float(hi);
       }
-      const size_t fidx = ((((size_t)b * g.Hkv + kvh) * a.wl.nt + plane) * (D / 16) + kk) * 32 + ln;
-      ws.qfrag[fidx] = make_uint2(regs[0], regs[1]);
+      regs[hpair] = pack_half2(v[0], v[1]);
     }
+    const size_t fidx = ((((size_t)b * g.Hkv + kvh) * a.wl.nt + plane) * (D / 16) + kk) * 32 + ln;
+    ws.qfrag[fidx] = make_uint2(regs[0], regs[1]);
   }
 }
 
@@ -990,10 +975,7 @@ int launch_splitk_p(const DecodeArgs& a, cudaStream_t s, bool pdl) {
 
 template <int D>
 int launch_q_rotate_t(const DecodeArgs& a, cudaStream_t s) {
-  const size_t smem = sizeof(float) * (D * D + 16 * D);
-  cudaError_t e = ensure_smem_limit(q_rotate_kernel<D>, smem);
-  if (e != cudaSuccess) return (int)e;
-  q_rotate_kernel<D><<<dim3(a.g.Hkv, a.batch), kThreads, smem, s>>>(a);
+  q_rotate_kernel<D><<<dim3(a.g.Hkv * (D / 32), a.batch), kThreads, 0, s>>>(a);
   return (int)cudaGetLastError();
 }
 

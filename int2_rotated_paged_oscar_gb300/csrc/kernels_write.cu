@@ -411,16 +411,19 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) evict_kernel(WriteArgs a) {
 }
 
 // ------------------------------------------------------------------ decode append
-// grid = (batch, Hkv), block = 8 warps: warp w works on K (w < 4) or V, and on
-// rotation chain k = w % 4 (input channels [kD/4, (k+1)D/4)), so each warp has
-// all of its R loads in flight at once.  The chain-0 warp of K and of V adds
-// the four chains in the canonical order, quantises and packs.
+// grid = (batch, Hkv), block = 8 warps, dynamic shared memory = R_K and R_V
+// (2*D*D floats), brought in by two bulk copies.  Warp w works on K (w < 4) or V,
+// and on rotation chain k = w % 4 (input channels [kD/4, (k+1)D/4)).  The
+// chain-0 warp of K and of V adds the four chains in the canonical order,
+// quantises and packs.
 template <int D>
 __global__ void __launch_bounds__(256) append_kernel(WriteArgs a) {
   constexpr int C = D / 32;
+  extern __shared__ __align__(16) float Rsm[];  // [2][D][D]
   __shared__ float xs[2][D];
   __shared__ float part[2][4][D];
   __shared__ uint8_t code_scratch[2][D];
+  __shared__ __align__(8) uint64_t bar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geom& g = a.g;
   const int b = blockIdx.x, h = blockIdx.y;
@@ -441,31 +444,31 @@ __global__ void __launch_bounds__(256) append_kernel(WriteArgs a) {
   const int e = n0 - g.W;
   const bool evict = e >= g.S;  // the evicted token occupies the slot the new token takes
   if (evict) {
+    if (threadIdx.x == 0) {
+      mbar_init(&bar, 1);
+      fence_barrier_init();
+      mbar_arrive_expect_tx(&bar, 2 * D * D * sizeof(float));
+      bulk_g2s(Rsm, a.R_K, D * D * sizeof(float), &bar);
+      bulk_g2s(Rsm + D * D, a.R_V, D * D * sizeof(float), &bar);
+    }
     if (k == 0)
       for (int c = lane; c < D; c += 32) xs[kv][c] = __uint_as_float(static_cast<uint32_t>(ring[c]) << 16);
     __syncthreads();
-    const float* R = is_v ? a.R_V : a.R_K;
+    if (!mbar_wait_bounded(&bar, 0, a.status)) {
+      (void)mbar_wait_bounded(&bar, 0, nullptr);
+      return;  // uniform: every thread times out on the same copy
+    }
+    const float* R = Rsm + kv * D * D;
     float acc[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) acc[c] = 0.f;
-    // all of this chain's R rows are loaded before the FMAs (16-byte vectors)
-    float rv[D / 4][C];
-#pragma unroll
+#pragma unroll 8
     for (int i = 0; i < D / 4; ++i) {
-      const float* r = R + (size_t)(k * (D / 4) + i) * D + lane * C;
-      if constexpr (C == 4) {
-        const float4 q4 = __ldg(reinterpret_cast<const float4*>(r));
-        rv[i][0] = q4.x; rv[i][1] = q4.y; rv[i][2] = q4.z; rv[i][3] = q4.w;
-      } else {
-        const float2 q2 = __ldg(reinterpret_cast<const float2*>(r));
-        rv[i][0] = q2.x; rv[i][1] = q2.y;
-      }
-    }
+      const int ii = k * (D / 4) + i;
+      const float xi = xs[kv][ii];
+      const float* r = R + ii * D + lane * C;
 #pragma unroll
-    for (int i = 0; i < D / 4; ++i) {
-      const float xi = xs[kv][k * (D / 4) + i];
-#pragma unroll
-      for (int c = 0; c < C; ++c) acc[c] = fmaf(xi, rv[i][c], acc[c]);
+      for (int c = 0; c < C; ++c) acc[c] = fmaf(xi, r[c], acc[c]);
     }
 #pragma unroll
     for (int c = 0; c < C; ++c) part[kv][k][lane * C + c] = acc[c];
@@ -527,8 +530,15 @@ int launch_append(const WriteArgs& a, void* stream) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.batch == 0) return 0;
   dim3 grid(a.batch, a.g.Hkv);
-  if (a.g.D == 128) append_kernel<128><<<grid, 256, 0, s>>>(a);
-  else append_kernel<64><<<grid, 256, 0, s>>>(a);
+  const size_t smem = 2 * sizeof(float) * a.g.D * a.g.D;
+  cudaError_t e;
+  if (a.g.D == 128) {
+    if ((e = ensure_smem_limit(append_kernel<128>, smem)) != cudaSuccess) return (int)e;
+    append_kernel<128><<<grid, 256, smem, s>>>(a);
+  } else {
+    if ((e = ensure_smem_limit(append_kernel<64>, smem)) != cudaSuccess) return (int)e;
+    append_kernel<64><<<grid, 256, smem, s>>>(a);
+  }
   return static_cast<int>(cudaGetLastError());
 }
 

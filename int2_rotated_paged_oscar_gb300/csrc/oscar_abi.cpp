@@ -213,7 +213,9 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   const size_t budget = 200 * 1024;
   w.combine_hpc = 1;
   w.combine_part_smem = 0;
-  for (int h = gq; h >= 1; h >>= 1) {
+  // few (request, head) pairs: one head per CTA for parallelism; many: share R_V across the group
+  const int h_max = (long long)batch * g.Hq <= 2 * 152 ? 1 : gq;
+  for (int h = h_max; h >= 1; h >>= 1) {
     if (rv_bytes + (size_t)h * per_head <= budget) {
       w.combine_hpc = h;
       w.combine_part_smem = 1;
