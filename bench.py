@@ -366,14 +366,17 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     dec_only_ms = ev0.elapsed_time(ev1) / args.steps
 
-    def decode_step(i, append=False):
-        layer_pass(append, qs[i % nvar], kn[i % nvar], vn[i % nvar])
+    # per-kernel device times: a decode-only pass captured with timing on (each
+    # launch bracketed by event-record nodes, no programmatic overlap), replayed
+    # once per capture so that host launch overhead stays out of the figures
     osc.oscar_set_timing(ctx, True)
     osc.oscar_reset_timing(ctx)
-    for i in range(args.steps):
-        decode_step(i, append=False)
-    torch.cuda.synchronize()
-    kms, kl = osc.oscar_kernel_time(ctx, "decode_splitk")
+    for i in range(max(1, min(args.steps, 8))):
+        g_t = capture(lambda: layer_pass(False, qs[i % nvar], kn[i % nvar], vn[i % nvar]))
+        g_t.replay()
+        torch.cuda.synchronize()
+        kms, kl = osc.oscar_kernel_time(ctx, "decode_splitk")
+        del g_t
     qms, _ = osc.oscar_kernel_time(ctx, "q_rotate")
     cms, _ = osc.oscar_kernel_time(ctx, "decode_combine")
     osc.oscar_set_timing(ctx, False)

@@ -184,6 +184,16 @@ oscar_status oscar_append_step(oscar_ctx* ctx, int32_t layer, const void* K_new,
                                float clip_K, float clip_V, const int32_t* block_table, int32_t bt_stride,
                                const int32_t* req_slot, void* stream);
 
+/* Declare the clip thresholds a layer's INT2 history was written with, for a
+ * cache filled outside this library (an uploaded image).  The write and append
+ * calls declare theirs implicitly.  The decode kernels feed the history's BF16
+ * scales and zeros to f16 tensor-core operands multiplied by 2^k, where k is the
+ * largest exponent with clip * 2^k < 2^14 over every clip declared for the
+ * layer (the smallest k is kept); INT2 decode of a layer with no declared clip
+ * returns OSCAR_ERR_INVALID.  Clips must lie in [2^-86, 16384) (else
+ * OSCAR_ERR_UNSUPPORTED, also from the write calls).  Host-only. */
+oscar_status oscar_set_layer_clip(oscar_ctx* ctx, int32_t layer, float clip_K, float clip_V);
+
 /* ---------------------------------------------------------------- decode
  * Bytes of decode workspace for batch requests of at most max_seq tokens. */
 oscar_status oscar_decode_workspace_size(const oscar_config* cfg, int32_t batch, int32_t max_seq, size_t* bytes);
@@ -200,7 +210,8 @@ oscar_status oscar_decode_workspace_size(const oscar_config* cfg, int32_t batch,
  * unrotated; both share one softmax.  sink/recent must equal the
  * configuration.  max_seq (host) bounds seq_lens and sizes the grid.
  * workspace: device scratch of oscar_decode_workspace_size bytes (256-byte
- * aligned); its contents need no initialisation. */
+ * aligned); its contents need no initialisation.  The layer needs a declared
+ * clip threshold (a write to it, or oscar_set_layer_clip). */
 oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
                                int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
                                const int32_t* seq_lens, const int32_t* req_slot, int32_t batch, int32_t max_seq,
@@ -255,7 +266,11 @@ oscar_status oscar_check_status(oscar_ctx* ctx, void* stream, int32_t* out_bits)
  * of the named kernel family with CUDA events on the launch stream.
  * oscar_kernel_time returns the summed milliseconds and launch count since the
  * last reset (synchronises the recorded events).  Names: "decode_splitk",
- * "decode_combine", "q_rotate", "append", "write", "bf16_decode". */
+ * "decode_combine", "q_rotate", "append", "write", "bf16_decode".  Launches
+ * recorded into a CUDA graph get external event-record nodes: replay the graph
+ * once, then read; the events return to the library when read, so a graph
+ * captured with timing on is replayed at most once.  With timing on, the decode
+ * kernels are launched without programmatic dependent launch. */
 oscar_status oscar_set_timing(oscar_ctx* ctx, int32_t enable);
 oscar_status oscar_kernel_time(oscar_ctx* ctx, const char* name, double* out_ms, int32_t* out_launches);
 oscar_status oscar_reset_timing(oscar_ctx* ctx);

@@ -72,6 +72,7 @@ _SIGS = {
                               _vp, _vp]),
     "oscar_write_kv_hadamard": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _f32, _f32, _vp, _i32,
                                        _vp, _vp]),
+    "oscar_set_layer_clip": (_i32, [_vp, _i32, _f32, _f32]),
     "oscar_append_step": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _f32, _f32, _vp, _i32, _vp, _vp]),
     "oscar_decode_workspace_size": (_i32, [_cfgp, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)]),
     "oscar_decode_attn": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
@@ -219,6 +220,10 @@ def oscar_append_step(ctx, layer, K_new, V_new, dtype, seq_lens_before, batch, R
     _check(load().oscar_append_step(ctx, layer, ptr(K_new), ptr(V_new), dtype, ptr(seq_lens_before), batch,
                                     ptr(R_K), ptr(R_V), float(clip_K), float(clip_V), ptr(block_table), bt_stride,
                                     ptr(req_slot), stream_ptr(stream)))
+
+
+def oscar_set_layer_clip(ctx, layer, clip_K, clip_V) -> None:
+    _check(load().oscar_set_layer_clip(ctx, layer, float(clip_K), float(clip_V)))
 
 
 def oscar_decode_workspace_size(cfg: oscar_config, batch: int, max_seq: int) -> int:

@@ -109,6 +109,31 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint3
       : "memory");
 }
 
+// L2 policy for data read once per step (the INT2 page stream): evict first, so
+// that streaming the cache does not push small reused data (rotations, window
+// slabs, workspaces) out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// bulk_g2s with an L2 cache-eviction policy from l2_evict_first_policy().
+__device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before its
+// later async-proxy ones (a bulk copy into a buffer the warp has just read).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ PDL
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -203,6 +228,44 @@ __device__ __forceinline__ void unpack_word_bf16(uint32_t w, uint32_t (&o)[8]) {
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
+
+// ------------------------------------------------------------------ scaled code operands
+// f16 pair of slot X of a code word (w6 = w >> 6): -(1 + c * 2^(pos-10)) in each
+// half, the f16 pattern of -1.0 with the code OR-ed into its mantissa.
+// magic is kCodeMagic, passed in from the host so that it stays in a register
+// and (w & mask) | magic is a single LOP3 with the mask as its immediate.
+template <int X>
+__device__ __forceinline__ uint32_t magic_slot(uint32_t w, uint32_t w6, uint32_t magic) {
+  constexpr int pos = slot_pos(X);
+  constexpr uint32_t mask = (3u << pos) | (3u << (16 + pos));
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(X < 5 ? w : w6), "n"(mask), "r"(magic));  // (a & b) | c
+  return r;
+}
+
+// x * N + N = S * c * 2^(pos-10) for x = -(1 + c * 2^(pos-10)) and N = -S: one
+// fused f16 multiply-add per pair, with no separate negation.  The result is
+// exact whenever it is an f16 normal number: S carries at most 8 significant
+// bits (a BF16 value times a power of two) and c * 2^(pos-10) at most 2.
+__device__ __forceinline__ uint32_t scale_codes(uint32_t x, uint32_t n2) {
+  const __half2 xv = *reinterpret_cast<const __half2*>(&x);
+  const __half2 nv = *reinterpret_cast<const __half2*>(&n2);
+  const __half2 r = __hfma2(xv, nv, nv);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// A (scale, zero) word holds the BF16 scale in its low half and the BF16 zero
+// in its high half.  neg_scale_times_pow2 returns -scale * 2^k and
+// zero_times_pow2 zero * 2^k as float32, by adding k to the exponent field
+// (k23 = k << 23, k >= 0; the scale is never negative, so adding the sign bit
+// negates it).  A zero field turns into +-2^(k-127), below every f16 number,
+// which converts to 0.
+__device__ __forceinline__ float neg_scale_times_pow2(uint32_t w, uint32_t k23) {
+  return __uint_as_float(w * 65536u + (k23 + 0x80000000u));
+}
+__device__ __forceinline__ float zero_times_pow2(uint32_t w, uint32_t k23) {
+  return __uint_as_float((w & 0xFFFF0000u) + k23);
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo_elem, float hi_elem) {
   __half2 h = __floats2half2_rn(lo_elem, hi_elem);

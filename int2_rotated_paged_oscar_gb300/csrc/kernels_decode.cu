@@ -41,6 +41,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "oscar_internal.h"
@@ -57,13 +58,13 @@ static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
 namespace {
 
 constexpr int kThreads = 128;  // 4 warps
-constexpr int kStages = 4;
-constexpr int kStageTokens = 64;
+constexpr int kWarps = kThreads / 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSplits = 1023;  // the host plan never asks for more
 constexpr int kWinChunk = 16;     // window slots per window CTA
 constexpr int kMaxWinChunks = 32;
-constexpr float kRescaleLog2 = 8.f;
+constexpr float kRescaleLog2 = 8.f;   // the softmax reference moves when a score exceeds it by more
+constexpr float kWeightShift = 6.f;   // weights are 2^(s - mm) with mm = reference - kWeightShift
 
 // ------------------------------------------------------------------ workspace views
 struct WsView {
@@ -309,6 +310,8 @@ __device__ void window_chunk(const DecodeArgs& a, int b, int kvh, int chunk, uin
 }
 
 // ------------------------------------------------------------------ INT2 split
+// Page block of one (page, kv head), as stored in the pool:
+//   K codes [P][D/4] | K (scale, zero) [P][D/32] | V codes [P][D/4] | V (scale, zero) [P][D/32]
 template <int D, int NT, int P>
 struct Int2Layout {
   static constexpr int ROW = D / 4;
@@ -317,20 +320,49 @@ struct Int2Layout {
   static constexpr int VC = KSZ + P * SZ;
   static constexpr int VSZ = VC + P * ROW;
   static constexpr int BLOCK = VSZ + P * SZ;
-  static constexpr int PPS = kStageTokens / P;  // pages per stage
-  static constexpr int STAGE = PPS * BLOCK;
   static constexpr int GROUPS = D / 32;
   static constexpr int KT = D / 16;             // QK k-tiles
   static constexpr int MT = D / 16;             // PV m-tiles
+  static constexpr int WS = P == 64 ? 2 : 4;    // ring stages per warp (one page block each)
+  static constexpr int RING = kWarps * WS * BLOCK;
+  static constexpr int SMEM = RING + kWarps * WS * (8 + 4);  // + mbarriers + page-valid flags
 };
 
+// One INT2 split: pages [pg0, pg1) of one (request, kv head).  Warp w owns pages
+// pg0 + w + 4i and streams them through its own ring of WS page blocks (bulk
+// copies completing on per-stage mbarriers), so warps never wait on each other
+// inside the loop.  A page is processed as P/16 blocks of 16 tokens.
+//
+// Operands (mma.sync m16n8k16, f32 accumulate).  Let k_K, k_V be the layer's
+// operand exponents (scales and zeros times 2^k stay below 2^14 in f16), e_h the
+// per-head query exponent written by q_rotate, and j = 6 the softmax-weight shift.
+//   QK  A = K codes times their group scale: S * c * 2^(pos-10) in f16 with
+//       S = f16(s * 2^k_K), formed exactly by one HFMA2 per register from the
+//       code pattern -(1 + c * 2^(pos-10)) and -S;
+//       B = q' * 2^(e_h) * 2^(10-pos) split into f16 hi/lo.  One accumulator holds
+//       every group, so no per-group epilogue is needed.  The zero term
+//       sum_g z_g Q_g is one more MMA: A = the raw BF16 (scale, zero) word of
+//       group tig in columns (2tig, 2tig+1), B = (0, Q_tig * 2^(e_h + k_K)) in
+//       BF16 hi/lo, the scale meeting a zero row.
+//   PV  A = V codes times their token's group scale (as for K, per token pair);
+//       B = p * 2^j split into f16 hi/lo; the zero term sum_t p_t z_{t,g} is one
+//       MMA with A rows = groups holding f16(z * 2^k_V).
+//   Columns: <= 4 query heads: (head, hi|lo); 8 query heads: heads, with the hi
+//   and lo planes as two MMAs into the same accumulator.
+// Token order inside a 16-token block: MMA row / PV k-index r is token
+// sigma(r) = r/2 + 8(r%2), which lets the PV weights of a lane come from two
+// lanes' QK accumulators.
+// Online softmax in the log2 domain with a lazy reference mm: it moves only
+// when a block maximum exceeds mm + 8 + j, so weights 2^(s - mm) stay below
+// 2^14 (f16) and rescaling is rare; the reference check is one warp vote.
 template <int D, int NT, int P>
-__global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, NT == 2 ? 3 : 4) decode_splitk_kernel(DecodeArgs a) {
   using Lay = Int2Layout<D, NT, P>;
+  constexpr int WS = Lay::WS;
+  constexpr int GROUPS = Lay::GROUPS;
+  constexpr bool G8 = NT == 2;
+  constexpr int NH = G8 ? 2 : 1;  // query heads per lane
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* stage_buf = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * Lay::STAGE);
-  int* stage_valid = reinterpret_cast<int*>(bars + kStages);
 
   const Geom& g = a.g;
   const int b = blockIdx.z, kvh = blockIdx.y;
@@ -362,67 +394,40 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
   const int pg0 = split * a.wl.pages_per_split;
   if (pg0 >= n_hist_pages) { pdl_launch_dependents(); return; }
   const int pg1 = min(pg0 + a.wl.pages_per_split, n_hist_pages);
-  const int n_iters = (pg1 - pg0 + Lay::PPS - 1) / Lay::PPS;
+  const int n_mine = pg0 + warp < pg1 ? (pg1 - pg0 - warp + kWarps - 1) / kWarps : 0;
 
   const int* bt = a.block_table + (size_t)b * a.bt_stride;
   const uint8_t* pool_l = a.pool + (size_t)a.layer * g.layer_pool_bytes();
+  uint8_t* ring = smem + warp * WS * Lay::BLOCK;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::RING) + warp * WS;
+  int* stage_ok = reinterpret_cast<int*>(smem + Lay::RING + kWarps * WS * 8) + warp * WS;
 
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+  if (lane == 0) {
+    for (int s = 0; s < WS; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
   }
-  __syncthreads();
-
-  auto issue = [&](int it) {
-    const int s = it % kStages;
-    uint32_t bytes = 0;
-    int mask = 0;
-    int pages[Lay::PPS];
-#pragma unroll
-    for (int i = 0; i < Lay::PPS; ++i) {
-      const int lp = pg0 + it * Lay::PPS + i;
-      pages[i] = -1;
-      if (lp < pg1) {
-        const int pid = (lp < a.bt_stride && lp < g.max_pages_per_req) ? bt[lp] : -1;
-        if (pid >= 0 && pid < g.num_pages) {
-          pages[i] = pid;
-          bytes += Lay::BLOCK;
-          mask |= 1 << i;
-        } else {
-          flag_error(a.status, kDevBadPage);
-        }
-      }
-    }
-    stage_valid[s] = mask;
-    mbar_arrive_expect_tx(&bars[s], bytes);
-#pragma unroll
-    for (int i = 0; i < Lay::PPS; ++i) {
-      if (pages[i] >= 0) {
-        const uint8_t* src = pool_l + ((size_t)pages[i] * g.Hkv + kvh) * Lay::BLOCK;
-        bulk_g2s(stage_buf + s * Lay::STAGE + i * Lay::BLOCK, src, Lay::BLOCK, &bars[s]);
-      }
-    }
+  __syncwarp();
+  const uint64_t stream_policy = l2_evict_first_policy();  // pages are read once per step
+  auto issue = [&](int i) {  // lane 0: page i of this warp into stage i % WS
+    const int s = i % WS;
+    const int lp = pg0 + warp + kWarps * i;
+    const int pid = (lp < a.bt_stride && lp < g.max_pages_per_req) ? bt[lp] : -1;
+    const bool okp = pid >= 0 && pid < g.num_pages;
+    stage_ok[s] = okp ? 1 : 0;
+    if (!okp) flag_error(a.status, kDevBadPage);
+    mbar_arrive_expect_tx(&bars[s], okp ? (uint32_t)Lay::BLOCK : 0u);
+    if (okp)
+      bulk_g2s_hint(ring + s * Lay::BLOCK, pool_l + ((size_t)pid * g.Hkv + kvh) * Lay::BLOCK, Lay::BLOCK, &bars[s],
+                    stream_policy);
   };
+  // first page now; the rest of the ring after the query-side set-up, so that
+  // first pages tend to arrive before any warp's later pages
+  if (lane == 0 && n_mine > 0) issue(0);
 
-  if (tid == 0) {
-    for (int it = 0; it < kStages && it < n_iters; ++it) issue(it);
-  }
-
-  // query side (written by q_rotate): wait for the previous grid
+  // ---------------- query side (written by q_rotate): wait for the previous grid
   pdl_wait();
   WsView ws = ws_view(a);
-  // Column layout of the MMAs (see q_rotate):
-  //  G8 (8 query heads per kv head): columns are heads; the f16 (QK) / bf16 (PV)
-  //     hi and lo parts are separate operand planes accumulated into the same
-  //     registers.  A lane owns heads 2*tig and 2*tig + 1.
-  //  otherwise (<= 4 heads): QK columns are (head, hi|lo) = 2*head + part; PV
-  //     columns are (head, group parity) = 2*head + (g & 1) with hi and lo as two
-  //     MMAs.  A lane owns head tig.
-  constexpr bool G8 = NT == 2;
-  constexpr int NH = G8 ? 2 : 1;  // heads per lane
   uint32_t qb[NT][Lay::KT][2];
-  float qscale[NH];
-  float qg[NH][Lay::GROUPS];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const bool col_ok = G8 || (gid >> 1) < gq;
@@ -433,388 +438,414 @@ __global__ void __launch_bounds__(kThreads) decode_splitk_kernel(DecodeArgs a) {
       qb[nt][kk][1] = col_ok ? f.y : 0u;
     }
   }
+  const float* aux_base = ws.qaux + ((size_t)b * g.Hq + (size_t)kvh * gq) * 8;
+  const float sm_log2 = kLog2e * rsqrtf((float)D);
+  float F[NH];  // score = accumulator * F (log2 domain)
 #pragma unroll
   for (int j = 0; j < NH; ++j) {
     const int hh = G8 ? 2 * tig + j : tig;
-    const float* aux = ws.qaux + ((size_t)b * g.Hq + kvh * gq + min(hh, gq - 1)) * 8;
-    qscale[j] = hh < gq ? aux[0] : 0.f;
+    F[j] = hh < gq ? aux_base[hh * 8] * ldexpf(sm_log2, -a.k_exp_K) : 0.f;
+  }
+  // zero-term B fragment: column gid, row 2tig + 1 = Q_tig * 2^(e_h + k_K) (BF16 hi or lo part)
+  uint32_t qz[NT];
 #pragma unroll
-    for (int gi = 0; gi < Lay::GROUPS; ++gi) qg[j][gi] = hh < gq ? aux[1 + gi] : 0.f;
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hh = G8 ? gid : gid >> 1;
+    const int part = G8 ? nt : gid & 1;
+    float v = 0.f;
+    if (hh < gq && tig < GROUPS) {
+      const float* aux = aux_base + hh * 8;
+      const float qf = ldexpf(aux[1 + tig] / aux[0], a.k_exp_K);
+      const float hi = __bfloat162float(__float2bfloat16_rn(qf));
+      v = part ? __bfloat162float(__float2bfloat16_rn(qf - hi)) : hi;
+    }
+    const __nv_bfloat16 vb = __float2bfloat16_rn(v);
+    qz[nt] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&vb)) << 16;
   }
 
-  const float sm_log2 = kLog2e * rsqrtf((float)D);
-  float m_run[NH], l_run[NH];
+  if (lane == 0)
+    for (int i = 1; i < WS && i < n_mine; ++i) issue(i);
+
+  float mm[NH], thr[NH], l_run[NH];
   float acc[Lay::MT][4];
-  float zacc[NH][Lay::GROUPS];
+  float zacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < NH; ++j) {
-    m_run[j] = -INFINITY;
+    mm[j] = -INFINITY;
+    thr[j] = -INFINITY;
     l_run[j] = 0.f;
-#pragma unroll
-    for (int gi = 0; gi < Lay::GROUPS; ++gi) zacc[j][gi] = 0.f;
   }
 #pragma unroll
   for (int mt = 0; mt < Lay::MT; ++mt)
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
 
-  // rows of this lane inside a 16-token block (token order sigma(k) = k/2 + 8*(k%2))
-  const int ra = (gid >> 1) + 8 * (gid & 1);      // sigma(gid)
-  const int rb = 4 + (gid >> 1) + 8 * (gid & 1);  // sigma(gid + 8)
-  const int w_off = 16 * warp;                    // this warp's block inside the stage
-  const int pi = w_off / P, slot0 = w_off % P;
+  const uint32_t magic = a.code_magic;
+  const uint32_t k23 = static_cast<uint32_t>(a.k_exp_K) << 23;
+  const uint32_t v23 = static_cast<uint32_t>(a.k_exp_V) << 23;
+  // rows of this lane inside a 16-token block: QK rows gid, gid + 8 are tokens
+  // ra = sigma(gid), rb = sigma(gid + 8); PV k-indices 2tig, 2tig+1, 2tig+8, 2tig+9
+  // are tokens tig, tig + 8, tig + 4, tig + 12
+  const int ra = (gid >> 1) + 8 * (gid & 1);
+  const int rb = ra + 4;
+  const int zq = min(tig, GROUPS - 1);   // QK zero-term group of this lane
+  const int zv = gid & (GROUPS - 1);     // PV zero-term group row of this lane
+  const int src0 = (2 * tig) * 4 + (gid >> 1), src1 = src0 + 4;
+  const uint32_t psel = (gid & 1) ? 0x7632u : 0x5410u;
 
-  bool aborted = false;
-  int it_fail = 0;
-  for (int it = 0; it < n_iters; ++it) {
-    const int s = it % kStages;
-    const bool ok = mbar_wait_bounded(&bars[s], (it / kStages) & 1, a.status);
-    if (ok) {
-      const int valid_mask = stage_valid[s];
-      const bool page_ok = (valid_mask >> pi) & 1;
-      const int tb = (pg0 + it * Lay::PPS) * P + w_off;  // absolute token of row 0 of the block
-      const uint8_t* buf = stage_buf + s * Lay::STAGE + pi * Lay::BLOCK;
-      // ---------------- QK
-      uint32_t ua[D / 8], ub[D / 8];  // f16 code pairs of rows ra and rb
-      {
-        const uint8_t* kc = buf;
-        if constexpr (D == 128) {
-          const uint2 wa = *reinterpret_cast<const uint2*>(kc + (slot0 + ra) * Lay::ROW + tig * 8);
-          const uint2 wb = *reinterpret_cast<const uint2*>(kc + (slot0 + rb) * Lay::ROW + tig * 8);
-          uint32_t t8[8];
-          unpack_word(wa.x, t8);
+  // One 16-token block at slot0 of the stage buffer; FULL: every token is a
+  // history token (no masking).
+  auto process = [&](auto full_tag, const uint8_t* buf, int slot0, int tb) {
+    constexpr bool FULL = decltype(full_tag)::value;
+    // ---------------- QK
+    const int sA = slot0 + ra, sB = slot0 + rb;
+    bool va = true, vb = true;
+    if constexpr (!FULL) {
+      va = tb + ra >= g.S && tb + ra < h_end;
+      vb = tb + rb >= g.S && tb + rb < h_end;
+    }
+    uint32_t kwA[D / 64], kwB[D / 64];
+    uint32_t szA[GROUPS], szB[GROUPS];
+    if constexpr (D == 128) {
+      const uint2 x = *reinterpret_cast<const uint2*>(buf + sA * Lay::ROW + tig * 8);
+      const uint2 y = *reinterpret_cast<const uint2*>(buf + sB * Lay::ROW + tig * 8);
+      kwA[0] = x.x; kwA[1] = x.y; kwB[0] = y.x; kwB[1] = y.y;
+      const uint4 A4 = *reinterpret_cast<const uint4*>(buf + Lay::KSZ + sA * Lay::SZ);
+      const uint4 B4 = *reinterpret_cast<const uint4*>(buf + Lay::KSZ + sB * Lay::SZ);
+      szA[0] = A4.x; szA[1] = A4.y; szA[2] = A4.z; szA[3] = A4.w;
+      szB[0] = B4.x; szB[1] = B4.y; szB[2] = B4.z; szB[3] = B4.w;
+    } else {
+      kwA[0] = *reinterpret_cast<const uint32_t*>(buf + sA * Lay::ROW + tig * 4);
+      kwB[0] = *reinterpret_cast<const uint32_t*>(buf + sB * Lay::ROW + tig * 4);
+      const uint2 A2 = *reinterpret_cast<const uint2*>(buf + Lay::KSZ + sA * Lay::SZ);
+      const uint2 B2 = *reinterpret_cast<const uint2*>(buf + Lay::KSZ + sB * Lay::SZ);
+      szA[0] = A2.x; szA[1] = A2.y;
+      szB[0] = B2.x; szB[1] = B2.y;
+    }
+    uint32_t zA = *reinterpret_cast<const uint32_t*>(buf + Lay::KSZ + sA * Lay::SZ + 4 * zq);
+    uint32_t zB = *reinterpret_cast<const uint32_t*>(buf + Lay::KSZ + sB * Lay::SZ + 4 * zq);
+    uint32_t SA[GROUPS], SB[GROUPS];
 #pragma unroll
-          for (int x = 0; x < 8; ++x) ua[x] = t8[x];
-          unpack_word(wa.y, t8);
+    for (int gi = 0; gi < GROUPS; ++gi) {
+      float xa = neg_scale_times_pow2(szA[gi], k23), xb = neg_scale_times_pow2(szB[gi], k23);
+      if constexpr (!FULL) {
+        xa = va ? xa : 0.f;
+        xb = vb ? xb : 0.f;
+      }
+      SA[gi] = pack_half2(xa, xa);
+      SB[gi] = pack_half2(xb, xb);
+    }
+    if constexpr (!FULL) {
+      zA = va ? zA : 0u;
+      zB = vb ? zB : 0u;
+    }
+    float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-          for (int x = 0; x < 8; ++x) ua[8 + x] = t8[x];
-          unpack_word(wb.x, t8);
+    for (int w = 0; w < D / 64; ++w) {
+      const uint32_t a6 = kwA[w] >> 6, b6 = kwB[w] >> 6;
+      uint32_t ua[8], ub[8];
+#define OSCAR_K_SLOT(X)                                                   \
+      ua[X] = scale_codes(magic_slot<X>(kwA[w], a6, magic), SA[2 * w + (X >> 2)]); \
+      ub[X] = scale_codes(magic_slot<X>(kwB[w], b6, magic), SB[2 * w + (X >> 2)]);
+      OSCAR_K_SLOT(0) OSCAR_K_SLOT(1) OSCAR_K_SLOT(2) OSCAR_K_SLOT(3)
+      OSCAR_K_SLOT(4) OSCAR_K_SLOT(5) OSCAR_K_SLOT(6) OSCAR_K_SLOT(7)
+#undef OSCAR_K_SLOT
 #pragma unroll
-          for (int x = 0; x < 8; ++x) ub[x] = t8[x];
-          unpack_word(wb.y, t8);
+      for (int hg = 0; hg < 2; ++hg) {
+        const int gi = 2 * w + hg;
 #pragma unroll
-          for (int x = 0; x < 8; ++x) ub[8 + x] = t8[x];
-        } else {
-          const uint32_t wa = *reinterpret_cast<const uint32_t*>(kc + (slot0 + ra) * Lay::ROW + tig * 4);
-          const uint32_t wb = *reinterpret_cast<const uint32_t*>(kc + (slot0 + rb) * Lay::ROW + tig * 4);
-          unpack_word(wa, ua);
-          unpack_word(wb, ub);
+        for (int kt = 0; kt < 2; ++kt) {
+          const int x = 4 * hg + 2 * kt;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_f16(c[hg], ua[x], ub[x], ua[x + 1], ub[x + 1], qb[nt][2 * gi + kt][0], qb[nt][2 * gi + kt][1]);
         }
       }
-      float sc[NH][2];  // scores (log2 domain) of this lane's heads for rows ra, rb
-      {
-        uint32_t sza[Lay::GROUPS], szb[Lay::GROUPS];
-        if constexpr (Lay::GROUPS == 4) {
-          const uint4 A4 = *reinterpret_cast<const uint4*>(buf + Lay::KSZ + (slot0 + ra) * Lay::SZ);
-          const uint4 B4 = *reinterpret_cast<const uint4*>(buf + Lay::KSZ + (slot0 + rb) * Lay::SZ);
-          sza[0] = A4.x; sza[1] = A4.y; sza[2] = A4.z; sza[3] = A4.w;
-          szb[0] = B4.x; szb[1] = B4.y; szb[2] = B4.z; szb[3] = B4.w;
-        } else {
-          const uint2 A2 = *reinterpret_cast<const uint2*>(buf + Lay::KSZ + (slot0 + ra) * Lay::SZ);
-          const uint2 B2 = *reinterpret_cast<const uint2*>(buf + Lay::KSZ + (slot0 + rb) * Lay::SZ);
-          sza[0] = A2.x; sza[1] = A2.y;
-          szb[0] = B2.x; szb[1] = B2.y;
-        }
-        float dsum[NH][2], zsum[NH][2];
+    }
 #pragma unroll
-        for (int j = 0; j < NH; ++j) dsum[j][0] = dsum[j][1] = zsum[j][0] = zsum[j][1] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) mma_bf16(c[1], zA, zB, 0u, 0u, qz[nt], 0u);
+    float sa[NH], sb[NH];
+    if constexpr (G8) {
 #pragma unroll
-        for (int gi = 0; gi < Lay::GROUPS; ++gi) {
-          float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int kt = 0; kt < 2; ++kt) {
-            const int p8 = 4 * gi + 2 * kt;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma_f16(c, ua[p8], ub[p8], ua[p8 + 1], ub[p8 + 1], qb[nt][2 * gi + kt][0], qb[nt][2 * gi + kt][1]);
-          }
-          const float s_a = bf16_lo(sza[gi]), s_b = bf16_lo(szb[gi]);
-          const float z_a = bf16_hi(sza[gi]), z_b = bf16_hi(szb[gi]);
-          if constexpr (G8) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              dsum[j][0] = fmaf(s_a, c[j], dsum[j][0]);
-              dsum[j][1] = fmaf(s_b, c[2 + j], dsum[j][1]);
-              zsum[j][0] = fmaf(z_a, qg[j][gi], zsum[j][0]);
-              zsum[j][1] = fmaf(z_b, qg[j][gi], zsum[j][1]);
-            }
-          } else {
-            dsum[0][0] = fmaf(s_a, c[0] + c[1], dsum[0][0]);
-            dsum[0][1] = fmaf(s_b, c[2] + c[3], dsum[0][1]);
-            zsum[0][0] = fmaf(z_a, qg[0][gi], zsum[0][0]);
-            zsum[0][1] = fmaf(z_b, qg[0][gi], zsum[0][1]);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < NH; ++j) {
-          sc[j][0] = fmaf(dsum[j][0], qscale[j], zsum[j][0]) * sm_log2;
-          sc[j][1] = fmaf(dsum[j][1], qscale[j], zsum[j][1]) * sm_log2;
-        }
+      for (int j = 0; j < 2; ++j) {
+        sa[j] = (c[0][j] + c[1][j]) * F[j];
+        sb[j] = (c[0][2 + j] + c[1][2 + j]) * F[j];
       }
-      const int ta = tb + ra, tbk = tb + rb;
-      // every row of the block is a history token on a mapped page (warp-uniform)
-      const bool full_block = page_ok && tb >= g.S && tb + 15 < h_end;
-      const bool va = page_ok && ta >= g.S && ta < h_end;
-      const bool vb = page_ok && tbk >= g.S && tbk < h_end;
-      // ---------------- online softmax (per head: lanes sharing tig).  The running
-      // reference m_run only moves when a block maximum exceeds it by more than
-      // 2^kRescaleLog2, so the accumulators are rescaled rarely; p stays below
-      // 2^kRescaleLog2, which float32 sums and bf16 operands absorb.
-      float pa[NH], pb[NH];
-      float alpha[NH];
-      bool rescale = false;
+    } else {
+      sa[0] = ((c[0][0] + c[0][1]) + (c[1][0] + c[1][1])) * F[0];
+      sb[0] = ((c[0][2] + c[0][3]) + (c[1][2] + c[1][3])) * F[0];
+    }
+    if constexpr (!FULL) {
 #pragma unroll
       for (int j = 0; j < NH; ++j) {
-        const float s_a = va ? sc[j][0] : -INFINITY;
-        const float s_b = vb ? sc[j][1] : -INFINITY;
-        float mb = fmaxf(s_a, s_b);
+        sa[j] = va ? sa[j] : -INFINITY;
+        sb[j] = vb ? sb[j] : -INFINITY;
+      }
+    }
+    // ---------------- online softmax
+    bool need = false;
+#pragma unroll
+    for (int j = 0; j < NH; ++j) need |= fmaxf(sa[j], sb[j]) > thr[j];
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int j = 0; j < NH; ++j) {
+        float mb = fmaxf(sa[j], sb[j]);
         mb = warp_max_xor(mb, 4);
         mb = warp_max_xor(mb, 8);
         mb = warp_max_xor(mb, 16);
-        const float m_ref = (mb > m_run[j] + kRescaleLog2) ? mb : m_run[j];
-        alpha[j] = 1.f;
-        if (m_ref != m_run[j]) {
-          alpha[j] = (m_run[j] == -INFINITY) ? 0.f : ex2(m_run[j] - m_ref);
-          rescale = true;
-          m_run[j] = m_ref;
-        }
-        pa[j] = (s_a == -INFINITY) ? 0.f : ex2(s_a - m_run[j]);
-        pb[j] = (s_b == -INFINITY) ? 0.f : ex2(s_b - m_run[j]);
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-        for (int j = 0; j < NH; ++j) {
-          l_run[j] *= alpha[j];
-#pragma unroll
-          for (int gi = 0; gi < Lay::GROUPS; ++gi) zacc[j][gi] *= alpha[j];
-        }
-#pragma unroll
-        for (int mt = 0; mt < Lay::MT; ++mt) {
-          if constexpr (G8) {
-            acc[mt][0] *= alpha[0];
-            acc[mt][1] *= alpha[NH - 1];
-            acc[mt][2] *= alpha[0];
-            acc[mt][3] *= alpha[NH - 1];
-          } else {
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[mt][r] *= alpha[0];
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < NH; ++j) l_run[j] += pa[j] + pb[j];
-      // ---------------- zero term of the values (rows ra, rb)
-      {
-        const uint32_t* vszA = reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + ra) * Lay::SZ);
-        const uint32_t* vszB = reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + rb) * Lay::SZ);
-#pragma unroll
-        for (int gi = 0; gi < Lay::GROUPS; ++gi) {
-          const float z_a = bf16_hi(vszA[gi]);
-          const float z_b = bf16_hi(vszB[gi]);
-#pragma unroll
-          for (int j = 0; j < NH; ++j) {
-            if (full_block) {
-              zacc[j][gi] = fmaf(pb[j], z_b, fmaf(pa[j], z_a, zacc[j][gi]));
-            } else {
-              if (pa[j] > 0.f) zacc[j][gi] = fmaf(pa[j], z_a, zacc[j][gi]);
-              if (pb[j] > 0.f) zacc[j][gi] = fmaf(pb[j], z_b, zacc[j][gi]);
-            }
-          }
-        }
-      }
-      // ---------------- PV
-      {
-        // value-side A fragments: rows k in {2tig, 2tig+1, 2tig+8, 2tig+9} are tokens
-        // sigma(k) = tig, tig+8, tig+4, tig+12; this lane reads word gid (D=128) of each.
-        const uint8_t* vc = buf + Lay::VC;
-        uint32_t ux[D / 8], uy[D / 8];
-        if constexpr (D == 128) {
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vc + (slot0 + tig) * Lay::ROW + gid * 4);
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vc + (slot0 + tig + 8) * Lay::ROW + gid * 4);
-          const uint32_t w8 = *reinterpret_cast<const uint32_t*>(vc + (slot0 + tig + 4) * Lay::ROW + gid * 4);
-          const uint32_t w9 = *reinterpret_cast<const uint32_t*>(vc + (slot0 + tig + 12) * Lay::ROW + gid * 4);
-          uint32_t t8[8];
-          unpack_word_bf16(prmt(w0, w1, 0x5410), t8);
-#pragma unroll
-          for (int x = 0; x < 8; ++x) ux[x] = t8[x];
-          unpack_word_bf16(prmt(w0, w1, 0x7632), t8);
-#pragma unroll
-          for (int x = 0; x < 8; ++x) ux[8 + x] = t8[x];
-          unpack_word_bf16(prmt(w8, w9, 0x5410), t8);
-#pragma unroll
-          for (int x = 0; x < 8; ++x) uy[x] = t8[x];
-          unpack_word_bf16(prmt(w8, w9, 0x7632), t8);
-#pragma unroll
-          for (int x = 0; x < 8; ++x) uy[8 + x] = t8[x];
-        } else {
-          const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
-          const int wo = (gid >> 1) * 4;
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vc + (slot0 + tig) * Lay::ROW + wo);
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vc + (slot0 + tig + 8) * Lay::ROW + wo);
-          const uint32_t w8 = *reinterpret_cast<const uint32_t*>(vc + (slot0 + tig + 4) * Lay::ROW + wo);
-          const uint32_t w9 = *reinterpret_cast<const uint32_t*>(vc + (slot0 + tig + 12) * Lay::ROW + wo);
-          unpack_word_bf16(prmt(w0, w1, sel), ux);
-          unpack_word_bf16(prmt(w8, w9, sel), uy);
-        }
-        // scales of rows 2tig, 2tig+1, 2tig+8, 2tig+9 (tokens tig, tig+8, tig+4, tig+12)
-        const uint32_t* vsr[4] = {
-            reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig) * Lay::SZ),
-            reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig + 8) * Lay::SZ),
-            reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig + 4) * Lay::SZ),
-            reinterpret_cast<const uint32_t*>(buf + Lay::VSZ + (slot0 + tig + 12) * Lay::SZ)};
-        // p of this lane's column head at rows 2tig, 2tig+1, 2tig+8, 2tig+9
-        const int src0 = (2 * tig) * 4 + (gid >> 1);
-        const int src1 = (2 * tig + 1) * 4 + (gid >> 1);
-        float pr[4];
-        if constexpr (G8) {
-          // column head gid lives in lane group tig = gid >> 1 as its head j = gid & 1
-          const bool second = (gid & 1) != 0;
-          const float a0 = __shfl_sync(0xffffffffu, pa[0], src0), a1 = __shfl_sync(0xffffffffu, pa[NH - 1], src0);
-          const float b0 = __shfl_sync(0xffffffffu, pa[0], src1), b1 = __shfl_sync(0xffffffffu, pa[NH - 1], src1);
-          const float c0 = __shfl_sync(0xffffffffu, pb[0], src0), c1 = __shfl_sync(0xffffffffu, pb[NH - 1], src0);
-          const float d0 = __shfl_sync(0xffffffffu, pb[0], src1), d1 = __shfl_sync(0xffffffffu, pb[NH - 1], src1);
-          pr[0] = second ? a1 : a0;
-          pr[1] = second ? b1 : b0;
-          pr[2] = second ? c1 : c0;
-          pr[3] = second ? d1 : d0;
-        } else {
-          pr[0] = __shfl_sync(0xffffffffu, pa[0], src0);
-          pr[1] = __shfl_sync(0xffffffffu, pa[0], src1);
-          pr[2] = __shfl_sync(0xffffffffu, pb[0], src0);
-          pr[3] = __shfl_sync(0xffffffffu, pb[0], src1);
-        }
-        // B operands: weights w = p * scale_g, split as hi = bf16 truncation of w and
-        // lo = bf16(w - hi) (round to nearest); both go through the MMA into one accumulator
-        auto weights = [&](int gi, uint32_t& bh0, uint32_t& bh1, uint32_t& bl0, uint32_t& bl1) {
-          float w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            w[u] = pr[u] * bf16_lo(vsr[u][gi]);
-            if (!full_block) w[u] = pr[u] > 0.f ? w[u] : 0.f;  // unwritten slots may hold NaN scales
-          }
-          uint32_t hw[4];
-          float lo[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            hw[u] = __float_as_uint(w[u]) & 0xFFFF0000u;
-            lo[u] = w[u] - __uint_as_float(hw[u]);
-          }
-          bh0 = prmt(hw[0], hw[1], 0x7632);
-          bh1 = prmt(hw[2], hw[3], 0x7632);
-          bl0 = pack_bf162(lo[0], lo[1]);
-          bl1 = pack_bf162(lo[2], lo[3]);
-        };
+        const float nm = mb > thr[j] ? mb - kWeightShift : mm[j];
+        const float alpha = nm == mm[j] ? 1.f : ex2(mm[j] - nm);
+        mm[j] = nm;
+        thr[j] = nm + kWeightShift + kRescaleLog2;
+        l_run[j] *= alpha;
         if constexpr (G8) {
 #pragma unroll
-          for (int gi = 0; gi < Lay::GROUPS; ++gi) {
-            uint32_t bh0, bh1, bl0, bl1;
-            weights(gi, bh0, bh1, bl0, bl1);
-#pragma unroll
-            for (int mq = 0; mq < 2; ++mq) {
-              const int mt = 2 * gi + mq;
-              mma_bf16(acc[mt], ux[2 * mt], ux[2 * mt + 1], uy[2 * mt], uy[2 * mt + 1], bh0, bh1);
-              mma_bf16(acc[mt], ux[2 * mt], ux[2 * mt + 1], uy[2 * mt], uy[2 * mt + 1], bl0, bl1);
-            }
+          for (int mt = 0; mt < Lay::MT; ++mt) {
+            acc[mt][j] *= alpha;
+            acc[mt][2 + j] *= alpha;
           }
+          zacc[j] *= alpha;
+          zacc[2 + j] *= alpha;
         } else {
-          // column (head, parity): parity gid & 1 selects group 2*gp + parity of pair gp
 #pragma unroll
-          for (int gp = 0; gp < (Lay::GROUPS + 1) / 2; ++gp) {
-            const int gi = min(2 * gp + (gid & 1), Lay::GROUPS - 1);
-            uint32_t bh0, bh1, bl0, bl1;
-            weights(gi, bh0, bh1, bl0, bl1);
+          for (int mt = 0; mt < Lay::MT; ++mt)
 #pragma unroll
-            for (int mq = 0; mq < 4; ++mq) {
-              const int mt = 4 * gp + mq;  // m-tiles of groups 2gp, 2gp+1
-              if (mt < Lay::MT) {
-                mma_bf16(acc[mt], ux[2 * mt], ux[2 * mt + 1], uy[2 * mt], uy[2 * mt + 1], bh0, bh1);
-                mma_bf16(acc[mt], ux[2 * mt], ux[2 * mt + 1], uy[2 * mt], uy[2 * mt + 1], bl0, bl1);
-              }
-            }
-          }
+            for (int r = 0; r < 4; ++r) acc[mt][r] *= alpha;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) zacc[r] *= alpha;
         }
       }
     }
-    // every warp is done with stage s (uniform abort decision)
-    aborted = __syncthreads_or(!ok) != 0;
-    if (aborted) {
-      it_fail = it;
+    float pa[NH], pb[NH];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+      pa[j] = ex2(sa[j] - mm[j]);
+      pb[j] = ex2(sb[j] - mm[j]);
+      l_run[j] += pa[j] + pb[j];
+    }
+    // ---------------- PV weights: f16 hi/lo of p, moved to the B layout
+    uint32_t bw[NT][2];
+    if constexpr (G8) {
+      const uint32_t ha = pack_half2(pa[0], pa[1]), hb = pack_half2(pb[0], pb[1]);
+      const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&ha));
+      const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&hb));
+      const uint32_t la = pack_half2(pa[0] - fa.x, pa[1] - fa.y), lb = pack_half2(pb[0] - fb.x, pb[1] - fb.y);
+      bw[0][0] = prmt(__shfl_sync(0xffffffffu, ha, src0), __shfl_sync(0xffffffffu, ha, src1), psel);
+      bw[0][1] = prmt(__shfl_sync(0xffffffffu, hb, src0), __shfl_sync(0xffffffffu, hb, src1), psel);
+      bw[NT - 1][0] = prmt(__shfl_sync(0xffffffffu, la, src0), __shfl_sync(0xffffffffu, la, src1), psel);
+      bw[NT - 1][1] = prmt(__shfl_sync(0xffffffffu, lb, src0), __shfl_sync(0xffffffffu, lb, src1), psel);
+    } else {
+      const uint32_t h = pack_half2(pa[0], pb[0]);
+      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&h));
+      const uint32_t lo = pack_half2(pa[0] - hf.x, pb[0] - hf.y);
+      const uint32_t hla = prmt(h, lo, 0x5410), hlb = prmt(h, lo, 0x7632);
+      bw[0][0] = prmt(__shfl_sync(0xffffffffu, hla, src0), __shfl_sync(0xffffffffu, hla, src1), psel);
+      bw[0][1] = prmt(__shfl_sync(0xffffffffu, hlb, src0), __shfl_sync(0xffffffffu, hlb, src1), psel);
+    }
+    // ---------------- PV
+    const int r0 = slot0 + tig, r1 = r0 + 8, r2 = r0 + 4, r3 = r0 + 12;
+    bool v0 = true, v1 = true, v2 = true, v3 = true;
+    if constexpr (!FULL) {
+      v0 = tb + tig >= g.S && tb + tig < h_end;
+      v1 = tb + tig + 8 >= g.S && tb + tig + 8 < h_end;
+      v2 = tb + tig + 4 >= g.S && tb + tig + 4 < h_end;
+      v3 = tb + tig + 12 >= g.S && tb + tig + 12 < h_end;
+    }
+    const uint8_t* vc = buf + Lay::VC;
+    const uint8_t* vs = buf + Lay::VSZ;
+    uint32_t xw[D / 64], yw[D / 64];  // code words: tokens (r0 | r1) and (r2 | r3) per half-word
+    if constexpr (D == 128) {
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vc + r0 * Lay::ROW + gid * 4);
+      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vc + r1 * Lay::ROW + gid * 4);
+      const uint32_t w2 = *reinterpret_cast<const uint32_t*>(vc + r2 * Lay::ROW + gid * 4);
+      const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vc + r3 * Lay::ROW + gid * 4);
+      xw[0] = prmt(w0, w1, 0x5410); xw[1] = prmt(w0, w1, 0x7632);
+      yw[0] = prmt(w2, w3, 0x5410); yw[1] = prmt(w2, w3, 0x7632);
+    } else {
+      const int wo = (gid >> 1) * 4;
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vc + r0 * Lay::ROW + wo);
+      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vc + r1 * Lay::ROW + wo);
+      const uint32_t w2 = *reinterpret_cast<const uint32_t*>(vc + r2 * Lay::ROW + wo);
+      const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vc + r3 * Lay::ROW + wo);
+      xw[0] = prmt(w0, w1, psel);
+      yw[0] = prmt(w2, w3, psel);
+    }
+    uint32_t Sx[GROUPS], Sy[GROUPS];
+    {
+      uint32_t s0[GROUPS], s1[GROUPS], s2[GROUPS], s3[GROUPS];
+      if constexpr (D == 128) {
+        const uint4 q0 = *reinterpret_cast<const uint4*>(vs + r0 * Lay::SZ);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(vs + r1 * Lay::SZ);
+        const uint4 q2 = *reinterpret_cast<const uint4*>(vs + r2 * Lay::SZ);
+        const uint4 q3 = *reinterpret_cast<const uint4*>(vs + r3 * Lay::SZ);
+        s0[0] = q0.x; s0[1] = q0.y; s0[2] = q0.z; s0[3] = q0.w;
+        s1[0] = q1.x; s1[1] = q1.y; s1[2] = q1.z; s1[3] = q1.w;
+        s2[0] = q2.x; s2[1] = q2.y; s2[2] = q2.z; s2[3] = q2.w;
+        s3[0] = q3.x; s3[1] = q3.y; s3[2] = q3.z; s3[3] = q3.w;
+      } else {
+        const uint2 q0 = *reinterpret_cast<const uint2*>(vs + r0 * Lay::SZ);
+        const uint2 q1 = *reinterpret_cast<const uint2*>(vs + r1 * Lay::SZ);
+        const uint2 q2 = *reinterpret_cast<const uint2*>(vs + r2 * Lay::SZ);
+        const uint2 q3 = *reinterpret_cast<const uint2*>(vs + r3 * Lay::SZ);
+        s0[0] = q0.x; s0[1] = q0.y; s1[0] = q1.x; s1[1] = q1.y;
+        s2[0] = q2.x; s2[1] = q2.y; s3[0] = q3.x; s3[1] = q3.y;
+      }
+#pragma unroll
+      for (int gi = 0; gi < GROUPS; ++gi) {
+        float f0 = neg_scale_times_pow2(s0[gi], v23), f1 = neg_scale_times_pow2(s1[gi], v23);
+        float f2 = neg_scale_times_pow2(s2[gi], v23), f3 = neg_scale_times_pow2(s3[gi], v23);
+        if constexpr (!FULL) {
+          f0 = v0 ? f0 : 0.f;
+          f1 = v1 ? f1 : 0.f;
+          f2 = v2 ? f2 : 0.f;
+          f3 = v3 ? f3 : 0.f;
+        }
+        Sx[gi] = pack_half2(f0, f1);
+        Sy[gi] = pack_half2(f2, f3);
+      }
+    }
+    // ux[k] / uy[k]: half-word part k >> 3, slot k & 7 -> channel 64 (k >> 3) + 8 (k & 7) + gid, group k >> 2
+    uint32_t ux[D / 8], uy[D / 8];
+#pragma unroll
+    for (int w = 0; w < D / 64; ++w) {
+      const uint32_t x6 = xw[w] >> 6, y6 = yw[w] >> 6;
+#define OSCAR_V_SLOT(X)                                                              \
+      ux[8 * w + X] = scale_codes(magic_slot<X>(xw[w], x6, magic), Sx[(8 * w + X) >> 2]);    \
+      uy[8 * w + X] = scale_codes(magic_slot<X>(yw[w], y6, magic), Sy[(8 * w + X) >> 2]);
+      OSCAR_V_SLOT(0) OSCAR_V_SLOT(1) OSCAR_V_SLOT(2) OSCAR_V_SLOT(3)
+      OSCAR_V_SLOT(4) OSCAR_V_SLOT(5) OSCAR_V_SLOT(6) OSCAR_V_SLOT(7)
+#undef OSCAR_V_SLOT
+    }
+#pragma unroll
+    for (int mt = 0; mt < Lay::MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma_f16(acc[mt], ux[2 * mt], ux[2 * mt + 1], uy[2 * mt], uy[2 * mt + 1], bw[nt][0], bw[nt][1]);
+    // zero term: rows = groups (row gid holds group zv), k = the lane's four tokens
+    {
+      float z0 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(vs + r0 * Lay::SZ + 4 * zv), v23);
+      float z1 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(vs + r1 * Lay::SZ + 4 * zv), v23);
+      float z2 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(vs + r2 * Lay::SZ + 4 * zv), v23);
+      float z3 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(vs + r3 * Lay::SZ + 4 * zv), v23);
+      if constexpr (!FULL) {
+        z0 = v0 ? z0 : 0.f;
+        z1 = v1 ? z1 : 0.f;
+        z2 = v2 ? z2 : 0.f;
+        z3 = v3 ? z3 : 0.f;
+      }
+      const uint32_t az0 = pack_half2(z0, z1), az2 = pack_half2(z2, z3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_f16(zacc, az0, 0u, az2, 0u, bw[nt][0], bw[nt][1]);
+    }
+  };
+
+  bool aborted = false;
+  int i_fail = 0;
+  for (int i = 0; i < n_mine; ++i) {
+    const int s = i % WS;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (i / WS) & 1, a.status));
+    if (!ok) {
+      aborted = true;
+      i_fail = i;
       break;
     }
-    if (tid == 0 && it + kStages < n_iters) issue(it + kStages);
-  }
-  if (aborted) {
-    // drain copies still in flight before the CTA exits, again bounded
-    if (tid == 0) {
-      const int last = min(n_iters, it_fail + kStages);
-      for (int it = it_fail; it < last; ++it) (void)mbar_wait_bounded(&bars[it % kStages], (it / kStages) & 1, nullptr);
+    if (stage_ok[s]) {
+      const uint8_t* buf = ring + s * Lay::BLOCK;
+      const int tp = (pg0 + warp + kWarps * i) * P;  // first token of the page
+#pragma unroll 1
+      for (int blk = 0; blk < P / 16; ++blk) {
+        const int tb = tp + 16 * blk;
+        if (tb >= g.S && tb + 16 <= h_end)
+          process(std::integral_constant<bool, true>{}, buf, 16 * blk, tb);
+        else if (tb + 16 > g.S && tb < h_end)
+          process(std::integral_constant<bool, false>{}, buf, 16 * blk, tb);
+      }
     }
-    __syncthreads();
-    pdl_launch_dependents();
-    return;
+    __syncwarp();
+    if (lane == 0 && i + WS < n_mine) {
+      fence_proxy_async_smem();
+      issue(i + WS);
+    }
+  }
+  if (aborted && lane == 0) {
+    // drain this warp's copies still in flight before the CTA exits, again bounded
+    const int last = min(n_mine, i_fail + WS);
+    for (int i = i_fail; i < last; ++i) (void)mbar_wait_bounded(&bars[i % WS], (i / WS) & 1, nullptr);
   }
   pdl_launch_dependents();
+  if (__syncthreads_or(aborted)) return;
 
   // ---------------- per-warp finalisation
+  // zero-term sums of head j for group gi live in lane (gid = gi, tig)
+  float zs[NH];
+#pragma unroll
+  for (int j = 0; j < NH; ++j) zs[j] = G8 ? zacc[j] : zacc[0] + zacc[1];
+  float zg[NH][GROUPS];
 #pragma unroll
   for (int j = 0; j < NH; ++j) {
     l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
     l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
     l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
 #pragma unroll
-    for (int gi = 0; gi < Lay::GROUPS; ++gi) {
-      zacc[j][gi] += __shfl_xor_sync(0xffffffffu, zacc[j][gi], 4);
-      zacc[j][gi] += __shfl_xor_sync(0xffffffffu, zacc[j][gi], 8);
-      zacc[j][gi] += __shfl_xor_sync(0xffffffffu, zacc[j][gi], 16);
-    }
+    for (int gi = 0; gi < GROUPS; ++gi) zg[j][gi] = __shfl_sync(0xffffffffu, zs[j], gi * 4 + tig);
   }
-  // cross-warp merge through shared memory (the stage ring is free now)
+  // cross-warp merge through shared memory (every ring is idle now)
   float* wm = reinterpret_cast<float*>(smem);   // [4][8]
   float* wl = wm + 32;                          // [4][8]
   float* wacc = wl + 32;                        // [4][8][D]
+  const float vscale = ldexpf(1.f, -a.k_exp_V);
 #pragma unroll
   for (int j = 0; j < NH; ++j) {
     const int hh = G8 ? 2 * tig + j : tig;
     if (hh < gq) {
       if (gid == 0) {
-        wm[warp * 8 + hh] = m_run[j];
+        wm[warp * 8 + hh] = mm[j];
         wl[warp * 8 + hh] = l_run[j];
       }
 #pragma unroll
       for (int mt = 0; mt < Lay::MT; ++mt) {
         const int ch_a = 16 * mt + gid, ch_b = ch_a + 8;
-        // G8: registers (0, 2) hold head 2tig, (1, 3) head 2tig+1.  Otherwise the
-        // register of the group's parity holds the value (the other is a discarded column).
-        const int par = (mt >> 1) & 1;
-        const float ra_ = G8 ? acc[mt][j] : acc[mt][par];
-        const float rb_ = G8 ? acc[mt][2 + j] : acc[mt][2 + par];
-        // channel ch of the V row sits in slot s = (ch mod 64) / 8 with bit position vpos(s)
-        const int sa = (ch_a & 63) >> 3, sb = (ch_b & 63) >> 3;
-        wacc[(warp * 8 + hh) * D + ch_a] = ldexpf(ra_, 7 - slot_pos_bf16(sa)) + zacc[j][ch_a / 32];
-        wacc[(warp * 8 + hh) * D + ch_b] = ldexpf(rb_, 7 - slot_pos_bf16(sb)) + zacc[j][ch_b / 32];
+        const float va_ = G8 ? acc[mt][j] : acc[mt][0] + acc[mt][1];
+        const float vb_ = G8 ? acc[mt][2 + j] : acc[mt][2] + acc[mt][3];
+        // channel 16mt + gid (+ 8) sits in slot (2mt) mod 8 (+ 1) of its half-word:
+        // code scale 2^(slot_pos - 10)
+        const float za = zg[j][mt >> 1] * vscale;
+        wacc[(warp * 8 + hh) * D + ch_a] = fmaf(va_, ldexpf(vscale, 10 - slot_pos((2 * mt) & 7)), za);
+        wacc[(warp * 8 + hh) * D + ch_b] = fmaf(vb_, ldexpf(vscale, 10 - slot_pos((2 * mt + 1) & 7)), za);
       }
     }
+  }
+  __syncthreads();
+  // per head: the merged reference, the warps' weights and the merged sum
+  float* wf = wacc + kWarps * 8 * D;   // [8][kWarps + 2]: f_0..f_3, M, L
+  if (tid < gq) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 8 + tid]);
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = wm[w * 8 + tid];
+      const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+      wf[tid * (kWarps + 2) + w] = f;
+      L = fmaf(f, wl[w * 8 + tid], L);
+    }
+    wf[tid * (kWarps + 2) + kWarps] = M;
+    wf[tid * (kWarps + 2) + kWarps + 1] = L;
   }
   __syncthreads();
   const int stride = a.wl.win_chunks + a.wl.max_splits;
   for (int idx = tid; idx < gq * D; idx += kThreads) {
     const int hh = idx / D, ch = idx % D;
-    float M = -INFINITY;
+    const float* f = wf + hh * (kWarps + 2);
+    float accv = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * 8 + hh]);
-    float accv = 0.f, L = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float mw = wm[w * 8 + hh];
-      const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-      accv = fmaf(f, wacc[(w * 8 + hh) * D + ch], accv);
-      L = fmaf(f, wl[w * 8 + hh], L);
-    }
+    for (int w = 0; w < kWarps; ++w) accv = fmaf(f[w], wacc[(w * 8 + hh) * D + ch], accv);
     float* pp = ws.part + (((size_t)b * g.Hq + kvh * gq + hh) * stride + blockIdx.x) * (D + 4);
     pp[4 + ch] = accv;
     if (ch == 0) {
-      pp[0] = M;
-      pp[1] = L;
+      pp[0] = f[kWarps];
+      pp[1] = f[kWarps + 1];
     }
   }
 }
@@ -941,9 +972,9 @@ __global__ void __launch_bounds__(kThreads) decode_combine_kernel(DecodeArgs a) 
 template <int D, int NT, int P>
 int launch_splitk_t(const DecodeArgs& a, cudaStream_t s, bool pdl) {
   using Lay = Int2Layout<D, NT, P>;
-  size_t smem = kStages * Lay::STAGE + kStages * 8 + kStages * 4;
+  size_t smem = Lay::SMEM;
   const size_t win_smem = 2 * kWinChunk * D * sizeof(uint16_t) + 8 * D * sizeof(float);
-  const size_t merge_smem = (64 + 4 * 8 * D) * sizeof(float);
+  const size_t merge_smem = (64 + kWarps * 8 * D + 8 * (kWarps + 2)) * sizeof(float);
   if (win_smem > smem) smem = win_smem;
   if (merge_smem > smem) smem = merge_smem;
   smem = (smem + 127) & ~size_t(127);

@@ -8,6 +8,7 @@
 // message.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -65,6 +66,9 @@ struct oscar_ctx {
   std::map<std::string, Timing> timers;
   std::vector<cudaEvent_t> event_pool;
   long long launches = 0;
+  // per layer: operand exponents of the history's scales and zeros in the
+  // decode MMAs (kNoOperandExp until a clip threshold is known for the layer)
+  std::vector<int> opexp_K, opexp_V;
 };
 
 namespace {
@@ -126,17 +130,23 @@ struct LaunchScope {
   const char* name;
   cudaStream_t s;
   cudaEvent_t a = nullptr, b = nullptr;
+  // Inside stream capture the two records become external event-record nodes
+  // of the graph, so one replay of the graph times the kernel on the device.
+  unsigned flags = cudaEventRecordDefault;
   LaunchScope(oscar_ctx* c, const char* n, void* stream) : ctx(c), name(n), s(static_cast<cudaStream_t>(stream)) {
     if (ctx->timing) {
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        flags = cudaEventRecordExternal;
       a = take_event(ctx);
       b = take_event(ctx);
-      if (a) cudaEventRecord(a, s);
+      if (a) cudaEventRecordWithFlags(a, s, flags);
     }
   }
   void done(int err) {
     if (err == 0) ctx->launches++;
     if (ctx->timing && a && b) {
-      cudaEventRecord(b, s);
+      cudaEventRecordWithFlags(b, s, flags);
       ctx->timers[name].pending.push_back({a, b});
     }
   }
@@ -166,18 +176,26 @@ oscar_status check_layer(const oscar_ctx* ctx, int32_t layer) {
 // ====================================================================== planning
 namespace oscar {
 
+int operand_exponent_for_clip(float clip) {
+  if (!(clip > 0.f) || !std::isfinite(clip)) return kNoOperandExp;
+  int e2 = 0;
+  std::frexp(clip, &e2);  // clip < 2^e2
+  const int k = 14 - e2;  // clip * 2^k < 2^14
+  return (k < 0 || k > 100) ? kNoOperandExp : k;
+}
+
 DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   DecodeWs w{};
   const int gq = g.Hq / g.Hkv;
   w.nt = gq == 8 ? 2 : 1;
-  const int stage_pages = bf16_pool ? 1 : 64 / g.P;
+  const int stage_pages = bf16_pool ? 1 : 4;  // INT2: the 4 warps of a split CTA stream pages round-robin
   long long max_pages;
   if (bf16_pool) max_pages = max_seq > 0 ? (max_seq - 1) / g.P + 1 : 0;
   else max_pages = (max_seq - g.W > g.S) ? (long long)(max_seq - g.W - 1) / g.P + 1 : 0;
   // Size the INT2 splits so that window CTAs plus INT2 CTAs fill the resident
   // CTA slots of one wave (152 SMs x CTAs per SM at the kernel's register use);
   // more requests than that run in several full waves.
-  const int occ = bf16_pool ? 2 : (w.nt == 2 ? 3 : 5);
+  const int occ = bf16_pool ? 2 : (w.nt == 2 ? 3 : 4);
   const long long win_ctas = bf16_pool ? 0 : (long long)batch * g.Hkv * ((g.S + g.W + 15) / 16);
   long long free_slots = 152LL * occ - win_ctas;
   if (free_slots < (long long)batch * g.Hkv) free_slots = (long long)batch * g.Hkv;
@@ -269,6 +287,8 @@ oscar_status oscar_create(const oscar_config* cfg, void* int2_pool, void* window
   ctx->pool = static_cast<uint8_t*>(int2_pool);
   ctx->slab = static_cast<uint16_t*>(window_slab);
   ctx->refcount.assign(g.num_pages, 0);
+  ctx->opexp_K.assign(g.L, oscar::kNoOperandExp);
+  ctx->opexp_V.assign(g.L, oscar::kNoOperandExp);
   ctx->free_stack.reserve(g.num_pages);
   for (int i = g.num_pages - 1; i >= 0; --i) ctx->free_stack.push_back(i);  // lowest id first
   if (const char* f = std::getenv("OSCAR_FAULT_ALLOC_FAIL_AFTER")) ctx->alloc_fail_after = std::atoll(f);
@@ -416,6 +436,23 @@ oscar_status oscar_fork_prefix(oscar_ctx* ctx, const int32_t* src_bt, int32_t* d
 }
 
 // ---------------------------------------------------------------- write path
+// Remember the largest clip thresholds a layer's history was written with (as
+// the smallest operand exponents); the decode kernels scale the history's BF16
+// scales and zeros by 2^k into f16 operands and need |value| * 2^k < 2^14.
+static oscar_status record_clip(oscar_ctx* ctx, int32_t layer, float clip_K, float clip_V) {
+  if (!(clip_K > 0.f) || !(clip_V > 0.f) || !std::isfinite(clip_K) || !std::isfinite(clip_V))
+    return fail(OSCAR_ERR_INVALID, "clip thresholds must be positive and finite");
+  const int ek = oscar::operand_exponent_for_clip(clip_K), ev = oscar::operand_exponent_for_clip(clip_V);
+  if (ek == oscar::kNoOperandExp || ev == oscar::kNoOperandExp)
+    return fail(OSCAR_ERR_UNSUPPORTED, "clip thresholds (%g, %g) outside [2^-86, 16384)", clip_K, clip_V);
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  int& k = ctx->opexp_K[layer];
+  int& v = ctx->opexp_V[layer];
+  k = (k == oscar::kNoOperandExp || ek < k) ? ek : k;
+  v = (v == oscar::kNoOperandExp || ev < v) ? ev : v;
+  return OSCAR_OK;
+}
+
 static oscar_status write_common(oscar_ctx* ctx, int32_t layer, const void* K, const void* V, int32_t dtype,
                                  const int32_t* cu_seqlens, const int32_t* start_pos, int32_t batch,
                                  int32_t total_tokens, const float* R_K, const float* R_V, float clip_K,
@@ -431,7 +468,7 @@ static oscar_status write_common(oscar_ctx* ctx, int32_t layer, const void* K, c
   if (!hadamard && (!R_K || !R_V)) return fail(OSCAR_ERR_INVALID, "R_K / R_V are null");
   if (!hadamard && (st = check_r_align(R_K, R_V)) != OSCAR_OK) return st;
   if (dtype != OSCAR_DTYPE_BF16 && dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad dtype %d", dtype);
-  if (!(clip_K > 0.f) || !(clip_V > 0.f)) return fail(OSCAR_ERR_INVALID, "clip thresholds must be positive");
+  if ((st = record_clip(ctx, layer, clip_K, clip_V)) != OSCAR_OK) return st;
   WriteArgs a{};
   a.g = ctx->g;
   a.layer = layer;
@@ -495,7 +532,7 @@ oscar_status oscar_append_step(oscar_ctx* ctx, int32_t layer, const void* K_new,
     return fail(OSCAR_ERR_INVALID, "null tensor argument");
   if ((st = check_r_align(R_K, R_V)) != OSCAR_OK) return st;
   if (dtype != OSCAR_DTYPE_BF16 && dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad dtype %d", dtype);
-  if (!(clip_K > 0.f) || !(clip_V > 0.f)) return fail(OSCAR_ERR_INVALID, "clip thresholds must be positive");
+  if ((st = record_clip(ctx, layer, clip_K, clip_V)) != OSCAR_OK) return st;
   WriteArgs a{};
   a.g = ctx->g;
   a.layer = layer;
@@ -521,6 +558,13 @@ oscar_status oscar_append_step(oscar_ctx* ctx, int32_t layer, const void* K_new,
   return OSCAR_OK;
 }
 
+oscar_status oscar_set_layer_clip(oscar_ctx* ctx, int32_t layer, float clip_K, float clip_V) {
+  if (!ctx) return fail(OSCAR_ERR_INVALID, "ctx is null");
+  oscar_status st = check_layer(ctx, layer);
+  if (st != OSCAR_OK) return st;
+  return record_clip(ctx, layer, clip_K, clip_V);
+}
+
 // ---------------------------------------------------------------- decode
 oscar_status oscar_decode_workspace_size(const oscar_config* cfg, int32_t batch, int32_t max_seq, size_t* bytes) {
   Geom g;
@@ -538,6 +582,16 @@ oscar_status oscar_bf16_decode_workspace_size(const oscar_config* cfg, int32_t b
   if (st != OSCAR_OK) return st;
   if (!bytes || batch < 0 || max_seq < 0) return fail(OSCAR_ERR_INVALID, "bad arguments to workspace size");
   *bytes = oscar::plan_decode(g, batch, max_seq, true).total;
+  return OSCAR_OK;
+}
+
+static oscar_status layer_operand_exps(oscar_ctx* ctx, int32_t layer, int* ek, int* ev) {
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  *ek = ctx->opexp_K[layer];
+  *ev = ctx->opexp_V[layer];
+  if (*ek == oscar::kNoOperandExp || *ev == oscar::kNoOperandExp)
+    return fail(OSCAR_ERR_INVALID,
+                "no clip threshold known for layer %d: write to it or call oscar_set_layer_clip first", layer);
   return OSCAR_OK;
 }
 
@@ -571,9 +625,14 @@ oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
                 ctx->g.S, ctx->g.W);
   if (!req_slot || !R_K || !R_V) return fail(OSCAR_ERR_INVALID, "null tensor argument");
   if ((st = check_r_align(R_K, R_V)) != OSCAR_OK) return st;
+  int ek, ev;
+  if ((st = layer_operand_exps(ctx, layer, &ek, &ev)) != OSCAR_OK) return st;
   DecodeArgs a{};
   a.g = ctx->g;
   a.layer = layer;
+  a.k_exp_K = ek;
+  a.k_exp_V = ev;
+  a.code_magic = oscar::kCodeMagic;
   a.q = q;
   a.q_dtype = q_dtype;
   a.out = out;
@@ -635,6 +694,8 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
   if (sink != ctx->g.S || recent != ctx->g.W)
     return fail(OSCAR_ERR_INVALID, "sink/recent (%d, %d) differ from the cache configuration (%d, %d)", sink, recent,
                 ctx->g.S, ctx->g.W);
+  int ek, ev;
+  if ((st = layer_operand_exps(ctx, layer, &ek, &ev)) != OSCAR_OK) return st;
   const DecodeWs plan = oscar::plan_decode(ctx->g, batch, max_seq, false);
   if (plan.total > oscar::kStaticScratchBytes)
     return fail(OSCAR_ERR_INVALID,
@@ -648,6 +709,9 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
   DecodeArgs a{};
   a.g = ctx->g;
   a.layer = layer;
+  a.k_exp_K = ek;
+  a.k_exp_V = ev;
+  a.code_magic = oscar::kCodeMagic;
   a.q = q;
   a.q_dtype = q_dtype;
   a.out = out;

@@ -20,6 +20,9 @@ constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;  // 200 
 // Size of the file-scope scratch used by the allocation-free decode entry point.
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
 
+// f16 pair (-1.0, -1.0): the pattern into which the decode kernels OR 2-bit codes
+constexpr unsigned kCodeMagic = 0xBC00BC00u;
+
 constexpr int kDtypeF32 = 0;
 constexpr int kDtypeBF16 = 1;
 
@@ -68,7 +71,7 @@ struct WriteArgs {
 struct DecodeWs {
   size_t qfrag_off, qaux_off, qplain_off, part_off, total;
   int max_splits;        // INT2 splits per (request, kv head)
-  int pages_per_split;   // multiple of 64 / page_size
+  int pages_per_split;   // multiple of the 4 warps of a split CTA (each warp streams its own pages)
   int nt;                // query n-tiles (max(1, 2*gq/8))
   int win_chunks;        // BF16 window CTAs per (request, kv head): grid.x = win_chunks + max_splits
   int combine_hpc;       // query heads per combine CTA (divides gq)
@@ -97,12 +100,17 @@ struct DecodeArgs {
   int* status;
   uint8_t* ws;
   DecodeWs wl;
-  int v_prescale_exp;        // softmax weights times 2^v_prescale_exp before the f16 split
+  int k_exp_K, k_exp_V;      // operand exponents: K (V) scales and zeros enter the f16 MMAs times 2^k
+  unsigned code_magic;       // kCodeMagic (f16 pair -1.0, -1.0), a launch argument so it lives in a register
 };
 
 // Host-side planning (pure functions, no CUDA).
 DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool);
-int v_prescale_exponent_for_clip(float clip_v);
+// Operand exponent k for a clip threshold c: c * 2^k < 2^14, so scales
+// (<= 2c/3) and zeros (|z| <= c) times 2^k are f16 numbers below 2^14.
+// Returns kNoOperandExp when c is outside [2^-86, 2^14).
+constexpr int kNoOperandExp = -1000;
+int operand_exponent_for_clip(float clip);
 
 // Kernel launchers (return cudaError_t as int).  Each launches on `stream`.
 int launch_write(const WriteArgs& a, void* stream);

@@ -191,6 +191,8 @@ def run_decode(gc: GpuCache, layer, q: np.ndarray, q_dtype: str, bt: np.ndarray,
     qd = dev_input(q, q_dtype)
     out = torch.empty((b, q.shape[1], q.shape[2]), dtype=torch.bfloat16 if out_bf16 else torch.float32, device="cuda")
     bt_d = dev(bt.astype(np.int32))
+    # an uploaded image carries no write call: declare the layer's clip thresholds
+    osc.oscar_set_layer_clip(gc.ctx, layer, fx["clip_K"], fx["clip_V"])
     osc.oscar_decode_attn(gc.ctx, layer, qd, dtype_code(q_dtype), out, osc.DTYPE_BF16 if out_bf16 else osc.DTYPE_F32,
                           bt_d, bt.shape[1], dev(np.asarray(seq_lens, np.int32)), dev(np.asarray(req_slot, np.int32)),
                           b, max_seq, gc.geom.sink, gc.geom.recent, dev(fx["R_K"]), dev(fx["R_V"]), ws, ws_bytes)

@@ -280,6 +280,11 @@ def test_bad_page_sets_status_without_fault(osc):
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
         out = torch.empty((1, 32, 128), dtype=torch.float32, device="cuda")
         q = H.dev_input(syn.queries(wl, 0, 1), "bf16")
+        with pytest.raises(osc.OscarError):   # no clip threshold declared for the layer yet
+            osc.oscar_decode_attn(gc.ctx, 0, q, osc.DTYPE_BF16, out, osc.DTYPE_F32, H.dev(bt), 8,
+                                  H.dev(np.array([500], np.int32)), H.dev(np.zeros(1, np.int32)), 1, 500, 4, 128,
+                                  H.dev(fx["R_K"]), H.dev(fx["R_V"]), ws, ws_bytes)
+        osc.oscar_set_layer_clip(gc.ctx, 0, fx["clip_K"], fx["clip_V"])
         osc.oscar_decode_attn(gc.ctx, 0, q, osc.DTYPE_BF16, out, osc.DTYPE_F32, H.dev(bt), 8,
                               H.dev(np.array([500], np.int32)), H.dev(np.zeros(1, np.int32)), 1, 500, 4, 128,
                               H.dev(fx["R_K"]), H.dev(fx["R_V"]), ws, ws_bytes)

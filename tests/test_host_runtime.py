@@ -143,6 +143,25 @@ def test_kernel_calls_need_device_buffers(osc):
         osc.oscar_destroy(ctx)
 
 
+def test_layer_clip_declaration(osc):
+    """Clip thresholds feed the f16 operand exponent of the decode MMAs: the range is validated on the host."""
+    ctx = osc.oscar_create(_cfg(osc))   # host-only context: the declaration is host state
+    try:
+        osc.oscar_set_layer_clip(ctx, 0, 3.5, 120.0)
+        osc.oscar_set_layer_clip(ctx, 1, 2.0 ** -80, 16383.0)
+        for clip_k, clip_v, code in ((0.0, 1.0, osc.ERR_INVALID), (1.0, -2.0, osc.ERR_INVALID),
+                                     (16384.0, 1.0, osc.ERR_UNSUPPORTED), (1.0, float("inf"), osc.ERR_INVALID),
+                                     (2.0 ** -90, 1.0, osc.ERR_UNSUPPORTED)):
+            with pytest.raises(osc.OscarError) as ei:
+                osc.oscar_set_layer_clip(ctx, 0, clip_k, clip_v)
+            assert ei.value.status == code, (clip_k, clip_v)
+        with pytest.raises(osc.OscarError) as ei:
+            osc.oscar_set_layer_clip(ctx, 2, 1.0, 1.0)   # layer out of range
+        assert ei.value.status == osc.ERR_INVALID
+    finally:
+        osc.oscar_destroy(ctx)
+
+
 def test_workspace_planning(osc):
     c = _cfg(osc, num_layers=1, num_pages=600)
     small = osc.oscar_decode_workspace_size(c, 1, 100)          # window only

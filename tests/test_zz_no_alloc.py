@@ -46,6 +46,7 @@ def test_noalloc_decode_matches_workspace_decode_twice(osc):
     gc = H.make_gpu_cache(geom, 32, ppr)
     try:
         gc.upload(img)
+        osc.oscar_set_layer_clip(gc.ctx, 0, fx["clip_K"], fx["clip_V"])
         max_seq = max(lens)
         args_common = dict(bt=H.dev(bt), lens=H.dev(np.asarray(lens, np.int32)), slots=H.dev(np.arange(b, dtype=np.int32)),
                            rk=H.dev(fx["R_K"]), rv=H.dev(fx["R_V"]))
