@@ -308,13 +308,15 @@ def run_ours(args, world, rank, local):
         lens = lens2 if lens is None else lens
         lb = lens.data_ptr()
         for layer in range(L):
-            if append:
-                osc.oscar_append_step(ctx, layer, step_ptr(kv_, layer, kvsz), step_ptr(vv, layer, kvsz),
-                                      osc.DTYPE_BF16, lb, 1, rk[layer], rv[layer], ck[layer], cv[layer], bt, ppr,
-                                      slot0)
-            osc.oscar_decode_attn(ctx, layer, step_ptr(qv, layer, qsz), osc.DTYPE_BF16, out[layer], osc.DTYPE_F32,
-                                  bt, ppr, lb + 4 if append else lb, slot0, 1, max_seq, s.sink, s.recent, rk[layer],
-                                  rv[layer], ws, ws_bytes)
+            if append:   # one fused call per layer: append the new token, attend over the cache including it
+                osc.oscar_decode_step(ctx, layer, step_ptr(kv_, layer, kvsz), step_ptr(vv, layer, kvsz),
+                                      osc.DTYPE_BF16, step_ptr(qv, layer, qsz), osc.DTYPE_BF16, out[layer],
+                                      osc.DTYPE_F32, bt, ppr, lb + 4, slot0, 1, max_seq, s.sink, s.recent, rk[layer],
+                                      rv[layer], ck[layer], cv[layer], ws, ws_bytes)
+            else:
+                osc.oscar_decode_attn(ctx, layer, step_ptr(qv, layer, qsz), osc.DTYPE_BF16, out[layer],
+                                      osc.DTYPE_F32, bt, ppr, lb, slot0, 1, max_seq, s.sink, s.recent, rk[layer],
+                                      rv[layer], ws, ws_bytes)
         if append:
             lens.add_(1)
 

@@ -77,6 +77,8 @@ _SIGS = {
     "oscar_decode_workspace_size": (_i32, [_cfgp, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)]),
     "oscar_decode_attn": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
                                  _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "oscar_decode_step": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32,
+                                 _i32, _i32, _vp, _vp, _f32, _f32, _vp, ctypes.c_size_t, _vp]),
     "oscar_decode_attn_noalloc": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32,
                                          _i32, _vp, _vp, _vp]),
     "oscar_bf16_decode_workspace_size": (_i32, [_cfgp, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)]),
@@ -242,6 +244,15 @@ def oscar_decode_attn(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_st
                       max_seq, sink, recent, R_K, R_V, workspace, ws_bytes, stream=None) -> None:
     _check(load().oscar_decode_attn(ctx, layer, ptr(q), q_dtype, ptr(out), out_dtype, ptr(block_table), bt_stride,
                                     ptr(seq_lens), ptr(req_slot), batch, max_seq, sink, recent, ptr(R_K), ptr(R_V),
+                                    ptr(workspace), ws_bytes, stream_ptr(stream)))
+
+
+def oscar_decode_step(ctx, layer, K_new, V_new, kv_dtype, q, q_dtype, out, out_dtype, block_table, bt_stride,
+                      seq_lens, req_slot, batch, max_seq, sink, recent, R_K, R_V, clip_K, clip_V, workspace, ws_bytes,
+                      stream=None) -> None:
+    _check(load().oscar_decode_step(ctx, layer, ptr(K_new), ptr(V_new), kv_dtype, ptr(q), q_dtype, ptr(out),
+                                    out_dtype, ptr(block_table), bt_stride, ptr(seq_lens), ptr(req_slot), batch,
+                                    max_seq, sink, recent, ptr(R_K), ptr(R_V), float(clip_K), float(clip_V),
                                     ptr(workspace), ws_bytes, stream_ptr(stream)))
 
 

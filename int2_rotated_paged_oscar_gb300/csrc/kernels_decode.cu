@@ -14,26 +14,16 @@
 //   o = (sum_win p v + acc_rot R_V^T) / l, R_V^T applied once per output row.
 //
 // Kernels (one decode step):
-//   q_rotate       q' = q R_K per (request, q head); writes the query-side MMA
-//                  fragments (f16 hi/lo split, per-head power-of-two scale),
-//                  the group sums Q_g = sum_{j in g} q'_j, and q as float32.
-//   decode_splitk  grid (1 + splits, kv heads, requests).  x = 0 is the BF16
-//                  window split (CUDA cores, float32); x >= 1 streams a range of
-//                  INT2 pages through a 4-stage shared-memory ring filled by
-//                  non-multicast bulk copies (one per (page, kv head) block,
-//                  mbarrier completion), and runs QK and PV on the tensor cores
-//                  with mma.sync m16n8k16:
-//                    QK  M = 16 tokens, N = (q head, f16 hi|lo), K = 16 channels,
-//                        A = K codes unpacked to c*2^(pos-10) in f16 (exact),
-//                        B = q' * 2^(e_h) * 2^(10-pos) split hi/lo; one
-//                        accumulator per 32-channel group so the BF16 scale and
-//                        zero apply in the float32 epilogue;
-//                    PV  M = 16 channels, N = (q head, bf16 hi|lo), K = 16 tokens,
-//                        A = V codes unpacked to c*2^(pos-7) in bf16 (exact),
-//                        B = p_t * scale_{t,g} split hi/lo; the zero term
-//                        sum_t p_t zero_{t,g} accumulates in float32.
-//                  Online softmax in the log2 domain with float32 max/sum.
-//   decode_combine merges the split partials, applies R_V^T once and divides by l.
+//   q_rotate       q' = q R_K per (request, kv head, channel group); writes the
+//                  query-side MMA fragments (f16 hi/lo of q' times a per-head
+//                  power of two), the group sums Q_g and q as float32.
+//   decode_splitk  grid (window chunks + INT2 splits, kv heads, requests).  Window
+//                  chunk CTAs score 16 BF16 window slots each in float32.  INT2
+//                  split CTAs stream pages through per-warp rings and run QK and
+//                  PV on the tensor cores (mma.sync m16n8k16, f16 operands with
+//                  the BF16 group scales folded in; see the split section).  Each
+//                  CTA writes one partial (m, l, acc) per query head.
+//   decode_combine merges the partials, applies R_V^T once and divides by l.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -355,14 +345,14 @@ struct Int2Layout {
 // Online softmax in the log2 domain with a lazy reference mm: it moves only
 // when a block maximum exceeds mm + 8 + j, so weights 2^(s - mm) stay below
 // 2^14 (f16) and rescaling is rare; the reference check is one warp vote.
+// Returns false if a page copy timed out (the CTA then writes no partial).
 template <int D, int NT, int P>
-__global__ void __launch_bounds__(kThreads, NT == 2 ? 3 : 4) decode_splitk_kernel(DecodeArgs a) {
+__device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) {
   using Lay = Int2Layout<D, NT, P>;
   constexpr int WS = Lay::WS;
   constexpr int GROUPS = Lay::GROUPS;
   constexpr bool G8 = NT == 2;
   constexpr int NH = G8 ? 2 : 1;  // query heads per lane
-  extern __shared__ __align__(128) uint8_t smem[];
 
   const Geom& g = a.g;
   const int b = blockIdx.z, kvh = blockIdx.y;
@@ -373,26 +363,26 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 3 : 4) decode_splitk_kerne
   if (!seq_len_ok(a, n)) {
     if (tid == 0 && blockIdx.x == 0) flag_error(a.status, kDevBadLen);
     pdl_launch_dependents();
-    return;
+    return true;
   }
   if ((int)blockIdx.x < a.wl.win_chunks) {
     const int req = a.req_slot[b];
     if (req < 0 || req >= g.max_req) {
       if (tid == 0 && blockIdx.x == 0) flag_error(a.status, kDevBadSlot);
       pdl_launch_dependents();
-      return;
+      return true;
     }
     pdl_wait();
     window_chunk<D>(a, b, kvh, blockIdx.x, smem);
     pdl_launch_dependents();
-    return;
+    return true;
   }
   const int split = blockIdx.x - a.wl.win_chunks;
   const int h_end = n - g.W;
-  if (h_end <= g.S) { pdl_launch_dependents(); return; }
+  if (h_end <= g.S) { pdl_launch_dependents(); return true; }
   const int n_hist_pages = (h_end - 1) / P + 1;
   const int pg0 = split * a.wl.pages_per_split;
-  if (pg0 >= n_hist_pages) { pdl_launch_dependents(); return; }
+  if (pg0 >= n_hist_pages) { pdl_launch_dependents(); return true; }
   const int pg1 = min(pg0 + a.wl.pages_per_split, n_hist_pages);
   const int n_mine = pg0 + warp < pg1 ? (pg1 - pg0 - warp + kWarps - 1) / kWarps : 0;
 
@@ -420,9 +410,13 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 3 : 4) decode_splitk_kerne
       bulk_g2s_hint(ring + s * Lay::BLOCK, pool_l + ((size_t)pid * g.Hkv + kvh) * Lay::BLOCK, Lay::BLOCK, &bars[s],
                     stream_policy);
   };
-  // first page now; the rest of the ring after the query-side set-up, so that
-  // first pages tend to arrive before any warp's later pages
-  if (lane == 0 && n_mine > 0) issue(0);
+  // Fill the ring before waiting on the preceding grid, so the page stream
+  // overlaps it.  In a fused step that grid (the append) may still be writing
+  // the last history page: a stage holding that page is filled after the wait.
+  auto is_tail = [&](int i) { return a.defer_tail_page && pg0 + warp + kWarps * i == n_hist_pages - 1; };
+  if (lane == 0)
+    for (int i = 0; i < WS && i < n_mine; ++i)
+      if (!is_tail(i)) issue(i);
 
   // ---------------- query side (written by q_rotate): wait for the previous grid
   pdl_wait();
@@ -464,7 +458,8 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 3 : 4) decode_splitk_kerne
   }
 
   if (lane == 0)
-    for (int i = 1; i < WS && i < n_mine; ++i) issue(i);
+    for (int i = 0; i < WS && i < n_mine; ++i)
+      if (is_tail(i)) issue(i);
 
   float mm[NH], thr[NH], l_run[NH];
   float acc[Lay::MT][4];
@@ -773,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 3 : 4) decode_splitk_kerne
     for (int i = i_fail; i < last; ++i) (void)mbar_wait_bounded(&bars[i % WS], (i / WS) & 1, nullptr);
   }
   pdl_launch_dependents();
-  if (__syncthreads_or(aborted)) return;
+  if (__syncthreads_or(aborted)) return false;
 
   // ---------------- per-warp finalisation
   // zero-term sums of head j for group gi live in lane (gid = gi, tig)
@@ -848,6 +843,13 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 3 : 4) decode_splitk_kerne
       pp[1] = f[kWarps + 1];
     }
   }
+  return true;
+}
+
+template <int D, int NT, int P>
+__global__ void __launch_bounds__(kThreads, NT == 2 ? 3 : 4) decode_splitk_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  (void)splitk_work<D, NT, P>(a, smem);
 }
 
 // ------------------------------------------------------------------ combine
@@ -1043,6 +1045,7 @@ int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl) {
   if (a.g.D == 128) return nt == 2 ? launch_splitk_p<128, 2>(a, s, pdl) : launch_splitk_p<128, 1>(a, s, pdl);
   return nt == 2 ? launch_splitk_p<64, 2>(a, s, pdl) : launch_splitk_p<64, 1>(a, s, pdl);
 }
+
 
 int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -411,89 +411,126 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) evict_kernel(WriteArgs a) {
 }
 
 // ------------------------------------------------------------------ decode append
-// grid = (batch, Hkv), block = 8 warps, dynamic shared memory = R_K and R_V
-// (2*D*D floats), brought in by two bulk copies.  Warp w works on K (w < 4) or V,
-// and on rotation chain k = w % 4 (input channels [kD/4, (k+1)D/4)).  The
-// chain-0 warp of K and of V adds the four chains in the canonical order,
-// quantises and packs.
+// grid = (batch, 2, ceil(Hkv / kAppendHeads)), block = 4 warps, dynamic shared
+// memory = one rotation (D*D floats).  blockIdx.y selects K (0) or V (1); the
+// CTA handles kAppendHeads kv heads.  One bulk copy brings R_K or R_V into
+// shared memory; warp k runs rotation chain k (input channels [kD/4, (k+1)D/4))
+// for every head of the CTA, lane l producing outputs [lC, (l+1)C); the chains
+// meet in shared memory and warp h adds them in the canonical order for head
+// h, quantises and packs.  The CTA reads the evicted token's ring row before
+// overwriting that slot with the new token.
+constexpr int kAppendHeads = 2;
+
+// Returns false if the rotation copy timed out (flagged; nothing written).
 template <int D>
-__global__ void __launch_bounds__(256) append_kernel(WriteArgs a) {
+__device__ __forceinline__ bool append_body(const WriteArgs& a, float* Rsm, uint64_t* bar) {
   constexpr int C = D / 32;
-  extern __shared__ __align__(16) float Rsm[];  // [2][D][D]
-  __shared__ float xs[2][D];
-  __shared__ float part[2][4][D];
-  __shared__ uint8_t code_scratch[2][D];
-  __shared__ __align__(8) uint64_t bar;
+  constexpr int HPC = kAppendHeads;
+  __shared__ float xs[HPC][D];
+  __shared__ float part[4][HPC][D];
+  __shared__ uint8_t code_scratch[HPC][D];
+  __shared__ uint16_t new_row[HPC][D];   // the new token, BF16
+  __shared__ int page_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geom& g = a.g;
-  const int b = blockIdx.x, h = blockIdx.y;
-  const int kv = warp >> 2, k = warp & 3;
-  const bool is_v = kv == 1;
-  const int n0 = a.start_pos[b];
+  const int b = blockIdx.x;
+  const bool is_v = blockIdx.y == 1;
+  const int h0 = blockIdx.z * HPC;
+  const int nh = min(HPC, g.Hkv - h0);
+  const int n0 = a.start_pos[b] + a.start_offset;
   if (n0 < 0 || n0 + 1 > g.max_pages_per_req * g.P) {
     if (threadIdx.x == 0) flag_error(a.status, kDevBadLen);
-    return;
+    return true;
   }
   const int req = a.req_slot[b];
   if (req < 0 || req >= g.max_req) {
     if (threadIdx.x == 0) flag_error(a.status, kDevBadSlot);
-    return;
+    return true;
   }
   const int slot_new = window_slot(n0, g.S, g.W);
-  uint16_t* ring = window_row(a, req, h, is_v, slot_new);
   const int e = n0 - g.W;
   const bool evict = e >= g.S;  // the evicted token occupies the slot the new token takes
-  if (evict) {
-    if (threadIdx.x == 0) {
-      mbar_init(&bar, 1);
-      fence_barrier_init();
-      mbar_arrive_expect_tx(&bar, 2 * D * D * sizeof(float));
-      bulk_g2s(Rsm, a.R_K, D * D * sizeof(float), &bar);
-      bulk_g2s(Rsm + D * D, a.R_V, D * D * sizeof(float), &bar);
+  // every global read of this kernel happens before the dependent kernel is let
+  // in: its page stream would otherwise queue ahead of them
+  if (evict && threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(bar, D * D * sizeof(float));
+    bulk_g2s(Rsm, is_v ? a.R_V : a.R_K, D * D * sizeof(float), bar);
+  }
+  if (evict && threadIdx.x == 32) page_sh = history_page(a, b, e);
+  const void* src = is_v ? a.V : a.K;
+  for (int idx = threadIdx.x; idx < nh * D; idx += blockDim.x) {
+    const int hh = idx / D, c = idx % D;
+    new_row[hh][c] = to_bf16_bits(load_in(src, a.dtype, ((size_t)b * g.Hkv + h0 + hh) * D + c));
+    if (evict) {
+      const uint16_t* ring = window_row(a, req, h0 + hh, is_v, slot_new);
+      xs[hh][c] = __uint_as_float(static_cast<uint32_t>(ring[c]) << 16);
     }
-    if (k == 0)
-      for (int c = lane; c < D; c += 32) xs[kv][c] = __uint_as_float(static_cast<uint32_t>(ring[c]) << 16);
-    __syncthreads();
-    if (!mbar_wait_bounded(&bar, 0, a.status)) {
-      (void)mbar_wait_bounded(&bar, 0, nullptr);
-      return;  // uniform: every thread times out on the same copy
-    }
-    const float* R = Rsm + kv * D * D;
-    float acc[C];
-#pragma unroll
-    for (int c = 0; c < C; ++c) acc[c] = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < D / 4; ++i) {
-      const int ii = k * (D / 4) + i;
-      const float xi = xs[kv][ii];
-      const float* r = R + ii * D + lane * C;
-#pragma unroll
-      for (int c = 0; c < C; ++c) acc[c] = fmaf(xi, r[c], acc[c]);
-    }
-#pragma unroll
-    for (int c = 0; c < C; ++c) part[kv][k][lane * C + c] = acc[c];
   }
   __syncthreads();
-  if (evict && k == 0) {
+  if (evict && !mbar_wait_bounded(bar, 0, a.status)) {
+    (void)mbar_wait_bounded(bar, 0, nullptr);
+    return false;  // uniform: every thread times out on the same copy
+  }
+  pdl_launch_dependents();
+  if (evict) {
+    float acc[HPC][C];
+#pragma unroll
+    for (int hh = 0; hh < HPC; ++hh)
+#pragma unroll
+      for (int c = 0; c < C; ++c) acc[hh][c] = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < D / 4; ++i) {
+      const int ii = warp * (D / 4) + i;
+      const float* r = Rsm + ii * D + lane * C;
+#pragma unroll
+      for (int hh = 0; hh < HPC; ++hh) {
+        const float xi = xs[hh][ii];
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[hh][c] = fmaf(xi, r[c], acc[hh][c]);
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < HPC; ++hh)
+#pragma unroll
+      for (int c = 0; c < C; ++c) part[warp][hh][lane * C + c] = acc[hh][c];
+  }
+  __syncthreads();
+  if (evict && warp < nh) {
     float y[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) {
       const int j = lane * C + c;
-      y[c] = ((part[kv][0][j] + part[kv][1][j]) + part[kv][2][j]) + part[kv][3][j];
+      y[c] = ((part[0][warp][j] + part[1][warp][j]) + part[2][warp][j]) + part[3][warp][j];
     }
-    const int page = history_page(a, b, e);
+    const int page = page_sh;
     if (page >= 0) {
       uint8_t* codes;
       uint32_t* sz;
-      history_row_ptrs<D>(a, page, e % g.P, h, is_v, &codes, &sz);
-      quant_pack_store<D>(y, is_v ? a.clip_V : a.clip_K, is_v, codes, sz, code_scratch[kv]);
+      history_row_ptrs<D>(a, page, e % g.P, h0 + warp, is_v, &codes, &sz);
+      quant_pack_store<D>(y, is_v ? a.clip_V : a.clip_K, is_v, codes, sz, code_scratch[warp]);
     }
   }
-  if (k == 0) {
-    const void* src = is_v ? a.V : a.K;
-    const size_t in_base = ((size_t)b * g.Hkv + h) * D;
-    for (int c = lane; c < D; c += 32) ring[c] = to_bf16_bits(load_in(src, a.dtype, in_base + c));
+  // the new token takes the ring slot (the evicted row was read above)
+  for (int idx = threadIdx.x; idx < nh * D; idx += blockDim.x) {
+    const int hh = idx / D, c = idx % D;
+    window_row(a, req, h0 + hh, is_v, slot_new)[c] = new_row[hh][c];
   }
+  return true;
+}
+
+// Launched after the query rotation of a fused decode step (programmatic
+// dependent launch), the append runs alongside it.  It lets the split-K kernel
+// launch once its own rotation copy has landed, and waits for its predecessor
+// only at the end, so that its completion implies the rotation's.  Launched
+// on its own, both are no-ops.
+template <int D>
+__global__ void __launch_bounds__(128) append_kernel(WriteArgs a) {
+  extern __shared__ __align__(16) float Rsm[];  // [D][D]
+  __shared__ __align__(8) uint64_t bar;
+  if (!append_body<D>(a, Rsm, &bar)) pdl_launch_dependents();
+  pdl_wait();
 }
 
 }  // namespace
@@ -526,20 +563,26 @@ int launch_evict(const WriteArgs& a, void* stream) {
   return static_cast<int>(cudaGetLastError());
 }
 
-int launch_append(const WriteArgs& a, void* stream) {
+int launch_append(const WriteArgs& a, void* stream, bool pdl) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.batch == 0) return 0;
-  dim3 grid(a.batch, a.g.Hkv);
-  const size_t smem = 2 * sizeof(float) * a.g.D * a.g.D;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.batch, 2, (a.g.Hkv + kAppendHeads - 1) / kAppendHeads);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = sizeof(float) * a.g.D * a.g.D;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
   if (a.g.D == 128) {
-    if ((e = ensure_smem_limit(append_kernel<128>, smem)) != cudaSuccess) return (int)e;
-    append_kernel<128><<<grid, 256, smem, s>>>(a);
-  } else {
-    if ((e = ensure_smem_limit(append_kernel<64>, smem)) != cudaSuccess) return (int)e;
-    append_kernel<64><<<grid, 256, smem, s>>>(a);
+    if ((e = ensure_smem_limit(append_kernel<128>, cfg.dynamicSmemBytes)) != cudaSuccess) return (int)e;
+    return (int)cudaLaunchKernelEx(&cfg, append_kernel<128>, a);
   }
-  return static_cast<int>(cudaGetLastError());
+  if ((e = ensure_smem_limit(append_kernel<64>, cfg.dynamicSmemBytes)) != cudaSuccess) return (int)e;
+  return (int)cudaLaunchKernelEx(&cfg, append_kernel<64>, a);
 }
 
 }  // namespace oscar

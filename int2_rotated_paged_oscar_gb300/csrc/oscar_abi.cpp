@@ -519,27 +519,30 @@ oscar_status oscar_write_kv_hadamard(oscar_ctx* ctx, int32_t layer, const void* 
                       clip_V, block_table, bt_stride, req_slot, stream, 1);
 }
 
-oscar_status oscar_append_step(oscar_ctx* ctx, int32_t layer, const void* K_new, const void* V_new, int32_t dtype,
-                               const int32_t* seq_lens_before, int32_t batch, const float* R_K, const float* R_V,
-                               float clip_K, float clip_V, const int32_t* block_table, int32_t bt_stride,
-                               const int32_t* req_slot, void* stream) {
+static oscar_status prepare_append(oscar_ctx* ctx, int32_t layer, const void* K_new, const void* V_new,
+                                   int32_t dtype, const int32_t* seq_lens, int32_t start_offset, int32_t batch,
+                                   const float* R_K, const float* R_V, float clip_K, float clip_V,
+                                   const int32_t* block_table, int32_t bt_stride, const int32_t* req_slot,
+                                   WriteArgs* out) {
   oscar_status st = need_device(ctx);
   if (st != OSCAR_OK) return st;
   if ((st = check_layer(ctx, layer)) != OSCAR_OK) return st;
   if (batch < 0 || bt_stride < 1) return fail(OSCAR_ERR_INVALID, "bad batch/bt_stride");
   if (batch == 0) return OSCAR_OK;
-  if (!K_new || !V_new || !seq_lens_before || !R_K || !R_V || !block_table || !req_slot)
+  if (!K_new || !V_new || !seq_lens || !R_K || !R_V || !block_table || !req_slot)
     return fail(OSCAR_ERR_INVALID, "null tensor argument");
   if ((st = check_r_align(R_K, R_V)) != OSCAR_OK) return st;
   if (dtype != OSCAR_DTYPE_BF16 && dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad dtype %d", dtype);
   if ((st = record_clip(ctx, layer, clip_K, clip_V)) != OSCAR_OK) return st;
-  WriteArgs a{};
+  WriteArgs& a = *out;
+  a = WriteArgs{};
   a.g = ctx->g;
   a.layer = layer;
   a.K = K_new;
   a.V = V_new;
   a.dtype = dtype;
-  a.start_pos = seq_lens_before;
+  a.start_pos = seq_lens;
+  a.start_offset = start_offset;
   a.batch = batch;
   a.R_K = R_K;
   a.R_V = R_V;
@@ -551,8 +554,19 @@ oscar_status oscar_append_step(oscar_ctx* ctx, int32_t layer, const void* K_new,
   a.pool = ctx->pool;
   a.slab = ctx->slab;
   a.status = ctx->d_status;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_append_step(oscar_ctx* ctx, int32_t layer, const void* K_new, const void* V_new, int32_t dtype,
+                               const int32_t* seq_lens_before, int32_t batch, const float* R_K, const float* R_V,
+                               float clip_K, float clip_V, const int32_t* block_table, int32_t bt_stride,
+                               const int32_t* req_slot, void* stream) {
+  WriteArgs a;
+  oscar_status st = prepare_append(ctx, layer, K_new, V_new, dtype, seq_lens_before, 0, batch, R_K, R_V, clip_K,
+                                   clip_V, block_table, bt_stride, req_slot, &a);
+  if (st != OSCAR_OK || batch == 0) return st;
   LaunchScope ls(ctx, "append", stream);
-  int e = oscar::launch_append(a, stream);
+  int e = oscar::launch_append(a, stream, false);
   ls.done(e);
   if (e) return cuda_fail(e, "append launch");
   return OSCAR_OK;
@@ -612,11 +626,11 @@ static oscar_status decode_common_checks(oscar_ctx* ctx, int32_t layer, const vo
   return OSCAR_OK;
 }
 
-oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
-                               int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
-                               const int32_t* seq_lens, const int32_t* req_slot, int32_t batch, int32_t max_seq,
-                               int32_t sink, int32_t recent, const float* R_K, const float* R_V, void* workspace,
-                               size_t ws_bytes, void* stream) {
+static oscar_status prepare_decode(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
+                                   int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
+                                   const int32_t* seq_lens, const int32_t* req_slot, int32_t batch, int32_t max_seq,
+                                   int32_t sink, int32_t recent, const float* R_K, const float* R_V, void* workspace,
+                                   size_t ws_bytes, DecodeArgs* dst) {
   oscar_status st = decode_common_checks(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens,
                                          batch, max_seq, workspace);
   if (st != OSCAR_OK || batch == 0) return st;
@@ -627,7 +641,8 @@ oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
   if ((st = check_r_align(R_K, R_V)) != OSCAR_OK) return st;
   int ek, ev;
   if ((st = layer_operand_exps(ctx, layer, &ek, &ev)) != OSCAR_OK) return st;
-  DecodeArgs a{};
+  DecodeArgs& a = *dst;
+  a = DecodeArgs{};
   a.g = ctx->g;
   a.layer = layer;
   a.k_exp_K = ek;
@@ -652,12 +667,29 @@ oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
   a.wl = oscar::plan_decode(ctx->g, batch, max_seq, false);
   if (ws_bytes < a.wl.total)
     return fail(OSCAR_ERR_INVALID, "workspace too small: %zu < %zu bytes", ws_bytes, a.wl.total);
+  return OSCAR_OK;
+}
+
+// q_rotate, [append], split-K, combine.  q_rotate is an ordinary launch, so it
+// starts after all earlier work on the stream; the later kernels use
+// programmatic dependent launch (unless kernel timing is on).  With an append
+// (a fused step) the append runs alongside q_rotate and ends by waiting for it;
+// split-K reads every page except the last history page before its own
+// dependency wait, because the append may be writing that page.
+static oscar_status launch_decode_chain(oscar_ctx* ctx, DecodeArgs& a, const WriteArgs* append, void* stream) {
   const bool pdl = !ctx->timing;  // timing events between launches would break the programmatic overlap
+  a.defer_tail_page = append != nullptr;
   {
     LaunchScope ls(ctx, "q_rotate", stream);
     int e = oscar::launch_q_rotate(a, stream);
     ls.done(e);
     if (e) return cuda_fail(e, "q_rotate launch");
+  }
+  if (append) {
+    LaunchScope ls(ctx, "append", stream);
+    int e = oscar::launch_append(*append, stream, pdl);
+    ls.done(e);
+    if (e) return cuda_fail(e, "append launch");
   }
   {
     LaunchScope ls(ctx, "decode_splitk", stream);
@@ -670,6 +702,35 @@ oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
   ls.done(e);
   if (e) return cuda_fail(e, "decode_combine launch");
   return OSCAR_OK;
+}
+
+oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
+                               int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
+                               const int32_t* seq_lens, const int32_t* req_slot, int32_t batch, int32_t max_seq,
+                               int32_t sink, int32_t recent, const float* R_K, const float* R_V, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  DecodeArgs a;
+  oscar_status st = prepare_decode(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens, req_slot,
+                                   batch, max_seq, sink, recent, R_K, R_V, workspace, ws_bytes, &a);
+  if (st != OSCAR_OK || batch == 0) return st;
+  return launch_decode_chain(ctx, a, nullptr, stream);
+}
+
+oscar_status oscar_decode_step(oscar_ctx* ctx, int32_t layer, const void* K_new, const void* V_new, int32_t kv_dtype,
+                               const void* q, int32_t q_dtype, void* out, int32_t out_dtype,
+                               const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                               const int32_t* req_slot, int32_t batch, int32_t max_seq, int32_t sink, int32_t recent,
+                               const float* R_K, const float* R_V, float clip_K, float clip_V, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  WriteArgs w;
+  oscar_status st = prepare_append(ctx, layer, K_new, V_new, kv_dtype, seq_lens, -1, batch, R_K, R_V, clip_K, clip_V,
+                                   block_table, bt_stride, req_slot, &w);
+  if (st != OSCAR_OK || batch == 0) return st;
+  DecodeArgs a;
+  st = prepare_decode(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens, req_slot, batch,
+                      max_seq, sink, recent, R_K, R_V, workspace, ws_bytes, &a);
+  if (st != OSCAR_OK) return st;
+  return launch_decode_chain(ctx, a, &w, stream);
 }
 
 oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,

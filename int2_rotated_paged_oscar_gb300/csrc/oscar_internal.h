@@ -65,6 +65,7 @@ struct WriteArgs {
   uint16_t* slab;
   int* status;
   int hadamard;            // 1: rotation is H_Had . P_br computed by a fast Walsh-Hadamard transform
+  int start_offset;        // append: the new token of request b is at start_pos[b] + start_offset
 };
 
 // Decode workspace carve-up (offsets in bytes from the workspace base).
@@ -102,6 +103,7 @@ struct DecodeArgs {
   DecodeWs wl;
   int k_exp_K, k_exp_V;      // operand exponents: K (V) scales and zeros enter the f16 MMAs times 2^k
   unsigned code_magic;       // kCodeMagic (f16 pair -1.0, -1.0), a launch argument so it lives in a register
+  int defer_tail_page;       // 1: the preceding kernel may still write the last history page (fused step)
 };
 
 // Host-side planning (pure functions, no CUDA).
@@ -115,7 +117,7 @@ int operand_exponent_for_clip(float clip);
 // Kernel launchers (return cudaError_t as int).  Each launches on `stream`.
 int launch_write(const WriteArgs& a, void* stream);
 int launch_evict(const WriteArgs& a, void* stream);
-int launch_append(const WriteArgs& a, void* stream);
+int launch_append(const WriteArgs& a, void* stream, bool pdl);
 int launch_q_rotate(const DecodeArgs& a, void* stream);
 int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl);
 int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl);

@@ -155,6 +155,53 @@ def test_append_and_extend_parity(osc):
         gc.close()
 
 
+def test_fused_decode_step_equals_append_then_decode(osc):
+    """oscar_decode_step (append alongside the query rotation) leaves the same cache and output, bit for bit,
+    as oscar_append_step followed by oscar_decode_attn; checked against the oracle at the end."""
+    import torch
+    wl = syn.Workload("step", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=12)
+    fx = H.fixture(wl)
+    ppr = 24
+    lens0 = [1300, 131]          # the second request starts evicting at its first step
+    bt = _contiguous_bt(2, ppr)
+    ga, img, _, _, _ = _prefill_both(osc, wl, fx, lens0, bt, 2 * ppr)
+    gb, _, _, _, _ = _prefill_both(osc, wl, fx, lens0, bt, 2 * ppr)
+    try:
+        slots = np.arange(2, dtype=np.int32)
+        max_seq = 64 * ppr
+        ws_bytes = osc.oscar_decode_workspace_size(ga.cfg, 2, max_seq)
+        wsa = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        wsb = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        rk, rv, btd, sld = H.dev(fx["R_K"]), H.dev(fx["R_V"]), H.dev(bt), H.dev(slots)
+        lens = list(lens0)
+        for step in range(70):   # crosses a page boundary of the evicted tokens
+            kn, vn = syn.kv_tokens(wl, 0, 2, sub=300 + step)
+            q = syn.queries(wl, 0, 2, sub=300 + step)
+            before = H.dev(np.array(lens, np.int32))
+            after = H.dev(np.array(lens, np.int32) + 1)
+            kd, vd, qd = H.dev_input(kn, "bf16"), H.dev_input(vn, "bf16"), H.dev_input(q, "bf16")
+            oa = torch.empty((2, 32, 128), dtype=torch.float32, device="cuda")
+            ob = torch.empty_like(oa)
+            osc.oscar_append_step(ga.ctx, 0, kd, vd, osc.DTYPE_BF16, before, 2, rk, rv, fx["clip_K"], fx["clip_V"],
+                                  btd, ppr, sld)
+            osc.oscar_decode_attn(ga.ctx, 0, qd, osc.DTYPE_BF16, oa, osc.DTYPE_F32, btd, ppr, after, sld, 2, max_seq,
+                                  4, 128, rk, rv, wsa, ws_bytes)
+            osc.oscar_decode_step(gb.ctx, 0, kd, vd, osc.DTYPE_BF16, qd, osc.DTYPE_BF16, ob, osc.DTYPE_F32, btd, ppr,
+                                  after, sld, 2, max_seq, 4, 128, rk, rv, fx["clip_K"], fx["clip_V"], wsb, ws_bytes)
+            assert torch.equal(oa, ob), step
+            cache.append_step(img, 0, kn, vn, np.array(lens, np.int32), fx["R_K"], fx["R_V"], fx["clip_K"],
+                              fx["clip_V"], bt, slots)
+            lens = [n + 1 for n in lens]
+        assert osc.oscar_check_status(ga.ctx) == 0 and osc.oscar_check_status(gb.ctx) == 0
+        assert np.array_equal(ga.pool_np(), gb.pool_np())
+        assert np.array_equal(ga.slab_np(), gb.slab_np())
+        want = attention.decode(img, 0, q, bt, lens, slots, fx["R_K"], fx["R_V"])
+        H.assert_decode_close(ob.cpu().numpy().astype(np.float64), want)
+    finally:
+        ga.close()
+        gb.close()
+
+
 def test_prefill_plus_appends_equals_direct_prefill_on_gpu(osc):
     wl = syn.Workload("chain", syn.Shape(16, 8, 128, 64, 32, 4, 128, 1), [0], seed=9)
     fx = H.fixture(wl)
