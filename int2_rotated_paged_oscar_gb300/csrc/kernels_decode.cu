@@ -100,8 +100,14 @@ __device__ __forceinline__ bool seq_len_ok(const DecodeArgs& a, int n) {
 // query-side MMA fragments of its two k-tiles.  The power-of-two scale of head
 // h is set from ||q_h||_2, which bounds |q'_h|_inf (R_K is orthogonal), so the
 // CTAs of a head need not agree on a maximum.
+//
+// Launched as a programmatic dependent of whatever preceded it on the stream,
+// it first waits for that grid (q, R_K and the cache may come from it) and only
+// then lets its own dependents launch, so every kernel after it still sees all
+// earlier work complete; the launch itself overlaps the predecessor's tail.
 template <int D>
 __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
+  pdl_wait();
   pdl_launch_dependents();
   __shared__ __align__(16) float Rs[D][33];   // R_K[:, 32 grp + c], padded
   __shared__ float qs[8][D];
@@ -884,6 +890,7 @@ __global__ void __launch_bounds__(kThreads) decode_combine_kernel(DecodeArgs a) 
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_launch_dependents();  // the next kernel may launch and wait on this one
   // R_V does not depend on the previous kernel: start its copy before waiting on it
   if (tid == 0) {
     mbar_arrive_expect_tx(&bar, D * D * sizeof(float) + (a.wl.combine_part_smem ? hpc * head_bytes : 0));
@@ -1007,9 +1014,17 @@ int launch_splitk_p(const DecodeArgs& a, cudaStream_t s, bool pdl) {
 }
 
 template <int D>
-int launch_q_rotate_t(const DecodeArgs& a, cudaStream_t s) {
-  q_rotate_kernel<D><<<dim3(a.g.Hkv * (D / 32), a.batch), kThreads, 0, s>>>(a);
-  return (int)cudaGetLastError();
+int launch_q_rotate_t(const DecodeArgs& a, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.g.Hkv * (D / 32), a.batch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return (int)cudaLaunchKernelEx(&cfg, q_rotate_kernel<D>, a);
 }
 
 }  // namespace
@@ -1034,9 +1049,9 @@ int static_decode_scratch(void** out, size_t* capacity) {
   return 0;
 }
 
-int launch_q_rotate(const DecodeArgs& a, void* stream) {
+int launch_q_rotate(const DecodeArgs& a, void* stream, bool pdl) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return a.g.D == 128 ? launch_q_rotate_t<128>(a, s) : launch_q_rotate_t<64>(a, s);
+  return a.g.D == 128 ? launch_q_rotate_t<128>(a, s, pdl) : launch_q_rotate_t<64>(a, s, pdl);
 }
 
 int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl) {

@@ -458,22 +458,47 @@ __device__ __forceinline__ bool append_body(const WriteArgs& a, float* Rsm, uint
     mbar_arrive_expect_tx(bar, D * D * sizeof(float));
     bulk_g2s(Rsm, is_v ? a.R_V : a.R_K, D * D * sizeof(float), bar);
   }
-  if (evict && threadIdx.x == 32) page_sh = history_page(a, b, e);
+  // issue the loads, let the dependent kernel launch (its first requests then
+  // queue behind these), then consume them
+  constexpr int PER = (HPC * D + 127) / 128;  // elements per thread (blockDim 128)
   const void* src = is_v ? a.V : a.K;
-  for (int idx = threadIdx.x; idx < nh * D; idx += blockDim.x) {
-    const int hh = idx / D, c = idx % D;
-    new_row[hh][c] = to_bf16_bits(load_in(src, a.dtype, ((size_t)b * g.Hkv + h0 + hh) * D + c));
-    if (evict) {
-      const uint16_t* ring = window_row(a, req, h0 + hh, is_v, slot_new);
-      xs[hh][c] = __uint_as_float(static_cast<uint32_t>(ring[c]) << 16);
+  float nv[PER], rv[PER];
+  int pid = -1;
+  if (evict && threadIdx.x == 32) {
+    const int lp = e / g.P;
+    if (lp < a.bt_stride && lp < g.max_pages_per_req) pid = a.block_table[(size_t)b * a.bt_stride + lp];
+  }
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int idx = threadIdx.x + u * 128;
+    nv[u] = rv[u] = 0.f;
+    if (idx < nh * D) {
+      const int hh = idx / D, c = idx % D;
+      nv[u] = load_in(src, a.dtype, ((size_t)b * g.Hkv + h0 + hh) * D + c);
+      if (evict) rv[u] = __uint_as_float(static_cast<uint32_t>(window_row(a, req, h0 + hh, is_v, slot_new)[c]) << 16);
     }
+  }
+  pdl_launch_dependents();
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int idx = threadIdx.x + u * 128;
+    if (idx < nh * D) {
+      new_row[idx / D][idx % D] = to_bf16_bits(nv[u]);
+      xs[idx / D][idx % D] = rv[u];
+    }
+  }
+  if (evict && threadIdx.x == 32) {
+    if (pid < 0 || pid >= g.num_pages) {
+      flag_error(a.status, kDevBadPage);
+      pid = -1;
+    }
+    page_sh = pid;
   }
   __syncthreads();
   if (evict && !mbar_wait_bounded(bar, 0, a.status)) {
     (void)mbar_wait_bounded(bar, 0, nullptr);
     return false;  // uniform: every thread times out on the same copy
   }
-  pdl_launch_dependents();
   if (evict) {
     float acc[HPC][C];
 #pragma unroll
@@ -522,14 +547,15 @@ __device__ __forceinline__ bool append_body(const WriteArgs& a, float* Rsm, uint
 
 // Launched after the query rotation of a fused decode step (programmatic
 // dependent launch), the append runs alongside it.  It lets the split-K kernel
-// launch once its own rotation copy has landed, and waits for its predecessor
-// only at the end, so that its completion implies the rotation's.  Launched
-// on its own, both are no-ops.
+// launch once its own reads are issued, and waits for its predecessor only at
+// the end, so that its completion implies the rotation's.  Launched on its
+// own, both are no-ops.
 template <int D>
 __global__ void __launch_bounds__(128) append_kernel(WriteArgs a) {
   extern __shared__ __align__(16) float Rsm[];  // [D][D]
   __shared__ __align__(8) uint64_t bar;
-  if (!append_body<D>(a, Rsm, &bar)) pdl_launch_dependents();
+  (void)append_body<D>(a, Rsm, &bar);
+  pdl_launch_dependents();  // no-op if already done; covers the early exits
   pdl_wait();
 }
 

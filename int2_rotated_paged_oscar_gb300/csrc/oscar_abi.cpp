@@ -670,9 +670,10 @@ static oscar_status prepare_decode(oscar_ctx* ctx, int32_t layer, const void* q,
   return OSCAR_OK;
 }
 
-// q_rotate, [append], split-K, combine.  q_rotate is an ordinary launch, so it
-// starts after all earlier work on the stream; the later kernels use
-// programmatic dependent launch (unless kernel timing is on).  With an append
+// q_rotate, [append], split-K, combine, all as programmatic dependent launches
+// (unless kernel timing is on).  q_rotate waits for its predecessor before it
+// lets the next kernel launch, so every later kernel starts with all earlier
+// work on the stream complete.  With an append
 // (a fused step) the append runs alongside q_rotate and ends by waiting for it;
 // split-K reads every page except the last history page before its own
 // dependency wait, because the append may be writing that page.
@@ -681,7 +682,7 @@ static oscar_status launch_decode_chain(oscar_ctx* ctx, DecodeArgs& a, const Wri
   a.defer_tail_page = append != nullptr;
   {
     LaunchScope ls(ctx, "q_rotate", stream);
-    int e = oscar::launch_q_rotate(a, stream);
+    int e = oscar::launch_q_rotate(a, stream, pdl);
     ls.done(e);
     if (e) return cuda_fail(e, "q_rotate launch");
   }
@@ -790,7 +791,7 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
   a.status = ctx->d_status;
   a.ws = static_cast<uint8_t*>(scratch);
   a.wl = plan;
-  if ((e = oscar::launch_q_rotate(a, stream))) return cuda_fail(e, "q_rotate launch");
+  if ((e = oscar::launch_q_rotate(a, stream, true))) return cuda_fail(e, "q_rotate launch");
   ctx->launches++;
   if ((e = oscar::launch_decode_splitk(a, stream, true))) return cuda_fail(e, "decode_splitk launch");
   ctx->launches++;

@@ -118,7 +118,7 @@ int operand_exponent_for_clip(float clip);
 int launch_write(const WriteArgs& a, void* stream);
 int launch_evict(const WriteArgs& a, void* stream);
 int launch_append(const WriteArgs& a, void* stream, bool pdl);
-int launch_q_rotate(const DecodeArgs& a, void* stream);
+int launch_q_rotate(const DecodeArgs& a, void* stream, bool pdl);
 int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl);
 int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl);
 int launch_bf16_prepare(const DecodeArgs& a, void* stream);
