@@ -1,0 +1,433 @@
+// Prefill / extend write of the OSCAR INT2 cache on the 5th-generation tensor
+// cores (tcgen05 + TMEM), for BF16 inputs and a dense rotation R.
+//
+// Source: OSCAR technical summary (gist.science), section 2.2 B -- history is
+// stored in INT2 after the fixed rotation and clipping; arXiv abstract -- fused
+// write kernel.  The rotation y = x R of a tile of 128 (token, kv head) rows is
+// a 128 x D x D GEMM:
+//   A = the rows, BF16 as received, staged by TMA with 128-byte swizzling;
+//   B = R split exactly into three BF16 planes R = R1 + R2 + R3 (R1 = bf16(R),
+//       R2 = bf16(R - R1), R3 = bf16(R - R1 - R2): 3 x 8 significant bits cover
+//       float32's 24), held transposed (K-major) in shared memory for the
+//       whole launch;
+//   D = float32 in tensor memory: per tile two partial accumulators (the small
+//       planes and the first half of K of R1; the second half of K of R1), added in
+//       float32 by the epilogue, and two such buffers so that the MMAs of one tile
+//       overlap the epilogue of the previous one.
+// Products of BF16 values are exact and accumulate in float32, so y carries
+// float32-level error like the CUDA-core path (not the same rounding).
+// Epilogue: thread t of the four epilogue warps owns row t of the tile (TMEM lane
+// t): it reads the row group by group (32 columns), clips, finds min/max, forms
+// the BF16 zero and scale, rounds the codes (reciprocal multiply) and packs the
+// K or V code row in registers.  Window rows (sink / recent) are copied to the
+// BF16 slab unrotated.
+// Roles: warps 0-3 epilogue, warp 4 producer (TMA, MMA issue, TMEM allocation).
+// Every mbarrier wait is bounded by %globaltimer; a timeout flags the status
+// word and the CTA stops issuing work.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "oscar_internal.h"
+
+namespace oscar {
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kEpiWarps = 4;
+constexpr int kTcThreads = (kEpiWarps + 1) * 32;
+constexpr int kPlanes = 3;
+
+// ------------------------------------------------------------------ tcgen05 / TMA wrappers
+__device__ __forceinline__ void tma_load_2d_tc(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_result)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, M = 128, N and K from the descriptors; one thread issues.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on bar once every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes: thread l gets lane (base lane + l).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte swizzled
+// layout (8-row atoms of 128 B; stride between atoms 1024 B).  Fields: start
+// address >> 4 (bits 0-13), leading byte offset >> 4 (16-29, unused for this
+// layout: 1), stride byte offset >> 4 (32-45), descriptor version 1 (46-47),
+// layout 2 = 128-byte swizzle (61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: D float32, A and B BF16, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+  return (1u << 4)                          // D format: F32
+         | (1u << 7)                        // A format: BF16
+         | (1u << 10)                       // B format: BF16
+         | ((uint32_t)(n >> 3) << 17)       // N / 8
+         | ((uint32_t)(m >> 4) << 24);      // M / 16
+}
+
+// Byte offset of element (row, k) in a K-major tile of 128-byte swizzled rows
+// (64 BF16 per row chunk): chunks of `rows` rows for k in [64c, 64c + 64).
+__device__ __forceinline__ uint32_t sw128_offset(int row, int k, int rows) {
+  const int c = k >> 6, kk = k & 63;
+  return (uint32_t)(c * rows * 128 + row * 128 + ((((kk >> 3) ^ (row & 7)) << 4) | ((kk & 7) << 1)));
+}
+
+
+// ------------------------------------------------------------------ shared memory plan
+template <int D>
+struct TcPlan {
+  static constexpr int KCH = D / 64;                 // 128-byte K chunks per row
+  static constexpr int A_BYTES = kTileM * D * 2;     // one A stage
+  static constexpr int B_PLANE = D * D * 2;          // one BF16 plane of R^T
+  static constexpr int A_OFF = kPlanes * B_PLANE;    // multiple of 1024
+  static constexpr int BAR_OFF = A_OFF + 2 * A_BYTES;
+  static constexpr int BYTES = BAR_OFF + 8 * 8 + 16;
+  static constexpr int SMEM = BYTES + 1024;          // slack for the 1024-byte alignment of the base
+  // per tile buffer two float32 accumulators of D columns (see the MMA order); two buffers
+  static constexpr uint32_t TMEM_COLS = 4 * D;
+};
+
+__device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+// Clip, quantise and pack group gi (32 channels, this thread's row) into the code
+// words and the (scale, zero) word.  Codes: clamp(rne((y - z) * (1/s)), 0, 3).
+template <int D, bool IS_V>
+__device__ __forceinline__ void quant_group(float (&y)[32], int gi, float clip, uint32_t (&words)[D / 16],
+                                            uint32_t& szw) {
+  float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    y[j] = fminf(fmaxf(y[j], -clip), clip);
+    mn = fminf(mn, y[j]);
+    mx = fmaxf(mx, y[j]);
+  }
+  const uint16_t zb = bf16_bits_rn(mn);
+  const uint16_t sb = bf16_bits_rn((mx - mn) / 3.0f);
+  const float z = __uint_as_float(static_cast<uint32_t>(zb) << 16);
+  const float sc = __uint_as_float(static_cast<uint32_t>(sb) << 16);
+  const float inv = sc > 0.f ? 1.0f / sc : 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t code = sc > 0.f ? (uint32_t)min(3, max(0, __float2int_rn((y[j] - z) * inv))) : 0u;
+    const int c = 32 * gi + j;
+    if constexpr (!IS_V) {
+      // K row: word tig*(D/64) + w holds slot x at bits 2x (channel c) and 16 + 2x (c + 1)
+      const int tig = (j & 7) >> 1, e = j & 1, h = (j >> 3) & 1, kt = j >> 4;
+      const int word = tig * (D / 64) + (gi >> 1);
+      const int x = 4 * (gi & 1) + 2 * kt + h;
+      words[word] |= code << (16 * e + 2 * x);
+    } else {
+      // V row: half-word hw = (D/64)(c mod 8) + c/64 holds channel c at bits 2 ((c mod 64) / 8)
+      const int hw = (D / 64) * (c & 7) + (c >> 6);
+      words[hw >> 1] |= code << (16 * (hw & 1) + 2 * ((c & 63) >> 3));
+    }
+  }
+  szw = static_cast<uint32_t>(sb) | (static_cast<uint32_t>(zb) << 16);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1) write_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                                                 const __grid_constant__ CUtensorMap tmap_v,
+                                                                 WriteArgs a) {
+  using L = TcPlan<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool is_v = blockIdx.y == 1;
+  const Geom& g = a.g;
+  uint8_t* bsm = smem;
+  uint8_t* asm_ = smem + L::A_OFF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* a_full = bars;
+  uint64_t* a_empty = bars + 2;
+  uint64_t* acc_full = bars + 4;
+  uint64_t* acc_empty = bars + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  const long long rows = (long long)a.total_tokens * g.Hkv;
+  const int tiles = (int)((rows + kTileM - 1) / kTileM);
+
+  // R^T as three BF16 planes, K-major with the 128-byte swizzle (row n = column n of R)
+  const float* R = is_v ? a.R_V : a.R_K;
+  for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) {
+    const int k = idx / D, n = idx % D;
+    const float r = __ldg(R + idx);
+    const __nv_bfloat16 p1 = __float2bfloat16_rn(r);
+    const float r1 = r - __bfloat162float(p1);
+    const __nv_bfloat16 p2 = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 p3 = __float2bfloat16_rn(r1 - __bfloat162float(p2));
+    const uint32_t off = sw128_offset(n, k, D);
+    *reinterpret_cast<__nv_bfloat16*>(bsm + off) = p1;
+    *reinterpret_cast<__nv_bfloat16*>(bsm + L::B_PLANE + off) = p2;
+    *reinterpret_cast<__nv_bfloat16*>(bsm + 2 * L::B_PLANE + off) = p3;
+  }
+  if (warp == kEpiWarps) {
+    if (lane == 0) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&a_full[i], 1);
+        mbar_init(&a_empty[i], 1);
+        mbar_init(&acc_full[i], 1);
+        mbar_init(&acc_empty[i], kEpiWarps * 32);
+      }
+      fence_barrier_init();
+    }
+    __syncwarp();
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+  }
+  fence_proxy_async_smem();  // the planes were written by ordinary stores; the MMAs read them as async proxy
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kEpiWarps) {
+    // ---------------- producer: TMA of the row tiles, MMA issue (one thread)
+    if (lane == 0) {
+      const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
+      const uint32_t idesc = idesc_bf16_f32(kTileM, D);
+      const uint32_t b_base = smem_u32(bsm);
+      int i = 0;
+      for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++i) {
+        const int s = i & 1;
+        const uint32_t u = (uint32_t)(i >> 1);
+        if (u >= 1 && !mbar_wait_bounded(&a_empty[s], (u - 1) & 1, a.status)) break;
+        mbar_arrive_expect_tx(&a_full[s], L::A_BYTES);
+#pragma unroll
+        for (int c = 0; c < L::KCH; ++c)
+          tma_load_2d_tc(asm_ + s * L::A_BYTES + c * kTileM * 128, tmap, 64 * c, tile * kTileM, &a_full[s]);
+        if (!mbar_wait_bounded(&a_full[s], u & 1, a.status)) break;
+        if (u >= 1 && !mbar_wait_bounded(&acc_empty[s], (u - 1) & 1, a.status)) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(asm_ + s * L::A_BYTES);
+        const uint32_t acc0 = tmem + (uint32_t)(s * 2 * D), acc1 = acc0 + (uint32_t)D;
+        // Accuracy: each MMA rounds its float32 accumulation once, relative to the running
+        // magnitude.  The small planes R3, R2 go first (into acc0, still small), then the
+        // main plane R1 over the first half of K into acc0 and over the second half into
+        // acc1; the epilogue adds acc0 + acc1 in float32.
+#pragma unroll
+        for (int pp = 0; pp < kPlanes; ++pp) {
+          const int p = kPlanes - 1 - pp;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const bool second = p == 0 && kk >= D / 32;
+            const uint32_t ak = (uint32_t)((kk >> 2) * kTileM * 128 + (kk & 3) * 32);
+            const uint32_t bk = (uint32_t)(p * L::B_PLANE + (kk >> 2) * D * 128 + (kk & 3) * 32);
+            const uint32_t first = (pp == 0 && kk == 0) || (p == 0 && kk == D / 32);
+            tc_mma_bf16(second ? acc1 : acc0, smem_desc_sw128(a_base + ak), smem_desc_sw128(b_base + bk), idesc,
+                        first ? 0u : 1u);
+          }
+        }
+        tc_commit(&a_empty[s]);
+        tc_commit(&acc_full[s]);
+      }
+      // the last arrivals of each stage's empty barrier land before the CTA may exit
+      for (int j = (i > 2 ? i - 2 : 0); j < i; ++j)
+        (void)mbar_wait_bounded(&a_empty[j & 1], (uint32_t)(j >> 1) & 1, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: thread t owns row t of the tile (TMEM lane t)
+    const int t = warp * 32 + lane;
+    const float clip = is_v ? a.clip_V : a.clip_K;
+    const void* src = is_v ? a.V : a.K;
+    int i = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++i) {
+      const int s = i & 1;
+      const uint32_t u = (uint32_t)(i >> 1);
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[s], u & 1, a.status))) break;
+      tc_fence_after();
+      // where this row goes: 1 = INT2 history slot, 2 = BF16 window slot, 0 = nowhere
+      const long long r = (long long)tile * kTileM + t;
+      int kind = 0, b = 0, pos = 0, h = 0, token = 0;
+      if (r < rows) {
+        token = static_cast<int>(r / g.Hkv);
+        h = static_cast<int>(r % g.Hkv);
+        int lo = 0, hi = a.batch - 1;  // request: largest b with cu_seqlens[b] <= token
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (a.cu_seqlens[mid] <= token) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        const int t0 = a.start_pos[b];
+        const int n1 = t0 + (a.cu_seqlens[b + 1] - a.cu_seqlens[b]);
+        pos = t0 + (token - a.cu_seqlens[b]);
+        if (t0 < 0 || n1 > g.max_pages_per_req * g.P) {
+          flag_error(a.status, kDevBadLen);
+        } else {
+          kind = (pos >= g.S && pos < n1 - g.W) ? 1 : 2;
+        }
+      }
+      uint32_t words[D / 16];
+      uint32_t szw[D / 32];
+#pragma unroll
+      for (int w = 0; w < D / 16; ++w) words[w] = 0u;
+#pragma unroll
+      for (int gi = 0; gi < D / 32; ++gi) {
+        float y[32], y1[32];
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(s * 2 * D + 32 * gi);
+        tmem_ld32(lane_base, y);
+        tmem_ld32(lane_base + (uint32_t)D, y1);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] += y1[j];
+        if (is_v) quant_group<D, true>(y, gi, clip, words, szw[gi]);
+        else quant_group<D, false>(y, gi, clip, words, szw[gi]);
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[s]);  // this accumulator may be overwritten once all 128 rows are read
+      if (kind == 1) {
+        const int lp = pos / g.P;
+        int page = -1;
+        if (lp < a.bt_stride && lp < g.max_pages_per_req) page = a.block_table[(size_t)b * a.bt_stride + lp];
+        if (page < 0 || page >= g.num_pages) {
+          flag_error(a.status, kDevBadPage);
+        } else {
+          uint8_t* blk = a.pool + (((size_t)a.layer * g.num_pages + page) * g.Hkv + h) * g.block_bytes();
+          uint4* codes = reinterpret_cast<uint4*>(blk + (is_v ? g.v_codes_off() : 0) + (size_t)(pos % g.P) * (D / 4));
+#pragma unroll
+          for (int q = 0; q < D / 64; ++q) codes[q] = make_uint4(words[4 * q], words[4 * q + 1], words[4 * q + 2], words[4 * q + 3]);
+          uint8_t* szp = blk + (is_v ? g.v_sz_off() : g.k_sz_off()) + (size_t)(pos % g.P) * (D / 8);
+          if constexpr (D == 128) *reinterpret_cast<uint4*>(szp) = make_uint4(szw[0], szw[1], szw[2], szw[3]);
+          else *reinterpret_cast<uint2*>(szp) = make_uint2(szw[0], szw[1]);
+        }
+      } else if (kind == 2) {
+        const int req = a.req_slot[b];
+        if (req < 0 || req >= g.max_req) {
+          flag_error(a.status, kDevBadSlot);
+        } else {
+          const size_t sbase = ((size_t)a.layer * g.max_req + req) * g.slab_req_elems();
+          const int slot = pos < g.S ? pos : g.S + (pos - g.S) % g.W;
+          uint4* dst = reinterpret_cast<uint4*>(a.slab + sbase + (((size_t)h * 2 + (is_v ? 1 : 0)) * g.window() + slot) * D);
+          const uint4* in = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + (size_t)r * D);
+#pragma unroll
+          for (int q = 0; q < D / 8; ++q) dst[q] = in[q];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kEpiWarps) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tc_get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map over rows of D BF16 values (rows = tokens x kv heads), box 64 x 128, 128-byte swizzle.
+int make_row_map(CUtensorMap* map, const void* base, long long rows, int D) {
+  auto enc = tc_get_encode();
+  if (!enc) return (int)cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kTileM};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+}
+
+template <int D>
+int launch_write_tc_t(const WriteArgs& a, cudaStream_t s) {
+  using L = TcPlan<D>;
+  const long long rows = (long long)a.total_tokens * a.g.Hkv;
+  const long long tiles = (rows + kTileM - 1) / kTileM;
+  CUtensorMap mk, mv;
+  int e = make_row_map(&mk, a.K, rows, D);
+  if (e) return e;
+  if ((e = make_row_map(&mv, a.V, rows, D))) return e;
+  // at least 120 KB of shared memory: one CTA per SM, so the TMEM allocation never waits
+  const int smem = L::SMEM > 120 * 1024 ? L::SMEM : 120 * 1024;
+  cudaError_t ce = ensure_smem_limit(write_tc_kernel<D>, smem);
+  if (ce != cudaSuccess) return (int)ce;
+  const int ctas = (int)(tiles < 76 ? tiles : 76);  // x2 (K, V): one CTA per SM
+  write_tc_kernel<D><<<dim3(ctas, 2), kTcThreads, smem, s>>>(mk, mv, a);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+bool write_tc_supported(const WriteArgs& a) {
+  return !a.hadamard && a.dtype == kDtypeBF16 && (a.g.D == 128 || a.g.D == 64) &&
+         (reinterpret_cast<uintptr_t>(a.K) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.V) & 15) == 0;
+}
+
+int launch_write_tc(const WriteArgs& a, void* stream) {
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((long long)a.total_tokens * a.g.Hkv == 0) return 0;
+  return a.g.D == 128 ? launch_write_tc_t<128>(a, s) : launch_write_tc_t<64>(a, s);
+}
+
+}  // namespace oscar

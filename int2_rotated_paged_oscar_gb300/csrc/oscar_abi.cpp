@@ -496,8 +496,10 @@ static oscar_status write_common(oscar_ctx* ctx, int32_t layer, const void* K, c
     ls.done(e);
     if (e) return cuda_fail(e, "evict launch");
   }
-  LaunchScope ls(ctx, "write", stream);
-  int e = oscar::launch_write(a, stream);
+  // BF16 rows with a dense rotation: tensor-core kernel; FP32 rows or the Hadamard-only rotation: CUDA cores
+  const bool tc = oscar::write_tc_supported(a);
+  LaunchScope ls(ctx, tc ? "write_tc" : "write", stream);
+  int e = tc ? oscar::launch_write_tc(a, stream) : oscar::launch_write(a, stream);
   ls.done(e);
   if (e) return cuda_fail(e, "write launch");
   return OSCAR_OK;
