@@ -21,7 +21,8 @@
 // the BF16 zero and scale, rounds the codes (reciprocal multiply) and packs the
 // K or V code row in registers.  Window rows (sink / recent) are copied to the
 // BF16 slab unrotated.
-// Roles: warps 0-3 epilogue, warp 4 producer (TMA, MMA issue, TMEM allocation).
+// Roles: the epilogue warps (per TMEM buffer and per column half of the row, one warp
+// per TMEM lane quadrant), then one producer warp (TMA, MMA issue, TMEM allocation).
 // Every mbarrier wait is bounded by %globaltimer; a timeout flags the status
 // word and the CTA stops issuing work.
 #include <cuda.h>
@@ -30,6 +31,8 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "oscar_internal.h"
 
@@ -37,8 +40,11 @@ namespace oscar {
 namespace {
 
 constexpr int kTileM = 128;
-constexpr int kEpiWarps = 4;
-constexpr int kTcThreads = (kEpiWarps + 1) * 32;
+// Epilogue warps: for each of the two TMEM buffers and each column half of the row,
+// four warps (one per TMEM lane quadrant); the producer warp comes after them.
+template <int D> __host__ __device__ constexpr int epi_halves() { return 1; }
+template <int D> __host__ __device__ constexpr int epi_warps() { return 2 * epi_halves<D>() * 4; }
+template <int D> __host__ __device__ constexpr int tc_threads() { return (epi_warps<D>() + 1) * 32; }
 constexpr int kPlanes = 3;
 
 // ------------------------------------------------------------------ tcgen05 / TMA wrappers
@@ -79,6 +85,22 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes: thread l gets lane (base lane + l).
+// The registers are valid after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
 }
 
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes: thread l gets lane (base lane + l).
@@ -138,11 +160,13 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int k, int rows) {
 template <int D>
 struct TcPlan {
   static constexpr int KCH = D / 64;                 // 128-byte K chunks per row
+  static constexpr int NS = 4;                       // row-tile stages in flight
   static constexpr int A_BYTES = kTileM * D * 2;     // one A stage
   static constexpr int B_PLANE = D * D * 2;          // one BF16 plane of R^T
   static constexpr int A_OFF = kPlanes * B_PLANE;    // multiple of 1024
-  static constexpr int BAR_OFF = A_OFF + 2 * A_BYTES;
-  static constexpr int BYTES = BAR_OFF + 8 * 8 + 16;
+  static constexpr int BAR_OFF = A_OFF + NS * A_BYTES;
+  static constexpr int NBARS = 2 * NS + 4;           // a_full[NS], a_empty[NS], acc_full[2], acc_empty[2]
+  static constexpr int BYTES = BAR_OFF + NBARS * 8 + 16;
   static constexpr int SMEM = BYTES + 1024;          // slack for the 1024-byte alignment of the base
   // per tile buffer two float32 accumulators of D columns (see the MMA order); two buffers
   static constexpr uint32_t TMEM_COLS = 4 * D;
@@ -154,46 +178,90 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
 }
 
 // Clip, quantise and pack group gi (32 channels, this thread's row) into the code
-// words and the (scale, zero) word.  Codes: clamp(rne((y - z) * (1/s)), 0, 3).
+// words and the (scale, zero) word.  The group's min and max are clipped (clipping
+// is monotonic, so they equal those of the clipped values); the codes are
+// clamp(rne((clip(y) - z) / s), 0, 3) computed as y * (1/s) - z/s clamped to the
+// images of the clip range and to [0, 3] in float, then rounded to nearest-even by
+// adding 1.5 * 2^23, whose float pattern carries the code in its low bits.  The code
+// words accumulate pattern << shift with one integer multiply-add per code; the
+// caller starts each word at minus the patterns' constant part (code_bias).
+constexpr float kRoundMagic = 12582912.0f;     // 1.5 * 2^23
+constexpr uint32_t kRoundBits = 0x4B400000u;   // its float pattern
 template <int D, bool IS_V>
-__device__ __forceinline__ void quant_group(float (&y)[32], int gi, float clip, uint32_t (&words)[D / 16],
+__device__ __forceinline__ void quant_group(const float (&y)[32], int gi, float clip, uint32_t (&words)[D / 16],
                                             uint32_t& szw) {
-  float mn = INFINITY, mx = -INFINITY;
+  float mn = y[0], mx = y[0];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    y[j] = fminf(fmaxf(y[j], -clip), clip);
+  for (int j = 1; j < 32; ++j) {
     mn = fminf(mn, y[j]);
     mx = fmaxf(mx, y[j]);
   }
+  mn = fminf(fmaxf(mn, -clip), clip);
+  mx = fminf(fmaxf(mx, -clip), clip);
   const uint16_t zb = bf16_bits_rn(mn);
   const uint16_t sb = bf16_bits_rn((mx - mn) / 3.0f);
   const float z = __uint_as_float(static_cast<uint32_t>(zb) << 16);
   const float sc = __uint_as_float(static_cast<uint32_t>(sb) << 16);
-  const float inv = sc > 0.f ? 1.0f / sc : 0.f;
+  const float inv = sc > 0.f ? __frcp_rn(sc) : 0.f;  // s = 0: every code 0
+  const float zinv = -z * inv;
+  // y -> y * inv - z * inv is monotonic, so clamping it to the images of -clip and
+  // clip is the same as clipping y first; then clamp to [0, 3]
+  const float t_lo = fmaxf(fmaf(-clip, inv, zinv), 0.f);
+  const float t_hi = fminf(fmaf(clip, inv, zinv), 3.f);
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    const uint32_t code = sc > 0.f ? (uint32_t)min(3, max(0, __float2int_rn((y[j] - z) * inv))) : 0u;
+    const float t = fminf(fmaxf(fmaf(y[j], inv, zinv), t_lo), t_hi);
+    const uint32_t pat = __float_as_uint(t + kRoundMagic);  // kRoundBits + code
     const int c = 32 * gi + j;
+    int word, shift;
     if constexpr (!IS_V) {
       // K row: word tig*(D/64) + w holds slot x at bits 2x (channel c) and 16 + 2x (c + 1)
       const int tig = (j & 7) >> 1, e = j & 1, h = (j >> 3) & 1, kt = j >> 4;
-      const int word = tig * (D / 64) + (gi >> 1);
-      const int x = 4 * (gi & 1) + 2 * kt + h;
-      words[word] |= code << (16 * e + 2 * x);
+      word = tig * (D / 64) + (gi >> 1);
+      shift = 16 * e + 2 * (4 * (gi & 1) + 2 * kt + h);
     } else {
       // V row: half-word hw = (D/64)(c mod 8) + c/64 holds channel c at bits 2 ((c mod 64) / 8)
       const int hw = (D / 64) * (c & 7) + (c >> 6);
-      words[hw >> 1] |= code << (16 * (hw & 1) + 2 * ((c & 63) >> 3));
+      word = hw >> 1;
+      shift = 16 * (hw & 1) + 2 * ((c & 63) >> 3);
     }
+    words[word] += pat << shift;
   }
   szw = static_cast<uint32_t>(sb) | (static_cast<uint32_t>(zb) << 16);
 }
 
+// Sum over the codes of channels [c_lo, c_hi) of a row of kRoundBits << shift, per
+// word (the constant part of the accumulated patterns), for K or V rows;
+// constant-folded when unrolled.
+template <int D, bool IS_V>
+__device__ __forceinline__ uint32_t code_bias(int word, int c_lo, int c_hi) {
+  uint32_t acc = 0;
+#pragma unroll
+  for (int c = 0; c < D; ++c) {
+    if (c < c_lo || c >= c_hi) continue;
+    const int gi = c / 32, j = c % 32;
+    int w, sh;
+    if constexpr (!IS_V) {
+      const int tig = (j & 7) >> 1, e = j & 1, h = (j >> 3) & 1, kt = j >> 4;
+      w = tig * (D / 64) + (gi >> 1);
+      sh = 16 * e + 2 * (4 * (gi & 1) + 2 * kt + h);
+    } else {
+      const int hw = (D / 64) * (c & 7) + (c >> 6);
+      w = hw >> 1;
+      sh = 16 * (hw & 1) + 2 * ((c & 63) >> 3);
+    }
+    if (w == word) acc += kRoundBits << sh;
+  }
+  return acc;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1) write_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+__global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                  const __grid_constant__ CUtensorMap tmap_v,
                                                                  WriteArgs a) {
   using L = TcPlan<D>;
+  constexpr int kEpiWarps = epi_warps<D>();
+  constexpr int HALVES = epi_halves<D>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,34 +271,52 @@ __global__ void __launch_bounds__(kTcThreads, 1) write_tc_kernel(const __grid_co
   uint8_t* asm_ = smem + L::A_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* a_full = bars;
-  uint64_t* a_empty = bars + 2;
-  uint64_t* acc_full = bars + 4;
-  uint64_t* acc_empty = bars + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  uint64_t* a_empty = bars + L::NS;
+  uint64_t* acc_full = bars + 2 * L::NS;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBARS);
   const long long rows = (long long)a.total_tokens * g.Hkv;
   const int tiles = (int)((rows + kTileM - 1) / kTileM);
 
   // R^T as three BF16 planes, K-major with the 128-byte swizzle (row n = column n of R)
   const float* R = is_v ? a.R_V : a.R_K;
-  for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) {
-    const int k = idx / D, n = idx % D;
-    const float r = __ldg(R + idx);
-    const __nv_bfloat16 p1 = __float2bfloat16_rn(r);
-    const float r1 = r - __bfloat162float(p1);
-    const __nv_bfloat16 p2 = __float2bfloat16_rn(r1);
-    const __nv_bfloat16 p3 = __float2bfloat16_rn(r1 - __bfloat162float(p2));
-    const uint32_t off = sw128_offset(n, k, D);
-    *reinterpret_cast<__nv_bfloat16*>(bsm + off) = p1;
-    *reinterpret_cast<__nv_bfloat16*>(bsm + L::B_PLANE + off) = p2;
-    *reinterpret_cast<__nv_bfloat16*>(bsm + 2 * L::B_PLANE + off) = p3;
+  // item = (n, k-octet): 8 consecutive k of column n, contiguous in the swizzled row
+  for (int item = threadIdx.x; item < D * D / 8; item += blockDim.x) {
+    const int n = item % D, k0 = (item / D) * 8;
+    uint32_t pk[3][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t lo[3], hi[3];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float r = __ldg(R + (size_t)(k0 + 2 * q + e) * D + n);
+        const __nv_bfloat16 p1 = __float2bfloat16_rn(r);
+        const float r1 = r - __bfloat162float(p1);
+        const __nv_bfloat16 p2 = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 p3 = __float2bfloat16_rn(r1 - __bfloat162float(p2));
+        const uint32_t b1 = *reinterpret_cast<const uint16_t*>(&p1), b2 = *reinterpret_cast<const uint16_t*>(&p2),
+                       b3 = *reinterpret_cast<const uint16_t*>(&p3);
+        (e ? hi : lo)[0] = b1;
+        (e ? hi : lo)[1] = b2;
+        (e ? hi : lo)[2] = b3;
+      }
+#pragma unroll
+      for (int p = 0; p < 3; ++p) pk[p][q] = lo[p] | (hi[p] << 16);
+    }
+    const uint32_t off = sw128_offset(n, k0, D);
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+      *reinterpret_cast<uint4*>(bsm + p * L::B_PLANE + off) = make_uint4(pk[p][0], pk[p][1], pk[p][2], pk[p][3]);
   }
   if (warp == kEpiWarps) {
     if (lane == 0) {
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < L::NS; ++i) {
         mbar_init(&a_full[i], 1);
         mbar_init(&a_empty[i], 1);
+      }
+      for (int i = 0; i < 2; ++i) {
         mbar_init(&acc_full[i], 1);
-        mbar_init(&acc_empty[i], kEpiWarps * 32);
+        mbar_init(&acc_empty[i], (kEpiWarps / 2) * 32);  // every epilogue warp of that buffer
       }
       fence_barrier_init();
     }
@@ -244,24 +330,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) write_tc_kernel(const __grid_co
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kEpiWarps) {
-    // ---------------- producer: TMA of the row tiles, MMA issue (one thread)
+    // ---------------- producer: TMA of the row tiles (NS ahead), MMA issue (one thread)
     if (lane == 0) {
       const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
       const uint32_t idesc = idesc_bf16_f32(kTileM, D);
       const uint32_t b_base = smem_u32(bsm);
-      int i = 0;
-      for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++i) {
-        const int s = i & 1;
-        const uint32_t u = (uint32_t)(i >> 1);
-        if (u >= 1 && !mbar_wait_bounded(&a_empty[s], (u - 1) & 1, a.status)) break;
-        mbar_arrive_expect_tx(&a_full[s], L::A_BYTES);
+      const int n_mine = blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+      auto load = [&](int i) {  // tile i of this CTA into stage i % NS
+        const int st = i % L::NS;
+        mbar_arrive_expect_tx(&a_full[st], L::A_BYTES);
+        const int tile = (int)blockIdx.x + i * (int)gridDim.x;
 #pragma unroll
         for (int c = 0; c < L::KCH; ++c)
-          tma_load_2d_tc(asm_ + s * L::A_BYTES + c * kTileM * 128, tmap, 64 * c, tile * kTileM, &a_full[s]);
-        if (!mbar_wait_bounded(&a_full[s], u & 1, a.status)) break;
-        if (u >= 1 && !mbar_wait_bounded(&acc_empty[s], (u - 1) & 1, a.status)) break;
+          tma_load_2d_tc(asm_ + st * L::A_BYTES + c * kTileM * 128, tmap, 64 * c, tile * kTileM, &a_full[st]);
+      };
+      for (int i = 0; i < L::NS && i < n_mine; ++i) load(i);
+      int i = 0;
+      for (; i < n_mine; ++i) {
+        const int st = i % L::NS;
+        const int s = i & 1;  // TMEM buffer
+        if (!mbar_wait_bounded(&a_full[st], (uint32_t)(i / L::NS) & 1, a.status)) break;
+        if (i >= 2 && !mbar_wait_bounded(&acc_empty[s], (uint32_t)((i >> 1) - 1) & 1, a.status)) break;
         tc_fence_after();
-        const uint32_t a_base = smem_u32(asm_ + s * L::A_BYTES);
+        const uint32_t a_base = smem_u32(asm_ + st * L::A_BYTES);
         const uint32_t acc0 = tmem + (uint32_t)(s * 2 * D), acc1 = acc0 + (uint32_t)D;
         // Accuracy: each MMA rounds its float32 accumulation once, relative to the running
         // magnitude.  The small planes R3, R2 go first (into acc0, still small), then the
@@ -280,25 +371,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) write_tc_kernel(const __grid_co
                         first ? 0u : 1u);
           }
         }
-        tc_commit(&a_empty[s]);
+        tc_commit(&a_empty[st]);
         tc_commit(&acc_full[s]);
+        // refill the stage of the previous tile (its MMAs were issued one tile ago)
+        if (i >= 1 && i - 1 + L::NS < n_mine) {
+          const int pst = (i - 1) % L::NS;
+          if (!mbar_wait_bounded(&a_empty[pst], (uint32_t)((i - 1) / L::NS) & 1, a.status)) break;
+          load(i - 1 + L::NS);
+        }
       }
-      // the last arrivals of each stage's empty barrier land before the CTA may exit
-      for (int j = (i > 2 ? i - 2 : 0); j < i; ++j)
-        (void)mbar_wait_bounded(&a_empty[j & 1], (uint32_t)(j >> 1) & 1, nullptr);
+      // every MMA-completion arrival lands before the CTA may exit
+      for (int j = (i > L::NS ? i - L::NS : 0); j < i; ++j)
+        (void)mbar_wait_bounded(&a_empty[j % L::NS], (uint32_t)(j / L::NS) & 1, nullptr);
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue: thread t owns row t of the tile (TMEM lane t)
-    const int t = warp * 32 + lane;
+    // ---------------- epilogue: warp w reads TMEM lane quadrant w % 4, takes the tiles of
+    // buffer eg = (w / 4) % 2 and the column half ch = w / 8 (groups [ch G/H, (ch+1) G/H));
+    // thread t owns row t of the tile
+    const int eg = (warp >> 2) & 1;
+    const int ch = warp >> 3;
+    const int t = (warp & 3) * 32 + lane;
+    constexpr int GPH = D / 32 / HALVES;  // groups per half
+    const int c_lo = ch * GPH * 32, c_hi = c_lo + GPH * 32;
     const float clip = is_v ? a.clip_V : a.clip_K;
     const void* src = is_v ? a.V : a.K;
-    int i = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++i) {
+    int i = eg;
+    for (int tile = blockIdx.x + eg * gridDim.x; tile < tiles; tile += 2 * gridDim.x, i += 2) {
       const int s = i & 1;
       const uint32_t u = (uint32_t)(i >> 1);
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[s], u & 1, a.status))) break;
-      tc_fence_after();
       // where this row goes: 1 = INT2 history slot, 2 = BF16 window slot, 0 = nowhere
       const long long r = (long long)tile * kTileM + t;
       int kind = 0, b = 0, pos = 0, h = 0, token = 0;
@@ -320,40 +421,82 @@ __global__ void __launch_bounds__(kTcThreads, 1) write_tc_kernel(const __grid_co
           kind = (pos >= g.S && pos < n1 - g.W) ? 1 : 2;
         }
       }
-      uint32_t words[D / 16];
-      uint32_t szw[D / 32];
-#pragma unroll
-      for (int w = 0; w < D / 16; ++w) words[w] = 0u;
-#pragma unroll
-      for (int gi = 0; gi < D / 32; ++gi) {
-        float y[32], y1[32];
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(s * 2 * D + 32 * gi);
-        tmem_ld32(lane_base, y);
-        tmem_ld32(lane_base + (uint32_t)D, y1);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) y[j] += y1[j];
-        if (is_v) quant_group<D, true>(y, gi, clip, words, szw[gi]);
-        else quant_group<D, false>(y, gi, clip, words, szw[gi]);
-      }
-      tc_fence_before();
-      mbar_arrive(&acc_empty[s]);  // this accumulator may be overwritten once all 128 rows are read
+      int page = -1, req = -1;  // looked up while the tile's MMAs run
       if (kind == 1) {
         const int lp = pos / g.P;
-        int page = -1;
         if (lp < a.bt_stride && lp < g.max_pages_per_req) page = a.block_table[(size_t)b * a.bt_stride + lp];
+      } else if (kind == 2) {
+        req = a.req_slot[b];
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[s], u & 1, a.status))) break;
+      tc_fence_after();
+      // read this row's groups from TMEM, quantise and pack; CH (column half) and IS_V are
+      // compile-time so that every code lands at a constant bit position
+      auto quant_store = [&](auto ch_tag, auto v_tag) {
+        constexpr int CH = decltype(ch_tag)::value;
+        constexpr bool IS_V = decltype(v_tag)::value;
+        constexpr int C_LO = CH * GPH * 32, C_HI = C_LO + GPH * 32;
+        uint32_t words[D / 16];
+        uint32_t szw[D / 32];
+#pragma unroll
+        for (int w = 0; w < D / 16; ++w) words[w] = 0u - code_bias<D, IS_V>(w, C_LO, C_HI);
+#pragma unroll
+        for (int gq = 0; gq < GPH; ++gq) {
+          const int gi = CH * GPH + gq;
+          uint32_t r0[32], r1[32];
+          const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(s * 2 * D + 32 * gi);
+          tmem_ld32_nowait(lane_base, r0);
+          tmem_ld32_nowait(lane_base + (uint32_t)D, r1);
+          tmem_wait_ld();
+          float y[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(r0[j]) + __uint_as_float(r1[j]);
+          quant_group<D, IS_V>(y, gi, clip, words, szw[gi]);
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[s]);  // this accumulator may be overwritten once every row is read
+        if (kind != 1) return;
         if (page < 0 || page >= g.num_pages) {
           flag_error(a.status, kDevBadPage);
-        } else {
-          uint8_t* blk = a.pool + (((size_t)a.layer * g.num_pages + page) * g.Hkv + h) * g.block_bytes();
-          uint4* codes = reinterpret_cast<uint4*>(blk + (is_v ? g.v_codes_off() : 0) + (size_t)(pos % g.P) * (D / 4));
-#pragma unroll
-          for (int q = 0; q < D / 64; ++q) codes[q] = make_uint4(words[4 * q], words[4 * q + 1], words[4 * q + 2], words[4 * q + 3]);
-          uint8_t* szp = blk + (is_v ? g.v_sz_off() : g.k_sz_off()) + (size_t)(pos % g.P) * (D / 8);
-          if constexpr (D == 128) *reinterpret_cast<uint4*>(szp) = make_uint4(szw[0], szw[1], szw[2], szw[3]);
-          else *reinterpret_cast<uint2*>(szp) = make_uint2(szw[0], szw[1]);
+          return;
         }
-      } else if (kind == 2) {
-        const int req = a.req_slot[b];
+        uint8_t* blk = a.pool + (((size_t)a.layer * g.num_pages + page) * g.Hkv + h) * g.block_bytes();
+        uint8_t* crow = blk + (IS_V ? g.v_codes_off() : 0) + (size_t)(pos % g.P) * (D / 4);
+        uint32_t* szp =
+            reinterpret_cast<uint32_t*>(blk + (IS_V ? g.v_sz_off() : g.k_sz_off()) + (size_t)(pos % g.P) * (D / 8));
+        if constexpr (HALVES == 1) {
+          uint4* codes = reinterpret_cast<uint4*>(crow);
+#pragma unroll
+          for (int q = 0; q < D / 64; ++q)
+            codes[q] = make_uint4(words[4 * q], words[4 * q + 1], words[4 * q + 2], words[4 * q + 3]);
+#pragma unroll
+          for (int gi = 0; gi < D / 32; ++gi) szp[gi] = szw[gi];
+        } else {
+          // D = 128, half CH: K rows own words tig*2 + CH; V rows own the half-words of parity CH
+          if constexpr (!IS_V) {
+            uint32_t* cw = reinterpret_cast<uint32_t*>(crow);
+#pragma unroll
+            for (int tg = 0; tg < 4; ++tg) cw[2 * tg + CH] = words[2 * tg + CH];
+          } else {
+            uint16_t* hw16 = reinterpret_cast<uint16_t*>(crow);
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+              hw16[2 * w + CH] = static_cast<uint16_t>(CH ? (words[w] >> 16) : (words[w] & 0xFFFFu));
+          }
+#pragma unroll
+          for (int gq = 0; gq < GPH; ++gq) szp[CH * GPH + gq] = szw[CH * GPH + gq];
+        }
+      };
+      using I0 = std::integral_constant<int, 0>;
+      using I1 = std::integral_constant<int, HALVES - 1>;
+      using VT = std::integral_constant<bool, true>;
+      using VF = std::integral_constant<bool, false>;
+      if (ch == 0) {
+        if (is_v) quant_store(I0{}, VT{}); else quant_store(I0{}, VF{});
+      } else {
+        if (is_v) quant_store(I1{}, VT{}); else quant_store(I1{}, VF{});
+      }
+      if (kind == 2 && ch == 0) {
         if (req < 0 || req >= g.max_req) {
           flag_error(a.status, kDevBadSlot);
         } else {
@@ -413,7 +556,7 @@ int launch_write_tc_t(const WriteArgs& a, cudaStream_t s) {
   cudaError_t ce = ensure_smem_limit(write_tc_kernel<D>, smem);
   if (ce != cudaSuccess) return (int)ce;
   const int ctas = (int)(tiles < 76 ? tiles : 76);  // x2 (K, V): one CTA per SM
-  write_tc_kernel<D><<<dim3(ctas, 2), kTcThreads, smem, s>>>(mk, mv, a);
+  write_tc_kernel<D><<<dim3(ctas, 2), tc_threads<D>(), smem, s>>>(mk, mv, a);
   return (int)cudaGetLastError();
 }
 
