@@ -17,7 +17,10 @@ reads and writes, divided by the device time), plus decode-only steps/s, the
 in-house BF16 paged decode on the same shapes, the dominant kernel's roofline
 (measured live with CUDA events), the end-to-end figure through the C ABI with
 host buffers, clocks sampled during the timed region, and the CPU oracle
-baseline.  ``--impl reference`` times the CPU oracle instead.
+baseline.  ``batch_sweep`` adds decode-only figures of the batched workload
+(Qwen3-32B-shaped layer, ragged U[8K, 32K] contexts, shuffled pages) at batch
+1, 8, 32 and 64, each beside the BF16 kernel on the same requests.
+``--impl reference`` times the CPU oracle instead.
 """
 from __future__ import annotations
 
@@ -50,6 +53,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the batched-decode sweep")
+    ap.add_argument("--sweep-batches", default="1,8,32,64")
     return ap.parse_args()
 
 
@@ -232,6 +237,158 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ GPU arm
+def batch_sweep(osc, batches, steps, hbm_peak, row_shift=37, l2_bytes=129e6):
+    """Decode-only sweep over batch sizes on the Qwen3-32B-shaped layer (64 q / 8 kv heads, d=128):
+    ragged lengths U[8K, 32K], pages handed out in shuffled order.  Per batch, enough layers are stacked
+    that one step reads at least twice the L2 size, so every layer's pages come from HBM.  Reports the
+    step time per layer, the effective GB/s of the whole decode, the split-K kernel's own GB/s against
+    the HBM peak, and the in-house BF16 paged kernel on the same requests."""
+    import torch
+    from int2_rotated_paged_oscar_gb300 import calibrate
+    rows = []
+    for B in batches:
+        wl = syn.batched_ragged(B)
+        s = wl.shape
+        lens = list(wl.seq_lens)
+        hq, hkv, d, P = s.n_q_heads, s.n_kv_heads, s.head_dim, s.page_size
+        nmax = max(lens)
+        ppr = syn.pages_for(nmax, P)
+        per_layer = sum(sum(decode_bytes(n, hq=hq).values()) for n in lens)
+        L = max(1, int(np.ceil(2 * l2_bytes / per_layer)))
+        cfg = osc.make_config(num_layers=L, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, page_size=P, sink=s.sink,
+                              recent=s.recent, max_requests=B, max_pages_per_req=ppr, num_pages=B * ppr)
+        pool = torch.empty(osc.oscar_int2_pool_bytes(cfg), dtype=torch.uint8, device="cuda")
+        slab = torch.zeros(osc.oscar_window_slab_bytes(cfg) // 2, dtype=torch.int16, device="cuda")
+        ctx = osc.oscar_create(cfg, pool, slab)
+        perm = syn.page_permutation(wl.seed, B * ppr, shuffle=True).reshape(B, ppr)
+        bt = torch.from_numpy(perm.astype(np.int32)).cuda()
+        kh, vh = syn.kv_tokens(wl, 0, nmax + row_shift * B)
+        kd = torch.from_numpy(syn.to_bf16_bits(kh).view(np.int16)).cuda()
+        vd = torch.from_numpy(syn.to_bf16_bits(vh).view(np.int16)).cuda()
+        del kh, vh
+        fx = calibrate.calibrate_layer(syn.queries(wl, 0, 128, calib=True), *syn.kv_tokens(wl, 0, 128, calib=True))
+        rk, rv = torch.from_numpy(fx["R_K"]).cuda(), torch.from_numpy(fx["R_V"]).cuda()
+        for layer in range(L):
+            for b, n in enumerate(lens):
+                o = row_shift * b
+                osc.oscar_write_kv(ctx, layer, kd[o:o + n], vd[o:o + n], osc.DTYPE_BF16,
+                                   torch.tensor([0, n], dtype=torch.int32, device="cuda"),
+                                   torch.zeros(1, dtype=torch.int32, device="cuda"), 1, n, rk, rv, fx["clip_K"],
+                                   fx["clip_V"], bt[b:b + 1], ppr, torch.tensor([b], dtype=torch.int32, device="cuda"))
+        torch.cuda.synchronize()
+        assert osc.oscar_check_status(ctx) == 0
+        q = torch.from_numpy(syn.to_bf16_bits(syn.queries(wl, 0, B * L)).view(np.int16)).cuda().view(L, B, hq, d)
+        out = torch.empty((L, B, hq, d), dtype=torch.float32, device="cuda")
+        lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        slots = torch.arange(B, dtype=torch.int32, device="cuda")
+        ws_bytes = osc.oscar_decode_workspace_size(cfg, B, nmax)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+
+        def dec_pass():
+            for layer in range(L):
+                osc.oscar_decode_attn(ctx, layer, q[layer], osc.DTYPE_BF16, out[layer], osc.DTYPE_F32, bt, ppr,
+                                      lens_d, slots, B, nmax, s.sink, s.recent, rk, rv, ws, ws_bytes)
+
+        row = {"batch": B, "layers_per_step": L, "mean_context": float(np.mean(lens)),
+               "bytes_per_layer": per_layer}
+        row.update(_time_graph(dec_pass, steps, L))
+        row["int2_effective_gbs"] = per_layer / (row["ms_per_layer"] * 1e-3) / 1e9
+        row["int2_frac_of_step"] = row["int2_effective_gbs"] / hbm_peak
+        osc.oscar_set_timing(ctx, True)
+        osc.oscar_reset_timing(ctx)
+        for _ in range(3):
+            g_t = _capture(dec_pass)
+            g_t.replay()
+            torch.cuda.synchronize()
+            del g_t
+        kms, kl = osc.oscar_kernel_time(ctx, "decode_splitk")
+        cms, _ = osc.oscar_kernel_time(ctx, "decode_combine")
+        osc.oscar_set_timing(ctx, False)
+        kb = sum(decode_bytes(n, hq=hq)["int2"] + decode_bytes(n, hq=hq)["window"] + decode_bytes(n, hq=hq)["q"]
+                 for n in lens)
+        row["splitk_avg_us"] = kms / max(kl, 1) * 1e3
+        row["combine_avg_us"] = cms / max(kl, 1) * 1e3
+        row["splitk_gbs"] = kb / (kms / max(kl, 1) * 1e-3) / 1e9
+        row["splitk_frac"] = row["splitk_gbs"] / hbm_peak
+        assert osc.oscar_check_status(ctx) == 0
+        osc.oscar_destroy(ctx)
+        del pool, slab
+        row.update(_bf16_sweep_point(osc, cfg, kd, vd, lens, perm, L, q, out, steps, row_shift))
+        row["int2_speedup_vs_bf16"] = row["bf16_ms_per_layer"] / row["ms_per_layer"]
+        rows.append(row)
+        del kd, vd, q, out, ws
+        torch.cuda.empty_cache()
+    return rows
+
+
+def _capture(fn):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def _time_graph(fn, steps, layers):
+    """Warm up eagerly, capture one pass, time `steps` replays with CUDA events."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    g = _capture(fn)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"ms_per_step": ms, "ms_per_layer": ms / layers}
+
+
+def _bf16_sweep_point(osc, cfg, kd, vd, lens, perm, L, q, out, steps, row_shift):
+    """The in-house BF16 paged decode over the same requests: BF16 pages [L][pages][Hkv][K|V][P][d]."""
+    import torch
+    B = len(lens)
+    hq, hkv, d, P = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.page_size
+    ppr = cfg.max_pages_per_req
+    bpool = torch.zeros((L, B * ppr, hkv, 2, P, d), dtype=torch.int16, device="cuda")
+    for b, n in enumerate(lens):
+        o = row_shift * b
+        npg = syn.pages_for(n, P)
+        kk = torch.zeros((npg * P, hkv, d), dtype=torch.int16, device="cuda")
+        vv = torch.zeros_like(kk)
+        kk[:n] = kd[o:o + n].view(n, hkv, d)
+        vv[:n] = vd[o:o + n].view(n, hkv, d)
+        idx = torch.from_numpy(perm[b, :npg].astype(np.int64)).cuda()
+        for layer in range(L):
+            bpool[layer, idx, :, 0] = kk.view(npg, P, hkv, d).permute(0, 2, 1, 3)
+            bpool[layer, idx, :, 1] = vv.view(npg, P, hkv, d).permute(0, 2, 1, 3)
+    bt = torch.from_numpy(perm.astype(np.int32)).cuda()
+    nmax = max(lens)
+    bcfg = osc.make_config(num_layers=L, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, page_size=P, sink=cfg.sink,
+                           recent=cfg.recent, max_requests=B, max_pages_per_req=ppr, num_pages=B * ppr)
+    dummy_pool = torch.empty(osc.oscar_int2_pool_bytes(bcfg), dtype=torch.uint8, device="cuda")
+    dummy_slab = torch.zeros(osc.oscar_window_slab_bytes(bcfg) // 2, dtype=torch.int16, device="cuda")
+    bctx = osc.oscar_create(bcfg, dummy_pool, dummy_slab)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ws_bytes = osc.oscar_bf16_decode_workspace_size(bcfg, B, nmax)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+
+    def bf_pass():
+        for layer in range(L):
+            osc.oscar_bf16_decode_attn(bctx, layer, bpool, q[layer], osc.DTYPE_BF16, out[layer], osc.DTYPE_F32, bt,
+                                       ppr, lens_d, B, nmax, ws, ws_bytes)
+
+    t = _time_graph(bf_pass, steps, L)
+    assert osc.oscar_check_status(bctx) == 0
+    osc.oscar_destroy(bctx)
+    bf_bytes = sum(n * hkv * 2 * d * 2 + hq * d * 2 + hq * d * 4 for n in lens)
+    return {"bf16_ms_per_layer": t["ms_per_layer"], "bf16_effective_gbs": bf_bytes / (t["ms_per_layer"] * 1e-3) / 1e9}
+
+
 def run_ours(args, world, rank, local):
     import torch
     from int2_rotated_paged_oscar_gb300 import build as bld
@@ -490,6 +647,9 @@ def run_ours(args, world, rank, local):
     assert osc.oscar_check_status(ctx) == 0
 
     value = sum_over_ranks(value_rank, world)
+    sweep = None
+    if rank == 0 and not args.no_sweep:
+        sweep = batch_sweep(osc, [int(x) for x in args.sweep_batches.split(",") if x], min(args.steps, 20), hbm_peak)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         r = oracle_decode_sample(target_s=15.0)
@@ -508,7 +668,10 @@ def run_ours(args, world, rank, local):
                           "what": f"prefill write of {L} layers x {n0} tokens x {hkv} kv heads (K and V)"},
                 "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "ms_per_step": e2e_ms},
-                "gpu_launches": int(launches), "clocks": clk, "cpu_baseline": cpu}
+                "gpu_launches": int(launches), "clocks": clk, "cpu_baseline": cpu,
+                "batch_sweep": {"workload": "Qwen3-32B-shaped layer (64 q / 8 kv heads, d=128), ragged context "
+                                            "U[8K, 32K], shuffled pages, decode only", "peak_gbs": hbm_peak,
+                                "rows": sweep}}
         print(json.dumps(line), flush=True)
     return 0
 

@@ -112,6 +112,8 @@ size_t oscar_page_block_bytes(const oscar_config* cfg);
 
 /* Validate cfg and create a context over caller-owned device buffers:
  * int2_pool (oscar_int2_pool_bytes) and window_slab (oscar_window_slab_bytes).
+ * The context keeps the raw pointers: both buffers must stay allocated until
+ * oscar_destroy (and until any captured graph that uses them is destroyed).
  * Either pointer may be NULL for a host-only context (allocator calls work,
  * kernel calls return OSCAR_ERR_INVALID).  Creating a context with buffers
  * allocates a 4-byte device status word.  OSCAR_ERR_UNSUPPORTED for a shape

@@ -446,21 +446,27 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     const int hh = G8 ? 2 * tig + j : tig;
     F[j] = hh < gq ? aux_base[hh * 8] * ldexpf(sm_log2, -a.k_exp_K) : 0.f;
   }
-  // zero-term B fragment: column gid, row 2tig + 1 = Q_tig * 2^(e_h + k_K) (BF16 hi or lo part)
-  uint32_t qz[NT];
+  // zero-term B fragments: column gid, row 2tig + 1 = Q_tig * 2^(e_h + k_K) as three BF16
+  // terms (hi + lo + lo2, 24 bits): part 0 carries hi in rows 0..7 (qz) and lo2 in rows
+  // 8..15 (qz2), part 1 carries lo; the A rows 8..15 repeat the (s, z) words.  Two terms
+  // (16 bits) leave errors of a few 1e-3 of the output's RMS at 32K tokens.
+  uint32_t qz[NT], qz2[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int hh = G8 ? gid : gid >> 1;
     const int part = G8 ? nt : gid & 1;
-    float v = 0.f;
+    float v = 0.f, v2 = 0.f;
     if (hh < gq && tig < GROUPS) {
       const float* aux = aux_base + hh * 8;
       const float qf = ldexpf(aux[1 + tig] / aux[0], a.k_exp_K);
       const float hi = __bfloat162float(__float2bfloat16_rn(qf));
-      v = part ? __bfloat162float(__float2bfloat16_rn(qf - hi)) : hi;
+      const float lo = __bfloat162float(__float2bfloat16_rn(qf - hi));
+      v = part ? lo : hi;
+      v2 = part ? 0.f : qf - hi - lo;
     }
-    const __nv_bfloat16 vb = __float2bfloat16_rn(v);
+    const __nv_bfloat16 vb = __float2bfloat16_rn(v), vb2 = __float2bfloat16_rn(v2);
     qz[nt] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&vb)) << 16;
+    qz2[nt] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&vb2)) << 16;
   }
 
   if (lane == 0)
@@ -564,7 +570,7 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
       }
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma_bf16(c[1], zA, zB, 0u, 0u, qz[nt], 0u);
+    for (int nt = 0; nt < NT; ++nt) mma_bf16(c[1], zA, zB, zA, zB, qz[nt], qz2[nt]);
     float sa[NH], sb[NH];
     if constexpr (G8) {
 #pragma unroll

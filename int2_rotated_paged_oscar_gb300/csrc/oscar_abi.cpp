@@ -192,16 +192,34 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   long long max_pages;
   if (bf16_pool) max_pages = max_seq > 0 ? (max_seq - 1) / g.P + 1 : 0;
   else max_pages = (max_seq - g.W > g.S) ? (long long)(max_seq - g.W - 1) / g.P + 1 : 0;
-  // Size the INT2 splits so that window CTAs plus INT2 CTAs fill the resident
-  // CTA slots of one wave (152 SMs x CTAs per SM at the kernel's register use);
-  // more requests than that run in several full waves.
   const int occ = bf16_pool ? 2 : (w.nt == 2 ? 3 : 4);
+  const long long wave = 152LL * occ;  // resident CTAs of one wave at the kernel's register use
+  const long long pairs = (long long)batch * g.Hkv > 0 ? (long long)batch * g.Hkv : 1;
   const long long win_ctas = bf16_pool ? 0 : (long long)batch * g.Hkv * ((g.S + g.W + 15) / 16);
-  long long free_slots = 152LL * occ - win_ctas;
-  if (free_slots < (long long)batch * g.Hkv) free_slots = (long long)batch * g.Hkv;
-  long long split_target = free_slots / ((long long)batch * g.Hkv > 0 ? (long long)batch * g.Hkv : 1);
-  if (split_target < 1) split_target = 1;
-  long long pps = max_pages > 0 ? (max_pages + split_target - 1) / split_target : stage_pages;
+  long long pps = stage_pages;
+  if (bf16_pool) {
+    // one wave of splits
+    long long free_slots = wave < pairs ? pairs : wave;
+    long long split_target = free_slots / pairs;
+    if (split_target < 1) split_target = 1;
+    pps = max_pages > 0 ? (max_pages + split_target - 1) / split_target : stage_pages;
+  } else if (max_pages > 0) {
+    // INT2: size splits from the step's page count (an upper bound from max_seq).
+    // When one wave holds every split, the splits share it with the window CTAs.
+    // Otherwise CTAs of at least kMinSplitPages pages run in up to eight waves:
+    // the hardware hands each freed slot the next CTA, which evens out ragged
+    // lengths, while the partials stay a small fraction of the cache bytes.
+    constexpr long long kMinSplitPages = 16;
+    const long long total = pairs * max_pages;
+    long long ctas = total / kMinSplitPages;
+    if (ctas < wave) {
+      ctas = wave - win_ctas;
+      if (ctas < pairs) ctas = pairs;
+    } else if (ctas > 8 * wave) {
+      ctas = 8 * wave;
+    }
+    pps = (total + ctas - 1) / ctas;
+  }
   if (pps < stage_pages) pps = stage_pages;
   pps = (pps + stage_pages - 1) / stage_pages * stage_pages;
   long long splits = max_pages > 0 ? (max_pages + pps - 1) / pps : 0;

@@ -199,3 +199,51 @@ def run_decode(gc: GpuCache, layer, q: np.ndarray, q_dtype: str, bt: np.ndarray,
     status = osc.oscar_check_status(gc.ctx)
     assert status == 0, f"device status {status}"
     return out.float().cpu().numpy().astype(np.float64)
+
+
+# ------------------------------------------------------------------ full-size cases: sampled checks
+def sampled_history_diag(geom: cache.Geometry, bt: np.ndarray, samples, fx) -> dict:
+    """Oracle write diagnostics (as cache.write_kv returns) for sampled history rows.
+
+    samples: list of (b, t, k_row [Hkv, d], v_row [Hkv, d]) with the input values of token t of request b.
+    """
+    b = np.array([s[0] for s in samples], dtype=np.int64)
+    t = np.array([s[1] for s in samples], dtype=np.int64)
+    xk = np.stack([s[2] for s in samples]).astype(np.float64)
+    xv = np.stack([s[3] for s in samples]).astype(np.float64)
+    kq = cache.quantize_rows(xk, fx["R_K"], fx["clip_K"], geom.group_size)
+    vq = cache.quantize_rows(xv, fx["R_V"], fx["clip_V"], geom.group_size)
+    pages = bt[b, t // geom.page_size]
+    return {"b": b, "t": t, "k": kq, "v": vq, "pages": pages, "slots": t % geom.page_size}
+
+
+def gpu_pages(gc: GpuCache, layer: int, pages) -> np.ndarray:
+    """Pool blocks [len(pages), Hkv, block] of one layer, gathered on the device."""
+    torch = torch_mod()
+    g = gc.geom
+    view = gc.pool.view(g.num_layers, g.num_pages, g.n_kv_heads * g.block_bytes)[layer]
+    idx = torch.as_tensor(np.asarray(pages, dtype=np.int64), device=view.device)
+    return view.index_select(0, idx).cpu().numpy().reshape(len(pages), g.n_kv_heads, g.block_bytes)
+
+
+def compact_request_image(gc: GpuCache, layer: int, bt_row, n: int, slot: int, heads=None):
+    """An oracle CacheImage holding one request of the GPU cache (its pages renumbered 0..k-1, one
+    request slot), optionally restricted to some kv heads.  Returns (image, block_table [1, k])."""
+    g = gc.geom
+    heads = list(range(g.n_kv_heads)) if heads is None else list(heads)
+    k = cache_pages_for(n, g)
+    pages = np.asarray(bt_row[:k], dtype=np.int64)
+    geom = cache.Geometry(1, len(heads), g.head_dim, g.page_size, g.group_size, g.sink, g.recent, max(k, 1), 1)
+    img = cache.CacheImage(geom)
+    if k:
+        img.pool[0] = gpu_pages(gc, layer, pages)[:, heads]
+    torch = torch_mod()
+    slab = gc.slab.view(g.num_layers, g.max_requests, g.n_kv_heads, 2, g.window, g.head_dim)[layer, slot]
+    img.slab[0, 0] = slab[heads].cpu().numpy().view(np.uint16)
+    return img, np.arange(max(k, 1), dtype=np.int32)[None]
+
+
+def cache_pages_for(n: int, g: cache.Geometry) -> int:
+    """Pages holding the history of a request of length n (absolute-position paging)."""
+    h_end = max(g.sink, n - g.recent)
+    return 0 if h_end <= g.sink else (h_end - 1) // g.page_size + 1
