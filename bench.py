@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the batched-decode sweep")
     ap.add_argument("--sweep-batches", default="1,8,32,64")
+    ap.add_argument("--sweep-only", action="store_true",
+                    help="run only the batched-decode sweep and print its rows (a profiling entry point)")
     return ap.parse_args()
 
 
@@ -237,7 +239,7 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ GPU arm
-def batch_sweep(osc, batches, steps, hbm_peak, row_shift=37, l2_bytes=129e6):
+def batch_sweep(osc, batches, steps, hbm_peak, row_shift=37, l2_bytes=129e6, with_bf16=True):
     """Decode-only sweep over batch sizes on the Qwen3-32B-shaped layer (64 q / 8 kv heads, d=128):
     ragged lengths U[8K, 32K], pages handed out in shuffled order.  Per batch, enough layers are stacked
     that one step reads at least twice the L2 size, so every layer's pages come from HBM.  Reports the
@@ -313,8 +315,9 @@ def batch_sweep(osc, batches, steps, hbm_peak, row_shift=37, l2_bytes=129e6):
         assert osc.oscar_check_status(ctx) == 0
         osc.oscar_destroy(ctx)
         del pool, slab
-        row.update(_bf16_sweep_point(osc, cfg, kd, vd, lens, perm, L, q, out, steps, row_shift))
-        row["int2_speedup_vs_bf16"] = row["bf16_ms_per_layer"] / row["ms_per_layer"]
+        if with_bf16:
+            row.update(_bf16_sweep_point(osc, cfg, kd, vd, lens, perm, L, q, out, steps, row_shift))
+            row["int2_speedup_vs_bf16"] = row["bf16_ms_per_layer"] / row["ms_per_layer"]
         rows.append(row)
         del kd, vd, q, out, ws
         torch.cuda.empty_cache()
@@ -649,7 +652,8 @@ def run_ours(args, world, rank, local):
     value = sum_over_ranks(value_rank, world)
     sweep = None
     if rank == 0 and not args.no_sweep:
-        sweep = batch_sweep(osc, [int(x) for x in args.sweep_batches.split(",") if x], min(args.steps, 20), hbm_peak)
+        sweep = batch_sweep(osc, [int(x) for x in args.sweep_batches.split(",") if x], min(args.steps, 20), hbm_peak,
+                            with_bf16=not args.no_bf16)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         r = oracle_decode_sample(target_s=15.0)
@@ -676,9 +680,26 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def run_sweep_only(args):
+    import torch
+    from int2_rotated_paged_oscar_gb300 import build as bld
+    bld.build()
+    import int2_rotated_paged_oscar_gb300 as osc
+    torch.cuda.set_device(0)
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(pk_path)) if os.path.exists(pk_path) else {}
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    rows = batch_sweep(osc, [int(x) for x in args.sweep_batches.split(",") if x], args.steps, hbm_peak,
+                       with_bf16=not args.no_bf16)
+    print(json.dumps({"batch_sweep": rows, "peak_gbs": hbm_peak}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
+    if args.sweep_only:
+        return run_sweep_only(args)
     if args.impl == "reference":
         rc = run_reference(args, world, rank)
     else:

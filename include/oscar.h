@@ -213,7 +213,10 @@ oscar_status oscar_decode_workspace_size(const oscar_config* cfg, int32_t batch,
  * configuration.  max_seq (host) bounds seq_lens and sizes the grid.
  * workspace: device scratch of oscar_decode_workspace_size bytes (256-byte
  * aligned); its contents need no initialisation.  The layer needs a declared
- * clip threshold (a write to it, or oscar_set_layer_clip). */
+ * clip threshold (a write to it, or oscar_set_layer_clip).  R_K and R_V
+ * (device float32 [d][d], the layer's fixed rotations) are read before the
+ * kernels wait on the work queued ahead of them: they must not be written by
+ * the kernel launched immediately before this call on the stream. */
 oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
                                int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
                                const int32_t* seq_lens, const int32_t* req_slot, int32_t batch, int32_t max_seq,

@@ -266,6 +266,20 @@ __device__ __forceinline__ float neg_scale_times_pow2(uint32_t w, uint32_t k23) 
 __device__ __forceinline__ float zero_times_pow2(uint32_t w, uint32_t k23) {
   return __uint_as_float((w & 0xFFFF0000u) + k23);
 }
+// scale * 2^k as float32 (k23 = k << 23, k >= 0).
+__device__ __forceinline__ float scale_times_pow2(uint32_t w, uint32_t k23) {
+  return __uint_as_float(w * 65536u + k23);
+}
+
+// The codes of slot X of a packed word as an f16 pair of subnormals c * 2^(pos - 24):
+// exact tensor-core operands with no offset term, so a product with q * 2^(e + 10 - pos)
+// is exactly c * q * 2^(e - 14) and the group's scale can be applied after the MMA.
+template <int X>
+__device__ __forceinline__ uint32_t subnormal_slot(uint32_t w, uint32_t w6) {
+  constexpr int pos = slot_pos(X);
+  constexpr uint32_t mask = (3u << pos) | (3u << (16 + pos));
+  return (X < 5 ? w : w6) & mask;
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo_elem, float hi_elem) {
   __half2 h = __floats2half2_rn(lo_elem, hi_elem);

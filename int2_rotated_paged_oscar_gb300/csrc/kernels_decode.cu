@@ -101,14 +101,13 @@ __device__ __forceinline__ bool seq_len_ok(const DecodeArgs& a, int n) {
 // h is set from ||q_h||_2, which bounds |q'_h|_inf (R_K is orthogonal), so the
 // CTAs of a head need not agree on a maximum.
 //
-// Launched as a programmatic dependent of whatever preceded it on the stream,
-// it first waits for that grid (q, R_K and the cache may come from it) and only
-// then lets its own dependents launch, so every kernel after it still sees all
-// earlier work complete; the launch itself overlaps the predecessor's tail.
+// Launched as a programmatic dependent of whatever preceded it on the stream:
+// it issues the loads of its R_K slice (a per-layer constant), then waits for
+// that grid (q and the cache may come from it) and only then lets its own
+// dependents launch, so every kernel after it still sees all earlier work
+// complete; the launch and the R_K loads overlap the predecessor's tail.
 template <int D>
 __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
-  pdl_wait();
-  pdl_launch_dependents();
   __shared__ __align__(16) float Rs[D][33];   // R_K[:, 32 grp + c], padded
   __shared__ float qs[8][D];
   __shared__ float qr[8][32];
@@ -118,7 +117,9 @@ __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int gq = g.gq();
   WsView ws = ws_view(a);
-  // R_K column slice: D rows x 32 floats (8 float4 per row), 16-byte loads, all in flight
+  // R_K column slice: D rows x 32 floats (8 float4 per row), 16-byte loads, all in
+  // flight.  R_K is a per-layer constant that the preceding kernel does not write,
+  // so the loads are issued before the wait on that kernel.
   {
     const float4* Rg = reinterpret_cast<const float4*>(a.R_K);
     float4 v[D * 8 / kThreads];
@@ -127,6 +128,8 @@ __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
       const int idx = t + u * kThreads;  // row idx / 8, float4 idx % 8
       v[u] = __ldg(Rg + (size_t)(idx >> 3) * (D / 4) + grp * 8 + (idx & 7));
     }
+    pdl_wait();
+    pdl_launch_dependents();
 #pragma unroll
     for (int u = 0; u < D * 8 / kThreads; ++u) {
       const int idx = t + u * kThreads;
@@ -488,7 +491,7 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
 
   const uint32_t magic = a.code_magic;
-  const uint32_t k23 = static_cast<uint32_t>(a.k_exp_K) << 23;
+  const uint32_t k23 = static_cast<uint32_t>(a.k_exp_K + 14) << 23;   // K scales: s * 2^(k_K + 14)
   const uint32_t v23 = static_cast<uint32_t>(a.k_exp_V) << 23;
   // rows of this lane inside a 16-token block: QK rows gid, gid + 8 are tokens
   // ra = sigma(gid), rb = sigma(gid + 8); PV k-indices 2tig, 2tig+1, 2tig+8, 2tig+9
@@ -531,29 +534,30 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     }
     uint32_t zA = *reinterpret_cast<const uint32_t*>(buf + Lay::KSZ + sA * Lay::SZ + 4 * zq);
     uint32_t zB = *reinterpret_cast<const uint32_t*>(buf + Lay::KSZ + sB * Lay::SZ + 4 * zq);
-    uint32_t SA[GROUPS], SB[GROUPS];
+    // group scales s * 2^(k_K + 14), applied to each group's accumulator after its MMAs
+    float SA[GROUPS], SB[GROUPS];
 #pragma unroll
     for (int gi = 0; gi < GROUPS; ++gi) {
-      float xa = neg_scale_times_pow2(szA[gi], k23), xb = neg_scale_times_pow2(szB[gi], k23);
-      if constexpr (!FULL) {
-        xa = va ? xa : 0.f;
-        xb = vb ? xb : 0.f;
-      }
-      SA[gi] = pack_half2(xa, xa);
-      SB[gi] = pack_half2(xb, xb);
+      SA[gi] = scale_times_pow2(szA[gi], k23);
+      SB[gi] = scale_times_pow2(szB[gi], k23);
     }
     if constexpr (!FULL) {
       zA = va ? zA : 0u;
       zB = vb ? zB : 0u;
     }
-    float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // per group: sum_c code_c * q'_c * 2^(e - 14) over its 32 channels (codes as exact
+    // f16 subnormals); the zero term sum_g z_g Q_g * 2^(e + k) in its own accumulator
+    float c[GROUPS][4];
+    float cz[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int gi = 0; gi < GROUPS; ++gi) c[gi][0] = c[gi][1] = c[gi][2] = c[gi][3] = 0.f;
 #pragma unroll
     for (int w = 0; w < D / 64; ++w) {
       const uint32_t a6 = kwA[w] >> 6, b6 = kwB[w] >> 6;
       uint32_t ua[8], ub[8];
-#define OSCAR_K_SLOT(X)                                                   \
-      ua[X] = scale_codes(magic_slot<X>(kwA[w], a6, magic), SA[2 * w + (X >> 2)]); \
-      ub[X] = scale_codes(magic_slot<X>(kwB[w], b6, magic), SB[2 * w + (X >> 2)]);
+#define OSCAR_K_SLOT(X)                        \
+      ua[X] = subnormal_slot<X>(kwA[w], a6); \
+      ub[X] = subnormal_slot<X>(kwB[w], b6);
       OSCAR_K_SLOT(0) OSCAR_K_SLOT(1) OSCAR_K_SLOT(2) OSCAR_K_SLOT(3)
       OSCAR_K_SLOT(4) OSCAR_K_SLOT(5) OSCAR_K_SLOT(6) OSCAR_K_SLOT(7)
 #undef OSCAR_K_SLOT
@@ -565,22 +569,34 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
           const int x = 4 * hg + 2 * kt;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            mma_f16(c[hg], ua[x], ub[x], ua[x + 1], ub[x + 1], qb[nt][2 * gi + kt][0], qb[nt][2 * gi + kt][1]);
+            mma_f16(c[gi], ua[x], ub[x], ua[x + 1], ub[x + 1], qb[nt][2 * gi + kt][0], qb[nt][2 * gi + kt][1]);
         }
       }
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma_bf16(c[1], zA, zB, zA, zB, qz[nt], qz2[nt]);
+    for (int nt = 0; nt < NT; ++nt) mma_bf16(cz, zA, zB, zA, zB, qz[nt], qz2[nt]);
     float sa[NH], sb[NH];
     if constexpr (G8) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        sa[j] = (c[0][j] + c[1][j]) * F[j];
-        sb[j] = (c[0][2 + j] + c[1][2 + j]) * F[j];
+        float ta = cz[j], tb = cz[2 + j];
+#pragma unroll
+        for (int gi = 0; gi < GROUPS; ++gi) {
+          ta = fmaf(SA[gi], c[gi][j], ta);
+          tb = fmaf(SB[gi], c[gi][2 + j], tb);
+        }
+        sa[j] = ta * F[j];
+        sb[j] = tb * F[j];
       }
     } else {
-      sa[0] = ((c[0][0] + c[0][1]) + (c[1][0] + c[1][1])) * F[0];
-      sb[0] = ((c[0][2] + c[0][3]) + (c[1][2] + c[1][3])) * F[0];
+      float ta = cz[0] + cz[1], tb = cz[2] + cz[3];
+#pragma unroll
+      for (int gi = 0; gi < GROUPS; ++gi) {
+        ta = fmaf(SA[gi], c[gi][0] + c[gi][1], ta);
+        tb = fmaf(SB[gi], c[gi][2] + c[gi][3], tb);
+      }
+      sa[0] = ta * F[0];
+      sb[0] = tb * F[0];
     }
     if constexpr (!FULL) {
 #pragma unroll
@@ -865,13 +881,169 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 3 : 4) decode_splitk_kerne
 }
 
 // ------------------------------------------------------------------ combine
-// grid (Hq / hpc, B), block 128.  One CTA handles hpc query heads of one
-// request: it merges the window partials (plain basis) and the INT2 partials
-// (rotated basis), applies R_V^T once per head, divides by l.  R_V and, when the
-// plan says they fit, the heads' partials are staged in shared memory by bulk
-// copies; otherwise the partials are read from global memory.
+// grid (Hq / hpc, B, D / jb), block kCombThreads.  One CTA merges the partials
+// of hpc query heads of one request (window partials in the plain basis, INT2
+// partials in the rotated basis) and produces output channels [j0, j0 + jb) of
+// each: o_j = (plain_j + sum_k rot_k R_V[j][k]) / l.  Rows j0 .. j0 + jb of R_V
+// and, when the plan says they fit, the heads' partials are staged in shared
+// memory by bulk copies (R_V's before the wait on the split kernel).
+//   1. warp per head: the reference M, the split weights 2^(m_i - M) and l;
+//   2. every thread: merged rotated accumulators (all D channels) and the
+//      window accumulators of its output channels;
+//   3. thread per output channel (and head group, or k slice when the CTA has
+//      fewer heads than threads per channel): float4 rows of R_V, each thread
+//      starting at its own k offset so that a phase of 8 threads reads 8
+//      different bank groups.
+constexpr int kCombThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(kThreads) decode_combine_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(DecodeArgs a) {
+  extern __shared__ __align__(16) float csm[];
+  __shared__ __align__(8) uint64_t bar;
+  const Geom& g = a.g;
+  const int hpc = a.wl.combine_hpc, jb = a.wl.combine_jb;
+  const int b = blockIdx.y, h0 = blockIdx.x * hpc, j0 = blockIdx.z * jb;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  WsView ws = ws_view(a);
+  const int wc = a.wl.win_chunks;
+  const int stride = wc + a.wl.max_splits;
+  const size_t head_floats = (size_t)stride * (D + 4);
+  float* Rs = csm;                             // [jb][D]: rows j0 .. j0 + jb of R_V
+  float* rot = Rs + jb * D;                    // [hpc][D]
+  float* plain = rot + hpc * D;                // [hpc][jb]
+  float* red = plain + hpc * jb;               // [kCombThreads] k-slice partial sums
+  float* lsum = red + kCombThreads;            // [16]
+  float* parts = lsum + 16;                    // [hpc][stride][D + 4] when staged (16-byte aligned)
+  float* wts = parts + (a.wl.combine_part_smem ? hpc * head_floats : 0);   // [hpc][stride]
+  const float* gbase = ws.part + ((size_t)b * g.Hq + h0) * head_floats;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();  // the next kernel may launch and wait on this one
+  const uint32_t r_bytes = (uint32_t)(jb * D * sizeof(float));
+  const uint32_t p_bytes = a.wl.combine_part_smem ? (uint32_t)(hpc * head_floats * sizeof(float)) : 0u;
+  // R_V does not depend on the previous kernel: start its copy before waiting on it
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar, r_bytes + p_bytes);
+    bulk_g2s(Rs, a.R_V + (size_t)j0 * D, r_bytes, &bar);
+  }
+  pdl_wait();
+  if (tid == 0 && p_bytes) bulk_g2s(parts, gbase, p_bytes, &bar);
+  const int n = a.seq_lens[b];
+  const int nsp = seq_len_ok(a, n) ? min(splits_for(a, n), kMaxSplits) : 0;
+  const int nslot = wc + nsp;
+  const float* P = p_bytes ? parts : gbase;
+  bool ok = true;
+  if (p_bytes) ok = mbar_wait_bounded(&bar, 0, a.status);
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) (void)mbar_wait_bounded(&bar, 0, nullptr);  // drain the copies before exiting
+    return;
+  }
+  // 1. weights and l, warp per head
+  for (int hi = warp; hi < hpc; hi += kCombThreads / 32) {
+    const float* base = P + hi * head_floats;
+    float M = -INFINITY;
+    for (int i = lane; i < nslot; i += 32) M = fmaxf(M, base[(size_t)i * (D + 4)]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int i = lane; i < nslot; i += 32) {
+      const float mi = base[(size_t)i * (D + 4)];
+      const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
+      wts[hi * stride + i] = w;
+      L = fmaf(w, base[(size_t)i * (D + 4) + 1], L);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) lsum[hi] = L;
+  }
+  __syncthreads();
+  // 2. merged accumulators
+  for (int idx = tid; idx < hpc * D; idx += kCombThreads) {
+    const int hi = idx / D, c = idx % D;
+    const float* base = P + hi * head_floats + 4 + c;
+    const float* w = wts + hi * stride;
+    float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+    int i = wc;
+    for (; i + 3 < nslot; i += 4) {
+      r0 = fmaf(w[i], base[(size_t)i * (D + 4)], r0);
+      r1 = fmaf(w[i + 1], base[(size_t)(i + 1) * (D + 4)], r1);
+      r2 = fmaf(w[i + 2], base[(size_t)(i + 2) * (D + 4)], r2);
+      r3 = fmaf(w[i + 3], base[(size_t)(i + 3) * (D + 4)], r3);
+    }
+    for (; i < nslot; ++i) r0 = fmaf(w[i], base[(size_t)i * (D + 4)], r0);
+    rot[hi * D + c] = (r0 + r1) + (r2 + r3);
+    const int cj = c - j0;
+    if (cj >= 0 && cj < jb) {
+      float p = 0.f;
+      for (int k = 0; k < wc; ++k) p = fmaf(w[k], base[(size_t)k * (D + 4)], p);
+      plain[hi * jb + cj] = p;
+    }
+  }
+  if (!p_bytes) ok = mbar_wait_bounded(&bar, 0, a.status);  // R_V rows
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) (void)mbar_wait_bounded(&bar, 0, nullptr);
+    return;
+  }
+  // 3. R_V^T: thread (jl, r); heads split over head groups, or k over slices
+  const int TJ = kCombThreads / jb;       // threads per output channel
+  const int hg = TJ < hpc ? TJ : hpc;     // head groups
+  const int KS = TJ / hg;                 // k slices per head group
+  const int NHT = hpc / hg;               // heads per thread (at most 8)
+  const int jl = tid % jb, r = tid / jb;
+  const int grp = r / KS, slice = r % KS;
+  const int m_per = (D / 4) / KS;
+  const float4* Rrow = reinterpret_cast<const float4*>(Rs + jl * D);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int mm = 0; mm < m_per; ++mm) {
+    const int k4 = slice * m_per + (mm + jl) % m_per;
+    const float4 rr = Rrow[k4];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (u < NHT) {
+        const float4 x = reinterpret_cast<const float4*>(rot + (grp + u * hg) * D)[k4];
+        acc[u] = fmaf(x.x, rr.x, fmaf(x.y, rr.y, fmaf(x.z, rr.z, fmaf(x.w, rr.w, acc[u]))));
+      }
+    }
+  }
+  if (KS > 1) {  // one head per thread: sum the k slices
+    red[tid] = acc[0];
+    __syncthreads();
+    if (slice == 0) {
+      float s = 0.f;
+      for (int sl = 0; sl < KS; ++sl) s += red[(grp * KS + sl) * jb + jl];
+      acc[0] = s;
+    }
+  }
+  if (slice == 0) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (u < NHT) {
+        const int hi = grp + u * hg;
+        const float L = lsum[hi];
+        const float o = (plain[hi * jb + jl] + acc[u]) * (L > 0.f ? 1.f / L : 0.f);
+        const size_t oi = ((size_t)b * g.Hq + h0 + hi) * D + j0 + jl;
+        if (a.out_dtype == kDtypeBF16) {
+          __nv_bfloat16 hb = __float2bfloat16_rn(o);
+          static_cast<uint16_t*>(a.out)[oi] = *reinterpret_cast<uint16_t*>(&hb);
+        } else {
+          static_cast<float*>(a.out)[oi] = o;
+        }
+      }
+    }
+  }
+}
+
+// Small batches: one CTA per (query head, request), block 128.  Rows of R_V and
+// the head's split partials are staged in shared memory by bulk copies; warp 0
+// forms the split weights, every thread one merged channel, and each warp a
+// quarter of the rows of R_V^T by shuffle reductions.  With at most one head
+// per SM this short chain beats the head-grouped kernel above, whose phases pay
+// off once many heads share a copy of R_V.
+template <int D>
+__global__ void __launch_bounds__(kThreads) decode_combine_head_kernel(DecodeArgs a) {
   constexpr int C = D / 32;
   extern __shared__ __align__(16) float csm[];
   float* Rs = csm;                 // [D][D]
@@ -882,7 +1054,7 @@ __global__ void __launch_bounds__(kThreads) decode_combine_kernel(DecodeArgs a) 
   __shared__ float s_l;
   __shared__ __align__(8) uint64_t bar;
   const Geom& g = a.g;
-  const int hpc = a.wl.combine_hpc;
+  const int hpc = 1;
   const int b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   WsView ws = ws_view(a);
@@ -1071,8 +1243,9 @@ int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl) {
 int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.g.Hq / a.wl.combine_hpc, a.batch);
-  cfg.blockDim = dim3(kThreads);
+  const bool per_head = a.wl.combine_head != 0;
+  cfg.gridDim = per_head ? dim3(a.g.Hq, a.batch) : dim3(a.g.Hq / a.wl.combine_hpc, a.batch, a.g.D / a.wl.combine_jb);
+  cfg.blockDim = dim3(per_head ? kThreads : kCombThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1080,13 +1253,13 @@ int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl) {
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cfg.dynamicSmemBytes = a.wl.combine_smem;
-  cudaError_t e;
-  if (a.g.D == 128) {
-    if ((e = ensure_smem_limit(decode_combine_kernel<128>, a.wl.combine_smem)) != cudaSuccess) return (int)e;
-    return (int)cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, a);
-  }
-  if ((e = ensure_smem_limit(decode_combine_kernel<64>, a.wl.combine_smem)) != cudaSuccess) return (int)e;
-  return (int)cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, a);
+  auto go = [&](auto kern) -> int {
+    cudaError_t e = ensure_smem_limit(kern, a.wl.combine_smem);
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaLaunchKernelEx(&cfg, kern, a);
+  };
+  if (a.g.D == 128) return per_head ? go(decode_combine_head_kernel<128>) : go(decode_combine_kernel<128>);
+  return per_head ? go(decode_combine_head_kernel<64>) : go(decode_combine_kernel<64>);
 }
 
 }  // namespace oscar

@@ -242,23 +242,37 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   const size_t slots = (size_t)w.max_splits + (size_t)w.win_chunks;
   off = align(off + (size_t)batch * g.Hq * slots * (g.D + 4) * sizeof(float));
   w.total = off;
-  // combine: R_V (D*D floats) plus, if they fit, the split partials of hpc heads
-  // in shared memory; hpc is the largest power-of-two divisor of gq that fits
+  // combine.  Small batches (a CTA per query head covers at most the SMs): one
+  // head per CTA with R_V and its partials staged in shared memory.  Otherwise
+  // enough CTAs to cover the SMs about twice, each with the fewest redundant
+  // merges: widen the output-channel block first (every CTA of a head merges all
+  // D rotated channels), then group heads so that one copy of the R_V rows
+  // serves several; the partials are staged when the CTA still fits twice on
+  // an SM.
+  const long long rows = (long long)batch * g.Hq > 0 ? (long long)batch * g.Hq : 1;
   const size_t rv_bytes = (size_t)g.D * g.D * sizeof(float);
   const size_t per_head = slots * (g.D + 4) * sizeof(float);
-  const size_t budget = 200 * 1024;
-  w.combine_hpc = 1;
-  w.combine_part_smem = 0;
-  // few (request, head) pairs: one head per CTA for parallelism; many: share R_V across the group
-  const int h_max = (long long)batch * g.Hq <= 2 * 152 ? 1 : gq;
-  for (int h = h_max; h >= 1; h >>= 1) {
-    if (rv_bytes + (size_t)h * per_head <= budget) {
-      w.combine_hpc = h;
-      w.combine_part_smem = 1;
-      break;
-    }
+  if (rows <= 152) {
+    w.combine_head = 1;
+    w.combine_hpc = 1;
+    w.combine_jb = g.D;
+    w.combine_part_smem = rv_bytes + per_head <= 200 * 1024 ? 1 : 0;
+    w.combine_smem = rv_bytes + (w.combine_part_smem ? per_head : 0) + 64;
+    return w;
   }
-  w.combine_smem = rv_bytes + (w.combine_part_smem ? (size_t)w.combine_hpc * per_head : 0) + 64;
+  int jb = 32, hpc = 1;
+  auto combine_ctas = [&]() { return rows / hpc * (g.D / jb); };
+  while (combine_ctas() > 2 * 152 && jb < g.D) jb *= 2;
+  while (combine_ctas() > 2 * 152 && hpc < 16 && g.Hq % (2 * hpc) == 0) hpc *= 2;
+  w.combine_head = 0;
+  w.combine_hpc = hpc;
+  w.combine_jb = jb;
+  const size_t base_floats = (size_t)jb * g.D + (size_t)hpc * g.D + (size_t)hpc * jb + 256 + 16;
+  const size_t wts_floats = (size_t)hpc * slots;
+  const size_t part_floats = (size_t)hpc * slots * (g.D + 4);
+  const size_t budget = 110 * 1024;
+  w.combine_part_smem = (base_floats + wts_floats + part_floats) * sizeof(float) <= budget ? 1 : 0;
+  w.combine_smem = (base_floats + wts_floats + (w.combine_part_smem ? part_floats : 0)) * sizeof(float) + 16;
   return w;
 }
 

@@ -75,7 +75,9 @@ struct DecodeWs {
   int pages_per_split;   // multiple of the 4 warps of a split CTA (each warp streams its own pages)
   int nt;                // query n-tiles (max(1, 2*gq/8))
   int win_chunks;        // BF16 window CTAs per (request, kv head): grid.x = win_chunks + max_splits
-  int combine_hpc;       // query heads per combine CTA (divides gq)
+  int combine_hpc;       // query heads per combine CTA (a power of two dividing Hq, at most 16)
+  int combine_jb;        // output channels per combine CTA (32, 64 or 128; divides D)
+  int combine_head;      // 1: one CTA per (query head, request) (small batches)
   int combine_part_smem; // 1: the combine CTA stages its split partials in shared memory
   size_t combine_smem;   // dynamic shared memory of the combine kernel
 };
