@@ -47,7 +47,7 @@ N_CTX = 32768
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=LAYERS)
@@ -90,6 +90,7 @@ class ClockSampler:
         self.proc = None
         self.path = None
         self.gpu = gpu_index
+        self.skip = 0
 
     def start(self):
         try:
@@ -97,9 +98,25 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-i", str(self.gpu), "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        t0 = time.time()   # wait until the sampler is running
+        while time.time() - t0 < 5.0 and self.proc.poll() is None and self._lines() == 0:
+            time.sleep(0.02)
+
+    def _lines(self):
+        try:
+            with open(self.path) as f:
+                return sum(1 for _ in f)
+        except OSError:
+            return 0
+
+    def mark(self):
+        """Called as the timed region starts: samples written before now are not used."""
+        if self.proc:
+            self.skip = self._lines()
 
     def stop(self):
         if not self.proc:
@@ -111,7 +128,7 @@ class ClockSampler:
             self.proc.kill()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for line in list(open(self.path))[self.skip:]:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -500,6 +517,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     clocks = ClockSampler(local)
     clocks.start()
+    clocks.mark()
     ev0.record()
     for i in range(args.steps):
         g_step.replay()

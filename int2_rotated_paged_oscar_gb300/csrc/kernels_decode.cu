@@ -324,7 +324,8 @@ struct Int2Layout {
   static constexpr int MT = D / 16;             // PV m-tiles
   static constexpr int WS = P == 64 ? 2 : 4;    // ring stages per warp (one page block each)
   static constexpr int RING = kWarps * WS * BLOCK;
-  static constexpr int SMEM = RING + kWarps * WS * (8 + 4);  // + mbarriers + page-valid flags
+  static constexpr int QOFF = (RING + kWarps * WS * (8 + 4) + 15) / 16 * 16;  // after mbarriers + page-valid flags
+  static constexpr int SMEM = QOFF + (NT == 1 ? KT * 32 * 8 : 0);  // + the NT = 1 query fragments
 };
 
 // One INT2 split: pages [pg0, pg1) of one (request, kv head).  Warp w owns pages
@@ -335,14 +336,15 @@ struct Int2Layout {
 // Operands (mma.sync m16n8k16, f32 accumulate).  Let k_K, k_V be the layer's
 // operand exponents (scales and zeros times 2^k stay below 2^14 in f16), e_h the
 // per-head query exponent written by q_rotate, and j = 6 the softmax-weight shift.
-//   QK  A = K codes times their group scale: S * c * 2^(pos-10) in f16 with
-//       S = f16(s * 2^k_K), formed exactly by one HFMA2 per register from the
-//       code pattern -(1 + c * 2^(pos-10)) and -S;
-//       B = q' * 2^(e_h) * 2^(10-pos) split into f16 hi/lo.  One accumulator holds
-//       every group, so no per-group epilogue is needed.  The zero term
-//       sum_g z_g Q_g is one more MMA: A = the raw BF16 (scale, zero) word of
-//       group tig in columns (2tig, 2tig+1), B = (0, Q_tig * 2^(e_h + k_K)) in
-//       BF16 hi/lo, the scale meeting a zero row.
+//   QK  A = K codes as f16 subnormals c * 2^(pos-24), one LOP3 per register
+//       (exact, no offset term); B = q' * 2^(e_h) * 2^(10-pos) split into f16
+//       hi/lo, so each product is c * q' * 2^(e_h - 14) exactly.  One accumulator
+//       per 32-channel group; after its MMAs it is multiplied by the group's
+//       scale s * 2^(k_K + 14) (float32 from the BF16 bits) and summed.  The zero
+//       term sum_g z_g Q_g is one more MMA: A = the raw BF16 (scale, zero) word of
+//       group tig in columns (2tig, 2tig+1), repeated in the upper k-half,
+//       B = (0, Q_tig * 2^(e_h + k_K)) as three BF16 terms, the scale meeting a
+//       zero row.
 //   PV  A = V codes times their token's group scale (as for K, per token pair);
 //       B = p * 2^j split into f16 hi/lo; the zero term sum_t p_t z_{t,g} is one
 //       MMA with A rows = groups holding f16(z * 2^k_V).
@@ -430,16 +432,31 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
   // ---------------- query side (written by q_rotate): wait for the previous grid
   pdl_wait();
   WsView ws = ws_view(a);
-  uint32_t qb[NT][Lay::KT][2];
+  // The query-side B fragments are the same for every warp of the CTA.  With up to
+  // four query heads (NT = 1) they are staged once in shared memory (one LDS.64 per
+  // MMA): the registers they free buy the 128-register kernel scheduling room.  With
+  // eight heads (NT = 2) the kernel runs at three CTAs per SM with registers to
+  // spare, and register operands avoid the extra loads.
+  uint2* qsm = reinterpret_cast<uint2*>(smem + Lay::QOFF);   // [NT][KT][32 lanes]
+  uint32_t qb[G8 ? NT : 1][G8 ? Lay::KT : 1][2];
+  if constexpr (G8) {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const bool col_ok = G8 || (gid >> 1) < gq;
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int kk = 0; kk < Lay::KT; ++kk) {
-      const uint2 f = ws.qfrag[((((size_t)b * g.Hkv + kvh) * NT + nt) * Lay::KT + kk) * 32 + lane];
-      qb[nt][kk][0] = col_ok ? f.x : 0u;
-      qb[nt][kk][1] = col_ok ? f.y : 0u;
+      for (int kk = 0; kk < Lay::KT; ++kk) {
+        const uint2 f = ws.qfrag[((((size_t)b * g.Hkv + kvh) * NT + nt) * Lay::KT + kk) * 32 + lane];
+        qb[nt][kk][0] = f.x;
+        qb[nt][kk][1] = f.y;
+      }
+  } else {
+    for (int i = tid; i < NT * Lay::KT * 32; i += kThreads) {
+      const int nt = i / (Lay::KT * 32), rem = i % (Lay::KT * 32);
+      const int kk = rem >> 5, ln = rem & 31;
+      const bool col_ok = ((ln >> 2) >> 1) < gq;
+      const uint2 f = ws.qfrag[((((size_t)b * g.Hkv + kvh) * NT + nt) * Lay::KT + kk) * 32 + ln];
+      qsm[i] = col_ok ? f : make_uint2(0u, 0u);
     }
+    __syncthreads();
   }
   const float* aux_base = ws.qaux + ((size_t)b * g.Hq + (size_t)kvh * gq) * 8;
   const float sm_log2 = kLog2e * rsqrtf((float)D);
@@ -502,13 +519,23 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
   const int zv = gid & (GROUPS - 1);     // PV zero-term group row of this lane
   const int src0 = (2 * tig) * 4 + (gid >> 1), src1 = src0 + 4;
   const uint32_t psel = (gid & 1) ? 0x7632u : 0x5410u;
+  // this lane's byte offsets inside a 16-token block of a stage buffer, relative to
+  // the block's code rows (pc) or (scale, zero) rows (ps): K row ra (row rb is 4 rows
+  // on), V token tig (tokens tig + 8, tig + 4, tig + 12 are 8, 4, 12 rows on)
+  const int oK = ra * Lay::ROW + (D == 128 ? tig * 8 : tig * 4);
+  const int oKs = Lay::KSZ + ra * Lay::SZ;
+  const int oKz = oKs + 4 * zq;
+  const int oV = Lay::VC + tig * Lay::ROW + (D == 128 ? gid * 4 : (gid >> 1) * 4);
+  const int oVs = Lay::VSZ + tig * Lay::SZ;
+  const int oVz = oVs + 4 * zv;
 
   // One 16-token block at slot0 of the stage buffer; FULL: every token is a
   // history token (no masking).
   auto process = [&](auto full_tag, const uint8_t* buf, int slot0, int tb) {
     constexpr bool FULL = decltype(full_tag)::value;
     // ---------------- QK
-    const int sA = slot0 + ra, sB = slot0 + rb;
+    const uint8_t* pc = buf + slot0 * Lay::ROW;
+    const uint8_t* ps = buf + slot0 * Lay::SZ;
     bool va = true, vb = true;
     if constexpr (!FULL) {
       va = tb + ra >= g.S && tb + ra < h_end;
@@ -517,23 +544,23 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     uint32_t kwA[D / 64], kwB[D / 64];
     uint32_t szA[GROUPS], szB[GROUPS];
     if constexpr (D == 128) {
-      const uint2 x = *reinterpret_cast<const uint2*>(buf + sA * Lay::ROW + tig * 8);
-      const uint2 y = *reinterpret_cast<const uint2*>(buf + sB * Lay::ROW + tig * 8);
+      const uint2 x = *reinterpret_cast<const uint2*>(pc + oK);
+      const uint2 y = *reinterpret_cast<const uint2*>(pc + oK + 4 * Lay::ROW);
       kwA[0] = x.x; kwA[1] = x.y; kwB[0] = y.x; kwB[1] = y.y;
-      const uint4 A4 = *reinterpret_cast<const uint4*>(buf + Lay::KSZ + sA * Lay::SZ);
-      const uint4 B4 = *reinterpret_cast<const uint4*>(buf + Lay::KSZ + sB * Lay::SZ);
+      const uint4 A4 = *reinterpret_cast<const uint4*>(ps + oKs);
+      const uint4 B4 = *reinterpret_cast<const uint4*>(ps + oKs + 4 * Lay::SZ);
       szA[0] = A4.x; szA[1] = A4.y; szA[2] = A4.z; szA[3] = A4.w;
       szB[0] = B4.x; szB[1] = B4.y; szB[2] = B4.z; szB[3] = B4.w;
     } else {
-      kwA[0] = *reinterpret_cast<const uint32_t*>(buf + sA * Lay::ROW + tig * 4);
-      kwB[0] = *reinterpret_cast<const uint32_t*>(buf + sB * Lay::ROW + tig * 4);
-      const uint2 A2 = *reinterpret_cast<const uint2*>(buf + Lay::KSZ + sA * Lay::SZ);
-      const uint2 B2 = *reinterpret_cast<const uint2*>(buf + Lay::KSZ + sB * Lay::SZ);
+      kwA[0] = *reinterpret_cast<const uint32_t*>(pc + oK);
+      kwB[0] = *reinterpret_cast<const uint32_t*>(pc + oK + 4 * Lay::ROW);
+      const uint2 A2 = *reinterpret_cast<const uint2*>(ps + oKs);
+      const uint2 B2 = *reinterpret_cast<const uint2*>(ps + oKs + 4 * Lay::SZ);
       szA[0] = A2.x; szA[1] = A2.y;
       szB[0] = B2.x; szB[1] = B2.y;
     }
-    uint32_t zA = *reinterpret_cast<const uint32_t*>(buf + Lay::KSZ + sA * Lay::SZ + 4 * zq);
-    uint32_t zB = *reinterpret_cast<const uint32_t*>(buf + Lay::KSZ + sB * Lay::SZ + 4 * zq);
+    uint32_t zA = *reinterpret_cast<const uint32_t*>(ps + oKz);
+    uint32_t zB = *reinterpret_cast<const uint32_t*>(ps + oKz + 4 * Lay::SZ);
     // group scales s * 2^(k_K + 14), applied to each group's accumulator after its MMAs
     float SA[GROUPS], SB[GROUPS];
 #pragma unroll
@@ -569,7 +596,12 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
           const int x = 4 * hg + 2 * kt;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
+          if constexpr (G8) {
             mma_f16(c[gi], ua[x], ub[x], ua[x + 1], ub[x + 1], qb[nt][2 * gi + kt][0], qb[nt][2 * gi + kt][1]);
+          } else {
+            const uint2 qf = qsm[(nt * Lay::KT + 2 * gi + kt) * 32 + lane];
+            mma_f16(c[gi], ua[x], ub[x], ua[x + 1], ub[x + 1], qf.x, qf.y);
+          }
         }
       }
     }
@@ -666,7 +698,6 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
       bw[0][1] = prmt(__shfl_sync(0xffffffffu, hlb, src0), __shfl_sync(0xffffffffu, hlb, src1), psel);
     }
     // ---------------- PV
-    const int r0 = slot0 + tig, r1 = r0 + 8, r2 = r0 + 4, r3 = r0 + 12;
     bool v0 = true, v1 = true, v2 = true, v3 = true;
     if constexpr (!FULL) {
       v0 = tb + tig >= g.S && tb + tig < h_end;
@@ -674,22 +705,19 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
       v2 = tb + tig + 4 >= g.S && tb + tig + 4 < h_end;
       v3 = tb + tig + 12 >= g.S && tb + tig + 12 < h_end;
     }
-    const uint8_t* vc = buf + Lay::VC;
-    const uint8_t* vs = buf + Lay::VSZ;
     uint32_t xw[D / 64], yw[D / 64];  // code words: tokens (r0 | r1) and (r2 | r3) per half-word
     if constexpr (D == 128) {
-      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vc + r0 * Lay::ROW + gid * 4);
-      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vc + r1 * Lay::ROW + gid * 4);
-      const uint32_t w2 = *reinterpret_cast<const uint32_t*>(vc + r2 * Lay::ROW + gid * 4);
-      const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vc + r3 * Lay::ROW + gid * 4);
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(pc + oV);
+      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(pc + oV + 8 * Lay::ROW);
+      const uint32_t w2 = *reinterpret_cast<const uint32_t*>(pc + oV + 4 * Lay::ROW);
+      const uint32_t w3 = *reinterpret_cast<const uint32_t*>(pc + oV + 12 * Lay::ROW);
       xw[0] = prmt(w0, w1, 0x5410); xw[1] = prmt(w0, w1, 0x7632);
       yw[0] = prmt(w2, w3, 0x5410); yw[1] = prmt(w2, w3, 0x7632);
     } else {
-      const int wo = (gid >> 1) * 4;
-      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vc + r0 * Lay::ROW + wo);
-      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vc + r1 * Lay::ROW + wo);
-      const uint32_t w2 = *reinterpret_cast<const uint32_t*>(vc + r2 * Lay::ROW + wo);
-      const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vc + r3 * Lay::ROW + wo);
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(pc + oV);
+      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(pc + oV + 8 * Lay::ROW);
+      const uint32_t w2 = *reinterpret_cast<const uint32_t*>(pc + oV + 4 * Lay::ROW);
+      const uint32_t w3 = *reinterpret_cast<const uint32_t*>(pc + oV + 12 * Lay::ROW);
       xw[0] = prmt(w0, w1, psel);
       yw[0] = prmt(w2, w3, psel);
     }
@@ -697,19 +725,19 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     {
       uint32_t s0[GROUPS], s1[GROUPS], s2[GROUPS], s3[GROUPS];
       if constexpr (D == 128) {
-        const uint4 q0 = *reinterpret_cast<const uint4*>(vs + r0 * Lay::SZ);
-        const uint4 q1 = *reinterpret_cast<const uint4*>(vs + r1 * Lay::SZ);
-        const uint4 q2 = *reinterpret_cast<const uint4*>(vs + r2 * Lay::SZ);
-        const uint4 q3 = *reinterpret_cast<const uint4*>(vs + r3 * Lay::SZ);
+        const uint4 q0 = *reinterpret_cast<const uint4*>(ps + oVs);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(ps + oVs + 8 * Lay::SZ);
+        const uint4 q2 = *reinterpret_cast<const uint4*>(ps + oVs + 4 * Lay::SZ);
+        const uint4 q3 = *reinterpret_cast<const uint4*>(ps + oVs + 12 * Lay::SZ);
         s0[0] = q0.x; s0[1] = q0.y; s0[2] = q0.z; s0[3] = q0.w;
         s1[0] = q1.x; s1[1] = q1.y; s1[2] = q1.z; s1[3] = q1.w;
         s2[0] = q2.x; s2[1] = q2.y; s2[2] = q2.z; s2[3] = q2.w;
         s3[0] = q3.x; s3[1] = q3.y; s3[2] = q3.z; s3[3] = q3.w;
       } else {
-        const uint2 q0 = *reinterpret_cast<const uint2*>(vs + r0 * Lay::SZ);
-        const uint2 q1 = *reinterpret_cast<const uint2*>(vs + r1 * Lay::SZ);
-        const uint2 q2 = *reinterpret_cast<const uint2*>(vs + r2 * Lay::SZ);
-        const uint2 q3 = *reinterpret_cast<const uint2*>(vs + r3 * Lay::SZ);
+        const uint2 q0 = *reinterpret_cast<const uint2*>(ps + oVs);
+        const uint2 q1 = *reinterpret_cast<const uint2*>(ps + oVs + 8 * Lay::SZ);
+        const uint2 q2 = *reinterpret_cast<const uint2*>(ps + oVs + 4 * Lay::SZ);
+        const uint2 q3 = *reinterpret_cast<const uint2*>(ps + oVs + 12 * Lay::SZ);
         s0[0] = q0.x; s0[1] = q0.y; s1[0] = q1.x; s1[1] = q1.y;
         s2[0] = q2.x; s2[1] = q2.y; s3[0] = q3.x; s3[1] = q3.y;
       }
@@ -746,10 +774,10 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
         mma_f16(acc[mt], ux[2 * mt], ux[2 * mt + 1], uy[2 * mt], uy[2 * mt + 1], bw[nt][0], bw[nt][1]);
     // zero term: rows = groups (row gid holds group zv), k = the lane's four tokens
     {
-      float z0 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(vs + r0 * Lay::SZ + 4 * zv), v23);
-      float z1 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(vs + r1 * Lay::SZ + 4 * zv), v23);
-      float z2 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(vs + r2 * Lay::SZ + 4 * zv), v23);
-      float z3 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(vs + r3 * Lay::SZ + 4 * zv), v23);
+      float z0 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(ps + oVz), v23);
+      float z1 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(ps + oVz + 8 * Lay::SZ), v23);
+      float z2 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(ps + oVz + 4 * Lay::SZ), v23);
+      float z3 = zero_times_pow2(*reinterpret_cast<const uint32_t*>(ps + oVz + 12 * Lay::SZ), v23);
       if constexpr (!FULL) {
         z0 = v0 ? z0 : 0.f;
         z1 = v1 ? z1 : 0.f;
@@ -775,13 +803,15 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     if (stage_ok[s]) {
       const uint8_t* buf = ring + s * Lay::BLOCK;
       const int tp = (pg0 + warp + kWarps * i) * P;  // first token of the page
+      if (tp >= g.S && tp + P <= h_end) {  // every token of the page is history: no checks
 #pragma unroll 1
-      for (int blk = 0; blk < P / 16; ++blk) {
-        const int tb = tp + 16 * blk;
-        if (tb >= g.S && tb + 16 <= h_end)
-          process(std::integral_constant<bool, true>{}, buf, 16 * blk, tb);
-        else if (tb + 16 > g.S && tb < h_end)
-          process(std::integral_constant<bool, false>{}, buf, 16 * blk, tb);
+        for (int blk = 0; blk < P / 16; ++blk) process(std::integral_constant<bool, true>{}, buf, 16 * blk, tp + 16 * blk);
+      } else {
+#pragma unroll 1
+        for (int blk = 0; blk < P / 16; ++blk) {
+          const int tb = tp + 16 * blk;
+          if (tb + 16 > g.S && tb < h_end) process(std::integral_constant<bool, false>{}, buf, 16 * blk, tb);
+        }
       }
     }
     __syncwarp();
@@ -833,8 +863,10 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
         // channel 16mt + gid (+ 8) sits in slot (2mt) mod 8 (+ 1) of its half-word:
         // code scale 2^(slot_pos - 10)
         const float za = zg[j][mt >> 1] * vscale;
-        wacc[(warp * 8 + hh) * D + ch_a] = fmaf(va_, ldexpf(vscale, 10 - slot_pos((2 * mt) & 7)), za);
-        wacc[(warp * 8 + hh) * D + ch_b] = fmaf(vb_, ldexpf(vscale, 10 - slot_pos((2 * mt + 1) & 7)), za);
+        const float pa_ = static_cast<float>(1 << (10 - slot_pos((2 * mt) & 7)));   // folded after unrolling
+        const float pb_ = static_cast<float>(1 << (10 - slot_pos((2 * mt + 1) & 7)));
+        wacc[(warp * 8 + hh) * D + ch_a] = fmaf(va_, vscale * pa_, za);
+        wacc[(warp * 8 + hh) * D + ch_b] = fmaf(vb_, vscale * pb_, za);
       }
     }
   }
