@@ -992,26 +992,28 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(DecodeArgs
     if (lane == 0) lsum[hi] = L;
   }
   __syncthreads();
-  // 2. merged accumulators
-  for (int idx = tid; idx < hpc * D; idx += kCombThreads) {
-    const int hi = idx / D, c = idx % D;
-    const float* base = P + hi * head_floats + 4 + c;
+  // 2. merged accumulators: warp per head, lane per four channels; each slot is one
+  //    float4 per lane and eight slots' loads are in flight at a time
+  for (int hi = warp; hi < hpc; hi += kCombThreads / 32) {
+    const float* base = P + hi * head_floats + 4;   // slot i, channel c: base[i * (D + 4) + c]
     const float* w = wts + hi * stride;
-    float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-    int i = wc;
-    for (; i + 3 < nslot; i += 4) {
-      r0 = fmaf(w[i], base[(size_t)i * (D + 4)], r0);
-      r1 = fmaf(w[i + 1], base[(size_t)(i + 1) * (D + 4)], r1);
-      r2 = fmaf(w[i + 2], base[(size_t)(i + 2) * (D + 4)], r2);
-      r3 = fmaf(w[i + 3], base[(size_t)(i + 3) * (D + 4)], r3);
-    }
-    for (; i < nslot; ++i) r0 = fmaf(w[i], base[(size_t)i * (D + 4)], r0);
-    rot[hi * D + c] = (r0 + r1) + (r2 + r3);
-    const int cj = c - j0;
-    if (cj >= 0 && cj < jb) {
-      float p = 0.f;
-      for (int k = 0; k < wc; ++k) p = fmaf(w[k], base[(size_t)k * (D + 4)], p);
-      plain[hi * jb + cj] = p;
+    for (int c4 = lane; c4 < D / 4; c4 += 32) {
+      const int c = 4 * c4;
+      float4 pl = make_float4(0.f, 0.f, 0.f, 0.f), r = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < wc; ++i) {
+        const float4 v = *reinterpret_cast<const float4*>(base + (size_t)i * (D + 4) + c);
+        const float wi = w[i];
+        pl.x = fmaf(wi, v.x, pl.x); pl.y = fmaf(wi, v.y, pl.y); pl.z = fmaf(wi, v.z, pl.z); pl.w = fmaf(wi, v.w, pl.w);
+      }
+#pragma unroll 8
+      for (int i = wc; i < nslot; ++i) {
+        const float4 v = *reinterpret_cast<const float4*>(base + (size_t)i * (D + 4) + c);
+        const float wi = w[i];
+        r.x = fmaf(wi, v.x, r.x); r.y = fmaf(wi, v.y, r.y); r.z = fmaf(wi, v.z, r.z); r.w = fmaf(wi, v.w, r.w);
+      }
+      *reinterpret_cast<float4*>(rot + hi * D + c) = r;
+      const int cj = c - j0;
+      if (cj >= 0 && cj < jb) *reinterpret_cast<float4*>(plain + hi * jb + cj) = pl;
     }
   }
   if (!p_bytes) ok = mbar_wait_bounded(&bar, 0, a.status);  // R_V rows
