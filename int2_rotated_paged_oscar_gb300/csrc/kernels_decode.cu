@@ -907,7 +907,7 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
 }
 
 template <int D, int NT, int P>
-__global__ void __launch_bounds__(kThreads, NT == 2 ? 3 : 4) decode_splitk_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) decode_splitk_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   (void)splitk_work<D, NT, P>(a, smem);
 }

@@ -192,7 +192,7 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   long long max_pages;
   if (bf16_pool) max_pages = max_seq > 0 ? (max_seq - 1) / g.P + 1 : 0;
   else max_pages = (max_seq - g.W > g.S) ? (long long)(max_seq - g.W - 1) / g.P + 1 : 0;
-  const int occ = bf16_pool ? 2 : (w.nt == 2 ? 3 : 4);  // resident CTAs per SM at the kernels' register use
+  const int occ = bf16_pool ? 2 : 3;  // resident CTAs per SM at the kernels' register use
   const long long wave = 152LL * occ;  // resident CTAs of one wave at the kernel's register use
   const long long pairs = (long long)batch * g.Hkv > 0 ? (long long)batch * g.Hkv : 1;
   const long long win_ctas = bf16_pool ? 0 : (long long)batch * g.Hkv * ((g.S + g.W + 15) / 16);
