@@ -229,11 +229,11 @@ oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
  * seq_lens on the same stream (identical cache contents and outputs), with the
  * same arguments as those two calls (K_new, V_new: [batch][n_kv_heads][d] in
  * kv_dtype; seq_lens [batch] device int32 counts the new token).  The query
- * rotation runs while the append quantises the evicted token: the append is
- * launched as a programmatic dependent of the rotation and the split-K kernel
- * as a dependent of the append, which reads only the page the append may be
- * writing after the dependency resolves.  The caller maps the page of the
- * evicted token beforehand, as for oscar_append_step. */
+ * rotation and the append run as one grid ("step_prep": rotation CTAs first,
+ * then append CTAs), launched as a programmatic dependent of the preceding
+ * kernel; the split-K kernel is its dependent and reads only the page the
+ * append may be writing after the dependency resolves.  The caller maps the
+ * page of the evicted token beforehand, as for oscar_append_step. */
 oscar_status oscar_decode_step(oscar_ctx* ctx, int32_t layer, const void* K_new, const void* V_new, int32_t kv_dtype,
                                const void* q, int32_t q_dtype, void* out, int32_t out_dtype,
                                const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
@@ -289,7 +289,7 @@ oscar_status oscar_check_status(oscar_ctx* ctx, void* stream, int32_t* out_bits)
  * of the named kernel family with CUDA events on the launch stream.
  * oscar_kernel_time returns the summed milliseconds and launch count since the
  * last reset (synchronises the recorded events).  Names: "decode_splitk",
- * "decode_combine", "q_rotate", "append", "evict", "write", "bf16_prepare",
+ * "decode_combine", "q_rotate", "step_prep", "append", "evict", "write", "bf16_prepare",
  * "bf16_decode", "bf16_combine".  Launches
  * recorded into a CUDA graph get external event-record nodes: replay the graph
  * once, then read; the events return to the library when read, so a graph

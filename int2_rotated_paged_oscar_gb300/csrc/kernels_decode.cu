@@ -56,30 +56,7 @@ constexpr int kMaxWinChunks = 32;
 constexpr float kRescaleLog2 = 8.f;   // the softmax reference moves when a score exceeds it by more
 constexpr float kWeightShift = 6.f;   // weights are 2^(s - mm) with mm = reference - kWeightShift
 
-// ------------------------------------------------------------------ workspace views
-struct WsView {
-  uint2* qfrag;   // [B][Hkv][NT][D/16][32]
-  float* qaux;    // [B][Hq][8]: [0] = 2^-e_h, [1 + g] = Q_g
-  float* qplain;  // [B][Hq][D]
-  float* part;    // [B][Hq][win_chunks + max_splits][D + 4]: [0] m (log2 domain), [1] l, [4..] acc
-};
-
-__device__ __forceinline__ WsView ws_view(const DecodeArgs& a) {
-  WsView v;
-  v.qfrag = reinterpret_cast<uint2*>(a.ws + a.wl.qfrag_off);
-  v.qaux = reinterpret_cast<float*>(a.ws + a.wl.qaux_off);
-  v.qplain = reinterpret_cast<float*>(a.ws + a.wl.qplain_off);
-  v.part = reinterpret_cast<float*>(a.ws + a.wl.part_off);
-  return v;
-}
-
-__device__ __forceinline__ float load_q(const DecodeArgs& a, size_t idx) {
-  if (a.q_dtype == kDtypeBF16) {
-    const uint16_t v = static_cast<const uint16_t*>(a.q)[idx];
-    return __uint_as_float(static_cast<uint32_t>(v) << 16);
-  }
-  return static_cast<const float*>(a.q)[idx];
-}
+#include "q_rotate.cuh"
 
 // Number of INT2 splits request b needs (0 if it has no history).
 __device__ __forceinline__ int splits_for(const DecodeArgs& a, int n) {
@@ -94,112 +71,14 @@ __device__ __forceinline__ bool seq_len_ok(const DecodeArgs& a, int n) {
 }
 
 // ------------------------------------------------------------------ q rotate
-// grid (Hkv * D/32, B), block 128.  CTA (kvh, grp) computes the 32 rotated
-// channels of group grp, q'_j = sum_i q_i R_K[i][j] for j in [32 grp, 32 grp + 32),
-// for every query head of kv head kvh, and writes the group sum Q_g and the
-// query-side MMA fragments of its two k-tiles.  The power-of-two scale of head
-// h is set from ||q_h||_2, which bounds |q'_h|_inf (R_K is orthogonal), so the
-// CTAs of a head need not agree on a maximum.
-//
-// Launched as a programmatic dependent of whatever preceded it on the stream:
-// it issues the loads of its R_K slice (a per-layer constant), then waits for
-// that grid (q and the cache may come from it) and only then lets its own
-// dependents launch, so every kernel after it still sees all earlier work
-// complete; the launch and the R_K loads overlap the predecessor's tail.
+// grid (Hkv * D/32, B), block 128: CTA (kvh, grp) of request b runs q_rotate_cta
+// (q_rotate.cuh).  Launched as a programmatic dependent of whatever preceded it
+// on the stream; it lets its own dependents launch after its wait on that grid,
+// so every kernel after it still sees all earlier work complete.
 template <int D>
 __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
-  __shared__ __align__(16) float Rs[D][33];   // R_K[:, 32 grp + c], padded
-  __shared__ float qs[8][D];
-  __shared__ float qr[8][32];
-  __shared__ float nrm[8];
-  const Geom& g = a.g;
-  const int grp = blockIdx.x % (D / 32), kvh = blockIdx.x / (D / 32), b = blockIdx.y;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int gq = g.gq();
-  WsView ws = ws_view(a);
-  // R_K column slice: D rows x 32 floats (8 float4 per row), 16-byte loads, all in
-  // flight.  R_K is a per-layer constant that the preceding kernel does not write,
-  // so the loads are issued before the wait on that kernel.
-  {
-    const float4* Rg = reinterpret_cast<const float4*>(a.R_K);
-    float4 v[D * 8 / kThreads];
-#pragma unroll
-    for (int u = 0; u < D * 8 / kThreads; ++u) {
-      const int idx = t + u * kThreads;  // row idx / 8, float4 idx % 8
-      v[u] = __ldg(Rg + (size_t)(idx >> 3) * (D / 4) + grp * 8 + (idx & 7));
-    }
-    pdl_wait();
-    pdl_launch_dependents();
-#pragma unroll
-    for (int u = 0; u < D * 8 / kThreads; ++u) {
-      const int idx = t + u * kThreads;
-      float* dst = &Rs[idx >> 3][(idx & 7) * 4];
-      dst[0] = v[u].x; dst[1] = v[u].y; dst[2] = v[u].z; dst[3] = v[u].w;
-    }
-  }
-  const size_t qbase = ((size_t)b * g.Hq + (size_t)kvh * gq) * D;
-  for (int i = t; i < gq * D; i += kThreads) {
-    const float x = load_q(a, qbase + i);
-    qs[i / D][i % D] = x;
-    if (grp == 0) ws.qplain[qbase + i] = x;
-  }
-  __syncthreads();
-  // squared norms: warp w sums heads w, w + 4
-  for (int hh = warp; hh < gq; hh += kThreads / 32) {
-    float ss = 0.f;
-    for (int i = lane; i < D; i += 32) ss = fmaf(qs[hh][i], qs[hh][i], ss);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) nrm[hh] = sqrtf(ss);
-  }
-  // rotation: lane = channel 32 grp + lane, warp w handles heads w, w + 4
-  for (int hh = warp; hh < gq; hh += kThreads / 32) {
-    float acc = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < D; ++i) acc = fmaf(qs[hh][i], Rs[i][lane], acc);
-    qr[hh][lane] = acc;
-    float gs = acc;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-    if (lane == 0) ws.qaux[((size_t)b * g.Hq + (size_t)kvh * gq + hh) * 8 + 1 + grp] = gs;
-  }
-  __syncthreads();
-  // fragments of the two k-tiles of this group: 8 lanes x 2 k-tiles per head
-  for (int idx = t; idx < gq * 16; idx += kThreads) {
-    const int hh = idx >> 4, sub = idx & 15;
-    const int kt = sub >> 3, hl = (sub >> 2) & 1, tig = sub & 3;
-    int e = 0;
-    const float mx = nrm[hh];
-    if (mx > 0.f) {
-      int E;
-      frexpf(mx, &E);  // |q'|_inf <= ||q||_2 = mx * (1 + rounding) < 2^E
-      e = 5 - E;       // |q'| * 2^e < 32: times 2^(10-pos) <= 1024 stays below the f16 maximum
-    }
-    if (grp == 0 && sub == 0) ws.qaux[((size_t)b * g.Hq + (size_t)kvh * gq + hh) * 8] = ldexpf(1.f, -e);
-    const bool g8 = gq == 8;
-    const int gid = g8 ? hh : 2 * (hh & 3) + hl;
-    const int plane = g8 ? hl : 0;
-    const int ln = gid * 4 + tig;
-    const int kk = 2 * grp + kt;
-    const int p8 = 4 * grp + 2 * kt;
-    uint32_t regs[2];
-#pragma unroll
-    for (int hpair = 0; hpair < 2; ++hpair) {
-      const int ch = 16 * kt + 8 * hpair + 2 * tig;  // channel within the group
-      const int pos = slot_pos((p8 + hpair) & 7);
-      float v[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const float x = ldexpf(qr[hh][ch + u], e + 10 - pos);
-        const __half hi = __float2half_rn(x);
-        const float lo = x - __half2float(hi);
-        v[u] = hl ? lo : __half2float(hi);
-      }
-      regs[hpair] = pack_half2(v[0], v[1]);
-    }
-    const size_t fidx = ((((size_t)b * g.Hkv + kvh) * a.wl.nt + plane) * (D / 16) + kk) * 32 + ln;
-    ws.qfrag[fidx] = make_uint2(regs[0], regs[1]);
-  }
+  __shared__ __align__(16) float sm[kQRotSmemFloats<D>()];
+  q_rotate_cta<D>(a, blockIdx.x % (D / 32), blockIdx.x / (D / 32), blockIdx.y, sm);
 }
 
 // ------------------------------------------------------------------ window chunks (BF16, float32 math)

@@ -18,6 +18,7 @@
 // the dense product by a fast Walsh-Hadamard transform followed by the
 // bit-reversal gather.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,6 +27,8 @@
 
 namespace oscar {
 namespace {
+
+#include "q_rotate.cuh"
 
 constexpr int kWarpsPerCta = 8;
 
@@ -422,8 +425,12 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) evict_kernel(WriteArgs a) {
 constexpr int kAppendHeads = 2;
 
 // Returns false if the rotation copy timed out (flagged; nothing written).
+// (b, by, bz): request, K|V, head group.  early_r: the fused step's form, which
+// fetches R (a per-layer constant) first and then waits on the preceding grid
+// before it reads anything that grid may write.
 template <int D>
-__device__ __forceinline__ bool append_body(const WriteArgs& a, float* Rsm, uint64_t* bar) {
+__device__ __forceinline__ bool append_body(const WriteArgs& a, float* Rsm, uint64_t* bar, int b, int by, int bz,
+                                            bool early_r) {
   constexpr int C = D / 32;
   constexpr int HPC = kAppendHeads;
   __shared__ float xs[HPC][D];
@@ -433,18 +440,32 @@ __device__ __forceinline__ bool append_body(const WriteArgs& a, float* Rsm, uint
   __shared__ int page_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geom& g = a.g;
-  const int b = blockIdx.x;
-  const bool is_v = blockIdx.y == 1;
-  const int h0 = blockIdx.z * HPC;
+  const bool is_v = by == 1;
+  const int h0 = bz * HPC;
   const int nh = min(HPC, g.Hkv - h0);
+  if (early_r) {
+    if (threadIdx.x == 0) {
+      mbar_init(bar, 1);
+      fence_barrier_init();
+      mbar_arrive_expect_tx(bar, D * D * sizeof(float));
+      bulk_g2s(Rsm, is_v ? a.R_V : a.R_K, D * D * sizeof(float), bar);
+    }
+    pdl_wait();
+  }
+  // an exit that leaves the early rotation copy unused waits for it first
+  auto drain = [&]() {
+    if (early_r && threadIdx.x == 0) (void)mbar_wait_bounded(bar, 0, nullptr);
+  };
   const int n0 = a.start_pos[b] + a.start_offset;
   if (n0 < 0 || n0 + 1 > g.max_pages_per_req * g.P) {
     if (threadIdx.x == 0) flag_error(a.status, kDevBadLen);
+    drain();
     return true;
   }
   const int req = a.req_slot[b];
   if (req < 0 || req >= g.max_req) {
     if (threadIdx.x == 0) flag_error(a.status, kDevBadSlot);
+    drain();
     return true;
   }
   const int slot_new = window_slot(n0, g.S, g.W);
@@ -452,7 +473,7 @@ __device__ __forceinline__ bool append_body(const WriteArgs& a, float* Rsm, uint
   const bool evict = e >= g.S;  // the evicted token occupies the slot the new token takes
   // every global read of this kernel happens before the dependent kernel is let
   // in: its page stream would otherwise queue ahead of them
-  if (evict && threadIdx.x == 0) {
+  if (!early_r && evict && threadIdx.x == 0) {
     mbar_init(bar, 1);
     fence_barrier_init();
     mbar_arrive_expect_tx(bar, D * D * sizeof(float));
@@ -499,6 +520,7 @@ __device__ __forceinline__ bool append_body(const WriteArgs& a, float* Rsm, uint
     (void)mbar_wait_bounded(bar, 0, nullptr);
     return false;  // uniform: every thread times out on the same copy
   }
+  if (!evict) drain();
   if (evict) {
     float acc[HPC][C];
 #pragma unroll
@@ -554,9 +576,31 @@ template <int D>
 __global__ void __launch_bounds__(128) append_kernel(WriteArgs a) {
   extern __shared__ __align__(16) float Rsm[];  // [D][D]
   __shared__ __align__(8) uint64_t bar;
-  (void)append_body<D>(a, Rsm, &bar);
+  (void)append_body<D>(a, Rsm, &bar, blockIdx.x, blockIdx.y, blockIdx.z, false);
   pdl_launch_dependents();  // no-op if already done; covers the early exits
   pdl_wait();
+}
+
+// The first kernel of a fused decode step: CTAs [0, nq) rotate the query
+// (q_rotate_cta, nq = Hkv * D/32 * batch), the rest run the append, one grid
+// instead of two so that no second launch sits on the step's critical path.
+// Every CTA waits on the preceding grid before it reads anything that grid may
+// write; the split-K kernel, its programmatic dependent, waits for the whole grid.
+template <int D>
+__global__ void __launch_bounds__(128) step_prep_kernel(const __grid_constant__ WriteArgs w,
+                                                        const __grid_constant__ DecodeArgs d) {
+  extern __shared__ __align__(16) float Rsm[];  // [D][D] (append) or the rotation's arrays
+  __shared__ __align__(8) uint64_t bar;
+  const int qx = d.g.Hkv * (D / 32);
+  const int nq = qx * d.batch;
+  if ((int)blockIdx.x < nq) {
+    q_rotate_cta<D>(d, blockIdx.x % (D / 32), (blockIdx.x % qx) / (D / 32), blockIdx.x / qx, Rsm);
+    return;
+  }
+  const int i = blockIdx.x - nq;
+  const int nz = (w.g.Hkv + kAppendHeads - 1) / kAppendHeads;
+  (void)append_body<D>(w, Rsm, &bar, i / (2 * nz), (i % (2 * nz)) / nz, (i % (2 * nz)) % nz, true);
+  pdl_launch_dependents();  // covers the early exits
 }
 
 }  // namespace
@@ -587,6 +631,28 @@ int launch_evict(const WriteArgs& a, void* stream) {
   if (a.g.D == 128) evict_kernel<128><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
   else evict_kernel<64><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
   return static_cast<int>(cudaGetLastError());
+}
+
+int launch_step_prep(const WriteArgs& w, const DecodeArgs& d, void* stream, bool pdl) {
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (w.batch == 0) return 0;
+  const int nz = (w.g.Hkv + kAppendHeads - 1) / kAppendHeads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(d.g.Hkv * (d.g.D / 32) * d.batch + w.batch * 2 * nz);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = sizeof(float) * w.g.D * w.g.D;   // holds the rotation's arrays as well
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  auto go = [&](auto kern) -> int {
+    cudaError_t e = ensure_smem_limit(kern, cfg.dynamicSmemBytes);
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaLaunchKernelEx(&cfg, kern, w, d);
+  };
+  return w.g.D == 128 ? go(step_prep_kernel<128>) : go(step_prep_kernel<64>);
 }
 
 int launch_append(const WriteArgs& a, void* stream, bool pdl) {

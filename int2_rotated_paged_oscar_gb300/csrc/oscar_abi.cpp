@@ -283,7 +283,7 @@ extern "C" {
 
 const char* oscar_last_error(void) { return g_last_error.c_str(); }
 
-const char* oscar_version(void) { return "oscar-gb300 0.4 (sm_103a)"; }
+const char* oscar_version(void) { return "oscar-gb300 0.5 (sm_103a)"; }
 
 size_t oscar_int2_pool_bytes(const oscar_config* cfg) {
   Geom g;
@@ -704,27 +704,26 @@ static oscar_status prepare_decode(oscar_ctx* ctx, int32_t layer, const void* q,
   return OSCAR_OK;
 }
 
-// q_rotate, [append], split-K, combine, all as programmatic dependent launches
-// (unless kernel timing is on).  q_rotate waits for its predecessor before it
-// lets the next kernel launch, so every later kernel starts with all earlier
-// work on the stream complete.  With an append
-// (a fused step) the append runs alongside q_rotate and ends by waiting for it;
-// split-K reads every page except the last history page before its own
-// dependency wait, because the append may be writing that page.
+// q_rotate (or, in a fused step, step_prep: the rotation and the append in one
+// grid), split-K, combine, all as programmatic dependent launches (unless
+// kernel timing is on).  The first kernel waits for its predecessor before it
+// reads anything that kernel may write, so every later kernel starts with all
+// earlier work on the stream complete.  In a fused step split-K reads every
+// page except the last history page before its own dependency wait, because
+// the append may be writing that page.
 static oscar_status launch_decode_chain(oscar_ctx* ctx, DecodeArgs& a, const WriteArgs* append, void* stream) {
   const bool pdl = !ctx->timing;  // timing events between launches would break the programmatic overlap
   a.defer_tail_page = append != nullptr;
-  {
+  if (append) {
+    LaunchScope ls(ctx, "step_prep", stream);
+    int e = oscar::launch_step_prep(*append, a, stream, pdl);
+    ls.done(e);
+    if (e) return cuda_fail(e, "step_prep launch");
+  } else {
     LaunchScope ls(ctx, "q_rotate", stream);
     int e = oscar::launch_q_rotate(a, stream, pdl);
     ls.done(e);
     if (e) return cuda_fail(e, "q_rotate launch");
-  }
-  if (append) {
-    LaunchScope ls(ctx, "append", stream);
-    int e = oscar::launch_append(*append, stream, pdl);
-    ls.done(e);
-    if (e) return cuda_fail(e, "append launch");
   }
   {
     LaunchScope ls(ctx, "decode_splitk", stream);

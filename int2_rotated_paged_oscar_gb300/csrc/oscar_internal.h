@@ -126,6 +126,8 @@ int launch_append(const WriteArgs& a, void* stream, bool pdl);
 int launch_q_rotate(const DecodeArgs& a, void* stream, bool pdl);
 int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl);
 int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl);
+// The fused step's first kernel: the query rotation and the append in one grid.
+int launch_step_prep(const WriteArgs& w, const DecodeArgs& d, void* stream, bool pdl);
 int launch_bf16_prepare(const DecodeArgs& a, void* stream);
 // Device address (for the current device) and size of the file-scope decode
 // scratch; the first call on a device looks the address up (not during stream
