@@ -410,9 +410,16 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
 
   // One 16-token block at slot0 of the stage buffer; FULL: every token is a
   // history token (no masking).
-  auto process = [&](auto full_tag, const uint8_t* buf, int slot0, int tb) {
+  // ---------------- QK scores of one 16-token block at slot0 of a stage buffer
+  // (log2 domain, masked to -inf outside the history unless FULL)
+  struct Scores {
+    float a[NH], b[NH];  // rows ra, rb of the block, per query head of the lane
+  };
+  auto qk = [&](auto full_tag, const uint8_t* buf, int slot0, int tb) -> Scores {
     constexpr bool FULL = decltype(full_tag)::value;
-    // ---------------- QK
+    Scores sc;
+    float* sa = sc.a;
+    float* sb = sc.b;
     const uint8_t* pc = buf + slot0 * Lay::ROW;
     const uint8_t* ps = buf + slot0 * Lay::SZ;
     bool va = true, vb = true;
@@ -486,7 +493,6 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) mma_bf16(cz, zA, zB, zA, zB, qz[nt], qz2[nt]);
-    float sa[NH], sb[NH];
     if constexpr (G8) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -516,14 +522,19 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
         sb[j] = vb ? sb[j] : -INFINITY;
       }
     }
-    // ---------------- online softmax
+    return sc;
+  };
+  // ---------------- online softmax: the reference moves (and the accumulators are
+  // rescaled) only when a lane's block maximum mloc exceeds the threshold
+  auto update_ref = [&](float m0, float m1) {
+    const float mloc[2] = {m0, m1};
     bool need = false;
 #pragma unroll
-    for (int j = 0; j < NH; ++j) need |= fmaxf(sa[j], sb[j]) > thr[j];
+    for (int j = 0; j < NH; ++j) need |= mloc[j] > thr[j];
     if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
       for (int j = 0; j < NH; ++j) {
-        float mb = fmaxf(sa[j], sb[j]);
+        float mb = mloc[j];
         mb = warp_max_xor(mb, 4);
         mb = warp_max_xor(mb, 8);
         mb = warp_max_xor(mb, 16);
@@ -550,6 +561,14 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
         }
       }
     }
+  };
+  // ---------------- weights 2^(s - mm) of one block's scores, their sum, and PV
+  auto pv = [&](auto full_tag, const uint8_t* buf, int slot0, int tb, const Scores& sc) {
+    constexpr bool FULL = decltype(full_tag)::value;
+    const float* sa = sc.a;
+    const float* sb = sc.b;
+    const uint8_t* pc = buf + slot0 * Lay::ROW;
+    const uint8_t* ps = buf + slot0 * Lay::SZ;
     float pa[NH], pb[NH];
 #pragma unroll
     for (int j = 0; j < NH; ++j) {
@@ -668,6 +687,22 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
       for (int nt = 0; nt < NT; ++nt) mma_f16(zacc, az0, 0u, az2, 0u, bw[nt][0], bw[nt][1]);
     }
   };
+  // one block (masked pages)
+  auto process = [&](auto full_tag, const uint8_t* buf, int slot0, int tb) {
+    const Scores s0 = qk(full_tag, buf, slot0, tb);
+    update_ref(fmaxf(s0.a[0], s0.b[0]), fmaxf(s0.a[NH - 1], s0.b[NH - 1]));
+    pv(full_tag, buf, slot0, tb, s0);
+  };
+  // two blocks of a page wholly inside the history: both QK first (independent
+  // work for the schedulers), one reference update for the 32 tokens, then PV
+  auto process_pair = [&](const uint8_t* buf, int slot0, int tb) {
+    const Scores s0 = qk(std::integral_constant<bool, true>{}, buf, slot0, tb);
+    const Scores s1 = qk(std::integral_constant<bool, true>{}, buf, slot0 + 16, tb + 16);
+    update_ref(fmaxf(fmaxf(s0.a[0], s0.b[0]), fmaxf(s1.a[0], s1.b[0])),
+               fmaxf(fmaxf(s0.a[NH - 1], s0.b[NH - 1]), fmaxf(s1.a[NH - 1], s1.b[NH - 1])));
+    pv(std::integral_constant<bool, true>{}, buf, slot0, tb, s0);
+    pv(std::integral_constant<bool, true>{}, buf, slot0 + 16, tb + 16, s1);
+  };
 
   bool aborted = false;
   int i_fail = 0;
@@ -683,8 +718,12 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
       const uint8_t* buf = ring + s * Lay::BLOCK;
       const int tp = (pg0 + warp + kWarps * i) * P;  // first token of the page
       if (tp >= g.S && tp + P <= h_end) {  // every token of the page is history: no checks
+        if constexpr (P >= 32) {
 #pragma unroll 1
-        for (int blk = 0; blk < P / 16; ++blk) process(std::integral_constant<bool, true>{}, buf, 16 * blk, tp + 16 * blk);
+          for (int blk = 0; blk < P / 16; blk += 2) process_pair(buf, 16 * blk, tp + 16 * blk);
+        } else {
+          process(std::integral_constant<bool, true>{}, buf, 0, tp);   // a 16-token page is one block
+        }
       } else {
 #pragma unroll 1
         for (int blk = 0; blk < P / 16; ++blk) {
