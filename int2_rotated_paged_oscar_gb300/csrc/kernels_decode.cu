@@ -703,6 +703,25 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     pv(std::integral_constant<bool, true>{}, buf, slot0, tb, s0);
     pv(std::integral_constant<bool, true>{}, buf, slot0 + 16, tb + 16, s1);
   };
+  // the four blocks of a 64-token page wholly inside the history, one reference update
+  auto process_quad = [&](const uint8_t* buf, int tb) {
+    const Scores s0 = qk(std::integral_constant<bool, true>{}, buf, 0, tb);
+    const Scores s1 = qk(std::integral_constant<bool, true>{}, buf, 16, tb + 16);
+    const Scores s2 = qk(std::integral_constant<bool, true>{}, buf, 32, tb + 32);
+    const Scores s3 = qk(std::integral_constant<bool, true>{}, buf, 48, tb + 48);
+    float m[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int jj = j < NH ? j : NH - 1;
+      m[j] = fmaxf(fmaxf(fmaxf(s0.a[jj], s0.b[jj]), fmaxf(s1.a[jj], s1.b[jj])),
+                   fmaxf(fmaxf(s2.a[jj], s2.b[jj]), fmaxf(s3.a[jj], s3.b[jj])));
+    }
+    update_ref(m[0], m[1]);
+    pv(std::integral_constant<bool, true>{}, buf, 0, tb, s0);
+    pv(std::integral_constant<bool, true>{}, buf, 16, tb + 16, s1);
+    pv(std::integral_constant<bool, true>{}, buf, 32, tb + 32, s2);
+    pv(std::integral_constant<bool, true>{}, buf, 48, tb + 48, s3);
+  };
 
   bool aborted = false;
   int i_fail = 0;
@@ -718,9 +737,10 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
       const uint8_t* buf = ring + s * Lay::BLOCK;
       const int tp = (pg0 + warp + kWarps * i) * P;  // first token of the page
       if (tp >= g.S && tp + P <= h_end) {  // every token of the page is history: no checks
-        if constexpr (P >= 32) {
-#pragma unroll 1
-          for (int blk = 0; blk < P / 16; blk += 2) process_pair(buf, 16 * blk, tp + 16 * blk);
+        if constexpr (P == 64) {
+          process_quad(buf, tp);
+        } else if constexpr (P == 32) {
+          process_pair(buf, 0, tp);
         } else {
           process(std::integral_constant<bool, true>{}, buf, 0, tp);   // a 16-token page is one block
         }

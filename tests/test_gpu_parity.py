@@ -155,39 +155,44 @@ def test_append_and_extend_parity(osc):
         gc.close()
 
 
-def test_fused_decode_step_equals_append_then_decode(osc):
-    """oscar_decode_step (append alongside the query rotation) leaves the same cache and output, bit for bit,
-    as oscar_append_step followed by oscar_decode_attn; checked against the oracle at the end."""
+@pytest.mark.parametrize("shape,ppr,lens0,steps", [
+    (syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), 24, [1300, 131], 70),   # crosses a page of evicted tokens
+    (syn.Shape(8, 4, 64, 16, 32, 4, 32, 1), 24, [300, 35], 40),        # d = 64, 16-token pages, GQA 2
+], ids=["d128_p64_gq4", "d64_p16_gq2"])
+def test_fused_decode_step_equals_append_then_decode(osc, shape, ppr, lens0, steps):
+    """oscar_decode_step (the query rotation and the append in one grid) leaves the same cache and output,
+    bit for bit, as oscar_append_step followed by oscar_decode_attn; checked against the oracle at the end.
+    The second request is one token short of evicting at the first step."""
     import torch
-    wl = syn.Workload("step", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=12)
+    wl = syn.Workload("step", shape, [0], seed=12)
     fx = H.fixture(wl)
-    ppr = 24
-    lens0 = [1300, 131]          # the second request starts evicting at its first step
     bt = _contiguous_bt(2, ppr)
     ga, img, _, _, _ = _prefill_both(osc, wl, fx, lens0, bt, 2 * ppr)
     gb, _, _, _, _ = _prefill_both(osc, wl, fx, lens0, bt, 2 * ppr)
     try:
+        hq, d = shape.n_q_heads, shape.head_dim
         slots = np.arange(2, dtype=np.int32)
-        max_seq = 64 * ppr
+        max_seq = shape.page_size * ppr
         ws_bytes = osc.oscar_decode_workspace_size(ga.cfg, 2, max_seq)
         wsa = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
         wsb = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
         rk, rv, btd, sld = H.dev(fx["R_K"]), H.dev(fx["R_V"]), H.dev(bt), H.dev(slots)
         lens = list(lens0)
-        for step in range(70):   # crosses a page boundary of the evicted tokens
+        for step in range(steps):
             kn, vn = syn.kv_tokens(wl, 0, 2, sub=300 + step)
             q = syn.queries(wl, 0, 2, sub=300 + step)
             before = H.dev(np.array(lens, np.int32))
             after = H.dev(np.array(lens, np.int32) + 1)
             kd, vd, qd = H.dev_input(kn, "bf16"), H.dev_input(vn, "bf16"), H.dev_input(q, "bf16")
-            oa = torch.empty((2, 32, 128), dtype=torch.float32, device="cuda")
+            oa = torch.empty((2, hq, d), dtype=torch.float32, device="cuda")
             ob = torch.empty_like(oa)
             osc.oscar_append_step(ga.ctx, 0, kd, vd, osc.DTYPE_BF16, before, 2, rk, rv, fx["clip_K"], fx["clip_V"],
                                   btd, ppr, sld)
             osc.oscar_decode_attn(ga.ctx, 0, qd, osc.DTYPE_BF16, oa, osc.DTYPE_F32, btd, ppr, after, sld, 2, max_seq,
-                                  4, 128, rk, rv, wsa, ws_bytes)
+                                  shape.sink, shape.recent, rk, rv, wsa, ws_bytes)
             osc.oscar_decode_step(gb.ctx, 0, kd, vd, osc.DTYPE_BF16, qd, osc.DTYPE_BF16, ob, osc.DTYPE_F32, btd, ppr,
-                                  after, sld, 2, max_seq, 4, 128, rk, rv, fx["clip_K"], fx["clip_V"], wsb, ws_bytes)
+                                  after, sld, 2, max_seq, shape.sink, shape.recent, rk, rv, fx["clip_K"],
+                                  fx["clip_V"], wsb, ws_bytes)
             assert torch.equal(oa, ob), step
             cache.append_step(img, 0, kn, vn, np.array(lens, np.int32), fx["R_K"], fx["R_V"], fx["clip_K"],
                               fx["clip_V"], bt, slots)
