@@ -1008,33 +1008,35 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(DecodeArgs
   }
 }
 
-// Small batches: one CTA per (query head, request), block 128.  Rows of R_V and
-// the head's split partials are staged in shared memory by bulk copies; warp 0
-// forms the split weights, every thread one merged channel, and each warp a
-// quarter of the rows of R_V^T by shuffle reductions.  With at most one head
-// per SM this short chain beats the head-grouped kernel above, whose phases pay
-// off once many heads share a copy of R_V.
+// Small batches: one CTA per (query head, request), kHeadThreads threads.  R_V
+// and the head's split partials are staged in shared memory by bulk copies
+// (R_V's before the wait on the split kernel).  Warp 0 forms the split weights;
+// NP = kHeadThreads / D threads per channel merge a share of the slots each;
+// NP threads per output channel split R_V^T's k range (float4 rows, each thread
+// starting at its own offset so that a phase of 8 threads reads 8 different
+// bank groups).  The whole tail after the split kernel is a few short steps.
+constexpr int kHeadThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(kThreads) decode_combine_head_kernel(DecodeArgs a) {
-  constexpr int C = D / 32;
+__global__ void __launch_bounds__(kHeadThreads) decode_combine_head_kernel(DecodeArgs a) {
+  constexpr int NP = kHeadThreads / D;
   extern __shared__ __align__(16) float csm[];
   float* Rs = csm;                 // [D][D]
-  float* parts = Rs + D * D;       // [hpc][stride][D + 4] when staged
-  __shared__ float rot[D];
-  __shared__ float rotated_out[D];
+  float* parts = Rs + D * D;       // [stride][D + 4] when staged
+  __shared__ __align__(16) float rot[D];
+  __shared__ float plain[D];
+  __shared__ float share[NP][D];   // per-part sums (merge, then R_V^T)
   __shared__ float wts[kMaxSplits + kMaxWinChunks];
   __shared__ float s_l;
   __shared__ __align__(8) uint64_t bar;
   const Geom& g = a.g;
-  const int hpc = 1;
-  const int b = blockIdx.y;
+  const int b = blockIdx.y, h = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   WsView ws = ws_view(a);
   const int wc = a.wl.win_chunks;
   const int stride = wc + a.wl.max_splits;
   const size_t head_bytes = (size_t)stride * (D + 4) * sizeof(float);
-  const int h0 = blockIdx.x * hpc;
-  const float* gbase = ws.part + ((size_t)b * g.Hq + h0) * stride * (D + 4);
+  const float* gbase = ws.part + ((size_t)b * g.Hq + h) * stride * (D + 4);
   if (tid == 0) {
     mbar_init(&bar, 1);
     fence_barrier_init();
@@ -1043,11 +1045,11 @@ __global__ void __launch_bounds__(kThreads) decode_combine_head_kernel(DecodeArg
   pdl_launch_dependents();  // the next kernel may launch and wait on this one
   // R_V does not depend on the previous kernel: start its copy before waiting on it
   if (tid == 0) {
-    mbar_arrive_expect_tx(&bar, D * D * sizeof(float) + (a.wl.combine_part_smem ? hpc * head_bytes : 0));
+    mbar_arrive_expect_tx(&bar, D * D * sizeof(float) + (a.wl.combine_part_smem ? head_bytes : 0));
     bulk_g2s(Rs, a.R_V, D * D * sizeof(float), &bar);
   }
   pdl_wait();
-  if (tid == 0 && a.wl.combine_part_smem) bulk_g2s(parts, gbase, (uint32_t)(hpc * head_bytes), &bar);
+  if (tid == 0 && a.wl.combine_part_smem) bulk_g2s(parts, gbase, (uint32_t)head_bytes, &bar);
   const int n = a.seq_lens[b];
   const int nsp = seq_len_ok(a, n) ? min(splits_for(a, n), kMaxSplits) : 0;
   const int nslot = wc + nsp;
@@ -1055,76 +1057,88 @@ __global__ void __launch_bounds__(kThreads) decode_combine_head_kernel(DecodeArg
     (void)mbar_wait_bounded(&bar, 0, nullptr);
     return;
   }
-  for (int hi = 0; hi < hpc; ++hi) {
-    const int h = h0 + hi;
-    const float* base = a.wl.combine_part_smem ? parts + (size_t)hi * stride * (D + 4)
-                                               : gbase + (size_t)hi * stride * (D + 4);
-    if (warp == 0) {
-      float M = -INFINITY;
-      for (int i = lane; i < nslot; i += 32) M = fmaxf(M, base[(size_t)i * (D + 4)]);
+  const float* base = a.wl.combine_part_smem ? parts : gbase;
+  // 1. split weights and l (warp 0)
+  if (warp == 0) {
+    float M = -INFINITY;
+    for (int i = lane; i < nslot; i += 32) M = fmaxf(M, base[(size_t)i * (D + 4)]);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      float L = 0.f;
-      for (int i = lane; i < nslot; i += 32) {
-        const float mi = base[(size_t)i * (D + 4)];
-        const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
-        wts[i] = w;
-        L = fmaf(w, base[(size_t)i * (D + 4) + 1], L);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      if (lane == 0) s_l = L;
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int i = lane; i < nslot; i += 32) {
+      const float mi = base[(size_t)i * (D + 4)];
+      const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
+      wts[i] = w;
+      L = fmaf(w, base[(size_t)i * (D + 4) + 1], L);
     }
-    __syncthreads();
-    float plain = 0.f;
-    if (tid < D) {
-      for (int i = 0; i < wc; ++i) plain = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + tid], plain);
-      float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-      int i = wc;
-      for (; i + 3 < nslot; i += 4) {
-        r0 = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + tid], r0);
-        r1 = fmaf(wts[i + 1], base[(size_t)(i + 1) * (D + 4) + 4 + tid], r1);
-        r2 = fmaf(wts[i + 2], base[(size_t)(i + 2) * (D + 4) + 4 + tid], r2);
-        r3 = fmaf(wts[i + 3], base[(size_t)(i + 3) * (D + 4) + 4 + tid], r3);
-      }
-      for (; i < nslot; ++i) r0 = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + tid], r0);
-      rot[tid] = (r0 + r1) + (r2 + r3);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) s_l = L;
+  }
+  __syncthreads();
+  // 2. merge: channel c, part p takes slots [lo, hi) of the INT2 splits; part 0 the window
+  {
+    const int c = tid % D, p = tid / D;
+    const int nint = nslot - wc;
+    const int lo = wc + nint * p / NP, hi = wc + nint * (p + 1) / NP;
+    float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+    int i = lo;
+    for (; i + 3 < hi; i += 4) {
+      r0 = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + c], r0);
+      r1 = fmaf(wts[i + 1], base[(size_t)(i + 1) * (D + 4) + 4 + c], r1);
+      r2 = fmaf(wts[i + 2], base[(size_t)(i + 2) * (D + 4) + 4 + c], r2);
+      r3 = fmaf(wts[i + 3], base[(size_t)(i + 3) * (D + 4) + 4 + c], r3);
     }
-    __syncthreads();
-    // (rot R_V^T)_j = sum_k rot_k R_V[j][k]: warp w handles rows [w*D/4, (w+1)*D/4) in batches of 8
-    float rl[C];
-#pragma unroll
-    for (int c = 0; c < C; ++c) rl[c] = rot[lane * C + c];
-    for (int j0 = warp * (D / 4); j0 < (warp + 1) * (D / 4); j0 += 8) {
-      float sacc[8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const float* row = Rs + (j0 + r) * D + lane * C;
-        float t = 0.f;
-#pragma unroll
-        for (int c = 0; c < C; ++c) t = fmaf(rl[c], row[c], t);
-        sacc[r] = t;
+    for (; i < hi; ++i) r0 = fmaf(wts[i], base[(size_t)i * (D + 4) + 4 + c], r0);
+    share[p][c] = (r0 + r1) + (r2 + r3);
+    if (p == 0) {
+      float q0 = 0.f, q1 = 0.f;
+      int k = 0;
+      for (; k + 1 < wc; k += 2) {
+        q0 = fmaf(wts[k], base[(size_t)k * (D + 4) + 4 + c], q0);
+        q1 = fmaf(wts[k + 1], base[(size_t)(k + 1) * (D + 4) + 4 + c], q1);
       }
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sacc[r] += __shfl_xor_sync(0xffffffffu, sacc[r], o);
-        if (lane == r) rotated_out[j0 + r] = sacc[r];
-      }
+      if (k < wc) q0 = fmaf(wts[k], base[(size_t)k * (D + 4) + 4 + c], q0);
+      plain[c] = q0 + q1;
     }
-    __syncthreads();
-    if (tid < D) {
-      const float inv = s_l > 0.f ? 1.f / s_l : 0.f;
-      const float o = (plain + rotated_out[tid]) * inv;
-      const size_t oi = ((size_t)b * g.Hq + h) * D + tid;
-      if (a.out_dtype == kDtypeBF16) {
-        __nv_bfloat16 hb = __float2bfloat16_rn(o);
-        static_cast<uint16_t*>(a.out)[oi] = *reinterpret_cast<uint16_t*>(&hb);
-      } else {
-        static_cast<float*>(a.out)[oi] = o;
-      }
+  }
+  __syncthreads();
+  if (tid < D) {
+    float r = 0.f;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) r += share[p][tid];
+    rot[tid] = r;
+  }
+  __syncthreads();
+  // 3. (rot R_V^T)_j = sum_k rot_k R_V[j][k]: output j, k part kp
+  {
+    const int j = tid % D, kp = tid / D;
+    constexpr int M4 = (D / 4) / NP;   // float4 per part
+    const float4* Rrow = reinterpret_cast<const float4*>(Rs + j * D);
+    const float4* r4 = reinterpret_cast<const float4*>(rot);
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 4
+    for (int mm = 0; mm < M4; mm += 2) {
+      const int k4a = kp * M4 + (mm + j) % M4, k4b = kp * M4 + (mm + 1 + j) % M4;
+      const float4 ra = Rrow[k4a], xa = r4[k4a], rb = Rrow[k4b], xb = r4[k4b];
+      acc0 = fmaf(xa.x, ra.x, fmaf(xa.y, ra.y, fmaf(xa.z, ra.z, fmaf(xa.w, ra.w, acc0))));
+      acc1 = fmaf(xb.x, rb.x, fmaf(xb.y, rb.y, fmaf(xb.z, rb.z, fmaf(xb.w, rb.w, acc1))));
     }
-    __syncthreads();
+    share[kp][j] = acc0 + acc1;
+  }
+  __syncthreads();
+  if (tid < D) {
+    float o = plain[tid];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) o += share[p][tid];
+    o *= s_l > 0.f ? 1.f / s_l : 0.f;
+    const size_t oi = ((size_t)b * g.Hq + h) * D + tid;
+    if (a.out_dtype == kDtypeBF16) {
+      __nv_bfloat16 hb = __float2bfloat16_rn(o);
+      static_cast<uint16_t*>(a.out)[oi] = *reinterpret_cast<uint16_t*>(&hb);
+    } else {
+      static_cast<float*>(a.out)[oi] = o;
+    }
   }
 }
 
@@ -1217,7 +1231,7 @@ int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   const bool per_head = a.wl.combine_head != 0;
   cfg.gridDim = per_head ? dim3(a.g.Hq, a.batch) : dim3(a.g.Hq / a.wl.combine_hpc, a.batch, a.g.D / a.wl.combine_jb);
-  cfg.blockDim = dim3(per_head ? kThreads : kCombThreads);
+  cfg.blockDim = dim3(per_head ? kHeadThreads : kCombThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

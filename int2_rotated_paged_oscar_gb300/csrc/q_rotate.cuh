@@ -62,20 +62,32 @@ __device__ __forceinline__ void q_rotate_cta(const DecodeArgs& a, int grp, int k
       const int idx = t + u * T;  // row idx / 8, float4 idx % 8
       v[u] = __ldg(Rg + (size_t)(idx >> 3) * (D / 4) + grp * 8 + (idx & 7));
     }
-    pdl_wait();
-    pdl_launch_dependents();
 #pragma unroll
     for (int u = 0; u < D * 8 / T; ++u) {
       const int idx = t + u * T;
       float* dst = &Rs[idx >> 3][(idx & 7) * 4];
       dst[0] = v[u].x; dst[1] = v[u].y; dst[2] = v[u].z; dst[3] = v[u].w;
     }
+    pdl_wait();
+    pdl_launch_dependents();
   }
   const size_t qbase = ((size_t)b * g.Hq + (size_t)kvh * gq) * D;
-  for (int i = t; i < gq * D; i += T) {
-    const float x = load_q(a, qbase + i);
-    qs[i / D][i % D] = x;
-    if (grp == 0) ws.qplain[qbase + i] = x;
+  {
+    constexpr int QMAX = 8 * D / T;   // gq <= 8: every load of q in flight at once
+    float qv[QMAX];
+#pragma unroll
+    for (int u = 0; u < QMAX; ++u) {
+      const int i = t + u * T;
+      qv[u] = i < gq * D ? load_q(a, qbase + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < QMAX; ++u) {
+      const int i = t + u * T;
+      if (i < gq * D) {
+        qs[i / D][i % D] = qv[u];
+        if (grp == 0) ws.qplain[qbase + i] = qv[u];
+      }
+    }
   }
   __syncthreads();
   // squared norms: warp w sums heads w, w + 4
@@ -86,11 +98,18 @@ __device__ __forceinline__ void q_rotate_cta(const DecodeArgs& a, int grp, int k
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) nrm[hh] = sqrtf(ss);
   }
-  // rotation: lane = channel 32 grp + lane, warp w handles heads w, w + 4
+  // rotation: lane = channel 32 grp + lane, warp w handles heads w, w + 4; four
+  // partial sums (inputs i = 4m + r) shorten the dependent chain fourfold
   for (int hh = warp; hh < gq; hh += T / 32) {
-    float acc = 0.f;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll 8
-    for (int i = 0; i < D; ++i) acc = fmaf(qs[hh][i], Rs[i][lane], acc);
+    for (int i = 0; i < D; i += 4) {
+      a0 = fmaf(qs[hh][i], Rs[i][lane], a0);
+      a1 = fmaf(qs[hh][i + 1], Rs[i + 1][lane], a1);
+      a2 = fmaf(qs[hh][i + 2], Rs[i + 2][lane], a2);
+      a3 = fmaf(qs[hh][i + 3], Rs[i + 3][lane], a3);
+    }
+    const float acc = (a0 + a1) + (a2 + a3);
     qr[hh][lane] = acc;
     float gs = acc;
 #pragma unroll
