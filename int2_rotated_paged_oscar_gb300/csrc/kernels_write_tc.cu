@@ -208,10 +208,22 @@ __device__ __forceinline__ void quant_group(const float (&y)[32], int gi, float 
   // clip is the same as clipping y first; then clamp to [0, 3]
   const float t_lo = fmaxf(fmaf(-clip, inv, zinv), 0.f);
   const float t_hi = fminf(fmaf(clip, inv, zinv), 3.f);
+  // the code argument and the rounding add in float32 pairs (two IEEE operations each,
+  // the same results as the scalar forms)
+  const float2 inv2 = make_float2(inv, inv), zinv2 = make_float2(zinv, zinv);
+  const float2 mag2 = make_float2(kRoundMagic, kRoundMagic);
+  float tp[32];
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const float2 t2 = __ffma2_rn(make_float2(y[j], y[j + 1]), inv2, zinv2);
+    const float2 c2 = make_float2(fminf(fmaxf(t2.x, t_lo), t_hi), fminf(fmaxf(t2.y, t_lo), t_hi));
+    const float2 p2 = __fadd2_rn(c2, mag2);
+    tp[j] = p2.x;
+    tp[j + 1] = p2.y;
+  }
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    const float t = fminf(fmaxf(fmaf(y[j], inv, zinv), t_lo), t_hi);
-    const uint32_t pat = __float_as_uint(t + kRoundMagic);  // kRoundBits + code
+    const uint32_t pat = __float_as_uint(tp[j]);  // kRoundBits + code
     const int c = 32 * gi + j;
     int word, shift;
     if constexpr (!IS_V) {
@@ -450,7 +462,12 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
           tmem_wait_ld();
           float y[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(r0[j]) + __uint_as_float(r1[j]);
+          for (int j = 0; j < 32; j += 2) {
+            const float2 s2 = __fadd2_rn(make_float2(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1])),
+                                         make_float2(__uint_as_float(r1[j]), __uint_as_float(r1[j + 1])));
+            y[j] = s2.x;
+            y[j + 1] = s2.y;
+          }
           quant_group<D, IS_V>(y, gi, clip, words, szw[gi]);
         }
         tc_fence_before();
