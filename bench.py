@@ -55,6 +55,7 @@ def parse():
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the batched-decode sweep")
     ap.add_argument("--sweep-batches", default="1,8,32,64")
+    ap.add_argument("--no-extra", action="store_true", help="skip the long-context, capacity and write configurations")
     ap.add_argument("--sweep-only", action="store_true",
                     help="run only the batched-decode sweep and print its rows (a profiling entry point)")
     return ap.parse_args()
@@ -409,6 +410,148 @@ def _bf16_sweep_point(osc, cfg, kd, vd, lens, perm, L, q, out, steps, row_shift)
     return {"bf16_ms_per_layer": t["ms_per_layer"], "bf16_effective_gbs": bf_bytes / (t["ms_per_layer"] * 1e-3) / 1e9}
 
 
+def _ctx_for(osc, wl, num_layers, max_requests, ppr):
+    import torch
+    s = wl.shape
+    cfg = osc.make_config(num_layers=num_layers, n_q_heads=s.n_q_heads, n_kv_heads=s.n_kv_heads, head_dim=s.head_dim,
+                          page_size=s.page_size, sink=s.sink, recent=s.recent, max_requests=max_requests,
+                          max_pages_per_req=ppr, num_pages=max_requests * ppr)
+    pool = torch.empty(osc.oscar_int2_pool_bytes(cfg), dtype=torch.uint8, device="cuda")
+    slab = torch.zeros(osc.oscar_window_slab_bytes(cfg) // 2, dtype=torch.int16, device="cuda")
+    return cfg, pool, slab, osc.oscar_create(cfg, pool, slab)
+
+
+def _stream(wl, rows):
+    import torch
+    kh, vh = syn.kv_tokens(wl, 0, rows)
+    kd = torch.from_numpy(syn.to_bf16_bits(kh).view(np.int16)).cuda()
+    vd = torch.from_numpy(syn.to_bf16_bits(vh).view(np.int16)).cuda()
+    return kd, vd
+
+
+def long_and_capacity(osc, hbm_peak, steps=5, row_shift=37):
+    """The long-context, capacity and write configurations of the workload list, timed with CUDA events:
+    4a: batch-1 decode at 131,072 tokens (32 q / 8 kv heads), three layers per step so that a step exceeds L2;
+    4b: 28 requests x 100,000 tokens x 64 layers (64 q / 8 kv heads), one decode step over all 64 layers
+        with the whole INT2 cache (137.7 GB) resident on the GPU (a BF16 cache of the same tokens, 734 GB,
+        would not fit);
+    5:  the prefill write of 8 requests x 32,768 tokens (8 kv heads), then fused decode steps (append +
+        attention) of the 8 requests.
+    Request b reads rows [37 b, 37 b + n) of one seeded input stream; one calibrated rotation serves every
+    layer (the kernels' work does not depend on which rotation they apply)."""
+    import torch
+    from int2_rotated_paged_oscar_gb300 import calibrate
+    res = {}
+    i32 = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+
+    def calib(wl):
+        fx = calibrate.calibrate_layer(syn.queries(wl, 0, 128, calib=True), *syn.kv_tokens(wl, 0, 128, calib=True))
+        return fx, torch.from_numpy(fx["R_K"]).cuda(), torch.from_numpy(fx["R_V"]).cuda()
+
+    def fill(ctx, L, lens, bt, ppr, kd, vd, fx, rk, rv):
+        for layer in range(L):
+            for b, n in enumerate(lens):
+                o = row_shift * b
+                osc.oscar_write_kv(ctx, layer, kd[o:o + n], vd[o:o + n], osc.DTYPE_BF16, i32([0, n]), i32([0]), 1, n,
+                                   rk, rv, fx["clip_K"], fx["clip_V"], bt[b:b + 1], ppr, i32([b]))
+        torch.cuda.synchronize()
+        assert osc.oscar_check_status(ctx) == 0
+
+    def decode_point(wl, lens, L, n_steps, kd, vd):
+        s = wl.shape
+        B, nmax = len(lens), max(lens)
+        ppr = syn.pages_for(nmax, s.page_size)
+        cfg, pool, slab, ctx = _ctx_for(osc, wl, L, B, ppr)
+        bt = torch.arange(B * ppr, dtype=torch.int32, device="cuda").view(B, ppr)
+        fx, rk, rv = calib(wl)
+        fill(ctx, L, lens, bt, ppr, kd, vd, fx, rk, rv)
+        q = torch.from_numpy(syn.to_bf16_bits(syn.queries(wl, 0, B * L)).view(np.int16)).cuda().view(
+            L, B, s.n_q_heads, s.head_dim)
+        out = torch.empty((L, B, s.n_q_heads, s.head_dim), dtype=torch.float32, device="cuda")
+        lens_d, slots = i32(lens), torch.arange(B, dtype=torch.int32, device="cuda")
+        ws_bytes = osc.oscar_decode_workspace_size(cfg, B, nmax)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+
+        def dec_pass():
+            for layer in range(L):
+                osc.oscar_decode_attn(ctx, layer, q[layer], osc.DTYPE_BF16, out[layer], osc.DTYPE_F32, bt, ppr, lens_d,
+                                      slots, B, nmax, s.sink, s.recent, rk, rv, ws, ws_bytes)
+        t = _time_graph(dec_pass, n_steps, L)
+        assert osc.oscar_check_status(ctx) == 0
+        per_layer = sum(sum(decode_bytes(n, hq=s.n_q_heads, hkv=s.n_kv_heads, d=s.head_dim, s=s.sink,
+                                         w=s.recent).values()) for n in lens)
+        osc.oscar_destroy(ctx)
+        del pool, slab
+        torch.cuda.empty_cache()
+        gbs = per_layer * L / (t["ms_per_step"] * 1e-3) / 1e9
+        return {"layers_per_step": L, "batch": B, "context": nmax, "ms_per_step": t["ms_per_step"],
+                "ms_per_layer": t["ms_per_layer"], "bytes_per_step": per_layer * L, "effective_gbs": gbs,
+                "frac_of_peak": gbs / hbm_peak}
+
+    # ---- 4a: batch 1 at 131K
+    wl = syn.long_131k()
+    kd, vd = _stream(wl, 131072)
+    res["long_131k"] = decode_point(wl, [131072], 3, max(steps, 5), kd, vd)
+    del kd, vd
+    # ---- 4b: 28 x 100K x 64 layers, one step over every layer
+    wl = syn.capacity_28x100k(num_layers=64)
+    kd, vd = _stream(wl, 100000 + row_shift * 28)
+    res["capacity_28x100k_64_layers"] = decode_point(wl, [100000] * 28, 64, 3, kd, vd)
+    res["capacity_28x100k_64_layers"]["int2_cache_gb"] = 64 * 28 * syn.pages_for(100000, 64) * 8 * 6144 / 1e9
+    res["capacity_28x100k_64_layers"]["bf16_cache_gb_would_be"] = 64 * 28 * 100000 * 8 * 128 * 2 * 2 / 1e9
+    del kd, vd
+    torch.cuda.empty_cache()
+    # ---- 5: prefill write of 8 x 32K, then fused steps
+    wl = syn.write_prefill()
+    s = wl.shape
+    B, n, L = 8, 32768, 1
+    ppr = syn.pages_for(n + 64, s.page_size)
+    cfg, pool, slab, ctx = _ctx_for(osc, wl, L, B, ppr)
+    bt = torch.arange(B * ppr, dtype=torch.int32, device="cuda").view(B, ppr)
+    fx, rk, rv = calib(wl)
+    kd, vd = _stream(wl, B * n)
+    cu = i32([n * b for b in range(B + 1)])
+    start, slots = i32([0] * B), torch.arange(B, dtype=torch.int32, device="cuda")
+
+    def write():
+        osc.oscar_write_kv(ctx, 0, kd, vd, osc.DTYPE_BF16, cu, start, B, B * n, rk, rv, fx["clip_K"], fx["clip_V"], bt,
+                           ppr, slots)
+    write()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        write()
+    e1.record()
+    torch.cuda.synchronize()
+    wms = e0.elapsed_time(e1) / 5
+    res["write_prefill_8x32k"] = {"tokens": B * n, "ms": wms, "tokens_per_s": B * n / (wms * 1e-3),
+                                  "bytes": B * n * 8 * 2 * (128 * 2 + 48),
+                                  "gbs": B * n * 8 * 2 * (128 * 2 + 48) / (wms * 1e-3) / 1e9}
+    kn = torch.from_numpy(syn.to_bf16_bits(syn.kv_tokens(wl, 0, B, sub=9)[0]).view(np.int16)).cuda()
+    vn = torch.from_numpy(syn.to_bf16_bits(syn.kv_tokens(wl, 0, B, sub=9)[1]).view(np.int16)).cuda()
+    q = torch.from_numpy(syn.to_bf16_bits(syn.queries(wl, 0, B)).view(np.int16)).cuda()
+    out = torch.empty((B, s.n_q_heads, s.head_dim), dtype=torch.float32, device="cuda")
+    lens = i32([n + 1] * B)
+    max_seq = ppr * s.page_size
+    ws_bytes = osc.oscar_decode_workspace_size(cfg, B, max_seq)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+
+    def step():
+        osc.oscar_decode_step(ctx, 0, kn, vn, osc.DTYPE_BF16, q, osc.DTYPE_BF16, out, osc.DTYPE_F32, bt, ppr, lens,
+                              slots, B, max_seq, s.sink, s.recent, rk, rv, fx["clip_K"], fx["clip_V"], ws, ws_bytes)
+        lens.add_(1)
+    t = _time_graph(step, 40, 1)
+    assert osc.oscar_check_status(ctx) == 0
+    step_bytes = B * (sum(decode_bytes(n + 20, hq=8).values()) + append_bytes())
+    res["decode_step_8x32k"] = {"batch": B, "context": n, "ms_per_step": t["ms_per_step"],
+                                "effective_gbs": step_bytes / (t["ms_per_step"] * 1e-3) / 1e9}
+    osc.oscar_destroy(ctx)
+    del pool, slab, kd, vd
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, world, rank, local):
     import torch
     from int2_rotated_paged_oscar_gb300 import build as bld
@@ -669,6 +812,9 @@ def run_ours(args, world, rank, local):
 
     value = sum_over_ranks(value_rank, world)
     sweep = None
+    extra = None
+    if rank == 0 and not args.no_extra:
+        extra = long_and_capacity(osc, hbm_peak)
     if rank == 0 and not args.no_sweep:
         sweep = batch_sweep(osc, [int(x) for x in args.sweep_batches.split(",") if x], min(args.steps, 20), hbm_peak,
                             with_bf16=not args.no_bf16)
@@ -691,6 +837,7 @@ def run_ours(args, world, rank, local):
                 "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "ms_per_step": e2e_ms},
                 "gpu_launches": int(launches), "clocks": clk, "cpu_baseline": cpu,
+                "long_capacity_write": extra,
                 "batch_sweep": {"workload": "Qwen3-32B-shaped layer (64 q / 8 kv heads, d=128), ragged context "
                                             "U[8K, 32K], shuffled pages, decode only", "peak_gbs": hbm_peak,
                                 "rows": sweep}}
