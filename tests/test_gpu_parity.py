@@ -77,6 +77,34 @@ def test_write_parity(osc, wl, lens):
         gc.close()
 
 
+def test_naive_int2_identity_rotation(osc):
+    """The pages' naive INT2 baseline (no rotation, R_K = R_V = I; clip from the unrotated calibration values)
+    runs on the same kernels: write codes against the oracle, and decode against the oracle on the GPU's cache."""
+    from oracle import rotation
+    wl = syn.Workload("naive", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=11)
+    s = wl.shape
+    eye = np.eye(s.head_dim, dtype=np.float32)
+    kc, vc = syn.kv_tokens(wl, 0, 256, calib=True)
+    fx = {"R_K": eye, "R_V": eye, "clip_K": float(np.float32(rotation.clip_threshold(kc, eye))),
+          "clip_V": float(np.float32(rotation.clip_threshold(vc, eye)))}
+    lens = [2100, 600]
+    ppr = max(syn.pages_for(n, s.page_size) for n in lens) + 1
+    bt = _contiguous_bt(len(lens), ppr)
+    gc, img, diag, _, _ = _prefill_both(osc, wl, fx, lens, bt, len(lens) * ppr)
+    try:
+        res = H.compare_history(gc.pool_np(), img.g, 0, diag, exact_ties=True)
+        assert res["elements"] > 0
+        H.compare_window(gc.slab_np(), img.slab, 0, range(len(lens)))
+        q = syn.queries(wl, 0, len(lens))
+        got = H.run_decode(gc, 0, q, "bf16", bt, lens, [0, 1], fx)
+        gimg = cache.CacheImage(img.g)
+        gimg.pool, gimg.slab = gc.pool_np(), gc.slab_np()
+        want = attention.decode(gimg, 0, q, bt, lens, [0, 1], fx["R_K"], fx["R_V"])
+        H.assert_decode_close(got, want)
+    finally:
+        gc.close()
+
+
 def test_write_hadamard_only_parity(osc):
     """Data-oblivious rotation R = H P (U = I): the FWHT path against the oracle's dense fp32 R."""
     wl = syn.Workload("had", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=7)
