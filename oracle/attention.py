@@ -126,3 +126,45 @@ def bf16_paged_decode(pool_bits, layer: int, q, block_table, seq_lens, page_size
         for h in range(hq):
             out[b, h] = softmax_attention(q[b, h], kk[:, h // grp], vv[:, h // grp])
     return out
+
+
+def extend(cache: CacheImage, layer: int, q, k_new, v_new, cu_seqlens, prefix_lens, block_table, req_slot,
+           r_k, r_v) -> np.ndarray:
+    """Extend (chunked prefill) attention over the mixed cache: the plain definition, float64.
+
+    Source: the OSCAR technical summaries on gist.science, section 2.2 B (the serving
+    kernel covers paged attention and prefix caching over the INT2 history) and the
+    same page's systems contribution (prefix reuse kept in the INT2 cache).  The pages
+    do not spell out the extend step; the reading taken here is the usual one for a
+    prefix cache: request b holds prefix_lens[b] cached tokens, in the form the cache
+    stores them at that length (history dequantised and rotated back, sink and recent
+    tokens in BF16), and brings a chunk of len_b = cu_seqlens[b+1] - cu_seqlens[b] new
+    tokens at positions prefix_lens[b] + i.  Query i of the chunk attends to every
+    cached token and to the chunk's tokens 0..i (causal), whose keys and values are the
+    chunk's own inputs (k_new, v_new, already BF16-valued).  The chunk is written to
+    the cache afterwards.
+
+    q [T, Hq, d], k_new / v_new [T, Hkv, d] (T = cu_seqlens[-1]) -> o [T, Hq, d].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k_new = np.asarray(k_new, dtype=np.float64)
+    v_new = np.asarray(v_new, dtype=np.float64)
+    total, hq, d = q.shape
+    g = cache.g
+    grp = hq // g.n_kv_heads
+    rk = np.asarray(r_k, dtype=np.float64)
+    rv = np.asarray(r_v, dtype=np.float64)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    out = np.zeros((total, hq, d))
+    for b in range(cu.size - 1):
+        n_pre = int(prefix_lens[b])
+        yk, yv, wk, wv = _gather(cache, layer, b, n_pre, block_table, req_slot)
+        k_pre = np.concatenate([yk @ rk.T, wk], axis=0)
+        v_pre = np.concatenate([yv @ rv.T, wv], axis=0)
+        c0, c1 = int(cu[b]), int(cu[b + 1])
+        for i in range(c1 - c0):
+            k_all = np.concatenate([k_pre, k_new[c0:c0 + i + 1]], axis=0)
+            v_all = np.concatenate([v_pre, v_new[c0:c0 + i + 1]], axis=0)
+            for h in range(hq):
+                out[c0 + i, h] = softmax_attention(q[c0 + i, h], k_all[:, h // grp], v_all[:, h // grp])
+    return out

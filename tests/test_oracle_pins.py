@@ -467,3 +467,97 @@ def test_bf16_paged_decode_matches_textbook():
     out = attention.bf16_paged_decode(pool, 0, q, bt, [n], p)
     for h in range(4):
         assert np.allclose(out[0, h], _brute_attention(q[0, h], k[:, h // 2], v[:, h // 2]), rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- extend (chunked prefill) attention
+def _sdpa(q, k, v, mask):
+    """torch's scaled_dot_product_attention in float64 on the CPU: q [T, Hq, d], k, v [N, Hkv, d],
+    mask [T, N] (True = visible); kv heads repeated to the query heads."""
+    import torch
+    grp = q.shape[1] // k.shape[1]
+    tq = torch.from_numpy(np.asarray(q, np.float64)).permute(1, 0, 2)
+    tk = torch.from_numpy(np.asarray(k, np.float64)).permute(1, 0, 2).repeat_interleave(grp, dim=0)
+    tv = torch.from_numpy(np.asarray(v, np.float64)).permute(1, 0, 2).repeat_interleave(grp, dim=0)
+    out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.from_numpy(mask))
+    return out.permute(1, 0, 2).numpy()
+
+
+def _chunk(wl, n, sub=1):
+    k, v = syn.kv_tokens(wl, 0, n, sub=sub)
+    return quant.bf16_round(k.astype(np.float64)), quant.bf16_round(v.astype(np.float64))
+
+
+def test_extend_without_prefix_is_causal_sdpa():
+    g = _geom()
+    wl, fx = _fixture()
+    img = cache.CacheImage(g)
+    bt = np.arange(40, dtype=np.int32)[None, :]
+    t = 23
+    k, v = _chunk(wl, t)
+    q = syn.queries(wl, 0, t, sub=3)
+    out = attention.extend(img, 0, q, k, v, [0, t], [0], bt, [0], fx["R_K"], fx["R_V"])
+    want = _sdpa(q, k, v, np.tril(np.ones((t, t), dtype=bool)))
+    assert np.allclose(out, want, rtol=1e-12, atol=1e-13)
+
+
+def test_extend_over_a_bf16_prefix_is_masked_sdpa():
+    """Prefix short enough to be all sink + recent (no INT2 history): keys = BF16 prefix ++ chunk."""
+    g = _geom()
+    wl, fx = _fixture()
+    img = cache.CacheImage(g)
+    bt = np.arange(40, dtype=np.int32)[None, :]
+    n_pre, t = 11, 9    # 11 <= S + W = 12
+    kp, vp = _prefill(img, wl, fx, n_pre, bt)
+    k, v = _chunk(wl, t)
+    q = syn.queries(wl, 0, t, sub=3)
+    out = attention.extend(img, 0, q, k, v, [0, t], [n_pre], bt, [0], fx["R_K"], fx["R_V"])
+    keys = np.concatenate([quant.bf16_round(kp.astype(np.float64)), k])
+    vals = np.concatenate([quant.bf16_round(vp.astype(np.float64)), v])
+    mask = np.concatenate([np.ones((t, n_pre), dtype=bool), np.tril(np.ones((t, t), dtype=bool))], axis=1)
+    assert np.allclose(out, _sdpa(q, keys, vals, mask), rtol=1e-12, atol=1e-13)
+
+
+def test_extend_with_an_invisible_chunk_token_is_decode_over_the_prefix():
+    """A one-token chunk whose key scores -1e6 * |q|^2 has weight exactly 0 in float64, so extend
+    reduces to decode over the cached prefix (INT2 history, rotated back, plus the BF16 window)."""
+    g = _geom(hkv=2)
+    wl, fx = _fixture()
+    img = cache.CacheImage(g)
+    bt = np.arange(40, dtype=np.int32)[None, :]
+    n_pre = 45   # history tokens 4 .. 36
+    _prefill(img, wl, fx, n_pre, bt)
+    q = syn.queries(wl, 0, 1, sub=3).astype(np.float64)
+    q[0, 1] = q[0, 0]   # both query heads of kv head 0 alike, and of kv head 1
+    q[0, 3] = q[0, 2]
+    k = np.stack([-1e6 * q[0, 0], -1e6 * q[0, 2]])[None]
+    v = np.full_like(k, 7.0)
+    out = attention.extend(img, 0, q, k, v, [0, 1], [n_pre], bt, [0], fx["R_K"], fx["R_V"])
+    want = attention.decode(img, 0, q, bt, [n_pre], [0], fx["R_K"], fx["R_V"])
+    assert np.array_equal(out, want)
+
+
+def test_extend_is_causal_and_requests_are_independent():
+    g = _geom()
+    wl, fx = _fixture()
+    img = cache.CacheImage(g)
+    bt = np.arange(40, dtype=np.int32).reshape(2, 20)
+    lens_pre, lens = [37, 5], [6, 4]
+    _prefill(img, wl, fx, lens_pre[0], bt, slot=0, sub=0)
+    cache.write_kv(img, 0, *syn.kv_tokens(wl, 0, lens_pre[1], sub=5), [0, lens_pre[1]], [0], fx["R_K"], fx["R_V"],
+                   fx["clip_K"], fx["clip_V"], bt[1:], [1])
+    k, v = _chunk(wl, sum(lens))
+    q = syn.queries(wl, 0, sum(lens), sub=3)
+    cu = [0, lens[0], sum(lens)]
+    both = attention.extend(img, 0, q, k, v, cu, lens_pre, bt, [0, 1], fx["R_K"], fx["R_V"])
+    # request 1 alone (its own block-table row and slot)
+    alone = attention.extend(img, 0, q[lens[0]:], k[lens[0]:], v[lens[0]:], [0, lens[1]], lens_pre[1:], bt[1:], [1],
+                             fx["R_K"], fx["R_V"])
+    assert np.array_equal(both[lens[0]:], alone)
+    # changing chunk token j changes no output before j
+    k2, v2 = k.copy(), v.copy()
+    k2[3] += 5.0
+    v2[3] -= 5.0
+    moved = attention.extend(img, 0, q, k2, v2, cu, lens_pre, bt, [0, 1], fx["R_K"], fx["R_V"])
+    assert np.array_equal(moved[:3], both[:3])
+    assert not np.allclose(moved[3:lens[0]], both[3:lens[0]])
+    assert np.array_equal(moved[lens[0]:], both[lens[0]:])
