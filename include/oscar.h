@@ -268,6 +268,41 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
                                        int32_t max_seq, int32_t sink, int32_t recent, const float* R_K,
                                        const float* R_V, void* stream);
 
+/* ---------------------------------------------------------------- extend
+ * Extend (chunked prefill) attention over the mixed cache (summary section 2.2 B:
+ * the serving kernel handles paged attention and prefix caching over the INT2
+ * history; section 3: prefix reuse kept with the INT2 cache).  Request b holds
+ * prefix_lens[b] cached tokens and brings len_b = cu_seqlens[b+1] - cu_seqlens[b]
+ * new tokens at positions prefix_lens[b] + i.  Query token i of request b
+ * attends to every cached token in the form the cache stores it at length
+ * prefix_lens[b] (INT2 history dequantised and rotated back, sink and recent
+ * tokens BF16) and, causally, to the chunk's tokens 0..i, whose keys and
+ * values are the K_new / V_new rows themselves.  Call it before writing the
+ * chunk (oscar_write_kv with start_pos = prefix_lens): the cache must hold
+ * exactly prefix_lens[b] tokens of request b.
+ *  q: [total_tokens][n_q_heads][d] (q_dtype); K_new, V_new:
+ *  [total_tokens][n_kv_heads][d] BF16 (other kv_dtype: OSCAR_ERR_UNSUPPORTED);
+ *  out: [total_tokens][n_q_heads][d] float32 or bf16 (out_dtype).  q, K_new,
+ *  V_new and out 16-byte aligned.  cu_seqlens [batch+1], prefix_lens [batch],
+ *  req_slot [batch]: device int32; total_tokens = cu_seqlens[batch] and
+ *  max_chunk >= every len_b (host values, they size the grids).
+ *  block_table [batch][bt_stride] maps the history pages of each prefix (a
+ *  missing one sets OSCAR_DEV_BAD_PAGE); R_K, R_V: the layer's rotations
+ *  (device float32 [d][d]); the layer needs a declared clip threshold.
+ *  n_q_heads / n_kv_heads must divide 128 (else OSCAR_ERR_UNSUPPORTED).
+ *  workspace: device scratch of oscar_extend_workspace_size(cfg, total_tokens)
+ *  bytes (256-byte aligned, no initialisation); it holds q R_K for every query
+ *  row and R_V^T.  Softmax scale 1/sqrt(d), query head h reads kv head
+ *  h / (n_q_heads / n_kv_heads).  Two kernels on the stream: the query
+ *  rotation, then the tensor-core attention (timing name "extend"). */
+oscar_status oscar_extend_workspace_size(const oscar_config* cfg, int32_t total_tokens, size_t* bytes);
+oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, const void* K_new,
+                               const void* V_new, int32_t kv_dtype, void* out, int32_t out_dtype,
+                               const int32_t* cu_seqlens, const int32_t* prefix_lens, int32_t batch,
+                               int32_t total_tokens, int32_t max_chunk, const int32_t* block_table, int32_t bt_stride,
+                               const int32_t* req_slot, const float* R_K, const float* R_V, void* workspace,
+                               size_t ws_bytes, void* stream);
+
 /* In-house comparison: standard split-K paged decode over an all-BF16 cache
  * (layout above), same grid and staging as the INT2 kernel.  bf16_pool points
  * at the whole [num_layers][num_pages]... pool; workspace from
@@ -290,7 +325,7 @@ oscar_status oscar_check_status(oscar_ctx* ctx, void* stream, int32_t* out_bits)
  * oscar_kernel_time returns the summed milliseconds and launch count since the
  * last reset (synchronises the recorded events).  Names: "decode_splitk",
  * "decode_combine", "q_rotate", "step_prep", "append", "evict", "write", "bf16_prepare",
- * "bf16_decode", "bf16_combine".  Launches
+ * "bf16_decode", "bf16_combine", "extend".  Launches
  * recorded into a CUDA graph get external event-record nodes: replay the graph
  * once, then read; the events return to the library when read, so a graph
  * captured with timing on is replayed at most once.  With timing on, the decode

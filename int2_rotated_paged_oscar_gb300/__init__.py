@@ -81,6 +81,9 @@ _SIGS = {
                                  _i32, _i32, _vp, _vp, _f32, _f32, _vp, ctypes.c_size_t, _vp]),
     "oscar_decode_attn_noalloc": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32,
                                          _i32, _vp, _vp, _vp]),
+    "oscar_extend_workspace_size": (_i32, [_cfgp, _i32, ctypes.POINTER(ctypes.c_size_t)]),
+    "oscar_extend_attn": (_i32, [_vp, _i32, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _vp,
+                                 _i32, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "oscar_bf16_decode_workspace_size": (_i32, [_cfgp, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)]),
     "oscar_bf16_decode_attn": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _vp,
                                       ctypes.c_size_t, _vp]),
@@ -262,6 +265,21 @@ def oscar_decode_attn_noalloc(ctx, layer, q, q_dtype, out, out_dtype, block_tabl
     _check(load().oscar_decode_attn_noalloc(ctx, layer, ptr(q), q_dtype, ptr(out), out_dtype, ptr(block_table),
                                             bt_stride, ptr(seq_lens), ptr(req_slot), batch, max_seq, sink, recent,
                                             ptr(R_K), ptr(R_V), stream_ptr(stream)))
+
+
+def oscar_extend_workspace_size(cfg: oscar_config, total_tokens: int) -> int:
+    out = ctypes.c_size_t()
+    _check(load().oscar_extend_workspace_size(ctypes.byref(cfg), total_tokens, ctypes.byref(out)))
+    return out.value
+
+
+def oscar_extend_attn(ctx, layer, q, q_dtype, K_new, V_new, kv_dtype, out, out_dtype, cu_seqlens, prefix_lens, batch,
+                      total_tokens, max_chunk, block_table, bt_stride, req_slot, R_K, R_V, workspace, ws_bytes,
+                      stream=None) -> None:
+    _check(load().oscar_extend_attn(ctx, layer, ptr(q), q_dtype, ptr(K_new), ptr(V_new), kv_dtype, ptr(out),
+                                    out_dtype, ptr(cu_seqlens), ptr(prefix_lens), batch, total_tokens, max_chunk,
+                                    ptr(block_table), bt_stride, ptr(req_slot), ptr(R_K), ptr(R_V), ptr(workspace),
+                                    ws_bytes, stream_ptr(stream)))
 
 
 def oscar_bf16_decode_attn(ctx, layer, bf16_pool, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens,

@@ -1,0 +1,959 @@
+// Extend (chunked prefill) attention over the mixed INT2 / BF16 paged cache on the
+// 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// Source: OSCAR technical summary (gist.science), section 2.2 B -- the serving kernel
+// unpacks, dequantises and inverse-rotates the INT2 history and computes attention over
+// it, compatible with paged attention and prefix caching; section 3 -- prefix reuse kept
+// with the INT2 cache.  Request b holds prefix_lens[b] cached tokens (history INT2 in the
+// rotated basis, sink and recent tokens BF16) and brings a chunk of new tokens; query i
+// of the chunk attends to every cached token and, causally, to chunk tokens 0..i, whose
+// keys and values are the chunk's own BF16 inputs.
+//
+// One CTA owns 128 query rows (chunk tokens x the query heads of one kv head, row r =
+// token i0 + r / gq, head r % gq) and walks 64-key tiles: first the INT2 history tiles,
+// then the BF16 window tiles, then the chunk's own tiles.  Per tile:
+//   S = Q K^T into TMEM (two buffers, so the next tile's scores are computed while the
+//   softmax reads this tile's), softmax by the row's own thread, P to shared memory,
+//   O += P V into TMEM.
+// History tiles run in the rotated basis with f16 operands, each dequantised value split
+// about its group's centre, z + c s = (z + 1.5 s) + (c - 1.5) s, so that the two parts do
+// not cancel in the float32 accumulators (a group straddling zero has z near -1.5 s):
+//   K operand  = (code - 1.5) * s * 2^(k_K + pos - 10)  (exact: an 8-bit scale times
+//                +-0.5 or +-1.5),
+//   Q operand  = q' * 2^(e_r + 10 - pos), split into f16 hi + lo (22 bits),
+//   centre term = one more MMA (K = 16): the q' group sums Q_g in three f16 terms times
+//                the centres m = z + 1.5 s in two (hi, lo), the four (five for d = 64)
+//                largest of the six cross products,
+//   V operand  = (code - 1.5) * s_V * 2^(k_V + pos - 10), the slot factor 2^(10 - pos)
+//   and the V centres (a 16-column accumulator of sum_j p_j m_j, hi and lo columns)
+//   applied in the epilogue,
+//   P as f16 hi + lo (weights <= 2^14), the row sum l taken over the rounded pair.
+// BF16 tiles run in the plain basis with BF16 operands: Q as hi + lo (hi alone for a BF16
+// query), P as three BF16 terms (24 bits; the values are unbounded BF16), K and V exactly
+// as stored.  Both kinds share one running softmax reference per row; the two
+// output accumulators (rotated and plain) are rescaled together.  The epilogue forms
+// out = (O_plain + y R_V^T) / l, y the rotated accumulator put back to value scale.
+//
+// Roles: warps 0-3 (softmax; thread r owns row r = TMEM lane r), warps 4-7 (unpack of
+// the next tile into the shared-memory operand tiles, INT2 pages staged one tile ahead
+// by cp.async), warp 8 (TMEM allocation, MMA issue).  The warps meet at one CTA barrier
+// per tile; MMAs run asynchronously between barriers.  Every mbarrier wait is bounded
+// by %globaltimer: a timeout flags the status word and the CTA drains and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+#include <utility>
+
+#include "common.cuh"
+#include "oscar_internal.h"
+
+namespace oscar {
+namespace {
+
+#include "tc_common.cuh"
+
+constexpr int kXRows = 128;                  // query rows per CTA (TMEM lanes)
+constexpr int kXKeys = 64;                   // keys per tile
+constexpr int kXThreads = 9 * 32;            // softmax 0-3, unpack 4-7, MMA 8
+constexpr float kXLog2e = 1.4426950408889634f;
+constexpr float kXRescaleLog2 = 8.f;         // the reference moves when a score exceeds it by more
+constexpr float kXWeightShift = 6.f;         // weights 2^(s - m), m = reference - shift: at most 2^14
+
+enum TileKind { kTileInt2 = 0, kTileWindow = 1, kTileChunk = 2 };
+
+template <typename F, size_t... I>
+__device__ __forceinline__ void static_for_impl(F&& f, std::index_sequence<I...>) {
+  (f(std::integral_constant<int, (int)I>{}), ...);
+}
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  static_for_impl(f, std::make_index_sequence<N>{});
+}
+
+// Shared memory plan (bytes from a 1024-aligned base).  Every operand tile is K-major
+// with the 128-byte swizzle, 1024-aligned.
+template <int D>
+struct XLayout {
+  static constexpr int G = D / 32;
+  static constexpr int Q_PLANE = kXRows * D * 2;
+  static constexpr int QHI = 0, QLO = Q_PLANE, QZ = 2 * Q_PLANE;   // QZ: [128][64] 16-bit, 16 columns used
+  static constexpr int QZ_BYTES = kXRows * 128;
+  static constexpr int KT = 0, KT_BYTES = kXKeys * D * 2;         // [64 keys][D]
+  static constexpr int KZ = KT + KT_BYTES, KZ_BYTES = kXKeys * 128;  // [64 keys][64], 16 columns used
+  static constexpr int VT = KZ + KZ_BYTES, VT_BYTES = D * kXKeys * 2;  // [D channels][64 keys]
+  static constexpr int ZV = VT + VT_BYTES, ZV_BYTES = 16 * 128;   // [16 (groups, padded)][64 keys]
+  static constexpr int STAGE = ZV + ZV_BYTES;
+  static constexpr int ST0 = QZ + QZ_BYTES;
+  static constexpr int P_BYTES = kXRows * kXKeys * 2;
+  static constexpr int PHI = ST0 + 2 * STAGE, PLO = PHI + P_BYTES, PLO2 = PLO + P_BYTES;
+  static constexpr int RAW_BYTES = kXKeys * 3 * D / 4;           // 64 INT2 tokens: codes and (scale, zero) of K, V
+  static constexpr int RAW0 = PLO2 + P_BYTES;
+  static constexpr int BAR = RAW0 + 2 * RAW_BYTES;
+  static constexpr int BYTES = BAR + 4 * 8 + 16;                 // s_full[2], pv_done, spare; tmem slot, abort
+  static constexpr int SMEM = BYTES + 1024;
+  // epilogue reuse (after the last MMA): R_V^T [D][D] f32 over the Q planes, y [128][D+1] f32
+  // over the stages, 1/l [128] over the P planes
+  static constexpr int RT = 0, Y = ST0, LINV = PHI;
+  static constexpr int YS = D + 1;
+  // TMEM columns
+  static constexpr uint32_t C_S = 0, C_OROT = 2 * kXKeys, C_OPLAIN = C_OROT + D, C_OZ = C_OPLAIN + D;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(STAGE % 1024 == 0 && ST0 % 1024 == 0 && PHI % 1024 == 0, "operand tiles 1024-aligned");
+  static_assert(C_OZ + 32 <= TMEM_COLS, "TMEM plan");
+  static_assert(D * (D + 0) * 4 <= ST0, "R_V^T fits over the Q planes");
+  static_assert(kXRows * YS * 4 <= 2 * STAGE, "y fits over the stages");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+};
+
+// ------------------------------------------------------------------ query rotation
+// q' = q R_K for every (chunk token, query head) row, float32, into the workspace; the
+// last CTA writes R_V^T for the epilogues.  CTA: 64 rows x D columns, thread (row t/4,
+// column quarter t%4).
+template <int D>
+__global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
+  extern __shared__ __align__(16) float xq_sm[];
+  float* Rs = xq_sm;              // [D][D]
+  float* qs = xq_sm + D * D;      // [64][D]
+  const int t = threadIdx.x;
+  const long long rows = (long long)a.total_tokens * a.g.Hq;
+  float* qrot = reinterpret_cast<float*>(a.ws + a.qrot_off);
+  if (blockIdx.x == gridDim.x - 1) {
+    float* rvt = reinterpret_cast<float*>(a.ws + a.rvt_off);
+    for (int idx = t; idx < D * D; idx += 256) {
+      const int i = idx / D, j = idx % D;   // rvt[i][j] = R_V[j][i]; coalesced writes
+      rvt[idx] = __ldg(a.R_V + (size_t)j * D + i);
+    }
+    return;
+  }
+  for (int idx = t; idx < D * D / 4; idx += 256)
+    reinterpret_cast<float4*>(Rs)[idx] = __ldg(reinterpret_cast<const float4*>(a.R_K) + idx);
+  const long long r0 = (long long)blockIdx.x * 64;
+  for (int idx = t; idx < 64 * D; idx += 256) {
+    const long long r = r0 + idx / D;
+    float v = 0.f;
+    if (r < rows) {
+      const size_t e = (size_t)r * D + idx % D;
+      v = a.q_dtype == kDtypeBF16 ? __uint_as_float((uint32_t) static_cast<const uint16_t*>(a.q)[e] << 16)
+                                  : static_cast<const float*>(a.q)[e];
+    }
+    qs[idx] = v;
+  }
+  __syncthreads();
+  constexpr int NC = D / 4;
+  const int rr = t >> 2, cq = t & 3;
+  float acc[NC];
+#pragma unroll
+  for (int j = 0; j < NC; ++j) acc[j] = 0.f;
+  const float* qrow = qs + rr * D;
+#pragma unroll 4
+  for (int i = 0; i < D; ++i) {
+    const float qi = qrow[i];
+    const float4* rrow = reinterpret_cast<const float4*>(Rs + i * D + cq * NC);
+#pragma unroll
+    for (int j4 = 0; j4 < NC / 4; ++j4) {
+      const float4 rv = rrow[j4];
+      acc[4 * j4] = fmaf(qi, rv.x, acc[4 * j4]);
+      acc[4 * j4 + 1] = fmaf(qi, rv.y, acc[4 * j4 + 1]);
+      acc[4 * j4 + 2] = fmaf(qi, rv.z, acc[4 * j4 + 2]);
+      acc[4 * j4 + 3] = fmaf(qi, rv.w, acc[4 * j4 + 3]);
+    }
+  }
+  const long long r = r0 + rr;
+  if (r < rows) {
+    float4* dst = reinterpret_cast<float4*>(qrot + (size_t)r * D + cq * NC);
+#pragma unroll
+    for (int j4 = 0; j4 < NC / 4; ++j4)
+      dst[j4] = make_float4(acc[4 * j4], acc[4 * j4 + 1], acc[4 * j4 + 2], acc[4 * j4 + 3]);
+  }
+}
+
+// ------------------------------------------------------------------ attention
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// named barrier 1 among the 128 unpack threads
+__device__ __forceinline__ void unpack_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t half2_bits(float lo_elem, float hi_elem) { return pack_half2(lo_elem, hi_elem); }
+__device__ __forceinline__ float bf16_round_f(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+// 2^e for e in the float32 normal range
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
+// f16 pair (1.5 * 2^(pos - 10), same): the centring constant of a code slot at bit pos
+__host__ __device__ constexpr uint32_t centre_pair(int pos) {
+  // f16 of 1.5 * 2^(pos - 10): exponent field pos - 10 + 15, mantissa 0x200
+  return ((uint32_t)((pos + 5) << 10 | 0x200)) * 0x10001u;
+}
+// r = s * c * 2^(pos - 10) (from scale_codes with n2 = -s) -> s * (c - 1.5) * 2^(pos - 10),
+// one f16 fused multiply-add per pair, exact (the result has at most 10 significant bits)
+__device__ __forceinline__ uint32_t centre_codes(uint32_t r, uint32_t n2, uint32_t kc) {
+  const __half2 rv = *reinterpret_cast<const __half2*>(&r);
+  const __half2 nv = *reinterpret_cast<const __half2*>(&n2);
+  const __half2 cv = *reinterpret_cast<const __half2*>(&kc);
+  const __half2 o = __hfma2(nv, cv, rv);
+  return *reinterpret_cast<const uint32_t*>(&o);
+}
+// group centre m = z + 1.5 s (from a (scale, zero) word) times 2^k as f16 hi + lo (exact)
+__device__ __forceinline__ void centre_hi_lo(uint32_t w, uint32_t k23, __half& hi, __half& lo) {
+  const float m = zero_times_pow2(w, k23) + 1.5f * scale_times_pow2(w, k23);
+  hi = __float2half_rn(m);
+  lo = __float2half_rn(m - __half2float(hi));
+}
+__device__ __forceinline__ uint32_t hpair(__half a, __half b) {
+  return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+}
+// centre-term columns: term t pairs query term kCentreQ[t] (0 hi, 1 lo, 2 lo2 of Q_g) with
+// centre term kCentreZ[t] (0 hi, 1 lo of m); G groups per term, 16 columns in all
+__device__ constexpr int kCentreQ[5] = {0, 1, 0, 2, 1};
+__device__ constexpr int kCentreZ[5] = {0, 0, 1, 0, 1};
+template <int G>
+__host__ __device__ constexpr int kCentreTerms() { return 16 / G < 5 ? 16 / G : 5; }
+
+// What one CTA walks: nR INT2 tiles (positions 64u, u >= u0), nW window tiles (slab
+// slots 64w), nC chunk tiles (chunk keys 64c).
+struct XTiles {
+  int nR, nW, nC, u0;
+  int S, hist_end, n_sink, n_rec;   // history [S, hist_end); window slots [0, n_sink) and [S, S + n_rec)
+  __device__ int n() const { return nR + nW + nC; }
+  __device__ int kind(int j) const { return j < nR ? kTileInt2 : (j < nR + nW ? kTileWindow : kTileChunk); }
+  __device__ int base(int j) const {
+    return j < nR ? 64 * (u0 + j) : (j < nR + nW ? 64 * (j - nR) : 64 * (j - nR - nW));
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a) {
+  using L = XLayout<D>;
+  constexpr int G = L::G;
+  extern __shared__ __align__(1024) uint8_t x_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(x_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(smem + L::BAR);   // [2]
+  uint64_t* pv_done = s_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR + 32);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR + 36);
+
+  const Geom& g = a.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int gq = g.gq();
+  const int tq = kXRows / gq;                 // chunk tokens per CTA
+  const int i0 = blockIdx.x * tq;
+  const int c0 = a.cu_seqlens[b];
+  const int len = a.cu_seqlens[b + 1] - c0;
+  if (i0 >= len) return;
+  const int n_pre = a.prefix_lens[b];
+  if (n_pre < 0 || (long long)n_pre > (long long)g.max_pages_per_req * g.P) {
+    if (tid == 0) flag_error(a.status, kDevBadLen);
+    return;
+  }
+  XTiles tl;
+  tl.S = g.S;
+  tl.hist_end = max(g.S, n_pre - g.W);
+  tl.n_sink = min(g.S, n_pre);
+  tl.n_rec = n_pre > g.S ? n_pre - max(g.S, n_pre - g.W) : 0;
+  if (tl.hist_end > g.S) {
+    tl.u0 = g.S / 64;
+    tl.nR = (tl.hist_end - 1) / 64 - tl.u0 + 1;
+  } else {
+    tl.u0 = 0;
+    tl.nR = 0;
+  }
+  const int win_end = tl.n_rec > 0 ? g.S + tl.n_rec : tl.n_sink;
+  tl.nW = (win_end + 63) / 64;
+  const int kend = min(len, i0 + tq);
+  tl.nC = (kend + 63) / 64;
+  const int n_tiles = tl.n();
+  int req = 0;
+  if (tl.nW > 0) {
+    req = a.req_slot[b];
+    if (req < 0 || req >= g.max_req) {
+      if (tid == 0) flag_error(a.status, kDevBadSlot);
+      return;
+    }
+  }
+
+  const uint32_t kK23 = static_cast<uint32_t>(a.k_exp_K) << 23;
+  const uint32_t kV23 = static_cast<uint32_t>(a.k_exp_V) << 23;
+  const uint8_t* pool_l = a.pool + (size_t)a.layer * g.layer_pool_bytes();
+  const size_t BB = g.block_bytes();
+  const uint16_t* slab_req =
+      a.slab + ((size_t)a.layer * g.max_req + req) * g.slab_req_elems() + (size_t)kvh * 2 * g.window() * D;
+
+  // ---------------- setup: barriers, TMEM, Zv padding rows
+  if (warp == 8) {
+    if (lane == 0) {
+      mbar_init(&s_full[0], 1);
+      mbar_init(&s_full[1], 1);
+      mbar_init(pv_done, 1);
+      *abort_flag = 0;
+      fence_barrier_init();
+    }
+    __syncwarp();
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+  }
+  // rows 2G..15 of both stages' Zv tiles stay zero (padding of the V centre term)
+  for (int idx = tid; idx < 2 * (16 - 2 * G) * 8; idx += kXThreads) {
+    const int st = idx / ((16 - 2 * G) * 8), rem = idx % ((16 - 2 * G) * 8);
+    const int row = 2 * G + rem / 8, ck = rem % 8;
+    *reinterpret_cast<uint4*>(smem + L::ST0 + st * L::STAGE + L::ZV + sw128_offset(row, 8 * ck, 16)) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---------------- per-row state of the softmax threads (warps 0-3: row r = tid)
+  const int r = tid & (kXRows - 1);
+  const int qi = i0 + r / gq;
+  const bool row_ok = qi < len;
+  const size_t qrow = (size_t)(c0 + (row_ok ? qi : i0)) * g.Hq + (size_t)kvh * gq + r % gq;
+  const float sm_log2 = kXLog2e * rsqrtf((float)D);
+  float F_rot = 0.f;
+  const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+
+  // Q planes for INT2 tiles: q' * 2^(e + 10 - pos) as f16 hi + lo, and the group sums
+  // Q_g * 2^e as three f16 terms; |q'| * 2^e < 32 keeps every operand below 2^15.
+  auto write_q_rot = [&]() {
+    const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.ws + a.qrot_off) + qrow * D);
+    float mx = 0.f, qg[G];
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) qg[gg] = 0.f;
+    if (row_ok) {
+#pragma unroll 8
+      for (int c = 0; c < D / 4; ++c) {
+        const float4 v = src[c];
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        qg[c / 8] += (v.x + v.y) + (v.z + v.w);
+      }
+    }
+    int e = 0;
+    if (mx > 0.f) {
+      int E;
+      frexpf(mx, &E);
+      e = 5 - E;
+    }
+    F_rot = ldexpf(sm_log2, -e - a.k_exp_K);
+#pragma unroll 2
+    for (int m = 0; m < D / 8; ++m) {
+      const float f = ldexpf(1.f, e + 10 - slot_pos(m & 7));
+      float v[8];
+      if (row_ok) {
+        const float4 x0 = src[2 * m], x1 = src[2 * m + 1];
+        v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = 0.f;
+      }
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float x0 = v[2 * k] * f, x1 = v[2 * k + 1] * f;
+        hi[k] = half2_bits(x0, x1);
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
+        lo[k] = half2_bits(x0 - hf.x, x1 - hf.y);
+      }
+      const uint32_t off = sw128_offset(r, 8 * m, kXRows);
+      *reinterpret_cast<uint4*>(smem + L::QHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(smem + L::QLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    __half hz[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) hz[k] = __float2half_rn(0.f);
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+      const float x = ldexpf(qg[gg], e);
+      const __half h1 = __float2half_rn(x);
+      const float r1 = x - __half2float(h1);
+      const __half h2 = __float2half_rn(r1);
+      const __half h3 = __float2half_rn(r1 - __half2float(h2));
+      const __half qt[3] = {h1, h2, h3};
+#pragma unroll
+      for (int tt = 0; tt < kCentreTerms<G>(); ++tt) hz[tt * G + gg] = qt[kCentreQ[tt]];
+    }
+    const uint4* hz4 = reinterpret_cast<const uint4*>(hz);
+    *reinterpret_cast<uint4*>(smem + L::QZ + sw128_offset(r, 0, kXRows)) = hz4[0];
+    *reinterpret_cast<uint4*>(smem + L::QZ + sw128_offset(r, 8, kXRows)) = hz4[1];
+  };
+  // Q planes for BF16 tiles: q as BF16 hi + lo (16 bits)
+  auto write_q_plain = [&]() {
+#pragma unroll 2
+    for (int m = 0; m < D / 8; ++m) {
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = 0.f;
+      if (row_ok) {
+        if (a.q_dtype == kDtypeBF16) {
+          const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + qrow * D + 8 * m);
+          const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v[2 * k] = bf16_lo(ws4[k]);
+            v[2 * k + 1] = bf16_hi(ws4[k]);
+          }
+        } else {
+          const float4* s4 = reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + qrow * D + 8 * m);
+          const float4 x0 = s4[0], x1 = s4[1];
+          v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+        }
+      }
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float h0 = bf16_round_f(v[2 * k]), h1 = bf16_round_f(v[2 * k + 1]);
+        hi[k] = pack_bf162(h0, h1);
+        lo[k] = pack_bf162(v[2 * k] - h0, v[2 * k + 1] - h1);
+      }
+      const uint32_t off = sw128_offset(r, 8 * m, kXRows);
+      *reinterpret_cast<uint4*>(smem + L::QHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(smem + L::QLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+  };
+
+  // ---------------- unpack threads (warps 4-7: u = tid - 128)
+  const int u = tid - 128;
+  auto hist_ok = [&](int t) { return t >= tl.S && t < tl.hist_end; };
+  // INT2 pages of tile j into raw buffer j & 1 (one cp.async group per call, possibly empty)
+  auto issue_raw = [&](int j) {
+    if (j < n_tiles && tl.kind(j) == kTileInt2) {
+      const int base = tl.base(j);
+      uint8_t* dst0 = smem + L::RAW0 + (j & 1) * L::RAW_BYTES;
+      for (int bi = 0; bi < kXKeys / g.P; ++bi) {
+        const int p0 = base + bi * g.P;
+        if (p0 + g.P <= tl.S || p0 >= tl.hist_end) continue;
+        const int lp = p0 / g.P;
+        int page = -1;
+        if (lp < a.bt_stride && lp < g.max_pages_per_req) page = a.block_table[(size_t)b * a.bt_stride + lp];
+        if (page < 0 || page >= g.num_pages) {
+          if (u == 0) flag_error(a.status, kDevBadPage);
+          continue;
+        }
+        const uint8_t* src = pool_l + ((size_t)page * g.Hkv + kvh) * BB;
+        uint8_t* dst = dst0 + bi * BB;
+        for (int c = u; c < (int)(BB / 16); c += 128) cp_async16(dst + 16 * c, src + 16 * c);
+      }
+    }
+    cp_async_commit();
+  };
+  auto unpack_int2 = [&](int j, uint8_t* stg) {
+    const int base = tl.base(j);
+    const uint8_t* raw = smem + L::RAW0 + (j & 1) * L::RAW_BYTES;
+    const uint32_t magic = a.code_magic;
+    // K codes -> code * s * 2^(k_K + pos - 10); thread (key, w) writes channels [64w, 64w + 64)
+    if (u < kXKeys * (D / 64)) {
+      const int key = u / (D / 64), w = u % (D / 64);
+      const bool ok = hist_ok(base + key);
+      const uint8_t* kb = raw + (key / g.P) * BB;
+      const int slot = key % g.P;
+      uint32_t wd[4], w6[4];
+#pragma unroll
+      for (int tg = 0; tg < 4; ++tg) {
+        wd[tg] = *reinterpret_cast<const uint32_t*>(kb + slot * (D / 4) + (tg * (D / 64) + w) * 4);
+        w6[tg] = wd[tg] >> 6;
+      }
+      uint32_t szw[G];
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg)
+        szw[gg] = *reinterpret_cast<const uint32_t*>(kb + g.k_sz_off() + slot * (D / 8) + gg * 4);
+      const uint32_t sA = (D == 128 && w) ? szw[G - 2] : szw[0];
+      const uint32_t sB = (D == 128 && w) ? szw[G - 1] : szw[1];
+      const uint32_t nA = ok ? half2_bits(neg_scale_times_pow2(sA, kK23), neg_scale_times_pow2(sA, kK23)) : 0u;
+      const uint32_t nB = ok ? half2_bits(neg_scale_times_pow2(sB, kK23), neg_scale_times_pow2(sB, kK23)) : 0u;
+      static_for<8>([&](auto X) {
+        constexpr int x = decltype(X)::value;
+        const uint32_t n2 = x < 4 ? nA : nB;
+        constexpr uint32_t kc = centre_pair(slot_pos(x));
+        uint4 c;
+        c.x = centre_codes(scale_codes(magic_slot<x>(wd[0], w6[0], magic), n2), n2, kc);
+        c.y = centre_codes(scale_codes(magic_slot<x>(wd[1], w6[1], magic), n2), n2, kc);
+        c.z = centre_codes(scale_codes(magic_slot<x>(wd[2], w6[2], magic), n2), n2, kc);
+        c.w = centre_codes(scale_codes(magic_slot<x>(wd[3], w6[3], magic), n2), n2, kc);
+        *reinterpret_cast<uint4*>(stg + L::KT + sw128_offset(key, 8 * (8 * w + x), kXKeys)) = c;
+      });
+      if (w == 0) {
+        __half hz[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) hz[k] = __float2half_rn(0.f);
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          __half mh, ml;
+          centre_hi_lo(ok ? szw[gg] : 0u, kK23, mh, ml);
+          const __half mt[2] = {mh, ml};
+#pragma unroll
+          for (int tt = 0; tt < kCentreTerms<G>(); ++tt) hz[tt * G + gg] = mt[kCentreZ[tt]];
+        }
+        const uint4* hz4 = reinterpret_cast<const uint4*>(hz);
+        *reinterpret_cast<uint4*>(stg + L::KZ + sw128_offset(key, 0, kXKeys)) = hz4[0];
+        *reinterpret_cast<uint4*>(stg + L::KZ + sw128_offset(key, 8, kXKeys)) = hz4[1];
+      }
+    }
+    // V codes -> code * s_V * 2^(k_V + pos - 10), transposed: thread (half-word hw, keys 8kb..8kb+7)
+    if (u < (D / 8) * 8) {
+      const int hw = u % (D / 8), kb8 = u / (D / 8);
+      const int chbase = 64 * (hw % (D / 64)) + hw / (D / 64);
+      const int gA = chbase / 32;
+      uint32_t W[4], W6[4], nA[4], nB[4];
+      __half zh[8][G], zl[8][G];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        uint32_t hv[2];
+        float sa[2], sb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = 8 * kb8 + 2 * p + e;
+          const bool ok = hist_ok(base + key);
+          const uint8_t* vb = raw + (key / g.P) * BB;
+          const int slot = key % g.P;
+          hv[e] = *reinterpret_cast<const uint16_t*>(vb + g.v_codes_off() + slot * (D / 4) + hw * 2);
+          const uint32_t* szr = reinterpret_cast<const uint32_t*>(vb + g.v_sz_off() + slot * (D / 8));
+          sa[e] = ok ? neg_scale_times_pow2(szr[gA], kV23) : 0.f;
+          sb[e] = ok ? neg_scale_times_pow2(szr[gA + 1], kV23) : 0.f;
+#pragma unroll
+          for (int gg = 0; gg < G; ++gg) centre_hi_lo(ok ? szr[gg] : 0u, kV23, zh[2 * p + e][gg], zl[2 * p + e][gg]);
+        }
+        W[p] = hv[0] | (hv[1] << 16);
+        W6[p] = W[p] >> 6;
+        nA[p] = half2_bits(sa[0], sa[1]);
+        nB[p] = half2_bits(sb[0], sb[1]);
+      }
+      static_for<8>([&](auto X) {
+        constexpr int s = decltype(X)::value;
+        constexpr uint32_t kc = centre_pair(slot_pos(s));
+        uint4 c;
+        c.x = centre_codes(scale_codes(magic_slot<s>(W[0], W6[0], magic), s < 4 ? nA[0] : nB[0]), s < 4 ? nA[0] : nB[0], kc);
+        c.y = centre_codes(scale_codes(magic_slot<s>(W[1], W6[1], magic), s < 4 ? nA[1] : nB[1]), s < 4 ? nA[1] : nB[1], kc);
+        c.z = centre_codes(scale_codes(magic_slot<s>(W[2], W6[2], magic), s < 4 ? nA[2] : nB[2]), s < 4 ? nA[2] : nB[2], kc);
+        c.w = centre_codes(scale_codes(magic_slot<s>(W[3], W6[3], magic), s < 4 ? nA[3] : nB[3]), s < 4 ? nA[3] : nB[3], kc);
+        *reinterpret_cast<uint4*>(stg + L::VT + sw128_offset(chbase + 8 * s, 8 * kb8, D)) = c;
+      });
+      if (hw == 0) {
+        // rows g: centre hi, rows G + g: centre lo, keys 8kb..8kb+7
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          const uint4 ch4 = make_uint4(hpair(zh[0][gg], zh[1][gg]), hpair(zh[2][gg], zh[3][gg]),
+                                       hpair(zh[4][gg], zh[5][gg]), hpair(zh[6][gg], zh[7][gg]));
+          const uint4 cl4 = make_uint4(hpair(zl[0][gg], zl[1][gg]), hpair(zl[2][gg], zl[3][gg]),
+                                       hpair(zl[4][gg], zl[5][gg]), hpair(zl[6][gg], zl[7][gg]));
+          *reinterpret_cast<uint4*>(stg + L::ZV + sw128_offset(gg, 8 * kb8, 16)) = ch4;
+          *reinterpret_cast<uint4*>(stg + L::ZV + sw128_offset(G + gg, 8 * kb8, 16)) = cl4;
+        }
+      }
+    }
+  };
+  // BF16 window or chunk tile: K rows copied into the swizzled K tile, V rows transposed
+  auto plain_row = [&](int kind, int base, int key, int kv) -> const uint16_t* {
+    if (kind == kTileWindow) {
+      const int slot = base + key;
+      const bool ok = slot < tl.n_sink || (slot >= tl.S && slot < tl.S + tl.n_rec);
+      return ok ? slab_req + ((size_t)kv * g.window() + slot) * D : nullptr;
+    }
+    const int kc = base + key;
+    if (kc >= kend) return nullptr;
+    const uint16_t* src = kv ? a.V_new : a.K_new;
+    return src + ((size_t)(c0 + kc) * g.Hkv + kvh) * D;
+  };
+  auto unpack_plain = [&](int j, uint8_t* stg) {
+    const int kind = tl.kind(j), base = tl.base(j);
+    constexpr int KI = kXKeys * (D / 8) / 128;   // 16-byte K pieces per thread
+    uint4 kv[KI];
+#pragma unroll
+    for (int m = 0; m < KI; ++m) {
+      const int item = u + 128 * m;
+      const int key = item / (D / 8), cc = item % (D / 8);
+      const uint16_t* row = plain_row(kind, base, key, 0);
+      kv[m] = row ? *reinterpret_cast<const uint4*>(row + 8 * cc) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint4 vr[8];
+    const bool vt = u < D;   // thread (channel block hw8, keys 8kb..8kb+7)
+    const int hw8 = u % (D / 8), kb8 = u / (D / 8);
+    if (vt) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint16_t* row = plain_row(kind, base, 8 * kb8 + k, 1);
+        vr[k] = row ? *reinterpret_cast<const uint4*>(row + 8 * hw8) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < KI; ++m) {
+      const int item = u + 128 * m;
+      const int key = item / (D / 8), cc = item % (D / 8);
+      *reinterpret_cast<uint4*>(stg + L::KT + sw128_offset(key, 8 * cc, kXKeys)) = kv[m];
+    }
+    if (vt) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+        uint32_t c[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const uint4 x = vr[2 * p], y = vr[2 * p + 1];
+          const uint32_t xs = (e >> 1) == 0 ? x.x : ((e >> 1) == 1 ? x.y : ((e >> 1) == 2 ? x.z : x.w));
+          const uint32_t ys = (e >> 1) == 0 ? y.x : ((e >> 1) == 1 ? y.y : ((e >> 1) == 2 ? y.z : y.w));
+          c[p] = prmt(xs, ys, sel);
+        }
+        *reinterpret_cast<uint4*>(stg + L::VT + sw128_offset(8 * hw8 + e, 8 * kb8, D)) =
+            make_uint4(c[0], c[1], c[2], c[3]);
+      }
+    }
+  };
+  auto unpack = [&](int j) {
+    uint8_t* stg = smem + L::ST0 + (j & 1) * L::STAGE;
+    if (tl.kind(j) == kTileInt2) unpack_int2(j, stg); else unpack_plain(j, stg);
+  };
+
+  // ---------------- MMA issue (warp 8, lane 0)
+  const uint32_t sbase = smem_u32(smem);
+  auto issue_qk = [&](int j) {
+    const uint32_t stg = sbase + L::ST0 + (uint32_t)((j & 1) * L::STAGE);
+    const uint32_t dS = tmem + L::C_S + (uint32_t)((j & 1) * kXKeys);
+    const bool rot = tl.kind(j) == kTileInt2;
+    const uint32_t idesc = rot ? idesc_f16_f32(kXRows, kXKeys) : idesc_bf16_f32(kXRows, kXKeys);
+    // a BF16 query has no lo part: the plain tiles skip that plane
+    const int planes = (rot || a.q_dtype != kDtypeBF16) ? 2 : 1;
+#pragma unroll
+    for (int pl = 0; pl < 2; ++pl)
+      if (pl < planes)
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ak = (uint32_t)((kk >> 2) * kXRows * 128 + (kk & 3) * 32);
+        const uint32_t bk = (uint32_t)((kk >> 2) * kXKeys * 128 + (kk & 3) * 32);
+        tc_mma(dS, smem_desc_sw128(sbase + (pl ? L::QLO : L::QHI) + ak), smem_desc_sw128(stg + L::KT + bk), idesc,
+               (pl | kk) ? 1u : 0u);
+      }
+    if (rot) tc_mma(dS, smem_desc_sw128(sbase + L::QZ), smem_desc_sw128(stg + L::KZ), idesc, 1u);
+  };
+  auto issue_pv = [&](int j) {
+    const uint32_t stg = sbase + L::ST0 + (uint32_t)((j & 1) * L::STAGE);
+    if (tl.kind(j) == kTileInt2) {
+#pragma unroll
+      for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+        for (int kk = 0; kk < kXKeys / 16; ++kk) {
+          const uint64_t pa = smem_desc_sw128(sbase + (pl ? L::PLO : L::PHI) + kk * 32);
+          tc_mma(tmem + L::C_OROT, pa, smem_desc_sw128(stg + L::VT + kk * 32), idesc_f16_f32(kXRows, D), 1u);
+          tc_mma(tmem + L::C_OZ, pa, smem_desc_sw128(stg + L::ZV + kk * 32), idesc_f16_f32(kXRows, 16), 1u);
+        }
+    } else {
+      // P as three BF16 terms (24 bits): window and chunk values are unbounded BF16
+#pragma unroll
+      for (int pl = 0; pl < 3; ++pl)
+#pragma unroll
+        for (int kk = 0; kk < kXKeys / 16; ++kk)
+          tc_mma(tmem + L::C_OPLAIN, smem_desc_sw128(sbase + (pl == 0 ? L::PHI : (pl == 1 ? L::PLO : L::PLO2)) + kk * 32),
+                 smem_desc_sw128(stg + L::VT + kk * 32), idesc_bf16_f32(kXRows, D), 1u);
+    }
+  };
+
+  // ---------------- softmax of tile i (warps 0-3); false on a wait timeout
+  float m_ref = -INFINITY, thr = -INFINITY, l_run = 0.f;
+  auto softmax_tile = [&](int i) -> bool {
+    const int kind = tl.kind(i), base = tl.base(i);
+    if (!mbar_wait_bounded(&s_full[i & 1], (uint32_t)(i >> 1) & 1, a.status)) return false;
+    tc_fence_after();
+    uint32_t s0[32], s1[32];
+    tmem_ld32_nowait(lane_base + L::C_S + (uint32_t)((i & 1) * kXKeys), s0);
+    tmem_ld32_nowait(lane_base + L::C_S + (uint32_t)((i & 1) * kXKeys + 32), s1);
+    tmem_wait_ld();
+    // the last INT2 tile's scores are read: the Q planes take the plain query for the BF16 tiles
+    if (i == tl.nR - 1) write_q_plain();
+    int a0 = 0, a1 = 0, b0 = 0, b1 = 0;   // visible keys [a0, a1) U [b0, b1)
+    if (kind == kTileInt2) {
+      a0 = max(0, tl.S - base);
+      a1 = min(kXKeys, tl.hist_end - base);
+    } else if (kind == kTileWindow) {
+      a1 = min(kXKeys, tl.n_sink - base);
+      b0 = max(0, tl.S - base);
+      b1 = min(kXKeys, tl.S + tl.n_rec - base);
+    } else {
+      a1 = min(kXKeys, qi - base + 1);
+    }
+    const float F = kind == kTileInt2 ? F_rot : sm_log2;
+    float sc[kXKeys];
+    float mloc = -INFINITY;
+#pragma unroll
+    for (int jj = 0; jj < kXKeys; ++jj) {
+      const float v = __uint_as_float(jj < 32 ? s0[jj] : s1[jj - 32]) * F;
+      const bool vis = (jj >= a0 && jj < a1) || (jj >= b0 && jj < b1);
+      sc[jj] = vis ? v : -INFINITY;
+      mloc = fmaxf(mloc, sc[jj]);
+    }
+    float alpha = 1.f;
+    if (mloc > thr) {
+      const float nm = mloc - kXWeightShift;
+      alpha = ex2(m_ref - nm);
+      m_ref = nm;
+      thr = nm + kXWeightShift + kXRescaleLog2;
+    }
+    // the P buffer and the accumulators are free once the previous tile's PV is done
+    if (i >= 1 && !mbar_wait_bounded(pv_done, (uint32_t)((i - 1) & 1), a.status)) return false;
+    tc_fence_after();
+    const bool resc = alpha != 1.f && l_run > 0.f;
+    if (__any_sync(0xffffffffu, resc)) {
+      const float f = resc ? alpha : 1.f;
+#pragma unroll 1
+      for (uint32_t c = L::C_OROT; c < L::C_OZ + 32; c += 32) {
+        uint32_t o[32];
+        tmem_ld32_nowait(lane_base + c, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+        tmem_st32(lane_base + c, o);
+      }
+      tmem_wait_st();
+    }
+    l_run *= alpha;
+    if (m_ref == -INFINITY) m_ref = 0.f;   // no visible key yet: every weight of this tile is 0
+    float lsum = 0.f;
+    if (kind == kTileInt2) {
+#pragma unroll
+      for (int c = 0; c < kXKeys / 8; ++c) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float p0 = ex2(sc[8 * c + 2 * k] - m_ref), p1 = ex2(sc[8 * c + 2 * k + 1] - m_ref);
+          hi[k] = half2_bits(p0, p1);
+          const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
+          lo[k] = half2_bits(p0 - hf.x, p1 - hf.y);
+          const float2 lf = __half22float2(*reinterpret_cast<const __half2*>(&lo[k]));
+          lsum += (hf.x + lf.x) + (hf.y + lf.y);
+        }
+        const uint32_t off = sw128_offset(r, 8 * c, kXRows);
+        *reinterpret_cast<uint4*>(smem + L::PHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(smem + L::PLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < kXKeys / 8; ++c) {
+        uint32_t hi[4], lo[4], lo2[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float p0 = ex2(sc[8 * c + 2 * k] - m_ref), p1 = ex2(sc[8 * c + 2 * k + 1] - m_ref);
+          const float h0 = bf16_round_f(p0), h1 = bf16_round_f(p1);
+          const float l0 = bf16_round_f(p0 - h0), l1 = bf16_round_f(p1 - h1);
+          const float m0 = bf16_round_f(p0 - h0 - l0), m1 = bf16_round_f(p1 - h1 - l1);
+          hi[k] = pack_bf162(h0, h1);
+          lo[k] = pack_bf162(l0, l1);
+          lo2[k] = pack_bf162(m0, m1);
+          lsum += ((h0 + l0) + m0) + ((h1 + l1) + m1);
+        }
+        const uint32_t off = sw128_offset(r, 8 * c, kXRows);
+        *reinterpret_cast<uint4*>(smem + L::PHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(smem + L::PLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(smem + L::PLO2 + off) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+      }
+    }
+    l_run += lsum;
+    return true;
+  };
+
+  // ---------------- preamble: zero the output accumulators, query planes, first tile
+  if (warp < 4) {
+    uint32_t z[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) z[k] = 0u;
+#pragma unroll 1
+    for (uint32_t c = L::C_OROT; c < L::C_OZ + 32; c += 32) tmem_st32(lane_base + c, z);
+    tmem_wait_st();
+    if (tl.nR > 0) write_q_rot(); else write_q_plain();
+  } else if (warp < 8) {
+    issue_raw(0);
+    issue_raw(1);
+    cp_async_wait1();
+    unpack_bar();
+    unpack(0);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  int committed = 0;               // MMA thread: 1 = s_full, 2 = pv_done last committed
+  int last_i = 0;
+  if (warp == 8 && lane == 0) {
+    issue_qk(0);
+    tc_commit(&s_full[0]);
+    committed = 1;
+  }
+
+  // ---------------- main loop: one CTA barrier per tile
+  bool aborted = false;
+  for (int i = 0; i < n_tiles; ++i) {
+    bool ok = true;
+    if (warp < 4) {
+      ok = softmax_tile(i);
+    } else if (warp < 8) {
+      if (i + 1 < n_tiles) {
+        issue_raw(i + 2);
+        // stage (i + 1) & 1 was last read by tile i - 1's MMAs
+        if (i >= 1) ok = mbar_wait_bounded(pv_done, (uint32_t)((i - 1) & 1), a.status);
+        cp_async_wait1();
+        unpack_bar();
+        if (ok) unpack(i + 1);
+      }
+    }
+    if (!ok) *abort_flag = 1;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (*abort_flag) {
+      aborted = true;
+      break;
+    }
+    if (warp == 8 && lane == 0) {
+      if (i + 1 < n_tiles) {
+        issue_qk(i + 1);
+        tc_commit(&s_full[(i + 1) & 1]);
+      }
+      issue_pv(i);
+      tc_commit(pv_done);
+      committed = 2;
+      last_i = i;
+    }
+  }
+
+  if (aborted) {
+    // drain: every issued MMA and copy completes before the CTA releases TMEM and exits
+    if (warp == 8 && lane == 0) {
+      if (committed == 2) (void)mbar_wait_bounded(pv_done, (uint32_t)(last_i & 1), nullptr);
+      else if (committed == 1) (void)mbar_wait_bounded(&s_full[0], 0u, nullptr);
+    }
+    if (warp >= 4 && warp < 8) cp_async_wait0();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) tmem_dealloc(tmem, L::TMEM_COLS);
+    return;
+  }
+
+  // ---------------- epilogue: out = (O_plain + y R_V^T) / l
+  bool ok = true;
+  if (warp >= 4 && warp < 8) cp_async_wait0();
+  if (warp < 8) {
+    ok = mbar_wait_bounded(pv_done, (uint32_t)((n_tiles - 1) & 1), a.status);
+    tc_fence_after();
+  }
+  float* Rt = reinterpret_cast<float*>(smem + L::RT);
+  float* Y = reinterpret_cast<float*>(smem + L::Y);
+  float* linv = reinterpret_cast<float*>(smem + L::LINV);
+  const int half = (tid >> 7) & 1;
+  constexpr int NJ = D / 2;
+  const int j0 = half * NJ;
+  if (warp < 8) {
+    const float4* rvt = reinterpret_cast<const float4*>(a.ws + a.rvt_off);
+    for (int idx = tid; idx < D * D / 4; idx += 256) reinterpret_cast<float4*>(Rt)[idx] = rvt[idx];
+    if (warp < 4) linv[r] = l_run > 0.f ? 1.f / l_run : 0.f;
+    // y: the rotated accumulator at value scale, this thread's half of row r
+    uint32_t oz[32];
+    tmem_ld32_nowait(lane_base + L::C_OZ, oz);
+    tmem_wait_ld();
+#pragma unroll
+    for (int cb = 0; cb < NJ / 32; ++cb) {
+      uint32_t o[32];
+      tmem_ld32_nowait(lane_base + L::C_OROT + (uint32_t)(j0 + 32 * cb), o);
+      tmem_wait_ld();
+      const int gidx = (j0 >> 5) + cb;   // this block's group
+      float zsel = 0.f;
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg)
+        zsel = gg == gidx ? __uint_as_float(oz[gg]) + __uint_as_float(oz[G + gg]) : zsel;
+      const float zv = zsel * pow2f(-a.k_exp_V);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int ch = j0 + 32 * cb + k;
+        const float fch = pow2f(10 - slot_pos((ch % 64) / 8) - a.k_exp_V);
+        Y[r * L::YS + ch] = fmaf(__uint_as_float(o[k]), fch, zv);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp < 8) {
+    // the TMEM loads are warp-collective: every lane takes part, rows outside the chunk included
+    float acc[NJ];
+#pragma unroll
+    for (int cb = 0; cb < NJ / 32; ++cb) {
+      uint32_t o[32];
+      tmem_ld32_nowait(lane_base + L::C_OPLAIN + (uint32_t)(j0 + 32 * cb), o);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 32; ++k) acc[32 * cb + k] = __uint_as_float(o[k]);
+    }
+    const float* yr = Y + r * L::YS;
+#pragma unroll 2
+    for (int i = 0; i < D; ++i) {
+      const float yi = yr[i];
+      const float4* rt = reinterpret_cast<const float4*>(Rt + i * D + j0);
+#pragma unroll
+      for (int j4 = 0; j4 < NJ / 4; ++j4) {
+        const float4 rv = rt[j4];
+        acc[4 * j4] = fmaf(yi, rv.x, acc[4 * j4]);
+        acc[4 * j4 + 1] = fmaf(yi, rv.y, acc[4 * j4 + 1]);
+        acc[4 * j4 + 2] = fmaf(yi, rv.z, acc[4 * j4 + 2]);
+        acc[4 * j4 + 3] = fmaf(yi, rv.w, acc[4 * j4 + 3]);
+      }
+    }
+    const float li = linv[r];
+    if (!ok || !row_ok) {
+      // nothing to store
+    } else if (a.out_dtype == kDtypeF32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + qrow * D + j0);
+#pragma unroll
+      for (int j4 = 0; j4 < NJ / 4; ++j4)
+        dst[j4] = make_float4(acc[4 * j4] * li, acc[4 * j4 + 1] * li, acc[4 * j4 + 2] * li, acc[4 * j4 + 3] * li);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + qrow * D + j0);
+#pragma unroll
+      for (int j8 = 0; j8 < NJ / 8; ++j8)
+        dst[j8] = make_uint4(pack_bf162(acc[8 * j8] * li, acc[8 * j8 + 1] * li),
+                             pack_bf162(acc[8 * j8 + 2] * li, acc[8 * j8 + 3] * li),
+                             pack_bf162(acc[8 * j8 + 4] * li, acc[8 * j8 + 5] * li),
+                             pack_bf162(acc[8 * j8 + 6] * li, acc[8 * j8 + 7] * li));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
+template <int D>
+int launch_extend_d(const ExtendArgs& a, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long rows = (long long)a.total_tokens * a.g.Hq;
+  const size_t qsm = (size_t)(D * D + 64 * D) * sizeof(float);
+  cudaError_t e = ensure_smem_limit(extend_qrot_kernel<D>, qsm);
+  if (e != cudaSuccess) return (int)e;
+  const unsigned qgrid = (unsigned)((rows + 63) / 64) + 1;
+  extend_qrot_kernel<D><<<qgrid, 256, qsm, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  e = ensure_smem_limit(extend_attn_kernel<D>, XLayout<D>::SMEM);
+  if (e != cudaSuccess) return (int)e;
+  const int tq = kXRows / a.g.gq();
+  dim3 grid((unsigned)((a.max_chunk + tq - 1) / tq), (unsigned)a.g.Hkv, (unsigned)a.batch);
+  extend_attn_kernel<D><<<grid, kXThreads, XLayout<D>::SMEM, s>>>(a);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+size_t extend_workspace_bytes(const Geom& g, long long total_tokens) {
+  const size_t rvt = ((size_t)g.D * g.D * 4 + 255) & ~size_t(255);
+  return rvt + (size_t)total_tokens * g.Hq * g.D * 4;
+}
+
+void extend_ws_offsets(const Geom& g, size_t* rvt_off, size_t* qrot_off) {
+  *rvt_off = 0;
+  *qrot_off = ((size_t)g.D * g.D * 4 + 255) & ~size_t(255);
+}
+
+int launch_extend(const ExtendArgs& a, void* stream) {
+  if (a.total_tokens == 0 || a.batch == 0 || a.max_chunk == 0) return 0;
+  if (a.g.D == 128) return launch_extend_d<128>(a, stream);
+  return launch_extend_d<64>(a, stream);
+}
+
+}  // namespace oscar

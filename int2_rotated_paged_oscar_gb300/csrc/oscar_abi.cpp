@@ -833,6 +833,79 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
   return OSCAR_OK;
 }
 
+// ---------------------------------------------------------------- extend
+oscar_status oscar_extend_workspace_size(const oscar_config* cfg, int32_t total_tokens, size_t* bytes) {
+  Geom g;
+  oscar_status st = validate(cfg, &g);
+  if (st != OSCAR_OK) return st;
+  if (!bytes || total_tokens < 0) return fail(OSCAR_ERR_INVALID, "bad arguments to extend workspace size");
+  *bytes = oscar::extend_workspace_bytes(g, total_tokens);
+  return OSCAR_OK;
+}
+
+oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, const void* K_new,
+                               const void* V_new, int32_t kv_dtype, void* out, int32_t out_dtype,
+                               const int32_t* cu_seqlens, const int32_t* prefix_lens, int32_t batch,
+                               int32_t total_tokens, int32_t max_chunk, const int32_t* block_table, int32_t bt_stride,
+                               const int32_t* req_slot, const float* R_K, const float* R_V, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  oscar_status st = need_device(ctx);
+  if (st != OSCAR_OK) return st;
+  if ((st = check_layer(ctx, layer)) != OSCAR_OK) return st;
+  if (batch < 0 || total_tokens < 0 || max_chunk < 0 || bt_stride < 1)
+    return fail(OSCAR_ERR_INVALID, "bad batch/total_tokens/max_chunk/bt_stride");
+  if (batch == 0 || total_tokens == 0) return OSCAR_OK;
+  if (!q || !K_new || !V_new || !out || !cu_seqlens || !prefix_lens || !block_table || !req_slot || !R_K || !R_V ||
+      !workspace)
+    return fail(OSCAR_ERR_INVALID, "null tensor argument");
+  if (kv_dtype != OSCAR_DTYPE_BF16) return fail(OSCAR_ERR_UNSUPPORTED, "extend: K_new / V_new must be BF16");
+  if (q_dtype != OSCAR_DTYPE_BF16 && q_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad q dtype");
+  if (out_dtype != OSCAR_DTYPE_BF16 && out_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad out dtype");
+  if (128 % ctx->g.gq() != 0)
+    return fail(OSCAR_ERR_UNSUPPORTED, "extend: n_q_heads / n_kv_heads = %d must divide 128", ctx->g.gq());
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(OSCAR_ERR_INVALID, "workspace must be 256-byte aligned");
+  if (((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(K_new) | reinterpret_cast<uintptr_t>(V_new) |
+        reinterpret_cast<uintptr_t>(out)) & 15) != 0)
+    return fail(OSCAR_ERR_INVALID, "q, K_new, V_new and out must be 16-byte aligned");
+  if ((st = check_r_align(R_K, R_V)) != OSCAR_OK) return st;
+  const size_t need = oscar::extend_workspace_bytes(ctx->g, total_tokens);
+  if (ws_bytes < need) return fail(OSCAR_ERR_INVALID, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  int ek, ev;
+  if ((st = layer_operand_exps(ctx, layer, &ek, &ev)) != OSCAR_OK) return st;
+  oscar::ExtendArgs a{};
+  a.g = ctx->g;
+  a.layer = layer;
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.K_new = static_cast<const uint16_t*>(K_new);
+  a.V_new = static_cast<const uint16_t*>(V_new);
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.cu_seqlens = cu_seqlens;
+  a.prefix_lens = prefix_lens;
+  a.batch = batch;
+  a.total_tokens = total_tokens;
+  a.max_chunk = max_chunk;
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.req_slot = req_slot;
+  a.R_K = R_K;
+  a.R_V = R_V;
+  a.pool = ctx->pool;
+  a.slab = ctx->slab;
+  a.status = ctx->d_status;
+  a.ws = static_cast<uint8_t*>(workspace);
+  oscar::extend_ws_offsets(ctx->g, &a.rvt_off, &a.qrot_off);
+  a.k_exp_K = ek;
+  a.k_exp_V = ev;
+  a.code_magic = oscar::kCodeMagic;
+  LaunchScope ls(ctx, "extend", stream);
+  int e = oscar::launch_extend(a, stream);
+  ls.done(e);
+  if (e) return cuda_fail(e, "extend launch");
+  return OSCAR_OK;
+}
+
 oscar_status oscar_bf16_decode_attn(oscar_ctx* ctx, int32_t layer, const void* bf16_pool, const void* q,
                                     int32_t q_dtype, void* out, int32_t out_dtype, const int32_t* block_table,
                                     int32_t bt_stride, const int32_t* seq_lens, int32_t batch, int32_t max_seq,

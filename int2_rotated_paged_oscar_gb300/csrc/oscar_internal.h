@@ -108,6 +108,38 @@ struct DecodeArgs {
   int defer_tail_page;       // 1: the preceding kernel may still write the last history page (fused step)
 };
 
+// Extend (chunked prefill) attention over the mixed cache.
+struct ExtendArgs {
+  Geom g;
+  int layer;
+  const void* q;             // [total_tokens][Hq][D], q_dtype
+  int q_dtype;
+  const uint16_t* K_new;     // [total_tokens][Hkv][D] bf16: the chunk's own keys and values
+  const uint16_t* V_new;
+  void* out;                 // [total_tokens][Hq][D], out_dtype
+  int out_dtype;
+  const int* cu_seqlens;     // [batch + 1]
+  const int* prefix_lens;    // [batch]: cached tokens of each request
+  int batch;
+  int total_tokens;
+  int max_chunk;             // host bound on cu_seqlens[b + 1] - cu_seqlens[b] (sizes the grid)
+  const int* block_table;
+  int bt_stride;
+  const int* req_slot;
+  const float* R_K;
+  const float* R_V;
+  const uint8_t* pool;
+  const uint16_t* slab;
+  int* status;
+  uint8_t* ws;               // R_V^T [D][D] f32 at rvt_off, q' = q R_K [total_tokens][Hq][D] f32 at qrot_off
+  size_t rvt_off, qrot_off;
+  int k_exp_K, k_exp_V;
+  unsigned code_magic;
+};
+size_t extend_workspace_bytes(const Geom& g, long long total_tokens);
+void extend_ws_offsets(const Geom& g, size_t* rvt_off, size_t* qrot_off);
+int launch_extend(const ExtendArgs& a, void* stream);
+
 // Host-side planning (pure functions, no CUDA).
 DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool);
 // Operand exponent k for a clip threshold c: c * 2^k < 2^14, so scales

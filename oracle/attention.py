@@ -14,6 +14,8 @@ max subtraction, no mask or soft-cap (every cached token is visible to the
 token being decoded).  ``decode_fused`` is the serving-side rearrangement
 (rotate q once, accumulate history in the rotated basis, apply R_V^T once);
 the two must agree to rounding.  Query head h reads KV head h // (Hq/Hkv).
+``extend`` is the chunked-prefill counterpart: new query tokens attend to a
+cached prefix (as stored) and causally to their own chunk.
 """
 from __future__ import annotations
 
@@ -162,9 +164,10 @@ def extend(cache: CacheImage, layer: int, q, k_new, v_new, cu_seqlens, prefix_le
         k_pre = np.concatenate([yk @ rk.T, wk], axis=0)
         v_pre = np.concatenate([yv @ rv.T, wv], axis=0)
         c0, c1 = int(cu[b]), int(cu[b + 1])
+        k_all = np.concatenate([k_pre, k_new[c0:c1]], axis=0)   # query i sees the first n_pre + i + 1 rows
+        v_all = np.concatenate([v_pre, v_new[c0:c1]], axis=0)
         for i in range(c1 - c0):
-            k_all = np.concatenate([k_pre, k_new[c0:c0 + i + 1]], axis=0)
-            v_all = np.concatenate([v_pre, v_new[c0:c0 + i + 1]], axis=0)
+            n = k_pre.shape[0] + i + 1
             for h in range(hq):
-                out[c0 + i, h] = softmax_attention(q[c0 + i, h], k_all[:, h // grp], v_all[:, h // grp])
+                out[c0 + i, h] = softmax_attention(q[c0 + i, h], k_all[:n, h // grp], v_all[:n, h // grp])
     return out

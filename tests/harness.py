@@ -273,3 +273,27 @@ def cache_pages_for(n: int, g: cache.Geometry) -> int:
     """Pages holding the history of a request of length n (absolute-position paging)."""
     h_end = max(g.sink, n - g.recent)
     return 0 if h_end <= g.sink else (h_end - 1) // g.page_size + 1
+
+
+def run_extend(gc: GpuCache, layer, q: np.ndarray, q_dtype: str, k_new: np.ndarray, v_new: np.ndarray, cu, prefix,
+               bt: np.ndarray, req_slot, fx, out_bf16=False, max_chunk=None):
+    """oscar_extend_attn on the GPU cache; k_new / v_new BF16-valued float arrays [T, Hkv, d]."""
+    torch = torch_mod()
+    import int2_rotated_paged_oscar_gb300 as osc
+    cu = np.asarray(cu, np.int32)
+    total = int(cu[-1])
+    b = cu.size - 1
+    max_chunk = int(np.diff(cu).max()) if max_chunk is None else max_chunk
+    ws_bytes = osc.oscar_extend_workspace_size(gc.cfg, total)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    out = torch.empty((total, q.shape[1], q.shape[2]), dtype=torch.bfloat16 if out_bf16 else torch.float32,
+                      device="cuda")
+    osc.oscar_set_layer_clip(gc.ctx, layer, fx["clip_K"], fx["clip_V"])
+    osc.oscar_extend_attn(gc.ctx, layer, dev_input(q, q_dtype), dtype_code(q_dtype), dev_input(k_new, "bf16"),
+                          dev_input(v_new, "bf16"), osc.DTYPE_BF16, out, osc.DTYPE_BF16 if out_bf16 else osc.DTYPE_F32,
+                          dev(cu), dev(np.asarray(prefix, np.int32)), b, total, max_chunk, dev(bt.astype(np.int32)),
+                          bt.shape[1], dev(np.asarray(req_slot, np.int32)), dev(fx["R_K"]), dev(fx["R_V"]), ws,
+                          ws_bytes)
+    status = osc.oscar_check_status(gc.ctx)
+    assert status == 0, f"device status {status}"
+    return out.float().cpu().numpy().astype(np.float64)

@@ -1,0 +1,85 @@
+"""GPU parity of extend (chunked prefill) attention over the mixed cache, against the oracle.
+
+The prefix of every request is written by the GPU's own write path; the oracle then attends over
+the GPU's cache image (pages and window slots read back), so these tests check the attention
+kernel alone.  Every case spans several 64-key tiles and query tiles with ragged tails.
+"""
+import numpy as np
+import pytest
+
+import synthetic as syn
+from oracle import attention, cache
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def osc():
+    from int2_rotated_paged_oscar_gb300 import build
+    build.build()
+    import int2_rotated_paged_oscar_gb300 as m
+    m.load()
+    return m
+
+
+def _setup(wl, fx, prefix):
+    """GPU cache with each request's prefix written (request b in slot b, pages b*ppr ...)."""
+    s = wl.shape
+    b = len(prefix)
+    ppr = max(syn.pages_for(max(n, 1), s.page_size) for n in prefix) + 1
+    bt = np.arange(b * ppr, dtype=np.int32).reshape(b, ppr)
+    geom = H.geometry(s, b * ppr, b)
+    gc = H.make_gpu_cache(geom, s.n_q_heads, ppr)
+    if sum(prefix):
+        import int2_rotated_paged_oscar_gb300 as osc
+        ks, vs = zip(*[syn.kv_tokens(wl, 0, n, sub=i) for i, n in enumerate(prefix)])
+        k = np.concatenate(ks)
+        v = np.concatenate(vs)
+        cu = np.concatenate([[0], np.cumsum(prefix)]).astype(np.int32)
+        osc.oscar_write_kv(gc.ctx, 0, H.dev_input(k, wl.dtype), H.dev_input(v, wl.dtype), H.dtype_code(wl.dtype),
+                           H.dev(cu), H.dev(np.zeros(b, np.int32)), b, int(cu[-1]), H.dev(fx["R_K"]),
+                           H.dev(fx["R_V"]), fx["clip_K"], fx["clip_V"], H.dev(bt), ppr,
+                           H.dev(np.arange(b, dtype=np.int32)))
+        assert osc.oscar_check_status(gc.ctx) == 0
+    return gc, geom, bt
+
+
+def _image(gc, geom):
+    img = cache.CacheImage(geom)
+    img.pool, img.slab = gc.pool_np(), gc.slab_np()
+    return img
+
+
+@pytest.mark.parametrize("shape,prefix,chunks,q_dtype,out_bf16", [
+    (syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [1300, 0, 90, 700], [200, 150, 37, 64], "bf16", False),
+    (syn.Shape(8, 4, 64, 16, 32, 4, 32, 1), [300, 35], [70, 9], "f32", False),
+    (syn.Shape(8, 8, 128, 32, 32, 0, 64, 1), [500, 64], [130, 1], "f32", True),
+    (syn.Shape(64, 8, 128, 64, 32, 4, 128, 1), [260], [40], "bf16", False),
+], ids=["d128_p64_gq4", "d64_p16_gq2", "d128_p32_gq1_nosink_bf16out", "d128_p64_gq8"])
+def test_extend_parity(osc, shape, prefix, chunks, q_dtype, out_bf16):
+    wl = syn.Workload("ext", shape, [0], seed=31, dtype="bf16")
+    fx = H.fixture(wl)
+    gc, geom, bt = _setup(wl, fx, prefix)
+    try:
+        total = sum(chunks)
+        k, v = syn.kv_tokens(wl, 0, total, sub=7)
+        q = syn.queries(wl, 0, total, sub=8)
+        if q_dtype == "f32":
+            q = q * np.float32(1.0 + 1.0 / 3.0)   # values off the BF16 grid
+        cu = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+        slots = np.arange(len(prefix), dtype=np.int32)
+        got = H.run_extend(gc, 0, q, q_dtype, k, v, cu, prefix, bt, slots, fx, out_bf16=out_bf16)
+        want = attention.extend(_image(gc, geom), 0, q, k, v, cu, prefix, bt, slots, fx["R_K"], fx["R_V"])
+        if out_bf16:
+            # a BF16 store rounds each element to 2^-9 of itself: one BF16 ulp of the element plus the
+            # float32 bound (outlier channels reach tens of times the output RMS)
+            rms = float(np.sqrt(np.mean(np.square(want))))
+            err = np.abs(got - want)
+            bound = 2.0 ** -8 * np.abs(want) + H.DECODE_MAX_ABS * rms
+            assert np.all(np.isfinite(got)) and np.all(err <= bound), f"worst excess {float((err - bound).max()):.3e}"
+            assert err.mean() <= 2e-3 * rms
+        else:
+            H.assert_decode_close(got, want)
+    finally:
+        gc.close()
