@@ -36,9 +36,11 @@
 //
 // Roles: warps 0-3 (softmax; thread r owns row r = TMEM lane r), warps 4-7 (unpack of
 // the next tile into the shared-memory operand tiles, INT2 pages staged one tile ahead
-// by cp.async), warp 8 (TMEM allocation, MMA issue).  The warps meet at one CTA barrier
-// per tile; MMAs run asynchronously between barriers.  Every mbarrier wait is bounded
-// by %globaltimer: a timeout flags the status word and the CTA drains and exits.
+// by cp.async), warp 8 (TMEM allocation, MMA issue).  The roles meet only at mbarriers:
+// kv_full (a stage unpacked), s_full (scores in TMEM), p_full (weights in shared
+// memory), pv_done and kv_empty (a tile's PV done, its stage free), so the scores of
+// tile j are computed while the softmax works on tile j - 1.  Every wait is bounded by
+// %globaltimer: a timeout flags the status word and the CTA drains and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -93,17 +95,21 @@ struct XLayout {
   static constexpr int RAW_BYTES = kXKeys * 3 * D / 4;           // 64 INT2 tokens: codes and (scale, zero) of K, V
   static constexpr int RAW0 = PLO2 + P_BYTES;
   static constexpr int BAR = RAW0 + 2 * RAW_BYTES;
-  static constexpr int BYTES = BAR + 4 * 8 + 16;                 // s_full[2], pv_done, spare; tmem slot, abort
+  static constexpr int BYTES = BAR + 8 * 8 + 16;   // s_full[2], pv_done, kv_full[2], kv_empty[2], p_full; tmem slot, abort
   static constexpr int SMEM = BYTES + 1024;
   // epilogue reuse (after the last MMA): R_V^T [D][D] f32 over the Q planes, y [128][D+1] f32
   // over the stages, 1/l [128] over the P planes
   static constexpr int RT = 0, Y = ST0, LINV = PHI;
   static constexpr int YS = D + 1;
   // TMEM columns
-  static constexpr uint32_t C_S = 0, C_OROT = 2 * kXKeys, C_OPLAIN = C_OROT + D, C_OZ = C_OPLAIN + D;
+  // the V centre accumulator (16 columns) directly follows the rotated one: one PV MMA with
+  // N = D + 16 reads the Zv rows that follow the Vt rows in shared memory
+  static constexpr uint32_t C_S = 0, C_OROT = 2 * kXKeys, C_OZ = C_OROT + D, C_OPLAIN = C_OZ + 32;
+  static constexpr uint32_t C_END = C_OPLAIN + D;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(STAGE % 1024 == 0 && ST0 % 1024 == 0 && PHI % 1024 == 0, "operand tiles 1024-aligned");
-  static_assert(C_OZ + 32 <= TMEM_COLS, "TMEM plan");
+  static_assert(C_END <= TMEM_COLS, "TMEM plan");
+  static_assert(ZV == VT + D * 128, "Zv rows follow the Vt rows");
   static_assert(D * (D + 0) * 4 <= ST0, "R_V^T fits over the Q planes");
   static_assert(kXRows * YS * 4 <= 2 * STAGE, "y fits over the stages");
   static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -176,15 +182,52 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 // named barrier 1 among the 128 unpack threads
 __device__ __forceinline__ void unpack_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// the same barrier, returning whether any of the 128 threads passed true
+__device__ __forceinline__ bool unpack_bar_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, 1, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ uint32_t half2_bits(float lo_elem, float hi_elem) { return pack_half2(lo_elem, hi_elem); }
 __device__ __forceinline__ float bf16_round_f(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 // 2^e for e in the float32 normal range
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
+// Bounded mbarrier wait that lets the waiting warp sleep (try_wait with a suspend-time hint:
+// the thread resumes when the phase completes or after the hint), so waiting roles leave
+// the issue slots to the working ones.  Gives up after kWaitLimitNs like mbar_wait_bounded.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool xwait(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(64);   // leave the issue slots to the warps doing work
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      flag_error(status, kDevTimeout);
+      return false;
+    }
+  }
+}
 
 // f16 pair (1.5 * 2^(pos - 10), same): the centring constant of a code slot at bit pos
 __host__ __device__ constexpr uint32_t centre_pair(int pos) {
@@ -206,13 +249,10 @@ __device__ __forceinline__ void centre_hi_lo(uint32_t w, uint32_t k23, __half& h
   hi = __float2half_rn(m);
   lo = __float2half_rn(m - __half2float(hi));
 }
-__device__ __forceinline__ uint32_t hpair(__half a, __half b) {
-  return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
-}
-// centre-term columns: term t pairs query term kCentreQ[t] (0 hi, 1 lo, 2 lo2 of Q_g) with
-// centre term kCentreZ[t] (0 hi, 1 lo of m); G groups per term, 16 columns in all
-__device__ constexpr int kCentreQ[5] = {0, 1, 0, 2, 1};
-__device__ constexpr int kCentreZ[5] = {0, 0, 1, 0, 1};
+// centre-term columns: term t pairs query term centre_q_term(t) (0 hi, 1 lo, 2 lo2 of Q_g)
+// with centre term centre_z_term(t) (0 hi, 1 lo of m); G groups per term, 16 columns in all
+__host__ __device__ constexpr int centre_q_term(int t) { return t == 3 ? 2 : (t == 1 || t == 4 ? 1 : 0); }
+__host__ __device__ constexpr int centre_z_term(int t) { return t == 2 || t == 4 ? 1 : 0; }
 template <int G>
 __host__ __device__ constexpr int kCentreTerms() { return 16 / G < 5 ? 16 / G : 5; }
 
@@ -234,10 +274,13 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   constexpr int G = L::G;
   extern __shared__ __align__(1024) uint8_t x_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(x_smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* s_full = reinterpret_cast<uint64_t*>(smem + L::BAR);   // [2]
-  uint64_t* pv_done = s_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR + 32);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR + 36);
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(smem + L::BAR);   // [2] scores of tile j in TMEM (commit)
+  uint64_t* pv_done = s_full + 2;      // PV of tile j done (commit)
+  uint64_t* kv_full = s_full + 3;      // [2] stage j & 1 holds tile j (128 unpack arrivals)
+  uint64_t* kv_empty = s_full + 5;     // [2] stage free again (commit after the tile's PV)
+  uint64_t* p_full = s_full + 7;       // weights of tile j in shared memory (128 softmax arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR + 68);
 
   const Geom& g = a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -292,11 +335,27 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       mbar_init(&s_full[0], 1);
       mbar_init(&s_full[1], 1);
       mbar_init(pv_done, 1);
+      mbar_init(&kv_full[0], 128);
+      mbar_init(&kv_full[1], 128);
+      mbar_init(&kv_empty[0], 1);
+      mbar_init(&kv_empty[1], 1);
+      mbar_init(p_full, 128);
       *abort_flag = 0;
       fence_barrier_init();
     }
     __syncwarp();
     tmem_alloc(tmem_slot, L::TMEM_COLS);
+  }
+  // columns past the centre terms of both stages' Kz tiles stay zero (the query side's
+  // matching columns are zero too; a zero times a zero keeps the padding out of the scores)
+  constexpr int PADC = 16 - kCentreTerms<G>() * G;
+  if constexpr (PADC > 0) {
+    for (int idx = tid; idx < 2 * kXKeys * PADC; idx += kXThreads) {
+      const int st = idx / (kXKeys * PADC), rem = idx % (kXKeys * PADC);
+      const int key = rem / PADC, col = kCentreTerms<G>() * G + rem % PADC;
+      *reinterpret_cast<__half*>(smem + L::ST0 + st * L::STAGE + L::KZ + sw128_offset(key, col, kXKeys)) =
+          __float2half_rn(0.f);
+    }
   }
   // rows 2G..15 of both stages' Zv tiles stay zero (padding of the V centre term)
   for (int idx = tid; idx < 2 * (16 - 2 * G) * 8; idx += kXThreads) {
@@ -376,7 +435,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       const __half h3 = __float2half_rn(r1 - __half2float(h2));
       const __half qt[3] = {h1, h2, h3};
 #pragma unroll
-      for (int tt = 0; tt < kCentreTerms<G>(); ++tt) hz[tt * G + gg] = qt[kCentreQ[tt]];
+      for (int tt = 0; tt < kCentreTerms<G>(); ++tt) hz[tt * G + gg] = qt[centre_q_term(tt)];
     }
     const uint4* hz4 = reinterpret_cast<const uint4*>(hz);
     *reinterpret_cast<uint4*>(smem + L::QZ + sw128_offset(r, 0, kXRows)) = hz4[0];
@@ -421,16 +480,33 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   const int u = tid - 128;
   auto hist_ok = [&](int t) { return t >= tl.S && t < tl.hist_end; };
   // INT2 pages of tile j into raw buffer j & 1 (one cp.async group per call, possibly empty)
-  auto issue_raw = [&](int j) {
+  // page sizes are powers of two (16, 32, 64): block and slot of a key by shift and mask
+  const int pshift = __ffs(g.P) - 1, pmask = g.P - 1, nblk = kXKeys >> pshift;
+  // page ids of tile j's blocks (-1: block outside the history), read one tile ahead of
+  // their copies so that the block-table load latency stays off the unpack path
+  constexpr int kMaxBlk = kXKeys / 16;
+  auto load_pages = [&](int j, int (&pg)[kMaxBlk]) {
+#pragma unroll
+    for (int bi = 0; bi < kMaxBlk; ++bi) pg[bi] = -1;
     if (j < n_tiles && tl.kind(j) == kTileInt2) {
       const int base = tl.base(j);
+#pragma unroll
+      for (int bi = 0; bi < kMaxBlk; ++bi) {
+        const int p0 = base + (bi << pshift);
+        if (bi >= nblk || p0 + g.P <= tl.S || p0 >= tl.hist_end) continue;
+        const int lp = p0 >> pshift;
+        pg[bi] = (lp < a.bt_stride && lp < g.max_pages_per_req) ? a.block_table[(size_t)b * a.bt_stride + lp] : -2;
+      }
+    }
+  };
+  // INT2 pages of tile j into raw buffer j & 1 (one cp.async group per call, possibly empty)
+  auto issue_raw = [&](int j, const int (&pg)[kMaxBlk]) {
+    if (j < n_tiles && tl.kind(j) == kTileInt2) {
       uint8_t* dst0 = smem + L::RAW0 + (j & 1) * L::RAW_BYTES;
-      for (int bi = 0; bi < kXKeys / g.P; ++bi) {
-        const int p0 = base + bi * g.P;
-        if (p0 + g.P <= tl.S || p0 >= tl.hist_end) continue;
-        const int lp = p0 / g.P;
-        int page = -1;
-        if (lp < a.bt_stride && lp < g.max_pages_per_req) page = a.block_table[(size_t)b * a.bt_stride + lp];
+#pragma unroll
+      for (int bi = 0; bi < kMaxBlk; ++bi) {
+        const int page = pg[bi];
+        if (bi >= nblk || page == -1) continue;
         if (page < 0 || page >= g.num_pages) {
           if (u == 0) flag_error(a.status, kDevBadPage);
           continue;
@@ -450,8 +526,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     if (u < kXKeys * (D / 64)) {
       const int key = u / (D / 64), w = u % (D / 64);
       const bool ok = hist_ok(base + key);
-      const uint8_t* kb = raw + (key / g.P) * BB;
-      const int slot = key % g.P;
+      const uint8_t* kb = raw + (key >> pshift) * BB;
+      const int slot = key & pmask;
       uint32_t wd[4], w6[4];
 #pragma unroll
       for (int tg = 0; tg < 4; ++tg) {
@@ -477,22 +553,6 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         c.w = centre_codes(scale_codes(magic_slot<x>(wd[3], w6[3], magic), n2), n2, kc);
         *reinterpret_cast<uint4*>(stg + L::KT + sw128_offset(key, 8 * (8 * w + x), kXKeys)) = c;
       });
-      if (w == 0) {
-        __half hz[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) hz[k] = __float2half_rn(0.f);
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          __half mh, ml;
-          centre_hi_lo(ok ? szw[gg] : 0u, kK23, mh, ml);
-          const __half mt[2] = {mh, ml};
-#pragma unroll
-          for (int tt = 0; tt < kCentreTerms<G>(); ++tt) hz[tt * G + gg] = mt[kCentreZ[tt]];
-        }
-        const uint4* hz4 = reinterpret_cast<const uint4*>(hz);
-        *reinterpret_cast<uint4*>(stg + L::KZ + sw128_offset(key, 0, kXKeys)) = hz4[0];
-        *reinterpret_cast<uint4*>(stg + L::KZ + sw128_offset(key, 8, kXKeys)) = hz4[1];
-      }
     }
     // V codes -> code * s_V * 2^(k_V + pos - 10), transposed: thread (half-word hw, keys 8kb..8kb+7)
     if (u < (D / 8) * 8) {
@@ -500,7 +560,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       const int chbase = 64 * (hw % (D / 64)) + hw / (D / 64);
       const int gA = chbase / 32;
       uint32_t W[4], W6[4], nA[4], nB[4];
-      __half zh[8][G], zl[8][G];
+
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
         uint32_t hv[2];
@@ -509,14 +569,12 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         for (int e = 0; e < 2; ++e) {
           const int key = 8 * kb8 + 2 * p + e;
           const bool ok = hist_ok(base + key);
-          const uint8_t* vb = raw + (key / g.P) * BB;
-          const int slot = key % g.P;
+          const uint8_t* vb = raw + (key >> pshift) * BB;
+          const int slot = key & pmask;
           hv[e] = *reinterpret_cast<const uint16_t*>(vb + g.v_codes_off() + slot * (D / 4) + hw * 2);
           const uint32_t* szr = reinterpret_cast<const uint32_t*>(vb + g.v_sz_off() + slot * (D / 8));
           sa[e] = ok ? neg_scale_times_pow2(szr[gA], kV23) : 0.f;
           sb[e] = ok ? neg_scale_times_pow2(szr[gA + 1], kV23) : 0.f;
-#pragma unroll
-          for (int gg = 0; gg < G; ++gg) centre_hi_lo(ok ? szr[gg] : 0u, kV23, zh[2 * p + e][gg], zl[2 * p + e][gg]);
         }
         W[p] = hv[0] | (hv[1] << 16);
         W6[p] = W[p] >> 6;
@@ -533,17 +591,29 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         c.w = centre_codes(scale_codes(magic_slot<s>(W[3], W6[3], magic), s < 4 ? nA[3] : nB[3]), s < 4 ? nA[3] : nB[3], kc);
         *reinterpret_cast<uint4*>(stg + L::VT + sw128_offset(chbase + 8 * s, 8 * kb8, D)) = c;
       });
-      if (hw == 0) {
-        // rows g: centre hi, rows G + g: centre lo, keys 8kb..8kb+7
+    }
+    // group centres m = z + 1.5 s of K and V: one (key, group) item per thread and step.
+    // K: Kz row key, column t G + g holds term centre_z_term(t) of m (the query side matches it);
+    // V: Zv rows g (hi) and G + g (lo), column key.
+    for (int item = u; item < 2 * kXKeys * G; item += 128) {
+      const bool is_v = item >= kXKeys * G;
+      const int rem = is_v ? item - kXKeys * G : item;
+      const int key = rem / G, gg = rem % G;
+      const bool ok = hist_ok(base + key);
+      const uint8_t* kb = raw + (key >> pshift) * BB;
+      const int slot = key & pmask;
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(kb + (is_v ? g.v_sz_off() : g.k_sz_off()) + slot * (D / 8) +
+                                                            gg * 4);
+      __half mh, ml;
+      centre_hi_lo(ok ? w : 0u, is_v ? kV23 : kK23, mh, ml);
+      if (!is_v) {
+        const __half mt[2] = {mh, ml};
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          const uint4 ch4 = make_uint4(hpair(zh[0][gg], zh[1][gg]), hpair(zh[2][gg], zh[3][gg]),
-                                       hpair(zh[4][gg], zh[5][gg]), hpair(zh[6][gg], zh[7][gg]));
-          const uint4 cl4 = make_uint4(hpair(zl[0][gg], zl[1][gg]), hpair(zl[2][gg], zl[3][gg]),
-                                       hpair(zl[4][gg], zl[5][gg]), hpair(zl[6][gg], zl[7][gg]));
-          *reinterpret_cast<uint4*>(stg + L::ZV + sw128_offset(gg, 8 * kb8, 16)) = ch4;
-          *reinterpret_cast<uint4*>(stg + L::ZV + sw128_offset(G + gg, 8 * kb8, 16)) = cl4;
-        }
+        for (int tt = 0; tt < kCentreTerms<G>(); ++tt)
+          *reinterpret_cast<__half*>(stg + L::KZ + sw128_offset(key, tt * G + gg, kXKeys)) = mt[centre_z_term(tt)];
+      } else {
+        *reinterpret_cast<__half*>(stg + L::ZV + sw128_offset(gg, key, 16)) = mh;
+        *reinterpret_cast<__half*>(stg + L::ZV + sw128_offset(G + gg, key, 16)) = ml;
       }
     }
   };
@@ -610,8 +680,16 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
 
   // ---------------- MMA issue (warp 8, lane 0)
   const uint32_t sbase = smem_u32(smem);
+  // descriptors: the start-address field is (address >> 4) in the low 14 bits, so an
+  // offset inside a tile is added to a base descriptor directly
+  const uint64_t dQHI = smem_desc_sw128(sbase + L::QHI), dQLO = smem_desc_sw128(sbase + L::QLO);
+  const uint64_t dQZ = smem_desc_sw128(sbase + L::QZ);
+  const uint64_t dP[3] = {smem_desc_sw128(sbase + L::PHI), smem_desc_sw128(sbase + L::PLO),
+                          smem_desc_sw128(sbase + L::PLO2)};
+  const uint64_t dST = smem_desc_sw128(sbase + L::ST0);
+  auto dadd = [](uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); };
   auto issue_qk = [&](int j) {
-    const uint32_t stg = sbase + L::ST0 + (uint32_t)((j & 1) * L::STAGE);
+    const uint32_t soff = (uint32_t)((j & 1) * L::STAGE);
     const uint32_t dS = tmem + L::C_S + (uint32_t)((j & 1) * kXKeys);
     const bool rot = tl.kind(j) == kTileInt2;
     const uint32_t idesc = rot ? idesc_f16_f32(kXRows, kXKeys) : idesc_bf16_f32(kXRows, kXKeys);
@@ -624,21 +702,19 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ak = (uint32_t)((kk >> 2) * kXRows * 128 + (kk & 3) * 32);
         const uint32_t bk = (uint32_t)((kk >> 2) * kXKeys * 128 + (kk & 3) * 32);
-        tc_mma(dS, smem_desc_sw128(sbase + (pl ? L::QLO : L::QHI) + ak), smem_desc_sw128(stg + L::KT + bk), idesc,
-               (pl | kk) ? 1u : 0u);
+        tc_mma(dS, dadd(pl ? dQLO : dQHI, ak), dadd(dST, soff + L::KT + bk), idesc, (pl | kk) ? 1u : 0u);
       }
-    if (rot) tc_mma(dS, smem_desc_sw128(sbase + L::QZ), smem_desc_sw128(stg + L::KZ), idesc, 1u);
+    if (rot) tc_mma(dS, dQZ, dadd(dST, soff + L::KZ), idesc, 1u);
   };
   auto issue_pv = [&](int j) {
-    const uint32_t stg = sbase + L::ST0 + (uint32_t)((j & 1) * L::STAGE);
+    const uint32_t soff = (uint32_t)((j & 1) * L::STAGE);
     if (tl.kind(j) == kTileInt2) {
 #pragma unroll
       for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
         for (int kk = 0; kk < kXKeys / 16; ++kk) {
-          const uint64_t pa = smem_desc_sw128(sbase + (pl ? L::PLO : L::PHI) + kk * 32);
-          tc_mma(tmem + L::C_OROT, pa, smem_desc_sw128(stg + L::VT + kk * 32), idesc_f16_f32(kXRows, D), 1u);
-          tc_mma(tmem + L::C_OZ, pa, smem_desc_sw128(stg + L::ZV + kk * 32), idesc_f16_f32(kXRows, 16), 1u);
+          const uint64_t pa = dadd(dP[pl], kk * 32);
+          tc_mma(tmem + L::C_OROT, pa, dadd(dST, soff + L::VT + kk * 32), idesc_f16_f32(kXRows, D + 16), 1u);
         }
     } else {
       // P as three BF16 terms (24 bits): window and chunk values are unbounded BF16
@@ -646,8 +722,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       for (int pl = 0; pl < 3; ++pl)
 #pragma unroll
         for (int kk = 0; kk < kXKeys / 16; ++kk)
-          tc_mma(tmem + L::C_OPLAIN, smem_desc_sw128(sbase + (pl == 0 ? L::PHI : (pl == 1 ? L::PLO : L::PLO2)) + kk * 32),
-                 smem_desc_sw128(stg + L::VT + kk * 32), idesc_bf16_f32(kXRows, D), 1u);
+          tc_mma(tmem + L::C_OPLAIN, dadd(dP[pl], kk * 32), dadd(dST, soff + L::VT + kk * 32),
+                 idesc_bf16_f32(kXRows, D), 1u);
     }
   };
 
@@ -655,7 +731,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   float m_ref = -INFINITY, thr = -INFINITY, l_run = 0.f;
   auto softmax_tile = [&](int i) -> bool {
     const int kind = tl.kind(i), base = tl.base(i);
-    if (!mbar_wait_bounded(&s_full[i & 1], (uint32_t)(i >> 1) & 1, a.status)) return false;
+    // waits are made warp-uniform: the TMEM accesses below are warp-collective
+    if (!__all_sync(0xffffffffu, xwait(&s_full[i & 1], (uint32_t)(i >> 1) & 1, a.status))) return false;
     tc_fence_after();
     uint32_t s0[32], s1[32];
     tmem_ld32_nowait(lane_base + L::C_S + (uint32_t)((i & 1) * kXKeys), s0);
@@ -674,16 +751,24 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     } else {
       a1 = min(kXKeys, qi - base + 1);
     }
-    const float F = kind == kTileInt2 ? F_rot : sm_log2;
-    float sc[kXKeys];
-    float mloc = -INFINITY;
+    const float F = kind == kTileInt2 ? F_rot : sm_log2;   // > 0: the maximum can be taken on raw values
+    float sc[kXKeys];   // raw accumulator values, invisible keys at -inf
+    float mraw = -INFINITY;
+    if (a0 <= 0 && a1 >= kXKeys) {
 #pragma unroll
-    for (int jj = 0; jj < kXKeys; ++jj) {
-      const float v = __uint_as_float(jj < 32 ? s0[jj] : s1[jj - 32]) * F;
-      const bool vis = (jj >= a0 && jj < a1) || (jj >= b0 && jj < b1);
-      sc[jj] = vis ? v : -INFINITY;
-      mloc = fmaxf(mloc, sc[jj]);
+      for (int jj = 0; jj < kXKeys; ++jj) {
+        sc[jj] = __uint_as_float(jj < 32 ? s0[jj] : s1[jj - 32]);
+        mraw = fmaxf(mraw, sc[jj]);
+      }
+    } else {
+#pragma unroll
+      for (int jj = 0; jj < kXKeys; ++jj) {
+        const bool vis = (jj >= a0 && jj < a1) || (jj >= b0 && jj < b1);
+        sc[jj] = vis ? __uint_as_float(jj < 32 ? s0[jj] : s1[jj - 32]) : -INFINITY;
+        mraw = fmaxf(mraw, sc[jj]);
+      }
     }
+    const float mloc = mraw * F;
     float alpha = 1.f;
     if (mloc > thr) {
       const float nm = mloc - kXWeightShift;
@@ -692,13 +777,14 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       thr = nm + kXWeightShift + kXRescaleLog2;
     }
     // the P buffer and the accumulators are free once the previous tile's PV is done
-    if (i >= 1 && !mbar_wait_bounded(pv_done, (uint32_t)((i - 1) & 1), a.status)) return false;
+    if (i >= 1 && !__all_sync(0xffffffffu, xwait(pv_done, (uint32_t)((i - 1) & 1), a.status)))
+      return false;
     tc_fence_after();
     const bool resc = alpha != 1.f && l_run > 0.f;
     if (__any_sync(0xffffffffu, resc)) {
       const float f = resc ? alpha : 1.f;
 #pragma unroll 1
-      for (uint32_t c = L::C_OROT; c < L::C_OZ + 32; c += 32) {
+      for (uint32_t c = L::C_OROT; c < L::C_END; c += 32) {
         uint32_t o[32];
         tmem_ld32_nowait(lane_base + c, o);
         tmem_wait_ld();
@@ -710,6 +796,9 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     }
     l_run *= alpha;
     if (m_ref == -INFINITY) m_ref = 0.f;   // no visible key yet: every weight of this tile is 0
+    const float negm = -m_ref;
+    // weights 2^(score - m) = ex2(raw * F - m); the row sum takes them in float32 (the split
+    // terms below carry 22 or 24 bits of each)
     float lsum = 0.f;
     if (kind == kTileInt2) {
 #pragma unroll
@@ -717,12 +806,11 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float p0 = ex2(sc[8 * c + 2 * k] - m_ref), p1 = ex2(sc[8 * c + 2 * k + 1] - m_ref);
+          const float p0 = ex2(fmaf(sc[8 * c + 2 * k], F, negm)), p1 = ex2(fmaf(sc[8 * c + 2 * k + 1], F, negm));
           hi[k] = half2_bits(p0, p1);
           const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
           lo[k] = half2_bits(p0 - hf.x, p1 - hf.y);
-          const float2 lf = __half22float2(*reinterpret_cast<const __half2*>(&lo[k]));
-          lsum += (hf.x + lf.x) + (hf.y + lf.y);
+          lsum += p0 + p1;
         }
         const uint32_t off = sw128_offset(r, 8 * c, kXRows);
         *reinterpret_cast<uint4*>(smem + L::PHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -734,14 +822,13 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         uint32_t hi[4], lo[4], lo2[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float p0 = ex2(sc[8 * c + 2 * k] - m_ref), p1 = ex2(sc[8 * c + 2 * k + 1] - m_ref);
+          const float p0 = ex2(fmaf(sc[8 * c + 2 * k], F, negm)), p1 = ex2(fmaf(sc[8 * c + 2 * k + 1], F, negm));
           const float h0 = bf16_round_f(p0), h1 = bf16_round_f(p1);
           const float l0 = bf16_round_f(p0 - h0), l1 = bf16_round_f(p1 - h1);
-          const float m0 = bf16_round_f(p0 - h0 - l0), m1 = bf16_round_f(p1 - h1 - l1);
           hi[k] = pack_bf162(h0, h1);
           lo[k] = pack_bf162(l0, l1);
-          lo2[k] = pack_bf162(m0, m1);
-          lsum += ((h0 + l0) + m0) + ((h1 + l1) + m1);
+          lo2[k] = pack_bf162(p0 - h0 - l0, p1 - h1 - l1);
+          lsum += p0 + p1;
         }
         const uint32_t off = sw128_offset(r, 8 * c, kXRows);
         *reinterpret_cast<uint4*>(smem + L::PHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -753,89 +840,127 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     return true;
   };
 
+  int pg_next[kMaxBlk];   // unpack threads: page ids of the tile after the next
   // ---------------- preamble: zero the output accumulators, query planes, first tile
   if (warp < 4) {
     uint32_t z[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) z[k] = 0u;
 #pragma unroll 1
-    for (uint32_t c = L::C_OROT; c < L::C_OZ + 32; c += 32) tmem_st32(lane_base + c, z);
+    for (uint32_t c = L::C_OROT; c < L::C_END; c += 32) tmem_st32(lane_base + c, z);
     tmem_wait_st();
     if (tl.nR > 0) write_q_rot(); else write_q_plain();
   } else if (warp < 8) {
-    issue_raw(0);
-    issue_raw(1);
-    cp_async_wait1();
+    int pg[kMaxBlk];
+    load_pages(0, pg);
+    issue_raw(0, pg);
+    load_pages(1, pg);
+    cp_async_wait0();
     unpack_bar();
+    issue_raw(1, pg);
+    load_pages(2, pg_next);
     unpack(0);
+    fence_proxy_async_smem();
+    mbar_arrive(&kv_full[0]);
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  int committed = 0;               // MMA thread: 1 = s_full, 2 = pv_done last committed
-  int last_i = 0;
-  if (warp == 8 && lane == 0) {
-    issue_qk(0);
-    tc_commit(&s_full[0]);
-    committed = 1;
-  }
 
-  // ---------------- main loop: one CTA barrier per tile
+  // ---------------- pipeline: the roles meet only at mbarriers.  The MMA thread issues the
+  // scores of tile j as soon as tile j is unpacked (the softmax may still be on tile j - 1)
+  // and the PV of tile j - 1 when its weights are in place.
   bool aborted = false;
-  for (int i = 0; i < n_tiles; ++i) {
-    bool ok = true;
-    if (warp < 4) {
-      ok = softmax_tile(i);
-    } else if (warp < 8) {
-      if (i + 1 < n_tiles) {
-        issue_raw(i + 2);
-        // stage (i + 1) & 1 was last read by tile i - 1's MMAs
-        if (i >= 1) ok = mbar_wait_bounded(pv_done, (uint32_t)((i - 1) & 1), a.status);
-        cp_async_wait1();
-        unpack_bar();
-        if (ok) unpack(i + 1);
+  if (warp < 4) {
+    for (int i = 0; i < n_tiles; ++i) {
+      const bool ok = __all_sync(0xffffffffu, *abort_flag == 0) && softmax_tile(i);
+      if (!ok) {
+        *abort_flag = 1;
+        aborted = true;
+        break;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+  } else if (warp < 8) {
+    for (int j = 1; j < n_tiles; ++j) {
+      cp_async_wait0();
+      // stage j & 1 was last read by tile j - 2's MMAs
+      const bool ok = j < 2 || xwait(&kv_empty[j & 1], (uint32_t)(((j >> 1) - 1) & 1), a.status);
+      // one named barrier per tile: every copy of tile j has landed, every thread is done with
+      // tile j - 1's raw buffer, and all agree on whether to stop
+      if (unpack_bar_any(!ok || *abort_flag != 0)) {
+        *abort_flag = 1;
+        aborted = true;
+        break;
+      }
+      issue_raw(j + 1, pg_next);
+      load_pages(j + 2, pg_next);
+      unpack(j);
+      fence_proxy_async_smem();
+      mbar_arrive(&kv_full[j & 1]);
+    }
+    cp_async_wait0();
+  } else if (lane == 0) {
+    // MMA issue: the scores of tile qk (its stage unpacked; the S buffer free once the weights
+    // of tile qk - 2 are out; at tile nR the query planes switch, after tile nR - 1's
+    // softmax) and the PV of tile pv (its weights in place), whichever is ready first
+    int qk = 0, pv = 0;
+    int last_commit = -1;   // 0: s_full of tile qk - 1, 1: pv_done of tile pv - 1
+    uint64_t t_last = globaltimer_ns();
+    while (pv < n_tiles) {
+      bool progressed = false;
+      if (qk < n_tiles && pv >= qk - 1 && (qk != tl.nR || pv >= tl.nR) &&
+          mbar_try_wait(&kv_full[qk & 1], (uint32_t)((qk >> 1) & 1))) {
+        tc_fence_after();
+        issue_qk(qk);
+        tc_commit(&s_full[qk & 1]);
+        last_commit = 0;
+        ++qk;
+        progressed = true;
+      }
+      if (pv < qk && mbar_try_wait(p_full, (uint32_t)(pv & 1))) {
+        tc_fence_after();
+        issue_pv(pv);
+        tc_commit(pv_done);
+        if (pv + 1 < n_tiles) tc_commit(&kv_empty[pv & 1]);
+        last_commit = 1;
+        ++pv;
+        progressed = true;
+      }
+      if (progressed) {
+        t_last = globaltimer_ns();
+        continue;
+      }
+      __nanosleep(32);
+      if (*abort_flag || globaltimer_ns() - t_last > kWaitLimitNs) {
+        if (!*abort_flag) flag_error(a.status, kDevTimeout);
+        *abort_flag = 1;
+        aborted = true;
+        break;
       }
     }
-    if (!ok) *abort_flag = 1;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (*abort_flag) {
-      aborted = true;
-      break;
-    }
-    if (warp == 8 && lane == 0) {
-      if (i + 1 < n_tiles) {
-        issue_qk(i + 1);
-        tc_commit(&s_full[(i + 1) & 1]);
-      }
-      issue_pv(i);
-      tc_commit(pv_done);
-      committed = 2;
-      last_i = i;
+    if (aborted) {
+      // drain: the last commit covers every MMA issued before it
+      if (last_commit == 1) (void)xwait(pv_done, (uint32_t)((pv - 1) & 1), nullptr);
+      else if (last_commit == 0) (void)xwait(&s_full[(qk - 1) & 1], (uint32_t)(((qk - 1) >> 1) & 1), nullptr);
     }
   }
-
-  if (aborted) {
-    // drain: every issued MMA and copy completes before the CTA releases TMEM and exits
-    if (warp == 8 && lane == 0) {
-      if (committed == 2) (void)mbar_wait_bounded(pv_done, (uint32_t)(last_i & 1), nullptr);
-      else if (committed == 1) (void)mbar_wait_bounded(&s_full[0], 0u, nullptr);
-    }
-    if (warp >= 4 && warp < 8) cp_async_wait0();
-    tc_fence_before();
-    __syncthreads();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (*abort_flag) {
     if (warp == 8) tmem_dealloc(tmem, L::TMEM_COLS);
     return;
   }
+  (void)aborted;
 
   // ---------------- epilogue: out = (O_plain + y R_V^T) / l
   bool ok = true;
-  if (warp >= 4 && warp < 8) cp_async_wait0();
   if (warp < 8) {
-    ok = mbar_wait_bounded(pv_done, (uint32_t)((n_tiles - 1) & 1), a.status);
+    ok = __all_sync(0xffffffffu, xwait(pv_done, (uint32_t)((n_tiles - 1) & 1), a.status));
     tc_fence_after();
   }
   float* Rt = reinterpret_cast<float*>(smem + L::RT);
