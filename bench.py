@@ -56,6 +56,10 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true", help="skip the batched-decode sweep")
     ap.add_argument("--sweep-batches", default="1,8,32,64")
     ap.add_argument("--no-extra", action="store_true", help="skip the long-context, capacity and write configurations")
+    ap.add_argument("--extend-only", action="store_true",
+                    help="run only the extend-attention measurement and print its rows (a profiling entry point)")
+    ap.add_argument("--extend-configs", default="4,32768,2048;8,0,4096",
+                    help="extend workloads as requests,prefix,chunk triples separated by ';'")
     ap.add_argument("--sweep-only", action="store_true",
                     help="run only the batched-decode sweep and print its rows (a profiling entry point)")
     return ap.parse_args()
@@ -552,6 +556,71 @@ def long_and_capacity(osc, hbm_peak, steps=5, row_shift=37):
     return res
 
 
+def extend_leg(osc, bf16_peak, reps=5, row_shift=37, configs=((4, 32768, 2048), (8, 0, 4096))):
+    """Extend (chunked prefill) attention over the mixed cache, timed with CUDA events.
+
+    Prefix caching: 4 requests, each with a 32,768-token prefix already in the cache (INT2 history
+    plus the BF16 window) and a new chunk of 2,048 tokens; and plain prefill: 8 requests of 4,096
+    new tokens with no prefix.  32 q / 8 kv heads, d = 128, pages of 64.  Algorithmic work per call:
+    4 d FLOPs (QK and PV) per query row and visible key (the prefix and the causal part of the
+    chunk); the kernel's own work is about twice that (split operands, see the kernel notes), and
+    the roofline is the measured dense BF16 tensor peak."""
+    import torch
+    wl = syn.Workload("extend", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=19, dtype="bf16")
+    from int2_rotated_paged_oscar_gb300 import calibrate
+    fx = calibrate.calibrate_layer(syn.queries(wl, 0, 128, calib=True), *syn.kv_tokens(wl, 0, 128, calib=True))
+    rk, rv = torch.from_numpy(fx["R_K"]).cuda(), torch.from_numpy(fx["R_V"]).cuda()
+    i32 = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    rows = []
+    for B, npre, T in configs:
+        ppr = syn.pages_for(npre + T, 64) + 1
+        cfg, pool, slab, ctx = _ctx_for(osc, wl, 1, B, ppr)
+        bt = torch.arange(B * ppr, dtype=torch.int32, device="cuda").view(B, ppr)
+        kd, vd = _stream(wl, row_shift * (B - 1) + npre + T)
+        for b in range(B):
+            if npre:
+                o = row_shift * b
+                osc.oscar_write_kv(ctx, 0, kd[o:o + npre], vd[o:o + npre], osc.DTYPE_BF16, i32([0, npre]), i32([0]), 1,
+                                   npre, rk, rv, fx["clip_K"], fx["clip_V"], bt[b:b + 1], ppr, i32([b]))
+        osc.oscar_set_layer_clip(ctx, 0, fx["clip_K"], fx["clip_V"])
+        kn = torch.cat([kd[row_shift * b + npre:row_shift * b + npre + T] for b in range(B)])
+        vn = torch.cat([vd[row_shift * b + npre:row_shift * b + npre + T] for b in range(B)])
+        q = torch.from_numpy(syn.to_bf16_bits(syn.queries(wl, 0, B * T)).view(np.int16)).cuda()
+        out = torch.empty((B * T, 32, 128), dtype=torch.bfloat16, device="cuda")
+        wsb = osc.oscar_extend_workspace_size(cfg, B * T)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        cu, pre, slots = i32([T * b for b in range(B + 1)]), i32([npre] * B), i32(list(range(B)))
+
+        def call():
+            osc.oscar_extend_attn(ctx, 0, q, osc.DTYPE_BF16, kn, vn, osc.DTYPE_BF16, out, osc.DTYPE_BF16, cu, pre,
+                                  B, B * T, T, bt, ppr, slots, rk, rv, ws, wsb)
+        for _ in range(2):
+            call()
+        torch.cuda.synchronize()
+        assert osc.oscar_check_status(ctx) == 0
+        osc.oscar_set_timing(ctx, 1)
+        osc.oscar_reset_timing(ctx)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        kms, kl = osc.oscar_kernel_time(ctx, "extend")
+        assert osc.oscar_check_status(ctx) == 0
+        flops = 4.0 * 128 * 32 * B * sum(npre + i + 1 for i in range(T))
+        tf = flops / (ms * 1e-3) / 1e12
+        rows.append({"requests": B, "prefix_tokens": npre, "chunk_tokens": T, "ms_per_call": ms,
+                     "kernel_ms": kms / max(kl, 1), "algorithmic_tflops": tf, "bf16_peak_tflops": bf16_peak,
+                     "frac_of_bf16_peak": tf / bf16_peak, "tokens_per_s": B * T / (ms * 1e-3)})
+        osc.oscar_destroy(ctx)
+        del pool, slab, kd, vd, kn, vn, q, out, ws
+        torch.cuda.empty_cache()
+    return {"workload": "extend attention: 32 q / 8 kv heads, d=128, pages of 64, BF16 queries and chunk K/V, "
+                        "BF16 output", "bound": "tensor", "rows": rows}
+
+
 def run_ours(args, world, rank, local):
     import torch
     from int2_rotated_paged_oscar_gb300 import build as bld
@@ -813,8 +882,10 @@ def run_ours(args, world, rank, local):
     value = sum_over_ranks(value_rank, world)
     sweep = None
     extra = None
+    ext = None
     if rank == 0 and not args.no_extra:
         extra = long_and_capacity(osc, hbm_peak)
+        ext = extend_leg(osc, float(peaks.get("bf16_tflops", 1900.0)), configs=parse_extend_configs(args.extend_configs))
     if rank == 0 and not args.no_sweep:
         sweep = batch_sweep(osc, [int(x) for x in args.sweep_batches.split(",") if x], min(args.steps, 20), hbm_peak,
                             with_bf16=not args.no_bf16)
@@ -838,10 +909,31 @@ def run_ours(args, world, rank, local):
                         "ms_per_step": e2e_ms},
                 "gpu_launches": int(launches), "clocks": clk, "cpu_baseline": cpu,
                 "long_capacity_write": extra,
+                "extend": ext,
                 "batch_sweep": {"workload": "Qwen3-32B-shaped layer (64 q / 8 kv heads, d=128), ragged context "
                                             "U[8K, 32K], shuffled pages, decode only", "peak_gbs": hbm_peak,
                                 "rows": sweep}}
         print(json.dumps(line), flush=True)
+    return 0
+
+
+def parse_extend_configs(text):
+    return tuple(tuple(int(x) for x in c.split(",")) for c in text.split(";") if c.strip())
+
+
+def run_extend_only(args):
+    import torch
+    from int2_rotated_paged_oscar_gb300 import build as bld
+    bld.build()
+    import int2_rotated_paged_oscar_gb300 as osc
+    torch.cuda.set_device(0)
+    osc.load()
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    res = extend_leg(osc, float(peaks.get("bf16_tflops", 1900.0)), configs=parse_extend_configs(args.extend_configs))
+    print(json.dumps(res), flush=True)
     return 0
 
 
@@ -865,6 +957,8 @@ def main():
     world, rank, local = dist_setup(args)
     if args.sweep_only:
         return run_sweep_only(args)
+    if args.extend_only:
+        return run_extend_only(args)
     if args.impl == "reference":
         rc = run_reference(args, world, rank)
     else:
