@@ -118,12 +118,17 @@ struct XLayout {
 // ------------------------------------------------------------------ query rotation
 // q' = q R_K for every (chunk token, query head) row, float32, into the workspace; the
 // last CTA writes R_V^T for the epilogues.  CTA: 64 rows x D columns, thread (row t/4,
-// column quarter t%4).
+// column set t%4: the float4 columns 4 (t%4) + 16 m, so that the four threads of a row
+// read R from four different bank groups); q rows padded by one float (row stride D + 1
+// puts the eight rows a warp reads in different banks).
+template <int D>
+__host__ __device__ constexpr size_t qrot_smem_floats() { return (size_t)D * D + 64 * (D + 1); }
+
 template <int D>
 __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
   extern __shared__ __align__(16) float xq_sm[];
   float* Rs = xq_sm;              // [D][D]
-  float* qs = xq_sm + D * D;      // [64][D]
+  float* qs = xq_sm + D * D;      // [64][D + 1]
   const int t = threadIdx.x;
   const long long rows = (long long)a.total_tokens * a.g.Hq;
   float* qrot = reinterpret_cast<float*>(a.ws + a.qrot_off);
@@ -146,34 +151,33 @@ __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
       v = a.q_dtype == kDtypeBF16 ? __uint_as_float((uint32_t) static_cast<const uint16_t*>(a.q)[e] << 16)
                                   : static_cast<const float*>(a.q)[e];
     }
-    qs[idx] = v;
+    qs[(idx / D) * (D + 1) + idx % D] = v;
   }
   __syncthreads();
-  constexpr int NC = D / 4;
+  constexpr int NM = D / 16;   // float4 columns per thread
   const int rr = t >> 2, cq = t & 3;
-  float acc[NC];
+  float4 acc[NM];
 #pragma unroll
-  for (int j = 0; j < NC; ++j) acc[j] = 0.f;
-  const float* qrow = qs + rr * D;
+  for (int m = 0; m < NM; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float* qrow = qs + rr * (D + 1);
 #pragma unroll 4
   for (int i = 0; i < D; ++i) {
     const float qi = qrow[i];
-    const float4* rrow = reinterpret_cast<const float4*>(Rs + i * D + cq * NC);
+    const float4* rrow = reinterpret_cast<const float4*>(Rs + i * D + 4 * cq);
 #pragma unroll
-    for (int j4 = 0; j4 < NC / 4; ++j4) {
-      const float4 rv = rrow[j4];
-      acc[4 * j4] = fmaf(qi, rv.x, acc[4 * j4]);
-      acc[4 * j4 + 1] = fmaf(qi, rv.y, acc[4 * j4 + 1]);
-      acc[4 * j4 + 2] = fmaf(qi, rv.z, acc[4 * j4 + 2]);
-      acc[4 * j4 + 3] = fmaf(qi, rv.w, acc[4 * j4 + 3]);
+    for (int m = 0; m < NM; ++m) {
+      const float4 rv = rrow[4 * m];
+      acc[m].x = fmaf(qi, rv.x, acc[m].x);
+      acc[m].y = fmaf(qi, rv.y, acc[m].y);
+      acc[m].z = fmaf(qi, rv.z, acc[m].z);
+      acc[m].w = fmaf(qi, rv.w, acc[m].w);
     }
   }
   const long long r = r0 + rr;
   if (r < rows) {
-    float4* dst = reinterpret_cast<float4*>(qrot + (size_t)r * D + cq * NC);
+    float4* dst = reinterpret_cast<float4*>(qrot + (size_t)r * D + 4 * cq);
 #pragma unroll
-    for (int j4 = 0; j4 < NC / 4; ++j4)
-      dst[j4] = make_float4(acc[4 * j4], acc[4 * j4 + 1], acc[4 * j4 + 2], acc[4 * j4 + 3]);
+    for (int m = 0; m < NM; ++m) dst[4 * m] = acc[m];
   }
 }
 
@@ -1049,7 +1053,7 @@ template <int D>
 int launch_extend_d(const ExtendArgs& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long rows = (long long)a.total_tokens * a.g.Hq;
-  const size_t qsm = (size_t)(D * D + 64 * D) * sizeof(float);
+  const size_t qsm = qrot_smem_floats<D>() * sizeof(float);
   cudaError_t e = ensure_smem_limit(extend_qrot_kernel<D>, qsm);
   if (e != cudaSuccess) return (int)e;
   const unsigned qgrid = (unsigned)((rows + 63) / 64) + 1;
