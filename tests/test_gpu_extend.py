@@ -83,3 +83,46 @@ def test_extend_parity(osc, shape, prefix, chunks, q_dtype, out_bf16):
             H.assert_decode_close(got, want)
     finally:
         gc.close()
+
+
+def test_extend_on_a_forked_prefix(osc):
+    """Prefix caching end to end: request 0 writes a prefix, request 1 forks it (full history pages
+    shared, the partial page copied, the window copied), and one extend call serves both with
+    different chunks.  The oracle writes each request's prefix from scratch into its own pages."""
+    shape = syn.Shape(32, 8, 128, 64, 32, 4, 128, 1)
+    wl = syn.Workload("fork_ext", shape, [0], seed=41, dtype="bf16")
+    fx = H.fixture(wl)
+    n_pre, chunks = 1500, [90, 70]
+    ppr = 30
+    geom = H.geometry(shape, 64, 2)
+    gc = H.make_gpu_cache(geom, shape.n_q_heads, ppr)
+    try:
+        ids = osc.oscar_alloc_pages(gc.ctx, syn.pages_for(n_pre, 64))
+        bt0 = np.full(ppr, -1, np.int32)
+        bt0[:len(ids)] = ids
+        k, v = syn.kv_tokens(wl, 0, n_pre)
+        osc.oscar_write_kv(gc.ctx, 0, H.dev_input(k, "bf16"), H.dev_input(v, "bf16"), osc.DTYPE_BF16,
+                           H.dev(np.array([0, n_pre], np.int32)), H.dev(np.zeros(1, np.int32)), 1, n_pre,
+                           H.dev(fx["R_K"]), H.dev(fx["R_V"]), fx["clip_K"], fx["clip_V"], H.dev(bt0[None]), ppr,
+                           H.dev(np.array([0], np.int32)))
+        import torch
+        torch.cuda.synchronize()
+        bt1 = np.array(osc.oscar_fork_prefix(gc.ctx, bt0, n_pre, 0, 1, ppr, stream=None), np.int32)
+        shared = int(np.sum((bt1 == bt0) & (bt0 >= 0)))
+        assert shared >= (n_pre - shape.recent - shape.sink) // 64 - 1, "full history pages are shared"
+        bt = np.stack([bt0, bt1])
+        total = sum(chunks)
+        kc, vc = syn.kv_tokens(wl, 0, total, sub=9)
+        q = syn.queries(wl, 0, total, sub=10)
+        cu = np.array([0, chunks[0], total], np.int32)
+        got = H.run_extend(gc, 0, q, "bf16", kc, vc, cu, [n_pre, n_pre], bt, [0, 1], fx)
+        # oracle: both prefixes written from scratch into separate pages
+        bt_o = np.stack([np.arange(ppr), ppr + np.arange(ppr)]).astype(np.int32)
+        img = cache.CacheImage(H.geometry(shape, 2 * ppr, 2))
+        for i in range(2):
+            cache.write_kv(img, 0, k, v, [0, n_pre], [0], fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"],
+                           bt_o[i:i + 1], [i])
+        want = attention.extend(img, 0, q, kc, vc, cu, [n_pre, n_pre], bt_o, [0, 1], fx["R_K"], fx["R_V"])
+        H.assert_decode_close(got, want)
+    finally:
+        gc.close()
