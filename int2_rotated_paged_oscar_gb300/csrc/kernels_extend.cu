@@ -24,10 +24,10 @@
 //   centre term = one more MMA (K = 16): the q' group sums Q_g in three f16 terms times
 //                the centres m = z + 1.5 s in two (hi, lo), the four (five for d = 64)
 //                largest of the six cross products,
-//   V operand  = (code - 1.5) * s_V * 2^(k_V + pos - 10), the slot factor 2^(10 - pos)
-//   and the V centres (a 16-column accumulator of sum_j p_j m_j, hi and lo columns)
-//   applied in the epilogue,
-//   P as f16 hi + lo (weights <= 2^14), the row sum l taken over the rounded pair.
+//   V operand  = (code - 1.5) * s_V * 2^(k_V + pos - 10), with the V centres (hi and lo
+//   rows) appended as 16 more B rows, so that one MMA with N = D + 16 also accumulates
+//   sum_j p_j m_j; the slot factor 2^(10 - pos) and the centres are applied in the epilogue,
+//   P as f16 hi + lo (weights <= 2^14), the row sum l kept in float32.
 // BF16 tiles run in the plain basis with BF16 operands: Q as hi + lo (hi alone for a BF16
 // query), P as three BF16 terms (24 bits; the values are unbounded BF16), K and V exactly
 // as stored.  Both kinds share one running softmax reference per row; the two
