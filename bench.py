@@ -151,6 +151,14 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ distributed (replicas)
+# One process per GPU, each running its own replica of the workload (the path shards by
+# request and kv head with no exchange).  The only collectives are the host-side barrier
+# and the max / sum of per-rank figures.  OSCAR_DIST_BACKEND=gloo runs the same logic on
+# CPU processes (tests); the default is NCCL.
+def dist_backend():
+    return os.environ.get("OSCAR_DIST_BACKEND", "nccl")
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -158,8 +166,9 @@ def dist_setup(args):
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if dist_backend() == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(dist_backend())
     return world, rank, local
 
 
@@ -169,24 +178,21 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
-    if world == 1:
-        return x
+def _all_reduce(x, op_name):
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cuda" if dist_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=getattr(dist.ReduceOp, op_name))
     return float(t.item())
+
+
+def max_over_ranks(x, world):
+    return x if world == 1 else _all_reduce(x, "MAX")
 
 
 def sum_over_ranks(x, world):
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return x if world == 1 else _all_reduce(x, "SUM")
 
 
 # ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
