@@ -562,7 +562,7 @@ def long_and_capacity(osc, hbm_peak, steps=5, row_shift=37):
     return res
 
 
-def extend_leg(osc, bf16_peak, reps=5, row_shift=37, configs=((4, 32768, 2048), (8, 0, 4096))):
+def extend_leg(osc, bf16_peak, reps=5, row_shift=37, configs=((4, 32768, 2048), (8, 0, 4096)), with_cpu=False):
     """Extend (chunked prefill) attention over the mixed cache, timed with CUDA events.
 
     Prefix caching: 4 requests, each with a 32,768-token prefix already in the cache (INT2 history
@@ -623,8 +623,34 @@ def extend_leg(osc, bf16_peak, reps=5, row_shift=37, configs=((4, 32768, 2048), 
         osc.oscar_destroy(ctx)
         del pool, slab, kd, vd, kn, vn, q, out, ws
         torch.cuda.empty_cache()
-    return {"workload": "extend attention: 32 q / 8 kv heads, d=128, pages of 64, BF16 queries and chunk K/V, "
-                        "BF16 output", "bound": "tensor", "rows": rows}
+    res = {"workload": "extend attention: 32 q / 8 kv heads, d=128, pages of 64, BF16 queries and chunk K/V, "
+                       "BF16 output", "bound": "tensor", "rows": rows}
+    if with_cpu:
+        res["cpu_baseline"] = oracle_extend_sample(wl, fx, row_shift)
+    return res
+
+
+def oracle_extend_sample(wl, fx, row_shift, npre=32768, t=8):
+    """The oracle's extend on the host cores, a bounded sample of the prefix-cache workload: one request
+    with the 32K-token prefix (written into an oracle cache image) and the first t tokens of its chunk."""
+    from oracle import attention, cache
+    s = wl.shape
+    g = cache.Geometry(1, s.n_kv_heads, s.head_dim, s.page_size, s.group_size, s.sink, s.recent,
+                       syn.pages_for(npre + t, s.page_size), 1)
+    img = cache.CacheImage(g)
+    bt = np.arange(g.num_pages, dtype=np.int32)[None]
+    k, v = syn.kv_tokens(wl, 0, npre + t)
+    cache.write_kv(img, 0, k[:npre], v[:npre], [0, npre], [0], fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"],
+                   bt, [0])
+    q = syn.queries(wl, 0, t)
+    t0 = time.perf_counter()
+    attention.extend(img, 0, q, k[npre:], v[npre:], [0, t], [npre], bt, [0], fx["R_K"], fx["R_V"])
+    sec = time.perf_counter() - t0
+    flops = 4.0 * s.head_dim * s.n_q_heads * sum(npre + i + 1 for i in range(t))
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": flops / sec / 1e12, "unit": "TFLOP/s (algorithmic)", "cores": cores, "kind": "oracle",
+            "sample": f"float64 oracle extend of one request: {npre}-token cached prefix, first {t} chunk tokens "
+                      f"({sec:.1f} s)"}
 
 
 def run_ours(args, world, rank, local):
@@ -891,7 +917,8 @@ def run_ours(args, world, rank, local):
     ext = None
     if rank == 0 and not args.no_extra:
         extra = long_and_capacity(osc, hbm_peak)
-        ext = extend_leg(osc, float(peaks.get("bf16_tflops", 1900.0)), configs=parse_extend_configs(args.extend_configs))
+        ext = extend_leg(osc, float(peaks.get("bf16_tflops", 1900.0)), configs=parse_extend_configs(args.extend_configs),
+                         with_cpu=not args.no_cpu_baseline)
     if rank == 0 and not args.no_sweep:
         sweep = batch_sweep(osc, [int(x) for x in args.sweep_batches.split(",") if x], min(args.steps, 20), hbm_peak,
                             with_bf16=not args.no_bf16)
