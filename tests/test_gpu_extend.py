@@ -56,7 +56,9 @@ def _image(gc, geom):
     (syn.Shape(8, 4, 64, 16, 32, 4, 32, 1), [300, 35], [70, 9], "f32", False),
     (syn.Shape(8, 8, 128, 32, 32, 0, 64, 1), [500, 64], [130, 1], "f32", True),
     (syn.Shape(64, 8, 128, 64, 32, 4, 128, 1), [260], [40], "bf16", False),
-], ids=["d128_p64_gq4", "d64_p16_gq2", "d128_p32_gq1_nosink_bf16out", "d128_p64_gq8"])
+    # edges: window exactly full (no history), one history token, sink only, an empty chunk
+    (syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [132, 133, 4, 200], [17, 0, 5, 64], "f32", False),
+], ids=["d128_p64_gq4", "d64_p16_gq2", "d128_p32_gq1_nosink_bf16out", "d128_p64_gq8", "edges"])
 def test_extend_parity(osc, shape, prefix, chunks, q_dtype, out_bf16):
     wl = syn.Workload("ext", shape, [0], seed=31, dtype="bf16")
     fx = H.fixture(wl)
