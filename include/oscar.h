@@ -280,8 +280,9 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
  * values are the K_new / V_new rows themselves.  Call it before writing the
  * chunk (oscar_write_kv with start_pos = prefix_lens): the cache must hold
  * exactly prefix_lens[b] tokens of request b.
- *  q: [total_tokens][n_q_heads][d] (q_dtype); K_new, V_new:
- *  [total_tokens][n_kv_heads][d] BF16 (other kv_dtype: OSCAR_ERR_UNSUPPORTED);
+ *  q: [total_tokens][n_q_heads][d] BF16; K_new, V_new: [total_tokens]
+ *  [n_kv_heads][d] BF16 (another q_dtype or kv_dtype: OSCAR_ERR_UNSUPPORTED;
+ *  the BF16 tiles take the query exactly as a BF16 tensor-core operand);
  *  out: [total_tokens][n_q_heads][d] float32 or bf16 (out_dtype).  q, K_new,
  *  V_new and out 16-byte aligned.  cu_seqlens [batch+1], prefix_lens [batch],
  *  req_slot [batch]: device int32; total_tokens = cu_seqlens[batch] and

@@ -28,8 +28,8 @@
 //   rows) appended as 16 more B rows, so that one MMA with N = D + 16 also accumulates
 //   sum_j p_j m_j; the slot factor 2^(10 - pos) and the centres are applied in the epilogue,
 //   P as f16 hi + lo (weights <= 2^14), the row sum l kept in float32.
-// BF16 tiles run in the plain basis with BF16 operands: Q as hi + lo (hi alone for a BF16
-// query), P as three BF16 terms (24 bits; the values are unbounded BF16), K and V exactly
+// BF16 tiles run in the plain basis with BF16 operands: Q as received (the query is BF16),
+// P as three BF16 terms (24 bits; the values are unbounded BF16), K and V exactly
 // as stored.  Both kinds share one running softmax reference per row; the two
 // output accumulators (rotated and plain) are rescaled together.  The epilogue forms
 // out = (O_plain + y R_V^T) / l, y the rotated accumulator put back to value scale.
@@ -148,8 +148,7 @@ __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
     float v = 0.f;
     if (r < rows) {
       const size_t e = (size_t)r * D + idx % D;
-      v = a.q_dtype == kDtypeBF16 ? __uint_as_float((uint32_t) static_cast<const uint16_t*>(a.q)[e] << 16)
-                                  : static_cast<const float*>(a.q)[e];
+      v = __uint_as_float((uint32_t) static_cast<const uint16_t*>(a.q)[e] << 16);   // BF16 query
     }
     qs[(idx / D) * (D + 1) + idx % D] = v;
   }
@@ -445,7 +444,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     *reinterpret_cast<uint4*>(smem + L::QZ + sw128_offset(r, 0, kXRows)) = hz4[0];
     *reinterpret_cast<uint4*>(smem + L::QZ + sw128_offset(r, 8, kXRows)) = hz4[1];
   };
-  // Q planes for BF16 tiles: q as BF16 hi + lo (16 bits)
+  // Q plane for BF16 tiles: the BF16 query itself (the lo plane stays zero and is skipped)
   auto write_q_plain = [&]() {
 #pragma unroll 2
     for (int m = 0; m < D / 8; ++m) {
@@ -453,18 +452,12 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
 #pragma unroll
       for (int k = 0; k < 8; ++k) v[k] = 0.f;
       if (row_ok) {
-        if (a.q_dtype == kDtypeBF16) {
-          const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + qrow * D + 8 * m);
-          const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+        const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + qrow * D + 8 * m);
+        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            v[2 * k] = bf16_lo(ws4[k]);
-            v[2 * k + 1] = bf16_hi(ws4[k]);
-          }
-        } else {
-          const float4* s4 = reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + qrow * D + 8 * m);
-          const float4 x0 = s4[0], x1 = s4[1];
-          v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+        for (int k = 0; k < 4; ++k) {
+          v[2 * k] = bf16_lo(ws4[k]);
+          v[2 * k + 1] = bf16_hi(ws4[k]);
         }
       }
       uint32_t hi[4], lo[4];
@@ -697,8 +690,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     const uint32_t dS = tmem + L::C_S + (uint32_t)((j & 1) * kXKeys);
     const bool rot = tl.kind(j) == kTileInt2;
     const uint32_t idesc = rot ? idesc_f16_f32(kXRows, kXKeys) : idesc_bf16_f32(kXRows, kXKeys);
-    // a BF16 query has no lo part: the plain tiles skip that plane
-    const int planes = (rot || a.q_dtype != kDtypeBF16) ? 2 : 1;
+    // the BF16 query is exact in one plane: the plain tiles skip the lo plane
+    const int planes = rot ? 2 : 1;
 #pragma unroll
     for (int pl = 0; pl < 2; ++pl)
       if (pl < planes)

@@ -859,7 +859,7 @@ oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
       !workspace)
     return fail(OSCAR_ERR_INVALID, "null tensor argument");
   if (kv_dtype != OSCAR_DTYPE_BF16) return fail(OSCAR_ERR_UNSUPPORTED, "extend: K_new / V_new must be BF16");
-  if (q_dtype != OSCAR_DTYPE_BF16 && q_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad q dtype");
+  if (q_dtype != OSCAR_DTYPE_BF16) return fail(OSCAR_ERR_UNSUPPORTED, "extend: q must be BF16");
   if (out_dtype != OSCAR_DTYPE_BF16 && out_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad out dtype");
   if (128 % ctx->g.gq() != 0)
     return fail(OSCAR_ERR_UNSUPPORTED, "extend: n_q_heads / n_kv_heads = %d must divide 128", ctx->g.gq());

@@ -53,11 +53,11 @@ def _image(gc, geom):
 
 @pytest.mark.parametrize("shape,prefix,chunks,q_dtype,out_bf16", [
     (syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [1300, 0, 90, 700], [200, 150, 37, 64], "bf16", False),
-    (syn.Shape(8, 4, 64, 16, 32, 4, 32, 1), [300, 35], [70, 9], "f32", False),
-    (syn.Shape(8, 8, 128, 32, 32, 0, 64, 1), [500, 64], [130, 1], "f32", True),
+    (syn.Shape(8, 4, 64, 16, 32, 4, 32, 1), [300, 35], [70, 9], "bf16", False),
+    (syn.Shape(8, 8, 128, 32, 32, 0, 64, 1), [500, 64], [130, 1], "bf16", True),
     (syn.Shape(64, 8, 128, 64, 32, 4, 128, 1), [260], [40], "bf16", False),
     # edges: window exactly full (no history), one history token, sink only, an empty chunk
-    (syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [132, 133, 4, 200], [17, 0, 5, 64], "f32", False),
+    (syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [132, 133, 4, 200], [17, 0, 5, 64], "bf16", False),
 ], ids=["d128_p64_gq4", "d64_p16_gq2", "d128_p32_gq1_nosink_bf16out", "d128_p64_gq8", "edges"])
 def test_extend_parity(osc, shape, prefix, chunks, q_dtype, out_bf16):
     wl = syn.Workload("ext", shape, [0], seed=31, dtype="bf16")
@@ -66,9 +66,7 @@ def test_extend_parity(osc, shape, prefix, chunks, q_dtype, out_bf16):
     try:
         total = sum(chunks)
         k, v = syn.kv_tokens(wl, 0, total, sub=7)
-        q = syn.queries(wl, 0, total, sub=8)
-        if q_dtype == "f32":
-            q = q * np.float32(1.0 + 1.0 / 3.0)   # values off the BF16 grid
+        q = syn.queries(wl, 0, total, sub=8)   # BF16-valued (the workload's dtype)
         cu = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
         slots = np.arange(len(prefix), dtype=np.int32)
         got = H.run_extend(gc, 0, q, q_dtype, k, v, cu, prefix, bt, slots, fx, out_bf16=out_bf16)
