@@ -132,6 +132,15 @@ oscar_status oscar_unref_pages(oscar_ctx* ctx, const int32_t* ids, int32_t n);
 oscar_status oscar_page_refcount(oscar_ctx* ctx, int32_t id, int32_t* out_refcount);
 oscar_status oscar_free_page_count(oscar_ctx* ctx, int32_t* out_n);
 
+/* Copy the INT2 blocks of n pages of one layer to host memory (a test and
+ * debugging aid; the cache itself is transient serving state).  host_dst
+ * receives n x [n_kv_heads][block] bytes, page ids[i] at offset i x n_kv_heads
+ * x block bytes (the layout above).  Synchronous: it waits for the copies (and
+ * so for earlier work on the legacy default stream).  A page id outside
+ * [0, num_pages) returns OSCAR_ERR_INVALID and copies nothing.  ids is a host
+ * array. */
+oscar_status oscar_read_pages(oscar_ctx* ctx, int32_t layer, const int32_t* ids, int32_t n, void* host_dst);
+
 /* Pages a request of length n needs mapped: logical pages 0 .. (n_hist_end-1)/P
  * where n_hist_end = n - recent (0 if no history). */
 int32_t oscar_pages_needed(const oscar_config* cfg, int32_t seq_len);

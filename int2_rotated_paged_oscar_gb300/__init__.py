@@ -67,6 +67,7 @@ _SIGS = {
     "oscar_page_refcount": (_i32, [_vp, _i32, _c_i32p]),
     "oscar_free_page_count": (_i32, [_vp, _c_i32p]),
     "oscar_pages_needed": (_i32, [_cfgp, _i32]),
+    "oscar_read_pages": (_i32, [_vp, _i32, _c_i32p, _i32, _vp]),
     "oscar_fork_prefix": (_i32, [_vp, _c_i32p, _c_i32p, _i32, _i32, _i32, _vp]),
     "oscar_write_kv": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _f32, _f32, _vp, _i32,
                               _vp, _vp]),
@@ -196,6 +197,16 @@ def oscar_free_page_count(ctx: int) -> int:
 
 def oscar_pages_needed(cfg: oscar_config, seq_len: int) -> int:
     return load().oscar_pages_needed(ctypes.byref(cfg), seq_len)
+
+
+def oscar_read_pages(ctx: int, cfg: oscar_config, layer: int, ids: Sequence[int]):
+    """The INT2 blocks of pages ``ids`` of ``layer`` as a host uint8 array [len(ids), n_kv_heads, block bytes]
+    (``cfg`` is the context's configuration; it gives the array's shape)."""
+    import numpy as np
+    bb = oscar_page_block_bytes(cfg)
+    out = np.empty((len(ids), cfg.n_kv_heads, bb), np.uint8)
+    _check(load().oscar_read_pages(ctx, layer, _i32_array(list(ids)), len(ids), out.ctypes.data))
+    return out
 
 
 def oscar_fork_prefix(ctx: int, src_bt: Sequence[int], n: int, src_slot: int, dst_slot: int, max_pages: int,

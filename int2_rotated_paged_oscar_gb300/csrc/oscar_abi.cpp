@@ -411,6 +411,24 @@ oscar_status oscar_free_page_count(oscar_ctx* ctx, int32_t* out_n) {
   return OSCAR_OK;
 }
 
+oscar_status oscar_read_pages(oscar_ctx* ctx, int32_t layer, const int32_t* ids, int32_t n, void* host_dst) {
+  oscar_status st = need_device(ctx);
+  if (st != OSCAR_OK) return st;
+  if ((st = check_layer(ctx, layer)) != OSCAR_OK) return st;
+  if (n < 0 || (n > 0 && (!ids || !host_dst))) return fail(OSCAR_ERR_INVALID, "bad arguments to oscar_read_pages");
+  for (int32_t i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= ctx->g.num_pages)
+      return fail(OSCAR_ERR_INVALID, "page id %d out of [0, %d)", ids[i], ctx->g.num_pages);
+  const size_t bytes = (size_t)ctx->g.Hkv * ctx->g.block_bytes();
+  for (int32_t i = 0; i < n; ++i) {
+    const uint8_t* src = ctx->pool + ((size_t)layer * ctx->g.num_pages + ids[i]) * bytes;
+    const cudaError_t e = cudaMemcpy(static_cast<uint8_t*>(host_dst) + (size_t)i * bytes, src, bytes,
+                                     cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read pages");
+  }
+  return OSCAR_OK;
+}
+
 int32_t oscar_pages_needed(const oscar_config* cfg, int32_t seq_len) {
   Geom g;
   if (validate(cfg, &g) != OSCAR_OK || seq_len < 0) return -1;

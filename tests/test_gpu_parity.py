@@ -476,3 +476,20 @@ def test_bf16_paged_decode_parity(osc, hq, lens):
         H.assert_decode_close(out.cpu().numpy().astype(np.float64), want)
     finally:
         gc.close()
+
+
+def test_read_pages_copies_the_blocks(osc):
+    """oscar_read_pages returns exactly the pool's blocks of the requested pages (any order), and rejects
+    page ids out of range."""
+    wl = syn.Workload("rp", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=3)
+    fx = H.fixture(wl)
+    bt = _contiguous_bt(1, 12)
+    gc, img, diag, _, _ = _prefill_both(osc, wl, fx, [600], bt, 12)
+    try:
+        ids = [5, 0, 3]
+        got = osc.oscar_read_pages(gc.ctx, gc.cfg, 0, ids)
+        assert np.array_equal(got, gc.pool_np()[0, ids])
+        with pytest.raises(osc.OscarError):
+            osc.oscar_read_pages(gc.ctx, gc.cfg, 0, [12])
+    finally:
+        gc.close()
