@@ -773,6 +773,18 @@ def run_ours(args, world, rank, local):
     clk = clocks.stop()
     st = osc.oscar_check_status(ctx)
     assert st == 0, f"device status {st}"
+    # per-replay spread, a separate measurement after the timed region: each of up to 50 step
+    # replays between its own pair of events
+    nd = min(50, args.steps)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nd)]
+    for e_a, e_b in evs:
+        e_a.record()
+        g_step.replay()
+        e_b.record()
+    torch.cuda.synchronize()
+    rep = np.array(sorted(e_a.elapsed_time(e_b) for e_a, e_b in evs))
+    step_spread = {"replays": nd, "p10_ms": float(np.percentile(rep, 10)), "p50_ms": float(np.percentile(rep, 50)),
+                   "p90_ms": float(np.percentile(rep, 90))}
     n_mid = n_start + args.steps // 2 + 1
     db = decode_bytes(n_mid)
     bytes_step = L * (sum(db.values()) + append_bytes())
@@ -933,6 +945,7 @@ def run_ours(args, world, rank, local):
                 "vs_baseline": None, "dtype": "int2 codes, f16/bf16 MMA, f32 accumulate", "data": "synthetic",
                 "config": workload_config(L),
                 "decode_steps_per_s": 1000.0 / step_ms,
+                "step_spread": step_spread,
                 "bytes_per_step": bytes_step,
                 "hbm_roofline_frac_of_step": value_rank / hbm_peak,
                 "roofline": roofline, "bf16_comparison": bf16_info,
