@@ -241,6 +241,19 @@ def oracle_decode_sample(target_s=15.0, max_reps=50):
             "sample": f"oracle float64 decode of 1 layer (batch 1, n={n}, 32q/8kv heads, d=128), {reps} reps"}
 
 
+def oracle_decode_one_thread(target_s=5.0):
+    """The same oracle sample with the BLAS and OpenMP pools limited to one thread (a subprocess, so
+    that the limits hold from the first import); None if the sample fails."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.oracle_decode_sample(target_s=%r, max_reps=3)))" % (ROOT, target_s))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return None
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
@@ -938,6 +951,9 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.no_cpu_baseline:
         r = oracle_decode_sample(target_s=15.0)
         cpu = {"value": r["gbs"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
+        r1 = oracle_decode_one_thread()
+        if r1 is not None:
+            cpu["one_thread"] = {"value": r1["gbs"], "unit": "GB/s", "cores": 1, "sample": r1["sample"]}
     osc.oscar_destroy(ctx)
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
