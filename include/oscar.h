@@ -295,7 +295,8 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
  *  out: [total_tokens][n_q_heads][d] float32 or bf16 (out_dtype).  q, K_new,
  *  V_new and out 16-byte aligned.  cu_seqlens [batch+1], prefix_lens [batch],
  *  req_slot [batch]: device int32; total_tokens = cu_seqlens[batch] and
- *  max_chunk >= every len_b (host values, they size the grids).
+ *  max_chunk >= every len_b (host values, they size the grids; a request whose
+ *  chunk they do not cover sets OSCAR_DEV_BAD_LEN and gets no output).
  *  block_table [batch][bt_stride] maps the history pages of each prefix (a
  *  missing one sets OSCAR_DEV_BAD_PAGE); R_K, R_V: the layer's rotations
  *  (device float32 [d][d]); the layer needs a declared clip threshold.

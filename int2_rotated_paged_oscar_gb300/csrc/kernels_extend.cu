@@ -293,6 +293,12 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   const int i0 = blockIdx.x * tq;
   const int c0 = a.cu_seqlens[b];
   const int len = a.cu_seqlens[b + 1] - c0;
+  // the host sizes (max_chunk, total_tokens) must cover the device lengths: a chunk longer than
+  // the grid or past the rotated rows would go partly uncomputed
+  if (len < 0 || c0 < 0 || c0 + len > a.total_tokens || len > (int)gridDim.x * tq) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.status, kDevBadLen);
+    return;
+  }
   if (i0 >= len) return;
   const int n_pre = a.prefix_lens[b];
   if (n_pre < 0 || (long long)n_pre > (long long)g.max_pages_per_req * g.P) {

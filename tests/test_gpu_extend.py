@@ -126,3 +126,31 @@ def test_extend_on_a_forked_prefix(osc):
         H.assert_decode_close(got, want)
     finally:
         gc.close()
+
+
+def test_extend_flags_host_sizes_that_miss_a_chunk(osc):
+    """A max_chunk below a request's chunk length sets OSCAR_DEV_BAD_LEN (no silent partial output);
+    the context stays usable and a correct call afterwards reports no error."""
+    import torch
+    shape = syn.Shape(32, 8, 128, 64, 32, 4, 128, 1)
+    wl = syn.Workload("badlen", shape, [0], seed=43, dtype="bf16")
+    fx = H.fixture(wl)
+    gc, geom, bt = _setup(wl, fx, [300])
+    try:
+        t = 100
+        k, v = syn.kv_tokens(wl, 0, t, sub=3)
+        q = syn.queries(wl, 0, t, sub=4)
+        cu = np.array([0, t], np.int32)
+        ws_bytes = osc.oscar_extend_workspace_size(gc.cfg, t)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        out = torch.zeros((t, shape.n_q_heads, shape.head_dim), dtype=torch.float32, device="cuda")
+        osc.oscar_set_layer_clip(gc.ctx, 0, fx["clip_K"], fx["clip_V"])
+        osc.oscar_extend_attn(gc.ctx, 0, H.dev_input(q, "bf16"), osc.DTYPE_BF16, H.dev_input(k, "bf16"),
+                              H.dev_input(v, "bf16"), osc.DTYPE_BF16, out, osc.DTYPE_F32, H.dev(cu),
+                              H.dev(np.array([300], np.int32)), 1, t, 40, H.dev(bt), bt.shape[1],
+                              H.dev(np.zeros(1, np.int32)), H.dev(fx["R_K"]), H.dev(fx["R_V"]), ws, ws_bytes)
+        assert osc.oscar_check_status(gc.ctx) & osc.DEV_BAD_LEN
+        got = H.run_extend(gc, 0, q, "bf16", k, v, cu, [300], bt, [0], fx)   # asserts a clean status
+        assert np.all(np.isfinite(got))
+    finally:
+        gc.close()
