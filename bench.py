@@ -248,10 +248,13 @@ def oracle_decode_one_thread(target_s=5.0):
                BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
     code = ("import json, sys; sys.path.insert(0, %r); import bench; "
             "print(json.dumps(bench.oracle_decode_sample(target_s=%r, max_reps=3)))" % (ROOT, target_s))
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
-    if r.returncode != 0:
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+        if r.returncode != 0:
+            return None
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.TimeoutExpired, ValueError, IndexError):
         return None
-    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def run_reference(args, world, rank):
