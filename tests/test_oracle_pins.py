@@ -561,3 +561,25 @@ def test_extend_is_causal_and_requests_are_independent():
     assert np.array_equal(moved[:3], both[:3])
     assert not np.allclose(moved[3:lens[0]], both[3:lens[0]])
     assert np.array_equal(moved[lens[0]:], both[lens[0]:])
+
+
+def test_extend_is_invariant_under_within_group_channel_permutation():
+    """R' = R P with P permuting channels inside each group of 32: every group keeps its values (same
+    min, max, scale, zero), the codes move with the channels, and y_hat' R'^T = y_hat R^T.  So extend
+    over a prefix written with R' equals extend over the prefix written with R (history, window and
+    chunk all visible); a transposed or misapplied R in the rotate-back breaks the equality."""
+    g = _geom(num_pages=40, d=64, p=16, s=4, w=8, hkv=2)
+    wl, fx = _fixture()
+    rng = np.random.default_rng(5)
+    perm = np.concatenate([32 * gi + rng.permutation(32) for gi in range(2)])
+    outs = []
+    for rk, rv in ((fx["R_K"], fx["R_V"]), (fx["R_K"][:, perm], fx["R_V"][:, perm])):
+        img = cache.CacheImage(g)
+        bt = np.arange(40, dtype=np.int32)[None, :]
+        k, v = syn.kv_tokens(wl, 0, 90)
+        cache.write_kv(img, 0, k, v, [0, 90], [0], rk, rv, fx["clip_K"], fx["clip_V"], bt, [0])
+        kc, vc = _chunk(wl, 6)
+        q = syn.queries(wl, 0, 6, sub=3)
+        outs.append(attention.extend(img, 0, q, kc, vc, [0, 6], [90], bt, [0], rk, rv))
+    assert np.allclose(outs[0], outs[1], rtol=1e-12, atol=1e-12)
+    assert not np.allclose(outs[0], 0.0)
