@@ -314,6 +314,21 @@ oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
                                const int32_t* req_slot, const float* R_K, const float* R_V, void* workspace,
                                size_t ws_bytes, void* stream);
 
+/* One chunked-prefill step of a layer: oscar_extend_attn followed by
+ * oscar_write_kv of the same chunk (start_pos = prefix_lens), with the
+ * arguments of those two calls on one stream (identical outputs and cache
+ * contents).  The write runs after the attention has read the window slots and
+ * pages it overwrites.  clip_K and clip_V are declared for the layer first, so
+ * the first chunk of a fresh layer may use this call.  The caller maps the pages
+ * that the chunk's history tokens (and the ring tokens it evicts) land in,
+ * as for oscar_write_kv. */
+oscar_status oscar_extend_step(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, const void* K_new,
+                               const void* V_new, int32_t kv_dtype, void* out, int32_t out_dtype,
+                               const int32_t* cu_seqlens, const int32_t* prefix_lens, int32_t batch,
+                               int32_t total_tokens, int32_t max_chunk, const int32_t* block_table, int32_t bt_stride,
+                               const int32_t* req_slot, const float* R_K, const float* R_V, float clip_K,
+                               float clip_V, void* workspace, size_t ws_bytes, void* stream);
+
 /* In-house comparison: standard split-K paged decode over an all-BF16 cache
  * (layout above), same grid and staging as the INT2 kernel.  bf16_pool points
  * at the whole [num_layers][num_pages]... pool; workspace from

@@ -83,6 +83,8 @@ _SIGS = {
     "oscar_decode_attn_noalloc": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32,
                                          _i32, _vp, _vp, _vp]),
     "oscar_extend_workspace_size": (_i32, [_cfgp, _i32, ctypes.POINTER(ctypes.c_size_t)]),
+    "oscar_extend_step": (_i32, [_vp, _i32, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _vp,
+                                 _i32, _vp, _vp, _vp, _f32, _f32, _vp, ctypes.c_size_t, _vp]),
     "oscar_extend_attn": (_i32, [_vp, _i32, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _vp,
                                  _i32, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "oscar_bf16_decode_workspace_size": (_i32, [_cfgp, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)]),
@@ -291,6 +293,15 @@ def oscar_extend_attn(ctx, layer, q, q_dtype, K_new, V_new, kv_dtype, out, out_d
                                     out_dtype, ptr(cu_seqlens), ptr(prefix_lens), batch, total_tokens, max_chunk,
                                     ptr(block_table), bt_stride, ptr(req_slot), ptr(R_K), ptr(R_V), ptr(workspace),
                                     ws_bytes, stream_ptr(stream)))
+
+
+def oscar_extend_step(ctx, layer, q, q_dtype, K_new, V_new, kv_dtype, out, out_dtype, cu_seqlens, prefix_lens, batch,
+                      total_tokens, max_chunk, block_table, bt_stride, req_slot, R_K, R_V, clip_K, clip_V, workspace,
+                      ws_bytes, stream=None) -> None:
+    _check(load().oscar_extend_step(ctx, layer, ptr(q), q_dtype, ptr(K_new), ptr(V_new), kv_dtype, ptr(out),
+                                    out_dtype, ptr(cu_seqlens), ptr(prefix_lens), batch, total_tokens, max_chunk,
+                                    ptr(block_table), bt_stride, ptr(req_slot), ptr(R_K), ptr(R_V), float(clip_K),
+                                    float(clip_V), ptr(workspace), ws_bytes, stream_ptr(stream)))
 
 
 def oscar_bf16_decode_attn(ctx, layer, bf16_pool, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens,

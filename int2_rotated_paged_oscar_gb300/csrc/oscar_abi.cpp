@@ -924,6 +924,26 @@ oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
   return OSCAR_OK;
 }
 
+oscar_status oscar_extend_step(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, const void* K_new,
+                               const void* V_new, int32_t kv_dtype, void* out, int32_t out_dtype,
+                               const int32_t* cu_seqlens, const int32_t* prefix_lens, int32_t batch,
+                               int32_t total_tokens, int32_t max_chunk, const int32_t* block_table, int32_t bt_stride,
+                               const int32_t* req_slot, const float* R_K, const float* R_V, float clip_K,
+                               float clip_V, void* workspace, size_t ws_bytes, void* stream) {
+  oscar_status st = need_device(ctx);
+  if (st != OSCAR_OK) return st;
+  if ((st = check_layer(ctx, layer)) != OSCAR_OK) return st;
+  // the chunk's write declares these clips anyway; declaring them first lets the first chunk of a
+  // fresh layer attend (its prefix is empty, so nothing was written with another clip)
+  if ((st = record_clip(ctx, layer, clip_K, clip_V)) != OSCAR_OK) return st;
+  st = oscar_extend_attn(ctx, layer, q, q_dtype, K_new, V_new, kv_dtype, out, out_dtype, cu_seqlens, prefix_lens,
+                         batch, total_tokens, max_chunk, block_table, bt_stride, req_slot, R_K, R_V, workspace,
+                         ws_bytes, stream);
+  if (st != OSCAR_OK || batch == 0 || total_tokens == 0) return st;
+  return oscar_write_kv(ctx, layer, K_new, V_new, kv_dtype, cu_seqlens, prefix_lens, batch, total_tokens, R_K, R_V,
+                        clip_K, clip_V, block_table, bt_stride, req_slot, stream);
+}
+
 oscar_status oscar_bf16_decode_attn(oscar_ctx* ctx, int32_t layer, const void* bf16_pool, const void* q,
                                     int32_t q_dtype, void* out, int32_t out_dtype, const int32_t* block_table,
                                     int32_t bt_stride, const int32_t* seq_lens, int32_t batch, int32_t max_seq,

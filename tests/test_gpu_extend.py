@@ -23,11 +23,12 @@ def osc():
     return m
 
 
-def _setup(wl, fx, prefix):
-    """GPU cache with each request's prefix written (request b in slot b, pages b*ppr ...)."""
+def _setup(wl, fx, prefix, room=0):
+    """GPU cache with each request's prefix written (request b in slot b, pages b*ppr ...); each request's
+    block-table row maps room more tokens than its prefix."""
     s = wl.shape
     b = len(prefix)
-    ppr = max(syn.pages_for(max(n, 1), s.page_size) for n in prefix) + 1
+    ppr = max(syn.pages_for(max(n + room, 1), s.page_size) for n in prefix) + 1
     bt = np.arange(b * ppr, dtype=np.int32).reshape(b, ppr)
     geom = H.geometry(s, b * ppr, b)
     gc = H.make_gpu_cache(geom, s.n_q_heads, ppr)
@@ -154,3 +155,54 @@ def test_extend_flags_host_sizes_that_miss_a_chunk(osc):
         assert np.all(np.isfinite(got))
     finally:
         gc.close()
+
+
+def test_extend_step_equals_extend_then_write(osc):
+    """oscar_extend_step = oscar_extend_attn then oscar_write_kv of the chunk: the same outputs and the same
+    cache bytes (pages and window slots), bit for bit; then a decode over the extended cache matches the oracle."""
+    import torch
+    shape = syn.Shape(32, 8, 128, 64, 32, 4, 128, 1)
+    wl = syn.Workload("xstep", shape, [0], seed=47, dtype="bf16")
+    fx = H.fixture(wl)
+    prefix, chunks = [700, 150], [300, 90]
+    outs, pools, slabs = [], [], []
+    for fused in (False, True):
+        gc, geom, bt = _setup(wl, fx, prefix, room=max(chunks))
+        ppr = bt.shape[1]
+        assert ppr * 64 >= max(p + c for p, c in zip(prefix, chunks))
+        try:
+            total = sum(chunks)
+            k, v = syn.kv_tokens(wl, 0, total, sub=11)
+            q = syn.queries(wl, 0, total, sub=12)
+            cu = np.array([0, chunks[0], total], np.int32)
+            ws_bytes = osc.oscar_extend_workspace_size(gc.cfg, total)
+            ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+            out = torch.empty((total, shape.n_q_heads, shape.head_dim), dtype=torch.float32, device="cuda")
+            args = (H.dev_input(q, "bf16"), osc.DTYPE_BF16, H.dev_input(k, "bf16"), H.dev_input(v, "bf16"),
+                    osc.DTYPE_BF16, out, osc.DTYPE_F32, H.dev(cu), H.dev(np.array(prefix, np.int32)), 2, total,
+                    max(chunks), H.dev(bt), ppr, H.dev(np.arange(2, dtype=np.int32)), H.dev(fx["R_K"]),
+                    H.dev(fx["R_V"]))
+            if fused:
+                osc.oscar_extend_step(gc.ctx, 0, *args, fx["clip_K"], fx["clip_V"], ws, ws_bytes)
+            else:
+                osc.oscar_extend_attn(gc.ctx, 0, *args, ws, ws_bytes)
+                q_d, _, k_d, v_d, _, _, _, cu_d, pre_d, _, _, _, bt_d, _, slots_d, rk_d, rv_d = args
+                osc.oscar_write_kv(gc.ctx, 0, k_d, v_d, osc.DTYPE_BF16, cu_d, pre_d, 2, total, rk_d, rv_d,
+                                   fx["clip_K"], fx["clip_V"], bt_d, ppr, slots_d)
+            assert osc.oscar_check_status(gc.ctx) == 0
+            outs.append(out.cpu().numpy())
+            pools.append(gc.pool_np().copy())
+            slabs.append(gc.slab_np().copy())
+            if fused:
+                n = [p + c for p, c in zip(prefix, chunks)]
+                qd = syn.queries(wl, 0, 2, sub=13)
+                got = H.run_decode(gc, 0, qd, "bf16", bt, n, [0, 1], fx)
+                img = cache.CacheImage(geom)
+                img.pool, img.slab = gc.pool_np(), gc.slab_np()
+                want = attention.decode(img, 0, qd, bt, n, [0, 1], fx["R_K"], fx["R_V"])
+                H.assert_decode_close(got, want)
+        finally:
+            gc.close()
+    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(pools[0], pools[1])
+    assert np.array_equal(slabs[0], slabs[1])
