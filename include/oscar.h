@@ -300,7 +300,8 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
  *  block_table [batch][bt_stride] maps the history pages of each prefix (a
  *  missing one sets OSCAR_DEV_BAD_PAGE); R_K, R_V: the layer's rotations
  *  (device float32 [d][d]); the layer needs a declared clip threshold.
- *  n_q_heads / n_kv_heads must divide 128 (else OSCAR_ERR_UNSUPPORTED).
+ *  n_q_heads / n_kv_heads must divide 128 and batch must not exceed 65535
+ *  (else OSCAR_ERR_UNSUPPORTED).
  *  workspace: device scratch of oscar_extend_workspace_size(cfg, total_tokens)
  *  bytes (256-byte aligned, no initialisation); it holds q R_K for every query
  *  row and R_V^T.  Softmax scale 1/sqrt(d), query head h reads kv head

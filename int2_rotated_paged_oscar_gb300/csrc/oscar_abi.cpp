@@ -873,6 +873,7 @@ oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
   if (batch < 0 || total_tokens < 0 || max_chunk < 0 || bt_stride < 1)
     return fail(OSCAR_ERR_INVALID, "bad batch/total_tokens/max_chunk/bt_stride");
   if (batch == 0 || total_tokens == 0) return OSCAR_OK;
+  if (batch > 65535) return fail(OSCAR_ERR_UNSUPPORTED, "extend: batch %d above 65535 (one grid dimension)", batch);
   if (!q || !K_new || !V_new || !out || !cu_seqlens || !prefix_lens || !block_table || !req_slot || !R_K || !R_V ||
       !workspace)
     return fail(OSCAR_ERR_INVALID, "null tensor argument");
