@@ -52,6 +52,7 @@ def _image(gc, geom):
     return img
 
 
+@pytest.mark.parametrize("q_scale", [1.0, 0.25])
 @pytest.mark.parametrize("shape,prefix,chunks,q_dtype,out_bf16", [
     (syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [1300, 0, 90, 700], [200, 150, 37, 64], "bf16", False),
     (syn.Shape(8, 4, 64, 16, 32, 4, 32, 1), [300, 35], [70, 9], "bf16", False),
@@ -60,14 +61,15 @@ def _image(gc, geom):
     # edges: window exactly full (no history), one history token, sink only, an empty chunk
     (syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [132, 133, 4, 200], [17, 0, 5, 64], "bf16", False),
 ], ids=["d128_p64_gq4", "d64_p16_gq2", "d128_p32_gq1_nosink_bf16out", "d128_p64_gq8", "edges"])
-def test_extend_parity(osc, shape, prefix, chunks, q_dtype, out_bf16):
+def test_extend_parity(osc, shape, prefix, chunks, q_dtype, out_bf16, q_scale):
     wl = syn.Workload("ext", shape, [0], seed=31, dtype="bf16")
     fx = H.fixture(wl)
     gc, geom, bt = _setup(wl, fx, prefix)
     try:
         total = sum(chunks)
         k, v = syn.kv_tokens(wl, 0, total, sub=7)
-        q = syn.queries(wl, 0, total, sub=8)   # BF16-valued (the workload's dtype)
+        # BF16-valued (the workload's dtype); q x 0.25 spreads the weights (a peaky softmax hides errors)
+        q = syn.queries(wl, 0, total, sub=8, scale=q_scale)
         cu = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
         slots = np.arange(len(prefix), dtype=np.int32)
         got = H.run_extend(gc, 0, q, q_dtype, k, v, cu, prefix, bt, slots, fx, out_bf16=out_bf16)
