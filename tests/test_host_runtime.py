@@ -39,6 +39,21 @@ def test_every_header_symbol_is_exported(osc):
     assert set(osc._SIGS) == names, set(osc._SIGS) ^ names
 
 
+def test_binding_argument_counts_match_the_header(osc):
+    """Each ctypes signature has as many arguments as its C prototype (a dropped or extra argument in the
+    binding would shift every later one)."""
+    header = open(os.path.join(ROOT, "include", "oscar.h")).read()
+    header = re.sub(r"/\*.*?\*/", "", header, flags=re.S)
+    proto = r"^\s*(?:oscar_status|size_t|int32_t|int64_t|const char\s*\*)\s*(oscar_[a-z0-9_]+)\s*\(([^;]*?)\)\s*;"
+    counts = {}
+    for name, params in re.findall(proto, header, flags=re.M | re.S):
+        params = params.strip()
+        counts[name] = 0 if params in ("", "void") else params.count(",") + 1
+    assert set(counts) == set(osc._SIGS)
+    bad = {n: (counts[n], len(osc._SIGS[n][1])) for n in counts if counts[n] != len(osc._SIGS[n][1])}
+    assert not bad, bad
+
+
 def test_version_and_sizes(osc):
     assert "sm_103a" in osc.oscar_version()
     c = _cfg(osc)
