@@ -341,6 +341,14 @@ oscar_status oscar_bf16_decode_attn(oscar_ctx* ctx, int32_t layer, const void* b
                                     int32_t bt_stride, const int32_t* seq_lens, int32_t batch, int32_t max_seq,
                                     void* workspace, size_t ws_bytes, void* stream);
 
+/* Self-test of the device-side failure path (no counterpart in the OSCAR
+ * paper).  Every kernel bounds its mbarrier waits and, when one runs out, sets
+ * OSCAR_DEV_TIMEOUT in the status word instead of trapping, so the context
+ * stays usable.  This call launches one small kernel that waits on a barrier
+ * nothing arrives on until limit_us microseconds (1 .. 1e6) have passed, then
+ * sets OSCAR_DEV_TIMEOUT; oscar_check_status reports it and clears it. */
+oscar_status oscar_selftest_wait_timeout(oscar_ctx* ctx, int32_t limit_us, void* stream);
+
 /* ---------------------------------------------------------------- status, tracing
  * Synchronise stream, read and clear the device status word.  Returns
  * OSCAR_ERR_DEVICE (bits in *out_bits if non-NULL) if any kernel flagged an

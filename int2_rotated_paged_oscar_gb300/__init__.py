@@ -90,6 +90,7 @@ _SIGS = {
     "oscar_bf16_decode_workspace_size": (_i32, [_cfgp, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)]),
     "oscar_bf16_decode_attn": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _vp,
                                       ctypes.c_size_t, _vp]),
+    "oscar_selftest_wait_timeout": (_i32, [_vp, _i32, _vp]),
     "oscar_check_status": (_i32, [_vp, _vp, _c_i32p]),
     "oscar_set_timing": (_i32, [_vp, _i32]),
     "oscar_kernel_time": (_i32, [_vp, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), _c_i32p]),
@@ -309,6 +310,10 @@ def oscar_bf16_decode_attn(ctx, layer, bf16_pool, q, q_dtype, out, out_dtype, bl
     _check(load().oscar_bf16_decode_attn(ctx, layer, ptr(bf16_pool), ptr(q), q_dtype, ptr(out), out_dtype,
                                          ptr(block_table), bt_stride, ptr(seq_lens), batch, max_seq, ptr(workspace),
                                          ws_bytes, stream_ptr(stream)))
+
+
+def oscar_selftest_wait_timeout(ctx, limit_us: int, stream=None) -> None:
+    _check(load().oscar_selftest_wait_timeout(ctx, int(limit_us), stream_ptr(stream)))
 
 
 def oscar_check_status(ctx, stream=None) -> int:

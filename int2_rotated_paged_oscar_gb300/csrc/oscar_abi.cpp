@@ -925,6 +925,17 @@ oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
   return OSCAR_OK;
 }
 
+oscar_status oscar_selftest_wait_timeout(oscar_ctx* ctx, int32_t limit_us, void* stream) {
+  oscar_status st = need_device(ctx);
+  if (st != OSCAR_OK) return st;
+  if (limit_us < 1 || limit_us > 1000000) return fail(OSCAR_ERR_INVALID, "limit_us %d outside [1, 1e6]", limit_us);
+  LaunchScope ls(ctx, "selftest", stream);
+  int e = oscar::launch_wait_selftest(ctx->d_status, (long long)limit_us * 1000, stream);
+  ls.done(e);
+  if (e) return cuda_fail(e, "self-test launch");
+  return OSCAR_OK;
+}
+
 oscar_status oscar_extend_step(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, const void* K_new,
                                const void* V_new, int32_t kv_dtype, void* out, int32_t out_dtype,
                                const int32_t* cu_seqlens, const int32_t* prefix_lens, int32_t batch,

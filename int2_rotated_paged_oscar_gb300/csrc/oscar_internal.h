@@ -139,6 +139,8 @@ struct ExtendArgs {
 size_t extend_workspace_bytes(const Geom& g, long long total_tokens);
 void extend_ws_offsets(const Geom& g, size_t* rvt_off, size_t* qrot_off);
 int launch_extend(const ExtendArgs& a, void* stream);
+// Self-test of the bounded-wait failure path: waits on an mbarrier that nothing arrives on.
+int launch_wait_selftest(int* status, long long limit_ns, void* stream);
 
 // Host-side planning (pure functions, no CUDA).
 DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool);

@@ -493,3 +493,31 @@ def test_read_pages_copies_the_blocks(osc):
             osc.oscar_read_pages(gc.ctx, gc.cfg, 0, [12])
     finally:
         gc.close()
+
+
+def test_bounded_wait_timeout_sets_status_and_context_stays_usable(osc):
+    """The failure path without a GPU fault: a wait on a barrier that nothing arrives on runs out after
+    20 ms and sets OSCAR_DEV_TIMEOUT; reading the status clears it, and the context then writes and
+    decodes correctly."""
+    wl = syn.tiny()
+    fx = H.fixture(wl)
+    bt = _contiguous_bt(1, 40)
+    s = wl.shape
+    geom = H.geometry(s, 40, 1)
+    gc = H.make_gpu_cache(geom, s.n_q_heads, 40)
+    try:
+        osc.oscar_selftest_wait_timeout(gc.ctx, 20000)
+        assert osc.oscar_check_status(gc.ctx) & osc.DEV_TIMEOUT
+        assert osc.oscar_check_status(gc.ctx) == 0
+    finally:
+        gc.close()
+    gc, img, diag, _, _ = _prefill_both(osc, wl, fx, [512], bt, 40)
+    try:
+        H.compare_history(gc.pool_np(), img.g, 0, diag)
+        q = syn.queries(wl, 0, 1)
+        got = H.run_decode(gc, 0, q, "f32", bt, [512], [0], fx)
+        gimg = cache.CacheImage(img.g)
+        gimg.pool, gimg.slab = gc.pool_np(), gc.slab_np()
+        H.assert_decode_close(got, attention.decode(gimg, 0, q, bt, [512], [0], fx["R_K"], fx["R_V"]))
+    finally:
+        gc.close()
