@@ -360,7 +360,7 @@ oscar_status oscar_check_status(oscar_ctx* ctx, void* stream, int32_t* out_bits)
  * oscar_kernel_time returns the summed milliseconds and launch count since the
  * last reset (synchronises the recorded events).  Names: "decode_splitk",
  * "decode_combine", "q_rotate", "step_prep", "append", "evict", "write", "bf16_prepare",
- * "bf16_decode", "bf16_combine", "extend".  Launches
+ * "bf16_decode", "bf16_combine", "extend", "selftest".  Launches
  * recorded into a CUDA graph get external event-record nodes: replay the graph
  * once, then read; the events return to the library when read, so a graph
  * captured with timing on is replayed at most once.  With timing on, the decode
