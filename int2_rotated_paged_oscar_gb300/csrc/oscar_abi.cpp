@@ -188,48 +188,53 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   DecodeWs w{};
   const int gq = g.Hq / g.Hkv;
   w.nt = gq == 8 ? 2 : 1;
-  const int stage_pages = bf16_pool ? 1 : 4;  // INT2: the 4 warps of a split CTA stream pages round-robin
   long long max_pages;
   if (bf16_pool) max_pages = max_seq > 0 ? (max_seq - 1) / g.P + 1 : 0;
   else max_pages = (max_seq - g.W > g.S) ? (long long)(max_seq - g.W - 1) / g.P + 1 : 0;
-  const int occ = bf16_pool ? 2 : 3;  // resident CTAs per SM at the kernels' register use
-  const long long wave = 152LL * occ;  // resident CTAs of one wave at the kernel's register use
   const long long pairs = (long long)batch * g.Hkv > 0 ? (long long)batch * g.Hkv : 1;
-  const long long win_ctas = bf16_pool ? 0 : (long long)batch * g.Hkv * ((g.S + g.W + 15) / 16);
-  long long pps = stage_pages;
+  long long pps = 1;
   if (bf16_pool) {
-    // one wave of splits
-    long long free_slots = wave < pairs ? pairs : wave;
-    long long split_target = free_slots / pairs;
+    // one wave of splits (two CTAs per SM)
+    const long long wave = 2 * 152;
+    long long split_target = (wave < pairs ? pairs : wave) / pairs;
     if (split_target < 1) split_target = 1;
-    pps = max_pages > 0 ? (max_pages + split_target - 1) / split_target : stage_pages;
+    pps = max_pages > 0 ? (max_pages + split_target - 1) / split_target : 1;
   } else if (max_pages > 0) {
-    // INT2: size splits from the step's page count (an upper bound from max_seq).
-    // When one wave holds every split, the splits share it with the window CTAs.
-    // Otherwise CTAs of at least kMinSplitPages pages run in up to eight waves:
-    // the hardware hands each freed slot the next CTA, which evens out ragged
-    // lengths, while the partials stay a small fraction of the cache bytes.
-    constexpr long long kMinSplitPages = 16;
+    // INT2 (one CTA per SM, the whole split's tiles in flight when they fit).  A step
+    // of at most 64 pages per SM runs as one wave of equal splits; larger steps use
+    // 64-page splits, and the hardware hands each freed SM the next split, which
+    // evens out ragged lengths.  The window chunks ride on the first splits' CTAs.
+    const long long wave = 152;
     const long long total = pairs * max_pages;
-    long long ctas = total / kMinSplitPages;
-    if (ctas < wave) {
-      ctas = wave - win_ctas;
-      if (ctas < pairs) ctas = pairs;
-    } else if (ctas > 8 * wave) {
-      ctas = 8 * wave;
+    if (total <= 64 * wave) {
+      const long long ctas = wave > pairs ? wave : pairs;
+      pps = (total + ctas - 1) / ctas;
+    } else {
+      pps = 64;
     }
-    pps = (total + ctas - 1) / ctas;
   }
-  if (pps < stage_pages) pps = stage_pages;
-  pps = (pps + stage_pages - 1) / stage_pages * stage_pages;
+  if (pps < 1) pps = 1;
+  if (!bf16_pool && pps > 256) pps = 256;
   long long splits = max_pages > 0 ? (max_pages + pps - 1) / pps : 0;
   while (splits > 1023) {
-    pps += stage_pages;
+    ++pps;
     splits = (max_pages + pps - 1) / pps;
   }
   w.pages_per_split = static_cast<int>(pps);
   w.max_splits = static_cast<int>(splits);
   w.win_chunks = bf16_pool ? 0 : (g.S + g.W + 15) / 16;
+  if (!bf16_pool) {
+    // tcgen05 split kernel: grid.x covers the window chunks and the splits; ring depth
+    // = the split's 128-token tiles, up to what fits in shared memory (at least 3:
+    // the ring also holds the value warps' partials at the end)
+    w.tc_grid_x = w.max_splits > w.win_chunks ? w.max_splits : w.win_chunks;
+    const int ppt = 128 / g.P;
+    int stages = (int)((pps + ppt - 1) / ppt);
+    if (stages > 16) stages = 16;
+    while (stages > 3 && decode_tc_smem_bytes(g.D, gq, stages) > 227 * 1024) --stages;
+    if (stages < 3) stages = 3;
+    w.tc_stages = stages;
+  }
   auto align = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
   w.qfrag_off = off;
@@ -661,9 +666,15 @@ static oscar_status layer_operand_exps(oscar_ctx* ctx, int32_t layer, int* ek, i
   return OSCAR_OK;
 }
 
+static oscar_status check_workspace(const void* workspace) {
+  if (!workspace) return fail(OSCAR_ERR_INVALID, "null tensor argument");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(OSCAR_ERR_INVALID, "workspace must be 256-byte aligned");
+  return OSCAR_OK;
+}
+
 static oscar_status decode_common_checks(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
                                          int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
-                                         const int32_t* seq_lens, int32_t batch, int32_t max_seq, void* workspace) {
+                                         const int32_t* seq_lens, int32_t batch, int32_t max_seq) {
   oscar_status st = need_device(ctx);
   if (st != OSCAR_OK) return st;
   if ((st = check_layer(ctx, layer)) != OSCAR_OK) return st;
@@ -671,20 +682,21 @@ static oscar_status decode_common_checks(oscar_ctx* ctx, int32_t layer, const vo
   if ((long long)max_seq > (long long)ctx->g.max_pages_per_req * ctx->g.P)
     return fail(OSCAR_ERR_INVALID, "max_seq %d exceeds max_pages_per_req * page_size", max_seq);
   if (batch == 0) return OSCAR_OK;
-  if (!q || !out || !block_table || !seq_lens || !workspace) return fail(OSCAR_ERR_INVALID, "null tensor argument");
-  if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(OSCAR_ERR_INVALID, "workspace must be 256-byte aligned");
+  if (!q || !out || !block_table || !seq_lens) return fail(OSCAR_ERR_INVALID, "null tensor argument");
   if (q_dtype != OSCAR_DTYPE_BF16 && q_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad q dtype");
   if (out_dtype != OSCAR_DTYPE_BF16 && out_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad out dtype");
   return OSCAR_OK;
 }
 
-static oscar_status prepare_decode(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
-                                   int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
-                                   const int32_t* seq_lens, const int32_t* req_slot, int32_t batch, int32_t max_seq,
-                                   int32_t sink, int32_t recent, const float* R_K, const float* R_V, void* workspace,
-                                   size_t ws_bytes, DecodeArgs* dst) {
+// Checks and argument fill shared by every INT2 decode entry point; the
+// workspace (caller scratch or the file-scope array) is set by the caller.
+static oscar_status prepare_decode_core(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
+                                        int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
+                                        const int32_t* seq_lens, const int32_t* req_slot, int32_t batch,
+                                        int32_t max_seq, int32_t sink, int32_t recent, const float* R_K,
+                                        const float* R_V, DecodeArgs* dst) {
   oscar_status st = decode_common_checks(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens,
-                                         batch, max_seq, workspace);
+                                         batch, max_seq);
   if (st != OSCAR_OK || batch == 0) return st;
   if (sink != ctx->g.S || recent != ctx->g.W)
     return fail(OSCAR_ERR_INVALID, "sink/recent (%d, %d) differ from the cache configuration (%d, %d)", sink, recent,
@@ -715,10 +727,22 @@ static oscar_status prepare_decode(oscar_ctx* ctx, int32_t layer, const void* q,
   a.pool = ctx->pool;
   a.slab = ctx->slab;
   a.status = ctx->d_status;
-  a.ws = static_cast<uint8_t*>(workspace);
   a.wl = oscar::plan_decode(ctx->g, batch, max_seq, false);
-  if (ws_bytes < a.wl.total)
-    return fail(OSCAR_ERR_INVALID, "workspace too small: %zu < %zu bytes", ws_bytes, a.wl.total);
+  return OSCAR_OK;
+}
+
+static oscar_status prepare_decode(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
+                                   int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
+                                   const int32_t* seq_lens, const int32_t* req_slot, int32_t batch, int32_t max_seq,
+                                   int32_t sink, int32_t recent, const float* R_K, const float* R_V, void* workspace,
+                                   size_t ws_bytes, DecodeArgs* dst) {
+  oscar_status st = prepare_decode_core(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens,
+                                        req_slot, batch, max_seq, sink, recent, R_K, R_V, dst);
+  if (st != OSCAR_OK || batch == 0) return st;
+  if ((st = check_workspace(workspace)) != OSCAR_OK) return st;
+  dst->ws = static_cast<uint8_t*>(workspace);
+  if (ws_bytes < dst->wl.total)
+    return fail(OSCAR_ERR_INVALID, "workspace too small: %zu < %zu bytes", ws_bytes, dst->wl.total);
   return OSCAR_OK;
 }
 
@@ -745,7 +769,7 @@ static oscar_status launch_decode_chain(oscar_ctx* ctx, DecodeArgs& a, const Wri
   }
   {
     LaunchScope ls(ctx, "decode_splitk", stream);
-    int e = oscar::launch_decode_splitk(a, stream, pdl);
+    int e = oscar::launch_decode_tc(a, stream, pdl);
     ls.done(e);
     if (e) return cuda_fail(e, "decode_splitk launch");
   }
@@ -791,64 +815,22 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
                                        int32_t max_seq, int32_t sink, int32_t recent, const float* R_K,
                                        const float* R_V, void* stream) {
   // Scratch comes from the library's file-scope device array: nothing here
-  // allocates (no cudaMalloc / cudaFree, no events, no torch).
-  oscar_status st = need_device(ctx);
-  if (st != OSCAR_OK) return st;
-  if ((st = check_layer(ctx, layer)) != OSCAR_OK) return st;
-  if (batch < 0 || bt_stride < 1 || max_seq < 0) return fail(OSCAR_ERR_INVALID, "bad batch/bt_stride/max_seq");
-  if ((long long)max_seq > (long long)ctx->g.max_pages_per_req * ctx->g.P)
-    return fail(OSCAR_ERR_INVALID, "max_seq %d exceeds max_pages_per_req * page_size", max_seq);
-  if (batch == 0) return OSCAR_OK;
-  if (!q || !out || !block_table || !seq_lens || !req_slot || !R_K || !R_V)
-    return fail(OSCAR_ERR_INVALID, "null tensor argument");
-  if ((st = check_r_align(R_K, R_V)) != OSCAR_OK) return st;
-  if (q_dtype != OSCAR_DTYPE_BF16 && q_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad q dtype");
-  if (out_dtype != OSCAR_DTYPE_BF16 && out_dtype != OSCAR_DTYPE_F32) return fail(OSCAR_ERR_INVALID, "bad out dtype");
-  if (sink != ctx->g.S || recent != ctx->g.W)
-    return fail(OSCAR_ERR_INVALID, "sink/recent (%d, %d) differ from the cache configuration (%d, %d)", sink, recent,
-                ctx->g.S, ctx->g.W);
-  int ek, ev;
-  if ((st = layer_operand_exps(ctx, layer, &ek, &ev)) != OSCAR_OK) return st;
-  const DecodeWs plan = oscar::plan_decode(ctx->g, batch, max_seq, false);
-  if (plan.total > oscar::kStaticScratchBytes)
+  // allocates (no cudaMalloc / cudaFree, no torch).
+  DecodeArgs a;
+  oscar_status st = prepare_decode_core(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens,
+                                        req_slot, batch, max_seq, sink, recent, R_K, R_V, &a);
+  if (st != OSCAR_OK || batch == 0) return st;
+  if (a.wl.total > oscar::kStaticScratchBytes)
     return fail(OSCAR_ERR_INVALID,
                 "decode needs %zu bytes of scratch for batch %d, max_seq %d; the allocation-free entry point has "
                 "%zu (use oscar_decode_attn with a caller workspace)",
-                plan.total, batch, max_seq, oscar::kStaticScratchBytes);
+                a.wl.total, batch, max_seq, oscar::kStaticScratchBytes);
   void* scratch = nullptr;
   size_t cap = 0;
   int e = oscar::static_decode_scratch(&scratch, &cap);
   if (e) return cuda_fail(e, "static scratch address");
-  DecodeArgs a{};
-  a.g = ctx->g;
-  a.layer = layer;
-  a.k_exp_K = ek;
-  a.k_exp_V = ev;
-  a.code_magic = oscar::kCodeMagic;
-  a.q = q;
-  a.q_dtype = q_dtype;
-  a.out = out;
-  a.out_dtype = out_dtype;
-  a.block_table = block_table;
-  a.bt_stride = bt_stride;
-  a.seq_lens = seq_lens;
-  a.req_slot = req_slot;
-  a.batch = batch;
-  a.max_seq = max_seq;
-  a.R_K = R_K;
-  a.R_V = R_V;
-  a.pool = ctx->pool;
-  a.slab = ctx->slab;
-  a.status = ctx->d_status;
   a.ws = static_cast<uint8_t*>(scratch);
-  a.wl = plan;
-  if ((e = oscar::launch_q_rotate(a, stream, true))) return cuda_fail(e, "q_rotate launch");
-  ctx->launches++;
-  if ((e = oscar::launch_decode_splitk(a, stream, true))) return cuda_fail(e, "decode_splitk launch");
-  ctx->launches++;
-  if ((e = oscar::launch_decode_combine(a, stream, true))) return cuda_fail(e, "decode_combine launch");
-  ctx->launches++;
-  return OSCAR_OK;
+  return launch_decode_chain(ctx, a, nullptr, stream);
 }
 
 // ---------------------------------------------------------------- extend
@@ -961,8 +943,9 @@ oscar_status oscar_bf16_decode_attn(oscar_ctx* ctx, int32_t layer, const void* b
                                     int32_t bt_stride, const int32_t* seq_lens, int32_t batch, int32_t max_seq,
                                     void* workspace, size_t ws_bytes, void* stream) {
   oscar_status st = decode_common_checks(ctx, layer, q, q_dtype, out, out_dtype, block_table, bt_stride, seq_lens,
-                                         batch, max_seq, workspace);
+                                         batch, max_seq);
   if (st != OSCAR_OK || batch == 0) return st;
+  if ((st = check_workspace(workspace)) != OSCAR_OK) return st;
   if (!bf16_pool) return fail(OSCAR_ERR_INVALID, "bf16_pool is null");
   if (reinterpret_cast<uintptr_t>(bf16_pool) & 15) return fail(OSCAR_ERR_INVALID, "bf16_pool must be 16-byte aligned");
   if (ctx->g.P != 64) return fail(OSCAR_ERR_UNSUPPORTED, "the BF16 comparison kernel needs page_size 64");
