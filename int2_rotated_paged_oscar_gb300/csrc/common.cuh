@@ -98,6 +98,36 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// try_wait with a suspend-time hint: a thread whose phase has not completed is
+// suspended (it issues nothing) until the phase completes or about hint_ns pass.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait_bounded for warps that wait while others work: the waiting thread
+// sleeps in the barrier (no spinning that would take issue slots from the warps
+// it waits for) and reads the timer only every 16 retries.  Same limit and
+// timeout behaviour as mbar_wait_bounded.
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t k = 1;; ++k) {
+    if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+    if ((k & 15) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+      flag_error(status, kDevTimeout);
+      return false;
+    }
+  }
+}
+
 // Non-multicast bulk copy global -> this CTA's shared memory, completion
 // signalled on an mbarrier (complete_tx).  Both addresses 16-byte aligned,
 // bytes a multiple of 16.

@@ -79,7 +79,8 @@ struct Int2Layout {
   static constexpr int MT = D / 16;             // PV m-tiles
   static constexpr int WS = P == 64 ? 2 : 4;    // ring stages per warp (one page block each)
   static constexpr int RING = kWarps * WS * BLOCK;
-  static constexpr int QOFF = (RING + kWarps * WS * (8 + 4) + 15) / 16 * 16;  // after mbarriers + page-valid flags
+  static constexpr int PIDS = RING + kWarps * WS * (8 + 4);                       // per-warp page ids [kWarps][32]
+  static constexpr int QOFF = (PIDS + kWarps * 32 * 4 + 15) / 16 * 16;  // after mbarriers, page-valid flags, page ids
   static constexpr int SMEM = QOFF + (NT == 1 ? KT * 32 * 8 : 0);  // + the NT = 1 query fragments
 };
 
@@ -158,6 +159,14 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::RING) + warp * WS;
   int* stage_ok = reinterpret_cast<int*>(smem + Lay::RING + kWarps * WS * 8) + warp * WS;
 
+  // the page ids of this warp's first 32 pages, read once (lane i: page i), so that
+  // refilling the ring needs no dependent global load
+  int* pidtab = reinterpret_cast<int*>(smem + Lay::PIDS) + warp * 32;
+  auto page_id = [&](int i) {
+    const int lp = pg0 + warp + kWarps * i;
+    return (lp < a.bt_stride && lp < g.max_pages_per_req) ? bt[lp] : -1;
+  };
+  if (lane < n_mine) pidtab[lane] = page_id(lane);
   if (lane == 0) {
     for (int s = 0; s < WS; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
@@ -166,8 +175,7 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
   const uint64_t stream_policy = l2_evict_first_policy();  // pages are read once per step
   auto issue = [&](int i) {  // lane 0: page i of this warp into stage i % WS
     const int s = i % WS;
-    const int lp = pg0 + warp + kWarps * i;
-    const int pid = (lp < a.bt_stride && lp < g.max_pages_per_req) ? bt[lp] : -1;
+    const int pid = i < 32 ? pidtab[i] : page_id(i);
     const bool okp = pid >= 0 && pid < g.num_pages;
     stage_ok[s] = okp ? 1 : 0;
     if (!okp) flag_error(a.status, kDevBadPage);
@@ -603,7 +611,7 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
   int i_fail = 0;
   for (int i = 0; i < n_mine; ++i) {
     const int s = i % WS;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (i / WS) & 1, a.status));
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_sleep_bounded(&bars[s], (i / WS) & 1, a.status));
     if (!ok) {
       aborted = true;
       i_fail = i;

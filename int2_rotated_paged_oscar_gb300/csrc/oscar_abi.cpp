@@ -188,53 +188,48 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   DecodeWs w{};
   const int gq = g.Hq / g.Hkv;
   w.nt = gq == 8 ? 2 : 1;
+  const int stage_pages = bf16_pool ? 1 : 4;  // INT2: the 4 warps of a split CTA stream pages round-robin
   long long max_pages;
   if (bf16_pool) max_pages = max_seq > 0 ? (max_seq - 1) / g.P + 1 : 0;
   else max_pages = (max_seq - g.W > g.S) ? (long long)(max_seq - g.W - 1) / g.P + 1 : 0;
+  const int occ = bf16_pool ? 2 : 3;  // resident CTAs per SM at the kernels' register use
+  const long long wave = 152LL * occ;  // resident CTAs of one wave at the kernel's register use
   const long long pairs = (long long)batch * g.Hkv > 0 ? (long long)batch * g.Hkv : 1;
-  long long pps = 1;
+  const long long win_ctas = bf16_pool ? 0 : (long long)batch * g.Hkv * ((g.S + g.W + 15) / 16);
+  long long pps = stage_pages;
   if (bf16_pool) {
-    // one wave of splits (two CTAs per SM)
-    const long long wave = 2 * 152;
-    long long split_target = (wave < pairs ? pairs : wave) / pairs;
+    // one wave of splits
+    long long free_slots = wave < pairs ? pairs : wave;
+    long long split_target = free_slots / pairs;
     if (split_target < 1) split_target = 1;
-    pps = max_pages > 0 ? (max_pages + split_target - 1) / split_target : 1;
+    pps = max_pages > 0 ? (max_pages + split_target - 1) / split_target : stage_pages;
   } else if (max_pages > 0) {
-    // INT2 (one CTA per SM, the whole split's tiles in flight when they fit).  A step
-    // of at most 64 pages per SM runs as one wave of equal splits; larger steps use
-    // 64-page splits, and the hardware hands each freed SM the next split, which
-    // evens out ragged lengths.  The window chunks ride on the first splits' CTAs.
-    const long long wave = 152;
+    // INT2: size splits from the step's page count (an upper bound from max_seq).
+    // When one wave holds every split, the splits share it with the window CTAs.
+    // Otherwise CTAs of at least kMinSplitPages pages run in up to eight waves:
+    // the hardware hands each freed slot the next CTA, which evens out ragged
+    // lengths, while the partials stay a small fraction of the cache bytes.
+    constexpr long long kMinSplitPages = 16;
     const long long total = pairs * max_pages;
-    if (total <= 64 * wave) {
-      const long long ctas = wave > pairs ? wave : pairs;
-      pps = (total + ctas - 1) / ctas;
-    } else {
-      pps = 64;
+    long long ctas = total / kMinSplitPages;
+    if (ctas < wave) {
+      ctas = wave - win_ctas;
+      if (ctas < pairs) ctas = pairs;
+    } else if (ctas > 8 * wave) {
+      ctas = 8 * wave;
     }
+    pps = (total + ctas - 1) / ctas;
   }
-  if (pps < 1) pps = 1;
-  if (!bf16_pool && pps > 256) pps = 256;
+  if (pps < stage_pages) pps = stage_pages;
+  pps = (pps + stage_pages - 1) / stage_pages * stage_pages;
   long long splits = max_pages > 0 ? (max_pages + pps - 1) / pps : 0;
   while (splits > 1023) {
-    ++pps;
+    pps += stage_pages;
     splits = (max_pages + pps - 1) / pps;
   }
   w.pages_per_split = static_cast<int>(pps);
   w.max_splits = static_cast<int>(splits);
   w.win_chunks = bf16_pool ? 0 : (g.S + g.W + 15) / 16;
-  if (!bf16_pool) {
-    // tcgen05 split kernel: grid.x covers the window chunks and the splits; ring depth
-    // = the split's 128-token tiles, up to what fits in shared memory (at least 3:
-    // the ring also holds the value warps' partials at the end)
-    w.tc_grid_x = w.max_splits > w.win_chunks ? w.max_splits : w.win_chunks;
-    const int ppt = 128 / g.P;
-    int stages = (int)((pps + ppt - 1) / ppt);
-    if (stages > 16) stages = 16;
-    while (stages > 3 && decode_tc_smem_bytes(g.D, gq, stages) > 227 * 1024) --stages;
-    if (stages < 3) stages = 3;
-    w.tc_stages = stages;
-  }
   auto align = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
   w.qfrag_off = off;
@@ -769,7 +764,7 @@ static oscar_status launch_decode_chain(oscar_ctx* ctx, DecodeArgs& a, const Wri
   }
   {
     LaunchScope ls(ctx, "decode_splitk", stream);
-    int e = oscar::launch_decode_tc(a, stream, pdl);
+    int e = oscar::launch_decode_splitk(a, stream, pdl);
     ls.done(e);
     if (e) return cuda_fail(e, "decode_splitk launch");
   }

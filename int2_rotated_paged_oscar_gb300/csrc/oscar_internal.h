@@ -72,9 +72,7 @@ struct WriteArgs {
 struct DecodeWs {
   size_t qfrag_off, qaux_off, qplain_off, part_off, total;
   int max_splits;        // INT2 splits per (request, kv head)
-  int pages_per_split;   // INT2 pages of one split (at most 256)
-  int tc_grid_x;         // grid.x of the split kernel: max(win_chunks, max_splits)
-  int tc_stages;         // 128-token tiles in flight per split CTA (shared-memory ring)
+  int pages_per_split;   // multiple of the 4 warps of a split CTA (each warp streams its own pages)
   int nt;                // query n-tiles (max(1, 2*gq/8))
   int win_chunks;        // BF16 window CTAs per (request, kv head): grid.x = win_chunks + max_splits
   int combine_hpc;       // query heads per combine CTA (a power of two dividing Hq, at most 16)
@@ -161,10 +159,6 @@ int launch_evict(const WriteArgs& a, void* stream);
 int launch_append(const WriteArgs& a, void* stream, bool pdl);
 int launch_q_rotate(const DecodeArgs& a, void* stream, bool pdl);
 int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl);
-// Split-K decode with the query-key product on tcgen05 (one CTA per SM): window
-// chunks and INT2 splits in one grid of tc_grid_x x Hkv x batch CTAs.
-int launch_decode_tc(const DecodeArgs& a, void* stream, bool pdl);
-size_t decode_tc_smem_bytes(int head_dim, int gq, int stages);
 int launch_decode_combine(const DecodeArgs& a, void* stream, bool pdl);
 // The fused step's first kernel: the query rotation and the append in one grid.
 int launch_step_prep(const WriteArgs& w, const DecodeArgs& d, void* stream, bool pdl);
