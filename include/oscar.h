@@ -123,9 +123,18 @@ oscar_status oscar_create(const oscar_config* cfg, void* int2_pool, void* window
 oscar_status oscar_destroy(oscar_ctx* ctx);
 
 /* ---------------------------------------------------------------- host page allocator
+ * Source: the OSCAR serving path keeps the INT2 history in a paged cache that is
+ * compatible with paged attention and prefix caching (gist.science technical
+ * summary, section 2.2 B and section 3; arXiv abstract: fused kernels inside the
+ * paged serving engines).  These calls are the page side of that cache: a page
+ * is the unit a block table maps, and a refcount lets requests that share a
+ * prefix share its pages.
  * Pages are shared by every layer (page id p addresses block p of each layer).
  * A freshly allocated page has refcount 1; a page returns to the free list
- * when its refcount drops to 0.  ids are host arrays. */
+ * when its refcount drops to 0.  ids are host arrays.  Host-only: no device
+ * work, no stream.  oscar_alloc_pages returns OSCAR_ERR_OOM (and allocates
+ * nothing) when fewer than n pages are free; ref/unref of an id outside
+ * [0, num_pages) or of a free page returns OSCAR_ERR_INVALID. */
 oscar_status oscar_alloc_pages(oscar_ctx* ctx, int32_t n, int32_t* out_ids);
 oscar_status oscar_ref_pages(oscar_ctx* ctx, const int32_t* ids, int32_t n);
 oscar_status oscar_unref_pages(oscar_ctx* ctx, const int32_t* ids, int32_t n);
@@ -146,8 +155,10 @@ oscar_status oscar_read_pages(oscar_ctx* ctx, int32_t layer, const int32_t* ids,
 int32_t oscar_pages_needed(const oscar_config* cfg, int32_t seq_len);
 
 /* Fork request dst off request src at src's current length n (a branch point,
- * as for parallel sampling or a shared prompt; the prefix caching the OSCAR
- * summaries require, section 2.2 B).  Host block-table rows: src_bt (read),
+ * as for parallel sampling or a shared prompt).  Source: prefix caching over the
+ * INT2 cache (gist.science technical summary, section 2.2 B: the serving kernel
+ * stays compatible with prefix caching; section 3: prefix reuse is kept with the
+ * compressed cache).  Host block-table rows: src_bt (read),
  * dst_bt (written, capacity max_pages_per_req; unused entries set to -1).
  * History pages that the prefix fills completely are shared (refcount + 1);
  * the page holding the end of the history, if partial, is copied into a newly
@@ -184,7 +195,12 @@ oscar_status oscar_write_kv_hadamard(oscar_ctx* ctx, int32_t layer, const void* 
                                      const int32_t* block_table, int32_t bt_stride, const int32_t* req_slot,
                                      void* stream);
 
-/* One decode-step append per request: K_new, V_new [batch][n_kv_heads][d]
+/* One decode-step append per request.  Source: the sink and most recent
+ * tokens stay BF16 and the history is stored as INT2 after the rotation and
+ * clipping (gist.science technical summary, section 2.2 B); so when a new token
+ * arrives, the oldest recent token leaves the BF16 window and is written into
+ * the INT2 history by the fused write path (arXiv abstract: fused write
+ * kernel).  K_new, V_new [batch][n_kv_heads][d]
  * (dtype) is token seq_lens_before[b].  If seq_lens_before[b] - W >= S the
  * oldest recent token e = seq_lens_before[b] - W is first quantised from the
  * ring into page block_table[b][e / P] slot e % P; the new token then takes
