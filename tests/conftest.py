@@ -9,3 +9,16 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built CUDA library")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Exemption counts of the write-parity cases that ran (the near-boundary rule for packed codes)."""
+    try:
+        from tests.harness import EXEMPTION_LOG
+    except Exception:
+        return
+    if not EXEMPTION_LOG:
+        return
+    terminalreporter.write_line("write parity exemptions (case: exempt / codes compared, by kind):")
+    for case, n, e, kinds in EXEMPTION_LOG:
+        terminalreporter.write_line(f"  {case}: {e} / {n} ({e / max(n, 1):.2e}) {kinds}")

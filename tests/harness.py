@@ -106,9 +106,11 @@ def dtype_code(dtype: str) -> int:
 def _near_bf16_boundary(x: np.ndarray, ref: np.ndarray) -> np.ndarray:
     """True where x lies within 1e-6 * max(|x|, ref) of a BF16 rounding boundary.
 
-    ref is the group's scale: a rotated value carries an absolute error set by the
-    magnitude of the group's values, so a group minimum close to zero is judged on
-    the scale of its group, the same reference the per-element rule uses.
+    ref is the magnitude x is computed from: a rotated value carries an absolute error set by the
+    magnitude of the values, so a group minimum close to zero is judged on the scale of its group
+    (the reference the per-element rule uses), and (max - min) / 3 on max(|max|, |min|), since a
+    narrow group of large values (a clipped group) has a range that is a small difference of large
+    numbers.
     """
     x = np.asarray(x, dtype=np.float64)
     w = BOUNDARY_REL * np.maximum(np.abs(x), np.asarray(ref, dtype=np.float64))
@@ -140,31 +142,52 @@ def _exact_ties(y: np.ndarray, scale: np.ndarray, zero: np.ndarray, group: int) 
 
 
 def compare_history(gpu_pool: np.ndarray, geom: cache.Geometry, layer: int, diag: dict,
-                    exact_ties: bool = False) -> dict:
+                    exact_ties: bool = False, enforce_budget: bool = True) -> dict:
     """Check GPU history rows against the oracle write diagnostics; returns counts, raises on violation.
+
+    Every element that is not bit-identical to the oracle is an exemption and is listed:
+    * a code that differs where the group's scale and zero agree (kind "K" / "V"): allowed only within
+      1e-6 relative of a decision boundary;
+    * a scale or a zero that differs (kinds "K-scale", "K-zero", ...): allowed only when the pre-rounding
+      value lies within 1e-6 relative of a BF16 rounding boundary; the group's codes must then equal a
+      re-quantisation with the GPU's own scale and zero, and each of them that differs from the oracle's
+      own code is listed too (kind "K-group-code", ...).
+    The exemptions may make up at most 1e-4 of the codes compared (enforce_budget; callers that compare
+    a case in several pieces check the budget over the whole case with check_budget).
 
     exact_ties: the rotated values are exact on both sides (R = I on BF16 inputs), so a value can sit
     exactly halfway between two codes; there both codes have the same error s/2, both are correct, and
     such elements are checked for that and not counted against the exemption budget.
     """
     if "k" not in diag:
-        return {"elements": 0, "exempt": 0}
+        return {"elements": 0, "exempt": 0, "list": []}
     gimg = cache.CacheImage(geom)
     gimg.pool = gpu_pool
     ck, sk, zk, cv, sv, zv = gimg.read_history(layer, diag["pages"], diag["slots"])
+    G = geom.group_size
     total, exempt_list = 0, []
     for name, qd, gc, gs, gz in (("K", diag["k"], ck, sk, zk), ("V", diag["v"], cv, sv, zv)):
         y = qd["y"]
-        same_sz = (gs == qd["scale"]) & (gz == qd["zero"])
-        group_exempt = _near_bf16_boundary(qd["mn"], qd["rng3"]) | _near_bf16_boundary(qd["rng3"], qd["rng3"])
+        same_s, same_z = gs == qd["scale"], gz == qd["zero"]
+        same_sz = same_s & same_z
+        # the zero is rounded from the group minimum, the scale from (max - min) / 3: each is judged
+        # relative to the magnitude of the values it is computed from (min; max and min)
+        mag = np.maximum(np.abs(qd["mn"]), np.abs(qd["mn"] + 3.0 * qd["rng3"]))
+        group_exempt = _near_bf16_boundary(qd["mn"], qd["rng3"]) | _near_bf16_boundary(qd["rng3"], mag)
         bad_groups = ~same_sz & ~group_exempt
         if bad_groups.any():
-            idx = np.argwhere(bad_groups)[:5]
-            raise AssertionError(f"{name}: scale/zero differ outside the boundary rule at {idx.tolist()}")
+            lines = []
+            for r, h, gi in np.argwhere(bad_groups)[:5]:
+                mn, r3 = float(qd["mn"][r, h, gi]), float(qd["rng3"][r, h, gi])
+                lines.append(f"(b {int(diag['b'][r])}, t {int(diag['t'][r])}, head {h}, group {gi}): "
+                             f"min {mn!r} rng/3 {r3!r}; oracle s {float(qd['scale'][r, h, gi])!r} "
+                             f"z {float(qd['zero'][r, h, gi])!r}; gpu s {float(gs[r, h, gi])!r} "
+                             f"z {float(gz[r, h, gi])!r}; group y {qd['y'][r, h, gi * G:(gi + 1) * G].tolist()}")
+            raise AssertionError(f"{name}: scale/zero differ outside the boundary rule: " + "; ".join(lines))
         # expected codes: oracle codes where (s, z) agree, else re-quantised with the GPU's own (s, z)
-        want = np.where(np.repeat(same_sz, geom.group_size, axis=-1), qd["codes"],
-                        quant.quantize_with(y, gs, gz, geom.group_size))
-        near = _near_code_boundary(y, gs, gz, geom.group_size)
+        in_same = np.repeat(same_sz, G, axis=-1)
+        want = np.where(in_same, qd["codes"], quant.quantize_with(y, gs, gz, G))
+        near = _near_code_boundary(y, gs, gz, G)
         diff = gc != want
         bad = diff & ~near
         if bad.any():
@@ -173,19 +196,92 @@ def compare_history(gpu_pool: np.ndarray, geom: cache.Geometry, layer: int, diag
                                  f"{idx.tolist()}")
         total += gc.size
         if exact_ties:
-            tie = _exact_ties(y, gs, gz, geom.group_size) & diff
+            tie = _exact_ties(y, gs, gz, G) & diff
             if tie.any():
-                sg = np.repeat(np.asarray(gs, np.float64), geom.group_size, axis=-1)
-                zg = np.repeat(np.asarray(gz, np.float64), geom.group_size, axis=-1)
+                sg = np.repeat(np.asarray(gs, np.float64), G, axis=-1)
+                zg = np.repeat(np.asarray(gz, np.float64), G, axis=-1)
                 err = np.abs(zg + gc.astype(np.float64) * sg - y)
                 assert np.all(err[tie] == 0.5 * sg[tie]), f"{name}: a tie took a code that is not one of its two nearest"
             diff = diff & ~tie
-        for i in np.argwhere(diff & near):
-            exempt_list.append((name, int(diag["b"][i[0]]), int(diag["t"][i[0]]), int(i[1]), int(i[2])))
-        for i in np.argwhere(~same_sz):
-            exempt_list.append((name + "-group", int(diag["b"][i[0]]), int(diag["t"][i[0]]), int(i[1]), int(i[2])))
-    assert len(exempt_list) <= EXEMPT_FRACTION * max(total, 1) + 1, f"too many exemptions: {len(exempt_list)}"
-    return {"elements": total, "exempt": len(exempt_list), "list": exempt_list}
+        b_of, t_of = diag["b"], diag["t"]
+        for i in np.argwhere(diff & in_same):
+            exempt_list.append((name, int(b_of[i[0]]), int(t_of[i[0]]), int(i[1]), int(i[2])))
+        for kind, mask in (("-scale", ~same_s), ("-zero", ~same_z)):
+            for i in np.argwhere(mask):  # (row, head, group)
+                exempt_list.append((name + kind, int(b_of[i[0]]), int(t_of[i[0]]), int(i[1]), int(i[2])))
+        for i in np.argwhere((gc != qd["codes"]) & ~in_same):
+            exempt_list.append((name + "-group-code", int(b_of[i[0]]), int(t_of[i[0]]), int(i[1]), int(i[2])))
+    res = {"elements": total, "exempt": len(exempt_list), "list": exempt_list}
+    if enforce_budget:
+        check_budget(res)
+    return res
+
+
+def check_budget(res: dict) -> None:
+    """At most 1e-4 of the compared codes may be exemptions (no slack)."""
+    assert res["exempt"] <= EXEMPT_FRACTION * res["elements"], \
+        f"too many exemptions: {res['exempt']} of {res['elements']} codes"
+
+
+def merge_results(results) -> dict:
+    out = {"elements": 0, "exempt": 0, "list": []}
+    for r in results:
+        out["elements"] += r["elements"]
+        out["exempt"] += r["exempt"]
+        out["list"] += r["list"]
+    return out
+
+
+def check_history_chunk(job) -> dict:
+    """Worker of a spawned process pool: the oracle quantises one chunk of history rows of request b
+    (tokens ts, input rows xk / xv [m, Hkv, d]) and compares them with the GPU's page blocks holding
+    those rows (blocks [k, Hkv, block bytes], remap[m] = the row's block)."""
+    geom_fields, fx, b, ts, xk, xv, blocks, remap = job
+    g = cache.Geometry(*geom_fields)
+    kq = cache.quantize_rows(xk, fx["R_K"], fx["clip_K"], g.group_size)
+    vq = cache.quantize_rows(xv, fx["R_V"], fx["clip_V"], g.group_size)
+    cg = cache.Geometry(1, g.n_kv_heads, g.head_dim, g.page_size, g.group_size, g.sink, g.recent, blocks.shape[0], 1)
+    diag = {"b": np.full(ts.size, b, np.int64), "t": ts, "k": kq, "v": vq, "pages": remap,
+            "slots": ts % g.page_size}
+    return compare_history(blocks[None], cg, 0, diag, enforce_budget=False)
+
+
+_ORACLE_POOL = None
+
+
+def oracle_pool():
+    """Process pool for oracle work (spawned, one BLAS thread per worker)."""
+    global _ORACLE_POOL
+    if _ORACLE_POOL is None:
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        import os
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"   # read by the workers' numpy at import
+        n = max(1, min(16, len(os.sched_getaffinity(0))))
+        _ORACLE_POOL = cf.ProcessPoolExecutor(n, mp_context=mp.get_context("spawn"))
+    return _ORACLE_POOL
+
+
+# exemption records of this test session: (case, elements, exemptions by kind); printed at the end
+EXEMPTION_LOG = []
+
+
+def record_exemptions(case: str, res: dict) -> None:
+    """Log a case's exemption counts (shown in the pytest summary) and, when OSCAR_EXEMPTION_DIR is set,
+    write every exemption (kind, request, token, kv head, channel or group) to <dir>/<case>.txt."""
+    import collections
+    import os
+    kinds = collections.Counter(e[0] for e in res["list"])
+    EXEMPTION_LOG.append((case, res["elements"], res["exempt"], dict(sorted(kinds.items()))))
+    d = os.environ.get("OSCAR_EXEMPTION_DIR")
+    if d:
+        os.makedirs(d, exist_ok=True)
+        with open(os.path.join(d, f"exemptions_{case}.txt"), "w") as f:
+            f.write(f"# {case}: {res['exempt']} exemptions of {res['elements']} codes compared\n")
+            f.write("# kind request token kv_head channel_or_group\n")
+            for e in res["list"]:
+                f.write(" ".join(str(v) for v in e) + "\n")
 
 
 def compare_window(gpu_slab: np.ndarray, oracle_slab: np.ndarray, layer: int, slots):

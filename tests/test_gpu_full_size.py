@@ -1,8 +1,10 @@
 """Full-size workloads on the GPU, checked on samples the oracle computes one by one.
 
 The cache is filled by the GPU write path (the tensor-core prefill for these BF16
-inputs).  Sampled history rows are re-quantised by the oracle from their inputs:
-codes, scales and zeros bit-exact up to the near-boundary rule.  Sampled requests
+inputs).  History rows are re-quantised by the oracle from their inputs (every row
+of the batch-1 32K and 131K, batched and prefill cases; sampled rows in the
+capacity case): codes, scales and zeros bit-exact up to the near-boundary rule,
+with the exemptions counted over the whole case and listed.  Sampled requests
 are decoded by the oracle from the GPU's own packed pages (identical caches),
 against the GPU decode of the whole batch in one launch: max abs error <= 2e-3 and
 mean abs error <= 2e-4 on unit-scale outputs.
@@ -102,6 +104,34 @@ def _check_rows(gc, layer, bt, samples):
     return res
 
 
+def _check_all_rows(gc, layer, bt, lens, rows_for, case, chunk=8192):
+    """Every history row of every request, re-quantised by the oracle from its inputs, against the GPU's
+    pages (codes, scales and zeros bit-exact up to the near-boundary rule).  The exemption budget holds
+    over the whole case and every exemption is listed.  rows_for(b, ts) gives the input rows of tokens
+    ts of request b ([m, Hkv, d] each for K and V).  Chunks of rows go to a spawned process pool; the
+    GPU's page blocks of each chunk are gathered on the device."""
+    g = gc.geom
+    fx = {k: gc.fx[layer][k] for k in ("R_K", "R_V", "clip_K", "clip_V")}
+    fields = (g.num_layers, g.n_kv_heads, g.head_dim, g.page_size, g.group_size, g.sink, g.recent, g.num_pages,
+              g.max_requests)
+    futs = []
+    pool = H.oracle_pool()
+    for b, n in enumerate(lens):
+        for t0 in range(g.sink, n - g.recent, chunk):
+            ts = np.arange(t0, min(n - g.recent, t0 + chunk), dtype=np.int64)
+            xk, xv = rows_for(b, ts)
+            pages = np.asarray(bt[b], np.int64)[ts // g.page_size]
+            used, remap = np.unique(pages, return_inverse=True)
+            blocks = H.gpu_pages(gc, layer, used)
+            futs.append(pool.submit(H.check_history_chunk, (fields, fx, b, ts, np.ascontiguousarray(xk),
+                                                            np.ascontiguousarray(xv), blocks, remap.reshape(-1))))
+    res = H.merge_results(f.result() for f in futs)
+    assert res["elements"] == sum(max(0, n - g.recent - g.sink) for n in lens) * 2 * g.n_kv_heads * g.head_dim
+    H.record_exemptions(case, res)
+    H.check_budget(res)
+    return res
+
+
 def _decode_all(osc, gc, layer, q, bt, lens, slots, max_seq):
     """GPU decode of the whole batch in one call (the layer's clip was declared by its writes)."""
     import torch
@@ -140,8 +170,8 @@ def _cache(wl, num_pages, max_requests, ppr, num_layers=1, layers=None):
     return geom, gc
 
 
-def _single_request(osc, wl, n, heads=None, seed=0):
-    """Batch-1 prefill of n tokens and one decode; sampled rows, the window and the decode are checked."""
+def _single_request(osc, wl, n, case, heads=None, seed=0):
+    """Batch-1 prefill of n tokens and one decode; every history row, the window and the decode are checked."""
     s = wl.shape
     ppr = syn.pages_for(n, s.page_size)
     geom, gc = _cache(wl, ppr, 1, ppr)
@@ -156,6 +186,7 @@ def _single_request(osc, wl, n, heads=None, seed=0):
         for t in (geom.sink, 63, 64, n // 2, n - geom.recent - 1):
             samples.append((0, t) + tuple(st.rows(t)))
         _check_rows(gc, 0, bt, samples)
+        _check_all_rows(gc, 0, bt, [n], lambda b, ts: (st.k[ts], st.v[ts]), case)
         _check_window(gc, 0, bt[0], n, 0, st.rows)
         q = syn.queries(wl, 0, 1)
         got = _decode_all(osc, gc, 0, q, bt, [n], [0], n)
@@ -166,17 +197,18 @@ def _single_request(osc, wl, n, heads=None, seed=0):
 
 def test_batch1_32k_full(osc):
     """Batch-1 decode at 32,768 tokens, 32 q / 8 kv heads, d=128, page 64; all heads checked."""
-    _single_request(osc, syn.batch1_32k(), 32768, seed=100)
+    _single_request(osc, syn.batch1_32k(), 32768, "batch1_32k", seed=100)
 
 
 def test_long_131k_full(osc):
-    """Batch-1 decode at 131,072 tokens (the oracle decodes kv heads 0 and 5, eight q heads)."""
-    _single_request(osc, syn.long_131k(), 131072, heads=[0, 5], seed=101)
+    """Batch-1 decode at 131,072 tokens; every history row and all eight kv heads (32 q heads) checked."""
+    _single_request(osc, syn.long_131k(), 131072, "long_131k", seed=101)
 
 
 def test_batched_ragged_b64_full(osc):
     """64 requests, lengths U[8K, 32K], 64 q / 8 kv heads, pages handed out in shuffled order, one decode
-    launch for the batch; the shortest, longest and two other requests are decoded by the oracle."""
+    launch for the batch; every history row of every request is checked, and the shortest, longest and
+    two other requests are decoded by the oracle."""
     wl = syn.batched_ragged(64)
     s = wl.shape
     lens = list(wl.seq_lens)
@@ -191,6 +223,8 @@ def test_batched_ragged_b64_full(osc):
         rows_of = lambda r, t: st.rows(ROW_SHIFT * r + t)
         rng = np.random.default_rng(102)
         _check_rows(gc, 0, bt, _sample_rows(rng, lens, geom, 128, rows_of))
+        _check_all_rows(gc, 0, bt, lens, lambda r, ts: (st.k[ROW_SHIFT * r + ts], st.v[ROW_SHIFT * r + ts]),
+                        "batched_ragged_b64")
         q = syn.queries(wl, 0, b)
         got = _decode_all(osc, gc, 0, q, bt, lens, list(range(b)), max(lens))
         for r in sorted({int(np.argmin(lens)), int(np.argmax(lens)), 17, 40}):
@@ -203,7 +237,8 @@ def test_batched_ragged_b64_full(osc):
 def test_prefill_8x32k_shared_prefix_and_appends(osc):
     """Eight requests of 32,768 tokens.  Requests 1-3 fork off request 0 after its 16,384-token prefix
     (whole history pages shared, the window slot copied) and each writes its own continuation; requests
-    4-7 are independent.  Then 256 fused decode steps (append + attention) for all eight."""
+    4-7 are independent.  Then 256 fused decode steps (append + attention) for all eight.  Every history
+    row of every request (the prefill, the evicted rings and the appends) is checked."""
     import torch
     wl = syn.write_prefill()
     s = wl.shape
@@ -278,6 +313,18 @@ def test_prefill_8x32k_shared_prefix_and_appends(osc):
             for t in (n_full - s.recent, n_full - 1, n_full + 10, n_end - s.recent - 1):
                 samples.append((r, t) + tuple(rows_of(r, t)))
         _check_rows(gc, 0, bts, samples)
+
+        def rows_for(r, ts):
+            k = np.empty((ts.size, s.n_kv_heads, s.head_dim), np.float32)
+            v = np.empty_like(k)
+            app = ts >= n_full
+            pre = ~app & (ts < n_pre) if r < sharers else np.zeros(ts.size, bool)
+            own = ~app & ~pre
+            k[app], v[app] = kn[ts[app] - n_full, r], vn[ts[app] - n_full, r]
+            k[pre], v[pre] = st.k[ts[pre]], st.v[ts[pre]]
+            k[own], v[own] = st.k[ROW_SHIFT * r + ts[own]], st.v[ROW_SHIFT * r + ts[own]]
+            return k, v
+        _check_all_rows(gc, 0, bts, [n_end] * b, rows_for, "prefill_8x32k_shared_prefix_256_appends")
         got = out.cpu().numpy().astype(np.float64)
         q_last = syn.as_input(q_all[steps - 1], "bf16")
         for r in (1, 5):

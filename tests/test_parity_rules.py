@@ -67,3 +67,48 @@ def test_code_change_away_from_a_boundary_is_rejected():
     pool = _replant(img, diag, codes)
     with pytest.raises(AssertionError, match="away from a rounding boundary"):
         H.compare_history(pool, img.g, 0, diag, exact_ties=True)
+
+
+def _clipped_group_case(offset):
+    """One token, one head, d = 64: group 0 holds 31 values at a clip threshold c = 12.3144 and one value
+    c - 3 (m - offset), where m = 0.0443115234375 is the midpoint between the BF16 numbers 0.044189453125
+    and 0.04443359375; so (max - min)/3 lies `offset` below a BF16 rounding boundary.  Returns the oracle
+    diagnostics and a planted image whose group-0 scale is the neighbouring BF16 number (codes
+    re-quantised with it), as a rotation that is not exact could produce."""
+    from oracle import quant
+    geom = cache.Geometry(1, 1, 64, 16, 32, 0, 1, 1, 1)
+    c, m = 12.314421653747559, 0.0443115234375
+    y = np.zeros((1, 1, 64))
+    y[0, 0, :32] = c
+    y[0, 0, 27] = c - 3.0 * (m - offset)
+    y[0, 0, 32:] = np.linspace(-1.0, 1.0, 32)
+    codes, scale, zero, mn, rng3 = quant.quantize_groups(y, 32)
+    assert scale[0, 0, 0] == 0.044189453125
+    qd = {"y": y, "codes": codes, "scale": scale, "zero": zero, "mn": mn, "rng3": rng3}
+    diag = {"b": np.zeros(1, np.int64), "t": np.zeros(1, np.int64), "k": qd, "v": qd,
+            "pages": np.zeros(1, np.int64), "slots": np.zeros(1, np.int64)}
+    s2 = scale.copy()
+    s2[0, 0, 0] = 0.04443359375
+    planted = cache.CacheImage(geom)
+    planted.store_history(0, diag["pages"], diag["slots"], dict(qd, scale=s2, codes=quant.quantize_with(y, s2, zero, 32)),
+                          qd)
+    return planted.pool, geom, diag
+
+
+def test_scale_of_a_narrow_group_of_large_values_is_judged_on_their_magnitude():
+    # 2e-7 below the boundary: outside 1e-6 of the range (4.4e-8) but inside 1e-6 of the values (1.2e-5)
+    pool, geom, diag = _clipped_group_case(2e-7)
+    res = H.compare_history(pool, geom, 0, diag, enforce_budget=False)
+    kinds = [e[0] for e in res["list"]]
+    assert kinds.count("K-scale") == 1 and "K-zero" not in kinds
+    # 5e-5 below the boundary is outside either window: a wrong scale
+    pool, geom, diag = _clipped_group_case(5e-5)
+    with pytest.raises(AssertionError, match="scale/zero differ outside the boundary rule"):
+        H.compare_history(pool, geom, 0, diag, enforce_budget=False)
+
+
+def test_exemption_budget_has_no_slack():
+    res = {"elements": 10000, "exempt": 1, "list": []}
+    H.check_budget(res)
+    with pytest.raises(AssertionError, match="too many exemptions"):
+        H.check_budget(dict(res, exempt=2))
