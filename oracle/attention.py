@@ -62,19 +62,32 @@ def _gather(cache: CacheImage, layer: int, b: int, n: int, block_table, req_slot
     return yk, yv, wk, wv
 
 
+def unrotate(y, r) -> np.ndarray:
+    """x_hat = y R^T for history rows y [n, Hkv, d]: r is [d, d] (shared by every kv head) or
+    [Hkv, d, d] (head h rotated by r[h])."""
+    y = np.asarray(y, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    if r.ndim == 2:
+        return y @ r.T
+    return np.stack([y[:, h] @ r[h].T for h in range(y.shape[1])], axis=1)
+
+
+def _head_rot(r, kv: int) -> np.ndarray:
+    r = np.asarray(r, dtype=np.float64)
+    return r if r.ndim == 2 else r[kv]
+
+
 def decode(cache: CacheImage, layer: int, q, block_table, seq_lens, req_slot, r_k, r_v) -> np.ndarray:
     """Plain definition.  q [B, Hq, d] -> o [B, Hq, d] float64."""
     q = np.asarray(q, dtype=np.float64)
     bsz, hq, d = q.shape
     g = cache.g
     grp = hq // g.n_kv_heads
-    rk = np.asarray(r_k, dtype=np.float64)
-    rv = np.asarray(r_v, dtype=np.float64)
     out = np.zeros((bsz, hq, d))
     for b in range(bsz):
         yk, yv, wk, wv = _gather(cache, layer, b, int(seq_lens[b]), block_table, req_slot)
-        k_all = np.concatenate([yk @ rk.T, wk], axis=0)
-        v_all = np.concatenate([yv @ rv.T, wv], axis=0)
+        k_all = np.concatenate([unrotate(yk, r_k), wk], axis=0)
+        v_all = np.concatenate([unrotate(yv, r_v), wv], axis=0)
         for h in range(hq):
             out[b, h] = softmax_attention(q[b, h], k_all[:, h // grp], v_all[:, h // grp])
     return out
@@ -87,13 +100,12 @@ def decode_fused(cache: CacheImage, layer: int, q, block_table, seq_lens, req_sl
     bsz, hq, d = q.shape
     g = cache.g
     grp = hq // g.n_kv_heads
-    rk = np.asarray(r_k, dtype=np.float64)
-    rv = np.asarray(r_v, dtype=np.float64)
     out = np.zeros((bsz, hq, d))
     for b in range(bsz):
         yk, yv, wk, wv = _gather(cache, layer, b, int(seq_lens[b]), block_table, req_slot)
         for h in range(hq):
             kv = h // grp
+            rk, rv = _head_rot(r_k, kv), _head_rot(r_v, kv)
             qr = q[b, h] @ rk
             s_h = yk[:, kv] @ qr / np.sqrt(d)
             s_w = wk[:, kv] @ q[b, h] / np.sqrt(d)
@@ -154,15 +166,13 @@ def extend(cache: CacheImage, layer: int, q, k_new, v_new, cu_seqlens, prefix_le
     total, hq, d = q.shape
     g = cache.g
     grp = hq // g.n_kv_heads
-    rk = np.asarray(r_k, dtype=np.float64)
-    rv = np.asarray(r_v, dtype=np.float64)
     cu = np.asarray(cu_seqlens, dtype=np.int64)
     out = np.zeros((total, hq, d))
     for b in range(cu.size - 1):
         n_pre = int(prefix_lens[b])
         yk, yv, wk, wv = _gather(cache, layer, b, n_pre, block_table, req_slot)
-        k_pre = np.concatenate([yk @ rk.T, wk], axis=0)
-        v_pre = np.concatenate([yv @ rv.T, wv], axis=0)
+        k_pre = np.concatenate([unrotate(yk, r_k), wk], axis=0)
+        v_pre = np.concatenate([unrotate(yv, r_v), wv], axis=0)
         c0, c1 = int(cu[b]), int(cu[b + 1])
         k_all = np.concatenate([k_pre, k_new[c0:c1]], axis=0)   # query i sees the first n_pre + i + 1 rows
         v_all = np.concatenate([v_pre, v_new[c0:c1]], axis=0)

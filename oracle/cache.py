@@ -144,12 +144,26 @@ class CacheImage:
                 quant.bits_to_f64(self.slab[layer, slot_req, :, 1, s, :]))
 
 
+def rotate_rows(x, r) -> np.ndarray:
+    """y = x R for token rows x [M, H, d], float64.
+
+    r is [d, d], the layer's rotation shared by every kv head (the pages' fixed per-layer
+    rotation), or [H, d, d], one rotation per kv head (head h of every row uses r[h]).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    if r.ndim == 2:
+        return x @ r
+    return np.stack([x[:, h] @ r[h] for h in range(x.shape[1])], axis=1)
+
+
 def quantize_rows(x, r, clip: float, group: int) -> dict:
-    """Rotate, clip and quantise token rows: x [M, H, d] (float64 values), r [d, d] (float32 values).
+    """Rotate, clip and quantise token rows: x [M, H, d] (float64 values), r [d, d] or [H, d, d]
+    (float32 values; see rotate_rows).
 
     y = x R (row-vector convention), y <- clamp(y, -c, c), then per-group INT2.
     """
-    y = np.asarray(x, dtype=np.float64) @ np.asarray(r, dtype=np.float64)
+    y = rotate_rows(x, r)
     c = float(np.float32(clip))
     y = np.clip(y, -c, c)
     codes, scale, zero, mn, rng3 = quant.quantize_groups(y, group)

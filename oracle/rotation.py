@@ -154,3 +154,28 @@ def layer_fixture(q_cal: np.ndarray, k_cal: np.ndarray, v_cal: np.ndarray, u_ide
     clip_v = np.float32(clip_threshold(v_cal, r_v32.astype(np.float64)))
     return {"R_K64": r_k, "R_V64": r_v, "R_K": r_k32, "R_V": r_v32,
             "clip_K": clip_k, "clip_V": clip_v, "U_Q": u_q, "U_S": u_s}
+
+
+def head_fixture(q_cal: np.ndarray, k_cal: np.ndarray, v_cal: np.ndarray) -> dict:
+    """Per-kv-head calibration artefacts (a variant of the pages' fixed per-layer rotation): kv head h
+    gets R_K[h] = U_Q,h H P from the queries of its own query-head group and R_V[h] = U_S,h H P from
+    its own attention outputs; the clip thresholds stay per layer, the 99.9th percentile of
+    |x R_h| over every head.
+
+    q_cal [T, Hq, d], k_cal / v_cal [T, Hkv, d] -> R_K, R_V [Hkv, d, d] (float64 and float32).
+    """
+    d = q_cal.shape[-1]
+    hkv = k_cal.shape[1]
+    grp = q_cal.shape[1] // hkv
+    r_k, r_v = [], []
+    for h in range(hkv):
+        qh = q_cal[:, h * grp:(h + 1) * grp]
+        r_k.append(composite_rotation(eigenbasis(query_covariance(qh.reshape(-1, d)))))
+        r_v.append(composite_rotation(eigenbasis(score_covariance(qh, k_cal[:, h:h + 1], v_cal[:, h:h + 1]))))
+    r_k, r_v = np.stack(r_k), np.stack(r_v)
+    r_k32, r_v32 = to_f32(r_k), to_f32(r_v)
+    rot_k = np.concatenate([np.asarray(k_cal[:, h], np.float64) @ r_k32[h].astype(np.float64) for h in range(hkv)])
+    rot_v = np.concatenate([np.asarray(v_cal[:, h], np.float64) @ r_v32[h].astype(np.float64) for h in range(hkv)])
+    clip_k = np.float32(np.percentile(np.abs(rot_k), 99.9))
+    clip_v = np.float32(np.percentile(np.abs(rot_v), 99.9))
+    return {"R_K64": r_k, "R_V64": r_v, "R_K": r_k32, "R_V": r_v32, "clip_K": clip_k, "clip_V": clip_v}

@@ -583,3 +583,80 @@ def test_extend_is_invariant_under_within_group_channel_permutation():
         outs.append(attention.extend(img, 0, q, kc, vc, [0, 6], [90], bt, [0], rk, rv))
     assert np.allclose(outs[0], outs[1], rtol=1e-12, atol=1e-12)
     assert not np.allclose(outs[0], 0.0)
+
+
+# ---------------------------------------------------------------- per-kv-head rotations
+def _head_fixture(d=64, hq=4, hkv=2, seed=23):
+    wl = syn.Workload("pinh", syn.Shape(hq, hkv, d, 16, 32, 4, 8, 1), [0], seed=seed, dtype="bf16")
+    q = syn.queries(wl, 0, 32, calib=True)
+    k, v = syn.kv_tokens(wl, 0, 32, calib=True)
+    return wl, rotation.head_fixture(q, k, v)
+
+
+def test_head_fixture_rotations_orthogonal_and_distinct():
+    _, fx = _head_fixture()
+    for key in ("R_K64", "R_V64"):
+        r = fx[key]
+        assert r.shape == (2, 64, 64)
+        for h in range(2):
+            assert np.abs(r[h] @ r[h].T - np.eye(64)).max() < 1e-12
+        assert np.abs(r[0] - r[1]).max() > 1e-3  # each kv head is calibrated on its own data
+
+
+def test_per_head_rotation_is_each_heads_own_rotation():
+    """Head h of a per-head quantisation equals quantising head h alone with its rotation (catches a
+    head / rotation mix-up or a transposed rotation)."""
+    wl, fx = _head_fixture()
+    x, _ = syn.kv_tokens(wl, 0, 50)
+    got = cache.quantize_rows(x, fx["R_K"], fx["clip_K"], 32)
+    for h in range(2):
+        one = cache.quantize_rows(x[:, h:h + 1], fx["R_K"][h], fx["clip_K"], 32)
+        for key in ("y", "codes", "scale", "zero"):
+            assert np.array_equal(got[key][:, h:h + 1], one[key])
+    # a transposed rotation gives other values
+    bad = cache.quantize_rows(x, np.transpose(fx["R_K"], (0, 2, 1)), fx["clip_K"], 32)
+    assert not np.array_equal(bad["codes"], got["codes"])
+
+
+def test_per_head_rotations_all_equal_reproduce_the_shared_rotation():
+    """Per-kv-head rotations that are all the layer's rotation give the shared path's codes, scales and
+    zeros bit for bit, and its decode output."""
+    g = _geom()
+    wl, fx = _fixture()
+    stack = lambda r: np.stack([r, r])
+    x, _ = syn.kv_tokens(wl, 0, 60)
+    a = cache.quantize_rows(x, fx["R_K"], fx["clip_K"], 32)
+    b = cache.quantize_rows(x, stack(fx["R_K"]), fx["clip_K"], 32)
+    for key in ("codes", "scale", "zero"):
+        assert np.array_equal(a[key], b[key])
+    assert np.abs(a["y"] - b["y"]).max() <= 1e-14 * np.abs(a["y"]).max()
+    bt = np.arange(40, dtype=np.int32)[None, :]
+    img1, img2 = cache.CacheImage(g), cache.CacheImage(g)
+    n = 200
+    k, v = syn.kv_tokens(wl, 0, n)
+    cache.write_kv(img1, 0, k, v, [0, n], [0], fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"], bt, [0])
+    cache.write_kv(img2, 0, k, v, [0, n], [0], stack(fx["R_K"]), stack(fx["R_V"]), fx["clip_K"], fx["clip_V"], bt,
+                   [0])
+    assert np.array_equal(img1.pool, img2.pool) and np.array_equal(img1.slab, img2.slab)
+    q = syn.queries(wl, 0, 1)
+    o1 = attention.decode(img1, 0, q, bt, [n], [0], fx["R_K"], fx["R_V"])
+    o2 = attention.decode(img2, 0, q, bt, [n], [0], stack(fx["R_K"]), stack(fx["R_V"]))
+    assert np.abs(o1 - o2).max() <= 1e-13 * np.abs(o1).max()
+
+
+def test_per_head_decode_fused_equals_plain():
+    """Rotating each query by its kv head's R_K and applying that head's R_V^T once is exact."""
+    g = _geom(d=64, p=16, s=4, w=8, hkv=2, num_pages=30)
+    wl, fx = _head_fixture()
+    img = cache.CacheImage(g)
+    bt = np.array([np.arange(30)], dtype=np.int32)
+    n = 300
+    _prefill(img, wl, fx, n, bt)
+    for scale in (1.0, 0.25):
+        q = syn.queries(wl, 0, 1, scale=scale)
+        a = attention.decode(img, 0, q, bt, [n], [0], fx["R_K"], fx["R_V"])
+        b = attention.decode_fused(img, 0, q, bt, [n], [0], fx["R_K"], fx["R_V"])
+        assert np.abs(a - b).max() <= 1e-12 * max(1.0, np.abs(a).max())
+        # decoding with the other head's rotations is wrong: the rotations are used per head
+        swapped = attention.decode(img, 0, q, bt, [n], [0], fx["R_K"][::-1], fx["R_V"][::-1])
+        assert np.abs(a - swapped).max() > 1e-3 * np.abs(a).max()
