@@ -24,6 +24,9 @@
  *    oscar_check_status().
  *  - Row-vector convention: a rotated vector is y = x R, R is d x d float32
  *    row-major (R[i*d + j]), 16-byte aligned (OSCAR_ERR_INVALID otherwise).
+ *    Every R_K / R_V argument holds one such matrix per layer call, or, when
+ *    the configuration's rotation_per_kv_head is 1, n_kv_heads of them back to
+ *    back ([n_kv_heads][d][d], kv head h at R + h*d*d).
  *  - bf16 tensors are uint16 bit patterns of bfloat16.
  *
  * Memory layout (all little-endian)
@@ -94,6 +97,11 @@ typedef struct {
   int32_t max_requests;      /* window-slab slots */
   int32_t max_pages_per_req; /* block-table row capacity used for bounds checks */
   int32_t num_pages;         /* INT2 pages per layer */
+  int32_t rotation_per_kv_head; /* 0: one R_K and one R_V per layer, shared by every kv head (the
+                                   pages' fixed per-layer rotation): R_K, R_V are [d][d].  1: one
+                                   rotation per (layer, kv head): R_K, R_V are [n_kv_heads][d][d],
+                                   kv head h rotated by R[h] (a variant of ours; the clip thresholds
+                                   stay per layer) */
 } oscar_config;
 
 typedef struct oscar_ctx oscar_ctx;
@@ -320,7 +328,7 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
  *  (else OSCAR_ERR_UNSUPPORTED).
  *  workspace: device scratch of oscar_extend_workspace_size(cfg, total_tokens)
  *  bytes (256-byte aligned, no initialisation); it holds q R_K for every query
- *  row and R_V^T.  Softmax scale 1/sqrt(d), query head h reads kv head
+ *  row and R_V^T (one per kv head with rotation_per_kv_head).  Softmax scale 1/sqrt(d), query head h reads kv head
  *  h / (n_q_heads / n_kv_heads).  Two kernels on the stream: the query
  *  rotation, then the tensor-core attention (timing name "extend"). */
 oscar_status oscar_extend_workspace_size(const oscar_config* cfg, int32_t total_tokens, size_t* bytes);

@@ -32,7 +32,7 @@ class OscarError(RuntimeError):
 class oscar_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_layers", "n_q_heads", "n_kv_heads", "head_dim", "page_size", "group_size", "sink", "recent",
-        "max_requests", "max_pages_per_req", "num_pages")]
+        "max_requests", "max_pages_per_req", "num_pages", "rotation_per_kv_head")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -781,7 +781,7 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(DecodeArgs
   // R_V does not depend on the previous kernel: start its copy before waiting on it
   if (tid == 0) {
     mbar_arrive_expect_tx(&bar, r_bytes + p_bytes);
-    bulk_g2s(Rs, a.R_V + (size_t)j0 * D, r_bytes, &bar);
+    bulk_g2s(Rs, a.R_V + (size_t)(h0 / g.gq()) * g.rot_stride() + (size_t)j0 * D, r_bytes, &bar);
   }
   pdl_wait();
   if (tid == 0 && p_bytes) bulk_g2s(parts, gbase, p_bytes, &bar);
@@ -930,7 +930,7 @@ __global__ void __launch_bounds__(kHeadThreads) decode_combine_head_kernel(Decod
   // R_V does not depend on the previous kernel: start its copy before waiting on it
   if (tid == 0) {
     mbar_arrive_expect_tx(&bar, D * D * sizeof(float) + (a.wl.combine_part_smem ? head_bytes : 0));
-    bulk_g2s(Rs, a.R_V, D * D * sizeof(float), &bar);
+    bulk_g2s(Rs, a.R_V + (size_t)(h / g.gq()) * g.rot_stride(), D * D * sizeof(float), &bar);
   }
   pdl_wait();
   if (tid == 0 && a.wl.combine_part_smem) bulk_g2s(parts, gbase, (uint32_t)head_bytes, &bar);

@@ -130,21 +130,33 @@ __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
   float* Rs = xq_sm;              // [D][D]
   float* qs = xq_sm + D * D;      // [64][D + 1]
   const int t = threadIdx.x;
-  const long long rows = (long long)a.total_tokens * a.g.Hq;
+  const Geom& g = a.g;
+  const long long rows = (long long)a.total_tokens * g.Hq;
   float* qrot = reinterpret_cast<float*>(a.ws + a.qrot_off);
+  // blockIdx.y: the kv head whose rotation the CTA applies (0 with one rotation per layer)
+  const int kvh = blockIdx.y;
   if (blockIdx.x == gridDim.x - 1) {
-    float* rvt = reinterpret_cast<float*>(a.ws + a.rvt_off);
+    float* rvt = reinterpret_cast<float*>(a.ws + a.rvt_off) + (size_t)kvh * D * D;
+    const float* rv = a.R_V + (size_t)kvh * g.rot_stride();
     for (int idx = t; idx < D * D; idx += 256) {
       const int i = idx / D, j = idx % D;   // rvt[i][j] = R_V[j][i]; coalesced writes
-      rvt[idx] = __ldg(a.R_V + (size_t)j * D + i);
+      rvt[idx] = __ldg(rv + (size_t)j * D + i);
     }
     return;
   }
   for (int idx = t; idx < D * D / 4; idx += 256)
-    reinterpret_cast<float4*>(Rs)[idx] = __ldg(reinterpret_cast<const float4*>(a.R_K) + idx);
-  const long long r0 = (long long)blockIdx.x * 64;
+    reinterpret_cast<float4*>(Rs)[idx] =
+        __ldg(reinterpret_cast<const float4*>(a.R_K + (size_t)kvh * g.rot_stride()) + idx);
+  // global row of local row l: one rotation per layer, rows 64 x + l of [tokens][Hq]; one per kv
+  // head, the 64 / gq tokens x gq query heads of kv head kvh starting at token (64 / gq) x
+  const int gq = g.gq();
+  auto row_of = [&](int l) -> long long {
+    if (!g.rph) return (long long)blockIdx.x * 64 + l;
+    const long long tok = (long long)blockIdx.x * (64 / gq) + l / gq;
+    return tok < a.total_tokens ? tok * g.Hq + (long long)kvh * gq + l % gq : rows;
+  };
   for (int idx = t; idx < 64 * D; idx += 256) {
-    const long long r = r0 + idx / D;
+    const long long r = row_of(idx / D);
     float v = 0.f;
     if (r < rows) {
       const size_t e = (size_t)r * D + idx % D;
@@ -172,7 +184,7 @@ __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
       acc[m].w = fmaf(qi, rv.w, acc[m].w);
     }
   }
-  const long long r = r0 + rr;
+  const long long r = row_of(rr);
   if (r < rows) {
     float4* dst = reinterpret_cast<float4*>(qrot + (size_t)r * D + 4 * cq);
 #pragma unroll
@@ -973,7 +985,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   constexpr int NJ = D / 2;
   const int j0 = half * NJ;
   if (warp < 8) {
-    const float4* rvt = reinterpret_cast<const float4*>(a.ws + a.rvt_off);
+    const float4* rvt = reinterpret_cast<const float4*>(a.ws + a.rvt_off + (g.rph ? (size_t)kvh * D * D * 4 : 0));
     for (int idx = tid; idx < D * D / 4; idx += 256) reinterpret_cast<float4*>(Rt)[idx] = rvt[idx];
     if (warp < 4) linv[r] = l_run > 0.f ? 1.f / l_run : 0.f;
     // y: the rotated accumulator at value scale, this thread's half of row r
@@ -1055,8 +1067,12 @@ int launch_extend_d(const ExtendArgs& a, void* stream) {
   const size_t qsm = qrot_smem_floats<D>() * sizeof(float);
   cudaError_t e = ensure_smem_limit(extend_qrot_kernel<D>, qsm);
   if (e != cudaSuccess) return (int)e;
-  const unsigned qgrid = (unsigned)((rows + 63) / 64) + 1;
-  extend_qrot_kernel<D><<<qgrid, 256, qsm, s>>>(a);
+  // one rotation per kv head: grid.y = kv heads, each CTA 64 / gq tokens of its head's query rows
+  const int heads = a.g.rph ? a.g.Hkv : 1;
+  const long long per = a.g.rph ? 64 / a.g.gq() : 64;
+  const long long units = a.g.rph ? (long long)a.total_tokens : rows;
+  const unsigned qgrid = (unsigned)((units + per - 1) / per) + 1;
+  extend_qrot_kernel<D><<<dim3(qgrid, heads), 256, qsm, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
   e = ensure_smem_limit(extend_attn_kernel<D>, XLayout<D>::SMEM);
   if (e != cudaSuccess) return (int)e;
@@ -1068,14 +1084,15 @@ int launch_extend_d(const ExtendArgs& a, void* stream) {
 
 }  // namespace
 
+// workspace: R_V^T ([Hkv][D][D] with a rotation per kv head, else [D][D]) then q R_K per row
 size_t extend_workspace_bytes(const Geom& g, long long total_tokens) {
-  const size_t rvt = ((size_t)g.D * g.D * 4 + 255) & ~size_t(255);
+  const size_t rvt = ((size_t)(g.rph ? g.Hkv : 1) * g.D * g.D * 4 + 255) & ~size_t(255);
   return rvt + (size_t)total_tokens * g.Hq * g.D * 4;
 }
 
 void extend_ws_offsets(const Geom& g, size_t* rvt_off, size_t* qrot_off) {
   *rvt_off = 0;
-  *qrot_off = ((size_t)g.D * g.D * 4 + 255) & ~size_t(255);
+  *qrot_off = ((size_t)(g.rph ? g.Hkv : 1) * g.D * g.D * 4 + 255) & ~size_t(255);
 }
 
 int launch_extend(const ExtendArgs& a, void* stream) {

@@ -272,13 +272,16 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 2) write_kernel(WriteArgs a
   const bool is_v = blockIdx.y == 1;
   const Geom& g = a.g;
   const void* src = is_v ? a.V : a.K;
+  // one rotation per layer: rows (token, kv head) of every head; one per kv head: this CTA
+  // takes the rows of kv head blockIdx.z with that head's rotation
+  const int hz = g.rph ? (int)blockIdx.z : 0;
   if (!a.hadamard) {  // the Hadamard-only rotation has no matrix (R_K, R_V are null)
-    const float4* Rg = reinterpret_cast<const float4*>(is_v ? a.R_V : a.R_K);
+    const float4* Rg = reinterpret_cast<const float4*>((is_v ? a.R_V : a.R_K) + (size_t)hz * g.rot_stride());
     float4* R4 = reinterpret_cast<float4*>(Rs);
     for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) R4[i] = Rg[i];
   }
   __syncthreads();
-  const long long rows = (long long)a.total_tokens * g.Hkv;
+  const long long rows = g.rph ? (long long)a.total_tokens : (long long)a.total_tokens * g.Hkv;
   const long long stride = (long long)gridDim.x * kWarpsPerCta * kRowsPerPass;
   for (long long base = ((long long)blockIdx.x * kWarpsPerCta + warp) * kRowsPerPass; base < rows; base += stride) {
     unsigned hist = 0;  // bit r: row r goes to an INT2 page
@@ -286,8 +289,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 2) write_kernel(WriteArgs a
     for (int r = 0; r < kRowsPerPass; ++r) {
       const long long item = base + r;
       if (item >= rows) continue;
-      const int row = static_cast<int>(item / g.Hkv);
-      const int h = static_cast<int>(item % g.Hkv);
+      const int row = g.rph ? static_cast<int>(item) : static_cast<int>(item / g.Hkv);
+      const int h = g.rph ? hz : static_cast<int>(item % g.Hkv);
       int lo = 0, hi = a.batch - 1;  // request of this row: largest b with cu_seqlens[b] <= row
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -408,7 +411,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) evict_kernel(WriteArgs a) {
     const uint16_t* ring = window_row(a, req, h, is_v, window_slot(e, g.S, g.W));
     for (int c = lane; c < D; c += 32) sm[warp].x[c] = __uint_as_float(static_cast<uint32_t>(ring[c]) << 16);
     __syncwarp();
-    store_history<D>(a, b, e, h, is_v, sm[warp].x, R, sm[warp].codes, sm[warp].f);
+    store_history<D>(a, b, e, h, is_v, sm[warp].x, R + (size_t)h * g.rot_stride(), sm[warp].codes, sm[warp].f);
     __syncwarp();
   }
 }
@@ -423,6 +426,10 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) evict_kernel(WriteArgs a) {
 // h, quantises and packs.  The CTA reads the evicted token's ring row before
 // overwriting that slot with the new token.
 constexpr int kAppendHeads = 2;
+
+// kv heads served by one append CTA: kAppendHeads share the CTA's staged rotation, so with a
+// rotation per kv head a CTA serves one head
+__host__ __device__ inline int append_heads_per_cta(const Geom& g) { return g.rph ? 1 : kAppendHeads; }
 
 // Returns false if the rotation copy timed out (flagged; nothing written).
 // (b, by, bz): request, K|V, head group.  early_r: the fused step's form, which
@@ -441,14 +448,16 @@ __device__ __forceinline__ bool append_body(const WriteArgs& a, float* Rsm, uint
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geom& g = a.g;
   const bool is_v = by == 1;
-  const int h0 = bz * HPC;
-  const int nh = min(HPC, g.Hkv - h0);
+  const int hpc = append_heads_per_cta(g);
+  const int h0 = bz * hpc;
+  const int nh = min(hpc, g.Hkv - h0);
+  const float* Rg = (is_v ? a.R_V : a.R_K) + (size_t)h0 * g.rot_stride();  // the rotation of this CTA's heads
   if (early_r) {
     if (threadIdx.x == 0) {
       mbar_init(bar, 1);
       fence_barrier_init();
       mbar_arrive_expect_tx(bar, D * D * sizeof(float));
-      bulk_g2s(Rsm, is_v ? a.R_V : a.R_K, D * D * sizeof(float), bar);
+      bulk_g2s(Rsm, Rg, D * D * sizeof(float), bar);
     }
     pdl_wait();
   }
@@ -477,7 +486,7 @@ __device__ __forceinline__ bool append_body(const WriteArgs& a, float* Rsm, uint
     mbar_init(bar, 1);
     fence_barrier_init();
     mbar_arrive_expect_tx(bar, D * D * sizeof(float));
-    bulk_g2s(Rsm, is_v ? a.R_V : a.R_K, D * D * sizeof(float), bar);
+    bulk_g2s(Rsm, Rg, D * D * sizeof(float), bar);
   }
   // issue the loads, let the dependent kernel launch (its first requests then
   // queue behind these), then consume them
@@ -598,7 +607,7 @@ __global__ void __launch_bounds__(128) step_prep_kernel(const __grid_constant__ 
     return;
   }
   const int i = blockIdx.x - nq;
-  const int nz = (w.g.Hkv + kAppendHeads - 1) / kAppendHeads;
+  const int nz = (w.g.Hkv + append_heads_per_cta(w.g) - 1) / append_heads_per_cta(w.g);
   (void)append_body<D>(w, Rsm, &bar, i / (2 * nz), (i % (2 * nz)) / nz, (i % (2 * nz)) % nz, true);
   pdl_launch_dependents();  // covers the early exits
 }
@@ -607,13 +616,14 @@ __global__ void __launch_bounds__(128) step_prep_kernel(const __grid_constant__ 
 
 template <int D>
 int launch_write_t(const WriteArgs& a, cudaStream_t s) {
-  const long long rows = (long long)a.total_tokens * a.g.Hkv;
+  const int heads = a.g.rph ? a.g.Hkv : 1;  // grid z: one kv head per z with a rotation per kv head
+  const long long rows = (long long)a.total_tokens * a.g.Hkv / heads;
   long long ctas = (rows + kWarpsPerCta * kRowsPerPass - 1) / (kWarpsPerCta * kRowsPerPass);
-  if (ctas > 152 * 2) ctas = 152 * 2;  // two CTAs per SM fit (R + row buffers)
+  if (ctas * heads > 152 * 2) ctas = (152 * 2 + heads - 1) / heads;  // two CTAs per SM fit (R + row buffers)
   const size_t smem = sizeof(float) * D * D + sizeof(WriteSmem<D>);
   cudaError_t e = ensure_smem_limit(write_kernel<D>, smem);
   if (e != cudaSuccess) return (int)e;
-  write_kernel<D><<<dim3((unsigned)ctas, 2), kWarpsPerCta * 32, smem, s>>>(a);
+  write_kernel<D><<<dim3((unsigned)ctas, 2, (unsigned)heads), kWarpsPerCta * 32, smem, s>>>(a);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -636,7 +646,7 @@ int launch_evict(const WriteArgs& a, void* stream) {
 int launch_step_prep(const WriteArgs& w, const DecodeArgs& d, void* stream, bool pdl) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (w.batch == 0) return 0;
-  const int nz = (w.g.Hkv + kAppendHeads - 1) / kAppendHeads;
+  const int nz = (w.g.Hkv + append_heads_per_cta(w.g) - 1) / append_heads_per_cta(w.g);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d.g.Hkv * (d.g.D / 32) * d.batch + w.batch * 2 * nz);
   cfg.blockDim = dim3(128);
@@ -659,7 +669,7 @@ int launch_append(const WriteArgs& a, void* stream, bool pdl) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.batch == 0) return 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.batch, 2, (a.g.Hkv + kAppendHeads - 1) / kAppendHeads);
+  cfg.gridDim = dim3(a.batch, 2, (a.g.Hkv + append_heads_per_cta(a.g) - 1) / append_heads_per_cta(a.g));
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = sizeof(float) * a.g.D * a.g.D;
   cfg.stream = s;

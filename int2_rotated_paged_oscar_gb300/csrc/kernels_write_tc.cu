@@ -180,11 +180,18 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
   uint64_t* acc_full = bars + 2 * L::NS;
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBARS);
-  const long long rows = (long long)a.total_tokens * g.Hkv;
+  // Work items are tiles of kTileM rows.  One rotation per layer: rows r = token * Hkv + h
+  // of the whole call, tile i covering rows [kTileM i, kTileM (i + 1)), split over the CTAs.
+  // A rotation per kv head: CTA x keeps kv head x mod Hkv (and that head's R planes) and
+  // takes the tiles of 128 consecutive tokens of that head, loaded by a 3-D tensor map.
+  const int hsel = g.rph ? (int)blockIdx.x % g.Hkv : 0;
+  const int cta_k = g.rph ? (int)blockIdx.x / g.Hkv : (int)blockIdx.x;
+  const int n_ctas = g.rph ? (int)gridDim.x / g.Hkv : (int)gridDim.x;
+  const long long rows = g.rph ? (long long)a.total_tokens : (long long)a.total_tokens * g.Hkv;
   const int tiles = (int)((rows + kTileM - 1) / kTileM);
 
   // R^T as three BF16 planes, K-major with the 128-byte swizzle (row n = column n of R)
-  const float* R = is_v ? a.R_V : a.R_K;
+  const float* R = (is_v ? a.R_V : a.R_K) + (size_t)hsel * g.rot_stride();
   // item = (n, k-octet): 8 consecutive k of column n, contiguous in the swizzled row
   for (int item = threadIdx.x; item < D * D / 8; item += blockDim.x) {
     const int n = item % D, k0 = (item / D) * 8;
@@ -240,14 +247,18 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
       const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
       const uint32_t idesc = idesc_bf16_f32(kTileM, D);
       const uint32_t b_base = smem_u32(bsm);
-      const int n_mine = blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+      const int n_mine = cta_k < tiles ? (tiles - 1 - cta_k) / n_ctas + 1 : 0;
       auto load = [&](int i) {  // tile i of this CTA into stage i % NS
         const int st = i % L::NS;
         mbar_arrive_expect_tx(&a_full[st], L::A_BYTES);
-        const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+        const int tile = cta_k + i * n_ctas;
 #pragma unroll
-        for (int c = 0; c < L::KCH; ++c)
-          tma_load_2d_tc(asm_ + st * L::A_BYTES + c * kTileM * 128, tmap, 64 * c, tile * kTileM, &a_full[st]);
+        for (int c = 0; c < L::KCH; ++c) {
+          if (g.rph)
+            tma_load_3d_tc(asm_ + st * L::A_BYTES + c * kTileM * 128, tmap, 64 * c, hsel, tile * kTileM, &a_full[st]);
+          else
+            tma_load_2d_tc(asm_ + st * L::A_BYTES + c * kTileM * 128, tmap, 64 * c, tile * kTileM, &a_full[st]);
+        }
       };
       for (int i = 0; i < L::NS && i < n_mine; ++i) load(i);
       int i = 0;
@@ -302,15 +313,15 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
     const float clip = is_v ? a.clip_V : a.clip_K;
     const void* src = is_v ? a.V : a.K;
     int i = eg;
-    for (int tile = blockIdx.x + eg * gridDim.x; tile < tiles; tile += 2 * gridDim.x, i += 2) {
+    for (int tile = cta_k + eg * n_ctas; tile < tiles; tile += 2 * n_ctas, i += 2) {
       const int s = i & 1;
       const uint32_t u = (uint32_t)(i >> 1);
       // where this row goes: 1 = INT2 history slot, 2 = BF16 window slot, 0 = nowhere
       const long long r = (long long)tile * kTileM + t;
       int kind = 0, b = 0, pos = 0, h = 0, token = 0;
       if (r < rows) {
-        token = static_cast<int>(r / g.Hkv);
-        h = static_cast<int>(r % g.Hkv);
+        token = g.rph ? static_cast<int>(r) : static_cast<int>(r / g.Hkv);
+        h = g.rph ? hsel : static_cast<int>(r % g.Hkv);
         int lo = 0, hi = a.batch - 1;  // request: largest b with cu_seqlens[b] <= token
         while (lo < hi) {
           const int mid = (lo + hi + 1) >> 1;
@@ -413,7 +424,8 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
           const size_t sbase = ((size_t)a.layer * g.max_req + req) * g.slab_req_elems();
           const int slot = pos < g.S ? pos : g.S + (pos - g.S) % g.W;
           uint4* dst = reinterpret_cast<uint4*>(a.slab + sbase + (((size_t)h * 2 + (is_v ? 1 : 0)) * g.window() + slot) * D);
-          const uint4* in = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + (size_t)r * D);
+          const uint4* in = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) +
+                                                           ((size_t)token * g.Hkv + h) * D);
 #pragma unroll
           for (int q = 0; q < D / 8; ++q) dst[q] = in[q];
         }
@@ -452,20 +464,42 @@ int make_row_map(CUtensorMap* map, const void* base, long long rows, int D) {
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
+// 3-D map over [tokens][Hkv][D] BF16, box 64 x 1 x 128: 128 tokens of one kv head (the same
+// shared-memory image as a 64 x 128 box of the 2-D map).
+int make_head_row_map(CUtensorMap* map, const void* base, long long tokens, int hkv, int D) {
+  auto enc = tc_get_encode();
+  if (!enc) return (int)cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)hkv * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kTileM};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+}
+
 template <int D>
 int launch_write_tc_t(const WriteArgs& a, cudaStream_t s) {
   using L = TcPlan<D>;
-  const long long rows = (long long)a.total_tokens * a.g.Hkv;
+  const bool rph = a.g.rph != 0;
+  const long long rows = rph ? (long long)a.total_tokens : (long long)a.total_tokens * a.g.Hkv;
   const long long tiles = (rows + kTileM - 1) / kTileM;
   CUtensorMap mk, mv;
-  int e = make_row_map(&mk, a.K, rows, D);
+  int e = rph ? make_head_row_map(&mk, a.K, a.total_tokens, a.g.Hkv, D) : make_row_map(&mk, a.K, rows, D);
   if (e) return e;
-  if ((e = make_row_map(&mv, a.V, rows, D))) return e;
+  if ((e = rph ? make_head_row_map(&mv, a.V, a.total_tokens, a.g.Hkv, D) : make_row_map(&mv, a.V, rows, D)))
+    return e;
   // at least 120 KB of shared memory: one CTA per SM, so the TMEM allocation never waits
   const int smem = L::SMEM > 120 * 1024 ? L::SMEM : 120 * 1024;
   cudaError_t ce = ensure_smem_limit(write_tc_kernel<D>, smem);
   if (ce != cudaSuccess) return (int)ce;
-  const int ctas = (int)(tiles < 76 ? tiles : 76);  // x2 (K, V): one CTA per SM
+  // x2 (K, V): one CTA per SM; with a rotation per kv head, the same number of CTAs for every head
+  int ctas = (int)(tiles < 76 ? tiles : 76);
+  if (rph) {
+    const long long per_head = tiles < 76 / a.g.Hkv ? tiles : (76 / a.g.Hkv > 0 ? 76 / a.g.Hkv : 1);
+    ctas = (int)(per_head * a.g.Hkv);
+  }
   write_tc_kernel<D><<<dim3(ctas, 2), tc_threads<D>(), smem, s>>>(mk, mv, a);
   return (int)cudaGetLastError();
 }

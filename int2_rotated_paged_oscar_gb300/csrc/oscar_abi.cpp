@@ -109,6 +109,9 @@ oscar_status validate(const oscar_config* c, Geom* out) {
   g.max_req = c->max_requests;
   g.max_pages_per_req = c->max_pages_per_req;
   g.num_pages = c->num_pages;
+  if (c->rotation_per_kv_head != 0 && c->rotation_per_kv_head != 1)
+    return fail(OSCAR_ERR_INVALID, "rotation_per_kv_head must be 0 or 1");
+  g.rph = c->rotation_per_kv_head;
   *out = g;
   return OSCAR_OK;
 }
@@ -263,7 +266,9 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   int jb = 32, hpc = 1;
   auto combine_ctas = [&]() { return rows / hpc * (g.D / jb); };
   while (combine_ctas() > 2 * 152 && jb < g.D) jb *= 2;
-  while (combine_ctas() > 2 * 152 && hpc < 16 && g.Hq % (2 * hpc) == 0) hpc *= 2;
+  // with a rotation per kv head, the heads of a CTA share one kv head (one R_V)
+  const int hpc_max = g.rph ? (gq < 16 ? gq : 16) : 16;
+  while (combine_ctas() > 2 * 152 && hpc < hpc_max && g.Hq % (2 * hpc) == 0) hpc *= 2;
   w.combine_head = 0;
   w.combine_hpc = hpc;
   w.combine_jb = jb;

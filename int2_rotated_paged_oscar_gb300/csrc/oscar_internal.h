@@ -29,7 +29,10 @@ constexpr int kDtypeBF16 = 1;
 // Cache geometry (validated copy of oscar_config).
 struct Geom {
   int L, Hq, Hkv, D, P, G, S, W, max_req, max_pages_per_req, num_pages;
+  int rph;  // 1: one rotation per kv head (R_K, R_V are [Hkv][D][D]); 0: one per layer
   OSCAR_HD int gq() const { return Hq / Hkv; }
+  // floats between the rotations of consecutive kv heads (0: every kv head shares one)
+  OSCAR_HD size_t rot_stride() const { return rph ? (size_t)D * D : 0; }
   OSCAR_HD size_t row_bytes() const { return (size_t)D / 4; }
   OSCAR_HD size_t sz_bytes() const { return 4 * (size_t)(D / G); }
   OSCAR_HD size_t k_sz_off() const { return (size_t)P * row_bytes(); }

@@ -55,7 +55,7 @@ __device__ __forceinline__ void q_rotate_cta(const DecodeArgs& a, int grp, int k
   WsView ws = ws_view(a);
   // R_K column slice: D rows x 32 floats (8 float4 per row), 16-byte loads, all in flight
   {
-    const float4* Rg = reinterpret_cast<const float4*>(a.R_K);
+    const float4* Rg = reinterpret_cast<const float4*>(a.R_K + (size_t)kvh * g.rot_stride());  // this kv head's R_K
     float4 v[D * 8 / T];
 #pragma unroll
     for (int u = 0; u < D * 8 / T; ++u) {

@@ -65,13 +65,15 @@ class GpuCache:
         self.slab.copy_(torch.from_numpy(img.slab.reshape(-1).view(np.int16)))
 
 
-def make_gpu_cache(geom: cache.Geometry, n_q_heads: int, max_pages_per_req: int, fill: int = 0) -> GpuCache:
+def make_gpu_cache(geom: cache.Geometry, n_q_heads: int, max_pages_per_req: int, fill: int = 0,
+                   rotation_per_kv_head: int = 0) -> GpuCache:
     torch = torch_mod()
     import int2_rotated_paged_oscar_gb300 as osc
     cfg = osc.make_config(num_layers=geom.num_layers, n_q_heads=n_q_heads, n_kv_heads=geom.n_kv_heads,
                           head_dim=geom.head_dim, page_size=geom.page_size, group_size=geom.group_size,
                           sink=geom.sink, recent=geom.recent, max_requests=geom.max_requests,
-                          max_pages_per_req=max_pages_per_req, num_pages=geom.num_pages)
+                          max_pages_per_req=max_pages_per_req, num_pages=geom.num_pages,
+                          rotation_per_kv_head=rotation_per_kv_head)
     nbytes = osc.oscar_int2_pool_bytes(cfg)
     assert nbytes == geom.num_layers * geom.num_pages * geom.n_kv_heads * geom.block_bytes
     pool = torch.full((nbytes,), fill, dtype=torch.uint8, device="cuda")
