@@ -184,13 +184,19 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
       bulk_g2s_hint(ring + s * Lay::BLOCK, pool_l + ((size_t)pid * g.Hkv + kvh) * Lay::BLOCK, Lay::BLOCK, &bars[s],
                     stream_policy);
   };
-  // Fill the ring before waiting on the preceding grid, so the page stream
-  // overlaps it.  In a fused step that grid (the append) may still be writing
-  // the last history page: a stage holding that page is filled after the wait.
+  // The warp's first page is requested before the wait on the preceding grid, so
+  // the page stream overlaps it; the rest of the ring is requested after that wait
+  // and the query-side set-up (staggered fill: when every warp of the grid requests
+  // its whole ring at once, each warp's first page lands only near the end of the
+  // burst, while first pages requested first arrive first).  In a fused step the preceding
+  // grid (the append) may still be writing the last history page: if that is the
+  // first page, it is requested after the wait.
   auto is_tail = [&](int i) { return a.defer_tail_page && pg0 + warp + kWarps * i == n_hist_pages - 1; };
-  if (lane == 0)
-    for (int i = 0; i < WS && i < n_mine; ++i)
-      if (!is_tail(i)) issue(i);
+  int n_issued = 0;  // pages requested so far (lane 0)
+  if (lane == 0 && n_mine > 0 && !is_tail(0)) {
+    issue(0);
+    n_issued = 1;
+  }
 
   // ---------------- query side (written by q_rotate): wait for the previous grid
   pdl_wait();
@@ -252,9 +258,13 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     qz2[nt] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&vb2)) << 16;
   }
 
+  if (lane == 0 && n_mine > 0 && n_issued == 0) {
+    issue(0);
+    n_issued = 1;
+  }
+  // the rest of the ring, a query-side set-up later than the first pages of the grid
   if (lane == 0)
-    for (int i = 0; i < WS && i < n_mine; ++i)
-      if (is_tail(i)) issue(i);
+    for (; n_issued < WS && n_issued < n_mine; ++n_issued) issue(n_issued);
 
   float mm[NH], thr[NH], l_run[NH];
   float acc[Lay::MT][4];
@@ -617,6 +627,7 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
       i_fail = i;
       break;
     }
+
     if (stage_ok[s]) {
       const uint8_t* buf = ring + s * Lay::BLOCK;
       const int tp = (pg0 + warp + kWarps * i) * P;  // first token of the page
@@ -640,12 +651,12 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     if (lane == 0 && i + WS < n_mine) {
       fence_proxy_async_smem();
       issue(i + WS);
+      n_issued = i + WS + 1;
     }
   }
   if (aborted && lane == 0) {
     // drain this warp's copies still in flight before the CTA exits, again bounded
-    const int last = min(n_mine, i_fail + WS);
-    for (int i = i_fail; i < last; ++i) (void)mbar_wait_bounded(&bars[i % WS], (i / WS) & 1, nullptr);
+    for (int i = i_fail; i < n_issued; ++i) (void)mbar_wait_bounded(&bars[i % WS], (i / WS) & 1, nullptr);
   }
   pdl_launch_dependents();
   if (__syncthreads_or(aborted)) return false;
