@@ -119,12 +119,14 @@ size_t oscar_window_slab_bytes(const oscar_config* cfg);
 size_t oscar_page_block_bytes(const oscar_config* cfg);
 
 /* Validate cfg and create a context over caller-owned device buffers:
- * int2_pool (oscar_int2_pool_bytes) and window_slab (oscar_window_slab_bytes).
+ * int2_pool (oscar_int2_pool_bytes) and window_slab (oscar_window_slab_bytes),
+ * both 16-byte aligned (else OSCAR_ERR_INVALID).
  * The context keeps the raw pointers: both buffers must stay allocated until
  * oscar_destroy (and until any captured graph that uses them is destroyed).
  * Either pointer may be NULL for a host-only context (allocator calls work,
  * kernel calls return OSCAR_ERR_INVALID).  Creating a context with buffers
- * allocates a 4-byte device status word.  OSCAR_ERR_UNSUPPORTED for a shape
+ * allocates a 4-byte device status word and max_requests x n_kv_heads int32
+ * counters of the one-launch decode (zero between launches).  OSCAR_ERR_UNSUPPORTED for a shape
  * outside head_dim {64,128}, page_size {16,32,64}, group_size 32,
  * n_q_heads/n_kv_heads in {1,2,4,8}. */
 oscar_status oscar_create(const oscar_config* cfg, void* int2_pool, void* window_slab, oscar_ctx** out);
@@ -249,7 +251,17 @@ oscar_status oscar_decode_workspace_size(const oscar_config* cfg, int32_t batch,
  * clip threshold (a write to it, or oscar_set_layer_clip).  R_K and R_V
  * (device float32 [d][d], the layer's fixed rotations) are read before the
  * kernels wait on the work queued ahead of them: they must not be written by
- * the kernel launched immediately before this call on the stream. */
+ * the kernel launched immediately before this call on the stream.
+ *
+ * Launches (oscar_set_decode_form).  Three kernels: q_rotate, split-K and
+ * combine.  One kernel: its split CTAs form the rotated query themselves and
+ * the last CTA of each (request, kv head) to finish (an atomic ticket on a
+ * counter the context owns; no CTA waits on another) merges that pair's
+ * partials and writes its output rows; before its dependency wait it only
+ * prefetches into L2.  One-launch calls on one context share its counters: do
+ * not run two of them concurrently on different streams (order them with
+ * events).  After a failed launch, oscar_check_status also resets the
+ * counters. */
 oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, void* out,
                                int32_t out_dtype, const int32_t* block_table, int32_t bt_stride,
                                const int32_t* seq_lens, const int32_t* req_slot, int32_t batch, int32_t max_seq,
@@ -263,9 +275,10 @@ oscar_status oscar_decode_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
  * same arguments as those two calls (K_new, V_new: [batch][n_kv_heads][d] in
  * kv_dtype; seq_lens [batch] device int32 counts the new token).  The query
  * rotation and the append run as one grid ("step_prep": rotation CTAs first,
- * then append CTAs), launched as a programmatic dependent of the preceding
- * kernel; the split-K kernel is its dependent and reads only the page the
- * append may be writing after the dependency resolves.  The caller maps the
+ * then append CTAs; no rotation CTAs when the decode is one launch), launched
+ * as a programmatic dependent of the preceding kernel; the split-K kernel is
+ * its dependent and reads only the page the append may be writing after the
+ * dependency resolves.  The caller maps the
  * page of the evicted token beforehand, as for oscar_append_step. */
 oscar_status oscar_decode_step(oscar_ctx* ctx, int32_t layer, const void* K_new, const void* V_new, int32_t kv_dtype,
                                const void* q, int32_t q_dtype, void* out, int32_t out_dtype,
@@ -378,6 +391,20 @@ oscar_status oscar_selftest_wait_timeout(oscar_ctx* ctx, int32_t limit_us, void*
  * OSCAR_ERR_DEVICE (bits in *out_bits if non-NULL) if any kernel flagged an
  * error since the last check. */
 oscar_status oscar_check_status(oscar_ctx* ctx, void* stream, int32_t* out_bits);
+
+/* ---------------------------------------------------------------- decode launch form
+ * How the INT2 decode calls (oscar_decode_attn, oscar_decode_step,
+ * oscar_decode_attn_noalloc) launch: OSCAR_DECODE_AUTO (the library's choice
+ * for the batch; the default), OSCAR_DECODE_THREE_KERNELS (query rotation,
+ * split-K and combine kernels) or OSCAR_DECODE_ONE_LAUNCH (the one-kernel
+ * form described at oscar_decode_attn whenever batch <= max_requests, three
+ * kernels otherwise).  The forms agree within floating-point rounding (the
+ * rotated query is summed in another order).  Host-only; OSCAR_ERR_INVALID
+ * for any other value. */
+#define OSCAR_DECODE_AUTO 0
+#define OSCAR_DECODE_THREE_KERNELS 1
+#define OSCAR_DECODE_ONE_LAUNCH 2
+oscar_status oscar_set_decode_form(oscar_ctx* ctx, int32_t form);
 
 /* Kernel timing for tracing: when enabled, the library brackets each launch
  * of the named kernel family with CUDA events on the launch stream.

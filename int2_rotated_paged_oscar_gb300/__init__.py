@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "liboscar.so")
 
 OK, ERR_INVALID, ERR_OOM, ERR_CUDA, ERR_DEVICE, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
 DTYPE_F32, DTYPE_BF16 = 0, 1
+DECODE_AUTO, DECODE_THREE_KERNELS, DECODE_ONE_LAUNCH = 0, 1, 2
 DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_LEN, DEV_BAD_SLOT = 1, 2, 4, 8
 
 
@@ -92,6 +93,7 @@ _SIGS = {
                                       ctypes.c_size_t, _vp]),
     "oscar_selftest_wait_timeout": (_i32, [_vp, _i32, _vp]),
     "oscar_check_status": (_i32, [_vp, _vp, _c_i32p]),
+    "oscar_set_decode_form": (_i32, [_vp, _i32]),
     "oscar_set_timing": (_i32, [_vp, _i32]),
     "oscar_kernel_time": (_i32, [_vp, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), _c_i32p]),
     "oscar_reset_timing": (_i32, [_vp]),
@@ -322,6 +324,10 @@ def oscar_check_status(ctx, stream=None) -> int:
     if st not in (OK, ERR_DEVICE):
         _check(st)
     return bits.value
+
+
+def oscar_set_decode_form(ctx, form: int) -> None:
+    _check(load().oscar_set_decode_form(ctx, int(form)))
 
 
 def oscar_set_timing(ctx, enable: bool) -> None:

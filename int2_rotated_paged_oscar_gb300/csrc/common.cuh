@@ -18,8 +18,11 @@ namespace oscar {
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device) (the
 // first launch on a device), so that later launches, including ones recorded
-// into a CUDA graph, issue nothing but the launch itself.
-inline cudaError_t ensure_smem_limit_ptr(const void* kern, size_t bytes) {
+// into a CUDA graph, issue nothing but the launch itself.  max_carveout: also ask
+// for the largest shared-memory share of the SM's L1/shared storage, for kernels
+// whose resident CTAs per SM need it (the driver's default split may leave room
+// for fewer).
+inline cudaError_t ensure_smem_limit_ptr(const void* kern, size_t bytes, bool max_carveout = false) {
   struct Entry { const void* k; int dev; size_t bytes; };
   static std::mutex mu;
   static Entry table[256];
@@ -32,6 +35,10 @@ inline cudaError_t ensure_smem_limit_ptr(const void* kern, size_t bytes) {
     if (table[i].k == kern && table[i].dev == dev && table[i].bytes >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
+  if (max_carveout) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
   for (int i = 0; i < used; ++i)
     if (table[i].k == kern && table[i].dev == dev) { table[i].bytes = bytes; return cudaSuccess; }
   if (used < 256) table[used++] = Entry{kern, dev, bytes};
@@ -39,8 +46,8 @@ inline cudaError_t ensure_smem_limit_ptr(const void* kern, size_t bytes) {
 }
 
 template <typename Kernel>
-inline cudaError_t ensure_smem_limit(Kernel kern, size_t bytes) {
-  return ensure_smem_limit_ptr(reinterpret_cast<const void*>(kern), bytes);
+inline cudaError_t ensure_smem_limit(Kernel kern, size_t bytes, bool max_carveout = false) {
+  return ensure_smem_limit_ptr(reinterpret_cast<const void*>(kern), bytes, max_carveout);
 }
 
 __device__ __forceinline__ void flag_error(int* status, int bits) {
@@ -60,6 +67,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Ends an mbarrier's life so that its shared memory can hold other data.
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void fence_barrier_init() {
@@ -156,6 +168,13 @@ __device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gsrc, 
           "r"(smem_u32(smem_dst)),
       "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+// Bring bytes of global memory into L2 ahead of a later read (no data reaches the
+// SM; L2 is the point of coherence, so a write that lands later is what that read
+// sees).  Address 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
 }
 
 // Order this thread's earlier generic-proxy shared-memory accesses before its

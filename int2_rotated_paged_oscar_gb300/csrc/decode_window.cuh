@@ -31,7 +31,9 @@ __device__ __forceinline__ bool seq_len_ok(const DecodeArgs& a, int n) {
 // product, and a 31-shuffle reduction leaves the score of slot l in lane l
 // (lanes 16..31 hold copies and are masked out).  Output: one partial (m, l, acc) per (query head, chunk) in the plain
 // basis.
-template <int D, int TH, typename Sync>
+// Q_INPUT: q is read from the call's input (the one-launch decode, which has no
+// q_rotate kernel) instead of the workspace copy q_rotate wrote.
+template <int D, int TH, bool Q_INPUT = false, typename Sync>
 __device__ void window_chunk(const DecodeArgs& a, int b, int kvh, int chunk, uint8_t* smem, int tid, Sync sync) {
   constexpr int C = D / 32;
   const Geom& g = a.g;
@@ -53,7 +55,9 @@ __device__ void window_chunk(const DecodeArgs& a, int b, int kvh, int chunk, uin
     reinterpret_cast<uint4*>(vs)[i] = reinterpret_cast<const uint4*>(vwin)[i];
   }
   WsView ws = ws_view(a);
-  for (int i = tid; i < gq * D; i += TH) qsm[i] = ws.qplain[((size_t)b * g.Hq + (size_t)kvh * gq) * D + i];
+  for (int i = tid; i < gq * D; i += TH)
+    qsm[i] = Q_INPUT ? load_q(a, ((size_t)b * g.Hq + (size_t)kvh * gq) * D + i)
+                     : ws.qplain[((size_t)b * g.Hq + (size_t)kvh * gq) * D + i];
   sync();
   const int n_recent = n > g.S ? min(n - g.S, g.W) : 0;
   const int slot = t0 + lane;

@@ -60,7 +60,250 @@ constexpr int kWarps = kThreads / 32;
 template <int D>
 __global__ void __launch_bounds__(kThreads) q_rotate_kernel(DecodeArgs a) {
   __shared__ __align__(16) float sm[kQRotSmemFloats<D>()];
-  q_rotate_cta<D>(a, blockIdx.x % (D / 32), blockIdx.x / (D / 32), blockIdx.y, sm);
+  q_rotate_cta<D>(a, blockIdx.x % (D / 32), blockIdx.x / (D / 32), blockIdx.y, sm,
+                  q_out_ws(a, blockIdx.x / (D / 32), blockIdx.y));
+}
+
+// ------------------------------------------------------------------ in-CTA query side
+// One-launch decode: every INT2 split CTA of a (request, kv head) forms that
+// pair's query side itself, after the wait on the preceding grid, with the
+// definitions q_rotate_cta uses (q' = q R_K for the gq query heads, the group
+// sums Q_g, 2^-e_h from ||q_h||_2 and the MMA fragments).  Thread (c4, part)
+// accumulates channels 4 c4 .. 4 c4 + 3 of q' over rows [part RPP, part RPP + RPP)
+// of R_K (16-byte loads, eight in flight); the parts are added in a fixed order.
+// scr: kQSideSmemFloats<D>() floats of shared memory; qf: fragments [NT][D/16][32]
+// (columns of absent heads zero); qaux: [gq][8] as in the workspace.  Ends with
+// a barrier after which every thread's shared-memory accesses are ordered
+// before later bulk copies into scr.
+template <int D>
+__host__ __device__ constexpr int kQSideParts() { return kThreads / (D / 4); }
+template <int D>
+__host__ __device__ constexpr int kQSideSmemFloats() { return 8 * D + kQSideParts<D>() * 8 * D + 8; }
+
+template <int D, int NT>
+__device__ __forceinline__ void q_side_cta(const DecodeArgs& a, int kvh, int b, float* scr, uint2* qf, float* qaux) {
+  constexpr int C4 = D / 4, PARTS = kQSideParts<D>(), RPP = D / PARTS;
+  constexpr int GROUPS = D / 32;
+  float (*qs)[D] = reinterpret_cast<float (*)[D]>(scr);                  // [8][D]: q
+  float (*red)[8][D] = reinterpret_cast<float (*)[8][D]>(scr + 8 * D);   // [PARTS][8][D]; red[0] ends as q'
+  float* nrm = scr + 8 * D + PARTS * 8 * D;                              // [8]
+  const Geom& g = a.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = g.gq();
+  const size_t qbase = ((size_t)b * g.Hq + (size_t)kvh * gq) * D;
+  for (int i = tid; i < gq * D; i += kThreads) qs[i / D][i % D] = load_q(a, qbase + i);
+  for (int i = tid; i < NT * (D / 16) * 32; i += kThreads) qf[i] = make_uint2(0u, 0u);
+  __syncthreads();
+  for (int hh = warp; hh < gq; hh += kWarps) {
+    float ss = 0.f;
+    for (int i = lane; i < D; i += 32) ss = fmaf(qs[hh][i], qs[hh][i], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) nrm[hh] = sqrtf(ss);
+  }
+  {
+    const int c4 = tid % C4, part = tid / C4;
+    const float4* Rg = reinterpret_cast<const float4*>(a.R_K + (size_t)kvh * g.rot_stride()) + c4;
+    float acc[8][4];
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[hh][c] = 0.f;
+#pragma unroll 4
+    for (int r = 0; r < RPP; ++r) {
+      const int i = part * RPP + r;
+      const float4 R4 = __ldg(Rg + (size_t)i * C4);
+#pragma unroll
+      for (int hh = 0; hh < 8; ++hh) {
+        if (hh < gq) {
+          const float x = qs[hh][i];
+          acc[hh][0] = fmaf(x, R4.x, acc[hh][0]);
+          acc[hh][1] = fmaf(x, R4.y, acc[hh][1]);
+          acc[hh][2] = fmaf(x, R4.z, acc[hh][2]);
+          acc[hh][3] = fmaf(x, R4.w, acc[hh][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh)
+      if (hh < gq)
+        *reinterpret_cast<float4*>(&red[part][hh][4 * c4]) = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+  }
+  __syncthreads();
+  for (int idx = tid; idx < gq * D; idx += kThreads) {
+    const int hh = idx / D, j = idx % D;
+    float y = red[0][hh][j];
+#pragma unroll
+    for (int p = 1; p < PARTS; ++p) y += red[p][hh][j];
+    red[0][hh][j] = y;
+  }
+  __syncthreads();
+  float (*qr)[D] = red[0];
+  for (int pr = warp; pr < gq * GROUPS; pr += kWarps) {   // Q_g: warp per (head, group)
+    const int hh = pr / GROUPS, grp = pr % GROUPS;
+    float gs = qr[hh][32 * grp + lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+    if (lane == 0) qaux[hh * 8 + 1 + grp] = gs;
+  }
+  for (int idx = tid; idx < gq * GROUPS * 16; idx += kThreads) {
+    const int hh = idx / (GROUPS * 16), grp = (idx >> 4) % GROUPS, sub = idx & 15;
+    const int e = q_head_exp(nrm[hh]);
+    if (grp == 0 && sub == 0) qaux[hh * 8] = ldexpf(1.f, -e);
+    q_frag_entry<D>(qr[hh] + 32 * grp, hh, grp, sub, e, gq, qf);
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ in-kernel combine
+// One-launch decode: each CTA of a (request, kv head) takes a ticket after its
+// partials are stored (a device-scope fence by every thread, then one atomic);
+// the CTA that draws the last ticket of the pair merges the pair's partials for
+// its gq query heads and writes their outputs, so no CTA ever waits on another.
+// That CTA puts the counter back to zero for the next launch (stream order: the
+// next launch takes tickets only after its wait on this grid).
+//   1. R_V (this kv head's) is copied into shared memory by one bulk copy;
+//   2. warp per head: the reference M over the pair's partials, then lane c4
+//      merges channels 4 c4 .. 4 c4 + 3 of every partial (eight partials' loads
+//      in flight, L2 loads: the partials were written by other CTAs): window
+//      partials into the plain sum, INT2 partials into the rotated sum, and l;
+//   3. thread per output channel j (and k half when D = 64): sum_k rot_k R_V[j][k]
+//      for every head from float4 rows, each thread starting at its own k so that
+//      a phase of 8 threads reads 8 different bank groups; o = (plain + that) / l.
+// Shared memory (from offset 0): R_V [D][D], rot [8][D], plain [8][D], l [8], and
+// for D = 64 the second k half's sums [8][D].
+template <int D>
+__host__ __device__ constexpr int kMergeSmemBytes() {
+  return (D * D + 16 * D + 8 + (kThreads / D > 1 ? 8 * D : 0)) * 4;
+}
+
+template <int D>
+__device__ __noinline__ void fused_merge(const DecodeArgs& a, int b, int kvh, uint8_t* smem, uint64_t* bar) {
+  constexpr int LPC = D / 4 < 32 ? D / 4 : 32;   // lanes per partial row (float4 each)
+  constexpr int SPW = 32 / LPC;                  // partials a warp reads side by side
+  constexpr int NPK = kThreads / D;              // k parts per output channel
+  const Geom& g = a.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = g.gq();
+  const int wc = a.wl.win_chunks;
+  const int stride = wc + a.wl.max_splits;
+  const int n = a.seq_lens[b];
+  const int nsp = seq_len_ok(a, n) ? min(splits_for(a, n), kMaxSplits) : 0;
+  const int nslot = wc + nsp;
+  float* Rs = reinterpret_cast<float*>(smem);
+  float* rot = Rs + D * D;
+  float* plain = rot + 8 * D;
+  float* Ls = plain + 8 * D;
+  float* xr = Ls + 8;
+  fence_proxy_async_smem();   // this thread's earlier shared-memory use, before the bulk copy
+  __syncthreads();
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(bar, D * D * sizeof(float));
+    bulk_g2s(Rs, a.R_V + (size_t)kvh * g.rot_stride(), D * D * sizeof(float), bar);
+  }
+  __syncthreads();   // the barrier is initialised before any thread waits on it
+  const WsView ws = ws_view(a);
+  const int c4 = lane % LPC, sub = lane / LPC;
+  for (int hh = warp; hh < gq; hh += kWarps) {
+    const float* base = ws.part + ((size_t)b * g.Hq + (size_t)kvh * gq + hh) * stride * (D + 4);
+    float M = -INFINITY;
+    for (int i = lane; i < nslot; i += 32) M = fmaxf(M, __ldcg(base + (size_t)i * (D + 4)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float4 pl = make_float4(0.f, 0.f, 0.f, 0.f), rr = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    for (int i0 = sub; i0 < nslot; i0 += 8 * SPW) {
+      float2 ml[8];
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * SPW;
+        if (i < nslot) {
+          ml[u] = __ldcg(reinterpret_cast<const float2*>(base + (size_t)i * (D + 4)));
+          v[u] = __ldcg(reinterpret_cast<const float4*>(base + (size_t)i * (D + 4) + 4) + c4);
+        } else {
+          ml[u] = make_float2(-INFINITY, 0.f);
+          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * SPW;
+        const float w = ml[u].x == -INFINITY ? 0.f : ex2(ml[u].x - M);
+        L = fmaf(w, ml[u].y, L);
+        if (i < wc) {
+          pl.x = fmaf(w, v[u].x, pl.x); pl.y = fmaf(w, v[u].y, pl.y);
+          pl.z = fmaf(w, v[u].z, pl.z); pl.w = fmaf(w, v[u].w, pl.w);
+        } else {
+          rr.x = fmaf(w, v[u].x, rr.x); rr.y = fmaf(w, v[u].y, rr.y);
+          rr.z = fmaf(w, v[u].z, rr.z); rr.w = fmaf(w, v[u].w, rr.w);
+        }
+      }
+    }
+    if constexpr (SPW == 2) {   // the two halves of the warp took alternate partials
+      pl.x += __shfl_xor_sync(0xffffffffu, pl.x, 16); pl.y += __shfl_xor_sync(0xffffffffu, pl.y, 16);
+      pl.z += __shfl_xor_sync(0xffffffffu, pl.z, 16); pl.w += __shfl_xor_sync(0xffffffffu, pl.w, 16);
+      rr.x += __shfl_xor_sync(0xffffffffu, rr.x, 16); rr.y += __shfl_xor_sync(0xffffffffu, rr.y, 16);
+      rr.z += __shfl_xor_sync(0xffffffffu, rr.z, 16); rr.w += __shfl_xor_sync(0xffffffffu, rr.w, 16);
+      L += __shfl_xor_sync(0xffffffffu, L, 16);
+    }
+    if (sub == 0) {
+      *reinterpret_cast<float4*>(rot + hh * D + 4 * c4) = rr;
+      *reinterpret_cast<float4*>(plain + hh * D + 4 * c4) = pl;
+    }
+    if (lane == 0) Ls[hh] = L;
+  }
+  const bool ok = mbar_wait_bounded(bar, 0, a.status);
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) (void)mbar_wait_bounded(bar, 0, nullptr);   // drain the copy before exiting
+    return;
+  }
+  constexpr int M4 = (D / 4) / NPK;   // float4 per k part
+  const int j = tid % D, kp = tid / D;
+  const float4* Rrow = reinterpret_cast<const float4*>(Rs + j * D);
+  float acc[8];
+#pragma unroll
+  for (int hh = 0; hh < 8; ++hh) acc[hh] = 0.f;
+#pragma unroll 4
+  for (int mm = 0; mm < M4; ++mm) {
+    const int k4 = kp * M4 + (mm + j) % M4;
+    const float4 r = Rrow[k4];
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh) {
+      if (hh < gq) {
+        const float4 x = reinterpret_cast<const float4*>(rot + hh * D)[k4];
+        acc[hh] = fmaf(x.x, r.x, fmaf(x.y, r.y, fmaf(x.z, r.z, fmaf(x.w, r.w, acc[hh]))));
+      }
+    }
+  }
+  if constexpr (NPK > 1) {
+    if (kp == 1)
+#pragma unroll
+      for (int hh = 0; hh < 8; ++hh)
+        if (hh < gq) xr[hh * D + j] = acc[hh];
+    __syncthreads();
+  }
+  if (kp == 0) {
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh) {
+      if (hh < gq) {
+        float t = acc[hh];
+        if constexpr (NPK > 1) t += xr[hh * D + j];
+        const float L = Ls[hh];
+        const float o = (plain[hh * D + j] + t) * (L > 0.f ? 1.f / L : 0.f);
+        const size_t oi = ((size_t)b * g.Hq + (size_t)kvh * gq + hh) * D + j;
+        if (a.out_dtype == kDtypeBF16) {
+          __nv_bfloat16 hb = __float2bfloat16_rn(o);
+          static_cast<uint16_t*>(a.out)[oi] = *reinterpret_cast<uint16_t*>(&hb);
+        } else {
+          static_cast<float*>(a.out)[oi] = o;
+        }
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------------ INT2 split
@@ -82,7 +325,49 @@ struct Int2Layout {
   static constexpr int PIDS = RING + kWarps * WS * (8 + 4);                       // per-warp page ids [kWarps][32]
   static constexpr int QOFF = (PIDS + kWarps * 32 * 4 + 15) / 16 * 16;  // after mbarriers, page-valid flags, page ids
   static constexpr int SMEM = QOFF + (NT == 1 ? KT * 32 * 8 : 0);  // + the NT = 1 query fragments
+  // one-launch decode: the CTA's own query side (fragments [NT][KT][32], 2^-e and Q_g per
+  // head); the query side's scratch over the ring stages 1.. (empty until the query side is
+  // done: the staggered fill requests them afterwards) when they are large enough, else after
+  // the rest; at the end, in the CTA that merges, the merge's arrays from offset 0.
+  static constexpr int QF = (SMEM + 15) / 16 * 16;
+  static constexpr int QAUX = QF + NT * KT * 32 * 8;
+  static constexpr int QR_BYTES = kQSideSmemFloats<D>() * 4;
+  static constexpr bool QR_ALIAS = (WS - 1) * kWarps * BLOCK >= QR_BYTES;
+  static constexpr int QR = QR_ALIAS ? kWarps * BLOCK : (QAUX + 8 * 8 * 4 + 15) / 16 * 16;
+  static constexpr int FUSED_END = QR_ALIAS ? QAUX + 8 * 8 * 4 : QR + QR_BYTES;
+  static constexpr int MERGE_END = kMergeSmemBytes<D>();
+  static constexpr int SMEM_FUSED = FUSED_END > MERGE_END ? FUSED_END : MERGE_END;
 };
+
+// Speculative L2 prefetch before a one-launch decode's dependency wait (lane 0 of
+// warp `warp`): an INT2 split CTA's warp prefetches its first page block, a window
+// CTA's warp 0 (1) the chunk's K (V) rows.  Every index is checked against its
+// buffer, so values the preceding grid has not finished writing give at worst a
+// useless prefetch.
+template <int P, int BLOCK>
+__device__ __forceinline__ void prefetch_first_reads(const DecodeArgs& a, int b, int kvh, int warp) {
+  const Geom& g = a.g;
+  const int x = blockIdx.x;
+  if (x < a.wl.win_chunks) {
+    if (warp > 1) return;
+    const int req = a.req_slot[b];
+    const int t0 = x * kWinChunk;
+    const int cnt = min(kWinChunk, g.window() - t0);
+    if (req < 0 || req >= g.max_req || cnt <= 0) return;
+    const size_t sbase = ((size_t)a.layer * g.max_req + req) * g.slab_req_elems();
+    bulk_prefetch_l2(a.slab + sbase + ((size_t)kvh * 2 + warp) * g.window() * g.D + (size_t)t0 * g.D,
+                     (uint32_t)(cnt * g.D * 2));
+    return;
+  }
+  const int n = a.seq_lens[b];
+  const int h_end = n - g.W;
+  if (n < 0 || n > a.max_seq || h_end <= g.S) return;
+  const int lp = (x - a.wl.win_chunks) * a.wl.pages_per_split + warp;
+  if (lp > (h_end - 1) / P || lp >= a.bt_stride || lp >= g.max_pages_per_req) return;
+  const int pid = a.block_table[(size_t)b * a.bt_stride + lp];
+  if (pid < 0 || pid >= g.num_pages) return;
+  bulk_prefetch_l2(a.pool + (size_t)a.layer * g.layer_pool_bytes() + ((size_t)pid * g.Hkv + kvh) * BLOCK, BLOCK);
+}
 
 // One INT2 split: pages [pg0, pg1) of one (request, kv head).  Warp w owns pages
 // pg0 + w + 4i and streams them through its own ring of WS page blocks (bulk
@@ -113,7 +398,9 @@ struct Int2Layout {
 // when a block maximum exceeds mm + 8 + j, so weights 2^(s - mm) stay below
 // 2^14 (f16) and rescaling is rare; the reference check is one warp vote.
 // Returns false if a page copy timed out (the CTA then writes no partial).
-template <int D, int NT, int P>
+// FUSED: the one-launch decode (the CTA forms its query side itself, window CTAs
+// read q from the call's input; see q_side_cta and fused_merge).
+template <int D, int NT, int P, bool FUSED>
 __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) {
   using Lay = Int2Layout<D, NT, P>;
   constexpr int WS = Lay::WS;
@@ -126,6 +413,15 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int gq = g.gq();
+  if (!a.pages_before_wait) {
+    // The preceding grid is the caller's and may write anything this CTA reads
+    // (lengths, block table, slots, pages).  Before waiting on it, lane 0 of each
+    // warp brings the data it will most likely read first into L2, from the view
+    // of those tables it has now: a stale view costs a useless prefetch, never a
+    // wrong result (every read that counts comes after the wait).
+    if (lane == 0) prefetch_first_reads<P, Int2Layout<D, NT, P>::BLOCK>(a, b, kvh, warp);
+    pdl_wait();
+  }
   const int n = a.seq_lens[b];
   if (!seq_len_ok(a, n)) {
     if (tid == 0 && blockIdx.x == 0) flag_error(a.status, kDevBadLen);
@@ -140,7 +436,7 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
       return true;
     }
     pdl_wait();
-    window_chunk<D, kThreads>(a, b, kvh, blockIdx.x, smem, tid, [] { __syncthreads(); });
+    window_chunk<D, kThreads, FUSED>(a, b, kvh, blockIdx.x, smem, tid, [] { __syncthreads(); });
     pdl_launch_dependents();
     return true;
   }
@@ -155,7 +451,8 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
 
   const int* bt = a.block_table + (size_t)b * a.bt_stride;
   const uint8_t* pool_l = a.pool + (size_t)a.layer * g.layer_pool_bytes();
-  uint8_t* ring = smem + warp * WS * Lay::BLOCK;
+  // ring stage s of this warp (stage-major: every warp's stage 0, then every warp's stage 1, ...)
+  auto stage_buf = [&](int s) { return smem + (s * kWarps + warp) * Lay::BLOCK; };
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::RING) + warp * WS;
   int* stage_ok = reinterpret_cast<int*>(smem + Lay::RING + kWarps * WS * 8) + warp * WS;
 
@@ -181,43 +478,55 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     if (!okp) flag_error(a.status, kDevBadPage);
     mbar_arrive_expect_tx(&bars[s], okp ? (uint32_t)Lay::BLOCK : 0u);
     if (okp)
-      bulk_g2s_hint(ring + s * Lay::BLOCK, pool_l + ((size_t)pid * g.Hkv + kvh) * Lay::BLOCK, Lay::BLOCK, &bars[s],
+      bulk_g2s_hint(stage_buf(s), pool_l + ((size_t)pid * g.Hkv + kvh) * Lay::BLOCK, Lay::BLOCK, &bars[s],
                     stream_policy);
   };
+
   // The warp's first page is requested before the wait on the preceding grid, so
   // the page stream overlaps it; the rest of the ring is requested after that wait
   // and the query-side set-up (staggered fill: when every warp of the grid requests
   // its whole ring at once, each warp's first page lands only near the end of the
   // burst, while first pages requested first arrive first).  In a fused step the preceding
   // grid (the append) may still be writing the last history page: if that is the
-  // first page, it is requested after the wait.
+  // first page, it is requested after the wait.  Behind a grid that is not this chain's
+  // (pages_before_wait = 0) the CTA has waited already (see the top).
   auto is_tail = [&](int i) { return a.defer_tail_page && pg0 + warp + kWarps * i == n_hist_pages - 1; };
   int n_issued = 0;  // pages requested so far (lane 0)
   if (lane == 0 && n_mine > 0 && !is_tail(0)) {
+    if (a.pages_before_wait) {
+      issue(0);
+      n_issued = 1;
+    }
+  }
+
+  // ---------------- query side (written by q_rotate, or formed here): wait for the previous grid
+  pdl_wait();
+  if (lane == 0 && n_mine > 0 && n_issued == 0) {
     issue(0);
     n_issued = 1;
   }
-
-  // ---------------- query side (written by q_rotate): wait for the previous grid
-  pdl_wait();
   WsView ws = ws_view(a);
+  uint2* qf_s = reinterpret_cast<uint2*>(smem + Lay::QF);     // one-launch decode: [NT][KT][32]
+  float* qaux_s = reinterpret_cast<float*>(smem + Lay::QAUX);  // one-launch decode: [gq][8]
+  if constexpr (FUSED) q_side_cta<D, NT>(a, kvh, b, reinterpret_cast<float*>(smem + Lay::QR), qf_s, qaux_s);
   // The query-side B fragments are the same for every warp of the CTA.  With up to
   // four query heads (NT = 1) they are staged once in shared memory (one LDS.64 per
   // MMA): the registers they free buy the 128-register kernel scheduling room.  With
   // eight heads (NT = 2) the kernel runs at three CTAs per SM with registers to
   // spare, and register operands avoid the extra loads.
-  uint2* qsm = reinterpret_cast<uint2*>(smem + Lay::QOFF);   // [NT][KT][32 lanes]
+  uint2* qsm = reinterpret_cast<uint2*>(smem + (FUSED ? Lay::QF : Lay::QOFF));   // [NT][KT][32 lanes]
   uint32_t qb[G8 ? NT : 1][G8 ? Lay::KT : 1][2];
   if constexpr (G8) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int kk = 0; kk < Lay::KT; ++kk) {
-        const uint2 f = ws.qfrag[((((size_t)b * g.Hkv + kvh) * NT + nt) * Lay::KT + kk) * 32 + lane];
+        const uint2 f = FUSED ? qf_s[(nt * Lay::KT + kk) * 32 + lane]
+                              : ws.qfrag[((((size_t)b * g.Hkv + kvh) * NT + nt) * Lay::KT + kk) * 32 + lane];
         qb[nt][kk][0] = f.x;
         qb[nt][kk][1] = f.y;
       }
-  } else {
+  } else if constexpr (!FUSED) {   // (the one-launch query side is in qsm already, absent heads zero)
     for (int i = tid; i < NT * Lay::KT * 32; i += kThreads) {
       const int nt = i / (Lay::KT * 32), rem = i % (Lay::KT * 32);
       const int kk = rem >> 5, ln = rem & 31;
@@ -227,7 +536,7 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     }
     __syncthreads();
   }
-  const float* aux_base = ws.qaux + ((size_t)b * g.Hq + (size_t)kvh * gq) * 8;
+  const float* aux_base = FUSED ? qaux_s : ws.qaux + ((size_t)b * g.Hq + (size_t)kvh * gq) * 8;
   const float sm_log2 = kLog2e * rsqrtf((float)D);
   float F[NH];  // score = accumulator * F (log2 domain)
 #pragma unroll
@@ -258,10 +567,6 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     qz2[nt] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&vb2)) << 16;
   }
 
-  if (lane == 0 && n_mine > 0 && n_issued == 0) {
-    issue(0);
-    n_issued = 1;
-  }
   // the rest of the ring, a query-side set-up later than the first pages of the grid
   if (lane == 0)
     for (; n_issued < WS && n_issued < n_mine; ++n_issued) issue(n_issued);
@@ -629,7 +934,7 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
     }
 
     if (stage_ok[s]) {
-      const uint8_t* buf = ring + s * Lay::BLOCK;
+      const uint8_t* buf = stage_buf(s);
       const int tp = (pg0 + warp + kWarps * i) * P;  // first token of the page
       if (tp >= g.S && tp + P <= h_end) {  // every token of the page is history: no checks
         if constexpr (P == 64) {
@@ -657,6 +962,10 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
   if (aborted && lane == 0) {
     // drain this warp's copies still in flight before the CTA exits, again bounded
     for (int i = i_fail; i < n_issued; ++i) (void)mbar_wait_bounded(&bars[i % WS], (i / WS) & 1, nullptr);
+  }
+  if constexpr (FUSED) {   // the merge may reuse the barriers' shared memory
+    if (lane == 0)
+      for (int st = 0; st < WS; ++st) mbar_inval(&bars[st]);
   }
   pdl_launch_dependents();
   if (__syncthreads_or(aborted)) return false;
@@ -739,10 +1048,28 @@ __device__ __forceinline__ bool splitk_work(const DecodeArgs& a, uint8_t* smem) 
   return true;
 }
 
-template <int D, int NT, int P>
+template <int D, int NT, int P, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 3) decode_splitk_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  (void)splitk_work<D, NT, P>(a, smem);
+  (void)splitk_work<D, NT, P, FUSED>(a, smem);
+  if constexpr (FUSED) {
+    __shared__ int s_last;
+    __shared__ __align__(8) uint64_t mbar;
+    pdl_wait();          // (every path has waited already but the early exits) tickets follow the previous grid
+    __threadfence();     // this thread's partial stores, device-wide, before the ticket
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int* ctr = a.tickets + (size_t)blockIdx.z * a.g.Hkv + blockIdx.y;
+      const bool last = atomicAdd(ctr, 1) == (int)gridDim.x - 1;
+      if (last) {
+        *ctr = 0;          // every CTA of the pair has its ticket: ready for the next launch
+        __threadfence();   // the other CTAs' partials, seen through their tickets
+      }
+      s_last = last ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_last) fused_merge<D>(a, blockIdx.z, blockIdx.y, smem, &mbar);
+  }
 }
 
 // ------------------------------------------------------------------ combine
@@ -1037,17 +1364,19 @@ __global__ void __launch_bounds__(kHeadThreads) decode_combine_head_kernel(Decod
   }
 }
 
-template <int D, int NT, int P>
+template <int D, int NT, int P, bool FUSED>
 int launch_splitk_t(const DecodeArgs& a, cudaStream_t s, bool pdl) {
   using Lay = Int2Layout<D, NT, P>;
-  size_t smem = Lay::SMEM;
+  size_t smem = FUSED ? Lay::SMEM_FUSED : Lay::SMEM;
   const size_t win_smem = 2 * kWinChunk * D * sizeof(uint16_t) + 8 * D * sizeof(float);
   const size_t merge_smem = (64 + kWarps * 8 * D + 8 * (kWarps + 2)) * sizeof(float);
   if (win_smem > smem) smem = win_smem;
   if (merge_smem > smem) smem = merge_smem;
   smem = (smem + 127) & ~size_t(127);
-  auto kern = decode_splitk_kernel<D, NT, P>;
-  cudaError_t e = ensure_smem_limit(kern, smem);
+  // three CTAs per SM (the plan sizes one wave as 3 x 152 CTAs)
+  static_assert(3 * (Lay::SMEM_FUSED + 128 + 1024) <= 228 * 1024, "three CTAs per SM");
+  auto kern = decode_splitk_kernel<D, NT, P, FUSED>;
+  cudaError_t e = ensure_smem_limit(kern, smem, true);
   if (e != cudaSuccess) return (int)e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.wl.win_chunks + a.wl.max_splits, a.g.Hkv, a.batch);
@@ -1063,13 +1392,18 @@ int launch_splitk_t(const DecodeArgs& a, cudaStream_t s, bool pdl) {
   return (int)e;
 }
 
+template <int D, int NT, bool FUSED>
+int launch_splitk_f(const DecodeArgs& a, cudaStream_t s, bool pdl) {
+  switch (a.g.P) {
+    case 16: return launch_splitk_t<D, NT, 16, FUSED>(a, s, pdl);
+    case 32: return launch_splitk_t<D, NT, 32, FUSED>(a, s, pdl);
+    default: return launch_splitk_t<D, NT, 64, FUSED>(a, s, pdl);
+  }
+}
+
 template <int D, int NT>
 int launch_splitk_p(const DecodeArgs& a, cudaStream_t s, bool pdl) {
-  switch (a.g.P) {
-    case 16: return launch_splitk_t<D, NT, 16>(a, s, pdl);
-    case 32: return launch_splitk_t<D, NT, 32>(a, s, pdl);
-    default: return launch_splitk_t<D, NT, 64>(a, s, pdl);
-  }
+  return a.wl.fused ? launch_splitk_f<D, NT, true>(a, s, pdl) : launch_splitk_f<D, NT, false>(a, s, pdl);
 }
 
 template <int D>

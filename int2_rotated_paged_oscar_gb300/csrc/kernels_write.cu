@@ -591,7 +591,8 @@ __global__ void __launch_bounds__(128) append_kernel(WriteArgs a) {
 }
 
 // The first kernel of a fused decode step: CTAs [0, nq) rotate the query
-// (q_rotate_cta, nq = Hkv * D/32 * batch), the rest run the append, one grid
+// (q_rotate_cta, nq = Hkv * D/32 * batch; none when the decode is one launch,
+// whose split CTAs form the query side), the rest run the append, one grid
 // instead of two so that no second launch sits on the step's critical path.
 // Every CTA waits on the preceding grid before it reads anything that grid may
 // write; the split-K kernel, its programmatic dependent, waits for the whole grid.
@@ -601,9 +602,10 @@ __global__ void __launch_bounds__(128) step_prep_kernel(const __grid_constant__ 
   extern __shared__ __align__(16) float Rsm[];  // [D][D] (append) or the rotation's arrays
   __shared__ __align__(8) uint64_t bar;
   const int qx = d.g.Hkv * (D / 32);
-  const int nq = qx * d.batch;
+  const int nq = d.wl.fused ? 0 : qx * d.batch;
   if ((int)blockIdx.x < nq) {
-    q_rotate_cta<D>(d, blockIdx.x % (D / 32), (blockIdx.x % qx) / (D / 32), blockIdx.x / qx, Rsm);
+    q_rotate_cta<D>(d, blockIdx.x % (D / 32), (blockIdx.x % qx) / (D / 32), blockIdx.x / qx, Rsm,
+                    q_out_ws(d, (blockIdx.x % qx) / (D / 32), blockIdx.x / qx));
     return;
   }
   const int i = blockIdx.x - nq;
@@ -648,7 +650,7 @@ int launch_step_prep(const WriteArgs& w, const DecodeArgs& d, void* stream, bool
   if (w.batch == 0) return 0;
   const int nz = (w.g.Hkv + append_heads_per_cta(w.g) - 1) / append_heads_per_cta(w.g);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(d.g.Hkv * (d.g.D / 32) * d.batch + w.batch * 2 * nz);
+  cfg.gridDim = dim3((d.wl.fused ? 0 : d.g.Hkv * (d.g.D / 32) * d.batch) + w.batch * 2 * nz);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = sizeof(float) * w.g.D * w.g.D;   // holds the rotation's arrays as well
   cfg.stream = s;

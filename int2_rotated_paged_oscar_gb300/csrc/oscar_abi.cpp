@@ -57,6 +57,7 @@ struct oscar_ctx {
   uint8_t* pool = nullptr;
   uint16_t* slab = nullptr;
   int* d_status = nullptr;
+  int* d_tickets = nullptr;  // one-launch decode counters [max_requests][n_kv_heads], zero between launches
   std::mutex mu;
   std::vector<int32_t> refcount;
   std::vector<int32_t> free_stack;  // top = back
@@ -69,6 +70,7 @@ struct oscar_ctx {
   // per layer: operand exponents of the history's scales and zeros in the
   // decode MMAs (kNoOperandExp until a clip threshold is known for the layer)
   std::vector<int> opexp_K, opexp_V;
+  int decode_form = OSCAR_DECODE_AUTO;
 };
 
 namespace {
@@ -187,6 +189,13 @@ int operand_exponent_for_clip(float clip) {
   return (k < 0 || k > 100) ? kNoOperandExp : k;
 }
 
+// Largest batch x n_q_heads that OSCAR_DECODE_AUTO decodes in one launch (query side and
+// merge inside the split kernel); 0: the automatic form is always three kernels.
+#ifndef OSCAR_FUSED_ROWS_MAX
+#define OSCAR_FUSED_ROWS_MAX 0
+#endif
+constexpr long long kFusedRowsMax = OSCAR_FUSED_ROWS_MAX;
+
 DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   DecodeWs w{};
   const int gq = g.Hq / g.Hkv;
@@ -253,6 +262,9 @@ DecodeWs plan_decode(const Geom& g, int batch, int max_seq, bool bf16_pool) {
   // serves several; the partials are staged when the CTA still fits twice on
   // an SM.
   const long long rows = (long long)batch * g.Hq > 0 ? (long long)batch * g.Hq : 1;
+  // One launch per decode (the split CTAs form the query side themselves and the
+  // last CTA of each (request, kv head) merges its partials): see kFusedRowsMax.
+  w.fused = (!bf16_pool && batch <= g.max_req && rows <= kFusedRowsMax) ? 1 : 0;
   const size_t rv_bytes = (size_t)g.D * g.D * sizeof(float);
   const size_t per_head = slots * (g.D + 4) * sizeof(float);
   if (rows <= 152) {
@@ -318,6 +330,8 @@ oscar_status oscar_create(const oscar_config* cfg, void* int2_pool, void* window
     return fail(OSCAR_ERR_INVALID, "pass both device buffers or neither");
   if (int2_pool && (reinterpret_cast<uintptr_t>(int2_pool) & 15))
     return fail(OSCAR_ERR_INVALID, "int2_pool must be 16-byte aligned");
+  if (window_slab && (reinterpret_cast<uintptr_t>(window_slab) & 15))   // 16-byte row loads and bulk copies
+    return fail(OSCAR_ERR_INVALID, "window_slab must be 16-byte aligned");
   oscar_ctx* ctx = new (std::nothrow) oscar_ctx();
   if (!ctx) return fail(OSCAR_ERR_OOM, "host allocation failed");
   ctx->g = g;
@@ -330,12 +344,16 @@ oscar_status oscar_create(const oscar_config* cfg, void* int2_pool, void* window
   for (int i = g.num_pages - 1; i >= 0; --i) ctx->free_stack.push_back(i);  // lowest id first
   if (const char* f = std::getenv("OSCAR_FAULT_ALLOC_FAIL_AFTER")) ctx->alloc_fail_after = std::atoll(f);
   if (int2_pool) {
+    const size_t tickets = (size_t)g.max_req * g.Hkv * sizeof(int);
     cudaError_t e = cudaMalloc(&ctx->d_status, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(ctx->d_status, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_tickets, tickets);
+    if (e == cudaSuccess) e = cudaMemset(ctx->d_tickets, 0, tickets);
     if (e != cudaSuccess) {
       if (ctx->d_status) cudaFree(ctx->d_status);
+      if (ctx->d_tickets) cudaFree(ctx->d_tickets);
       delete ctx;
-      return cuda_fail(e, "status word");
+      return cuda_fail(e, "status word and decode counters");
     }
   }
   *out = ctx;
@@ -351,6 +369,7 @@ oscar_status oscar_destroy(oscar_ctx* ctx) {
     }
   for (auto e : ctx->event_pool) cudaEventDestroy(e);
   if (ctx->d_status) cudaFree(ctx->d_status);
+  if (ctx->d_tickets) cudaFree(ctx->d_tickets);
   delete ctx;
   return OSCAR_OK;
 }
@@ -727,7 +746,10 @@ static oscar_status prepare_decode_core(oscar_ctx* ctx, int32_t layer, const voi
   a.pool = ctx->pool;
   a.slab = ctx->slab;
   a.status = ctx->d_status;
+  a.tickets = ctx->d_tickets;
   a.wl = oscar::plan_decode(ctx->g, batch, max_seq, false);
+  if (ctx->decode_form == OSCAR_DECODE_THREE_KERNELS) a.wl.fused = 0;
+  if (ctx->decode_form == OSCAR_DECODE_ONE_LAUNCH) a.wl.fused = batch <= ctx->g.max_req ? 1 : 0;
   return OSCAR_OK;
 }
 
@@ -756,6 +778,22 @@ static oscar_status prepare_decode(oscar_ctx* ctx, int32_t layer, const void* q,
 static oscar_status launch_decode_chain(oscar_ctx* ctx, DecodeArgs& a, const WriteArgs* append, void* stream) {
   const bool pdl = !ctx->timing;  // timing events between launches would break the programmatic overlap
   a.defer_tail_page = append != nullptr;
+  // split-K copies its first pages before its dependency wait only behind a kernel of this
+  // chain (q_rotate or step_prep); a one-launch decode follows the caller's last kernel
+  a.pages_before_wait = (append != nullptr || !a.wl.fused) ? 1 : 0;
+  if (a.wl.fused) {  // one launch (after the append CTAs of a fused step)
+    if (append) {
+      LaunchScope ls(ctx, "step_prep", stream);
+      int e = oscar::launch_step_prep(*append, a, stream, pdl);
+      ls.done(e);
+      if (e) return cuda_fail(e, "step_prep launch");
+    }
+    LaunchScope ls(ctx, "decode_splitk", stream);
+    int e = oscar::launch_decode_splitk(a, stream, pdl);
+    ls.done(e);
+    if (e) return cuda_fail(e, "decode_splitk launch");
+    return OSCAR_OK;
+  }
   if (append) {
     LaunchScope ls(ctx, "step_prep", stream);
     int e = oscar::launch_step_prep(*append, a, stream, pdl);
@@ -1000,9 +1038,20 @@ oscar_status oscar_check_status(oscar_ctx* ctx, void* stream, int32_t* out_bits)
   if (out_bits) *out_bits = bits;
   if (bits) {
     cudaMemset(ctx->d_status, 0, sizeof(int));
+    // a launch that failed may have left the one-launch decode counters mid-count
+    cudaMemset(ctx->d_tickets, 0, (size_t)ctx->g.max_req * ctx->g.Hkv * sizeof(int));
     return fail(OSCAR_ERR_DEVICE, "device status 0x%x (%s%s%s)", bits, (bits & oscar::kDevBadPage) ? "bad page " : "",
                 (bits & oscar::kDevTimeout) ? "wait timeout " : "", (bits & oscar::kDevBadLen) ? "bad length " : "");
   }
+  return OSCAR_OK;
+}
+
+oscar_status oscar_set_decode_form(oscar_ctx* ctx, int32_t form) {
+  if (!ctx) return fail(OSCAR_ERR_INVALID, "context is null");
+  if (form != OSCAR_DECODE_AUTO && form != OSCAR_DECODE_THREE_KERNELS && form != OSCAR_DECODE_ONE_LAUNCH)
+    return fail(OSCAR_ERR_INVALID, "unknown decode form %d", form);
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  ctx->decode_form = form;
   return OSCAR_OK;
 }
 

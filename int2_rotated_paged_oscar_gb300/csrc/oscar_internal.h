@@ -83,6 +83,8 @@ struct DecodeWs {
   int combine_head;      // 1: one CTA per (query head, request) (small batches)
   int combine_part_smem; // 1: the combine CTA stages its split partials in shared memory
   size_t combine_smem;   // dynamic shared memory of the combine kernel
+  int fused;             // 1: one launch per decode (query side formed by the split CTAs, last CTA of a
+                         //    (request, kv head) merges); no q_rotate or combine kernel
 };
 
 struct DecodeArgs {
@@ -109,6 +111,9 @@ struct DecodeArgs {
   int k_exp_K, k_exp_V;      // operand exponents: K (V) scales and zeros enter the f16 MMAs times 2^k
   unsigned code_magic;       // kCodeMagic (f16 pair -1.0, -1.0), a launch argument so it lives in a register
   int defer_tail_page;       // 1: the preceding kernel may still write the last history page (fused step)
+  int* tickets;              // one-launch decode: [batch][Hkv] counters, zero between launches (context-owned)
+  int pages_before_wait;     // 1: the preceding grid is this chain's own (it waited on everything before it
+                             //    and writes no page but, in a fused step, the last history page)
 };
 
 // Extend (chunked prefill) attention over the mixed cache.

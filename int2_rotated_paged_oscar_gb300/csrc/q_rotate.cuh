@@ -28,6 +28,70 @@ __device__ __forceinline__ float load_q(const DecodeArgs& a, size_t idx) {
   return static_cast<const float*>(a.q)[idx];
 }
 
+// Destinations of one (request, kv head)'s query side: the query-side MMA fragments
+// [NT][D/16][32 lanes], per head 2^-e_h and the group sums Q_g [gq][8], and q as
+// float32 [gq][D] (may be null).  In the decode workspace (q_rotate kernel, step
+// prep) or in the shared memory of a CTA that rotates its own query.
+struct QOut {
+  uint2* qfrag;
+  float* qaux;
+  float* qplain;
+};
+
+__device__ __forceinline__ QOut q_out_ws(const DecodeArgs& a, int kvh, int b) {
+  WsView ws = ws_view(a);
+  const int gq = a.g.gq();
+  QOut o;
+  o.qfrag = ws.qfrag + (((size_t)b * a.g.Hkv + kvh) * a.wl.nt) * (a.g.D / 16) * 32;
+  o.qaux = ws.qaux + ((size_t)b * a.g.Hq + (size_t)kvh * gq) * 8;
+  o.qplain = ws.qplain + ((size_t)b * a.g.Hq + (size_t)kvh * gq) * a.g.D;
+  return o;
+}
+
+// ------------------------------------------------------------------ query-side fragments
+// Power-of-two exponent e of a head: |q'|_inf <= ||q||_2 = nrm (R_K is orthogonal), and
+// |q'| * 2^e < 32, so that q' * 2^e * 2^(10 - pos) <= 1024 x 32 stays below the f16 maximum.
+__device__ __forceinline__ int q_head_exp(float nrm) {
+  int e = 0;
+  if (nrm > 0.f) {
+    int E;
+    frexpf(nrm, &E);  // nrm * (1 + rounding) < 2^E
+    e = 5 - E;
+  }
+  return e;
+}
+
+// One entry of the query-side MMA fragments: head hh of the kv head's gq, channel
+// group grp (k-tiles 2 grp, 2 grp + 1), sub in [0, 16) = (k-tile, hi|lo half, tig).
+// qg: q'_hh over the group's 32 channels; e: the head's exponent.  Writes the
+// register pair of lane ln in k-tile kk of plane `plane` of qfrag [NT][D/16][32].
+template <int D>
+__device__ __forceinline__ void q_frag_entry(const float* qg, int hh, int grp, int sub, int e, int gq, uint2* qfrag) {
+  const int kt = sub >> 3, hl = (sub >> 2) & 1, tig = sub & 3;
+  const bool g8 = gq == 8;
+  const int gid = g8 ? hh : 2 * (hh & 3) + hl;
+  const int plane = g8 ? hl : 0;
+  const int ln = gid * 4 + tig;
+  const int kk = 2 * grp + kt;
+  const int p8 = 4 * grp + 2 * kt;
+  uint32_t regs[2];
+#pragma unroll
+  for (int hpair = 0; hpair < 2; ++hpair) {
+    const int ch = 16 * kt + 8 * hpair + 2 * tig;  // channel within the group
+    const int pos = slot_pos((p8 + hpair) & 7);
+    float v[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float x = ldexpf(qg[ch + u], e + 10 - pos);
+      const __half hi = __float2half_rn(x);
+      const float lo = x - __half2float(hi);
+      v[u] = hl ? lo : __half2float(hi);
+    }
+    regs[hpair] = pack_half2(v[0], v[1]);
+  }
+  qfrag[((size_t)plane * (D / 16) + kk) * 32 + ln] = make_uint2(regs[0], regs[1]);
+}
+
 // ------------------------------------------------------------------ q rotate
 // One CTA of 128 threads, (kv head kvh, channel group grp, request b): the 32
 // rotated channels of group grp, q'_j = sum_i q_i R_K[i][j] for j in
@@ -42,8 +106,11 @@ __device__ __forceinline__ float load_q(const DecodeArgs& a, size_t idx) {
 template <int D>
 __host__ __device__ constexpr int kQRotSmemFloats() { return D * 33 + 8 * D + 8 * 32 + 8; }
 
+// pdl: the CTA waits on the preceding grid (after issuing its R_K loads) and lets its
+// dependents launch; false when the caller has already waited.
 template <int D>
-__device__ __forceinline__ void q_rotate_cta(const DecodeArgs& a, int grp, int kvh, int b, float* sm) {
+__device__ __forceinline__ void q_rotate_cta(const DecodeArgs& a, int grp, int kvh, int b, float* sm, QOut out,
+                                             bool pdl = true) {
   constexpr int T = 128;
   float (*Rs)[33] = reinterpret_cast<float (*)[33]>(sm);          // [D][33]: R_K[:, 32 grp + c], padded
   float (*qs)[D] = reinterpret_cast<float (*)[D]>(sm + D * 33);   // [8][D]
@@ -52,7 +119,6 @@ __device__ __forceinline__ void q_rotate_cta(const DecodeArgs& a, int grp, int k
   const Geom& g = a.g;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int gq = g.gq();
-  WsView ws = ws_view(a);
   // R_K column slice: D rows x 32 floats (8 float4 per row), 16-byte loads, all in flight
   {
     const float4* Rg = reinterpret_cast<const float4*>(a.R_K + (size_t)kvh * g.rot_stride());  // this kv head's R_K
@@ -68,8 +134,10 @@ __device__ __forceinline__ void q_rotate_cta(const DecodeArgs& a, int grp, int k
       float* dst = &Rs[idx >> 3][(idx & 7) * 4];
       dst[0] = v[u].x; dst[1] = v[u].y; dst[2] = v[u].z; dst[3] = v[u].w;
     }
-    pdl_wait();
-    pdl_launch_dependents();
+    if (pdl) {
+      pdl_wait();
+      pdl_launch_dependents();
+    }
   }
   const size_t qbase = ((size_t)b * g.Hq + (size_t)kvh * gq) * D;
   {
@@ -85,7 +153,7 @@ __device__ __forceinline__ void q_rotate_cta(const DecodeArgs& a, int grp, int k
       const int i = t + u * T;
       if (i < gq * D) {
         qs[i / D][i % D] = qv[u];
-        if (grp == 0) ws.qplain[qbase + i] = qv[u];
+        if (grp == 0 && out.qplain) out.qplain[i] = qv[u];
       }
     }
   }
@@ -114,43 +182,14 @@ __device__ __forceinline__ void q_rotate_cta(const DecodeArgs& a, int grp, int k
     float gs = acc;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-    if (lane == 0) ws.qaux[((size_t)b * g.Hq + (size_t)kvh * gq + hh) * 8 + 1 + grp] = gs;
+    if (lane == 0) out.qaux[hh * 8 + 1 + grp] = gs;
   }
   __syncthreads();
   // fragments of the two k-tiles of this group: 8 lanes x 2 k-tiles per head
   for (int idx = t; idx < gq * 16; idx += T) {
     const int hh = idx >> 4, sub = idx & 15;
-    const int kt = sub >> 3, hl = (sub >> 2) & 1, tig = sub & 3;
-    int e = 0;
-    const float mx = nrm[hh];
-    if (mx > 0.f) {
-      int E;
-      frexpf(mx, &E);  // |q'|_inf <= ||q||_2 = mx * (1 + rounding) < 2^E
-      e = 5 - E;       // |q'| * 2^e < 32: times 2^(10-pos) <= 1024 stays below the f16 maximum
-    }
-    if (grp == 0 && sub == 0) ws.qaux[((size_t)b * g.Hq + (size_t)kvh * gq + hh) * 8] = ldexpf(1.f, -e);
-    const bool g8 = gq == 8;
-    const int gid = g8 ? hh : 2 * (hh & 3) + hl;
-    const int plane = g8 ? hl : 0;
-    const int ln = gid * 4 + tig;
-    const int kk = 2 * grp + kt;
-    const int p8 = 4 * grp + 2 * kt;
-    uint32_t regs[2];
-#pragma unroll
-    for (int hpair = 0; hpair < 2; ++hpair) {
-      const int ch = 16 * kt + 8 * hpair + 2 * tig;  // channel within the group
-      const int pos = slot_pos((p8 + hpair) & 7);
-      float v[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const float x = ldexpf(qr[hh][ch + u], e + 10 - pos);
-        const __half hi = __float2half_rn(x);
-        const float lo = x - __half2float(hi);
-        v[u] = hl ? lo : __half2float(hi);
-      }
-      regs[hpair] = pack_half2(v[0], v[1]);
-    }
-    const size_t fidx = ((((size_t)b * g.Hkv + kvh) * a.wl.nt + plane) * (D / 16) + kk) * 32 + ln;
-    ws.qfrag[fidx] = make_uint2(regs[0], regs[1]);
+    const int e = q_head_exp(nrm[hh]);
+    if (grp == 0 && sub == 0) out.qaux[hh * 8] = ldexpf(1.f, -e);
+    q_frag_entry<D>(qr[hh], hh, grp, sub, e, gq, out.qfrag);
   }
 }

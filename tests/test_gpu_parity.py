@@ -187,16 +187,21 @@ def test_append_and_extend_parity(osc):
     (syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), 24, [1300, 131], 70),   # crosses a page of evicted tokens
     (syn.Shape(8, 4, 64, 16, 32, 4, 32, 1), 24, [300, 35], 40),        # d = 64, 16-token pages, GQA 2
 ], ids=["d128_p64_gq4", "d64_p16_gq2"])
-def test_fused_decode_step_equals_append_then_decode(osc, shape, ppr, lens0, steps):
-    """oscar_decode_step (the query rotation and the append in one grid) leaves the same cache and output,
-    bit for bit, as oscar_append_step followed by oscar_decode_attn; checked against the oracle at the end.
-    The second request is one token short of evicting at the first step."""
+@pytest.mark.parametrize("form", ["three_kernels", "one_launch"])
+def test_fused_decode_step_equals_append_then_decode(osc, shape, ppr, lens0, steps, form):
+    """oscar_decode_step (the query rotation and the append in one grid; in the one-launch form the
+    append alone, then the one decode kernel) leaves the same cache and output, bit for bit, as
+    oscar_append_step followed by oscar_decode_attn in the same form; checked against the oracle at
+    the end.  The second request is one token short of evicting at the first step."""
     import torch
     wl = syn.Workload("step", shape, [0], seed=12)
     fx = H.fixture(wl)
     bt = _contiguous_bt(2, ppr)
     ga, img, _, _, _ = _prefill_both(osc, wl, fx, lens0, bt, 2 * ppr)
     gb, _, _, _, _ = _prefill_both(osc, wl, fx, lens0, bt, 2 * ppr)
+    code = osc.DECODE_ONE_LAUNCH if form == "one_launch" else osc.DECODE_THREE_KERNELS
+    osc.oscar_set_decode_form(ga.ctx, code)
+    osc.oscar_set_decode_form(gb.ctx, code)
     try:
         hq, d = shape.n_q_heads, shape.head_dim
         slots = np.arange(2, dtype=np.int32)
