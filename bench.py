@@ -553,7 +553,26 @@ def long_and_capacity(osc, hbm_peak, steps=5, row_shift=37):
     wms = e0.elapsed_time(e1) / 5
     res["write_prefill_8x32k"] = {"tokens": B * n, "ms": wms, "tokens_per_s": B * n / (wms * 1e-3),
                                   "bytes": B * n * 8 * 2 * (128 * 2 + 48),
-                                  "gbs": B * n * 8 * 2 * (128 * 2 + 48) / (wms * 1e-3) / 1e9}
+                                  "gbs": B * n * 8 * 2 * (128 * 2 + 48) / (wms * 1e-3) / 1e9,
+                                  "frac_of_peak": B * n * 8 * 2 * (128 * 2 + 48) / (wms * 1e-3) / 1e9 / hbm_peak}
+
+    # the same write with the rotation H_Had . P_br alone (fast Walsh-Hadamard transform on CUDA cores)
+    def write_fwht():
+        osc.oscar_write_kv_hadamard(ctx, 0, kd, vd, osc.DTYPE_BF16, cu, start, B, B * n, fx["clip_K"], fx["clip_V"],
+                                    bt, ppr, slots)
+    write_fwht()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(5):
+        write_fwht()
+    e1.record()
+    torch.cuda.synchronize()
+    hms = e0.elapsed_time(e1) / 5
+    hb = B * n * 8 * 2 * (128 * 2 + 48)
+    res["write_prefill_8x32k_hadamard"] = {"tokens": B * n, "ms": hms, "tokens_per_s": B * n / (hms * 1e-3),
+                                           "bytes": hb, "gbs": hb / (hms * 1e-3) / 1e9,
+                                           "frac_of_peak": hb / (hms * 1e-3) / 1e9 / hbm_peak}
+    write()   # the dense-rotation cache again for the decode steps below
     kn = torch.from_numpy(syn.to_bf16_bits(syn.kv_tokens(wl, 0, B, sub=9)[0]).view(np.int16)).cuda()
     vn = torch.from_numpy(syn.to_bf16_bits(syn.kv_tokens(wl, 0, B, sub=9)[1]).view(np.int16)).cuda()
     q = torch.from_numpy(syn.to_bf16_bits(syn.queries(wl, 0, B)).view(np.int16)).cuda()

@@ -380,6 +380,216 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 2) write_kernel(WriteArgs a
   }
 }
 
+// ------------------------------------------------------------------ prefill / extend, rotation H_Had . P_br
+// The Hadamard-only write (no matrix).  The row x of a (token, kv head) is held by a
+// quad of lanes: quad lane q (0..3) holds elements [q E, q E + E), E = D/4.  The fast
+// Walsh-Hadamard transform (Sylvester order) runs its log2(E) low stages in registers
+// and its two top stages across the quad (xor shuffles); y = x H / sqrt(D).  The
+// bit-reversal gather P_br moves no data: element i = q E + c is output channel
+// j = br(i) = 4 br(c) + br2(q), so quantisation group gi is the register set
+// { c : c mod G = br(gi) } (eight registers per quad lane) and its channel
+// u = 4 br3(c / G) + br2(q).  Group min/max: eight registers, then two quad
+// shuffles.  Four codes fill one byte of a page code word; the bytes meet in a
+// per-warp row buffer, from which each quad lane stores a quarter of the row.
+// A warp takes 8 rows per pass; the request lookup is cached per lane.
+constexpr int kFwhtWarps = 8;
+
+__device__ __forceinline__ int brev_bits(int x, int nbits) { return nbits ? (int)(__brev((unsigned)x) >> (32 - nbits)) : 0; }
+
+template <int D>
+__global__ void __launch_bounds__(kFwhtWarps * 32) write_fwht_kernel(WriteArgs a) {
+  constexpr int E = D / 4, G = D / 32, NG = D == 128 ? 2 : 1;  // NG = log2(G)
+  constexpr int WPQ = D / 64;                                    // code words per quad lane
+  __shared__ __align__(16) uint8_t cbuf[kFwhtWarps][8][D / 4];  // [warp][row of the pass]: the row's code words
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = lane & 3, rl = lane >> 2;
+  const bool is_v = blockIdx.y == 1;
+  const Geom& g = a.g;
+  const float clip = is_v ? a.clip_V : a.clip_K;
+  // the page size is a power of two (checked by the host); n_kv_heads usually is
+  const bool hkv_pow2 = (g.Hkv & (g.Hkv - 1)) == 0;
+  const int hkv_sh = __ffs(g.Hkv) - 1, p_sh = __ffs(g.P) - 1;
+  const long long rows = (long long)a.total_tokens * g.Hkv;
+  const long long step = (long long)gridDim.x * kFwhtWarps * 8;
+  int cb = 0, cb0 = 0, cb1 = -1, ct0 = 0;  // cached request: tokens [cb0, cb1) of request cb, start_pos ct0
+  for (long long base = ((long long)blockIdx.x * kFwhtWarps + warp) * 8; base < rows; base += step) {
+    const long long r = base + rl;
+    const bool live = r < rows;
+    const int token = live ? static_cast<int>(hkv_pow2 ? r >> hkv_sh : r / g.Hkv) : 0;
+    const int h = live ? static_cast<int>(hkv_pow2 ? r & (g.Hkv - 1) : r % g.Hkv) : 0;
+    float v[E];
+    const size_t in_base = ((size_t)token * g.Hkv + h) * D + (size_t)q * E;
+    if (!live) {
+#pragma unroll
+      for (int c = 0; c < E; ++c) v[c] = 0.f;
+    } else if (a.dtype == kDtypeBF16) {
+      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(is_v ? a.V : a.K) + in_base);
+#pragma unroll
+      for (int k = 0; k < E / 8; ++k) {
+        const uint4 w = p[k];
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[8 * k + 2 * e] = __uint_as_float(ww[e] << 16);
+          v[8 * k + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+        }
+      }
+    } else {
+      const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(is_v ? a.V : a.K) + in_base);
+#pragma unroll
+      for (int k = 0; k < E / 4; ++k) {
+        const float4 w = p[k];
+        v[4 * k] = w.x; v[4 * k + 1] = w.y; v[4 * k + 2] = w.z; v[4 * k + 3] = w.w;
+      }
+    }
+    int kind = 0, t = 0;  // kind 1: INT2 history row, 2: BF16 window row
+    if (live) {
+      if (token < cb0 || token >= cb1) {
+        int lo = 0, hi = a.batch - 1;  // largest b with cu_seqlens[b] <= token
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (a.cu_seqlens[mid] <= token) lo = mid; else hi = mid - 1;
+        }
+        cb = lo;
+        cb0 = a.cu_seqlens[cb];
+        cb1 = a.cu_seqlens[cb + 1];
+        ct0 = a.start_pos[cb];
+      }
+      t = ct0 + (token - cb0);
+      const int n1 = ct0 + (cb1 - cb0);
+      if (ct0 < 0 || n1 > g.max_pages_per_req * g.P) {
+        if (q == 0) flag_error(a.status, kDevBadLen);
+      } else {
+        kind = (t >= g.S && t < n1 - g.W) ? 1 : 2;
+      }
+    }
+    int page = -1;  // read now, used after the transform
+    if (kind == 1) {
+      const int lp = t >> p_sh;
+      if (lp < a.bt_stride && lp < g.max_pages_per_req) page = a.block_table[(size_t)cb * a.bt_stride + lp];
+    }
+    if (kind == 2) {
+      const int req = a.req_slot[cb];
+      if (req < 0 || req >= g.max_req) {
+        if (q == 0) flag_error(a.status, kDevBadSlot);
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(window_row(a, req, h, is_v, window_slot(t, g.S, g.W)) + q * E);
+#pragma unroll
+        for (int k = 0; k < E / 8; ++k) {
+          uint32_t ww[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            ww[e] = static_cast<uint32_t>(to_bf16_bits(v[8 * k + 2 * e])) |
+                    (static_cast<uint32_t>(to_bf16_bits(v[8 * k + 2 * e + 1])) << 16);
+          dst[k] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+        }
+      }
+    }
+    // the transform runs on every quad (its shuffles need whole warps); only history rows are stored
+    // register stages: butterflies on pairs (c, c + hl) two at a time as float32 pairs
+#pragma unroll
+    for (int hl = 1; hl < E; hl <<= 1) {
+#pragma unroll
+      for (int c = 0; c < E; c += 2) {
+        if (hl == 1) {
+          if ((c & 1) == 0) {
+            const float x0 = v[c], x1 = v[c + 1];
+            v[c] = x0 + x1;
+            v[c + 1] = x0 - x1;
+          }
+        } else if ((c & hl) == 0) {
+          const float2 x0 = make_float2(v[c], v[c + 1]), x1 = make_float2(v[c + hl], v[c + hl + 1]);
+          const float2 sm = __fadd2_rn(x0, x1), df = __fadd2_rn(x0, make_float2(-x1.x, -x1.y));
+          v[c] = sm.x; v[c + 1] = sm.y;
+          v[c + hl] = df.x; v[c + hl + 1] = df.y;
+        }
+      }
+    }
+    // quad stages: partner o; the lower lane keeps v + o, the upper o - v, as o + sign * v
+#pragma unroll
+    for (int lm = 1; lm < 4; lm <<= 1) {
+      const float sgn = (q & lm) ? -1.f : 1.f;
+#pragma unroll
+      for (int c = 0; c < E; ++c) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[c], lm);
+        v[c] = fmaf(sgn, v[c], o);
+      }
+    }
+    const float inv_sqrt_d = D == 64 ? 0.125f : 0.08838834764831845f;  // 1/sqrt(D) rounded to float32
+    uint8_t* crow = cbuf[warp][rl];
+    const int bq = brev_bits(q, 2);
+    uint32_t szw = 0;
+#pragma unroll
+    for (int cg = 0; cg < G; ++cg) {
+      const int gi = brev_bits(cg, NG);
+      // y = v / sqrt(D), rounded once; the group's extremes are found on v (rounding a
+      // multiplication by a positive constant is monotonic) and then scaled
+      float mn = v[cg], mx = v[cg];
+#pragma unroll
+      for (int m = 1; m < 8; ++m) {
+        mn = fminf(mn, v[cg + G * m]);
+        mx = fmaxf(mx, v[cg + G * m]);
+      }
+#pragma unroll
+      for (int lm = 1; lm < 4; lm <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, lm));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, lm));
+      }
+      // clipping is monotonic: the clipped group's min and max are the clipped min and max
+      mn = fminf(fmaxf(mn * inv_sqrt_d, -clip), clip);
+      mx = fminf(fmaxf(mx * inv_sqrt_d, -clip), clip);
+      const uint16_t zb = to_bf16_bits(mn);
+      const uint16_t sb = to_bf16_bits((mx - mn) / 3.0f);
+      const float z = __uint_as_float(static_cast<uint32_t>(zb) << 16);
+      const float sc = __uint_as_float(static_cast<uint32_t>(sb) << 16);
+      const float inv = sc > 0.f ? __frcp_rn(sc) : 0.f;  // s = 0: every code 0
+      const float zinv = -z * inv;
+      // code = clamp(rne((clip(y) - z) / s), 0, 3) as y * (1/s) - z/s clamped to the images of the
+      // clip range and to [0, 3], rounded by adding 1.5 * 2^23 (the code is the pattern's low bits)
+      const float t_lo = fmaxf(fmaf(-clip, inv, zinv), 0.f);
+      const float t_hi = fminf(fmaf(clip, inv, zinv), 3.f);
+      uint32_t pat[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        pat[m] = __float_as_uint(fminf(fmaxf(fmaf(v[cg + G * m] * inv_sqrt_d, inv, zinv), t_lo), t_hi) + 12582912.0f);
+      // Channel u = 4 br3(m) + br2(q) of the group.  With mb = br3(m), the four codes of
+      // mb = 2k + lo (k = 0..3) fill one byte of a page word, field k at bits 2k: the byte is
+      // p0 + 4 p1 + 16 p2 + 64 p3 of the patterns (1.5 * 2^23 has a zero low byte).
+#pragma unroll
+      for (int lo = 0; lo < 2; ++lo) {
+        uint32_t by = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) by += pat[brev_bits(2 * k + lo, 3)] << (2 * k);
+        int w, bi;  // page word and byte within it
+        if (!is_v) {
+          w = (2 * lo + (bq >> 1)) * WPQ + (gi >> 1);
+          bi = 2 * (bq & 1) + (gi & 1);
+        } else {
+          const int hw = WPQ * (4 * lo + bq) + (gi >> 1);
+          w = hw >> 1;
+          bi = 2 * (hw & 1) + (gi & 1);
+        }
+        crow[4 * w + bi] = static_cast<uint8_t>(by);
+      }
+      if (q == gi) szw = static_cast<uint32_t>(sb) | (static_cast<uint32_t>(zb) << 16);
+    }
+    __syncwarp();
+    if (kind == 1) {
+      if (page < 0 || page >= g.num_pages) {
+        if (q == 0) flag_error(a.status, kDevBadPage);
+      } else {
+        uint8_t* codes;
+        uint32_t* sz;
+        history_row_ptrs<D>(a, page, t & (g.P - 1), h, is_v, &codes, &sz);
+        if constexpr (WPQ == 2) reinterpret_cast<uint2*>(codes)[q] = reinterpret_cast<const uint2*>(crow)[q];
+        else reinterpret_cast<uint32_t*>(codes)[q] = reinterpret_cast<const uint32_t*>(crow)[q];
+        if (q < G) sz[q] = szw;
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // ------------------------------------------------------------------ eviction before an extend
 // Ring tokens [max(S, t0-W), min(t0, n1-W)) of request b become history.
 // grid = (ceil(W / warps), batch, 2): one warp per (ring position, all heads).
@@ -629,10 +839,36 @@ int launch_write_t(const WriteArgs& a, cudaStream_t s) {
   return static_cast<int>(cudaGetLastError());
 }
 
+template <int D>
+int launch_write_fwht_t(const WriteArgs& a, cudaStream_t s) {
+  const long long rows = (long long)a.total_tokens * a.g.Hkv;
+  long long ctas = (rows + kFwhtWarps * 8 - 1) / (kFwhtWarps * 8);
+  // one wave (K and V CTAs together fill the SMs at the kernel's occupancy), then a grid-stride loop
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, write_fwht_kernel<D>, kFwhtWarps * 32, 0) != cudaSuccess ||
+        n < 1)
+      n = 1;
+    per_sm = n;
+  }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms < 1)
+    sms = 152;
+  const long long cap = (long long)sms * per_sm / 2 > 0 ? (long long)sms * per_sm / 2 : 1;
+  if (ctas > cap) ctas = cap;
+  write_fwht_kernel<D><<<dim3((unsigned)ctas, 2), kFwhtWarps * 32, 0, s>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+
 int launch_write(const WriteArgs& a, void* stream) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long rows = (long long)a.total_tokens * a.g.Hkv;
   if (rows == 0) return 0;
+  // the quad-lane transform reads each quarter row with 16-byte loads
+  const bool aligned = ((reinterpret_cast<uintptr_t>(a.K) | reinterpret_cast<uintptr_t>(a.V)) & 15) == 0;
+  if (a.hadamard && aligned) return a.g.D == 128 ? launch_write_fwht_t<128>(a, s) : launch_write_fwht_t<64>(a, s);
   return a.g.D == 128 ? launch_write_t<128>(a, s) : launch_write_t<64>(a, s);
 }
 

@@ -42,7 +42,10 @@ namespace {
 constexpr int kTileM = 128;
 // Epilogue warps: for each of the two TMEM buffers and each column half of the row,
 // four warps (one per TMEM lane quadrant); the producer warp comes after them.
-template <int D> __host__ __device__ constexpr int epi_halves() { return 1; }
+#ifndef OSCAR_WRITE_HALVES
+#define OSCAR_WRITE_HALVES 1
+#endif
+template <int D> __host__ __device__ constexpr int epi_halves() { return D == 128 ? OSCAR_WRITE_HALVES : 1; }
 template <int D> __host__ __device__ constexpr int epi_warps() { return 2 * epi_halves<D>() * 4; }
 template <int D> __host__ __device__ constexpr int tc_threads() { return (epi_warps<D>() + 1) * 32; }
 constexpr int kPlanes = 3;
@@ -58,7 +61,8 @@ struct TcPlan {
   static constexpr int B_PLANE = D * D * 2;          // one BF16 plane of R^T
   static constexpr int A_OFF = kPlanes * B_PLANE;    // multiple of 1024
   static constexpr int BAR_OFF = A_OFF + NS * A_BYTES;
-  static constexpr int NBARS = 2 * NS + 4;           // a_full[NS], a_empty[NS], acc_full[2], acc_empty[2]
+  static constexpr int NBARS = 2 * NS + 5;           // a_full[NS], a_empty[NS], acc_full[2], acc_empty[2], r_full
+  static_assert(NS * A_BYTES >= D * D * 4, "R (float32) is staged in the A stage buffers");
   static constexpr int BYTES = BAR_OFF + NBARS * 8 + 16;
   static constexpr int SMEM = BYTES + 1024;          // slack for the 1024-byte alignment of the base
   // per tile buffer two float32 accumulators of D columns (see the MMA order); two buffers
@@ -179,6 +183,7 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
   uint64_t* a_empty = bars + L::NS;
   uint64_t* acc_full = bars + 2 * L::NS;
   uint64_t* acc_empty = acc_full + 2;
+  uint64_t* r_full = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBARS);
   // Work items are tiles of kTileM rows.  One rotation per layer: rows r = token * Hkv + h
   // of the whole call, tile i covering rows [kTileM i, kTileM (i + 1)), split over the CTAs.
@@ -190,10 +195,22 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
   const long long rows = g.rph ? (long long)a.total_tokens : (long long)a.total_tokens * g.Hkv;
   const int tiles = (int)((rows + kTileM - 1) / kTileM);
 
-  // R^T as three BF16 planes, K-major with the 128-byte swizzle (row n = column n of R)
+  // R^T as three BF16 planes, K-major with the 128-byte swizzle (row n = column n of R).
+  // R (float32, D x D) arrives by one bulk copy in the A stage buffers, which the row
+  // tiles use only after the planes are built.
   const float* R = (is_v ? a.R_V : a.R_K) + (size_t)hsel * g.rot_stride();
+  const float* Rs = reinterpret_cast<const float*>(asm_);
+  if (threadIdx.x == 0) {
+    mbar_init(r_full, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(r_full, D * D * sizeof(float));
+    bulk_g2s(asm_, R, D * D * sizeof(float), r_full);
+  }
+  __syncthreads();
+  const bool r_ok = __syncthreads_and(mbar_wait_bounded(r_full, 0, a.status));
+  if (!r_ok && threadIdx.x == 0) (void)mbar_wait_bounded(r_full, 0, nullptr);  // drain before reusing the buffer
   // item = (n, k-octet): 8 consecutive k of column n, contiguous in the swizzled row
-  for (int item = threadIdx.x; item < D * D / 8; item += blockDim.x) {
+  for (int item = threadIdx.x; r_ok && item < D * D / 8; item += blockDim.x) {
     const int n = item % D, k0 = (item / D) * 8;
     uint32_t pk[3][4];
 #pragma unroll
@@ -201,7 +218,7 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
       uint32_t lo[3], hi[3];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float r = __ldg(R + (size_t)(k0 + 2 * q + e) * D + n);
+        const float r = Rs[(k0 + 2 * q + e) * D + n];
         const __nv_bfloat16 p1 = __float2bfloat16_rn(r);
         const float r1 = r - __bfloat162float(p1);
         const __nv_bfloat16 p2 = __float2bfloat16_rn(r1);
@@ -235,7 +252,9 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
     __syncwarp();
     tmem_alloc(tmem_slot, L::TMEM_COLS);
   }
-  fence_proxy_async_smem();  // the planes were written by ordinary stores; the MMAs read them as async proxy
+  // the planes were written and R read by ordinary accesses; the MMAs read the planes and the
+  // row-tile loads overwrite R through the async proxy
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -247,7 +266,7 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
       const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
       const uint32_t idesc = idesc_bf16_f32(kTileM, D);
       const uint32_t b_base = smem_u32(bsm);
-      const int n_mine = cta_k < tiles ? (tiles - 1 - cta_k) / n_ctas + 1 : 0;
+      const int n_mine = (r_ok && cta_k < tiles) ? (tiles - 1 - cta_k) / n_ctas + 1 : 0;
       auto load = [&](int i) {  // tile i of this CTA into stage i % NS
         const int st = i % L::NS;
         mbar_arrive_expect_tx(&a_full[st], L::A_BYTES);
@@ -313,7 +332,7 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
     const float clip = is_v ? a.clip_V : a.clip_K;
     const void* src = is_v ? a.V : a.K;
     int i = eg;
-    for (int tile = cta_k + eg * n_ctas; tile < tiles; tile += 2 * n_ctas, i += 2) {
+    for (int tile = cta_k + eg * n_ctas; r_ok && tile < tiles; tile += 2 * n_ctas, i += 2) {
       const int s = i & 1;
       const uint32_t u = (uint32_t)(i >> 1);
       // where this row goes: 1 = INT2 history slot, 2 = BF16 window slot, 0 = nowhere

@@ -105,30 +105,45 @@ def test_naive_int2_identity_rotation(osc):
         gc.close()
 
 
-def test_write_hadamard_only_parity(osc):
-    """Data-oblivious rotation R = H P (U = I): the FWHT path against the oracle's dense fp32 R."""
-    wl = syn.Workload("had", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=7)
+@pytest.mark.parametrize("shape", [syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), syn.Shape(8, 4, 64, 16, 32, 4, 32, 1),
+                                   syn.Shape(24, 6, 128, 32, 32, 4, 64, 1)],
+                         ids=["d128_p64", "d64_p16", "d128_p32_six_kv_heads"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_write_hadamard_only_parity(osc, shape, dtype):
+    """Data-oblivious rotation R = H P (U = I): the fast Walsh-Hadamard write against the oracle's dense
+    R, three requests of ragged lengths (row counts not a multiple of the kernel's 8-row passes), then
+    an extend chunk of each request after its prefix (eviction of ring tokens, then the write)."""
+    wl = syn.Workload("had", shape, [0], seed=7, dtype=dtype)
     fx = H.fixture(wl, u_identity=True)
-    lens = [700, 300]
+    lens = [700, 300, 37]
     s = wl.shape
-    ppr = 12
-    bt = _contiguous_bt(2, ppr)
-    geom = H.geometry(s, 2 * ppr, 2)
+    ppr = syn.pages_for(max(lens) + 200, s.page_size) + 1
+    bt = _contiguous_bt(3, ppr)
+    geom = H.geometry(s, 3 * ppr, 3)
     img = cache.CacheImage(geom)
     gc = H.make_gpu_cache(geom, s.n_q_heads, ppr)
-    try:
-        k = np.concatenate([syn.kv_tokens(wl, 0, n, sub=i)[0] for i, n in enumerate(lens)])
-        v = np.concatenate([syn.kv_tokens(wl, 0, n, sub=i)[1] for i, n in enumerate(lens)])
-        cu = np.array([0, lens[0], sum(lens)], np.int32)
-        sp = np.zeros(2, np.int32)
-        slots = np.arange(2, dtype=np.int32)
+    slots = np.arange(3, dtype=np.int32)
+
+    def write(lens_now, start, sub0):
+        k = np.concatenate([syn.kv_tokens(wl, 0, n, sub=sub0 + i)[0] for i, n in enumerate(lens_now)])
+        v = np.concatenate([syn.kv_tokens(wl, 0, n, sub=sub0 + i)[1] for i, n in enumerate(lens_now)])
+        cu = np.concatenate([[0], np.cumsum(lens_now)]).astype(np.int32)
+        sp = np.asarray(start, np.int32)
         diag = cache.write_kv(img, 0, k, v, cu, sp, fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"], bt, slots)
-        osc.oscar_write_kv_hadamard(gc.ctx, 0, H.dev_input(k, "bf16"), H.dev_input(v, "bf16"), osc.DTYPE_BF16,
-                                    H.dev(cu), H.dev(sp), 2, int(cu[-1]), fx["clip_K"], fx["clip_V"], H.dev(bt), ppr,
+        osc.oscar_write_kv_hadamard(gc.ctx, 0, H.dev_input(k, dtype), H.dev_input(v, dtype), H.dtype_code(dtype),
+                                    H.dev(cu), H.dev(sp), 3, int(cu[-1]), fx["clip_K"], fx["clip_V"], H.dev(bt), ppr,
                                     H.dev(slots))
         assert osc.oscar_check_status(gc.ctx) == 0
+        return diag
+
+    try:
+        diag = write(lens, [0, 0, 0], 0)
         H.compare_history(gc.pool_np(), geom, 0, diag)
-        H.compare_window(gc.slab_np(), img.slab, 0, range(2))
+        H.compare_window(gc.slab_np(), img.slab, 0, range(3))
+        chunk = [90, 33, 150]
+        diag = write(chunk, lens, 10)
+        H.compare_history(gc.pool_np(), geom, 0, diag)
+        H.compare_window(gc.slab_np(), img.slab, 0, range(3))
     finally:
         gc.close()
 
