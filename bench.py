@@ -87,15 +87,19 @@ def append_bytes(hkv=8, d=128):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms from start() to stop().  mark_start() / mark_end() bracket the
+    timed region by wall time; the record gives the samples taken inside it and, when it is shorter
+    than a few sampling periods, the samples of the whole measurement phase around it as well."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index=0):
         self.proc = None
         self.path = None
         self.gpu = gpu_index
-        self.skip = 0
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -103,12 +107,12 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(self.gpu), "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-i", str(self.gpu), "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
             return
         t0 = time.time()   # wait until the sampler is running
-        while time.time() - t0 < 5.0 and self.proc.poll() is None and self._lines() == 0:
+        while time.time() - t0 < 10.0 and self.proc.poll() is None and self._lines() < 2:
             time.sleep(0.02)
 
     def _lines(self):
@@ -118,10 +122,19 @@ class ClockSampler:
         except OSError:
             return 0
 
-    def mark(self):
-        """Called as the timed region starts: samples written before now are not used."""
-        if self.proc:
-            self.skip = self._lines()
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    @staticmethod
+    def _epoch(stamp):
+        day, _, frac = stamp.partition(".")
+        try:
+            return time.mktime(time.strptime(day, "%Y/%m/%d %H:%M:%S")) + (float("0." + frac) if frac else 0.0)
+        except ValueError:
+            return None
 
     def stop(self):
         if not self.proc:
@@ -131,23 +144,34 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in list(open(self.path))[self.skip:]:
+        rows = []
+        for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                rows.append((self._epoch(parts[0]), float(parts[2]), float(parts[3]),
+                             [v.lower().startswith("active") for v in parts[6:10]]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
         os.unlink(self.path)
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+
+        def summary(sel):
+            reasons = sorted({n for r in sel for n, on in zip(self.NAMES, r[3]) if on})
+            return {"sm_mhz": float(np.median([r[1] for r in sel])) if sel else None,
+                    "sm_max_mhz": max(r[2] for r in sel) if sel else None, "reasons": reasons, "samples": len(sel)}
+
+        inside = [r for r in rows if r[0] is not None and self.t0 is not None and self.t1 is not None
+                  and self.t0 <= r[0] <= self.t1]
+        out = summary(inside)
+        out["window_s"] = (self.t1 - self.t0) if self.t0 is not None and self.t1 is not None else None
+        out["period_ms"] = 50
+        if len(inside) < 5:   # a short timed region: the measurement phase around it, same workload
+            phase = summary(rows)
+            out["phase"] = phase
+            if not inside:
+                out.update({k: phase[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")})
+        return out
 
 
 # ------------------------------------------------------------------ distributed (replicas)
@@ -251,10 +275,13 @@ def oracle_decode_one_thread(target_s=5.0):
     try:
         r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
         if r.returncode != 0:
-            return None
+            tail = (r.stderr.strip().splitlines() or ["no output"])[-1]
+            return {"error": f"exit status {r.returncode}: {tail[:200]}"}
         return json.loads(r.stdout.strip().splitlines()[-1])
-    except (subprocess.TimeoutExpired, ValueError, IndexError):
-        return None
+    except subprocess.TimeoutExpired:
+        return {"error": "timed out after 300 s"}
+    except (ValueError, IndexError) as e:
+        return {"error": f"unreadable output: {e}"}
 
 
 def run_reference(args, world, rank):
@@ -782,7 +809,10 @@ def run_ours(args, world, rank, local):
             fn()
         return g
 
-    # ---------------- warm-up (eager: first-use set-up happens here), then capture one step
+    # ---------------- warm-up (eager: first-use set-up happens here), then capture one step.
+    # The clock sampler runs from here to the end of the decode-only timing below.
+    clocks = ClockSampler(local)
+    clocks.start()
     for i in range(args.warmup):
         layer_pass(True, qs[i % nvar], kn[i % nvar], vn[i % nvar])
     torch.cuda.synchronize()
@@ -794,18 +824,16 @@ def run_ours(args, world, rank, local):
     n_start = int(lens2[0].item())
     # ---------------- main timed loop: append + decode through all layers, one graph replay per step
     barrier(world)
-    clocks = ClockSampler(local)
-    clocks.start()
-    clocks.mark()
+    clocks.mark_start()
     ev0.record()
     for i in range(args.steps):
         g_step.replay()
     ev1.record()
     torch.cuda.synchronize()
+    clocks.mark_end()
     launches = launches_per_step * args.steps
     barrier(world)
     step_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
-    clk = clocks.stop()
     st = osc.oscar_check_status(ctx)
     assert st == 0, f"device status {st}"
     # per-replay spread, a separate measurement after the timed region: each of up to 50 step
@@ -836,6 +864,7 @@ def run_ours(args, world, rank, local):
     ev1.record()
     torch.cuda.synchronize()
     dec_only_ms = ev0.elapsed_time(ev1) / args.steps
+    clk = clocks.stop()
 
     # per-kernel device times: a decode-only pass captured with timing on (each
     # launch bracketed by event-record nodes, no programmatic overlap), replayed
@@ -862,15 +891,20 @@ def run_ours(args, world, rank, local):
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     achieved = kern_bytes / (kern_avg_ms * 1e-3) / 1e9
     traffic = None
+    ncu_us = None
     tr_path = os.path.join(ROOT, "profiles", "decode_splitk_traffic.json")
     if os.path.exists(tr_path):
         tr = json.load(open(tr_path))
         if tr.get("kernel_version") == osc.oscar_version():
             traffic = tr.get("bytes_per_launch")
+            ncu_us = tr.get("gpu_time_duration_us")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "traffic": traffic, "kernel": "decode_splitk", "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": kern_bytes, "avg_launch_us": kern_avg_ms * 1e3,
-                "q_rotate_avg_us": qms / max(kl, 1) * 1e3, "combine_avg_us": cms / max(kl, 1) * 1e3}
+                "q_rotate_avg_us": qms / max(kl, 1) * 1e3, "combine_avg_us": cms / max(kl, 1) * 1e3,
+                # the same kernel's gpu__time_duration from the committed ncu capture (one cold-cache
+                # launch, this library version), beside the event-timed avg_launch_us above
+                "ncu_gpu_time_us": ncu_us}
 
     # ---------------- in-house BF16 paged decode on the same shapes (decode only)
     bf16_info = None
@@ -974,7 +1008,9 @@ def run_ours(args, world, rank, local):
         r = oracle_decode_sample(target_s=15.0)
         cpu = {"value": r["gbs"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
         r1 = oracle_decode_one_thread()
-        if r1 is not None:
+        if "error" in r1:
+            cpu["one_thread"] = {"unavailable": r1["error"], "cores": 1}
+        else:
             cpu["one_thread"] = {"value": r1["gbs"], "unit": "GB/s", "cores": 1, "sample": r1["sample"]}
     osc.oscar_destroy(ctx)
     if rank == 0:

@@ -1373,10 +1373,13 @@ int launch_splitk_t(const DecodeArgs& a, cudaStream_t s, bool pdl) {
   if (win_smem > smem) smem = win_smem;
   if (merge_smem > smem) smem = merge_smem;
   smem = (smem + 127) & ~size_t(127);
-  // three CTAs per SM (the plan sizes one wave as 3 x 152 CTAs)
+  // three CTAs per SM (the plan sizes one wave as 3 x 152 CTAs).  The one-launch form needs the
+  // largest shared-memory carveout for that; the three-kernel form keeps the default, which
+  // its neighbours in the chain use too (an SM holds CTAs of one carveout at a time, so a
+  // different one would keep the programmatic overlap from happening)
   static_assert(3 * (Lay::SMEM_FUSED + 128 + 1024) <= 228 * 1024, "three CTAs per SM");
   auto kern = decode_splitk_kernel<D, NT, P, FUSED>;
-  cudaError_t e = ensure_smem_limit(kern, smem, true);
+  cudaError_t e = ensure_smem_limit(kern, smem, FUSED);
   if (e != cudaSuccess) return (int)e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.wl.win_chunks + a.wl.max_splits, a.g.Hkv, a.batch);

@@ -300,7 +300,7 @@ extern "C" {
 
 const char* oscar_last_error(void) { return g_last_error.c_str(); }
 
-const char* oscar_version(void) { return "oscar-gb300 0.8 (sm_103a)"; }
+const char* oscar_version(void) { return "oscar-gb300 0.9 (sm_103a)"; }
 
 size_t oscar_int2_pool_bytes(const oscar_config* cfg) {
   Geom g;
