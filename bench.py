@@ -60,6 +60,9 @@ def parse():
                     help="run only the extend-attention measurement and print its rows (a profiling entry point)")
     ap.add_argument("--extend-configs", default="4,32768,2048;8,0,4096",
                     help="extend workloads as requests,prefix,chunk triples separated by ';'")
+    ap.add_argument("--write-only", action="store_true",
+                    help="only the prefill write of --write-batch requests x 32,768 tokens, dense and Hadamard-only")
+    ap.add_argument("--write-batch", type=int, default=8)
     ap.add_argument("--sweep-only", action="store_true",
                     help="run only the batched-decode sweep and print its rows (a profiling entry point)")
     return ap.parse_args()
@@ -1057,6 +1060,63 @@ def run_extend_only(args):
     return 0
 
 
+def write_leg(osc, hbm_peak, batch=8, n=32768, reps=5):
+    """Prefill write of batch x n tokens x 8 kv heads (one layer, one launch per call) with the dense
+    calibrated rotation (tensor cores) and with the Hadamard-only rotation (fast Walsh-Hadamard
+    transform), timed with CUDA events over reps calls after two warm-up calls of each."""
+    import torch
+    from int2_rotated_paged_oscar_gb300 import calibrate
+    wl = syn.write_prefill(batch, n)
+    s = wl.shape
+    i32 = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    ppr = syn.pages_for(n + 64, s.page_size)
+    cfg, pool, slab, ctx = _ctx_for(osc, wl, 1, batch, ppr)
+    bt = torch.arange(batch * ppr, dtype=torch.int32, device="cuda").view(batch, ppr)
+    fx = calibrate.calibrate_layer(syn.queries(wl, 0, 128, calib=True), *syn.kv_tokens(wl, 0, 128, calib=True))
+    rk, rv = torch.from_numpy(fx["R_K"]).cuda(), torch.from_numpy(fx["R_V"]).cuda()
+    kd, vd = _stream(wl, batch * n)
+    cu = i32([n * b for b in range(batch + 1)])
+    start, slots = i32([0] * batch), torch.arange(batch, dtype=torch.int32, device="cuda")
+    nbytes = batch * n * s.n_kv_heads * 2 * (s.head_dim * 2 + s.head_dim // 4 + s.head_dim // 8)
+    forms = {
+        "dense_tensor_core": lambda: osc.oscar_write_kv(ctx, 0, kd, vd, osc.DTYPE_BF16, cu, start, batch, batch * n, rk,
+                                                        rv, fx["clip_K"], fx["clip_V"], bt, ppr, slots),
+        "hadamard_fwht": lambda: osc.oscar_write_kv_hadamard(ctx, 0, kd, vd, osc.DTYPE_BF16, cu, start, batch, batch * n,
+                                                             fx["clip_K"], fx["clip_V"], bt, ppr, slots),
+    }
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    res = {"workload": f"prefill write of {batch} x {n} tokens x {s.n_kv_heads} kv heads (K and V), d={s.head_dim}",
+           "bytes_per_call": nbytes}
+    for name, fn in forms.items():
+        fn()
+        fn()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = {"ms": ms, "tokens_per_s": batch * n / (ms * 1e-3), "gbs": nbytes / (ms * 1e-3) / 1e9,
+                     "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / hbm_peak}
+    assert osc.oscar_check_status(ctx) == 0
+    osc.oscar_destroy(ctx)
+    return res
+
+
+def run_write_only(args):
+    import torch
+    from int2_rotated_paged_oscar_gb300 import build as bld
+    bld.build()
+    import int2_rotated_paged_oscar_gb300 as osc
+    torch.cuda.set_device(0)
+    osc.load()
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(pk_path)) if os.path.exists(pk_path) else {}
+    print(json.dumps(write_leg(osc, float(peaks.get("hbm_gbs", 6800.0)), batch=args.write_batch)), flush=True)
+    return 0
+
+
 def run_sweep_only(args):
     import torch
     from int2_rotated_paged_oscar_gb300 import build as bld
@@ -1079,6 +1139,8 @@ def main():
         return run_sweep_only(args)
     if args.extend_only:
         return run_extend_only(args)
+    if args.write_only:
+        return run_write_only(args)
     if args.impl == "reference":
         rc = run_reference(args, world, rank)
     else:

@@ -50,6 +50,24 @@ inline cudaError_t ensure_smem_limit(Kernel kern, size_t bytes, bool max_carveou
   return ensure_smem_limit_ptr(reinterpret_cast<const void*>(kern), bytes, max_carveout);
 }
 
+// Launch kern<<<grid, block, smem, s>>>(args...) as a programmatic dependent of the
+// kernel before it on the stream when pdl is set (the kernel waits with pdl_wait()
+// before it touches what that kernel writes).
+template <typename Kernel, typename... Args>
+inline int launch_pdl(Kernel kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return (int)cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 __device__ __forceinline__ void flag_error(int* status, int bits) {
   if (status) atomicOr(status, bits);
 }

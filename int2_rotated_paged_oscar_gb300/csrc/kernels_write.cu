@@ -266,6 +266,7 @@ template <int D>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, 2) write_kernel(WriteArgs a) {
   constexpr int C = D / 32;
   extern __shared__ __align__(16) float wsm[];
+  pdl_wait();  // the eviction before it reads ring rows this kernel overwrites
   float* Rs = wsm;                                                  // [D][D]
   WriteSmem<D>& sm = *reinterpret_cast<WriteSmem<D>*>(wsm + D * D);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -398,6 +399,7 @@ __device__ __forceinline__ int brev_bits(int x, int nbits) { return nbits ? (int
 
 template <int D>
 __global__ void __launch_bounds__(kFwhtWarps * 32) write_fwht_kernel(WriteArgs a) {
+  pdl_wait();  // the eviction before it reads ring rows this kernel overwrites
   constexpr int E = D / 4, G = D / 32, NG = D == 128 ? 2 : 1;  // NG = log2(G)
   constexpr int WPQ = D / 64;                                    // code words per quad lane
   __shared__ __align__(16) uint8_t cbuf[kFwhtWarps][8][D / 4];  // [warp][row of the pass]: the row's code words
@@ -596,6 +598,7 @@ __global__ void __launch_bounds__(kFwhtWarps * 32) write_fwht_kernel(WriteArgs a
 template <int D>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) evict_kernel(WriteArgs a) {
   __shared__ WarpSmem sm[kWarpsPerCta];
+  pdl_launch_dependents();  // the write kernel after it may start its set-up; it waits before its stores
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geom& g = a.g;
   const int b = blockIdx.y;
@@ -827,7 +830,7 @@ __global__ void __launch_bounds__(128) step_prep_kernel(const __grid_constant__ 
 }  // namespace
 
 template <int D>
-int launch_write_t(const WriteArgs& a, cudaStream_t s) {
+int launch_write_t(const WriteArgs& a, cudaStream_t s, bool pdl) {
   const int heads = a.g.rph ? a.g.Hkv : 1;  // grid z: one kv head per z with a rotation per kv head
   const long long rows = (long long)a.total_tokens * a.g.Hkv / heads;
   long long ctas = (rows + kWarpsPerCta * kRowsPerPass - 1) / (kWarpsPerCta * kRowsPerPass);
@@ -835,12 +838,11 @@ int launch_write_t(const WriteArgs& a, cudaStream_t s) {
   const size_t smem = sizeof(float) * D * D + sizeof(WriteSmem<D>);
   cudaError_t e = ensure_smem_limit(write_kernel<D>, smem);
   if (e != cudaSuccess) return (int)e;
-  write_kernel<D><<<dim3((unsigned)ctas, 2, (unsigned)heads), kWarpsPerCta * 32, smem, s>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(write_kernel<D>, dim3((unsigned)ctas, 2, (unsigned)heads), dim3(kWarpsPerCta * 32), smem, s, pdl, a);
 }
 
 template <int D>
-int launch_write_fwht_t(const WriteArgs& a, cudaStream_t s) {
+int launch_write_fwht_t(const WriteArgs& a, cudaStream_t s, bool pdl) {
   const long long rows = (long long)a.total_tokens * a.g.Hkv;
   long long ctas = (rows + kFwhtWarps * 8 - 1) / (kFwhtWarps * 8);
   // one wave (K and V CTAs together fill the SMs at the kernel's occupancy), then a grid-stride loop
@@ -858,18 +860,18 @@ int launch_write_fwht_t(const WriteArgs& a, cudaStream_t s) {
     sms = 152;
   const long long cap = (long long)sms * per_sm / 2 > 0 ? (long long)sms * per_sm / 2 : 1;
   if (ctas > cap) ctas = cap;
-  write_fwht_kernel<D><<<dim3((unsigned)ctas, 2), kFwhtWarps * 32, 0, s>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(write_fwht_kernel<D>, dim3((unsigned)ctas, 2), dim3(kFwhtWarps * 32), 0, s, pdl, a);
 }
 
-int launch_write(const WriteArgs& a, void* stream) {
+int launch_write(const WriteArgs& a, void* stream, bool pdl) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long rows = (long long)a.total_tokens * a.g.Hkv;
   if (rows == 0) return 0;
   // the quad-lane transform reads each quarter row with 16-byte loads
   const bool aligned = ((reinterpret_cast<uintptr_t>(a.K) | reinterpret_cast<uintptr_t>(a.V)) & 15) == 0;
-  if (a.hadamard && aligned) return a.g.D == 128 ? launch_write_fwht_t<128>(a, s) : launch_write_fwht_t<64>(a, s);
-  return a.g.D == 128 ? launch_write_t<128>(a, s) : launch_write_t<64>(a, s);
+  if (a.hadamard && aligned)
+    return a.g.D == 128 ? launch_write_fwht_t<128>(a, s, pdl) : launch_write_fwht_t<64>(a, s, pdl);
+  return a.g.D == 128 ? launch_write_t<128>(a, s, pdl) : launch_write_t<64>(a, s, pdl);
 }
 
 int launch_evict(const WriteArgs& a, void* stream) {

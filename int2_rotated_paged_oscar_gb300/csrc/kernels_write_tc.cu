@@ -331,6 +331,9 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
     const int c_lo = ch * GPH * 32, c_hi = c_lo + GPH * 32;
     const float clip = is_v ? a.clip_V : a.clip_K;
     const void* src = is_v ? a.V : a.K;
+    // the eviction launched before this kernel reads ring rows that the tiles' window rows
+    // overwrite: every store waits for it (the set-up and the row-tile loads did not)
+    pdl_wait();
     int i = eg;
     for (int tile = cta_k + eg * n_ctas; r_ok && tile < tiles; tile += 2 * n_ctas, i += 2) {
       const int s = i & 1;
@@ -499,7 +502,7 @@ int make_head_row_map(CUtensorMap* map, const void* base, long long tokens, int 
 }
 
 template <int D>
-int launch_write_tc_t(const WriteArgs& a, cudaStream_t s) {
+int launch_write_tc_t(const WriteArgs& a, cudaStream_t s, bool pdl) {
   using L = TcPlan<D>;
   const bool rph = a.g.rph != 0;
   const long long rows = rph ? (long long)a.total_tokens : (long long)a.total_tokens * a.g.Hkv;
@@ -519,8 +522,7 @@ int launch_write_tc_t(const WriteArgs& a, cudaStream_t s) {
     const long long per_head = tiles < 76 / a.g.Hkv ? tiles : (76 / a.g.Hkv > 0 ? 76 / a.g.Hkv : 1);
     ctas = (int)(per_head * a.g.Hkv);
   }
-  write_tc_kernel<D><<<dim3(ctas, 2), tc_threads<D>(), smem, s>>>(mk, mv, a);
-  return (int)cudaGetLastError();
+  return launch_pdl(write_tc_kernel<D>, dim3(ctas, 2), dim3(tc_threads<D>()), (size_t)smem, s, pdl, mk, mv, a);
 }
 
 }  // namespace
@@ -530,10 +532,10 @@ bool write_tc_supported(const WriteArgs& a) {
          (reinterpret_cast<uintptr_t>(a.K) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.V) & 15) == 0;
 }
 
-int launch_write_tc(const WriteArgs& a, void* stream) {
+int launch_write_tc(const WriteArgs& a, void* stream, bool pdl) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((long long)a.total_tokens * a.g.Hkv == 0) return 0;
-  return a.g.D == 128 ? launch_write_tc_t<128>(a, s) : launch_write_tc_t<64>(a, s);
+  return a.g.D == 128 ? launch_write_tc_t<128>(a, s, pdl) : launch_write_tc_t<64>(a, s, pdl);
 }
 
 }  // namespace oscar

@@ -573,7 +573,8 @@ static oscar_status write_common(oscar_ctx* ctx, int32_t layer, const void* K, c
   // BF16 rows with a dense rotation: tensor-core kernel; FP32 rows or the Hadamard-only rotation: CUDA cores
   const bool tc = oscar::write_tc_supported(a);
   LaunchScope ls(ctx, tc ? "write_tc" : "write", stream);
-  int e = tc ? oscar::launch_write_tc(a, stream) : oscar::launch_write(a, stream);
+  const bool pdl = !ctx->timing;  // the write overlaps its set-up with the eviction
+  int e = tc ? oscar::launch_write_tc(a, stream, pdl) : oscar::launch_write(a, stream, pdl);
   ls.done(e);
   if (e) return cuda_fail(e, "write launch");
   return OSCAR_OK;

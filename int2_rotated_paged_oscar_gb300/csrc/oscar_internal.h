@@ -159,10 +159,11 @@ constexpr int kNoOperandExp = -1000;
 int operand_exponent_for_clip(float clip);
 
 // Kernel launchers (return cudaError_t as int).  Each launches on `stream`.
-int launch_write(const WriteArgs& a, void* stream);
+// pdl: a programmatic dependent of the eviction launched just before it
+int launch_write(const WriteArgs& a, void* stream, bool pdl);
 // Tensor-core (tcgen05) prefill write for BF16 inputs and a dense rotation.
 bool write_tc_supported(const WriteArgs& a);
-int launch_write_tc(const WriteArgs& a, void* stream);
+int launch_write_tc(const WriteArgs& a, void* stream, bool pdl);
 int launch_evict(const WriteArgs& a, void* stream);
 int launch_append(const WriteArgs& a, void* stream, bool pdl);
 int launch_q_rotate(const DecodeArgs& a, void* stream, bool pdl);
