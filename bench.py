@@ -60,6 +60,8 @@ def parse():
                     help="run only the extend-attention measurement and print its rows (a profiling entry point)")
     ap.add_argument("--extend-configs", default="4,32768,2048;8,0,4096",
                     help="extend workloads as requests,prefix,chunk triples separated by ';'")
+    ap.add_argument("--decode-form", default="auto", choices=["auto", "three", "one"],
+                    help="decode launch form of the main step (oscar_set_decode_form)")
     ap.add_argument("--write-only", action="store_true",
                     help="only the prefill write of --write-batch requests x 32,768 tokens, dense and Hadamard-only")
     ap.add_argument("--write-batch", type=int, default=8)
@@ -739,6 +741,8 @@ def run_ours(args, world, rank, local):
     pool = torch.empty(osc.oscar_int2_pool_bytes(cfg), dtype=torch.uint8, device="cuda")
     slab = torch.zeros(osc.oscar_window_slab_bytes(cfg) // 2, dtype=torch.int16, device="cuda")
     ctx = osc.oscar_create(cfg, pool, slab)
+    osc.oscar_set_decode_form(ctx, {"auto": osc.DECODE_AUTO, "three": osc.DECODE_THREE_KERNELS,
+                                    "one": osc.DECODE_ONE_LAUNCH}[args.decode_form])
     stream = torch.cuda.current_stream()
     ids = osc.oscar_alloc_pages(ctx, ppr)
     bt = torch.tensor([ids], dtype=torch.int32, device="cuda")
