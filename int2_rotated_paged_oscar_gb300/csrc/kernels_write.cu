@@ -599,6 +599,7 @@ template <int D>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) evict_kernel(WriteArgs a) {
   __shared__ WarpSmem sm[kWarpsPerCta];
   pdl_launch_dependents();  // the write kernel after it may start its set-up; it waits before its stores
+  pdl_wait();               // (when launched as a programmatic dependent) everything before it is complete
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geom& g = a.g;
   const int b = blockIdx.y;
@@ -874,13 +875,12 @@ int launch_write(const WriteArgs& a, void* stream, bool pdl) {
   return a.g.D == 128 ? launch_write_t<128>(a, s, pdl) : launch_write_t<64>(a, s, pdl);
 }
 
-int launch_evict(const WriteArgs& a, void* stream) {
+int launch_evict(const WriteArgs& a, void* stream, bool pdl) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.batch == 0) return 0;
   dim3 grid((a.g.W + kWarpsPerCta - 1) / kWarpsPerCta, a.batch, 2);
-  if (a.g.D == 128) evict_kernel<128><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
-  else evict_kernel<64><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  if (a.g.D == 128) return launch_pdl(evict_kernel<128>, grid, dim3(kWarpsPerCta * 32), 0, s, pdl, a);
+  return launch_pdl(evict_kernel<64>, grid, dim3(kWarpsPerCta * 32), 0, s, pdl, a);
 }
 
 int launch_step_prep(const WriteArgs& w, const DecodeArgs& d, void* stream, bool pdl) {

@@ -31,6 +31,7 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -501,6 +502,40 @@ int make_head_row_map(CUtensorMap* map, const void* base, long long tokens, int 
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
+// The row tensor maps of recent calls, keyed by (base, rows, kv heads, D, form): a map encodes
+// only the address, sizes and strides, so one that matches is the map the call would build.
+// Repeated writes from the same staging buffers (a layer loop) then skip the encode.
+int cached_row_map(CUtensorMap* map, const void* base, long long rows, int hkv, int D, bool per_head) {
+  struct Entry {
+    const void* base;
+    long long rows;
+    int hkv, d, per_head;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 16;
+  static std::mutex mu;
+  static Entry table[kEntries];
+  static int used = 0, next = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i) {
+      const Entry& e = table[i];
+      if (e.base == base && e.rows == rows && e.hkv == hkv && e.d == D && e.per_head == (int)per_head) {
+        *map = e.map;
+        return 0;
+      }
+    }
+  }
+  const int r = per_head ? make_head_row_map(map, base, rows, hkv, D) : make_row_map(map, base, rows, D);
+  if (r) return r;
+  std::lock_guard<std::mutex> lk(mu);
+  Entry& e = table[next];
+  e = Entry{base, rows, hkv, D, (int)per_head, *map};
+  next = (next + 1) % kEntries;
+  if (used < kEntries) ++used;
+  return 0;
+}
+
 template <int D>
 int launch_write_tc_t(const WriteArgs& a, cudaStream_t s, bool pdl) {
   using L = TcPlan<D>;
@@ -508,10 +543,9 @@ int launch_write_tc_t(const WriteArgs& a, cudaStream_t s, bool pdl) {
   const long long rows = rph ? (long long)a.total_tokens : (long long)a.total_tokens * a.g.Hkv;
   const long long tiles = (rows + kTileM - 1) / kTileM;
   CUtensorMap mk, mv;
-  int e = rph ? make_head_row_map(&mk, a.K, a.total_tokens, a.g.Hkv, D) : make_row_map(&mk, a.K, rows, D);
+  int e = cached_row_map(&mk, a.K, rph ? (long long)a.total_tokens : rows, a.g.Hkv, D, rph);
   if (e) return e;
-  if ((e = rph ? make_head_row_map(&mv, a.V, a.total_tokens, a.g.Hkv, D) : make_row_map(&mv, a.V, rows, D)))
-    return e;
+  if ((e = cached_row_map(&mv, a.V, rph ? (long long)a.total_tokens : rows, a.g.Hkv, D, rph))) return e;
   // at least 120 KB of shared memory: one CTA per SM, so the TMEM allocation never waits
   const int smem = L::SMEM > 120 * 1024 ? L::SMEM : 120 * 1024;
   cudaError_t ce = ensure_smem_limit(write_tc_kernel<D>, smem);

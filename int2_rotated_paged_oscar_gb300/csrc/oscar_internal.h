@@ -164,7 +164,7 @@ int launch_write(const WriteArgs& a, void* stream, bool pdl);
 // Tensor-core (tcgen05) prefill write for BF16 inputs and a dense rotation.
 bool write_tc_supported(const WriteArgs& a);
 int launch_write_tc(const WriteArgs& a, void* stream, bool pdl);
-int launch_evict(const WriteArgs& a, void* stream);
+int launch_evict(const WriteArgs& a, void* stream, bool pdl);
 int launch_append(const WriteArgs& a, void* stream, bool pdl);
 int launch_q_rotate(const DecodeArgs& a, void* stream, bool pdl);
 int launch_decode_splitk(const DecodeArgs& a, void* stream, bool pdl);
