@@ -63,7 +63,7 @@ struct TcPlan {
   static constexpr int A_OFF = kPlanes * B_PLANE;    // multiple of 1024
   static constexpr int BAR_OFF = A_OFF + NS * A_BYTES;
   static constexpr int NBARS = 2 * NS + 5;           // a_full[NS], a_empty[NS], acc_full[2], acc_empty[2], r_full
-  static_assert(NS * A_BYTES >= D * D * 4, "R (float32) is staged in the A stage buffers");
+  static_assert((NS - 2) * A_BYTES >= D * D * 4, "R (float32) is staged in A stages 2 .. NS-1");
   static constexpr int BYTES = BAR_OFF + NBARS * 8 + 16;
   static constexpr int SMEM = BYTES + 1024;          // slack for the 1024-byte alignment of the base
   // per tile buffer two float32 accumulators of D columns (see the MMA order); two buffers
@@ -197,19 +197,48 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
   const int tiles = (int)((rows + kTileM - 1) / kTileM);
 
   // R^T as three BF16 planes, K-major with the 128-byte swizzle (row n = column n of R).
-  // R (float32, D x D) arrives by one bulk copy in the A stage buffers, which the row
-  // tiles use only after the planes are built.
+  // R (float32, D x D) arrives by one bulk copy in A stages 2 .. NS-1, which the row tiles use
+  // only after the planes are built; the producer thread requests this CTA's first two row
+  // tiles (stages 0 and 1) at the same time, so their loads overlap the plane build.
   const float* R = (is_v ? a.R_V : a.R_K) + (size_t)hsel * g.rot_stride();
-  const float* Rs = reinterpret_cast<const float*>(asm_);
-  if (threadIdx.x == 0) {
+  const float* Rs = reinterpret_cast<const float*>(asm_ + 2 * L::A_BYTES);
+  const bool producer = threadIdx.x == kEpiWarps * 32;
+  const int n_mine = cta_k < tiles ? (tiles - 1 - cta_k) / n_ctas + 1 : 0;  // this CTA's row tiles
+  const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
+  auto load = [&](int i) {  // producer: tile i of this CTA into stage i % NS
+    const int st = i % L::NS;
+    mbar_arrive_expect_tx(&a_full[st], L::A_BYTES);
+    const int tile = cta_k + i * n_ctas;
+#pragma unroll
+    for (int c = 0; c < L::KCH; ++c) {
+      if (g.rph)
+        tma_load_3d_tc(asm_ + st * L::A_BYTES + c * kTileM * 128, tmap, 64 * c, hsel, tile * kTileM, &a_full[st]);
+      else
+        tma_load_2d_tc(asm_ + st * L::A_BYTES + c * kTileM * 128, tmap, 64 * c, tile * kTileM, &a_full[st]);
+    }
+  };
+  const int n_early = n_mine < 2 ? n_mine : 2;
+  if (producer) {
+    for (int i = 0; i < L::NS; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], (kEpiWarps / 2) * 32);  // every epilogue warp of that buffer
+    }
     mbar_init(r_full, 1);
     fence_barrier_init();
     mbar_arrive_expect_tx(r_full, D * D * sizeof(float));
-    bulk_g2s(asm_, R, D * D * sizeof(float), r_full);
+    bulk_g2s(asm_ + 2 * L::A_BYTES, R, D * D * sizeof(float), r_full);
+    for (int i = 0; i < n_early; ++i) load(i);
   }
   __syncthreads();
   const bool r_ok = __syncthreads_and(mbar_wait_bounded(r_full, 0, a.status));
-  if (!r_ok && threadIdx.x == 0) (void)mbar_wait_bounded(r_full, 0, nullptr);  // drain before reusing the buffer
+  if (!r_ok && producer) {  // drain every copy in flight before the CTA ends
+    (void)mbar_wait_bounded(r_full, 0, nullptr);
+    for (int i = 0; i < n_early; ++i) (void)mbar_wait_bounded(&a_full[i], 0, nullptr);
+  }
   // item = (n, k-octet): 8 consecutive k of column n, contiguous in the swizzled row
   for (int item = threadIdx.x; r_ok && item < D * D / 8; item += blockDim.x) {
     const int n = item % D, k0 = (item / D) * 8;
@@ -238,21 +267,7 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
     for (int p = 0; p < 3; ++p)
       *reinterpret_cast<uint4*>(bsm + p * L::B_PLANE + off) = make_uint4(pk[p][0], pk[p][1], pk[p][2], pk[p][3]);
   }
-  if (warp == kEpiWarps) {
-    if (lane == 0) {
-      for (int i = 0; i < L::NS; ++i) {
-        mbar_init(&a_full[i], 1);
-        mbar_init(&a_empty[i], 1);
-      }
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(&acc_full[i], 1);
-        mbar_init(&acc_empty[i], (kEpiWarps / 2) * 32);  // every epilogue warp of that buffer
-      }
-      fence_barrier_init();
-    }
-    __syncwarp();
-    tmem_alloc(tmem_slot, L::TMEM_COLS);
-  }
+  if (warp == kEpiWarps) tmem_alloc(tmem_slot, L::TMEM_COLS);
   // the planes were written and R read by ordinary accesses; the MMAs read the planes and the
   // row-tile loads overwrite R through the async proxy
   fence_proxy_async_smem();
@@ -264,25 +279,12 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
   if (warp == kEpiWarps) {
     // ---------------- producer: TMA of the row tiles (NS ahead), MMA issue (one thread)
     if (lane == 0) {
-      const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
       const uint32_t idesc = idesc_bf16_f32(kTileM, D);
       const uint32_t b_base = smem_u32(bsm);
-      const int n_mine = (r_ok && cta_k < tiles) ? (tiles - 1 - cta_k) / n_ctas + 1 : 0;
-      auto load = [&](int i) {  // tile i of this CTA into stage i % NS
-        const int st = i % L::NS;
-        mbar_arrive_expect_tx(&a_full[st], L::A_BYTES);
-        const int tile = cta_k + i * n_ctas;
-#pragma unroll
-        for (int c = 0; c < L::KCH; ++c) {
-          if (g.rph)
-            tma_load_3d_tc(asm_ + st * L::A_BYTES + c * kTileM * 128, tmap, 64 * c, hsel, tile * kTileM, &a_full[st]);
-          else
-            tma_load_2d_tc(asm_ + st * L::A_BYTES + c * kTileM * 128, tmap, 64 * c, tile * kTileM, &a_full[st]);
-        }
-      };
-      for (int i = 0; i < L::NS && i < n_mine; ++i) load(i);
+      const int n_run = r_ok ? n_mine : 0;
+      for (int i = n_early; i < L::NS && i < n_run; ++i) load(i);  // stages 2 .. NS-1, free of R now
       int i = 0;
-      for (; i < n_mine; ++i) {
+      for (; i < n_run; ++i) {
         const int st = i % L::NS;
         const int s = i & 1;  // TMEM buffer
         if (!mbar_wait_bounded(&a_full[st], (uint32_t)(i / L::NS) & 1, a.status)) break;
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
         tc_commit(&a_empty[st]);
         tc_commit(&acc_full[s]);
         // refill the stage of the previous tile (its MMAs were issued one tile ago)
-        if (i >= 1 && i - 1 + L::NS < n_mine) {
+        if (i >= 1 && i - 1 + L::NS < n_run) {
           const int pst = (i - 1) % L::NS;
           if (!mbar_wait_bounded(&a_empty[pst], (uint32_t)((i - 1) / L::NS) & 1, a.status)) break;
           load(i - 1 + L::NS);
