@@ -88,14 +88,24 @@ constexpr uint32_t kRoundBits = 0x4B400000u;   // its float pattern
 template <int D, bool IS_V>
 __device__ __forceinline__ void quant_group(const float (&y)[32], int gi, float clip, uint32_t (&words)[D / 16],
                                             uint32_t& szw) {
-  float mn = y[0], mx = y[0];
+  // the group's extremes as trees (depth 5, not a 31-long dependent chain; min and max are exact,
+  // so the order does not matter)
+  float tn[16], tx[16];
 #pragma unroll
-  for (int j = 1; j < 32; ++j) {
-    mn = fminf(mn, y[j]);
-    mx = fmaxf(mx, y[j]);
+  for (int j = 0; j < 16; ++j) {
+    tn[j] = fminf(y[2 * j], y[2 * j + 1]);
+    tx[j] = fmaxf(y[2 * j], y[2 * j + 1]);
   }
-  mn = fminf(fmaxf(mn, -clip), clip);
-  mx = fminf(fmaxf(mx, -clip), clip);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      tn[j] = fminf(tn[j], tn[j + w]);
+      tx[j] = fmaxf(tx[j], tx[j + w]);
+    }
+  }
+  const float mn = fminf(fmaxf(tn[0], -clip), clip);
+  const float mx = fminf(fmaxf(tx[0], -clip), clip);
   const uint16_t zb = bf16_bits_rn(mn);
   const uint16_t sb = bf16_bits_rn((mx - mn) / 3.0f);
   const float z = __uint_as_float(static_cast<uint32_t>(zb) << 16);
@@ -382,12 +392,14 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
 #pragma unroll
         for (int w = 0; w < D / 16; ++w) words[w] = 0u - code_bias<D, IS_V>(w, C_LO, C_HI);
 #pragma unroll
+        // a group's two accumulators are read from TMEM while the previous group is quantised
+        uint32_t r0[32], r1[32];
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(s * 2 * D);
+        tmem_ld32_nowait(lane_base + (uint32_t)(32 * CH * GPH), r0);
+        tmem_ld32_nowait(lane_base + (uint32_t)(32 * CH * GPH + D), r1);
+#pragma unroll
         for (int gq = 0; gq < GPH; ++gq) {
           const int gi = CH * GPH + gq;
-          uint32_t r0[32], r1[32];
-          const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(s * 2 * D + 32 * gi);
-          tmem_ld32_nowait(lane_base, r0);
-          tmem_ld32_nowait(lane_base + (uint32_t)D, r1);
           tmem_wait_ld();
           float y[32];
 #pragma unroll
@@ -396,6 +408,10 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
                                          make_float2(__uint_as_float(r1[j]), __uint_as_float(r1[j + 1])));
             y[j] = s2.x;
             y[j + 1] = s2.y;
+          }
+          if (gq + 1 < GPH) {
+            tmem_ld32_nowait(lane_base + (uint32_t)(32 * (gi + 1)), r0);
+            tmem_ld32_nowait(lane_base + (uint32_t)(32 * (gi + 1) + D), r1);
           }
           quant_group<D, IS_V>(y, gi, clip, words, szw[gi]);
         }
