@@ -88,24 +88,14 @@ constexpr uint32_t kRoundBits = 0x4B400000u;   // its float pattern
 template <int D, bool IS_V>
 __device__ __forceinline__ void quant_group(const float (&y)[32], int gi, float clip, uint32_t (&words)[D / 16],
                                             uint32_t& szw) {
-  // the group's extremes as trees (depth 5, not a 31-long dependent chain; min and max are exact,
-  // so the order does not matter)
-  float tn[16], tx[16];
+  float mn = y[0], mx = y[0];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    tn[j] = fminf(y[2 * j], y[2 * j + 1]);
-    tx[j] = fmaxf(y[2 * j], y[2 * j + 1]);
+  for (int j = 1; j < 32; ++j) {
+    mn = fminf(mn, y[j]);
+    mx = fmaxf(mx, y[j]);
   }
-#pragma unroll
-  for (int w = 8; w >= 1; w >>= 1) {
-#pragma unroll
-    for (int j = 0; j < w; ++j) {
-      tn[j] = fminf(tn[j], tn[j + w]);
-      tx[j] = fmaxf(tx[j], tx[j + w]);
-    }
-  }
-  const float mn = fminf(fmaxf(tn[0], -clip), clip);
-  const float mx = fminf(fmaxf(tx[0], -clip), clip);
+  mn = fminf(fmaxf(mn, -clip), clip);
+  mx = fminf(fmaxf(mx, -clip), clip);
   const uint16_t zb = bf16_bits_rn(mn);
   const uint16_t sb = bf16_bits_rn((mx - mn) / 3.0f);
   const float z = __uint_as_float(static_cast<uint32_t>(zb) << 16);
