@@ -13,8 +13,11 @@
 // token i0 + r / gq, head r % gq) and walks 64-key tiles: first the INT2 history tiles,
 // then the BF16 window tiles, then the chunk's own tiles.  Per tile:
 //   S = Q K^T into TMEM (two buffers, so the next tile's scores are computed while the
-//   softmax reads this tile's), softmax by the row's own thread, P to shared memory,
-//   O += P V into TMEM.
+//   softmax reads this tile's), softmax by the row's own thread, P back into TMEM over
+//   the tile's own scores (history tiles) or to shared memory (BF16 tiles), O += P V
+//   into TMEM.  History tiles take both A operands from TMEM (the rotated query planes,
+//   the weights), so the tensor core reads only the unpacked keys and values from shared
+//   memory, and their softmax waits for the previous tile's PV only to rescale.
 // History tiles run in the rotated basis with f16 operands, each dequantised value split
 // about its group's centre, z + c s = (z + 1.5 s) + (c - 1.5) s, so that the two parts do
 // not cancel in the float32 accumulators (a group straddling zero has z near -1.5 s):
@@ -37,8 +40,8 @@
 // Roles: warps 0-3 (softmax; thread r owns row r = TMEM lane r), warps 4-7 (unpack of
 // the next tile into the shared-memory operand tiles, INT2 pages staged one tile ahead
 // by cp.async), warp 8 (TMEM allocation, MMA issue).  The roles meet only at mbarriers:
-// kv_full (a stage unpacked), s_full (scores in TMEM), p_full (weights in shared
-// memory), pv_done and kv_empty (a tile's PV done, its stage free), so the scores of
+// kv_full (a stage unpacked), s_full (scores in TMEM), p_full (weights in place),
+// pv_done and kv_empty (a tile's PV done, its stage free), so the scores of
 // tile j are computed while the softmax works on tile j - 1.  Every wait is bounded by
 // %globaltimer: a timeout flags the status word and the CTA drains and exits.
 #include <cuda.h>
@@ -60,7 +63,7 @@ namespace {
 
 constexpr int kXRows = 128;                  // query rows per CTA (TMEM lanes)
 constexpr int kXKeys = 64;                   // keys per tile
-constexpr int kXThreads = 9 * 32;            // softmax 0-3, unpack 4-7, MMA 8
+constexpr int kXThreads = 9 * 32;            // softmax 0-3, unpack 4-7 (warp 4 also copies pages), MMA 8
 constexpr float kXLog2e = 1.4426950408889634f;
 constexpr float kXRescaleLog2 = 8.f;         // the reference moves when a score exceeds it by more
 constexpr float kXWeightShift = 6.f;         // weights 2^(s - m), m = reference - shift: at most 2^14
@@ -81,37 +84,47 @@ __device__ __forceinline__ void static_for(F&& f) {
 template <int D>
 struct XLayout {
   static constexpr int G = D / 32;
+  static constexpr int NST = 3;    // operand stages: tile j unpacked into stage j % NST
+  static constexpr int NRAW = 3;   // raw page buffers: tile j's pages requested NRAW - 1 tiles ahead
   static constexpr int Q_PLANE = kXRows * D * 2;
-  static constexpr int QHI = 0, QLO = Q_PLANE, QZ = 2 * Q_PLANE;   // QZ: [128][64] 16-bit, 16 columns used
-  static constexpr int QZ_BYTES = kXRows * 128;
+  static constexpr int QHI = 0;    // the BF16 query of the BF16 tiles (the rotated planes live in TMEM)
   static constexpr int KT = 0, KT_BYTES = kXKeys * D * 2;         // [64 keys][D]
   static constexpr int KZ = KT + KT_BYTES, KZ_BYTES = kXKeys * 128;  // [64 keys][64], 16 columns used
   static constexpr int VT = KZ + KZ_BYTES, VT_BYTES = D * kXKeys * 2;  // [D channels][64 keys]
   static constexpr int ZV = VT + VT_BYTES, ZV_BYTES = 16 * 128;   // [16 (groups, padded)][64 keys]
   static constexpr int STAGE = ZV + ZV_BYTES;
-  static constexpr int ST0 = QZ + QZ_BYTES;
-  static constexpr int P_BYTES = kXRows * kXKeys * 2;
-  static constexpr int PHI = ST0 + 2 * STAGE, PLO = PHI + P_BYTES, PLO2 = PLO + P_BYTES;
+  static constexpr int ST0 = QHI + Q_PLANE;
   static constexpr int RAW_BYTES = kXKeys * 3 * D / 4;           // 64 INT2 tokens: codes and (scale, zero) of K, V
-  static constexpr int RAW0 = PLO2 + P_BYTES;
-  static constexpr int BAR = RAW0 + 2 * RAW_BYTES;
-  static constexpr int BYTES = BAR + 8 * 8 + 16;   // s_full[2], pv_done, kv_full[2], kv_empty[2], p_full; tmem slot, abort
+  static constexpr int RAW0 = ST0 + NST * STAGE;
+  static constexpr int BAR = RAW0 + NRAW * RAW_BYTES;
+  // s_full[2], pv_done, kv_full[NST], kv_empty[NST], p_full[2], raw_full[NRAW]; then the TMEM
+  // slot, the abort flag
+  static constexpr int NBAR = 2 + 1 + 2 * NST + 2 + NRAW;
+  static constexpr int BYTES = BAR + NBAR * 8 + 16;
   static constexpr int SMEM = BYTES + 1024;
-  // epilogue reuse (after the last MMA): R_V^T [D][D] f32 over the Q planes, y [128][D+1] f32
-  // over the stages, 1/l [128] over the P planes
-  static constexpr int RT = 0, Y = ST0, LINV = PHI;
+  // epilogue reuse (after the last MMA): R_V^T [D][D] f32 from 0, then y [128][D+1] f32, then 1/l [128]
   static constexpr int YS = D + 1;
+  static constexpr int RT = 0, Y = (D * D * 4 + 1023) / 1024 * 1024, LINV = Y + kXRows * YS * 4;
   // TMEM columns
   // the V centre accumulator (16 columns) directly follows the rotated one: one PV MMA with
   // N = D + 16 reads the Zv rows that follow the Vt rows in shared memory
   static constexpr uint32_t C_S = 0, C_OROT = 2 * kXKeys, C_OZ = C_OROT + D, C_OPLAIN = C_OZ + 32;
   static constexpr uint32_t C_END = C_OPLAIN + D;
+  // While the INT2 tiles run, the plain output is not yet in use: its D columns hold the
+  // rotated query planes (hi, then lo: D / 2 columns each, a pair of channels per column),
+  // the A operand of the INT2 score MMAs; the group-sum operand (16 f16) follows C_END.
+  // The first BF16 tile's PV overwrites the plain output (its first MMA does not accumulate).
+  static constexpr uint32_t C_QHI = C_OPLAIN, C_QLO = C_OPLAIN + D / 2, C_QZ = C_END;
+  // Weights go back into TMEM over their tile's scores (a pair of keys per column: hi in the
+  // first 32 columns, lo in the next 32); a BF16 tile's third term (lo2) goes to C_P2 + 32 (j & 1),
+  // columns of the group-sum operand, which only the INT2 tiles before it read.
+  static constexpr uint32_t C_P2 = C_END;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(STAGE % 1024 == 0 && ST0 % 1024 == 0 && PHI % 1024 == 0, "operand tiles 1024-aligned");
-  static_assert(C_END <= TMEM_COLS, "TMEM plan");
+  static_assert(STAGE % 1024 == 0 && ST0 % 1024 == 0, "operand tiles 1024-aligned");
+  static_assert(C_QZ + 8 <= TMEM_COLS && C_P2 + kXKeys <= TMEM_COLS, "TMEM plan");
   static_assert(ZV == VT + D * 128, "Zv rows follow the Vt rows");
-  static_assert(D * (D + 0) * 4 <= ST0, "R_V^T fits over the Q planes");
-  static_assert(kXRows * YS * 4 <= 2 * STAGE, "y fits over the stages");
+  static_assert(LINV + kXRows * 4 <= RAW0, "R_V^T, y and 1/l fit below the raw buffers");
+  static_assert(RAW0 % 16 == 0 && RAW_BYTES % 16 == 0, "bulk copy destinations 16-byte aligned");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
@@ -193,14 +206,7 @@ __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
 }
 
 // ------------------------------------------------------------------ attention
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-// named barrier 1 among the 128 unpack threads
-__device__ __forceinline__ void unpack_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-// the same barrier, returning whether any of the 128 threads passed true
+// named barrier 1 among the 128 unpack threads, returning whether any of them passed true
 __device__ __forceinline__ bool unpack_bar_any(bool v) {
   uint32_t r;
   asm volatile(
@@ -290,12 +296,16 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   extern __shared__ __align__(1024) uint8_t x_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(x_smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* s_full = reinterpret_cast<uint64_t*>(smem + L::BAR);   // [2] scores of tile j in TMEM (commit)
-  uint64_t* pv_done = s_full + 2;      // PV of tile j done (commit)
-  uint64_t* kv_full = s_full + 3;      // [2] stage j & 1 holds tile j (128 unpack arrivals)
-  uint64_t* kv_empty = s_full + 5;     // [2] stage free again (commit after the tile's PV)
-  uint64_t* p_full = s_full + 7;       // weights of tile j in shared memory (128 softmax arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR + 64);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR + 68);
+  uint64_t* pv_done = s_full + 2;          // PV of tile j done (commit)
+  uint64_t* kv_full = s_full + 3;          // [NST] stage j % NST holds tile j (one arrival per unpack warp)
+  uint64_t* kv_empty = kv_full + L::NST;   // [NST] stage free again (commit after the tile's PV)
+  // [2] weights of tile j in place (one arrival per softmax warp), one barrier per tile parity: the
+  // softmax may finish tile j + 1 before the MMA thread has seen tile j's, never tile j + 2
+  // (its scores need tile j's PV issued first)
+  uint64_t* p_full = kv_empty + L::NST;
+  uint64_t* raw_full = p_full + 2;         // [NRAW] raw buffer j % NRAW holds INT2 tile j's pages (bulk copies)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR + 8 * L::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR + 8 * L::NBAR + 4);
 
   const Geom& g = a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -356,30 +366,32 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       mbar_init(&s_full[0], 1);
       mbar_init(&s_full[1], 1);
       mbar_init(pv_done, 1);
-      mbar_init(&kv_full[0], 128);
-      mbar_init(&kv_full[1], 128);
-      mbar_init(&kv_empty[0], 1);
-      mbar_init(&kv_empty[1], 1);
-      mbar_init(p_full, 128);
+      for (int st = 0; st < L::NST; ++st) {
+        mbar_init(&kv_full[st], 4);
+        mbar_init(&kv_empty[st], 1);
+      }
+      mbar_init(&p_full[0], 4);
+      mbar_init(&p_full[1], 4);
+      for (int rb = 0; rb < L::NRAW; ++rb) mbar_init(&raw_full[rb], 1);
       *abort_flag = 0;
       fence_barrier_init();
     }
     __syncwarp();
     tmem_alloc(tmem_slot, L::TMEM_COLS);
   }
-  // columns past the centre terms of both stages' Kz tiles stay zero (the query side's
+  // columns past the centre terms of every stage's Kz tile stay zero (the query side's
   // matching columns are zero too; a zero times a zero keeps the padding out of the scores)
   constexpr int PADC = 16 - kCentreTerms<G>() * G;
   if constexpr (PADC > 0) {
-    for (int idx = tid; idx < 2 * kXKeys * PADC; idx += kXThreads) {
+    for (int idx = tid; idx < L::NST * kXKeys * PADC; idx += kXThreads) {
       const int st = idx / (kXKeys * PADC), rem = idx % (kXKeys * PADC);
       const int key = rem / PADC, col = kCentreTerms<G>() * G + rem % PADC;
       *reinterpret_cast<__half*>(smem + L::ST0 + st * L::STAGE + L::KZ + sw128_offset(key, col, kXKeys)) =
           __float2half_rn(0.f);
     }
   }
-  // rows 2G..15 of both stages' Zv tiles stay zero (padding of the V centre term)
-  for (int idx = tid; idx < 2 * (16 - 2 * G) * 8; idx += kXThreads) {
+  // rows 2G..15 of every stage's Zv tile stay zero (padding of the V centre term)
+  for (int idx = tid; idx < L::NST * (16 - 2 * G) * 8; idx += kXThreads) {
     const int st = idx / ((16 - 2 * G) * 8), rem = idx % ((16 - 2 * G) * 8);
     const int row = 2 * G + rem / 8, ck = rem % 8;
     *reinterpret_cast<uint4*>(smem + L::ST0 + st * L::STAGE + L::ZV + sw128_offset(row, 8 * ck, 16)) =
@@ -400,7 +412,9 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 
   // Q planes for INT2 tiles: q' * 2^(e + 10 - pos) as f16 hi + lo, and the group sums
-  // Q_g * 2^e as three f16 terms; |q'| * 2^e < 32 keeps every operand below 2^15.
+  // Q_g * 2^e as three f16 terms; |q'| * 2^e < 32 keeps every operand below 2^15.  They
+  // go to this row's TMEM lane (column c of a plane: channels 2c, 2c + 1), the A operand
+  // of the INT2 score MMAs.
   auto write_q_rot = [&]() {
     const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.ws + a.qrot_off) + qrow * D);
     float mx = 0.f, qg[G];
@@ -421,28 +435,31 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       e = 5 - E;
     }
     F_rot = ldexpf(sm_log2, -e - a.k_exp_K);
-#pragma unroll 2
-    for (int m = 0; m < D / 8; ++m) {
-      const float f = ldexpf(1.f, e + 10 - slot_pos(m & 7));
-      float v[8];
-      if (row_ok) {
-        const float4 x0 = src[2 * m], x1 = src[2 * m + 1];
-        v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
-      } else {
+#pragma unroll 1
+    for (int mg = 0; mg < D / 32; ++mg) {   // 16 columns (32 channels) per store
+      uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = 0.f;
-      }
-      uint32_t hi[4], lo[4];
+      for (int mi = 0; mi < 4; ++mi) {
+        const int m = 4 * mg + mi;   // channels 8m .. 8m + 7: columns 4m .. 4m + 3
+        const float f = ldexpf(1.f, e + 10 - slot_pos(m & 7));
+        float v[8];
+        if (row_ok) {
+          const float4 x0 = src[2 * m], x1 = src[2 * m + 1];
+          v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+        } else {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float x0 = v[2 * k] * f, x1 = v[2 * k + 1] * f;
-        hi[k] = half2_bits(x0, x1);
-        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
-        lo[k] = half2_bits(x0 - hf.x, x1 - hf.y);
+          for (int k = 0; k < 8; ++k) v[k] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float x0 = v[2 * k] * f, x1 = v[2 * k + 1] * f;
+          hi[4 * mi + k] = half2_bits(x0, x1);
+          const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[4 * mi + k]));
+          lo[4 * mi + k] = half2_bits(x0 - hf.x, x1 - hf.y);
+        }
       }
-      const uint32_t off = sw128_offset(r, 8 * m, kXRows);
-      *reinterpret_cast<uint4*>(smem + L::QHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(smem + L::QLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      tmem_st16(lane_base + L::C_QHI + (uint32_t)(16 * mg), hi);
+      tmem_st16(lane_base + L::C_QLO + (uint32_t)(16 * mg), lo);
     }
     __half hz[16];
 #pragma unroll
@@ -458,36 +475,20 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
 #pragma unroll
       for (int tt = 0; tt < kCentreTerms<G>(); ++tt) hz[tt * G + gg] = qt[centre_q_term(tt)];
     }
-    const uint4* hz4 = reinterpret_cast<const uint4*>(hz);
-    *reinterpret_cast<uint4*>(smem + L::QZ + sw128_offset(r, 0, kXRows)) = hz4[0];
-    *reinterpret_cast<uint4*>(smem + L::QZ + sw128_offset(r, 8, kXRows)) = hz4[1];
+    uint32_t hz2[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      hz2[c] = static_cast<uint32_t>(__half_as_ushort(hz[2 * c])) |
+               (static_cast<uint32_t>(__half_as_ushort(hz[2 * c + 1])) << 16);
+    tmem_st8(lane_base + L::C_QZ, hz2);
   };
-  // Q plane for BF16 tiles: the BF16 query itself (the lo plane stays zero and is skipped)
+  // Q plane for BF16 tiles, in shared memory: the BF16 query itself (exact in one plane)
   auto write_q_plain = [&]() {
-#pragma unroll 2
+#pragma unroll 4
     for (int m = 0; m < D / 8; ++m) {
-      float v[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = 0.f;
-      if (row_ok) {
-        const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + qrow * D + 8 * m);
-        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          v[2 * k] = bf16_lo(ws4[k]);
-          v[2 * k + 1] = bf16_hi(ws4[k]);
-        }
-      }
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float h0 = bf16_round_f(v[2 * k]), h1 = bf16_round_f(v[2 * k + 1]);
-        hi[k] = pack_bf162(h0, h1);
-        lo[k] = pack_bf162(v[2 * k] - h0, v[2 * k + 1] - h1);
-      }
-      const uint32_t off = sw128_offset(r, 8 * m, kXRows);
-      *reinterpret_cast<uint4*>(smem + L::QHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(smem + L::QLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      const uint4 w = row_ok ? *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + qrow * D + 8 * m)
+                             : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(smem + L::QHI + sw128_offset(r, 8 * m, kXRows)) = w;
     }
   };
 
@@ -497,47 +498,64 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   // INT2 pages of tile j into raw buffer j & 1 (one cp.async group per call, possibly empty)
   // page sizes are powers of two (16, 32, 64): block and slot of a key by shift and mask
   const int pshift = __ffs(g.P) - 1, pmask = g.P - 1, nblk = kXKeys >> pshift;
-  // page ids of tile j's blocks (-1: block outside the history), read one tile ahead of
-  // their copies so that the block-table load latency stays off the unpack path
   constexpr int kMaxBlk = kXKeys / 16;
-  auto load_pages = [&](int j, int (&pg)[kMaxBlk]) {
-#pragma unroll
-    for (int bi = 0; bi < kMaxBlk; ++bi) pg[bi] = -1;
-    if (j < n_tiles && tl.kind(j) == kTileInt2) {
-      const int base = tl.base(j);
-#pragma unroll
-      for (int bi = 0; bi < kMaxBlk; ++bi) {
-        const int p0 = base + (bi << pshift);
-        if (bi >= nblk || p0 + g.P <= tl.S || p0 >= tl.hist_end) continue;
-        const int lp = p0 >> pshift;
-        pg[bi] = (lp < a.bt_stride && lp < g.max_pages_per_req) ? a.block_table[(size_t)b * a.bt_stride + lp] : -2;
-      }
-    }
+  // Page ids for the copying warp (warp 4): lane l holds the id of logical page 32 w + l of the
+  // request's block table for the current 32-page window w (pid_cur) and for the next one
+  // (pid_nxt, loaded a window ahead, so that its latency stays off the copy path).  -1: the
+  // page holds no history token; -2: outside the block table.
+  auto page_id_at = [&](int lp) -> int {
+    const int p0 = lp << pshift;
+    if (p0 + g.P <= tl.S || p0 >= tl.hist_end) return -1;
+    return (lp < a.bt_stride && lp < g.max_pages_per_req) ? a.block_table[(size_t)b * a.bt_stride + lp] : -2;
   };
-  // INT2 pages of tile j into raw buffer j & 1 (one cp.async group per call, possibly empty)
-  auto issue_raw = [&](int j, const int (&pg)[kMaxBlk]) {
-    if (j < n_tiles && tl.kind(j) == kTileInt2) {
-      uint8_t* dst0 = smem + L::RAW0 + (j & 1) * L::RAW_BYTES;
-#pragma unroll
-      for (int bi = 0; bi < kMaxBlk; ++bi) {
-        const int page = pg[bi];
-        if (bi >= nblk || page == -1) continue;
-        if (page < 0 || page >= g.num_pages) {
-          if (u == 0) flag_error(a.status, kDevBadPage);
-          continue;
-        }
-        const uint8_t* src = pool_l + ((size_t)page * g.Hkv + kvh) * BB;
-        uint8_t* dst = dst0 + bi * BB;
-        for (int c = u; c < (int)(BB / 16); c += 128) cp_async16(dst + 16 * c, src + 16 * c);
-      }
+  int pid_cur = -1, pid_nxt = -1, win_cur = -2;
+  // (copying warp, every lane) the page ids of INT2 tile j's blocks: nblk consecutive pages
+  // from lp0, a multiple of nblk, so inside one window
+  auto tile_pages = [&](int j, int (&pg)[kMaxBlk]) {
+    const int lp0 = tl.base(j) >> pshift;
+    const int w = lp0 >> 5;
+    if (w != win_cur) {
+      pid_cur = w == win_cur + 1 ? pid_nxt : page_id_at(32 * w + lane);
+      pid_nxt = page_id_at(32 * (w + 1) + lane);
+      win_cur = w;
     }
-    cp_async_commit();
+#pragma unroll
+    for (int bi = 0; bi < kMaxBlk; ++bi) pg[bi] = __shfl_sync(0xffffffffu, pid_cur, (lp0 + bi) & 31);
+  };
+  // INT2 pages of tile j into raw buffer j % NRAW: one bulk copy per page block, issued by
+  // lane 0 of the copying warp, completing on raw_full[j % NRAW] (an empty arrival when no
+  // block is valid).  Every unpack thread has left the buffer's previous tile behind: the
+  // caller passed the unpack barrier after that tile.
+  auto issue_raw = [&](int j, const int (&pg)[kMaxBlk]) {
+    if (j >= tl.nR) return;
+    uint8_t* dst0 = smem + L::RAW0 + (j % L::NRAW) * L::RAW_BYTES;
+    uint64_t* bar = &raw_full[j % L::NRAW];
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int bi = 0; bi < kMaxBlk; ++bi) {
+      const int page = pg[bi];
+      if (bi >= nblk || page == -1) continue;
+      if (page < 0 || page >= g.num_pages) {
+        flag_error(a.status, kDevBadPage);
+        continue;
+      }
+      bytes += (uint32_t)BB;
+    }
+    mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+    for (int bi = 0; bi < kMaxBlk; ++bi) {
+      const int page = pg[bi];
+      if (bi >= nblk || page < 0 || page >= g.num_pages) continue;
+      bulk_g2s(dst0 + bi * BB, pool_l + ((size_t)page * g.Hkv + kvh) * BB, (uint32_t)BB, bar);
+    }
   };
   auto unpack_int2 = [&](int j, uint8_t* stg) {
     const int base = tl.base(j);
-    const uint8_t* raw = smem + L::RAW0 + (j & 1) * L::RAW_BYTES;
+    const uint8_t* raw = smem + L::RAW0 + (j % L::NRAW) * L::RAW_BYTES;
     const uint32_t magic = a.code_magic;
-    // K codes -> code * s * 2^(k_K + pos - 10); thread (key, w) writes channels [64w, 64w + 64)
+    // K codes -> code * s * 2^(k_K + pos - 10); thread (key, w) writes channels [64w, 64w + 64),
+    // groups 2w and 2w + 1, and those groups' centres m = z + 1.5 s: Kz row key, column t G + g
+    // holds term centre_z_term(t) of m (the query side matches it)
     if (u < kXKeys * (D / 64)) {
       const int key = u / (D / 64), w = u % (D / 64);
       const bool ok = hist_ok(base + key);
@@ -553,8 +571,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
 #pragma unroll
       for (int gg = 0; gg < G; ++gg)
         szw[gg] = *reinterpret_cast<const uint32_t*>(kb + g.k_sz_off() + slot * (D / 8) + gg * 4);
-      const uint32_t sA = (D == 128 && w) ? szw[G - 2] : szw[0];
-      const uint32_t sB = (D == 128 && w) ? szw[G - 1] : szw[1];
+      const int gA = 2 * w;
+      const uint32_t sA = szw[gA], sB = szw[gA + 1];
       const uint32_t nA = ok ? half2_bits(neg_scale_times_pow2(sA, kK23), neg_scale_times_pow2(sA, kK23)) : 0u;
       const uint32_t nB = ok ? half2_bits(neg_scale_times_pow2(sB, kK23), neg_scale_times_pow2(sB, kK23)) : 0u;
       static_for<8>([&](auto X) {
@@ -568,6 +586,15 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         c.w = centre_codes(scale_codes(magic_slot<x>(wd[3], w6[3], magic), n2), n2, kc);
         *reinterpret_cast<uint4*>(stg + L::KT + sw128_offset(key, 8 * (8 * w + x), kXKeys)) = c;
       });
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        __half mh, ml;
+        centre_hi_lo(ok ? (e ? sB : sA) : 0u, kK23, mh, ml);
+        const __half mt[2] = {mh, ml};
+#pragma unroll
+        for (int tt = 0; tt < kCentreTerms<G>(); ++tt)
+          *reinterpret_cast<__half*>(stg + L::KZ + sw128_offset(key, tt * G + gA + e, kXKeys)) = mt[centre_z_term(tt)];
+      }
     }
     // V codes -> code * s_V * 2^(k_V + pos - 10), transposed: thread (half-word hw, keys 8kb..8kb+7)
     if (u < (D / 8) * 8) {
@@ -606,29 +633,18 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         c.w = centre_codes(scale_codes(magic_slot<s>(W[3], W6[3], magic), s < 4 ? nA[3] : nB[3]), s < 4 ? nA[3] : nB[3], kc);
         *reinterpret_cast<uint4*>(stg + L::VT + sw128_offset(chbase + 8 * s, 8 * kb8, D)) = c;
       });
-    }
-    // group centres m = z + 1.5 s of K and V: one (key, group) item per thread and step.
-    // K: Kz row key, column t G + g holds term centre_z_term(t) of m (the query side matches it);
-    // V: Zv rows g (hi) and G + g (lo), column key.
-    for (int item = u; item < 2 * kXKeys * G; item += 128) {
-      const bool is_v = item >= kXKeys * G;
-      const int rem = is_v ? item - kXKeys * G : item;
-      const int key = rem / G, gg = rem % G;
-      const bool ok = hist_ok(base + key);
-      const uint8_t* kb = raw + (key >> pshift) * BB;
-      const int slot = key & pmask;
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(kb + (is_v ? g.v_sz_off() : g.k_sz_off()) + slot * (D / 8) +
-                                                            gg * 4);
-      __half mh, ml;
-      centre_hi_lo(ok ? w : 0u, is_v ? kV23 : kK23, mh, ml);
-      if (!is_v) {
-        const __half mt[2] = {mh, ml};
+      // the centres of groups gA, gA + 1 for one key each of the 8 threads that share kb8 and
+      // gA: Zv rows g (hi) and G + g (lo), column key
+      const int ckey = 8 * kb8 + hw / (D / 64);
+      const bool cok = hist_ok(base + ckey);
+      const uint32_t* cszr = reinterpret_cast<const uint32_t*>(raw + (ckey >> pshift) * BB + g.v_sz_off() +
+                                                               (ckey & pmask) * (D / 8));
 #pragma unroll
-        for (int tt = 0; tt < kCentreTerms<G>(); ++tt)
-          *reinterpret_cast<__half*>(stg + L::KZ + sw128_offset(key, tt * G + gg, kXKeys)) = mt[centre_z_term(tt)];
-      } else {
-        *reinterpret_cast<__half*>(stg + L::ZV + sw128_offset(gg, key, 16)) = mh;
-        *reinterpret_cast<__half*>(stg + L::ZV + sw128_offset(G + gg, key, 16)) = ml;
+      for (int e = 0; e < 2; ++e) {
+        __half mh, ml;
+        centre_hi_lo(cok ? cszr[gA + e] : 0u, kV23, mh, ml);
+        *reinterpret_cast<__half*>(stg + L::ZV + sw128_offset(gA + e, ckey, 16)) = mh;
+        *reinterpret_cast<__half*>(stg + L::ZV + sw128_offset(G + gA + e, ckey, 16)) = ml;
       }
     }
   };
@@ -688,57 +704,77 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       }
     }
   };
-  auto unpack = [&](int j) {
-    uint8_t* stg = smem + L::ST0 + (j & 1) * L::STAGE;
-    if (tl.kind(j) == kTileInt2) unpack_int2(j, stg); else unpack_plain(j, stg);
+  // tile j into stage j % NST; false when an INT2 tile's pages did not arrive in time (the
+  // status word is flagged; the caller stops at its next barrier)
+  auto unpack = [&](int j) -> bool {
+    uint8_t* stg = smem + L::ST0 + (j % L::NST) * L::STAGE;
+    if (tl.kind(j) != kTileInt2) {
+      unpack_plain(j, stg);
+      return true;
+    }
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&raw_full[j % L::NRAW], (uint32_t)((j / L::NRAW) & 1), a.status)))
+      return false;
+    unpack_int2(j, stg);
+    return true;
   };
 
   // ---------------- MMA issue (warp 8, lane 0)
   const uint32_t sbase = smem_u32(smem);
   // descriptors: the start-address field is (address >> 4) in the low 14 bits, so an
   // offset inside a tile is added to a base descriptor directly
-  const uint64_t dQHI = smem_desc_sw128(sbase + L::QHI), dQLO = smem_desc_sw128(sbase + L::QLO);
-  const uint64_t dQZ = smem_desc_sw128(sbase + L::QZ);
-  const uint64_t dP[3] = {smem_desc_sw128(sbase + L::PHI), smem_desc_sw128(sbase + L::PLO),
-                          smem_desc_sw128(sbase + L::PLO2)};
+  const uint64_t dQHI = smem_desc_sw128(sbase + L::QHI);
   const uint64_t dST = smem_desc_sw128(sbase + L::ST0);
   auto dadd = [](uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); };
   auto issue_qk = [&](int j) {
-    const uint32_t soff = (uint32_t)((j & 1) * L::STAGE);
+    const uint32_t soff = (uint32_t)((j % L::NST) * L::STAGE);
     const uint32_t dS = tmem + L::C_S + (uint32_t)((j & 1) * kXKeys);
-    const bool rot = tl.kind(j) == kTileInt2;
-    const uint32_t idesc = rot ? idesc_f16_f32(kXRows, kXKeys) : idesc_bf16_f32(kXRows, kXKeys);
-    // the BF16 query is exact in one plane: the plain tiles skip the lo plane
-    const int planes = rot ? 2 : 1;
+    if (tl.kind(j) == kTileInt2) {
+      // A = the rotated query planes in TMEM (8 columns per K = 16 step), B = the key tile
+      const uint32_t idesc = idesc_f16_f32(kXRows, kXKeys);
 #pragma unroll
-    for (int pl = 0; pl < 2; ++pl)
-      if (pl < planes)
+      for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t bk = (uint32_t)((kk >> 2) * kXKeys * 128 + (kk & 3) * 32);
+          tc_mma_ts(dS, tmem + (pl ? L::C_QLO : L::C_QHI) + (uint32_t)(8 * kk), dadd(dST, soff + L::KT + bk), idesc,
+                    (pl | kk) ? 1u : 0u);
+        }
+      tc_mma_ts(dS, tmem + L::C_QZ, dadd(dST, soff + L::KZ), idesc, 1u);
+    } else {
+      // the BF16 query, exact in one plane, from shared memory
+      const uint32_t idesc = idesc_bf16_f32(kXRows, kXKeys);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ak = (uint32_t)((kk >> 2) * kXRows * 128 + (kk & 3) * 32);
         const uint32_t bk = (uint32_t)((kk >> 2) * kXKeys * 128 + (kk & 3) * 32);
-        tc_mma(dS, dadd(pl ? dQLO : dQHI, ak), dadd(dST, soff + L::KT + bk), idesc, (pl | kk) ? 1u : 0u);
+        tc_mma(dS, dadd(dQHI, ak), dadd(dST, soff + L::KT + bk), idesc, kk ? 1u : 0u);
       }
-    if (rot) tc_mma(dS, dQZ, dadd(dST, soff + L::KZ), idesc, 1u);
+    }
   };
   auto issue_pv = [&](int j) {
-    const uint32_t soff = (uint32_t)((j & 1) * L::STAGE);
+    const uint32_t soff = (uint32_t)((j % L::NST) * L::STAGE);
     if (tl.kind(j) == kTileInt2) {
+      // A = the weights, written by the softmax over this tile's scores in TMEM (hi in the
+      // first 32 columns, lo in the next 32; a pair of keys per column)
+      const uint32_t pcol = tmem + L::C_S + (uint32_t)((j & 1) * kXKeys);
 #pragma unroll
       for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
-        for (int kk = 0; kk < kXKeys / 16; ++kk) {
-          const uint64_t pa = dadd(dP[pl], kk * 32);
-          tc_mma(tmem + L::C_OROT, pa, dadd(dST, soff + L::VT + kk * 32), idesc_f16_f32(kXRows, D + 16), 1u);
-        }
+        for (int kk = 0; kk < kXKeys / 16; ++kk)
+          tc_mma_ts(tmem + L::C_OROT, pcol + (uint32_t)(32 * pl + 8 * kk), dadd(dST, soff + L::VT + kk * 32),
+                    idesc_f16_f32(kXRows, D + 16), 1u);
     } else {
-      // P as three BF16 terms (24 bits): window and chunk values are unbounded BF16
+      // P as three BF16 terms (24 bits): window and chunk values are unbounded BF16.  The
+      // first BF16 tile starts the plain accumulator, whose columns held the query planes.
+      const uint32_t pcol = tmem + L::C_S + (uint32_t)((j & 1) * kXKeys);
+      const uint32_t p2col = tmem + L::C_P2 + (uint32_t)((j & 1) * (kXKeys / 2));
 #pragma unroll
       for (int pl = 0; pl < 3; ++pl)
 #pragma unroll
         for (int kk = 0; kk < kXKeys / 16; ++kk)
-          tc_mma(tmem + L::C_OPLAIN, dadd(dP[pl], kk * 32), dadd(dST, soff + L::VT + kk * 32),
-                 idesc_bf16_f32(kXRows, D), 1u);
+          tc_mma_ts(tmem + L::C_OPLAIN, (pl < 2 ? pcol + (uint32_t)(32 * pl) : p2col) + (uint32_t)(8 * kk),
+                    dadd(dST, soff + L::VT + kk * 32), idesc_bf16_f32(kXRows, D),
+                    (j == tl.nR && pl == 0 && kk == 0) ? 0u : 1u);
     }
   };
 
@@ -753,8 +789,6 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     tmem_ld32_nowait(lane_base + L::C_S + (uint32_t)((i & 1) * kXKeys), s0);
     tmem_ld32_nowait(lane_base + L::C_S + (uint32_t)((i & 1) * kXKeys + 32), s1);
     tmem_wait_ld();
-    // the last INT2 tile's scores are read: the Q planes take the plain query for the BF16 tiles
-    if (i == tl.nR - 1) write_q_plain();
     int a0 = 0, a1 = 0, b0 = 0, b1 = 0;   // visible keys [a0, a1) U [b0, b1)
     if (kind == kTileInt2) {
       a0 = max(0, tl.S - base);
@@ -791,15 +825,23 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       m_ref = nm;
       thr = nm + kXWeightShift + kXRescaleLog2;
     }
-    // the P buffer and the accumulators are free once the previous tile's PV is done
-    if (i >= 1 && !__all_sync(0xffffffffu, xwait(pv_done, (uint32_t)((i - 1) & 1), a.status)))
+    // The weights go over the tile's own scores in TMEM, so only a rescale of the
+    // accumulators waits for the previous tile's PV.  (A tile's scores are complete only
+    // after every MMA issued before them, so tile i - 2's PV is done by now and the parity
+    // wait below cannot pass on an older phase.)
+    const bool resc = alpha != 1.f && l_run > 0.f;
+    const bool any_resc = __any_sync(0xffffffffu, resc);
+    if (i >= 1 && any_resc &&
+        !__all_sync(0xffffffffu, xwait(pv_done, (uint32_t)((i - 1) & 1), a.status)))
       return false;
     tc_fence_after();
-    const bool resc = alpha != 1.f && l_run > 0.f;
-    if (__any_sync(0xffffffffu, resc)) {
+    if (any_resc) {
       const float f = resc ? alpha : 1.f;
+      // the plain accumulator holds partial sums only after the first BF16 tile's PV
+      // (until then its columns are the query planes)
+      const uint32_t c_end = i > tl.nR ? L::C_END : L::C_OPLAIN;
 #pragma unroll 1
-      for (uint32_t c = L::C_OROT; c < L::C_END; c += 32) {
+      for (uint32_t c = L::C_OROT; c < c_end; c += 32) {
         uint32_t o[32];
         tmem_ld32_nowait(lane_base + c, o);
         tmem_wait_ld();
@@ -816,67 +858,74 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     // terms below carry 22 or 24 bits of each)
     float lsum = 0.f;
     if (kind == kTileInt2) {
+      // f16 hi / lo of the weights into this tile's score columns: column q of a plane holds
+      // keys 2q, 2q + 1 (hi in columns 0..31, lo in 32..63)
+      const uint32_t pcol = lane_base + L::C_S + (uint32_t)((i & 1) * kXKeys);
 #pragma unroll
-      for (int c = 0; c < kXKeys / 8; ++c) {
-        uint32_t hi[4], lo[4];
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float p0 = ex2(fmaf(sc[8 * c + 2 * k], F, negm)), p1 = ex2(fmaf(sc[8 * c + 2 * k + 1], F, negm));
-          hi[k] = half2_bits(p0, p1);
-          const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
-          lo[k] = half2_bits(p0 - hf.x, p1 - hf.y);
+        for (int q = 0; q < 16; ++q) {
+          const int k0 = 32 * hf + 2 * q;
+          const float p0 = ex2(fmaf(sc[k0], F, negm)), p1 = ex2(fmaf(sc[k0 + 1], F, negm));
+          hi[q] = half2_bits(p0, p1);
+          const float2 hv = __half22float2(*reinterpret_cast<const __half2*>(&hi[q]));
+          lo[q] = half2_bits(p0 - hv.x, p1 - hv.y);
           lsum += p0 + p1;
         }
-        const uint32_t off = sw128_offset(r, 8 * c, kXRows);
-        *reinterpret_cast<uint4*>(smem + L::PHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(smem + L::PLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        tmem_st16(pcol + (uint32_t)(16 * hf), hi);
+        tmem_st16(pcol + (uint32_t)(32 + 16 * hf), lo);
       }
+      tmem_wait_st();
     } else {
+      // three BF16 terms of the weights (24 bits: window and chunk values are unbounded BF16)
+      const uint32_t pcol = lane_base + L::C_S + (uint32_t)((i & 1) * kXKeys);
+      const uint32_t p2col = lane_base + L::C_P2 + (uint32_t)((i & 1) * (kXKeys / 2));
 #pragma unroll
-      for (int c = 0; c < kXKeys / 8; ++c) {
+      for (int qt = 0; qt < 8; ++qt) {
         uint32_t hi[4], lo[4], lo2[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float p0 = ex2(fmaf(sc[8 * c + 2 * k], F, negm)), p1 = ex2(fmaf(sc[8 * c + 2 * k + 1], F, negm));
+        for (int q = 0; q < 4; ++q) {
+          const int k0 = 8 * qt + 2 * q;
+          const float p0 = ex2(fmaf(sc[k0], F, negm)), p1 = ex2(fmaf(sc[k0 + 1], F, negm));
           const float h0 = bf16_round_f(p0), h1 = bf16_round_f(p1);
           const float l0 = bf16_round_f(p0 - h0), l1 = bf16_round_f(p1 - h1);
-          hi[k] = pack_bf162(h0, h1);
-          lo[k] = pack_bf162(l0, l1);
-          lo2[k] = pack_bf162(p0 - h0 - l0, p1 - h1 - l1);
+          hi[q] = pack_bf162(h0, h1);
+          lo[q] = pack_bf162(l0, l1);
+          lo2[q] = pack_bf162(p0 - h0 - l0, p1 - h1 - l1);
           lsum += p0 + p1;
         }
-        const uint32_t off = sw128_offset(r, 8 * c, kXRows);
-        *reinterpret_cast<uint4*>(smem + L::PHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(smem + L::PLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        *reinterpret_cast<uint4*>(smem + L::PLO2 + off) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+        tmem_st4(pcol + (uint32_t)(4 * qt), hi);
+        tmem_st4(pcol + (uint32_t)(32 + 4 * qt), lo);
+        tmem_st4(p2col + (uint32_t)(4 * qt), lo2);
       }
+      tmem_wait_st();
     }
     l_run += lsum;
     return true;
   };
 
-  int pg_next[kMaxBlk];   // unpack threads: page ids of the tile after the next
-  // ---------------- preamble: zero the output accumulators, query planes, first tile
+  int raw_issued = 0;     // copying warp: INT2 tiles [0, raw_issued) requested
+  int raw_done = 0;       // its lane 0: INT2 tiles [0, raw_done) arrived (waited on)
+  // ---------------- preamble: zero the output accumulators, query planes, first pages
   if (warp < 4) {
     uint32_t z[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) z[k] = 0u;
 #pragma unroll 1
-    for (uint32_t c = L::C_OROT; c < L::C_END; c += 32) tmem_st32(lane_base + c, z);
+    for (uint32_t c = L::C_OROT; c < L::C_OPLAIN; c += 32) tmem_st32(lane_base + c, z);
+    if (tl.nR > 0) write_q_rot();
+    write_q_plain();
     tmem_wait_st();
-    if (tl.nR > 0) write_q_rot(); else write_q_plain();
-  } else if (warp < 8) {
-    int pg[kMaxBlk];
-    load_pages(0, pg);
-    issue_raw(0, pg);
-    load_pages(1, pg);
-    cp_async_wait0();
-    unpack_bar();
-    issue_raw(1, pg);
-    load_pages(2, pg_next);
-    unpack(0);
-    fence_proxy_async_smem();
-    mbar_arrive(&kv_full[0]);
+  } else if (warp == 4) {
+    // the pages of the first NRAW - 1 tiles (the loop requests tile j + NRAW - 1 at tile j)
+#pragma unroll 1
+    for (int t = 0; t < L::NRAW - 1 && t < tl.nR; ++t) {
+      int pg[kMaxBlk];
+      tile_pages(t, pg);
+      if (lane == 0) issue_raw(t, pg);
+    }
+    raw_issued = min(L::NRAW - 1, tl.nR);
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -895,40 +944,52 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         aborted = true;
         break;
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[i & 1]);
     }
   } else if (warp < 8) {
-    for (int j = 1; j < n_tiles; ++j) {
-      cp_async_wait0();
-      // stage j & 1 was last read by tile j - 2's MMAs
-      const bool ok = j < 2 || xwait(&kv_empty[j & 1], (uint32_t)(((j >> 1) - 1) & 1), a.status);
-      // one named barrier per tile: every copy of tile j has landed, every thread is done with
-      // tile j - 1's raw buffer, and all agree on whether to stop
+    for (int j = 0; j < n_tiles; ++j) {
+      // stage j % NST was last read by tile j - NST's MMAs
+      const bool ok = j < L::NST || xwait(&kv_empty[j % L::NST], (uint32_t)(((j / L::NST) - 1) & 1), a.status);
+      // one named barrier per tile: every thread is done with tile j - 1 (so its raw buffer
+      // may take tile j + NRAW - 1), and all agree on whether to stop
       if (unpack_bar_any(!ok || *abort_flag != 0)) {
         *abort_flag = 1;
         aborted = true;
         break;
       }
-      issue_raw(j + 1, pg_next);
-      load_pages(j + 2, pg_next);
-      unpack(j);
+      if (warp == 4 && j + L::NRAW - 1 < tl.nR) {
+        int pg[kMaxBlk];
+        tile_pages(j + L::NRAW - 1, pg);
+        if (lane == 0) issue_raw(j + L::NRAW - 1, pg);
+        raw_issued = j + L::NRAW;
+      }
+      // a late page flags the CTA to stop at the next barrier (every thread still reaches it)
+      if (unpack(j)) {
+        if (j < tl.nR) raw_done = j + 1;
+      } else {
+        *abort_flag = 1;
+      }
       fence_proxy_async_smem();
-      mbar_arrive(&kv_full[j & 1]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&kv_full[j % L::NST]);
     }
-    cp_async_wait0();
-  } else if (lane == 0) {
-    // MMA issue: the scores of tile qk (its stage unpacked; the S buffer free once the weights
-    // of tile qk - 2 are out; at tile nR the query planes switch, after tile nR - 1's
-    // softmax) and the PV of tile pv (its weights in place), whichever is ready first
+    // no bulk copy may still be writing this CTA's shared memory when it exits (bounded waits)
+    if (u == 0)
+      for (int t = raw_done; t < raw_issued; ++t)
+        (void)mbar_wait_bounded(&raw_full[t % L::NRAW], (uint32_t)((t / L::NRAW) & 1), nullptr);
+  } else if (warp == 8 && lane == 0) {
+    // MMA issue: the scores of tile qk (its stage unpacked; its S buffer, which holds tile
+    // qk - 2's weights, free once that tile's PV is issued: the MMAs run in issue order) and
+    // the PV of tile pv (its weights in place), whichever is ready first
     int qk = 0, pv = 0;
     int last_commit = -1;   // 0: s_full of tile qk - 1, 1: pv_done of tile pv - 1
     uint64_t t_last = globaltimer_ns();
     while (pv < n_tiles) {
       bool progressed = false;
-      if (qk < n_tiles && pv >= qk - 1 && (qk != tl.nR || pv >= tl.nR) &&
-          mbar_try_wait(&kv_full[qk & 1], (uint32_t)((qk >> 1) & 1))) {
+      if (qk < n_tiles && pv >= qk - 1 &&
+          mbar_try_wait(&kv_full[qk % L::NST], (uint32_t)((qk / L::NST) & 1))) {
         tc_fence_after();
         issue_qk(qk);
         tc_commit(&s_full[qk & 1]);
@@ -936,11 +997,11 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         ++qk;
         progressed = true;
       }
-      if (pv < qk && mbar_try_wait(p_full, (uint32_t)(pv & 1))) {
+      if (pv < qk && mbar_try_wait(&p_full[pv & 1], (uint32_t)((pv >> 1) & 1))) {
         tc_fence_after();
         issue_pv(pv);
         tc_commit(pv_done);
-        if (pv + 1 < n_tiles) tc_commit(&kv_empty[pv & 1]);
+        if (pv + L::NST < n_tiles) tc_commit(&kv_empty[pv % L::NST]);
         last_commit = 1;
         ++pv;
         progressed = true;
