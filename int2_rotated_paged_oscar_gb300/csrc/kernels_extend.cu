@@ -223,31 +223,11 @@ __device__ __forceinline__ float bf16_round_f(float x) { return __bfloat162float
 // 2^e for e in the float32 normal range
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
 
-// Bounded mbarrier wait that lets the waiting warp sleep (try_wait with a suspend-time hint:
-// the thread resumes when the phase completes or after the hint), so waiting roles leave
-// the issue slots to the working ones.  Gives up after kWaitLimitNs like mbar_wait_bounded.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
-      : "memory");
-  return ok != 0;
-}
+// Bounded mbarrier wait for the role warps: the waiting thread is suspended in the barrier
+// (try_wait with a suspend-time hint) rather than spinning, so it leaves the issue slots to
+// the working warps; the limit is kWaitLimitNs as for every wait.
 __device__ __forceinline__ bool xwait(uint64_t* bar, uint32_t parity, int* status) {
-  if (mbar_try_wait_sleep(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    __nanosleep(64);   // leave the issue slots to the warps doing work
-    if (mbar_try_wait_sleep(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      flag_error(status, kDevTimeout);
-      return false;
-    }
-  }
+  return mbar_wait_sleep_bounded(bar, parity, status);
 }
 
 // f16 pair (1.5 * 2^(pos - 10), same): the centring constant of a code slot at bit pos
@@ -712,7 +692,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       unpack_plain(j, stg);
       return true;
     }
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&raw_full[j % L::NRAW], (uint32_t)((j / L::NRAW) & 1), a.status)))
+    if (!__all_sync(0xffffffffu, xwait(&raw_full[j % L::NRAW], (uint32_t)((j / L::NRAW) & 1), a.status)))
       return false;
     unpack_int2(j, stg);
     return true;
