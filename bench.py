@@ -588,15 +588,15 @@ def long_and_capacity(osc, hbm_peak, steps=5, row_shift=37):
                                   "gbs": B * n * 8 * 2 * (128 * 2 + 48) / (wms * 1e-3) / 1e9,
                                   "frac_of_peak": B * n * 8 * 2 * (128 * 2 + 48) / (wms * 1e-3) / 1e9 / hbm_peak}
 
-    # the same write with the rotation H_Had . P_br alone (fast Walsh-Hadamard transform on CUDA cores)
-    def write_fwht():
+    # the same write with the rotation H_Had . P_br alone (one exact +-1 BF16 plane on tcgen05)
+    def write_hadamard():
         osc.oscar_write_kv_hadamard(ctx, 0, kd, vd, osc.DTYPE_BF16, cu, start, B, B * n, fx["clip_K"], fx["clip_V"],
                                     bt, ppr, slots)
-    write_fwht()
+    write_hadamard()
     torch.cuda.synchronize()
     e0.record()
     for _ in range(5):
-        write_fwht()
+        write_hadamard()
     e1.record()
     torch.cuda.synchronize()
     hms = e0.elapsed_time(e1) / 5
@@ -1106,8 +1106,9 @@ def write_leg(osc, hbm_peak, batch=8, n=32768, reps=5):
     forms = {
         "dense_tensor_core": lambda: osc.oscar_write_kv(ctx, 0, kd, vd, osc.DTYPE_BF16, cu, start, batch, batch * n, rk,
                                                         rv, fx["clip_K"], fx["clip_V"], bt, ppr, slots),
-        "hadamard_fwht": lambda: osc.oscar_write_kv_hadamard(ctx, 0, kd, vd, osc.DTYPE_BF16, cu, start, batch, batch * n,
-                                                             fx["clip_K"], fx["clip_V"], bt, ppr, slots),
+        "hadamard_tensor_core": lambda: osc.oscar_write_kv_hadamard(ctx, 0, kd, vd, osc.DTYPE_BF16, cu, start, batch,
+                                                                    batch * n, fx["clip_K"], fx["clip_V"], bt, ppr,
+                                                                    slots),
     }
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     res = {"workload": f"prefill write of {batch} x {n} tokens x {s.n_kv_heads} kv heads (K and V), d={s.head_dim}",

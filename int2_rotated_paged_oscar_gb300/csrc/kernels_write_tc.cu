@@ -16,6 +16,10 @@
 //       overlap the epilogue of the previous one.
 // Products of BF16 values are exact and accumulate in float32, so y carries
 // float32-level error like the CUDA-core path (not the same rounding).
+// Hadamard-only rotation (R = H_Had P_br / sqrt(D), the data-oblivious baseline of
+// section 2.2 A): R sqrt(D) has entries +-1, exact in one BF16 plane built in the kernel,
+// (H P_br)[i][j] = (-1)^popcount(i & br(j)) for the natural-order Sylvester H and the
+// bit reversal br; one accumulator per tile, scaled by 1/sqrt(D) in the epilogue.
 // Epilogue: thread t of the four epilogue warps owns row t of the tile (TMEM lane
 // t): it reads the row group by group (32 columns), clips, finds min/max, forms
 // the BF16 zero and scale, rounds the codes (reciprocal multiply) and packs the
@@ -49,25 +53,27 @@ constexpr int kTileM = 128;
 template <int D> __host__ __device__ constexpr int epi_halves() { return D == 128 ? OSCAR_WRITE_HALVES : 1; }
 template <int D> __host__ __device__ constexpr int epi_warps() { return 2 * epi_halves<D>() * 4; }
 template <int D> __host__ __device__ constexpr int tc_threads() { return (epi_warps<D>() + 1) * 32; }
-constexpr int kPlanes = 3;
 
 #include "tc_common.cuh"
 
 // ------------------------------------------------------------------ shared memory plan
-template <int D>
+template <int D, bool HAD>
 struct TcPlan {
+  static constexpr int PLANES = HAD ? 1 : 3;         // BF16 planes of R^T
   static constexpr int KCH = D / 64;                 // 128-byte K chunks per row
   static constexpr int NS = 4;                       // row-tile stages in flight
   static constexpr int A_BYTES = kTileM * D * 2;     // one A stage
   static constexpr int B_PLANE = D * D * 2;          // one BF16 plane of R^T
-  static constexpr int A_OFF = kPlanes * B_PLANE;    // multiple of 1024
+  static constexpr int A_OFF = PLANES * B_PLANE;     // multiple of 1024
   static constexpr int BAR_OFF = A_OFF + NS * A_BYTES;
   static constexpr int NBARS = 2 * NS + 5;           // a_full[NS], a_empty[NS], acc_full[2], acc_empty[2], r_full
   static_assert((NS - 2) * A_BYTES >= D * D * 4, "R (float32) is staged in A stages 2 .. NS-1");
   static constexpr int BYTES = BAR_OFF + NBARS * 8 + 16;
   static constexpr int SMEM = BYTES + 1024;          // slack for the 1024-byte alignment of the base
-  // per tile buffer two float32 accumulators of D columns (see the MMA order); two buffers
-  static constexpr uint32_t TMEM_COLS = 4 * D;
+  // per tile buffer two float32 accumulators of D columns (see the MMA order; one with the
+  // Hadamard plane); two buffers
+  static constexpr uint32_t ACC_COLS = HAD ? D : 2 * D;
+  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 };
 
 __device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
@@ -165,11 +171,11 @@ __device__ __forceinline__ uint32_t code_bias(int word, int c_lo, int c_hi) {
   return acc;
 }
 
-template <int D>
+template <int D, bool HAD>
 __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                  const __grid_constant__ CUtensorMap tmap_v,
                                                                  WriteArgs a) {
-  using L = TcPlan<D>;
+  using L = TcPlan<D, HAD>;
   constexpr int kEpiWarps = epi_warps<D>();
   constexpr int HALVES = epi_halves<D>();
   extern __shared__ uint8_t smem_raw[];
@@ -229,18 +235,36 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
     }
     mbar_init(r_full, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(r_full, D * D * sizeof(float));
-    bulk_g2s(asm_ + 2 * L::A_BYTES, R, D * D * sizeof(float), r_full);
+    if constexpr (!HAD) {
+      mbar_arrive_expect_tx(r_full, D * D * sizeof(float));
+      bulk_g2s(asm_ + 2 * L::A_BYTES, R, D * D * sizeof(float), r_full);
+    }
     for (int i = 0; i < n_early; ++i) load(i);
   }
   __syncthreads();
-  const bool r_ok = __syncthreads_and(mbar_wait_bounded(r_full, 0, a.status));
+  const bool r_ok = HAD || __syncthreads_and(mbar_wait_bounded(r_full, 0, a.status));
   if (!r_ok && producer) {  // drain every copy in flight before the CTA ends
     (void)mbar_wait_bounded(r_full, 0, nullptr);
     for (int i = 0; i < n_early; ++i) (void)mbar_wait_bounded(&a_full[i], 0, nullptr);
   }
+  if constexpr (HAD) {
+    // the +-1 plane: item = (n, k-octet); column n of H P_br is column br(n) of H
+    constexpr int LOGD = D == 128 ? 7 : 6;
+    for (int item = threadIdx.x; item < D * D / 8; item += blockDim.x) {
+      const int n = item % D, k0 = (item / D) * 8;
+      const uint32_t brn = __brev((uint32_t)n) >> (32 - LOGD);
+      uint32_t pk[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t lo = (__popc((uint32_t)(k0 + 2 * q) & brn) & 1) ? 0xBF80u : 0x3F80u;
+        const uint32_t hi = (__popc((uint32_t)(k0 + 2 * q + 1) & brn) & 1) ? 0xBF80u : 0x3F80u;
+        pk[q] = lo | (hi << 16);
+      }
+      *reinterpret_cast<uint4*>(bsm + sw128_offset(n, k0, D)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  }
   // item = (n, k-octet): 8 consecutive k of column n, contiguous in the swizzled row
-  for (int item = threadIdx.x; r_ok && item < D * D / 8; item += blockDim.x) {
+  for (int item = threadIdx.x; !HAD && r_ok && item < D * D / 8; item += blockDim.x) {
     const int n = item % D, k0 = (item / D) * 8;
     uint32_t pk[3][4];
 #pragma unroll
@@ -291,22 +315,32 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
         if (i >= 2 && !mbar_wait_bounded(&acc_empty[s], (uint32_t)((i >> 1) - 1) & 1, a.status)) break;
         tc_fence_after();
         const uint32_t a_base = smem_u32(asm_ + st * L::A_BYTES);
-        const uint32_t acc0 = tmem + (uint32_t)(s * 2 * D), acc1 = acc0 + (uint32_t)D;
-        // Accuracy: each MMA rounds its float32 accumulation once, relative to the running
-        // magnitude.  The small planes R3, R2 go first (into acc0, still small), then the
-        // main plane R1 over the first half of K into acc0 and over the second half into
-        // acc1; the epilogue adds acc0 + acc1 in float32.
-#pragma unroll
-        for (int pp = 0; pp < kPlanes; ++pp) {
-          const int p = kPlanes - 1 - pp;
+        const uint32_t acc0 = tmem + (uint32_t)(s * L::ACC_COLS), acc1 = acc0 + (uint32_t)D;
+        if constexpr (HAD) {
+          // one exact +-1 plane, one accumulator
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const bool second = p == 0 && kk >= D / 32;
             const uint32_t ak = (uint32_t)((kk >> 2) * kTileM * 128 + (kk & 3) * 32);
-            const uint32_t bk = (uint32_t)(p * L::B_PLANE + (kk >> 2) * D * 128 + (kk & 3) * 32);
-            const uint32_t first = (pp == 0 && kk == 0) || (p == 0 && kk == D / 32);
-            tc_mma_bf16(second ? acc1 : acc0, smem_desc_sw128(a_base + ak), smem_desc_sw128(b_base + bk), idesc,
-                        first ? 0u : 1u);
+            const uint32_t bk = (uint32_t)((kk >> 2) * D * 128 + (kk & 3) * 32);
+            tc_mma_bf16(acc0, smem_desc_sw128(a_base + ak), smem_desc_sw128(b_base + bk), idesc, kk ? 1u : 0u);
+          }
+        } else {
+          // Accuracy: each MMA rounds its float32 accumulation once, relative to the running
+          // magnitude.  The small planes R3, R2 go first (into acc0, still small), then the
+          // main plane R1 over the first half of K into acc0 and over the second half into
+          // acc1; the epilogue adds acc0 + acc1 in float32.
+#pragma unroll
+          for (int pp = 0; pp < L::PLANES; ++pp) {
+            const int p = L::PLANES - 1 - pp;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const bool second = p == 0 && kk >= D / 32;
+              const uint32_t ak = (uint32_t)((kk >> 2) * kTileM * 128 + (kk & 3) * 32);
+              const uint32_t bk = (uint32_t)(p * L::B_PLANE + (kk >> 2) * D * 128 + (kk & 3) * 32);
+              const uint32_t first = (pp == 0 && kk == 0) || (p == 0 && kk == D / 32);
+              tc_mma_bf16(second ? acc1 : acc0, smem_desc_sw128(a_base + ak), smem_desc_sw128(b_base + bk), idesc,
+                          first ? 0u : 1u);
+            }
           }
         }
         tc_commit(&a_empty[st]);
@@ -331,7 +365,6 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
     const int ch = warp >> 3;
     const int t = (warp & 3) * 32 + lane;
     constexpr int GPH = D / 32 / HALVES;  // groups per half
-    const int c_lo = ch * GPH * 32, c_hi = c_lo + GPH * 32;
     const float clip = is_v ? a.clip_V : a.clip_K;
     const void* src = is_v ? a.V : a.K;
     // the eviction launched before this kernel reads ring rows that the tiles' window rows
@@ -381,12 +414,17 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
         uint32_t szw[D / 32];
 #pragma unroll
         for (int w = 0; w < D / 16; ++w) words[w] = 0u - code_bias<D, IS_V>(w, C_LO, C_HI);
-#pragma unroll
-        // a group's two accumulators are read from TMEM while the previous group is quantised
-        uint32_t r0[32], r1[32];
-        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(s * 2 * D);
-        tmem_ld32_nowait(lane_base + (uint32_t)(32 * CH * GPH), r0);
-        tmem_ld32_nowait(lane_base + (uint32_t)(32 * CH * GPH + D), r1);
+        // a group's accumulators are read from TMEM while the previous group is quantised
+        uint32_t r0[32], r1[HAD ? 1 : 32];
+        (void)r1;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(s * L::ACC_COLS);
+        constexpr float kInvSqrtD = D == 64 ? 0.125f : 0.08838834764831845f;   // 1/sqrt(D) rounded to float32
+        const float2 hscale = make_float2(kInvSqrtD, kInvSqrtD);
+        auto load_group = [&](int gg) {
+          tmem_ld32_nowait(lane_base + (uint32_t)(32 * gg), r0);
+          if constexpr (!HAD) tmem_ld32_nowait(lane_base + (uint32_t)(32 * gg + D), reinterpret_cast<uint32_t(&)[32]>(r1));
+        };
+        load_group(CH * GPH);
 #pragma unroll
         for (int gq = 0; gq < GPH; ++gq) {
           const int gi = CH * GPH + gq;
@@ -394,15 +432,14 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
           float y[32];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            const float2 s2 = __fadd2_rn(make_float2(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1])),
-                                         make_float2(__uint_as_float(r1[j]), __uint_as_float(r1[j + 1])));
+            const float2 a2 = make_float2(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1]));
+            float2 s2;
+            if constexpr (HAD) s2 = __fmul2_rn(a2, hscale);
+            else s2 = __fadd2_rn(a2, make_float2(__uint_as_float(r1[j]), __uint_as_float(r1[j + 1])));
             y[j] = s2.x;
             y[j + 1] = s2.y;
           }
-          if (gq + 1 < GPH) {
-            tmem_ld32_nowait(lane_base + (uint32_t)(32 * (gi + 1)), r0);
-            tmem_ld32_nowait(lane_base + (uint32_t)(32 * (gi + 1) + D), r1);
-          }
+          if (gq + 1 < GPH) load_group(gi + 1);
           quant_group<D, IS_V>(y, gi, clip, words, szw[gi]);
         }
         tc_fence_before();
@@ -544,9 +581,9 @@ int cached_row_map(CUtensorMap* map, const void* base, long long rows, int hkv, 
   return 0;
 }
 
-template <int D>
+template <int D, bool HAD>
 int launch_write_tc_t(const WriteArgs& a, cudaStream_t s, bool pdl) {
-  using L = TcPlan<D>;
+  using L = TcPlan<D, HAD>;
   const bool rph = a.g.rph != 0;
   const long long rows = rph ? (long long)a.total_tokens : (long long)a.total_tokens * a.g.Hkv;
   const long long tiles = (rows + kTileM - 1) / kTileM;
@@ -556,7 +593,7 @@ int launch_write_tc_t(const WriteArgs& a, cudaStream_t s, bool pdl) {
   if ((e = cached_row_map(&mv, a.V, rph ? (long long)a.total_tokens : rows, a.g.Hkv, D, rph))) return e;
   // at least 120 KB of shared memory: one CTA per SM, so the TMEM allocation never waits
   const int smem = L::SMEM > 120 * 1024 ? L::SMEM : 120 * 1024;
-  cudaError_t ce = ensure_smem_limit(write_tc_kernel<D>, smem);
+  cudaError_t ce = ensure_smem_limit(write_tc_kernel<D, HAD>, smem);
   if (ce != cudaSuccess) return (int)ce;
   // x2 (K, V): one CTA per SM; with a rotation per kv head, the same number of CTAs for every head
   int ctas = (int)(tiles < 76 ? tiles : 76);
@@ -564,20 +601,21 @@ int launch_write_tc_t(const WriteArgs& a, cudaStream_t s, bool pdl) {
     const long long per_head = tiles < 76 / a.g.Hkv ? tiles : (76 / a.g.Hkv > 0 ? 76 / a.g.Hkv : 1);
     ctas = (int)(per_head * a.g.Hkv);
   }
-  return launch_pdl(write_tc_kernel<D>, dim3(ctas, 2), dim3(tc_threads<D>()), (size_t)smem, s, pdl, mk, mv, a);
+  return launch_pdl(write_tc_kernel<D, HAD>, dim3(ctas, 2), dim3(tc_threads<D>()), (size_t)smem, s, pdl, mk, mv, a);
 }
 
 }  // namespace
 
 bool write_tc_supported(const WriteArgs& a) {
-  return !a.hadamard && a.dtype == kDtypeBF16 && (a.g.D == 128 || a.g.D == 64) &&
+  return a.dtype == kDtypeBF16 && (a.g.D == 128 || a.g.D == 64) &&
          (reinterpret_cast<uintptr_t>(a.K) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.V) & 15) == 0;
 }
 
 int launch_write_tc(const WriteArgs& a, void* stream, bool pdl) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((long long)a.total_tokens * a.g.Hkv == 0) return 0;
-  return a.g.D == 128 ? launch_write_tc_t<128>(a, s, pdl) : launch_write_tc_t<64>(a, s, pdl);
+  if (a.hadamard) return a.g.D == 128 ? launch_write_tc_t<128, true>(a, s, pdl) : launch_write_tc_t<64, true>(a, s, pdl);
+  return a.g.D == 128 ? launch_write_tc_t<128, false>(a, s, pdl) : launch_write_tc_t<64, false>(a, s, pdl);
 }
 
 }  // namespace oscar
