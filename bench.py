@@ -980,24 +980,32 @@ def run_ours(args, world, rank, local):
         del bpool
 
     # ---------------- end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    hq_host = [torch.empty_like(q, device="cpu").pin_memory() for q in qs]
-    hk_host = [torch.empty_like(k, device="cpu").pin_memory() for k in kn]
-    hv_host = [torch.empty_like(v, device="cpu").pin_memory() for v in vn]
-    for a, b in zip(hq_host + hk_host + hv_host, qs + kn + vn):
-        a.copy_(b)
+    # A step's inputs (q, K_new, V_new of every layer) sit back to back in one pinned host buffer and
+    # go over in one copy into one device buffer, of which the step's input tensors are views.
+    parts = [qs[0], kn[0], vn[0]]
+    nbytes_in = [t.numel() * t.element_size() for t in parts]
+    in_dev = torch.empty(sum(nbytes_in), dtype=torch.uint8, device="cuda")
+    views, off = [], 0
+    for t, nb in zip(parts, nbytes_in):
+        views.append(in_dev[off:off + nb].view(t.dtype).view(t.shape))
+        off += nb
+    q_in, k_in, v_in = views
+    in_host = []
+    for i in range(nvar):
+        h = torch.empty(sum(nbytes_in), dtype=torch.uint8).pin_memory()
+        off = 0
+        for t, nb in zip((qs[i], kn[i], vn[i]), nbytes_in):
+            h[off:off + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
+            off += nb
+        in_host.append(h)
     out_host = torch.empty_like(out, device="cpu").pin_memory()
-    q_in = torch.empty_like(qs[0])
-    k_in = torch.empty_like(kn[0])
-    v_in = torch.empty_like(vn[0])
 
     # the step graph for the end-to-end run reads its inputs from fixed device buffers that each
     # step fills from pinned host memory; the output is copied back to pinned host memory
     g_e2e = capture(lambda: layer_pass(True, q_in, k_in, v_in))
 
     def e2e_step(i):
-        q_in.copy_(hq_host[i % nvar], non_blocking=True)
-        k_in.copy_(hk_host[i % nvar], non_blocking=True)
-        v_in.copy_(hv_host[i % nvar], non_blocking=True)
+        in_dev.copy_(in_host[i % nvar], non_blocking=True)
         g_e2e.replay()
         out_host.copy_(out, non_blocking=True)
 
@@ -1014,7 +1022,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_wall_ms = (time.perf_counter() - t0) * 1000 / max(e2e_steps - 2, 1)
     e2e_ms = max_over_ranks(max(ev0.elapsed_time(ev1) / max(e2e_steps - 2, 1), e2e_wall_ms), world)
-    h2d = qs[0].numel() * 2 + kn[0].numel() * 2 * 2
+    h2d = sum(nbytes_in)
     d2h = out.numel() * 4
     e2e_value = sum_over_ranks(bytes_step / (e2e_ms * 1e-3) / 1e9, world)
     assert osc.oscar_check_status(ctx) == 0
