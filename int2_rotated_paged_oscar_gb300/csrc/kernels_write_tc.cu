@@ -371,6 +371,11 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
     // overwrite: every store waits for it (the set-up and the row-tile loads did not)
     pdl_wait();
     int i = eg;
+    // this thread's request from its previous tile (rows advance, and a request spans many
+    // tiles): tokens [c_lo, c_hi) of request c_b, first position c_t0; c_b < 0: none yet.  Kept
+    // by the one-plane form only: the dense form's epilogue has no registers to spare for it
+    // (168 a thread, the limit at nine warps; the four more spilled and made it slower).
+    int c_b = -1, c_lo = 0, c_hi = 0, c_t0 = 0;
     for (int tile = cta_k + eg * n_ctas; r_ok && tile < tiles; tile += 2 * n_ctas, i += 2) {
       const int s = i & 1;
       const uint32_t u = (uint32_t)(i >> 1);
@@ -380,15 +385,21 @@ __global__ void __launch_bounds__(tc_threads<D>(), 1) write_tc_kernel(const __gr
       if (r < rows) {
         token = g.rph ? static_cast<int>(r) : static_cast<int>(r / g.Hkv);
         h = g.rph ? hsel : static_cast<int>(r % g.Hkv);
-        int lo = 0, hi = a.batch - 1;  // request: largest b with cu_seqlens[b] <= token
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (a.cu_seqlens[mid] <= token) lo = mid; else hi = mid - 1;
+        if (!HAD || c_b < 0 || token < c_lo || token >= c_hi) {
+          int lo = 0, hi = a.batch - 1;  // request: largest b with cu_seqlens[b] <= token
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.cu_seqlens[mid] <= token) lo = mid; else hi = mid - 1;
+          }
+          c_b = lo;
+          c_lo = a.cu_seqlens[lo];
+          c_hi = a.cu_seqlens[lo + 1];
+          c_t0 = a.start_pos[lo];
         }
-        b = lo;
-        const int t0 = a.start_pos[b];
-        const int n1 = t0 + (a.cu_seqlens[b + 1] - a.cu_seqlens[b]);
-        pos = t0 + (token - a.cu_seqlens[b]);
+        b = c_b;
+        const int t0 = c_t0;
+        const int n1 = t0 + (c_hi - c_lo);
+        pos = t0 + (token - c_lo);
         if (t0 < 0 || n1 > g.max_pages_per_req * g.P) {
           flag_error(a.status, kDevBadLen);
         } else {
