@@ -105,14 +105,11 @@ def test_naive_int2_identity_rotation(osc):
         gc.close()
 
 
-@pytest.mark.parametrize("shape", [syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), syn.Shape(8, 4, 64, 16, 32, 4, 32, 1),
-                                   syn.Shape(24, 6, 128, 32, 32, 4, 64, 1)],
-                         ids=["d128_p64", "d64_p16", "d128_p32_six_kv_heads"])
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_write_hadamard_only_parity(osc, shape, dtype):
-    """Data-oblivious rotation R = H P (U = I): the fast Walsh-Hadamard write against the oracle's dense
-    R, three requests of ragged lengths (row counts not a multiple of the kernel's 8-row passes), then
-    an extend chunk of each request after its prefix (eviction of ring tokens, then the write)."""
+def _hadamard_case(osc, shape, dtype, rph):
+    """Data-oblivious rotation R = H P (U = I), written by oscar_write_kv_hadamard (BF16 rows: one exact
+    +-1 plane on the tensor cores; float32 rows: the fast Walsh-Hadamard transform) against the oracle's
+    dense R: three requests of ragged lengths (row counts not a multiple of a tile), then an extend chunk
+    of each request after its prefix (eviction of ring tokens, then the write)."""
     wl = syn.Workload("had", shape, [0], seed=7, dtype=dtype)
     fx = H.fixture(wl, u_identity=True)
     lens = [700, 300, 37]
@@ -121,7 +118,7 @@ def test_write_hadamard_only_parity(osc, shape, dtype):
     bt = _contiguous_bt(3, ppr)
     geom = H.geometry(s, 3 * ppr, 3)
     img = cache.CacheImage(geom)
-    gc = H.make_gpu_cache(geom, s.n_q_heads, ppr)
+    gc = H.make_gpu_cache(geom, s.n_q_heads, ppr, rotation_per_kv_head=rph)
     slots = np.arange(3, dtype=np.int32)
 
     def write(lens_now, start, sub0):
@@ -146,6 +143,24 @@ def test_write_hadamard_only_parity(osc, shape, dtype):
         H.compare_window(gc.slab_np(), img.slab, 0, range(3))
     finally:
         gc.close()
+
+
+@pytest.mark.parametrize("shape", [syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), syn.Shape(8, 4, 64, 16, 32, 4, 32, 1),
+                                   syn.Shape(24, 6, 128, 32, 32, 4, 64, 1)],
+                         ids=["d128_p64", "d64_p16", "d128_p32_six_kv_heads"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_write_hadamard_only_parity(osc, shape, dtype):
+    """The Hadamard-only write against the oracle (see _hadamard_case), one rotation per layer."""
+    _hadamard_case(osc, shape, dtype, 0)
+
+
+@pytest.mark.parametrize("shape", [syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), syn.Shape(8, 4, 64, 16, 32, 4, 32, 1)],
+                         ids=["d128_p64", "d64_p16"])
+def test_write_hadamard_only_parity_in_a_per_head_context(osc, shape):
+    """The same with BF16 rows in a context that keeps a rotation per kv head: the tensor-core write then
+    tiles each kv head's rows separately (a CTA per head, a 3-D row map), and the Hadamard rotation,
+    the same for every head, must give the same codes."""
+    _hadamard_case(osc, shape, "bf16", 1)
 
 
 def test_append_and_extend_parity(osc):
