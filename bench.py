@@ -660,35 +660,45 @@ def extend_leg(osc, bf16_peak, reps=5, row_shift=37, configs=((4, 32768, 2048), 
         vn = torch.cat([vd[row_shift * b + npre:row_shift * b + npre + T] for b in range(B)])
         q = torch.from_numpy(syn.to_bf16_bits(syn.queries(wl, 0, B * T)).view(np.int16)).cuda()
         out = torch.empty((B * T, 32, 128), dtype=torch.bfloat16, device="cuda")
-        wsb = osc.oscar_extend_workspace_size(cfg, B * T)
-        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
         cu, pre, slots = i32([T * b for b in range(B + 1)]), i32([npre] * B), i32(list(range(B)))
 
-        def call():
-            osc.oscar_extend_attn(ctx, 0, q, osc.DTYPE_BF16, kn, vn, osc.DTYPE_BF16, out, osc.DTYPE_BF16, cu, pre,
-                                  B, B * T, T, bt, ppr, slots, rk, rv, ws, wsb)
-        for _ in range(2):
-            call()
-        torch.cuda.synchronize()
-        assert osc.oscar_check_status(ctx) == 0
-        osc.oscar_set_timing(ctx, 1)
-        osc.oscar_reset_timing(ctx)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            call()
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
-        kms, kl = osc.oscar_kernel_time(ctx, "extend")
-        assert osc.oscar_check_status(ctx) == 0
+        def timed(wsb):
+            """ms per call and the library's per-call time of its "extend" launches, for a workspace of wsb bytes"""
+            ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+
+            def call():
+                osc.oscar_extend_attn(ctx, 0, q, osc.DTYPE_BF16, kn, vn, osc.DTYPE_BF16, out, osc.DTYPE_BF16, cu,
+                                      pre, B, B * T, T, bt, ppr, slots, rk, rv, ws, wsb)
+            for _ in range(2):
+                call()
+            torch.cuda.synchronize()
+            assert osc.oscar_check_status(ctx) == 0
+            osc.oscar_set_timing(ctx, 1)
+            osc.oscar_reset_timing(ctx)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                call()
+            e1.record()
+            torch.cuda.synchronize()
+            kms, kl = osc.oscar_kernel_time(ctx, "extend")
+            osc.oscar_set_timing(ctx, 0)
+            assert osc.oscar_check_status(ctx) == 0
+            return e0.elapsed_time(e1) / reps, kms / max(kl, 1)
+
+        # the unpacked-prefix form (the history dequantised once per call, its tiles copied by every
+        # query tile's CTA), and the form in which each CTA unpacks the pages itself
+        ms, kms = timed(osc.oscar_extend_workspace_size_unpacked(cfg, B * T, B, npre))
+        packed_ms = timed(osc.oscar_extend_workspace_size(cfg, B * T))[0] if npre else ms
         flops = 4.0 * 128 * 32 * B * sum(npre + i + 1 for i in range(T))
         tf = flops / (ms * 1e-3) / 1e12
         rows.append({"requests": B, "prefix_tokens": npre, "chunk_tokens": T, "ms_per_call": ms,
-                     "kernel_ms": kms / max(kl, 1), "algorithmic_tflops": tf, "bf16_peak_tflops": bf16_peak,
-                     "frac_of_bf16_peak": tf / bf16_peak, "tokens_per_s": B * T / (ms * 1e-3)})
+                     "kernel_ms": kms, "algorithmic_tflops": tf, "bf16_peak_tflops": bf16_peak,
+                     "frac_of_bf16_peak": tf / bf16_peak, "tokens_per_s": B * T / (ms * 1e-3),
+                     "form": "unpacked prefix" if npre else "no prefix",
+                     "ms_per_call_in_cta_unpack": packed_ms})
         osc.oscar_destroy(ctx)
-        del pool, slab, kd, vd, kn, vn, q, out, ws
+        del pool, slab, kd, vd, kn, vn, q, out
         torch.cuda.empty_cache()
     res = {"workload": "extend attention: 32 q / 8 kv heads, d=128, pages of 64, BF16 queries and chunk K/V, "
                        "BF16 output", "bound": "tensor", "rows": rows}

@@ -269,6 +269,160 @@ struct XTiles {
   }
 };
 
+// Unpacks one 64-key INT2 history tile (its pages contiguous at raw: block i holds keys
+// [i P, (i + 1) P)) into the operand tiles of a stage (Kt, Kz, Vt, Zv at stg), by 128
+// threads u = 0..127.  Keys outside the history [S, hist_end) get zero operands.  Used by the
+// attention kernel on its own shared-memory stage and by the pre-pass that dequantises a
+// prefix once per call.
+template <int D>
+__device__ __forceinline__ void unpack_int2_tile(const uint8_t* raw, uint8_t* stg, int u, int base, int S,
+                                                 int hist_end, int pshift, int pmask, size_t BB, const Geom& g,
+                                                 uint32_t magic, uint32_t kK23, uint32_t kV23) {
+  using L = XLayout<D>;
+  constexpr int G = L::G;
+  // K codes -> code * s * 2^(k_K + pos - 10); thread (key, w) writes channels [64w, 64w + 64),
+  // groups 2w and 2w + 1, and those groups' centres m = z + 1.5 s: Kz row key, column t G + g
+  // holds term centre_z_term(t) of m (the query side matches it)
+  if (u < kXKeys * (D / 64)) {
+    const int key = u / (D / 64), w = u % (D / 64);
+    const bool ok = (base + key >= S && base + key < hist_end);
+    const uint8_t* kb = raw + (key >> pshift) * BB;
+    const int slot = key & pmask;
+    uint32_t wd[4], w6[4];
+#pragma unroll
+    for (int tg = 0; tg < 4; ++tg) {
+      wd[tg] = *reinterpret_cast<const uint32_t*>(kb + slot * (D / 4) + (tg * (D / 64) + w) * 4);
+      w6[tg] = wd[tg] >> 6;
+    }
+    uint32_t szw[G];
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg)
+      szw[gg] = *reinterpret_cast<const uint32_t*>(kb + g.k_sz_off() + slot * (D / 8) + gg * 4);
+    const int gA = 2 * w;
+    const uint32_t sA = szw[gA], sB = szw[gA + 1];
+    const uint32_t nA = ok ? half2_bits(neg_scale_times_pow2(sA, kK23), neg_scale_times_pow2(sA, kK23)) : 0u;
+    const uint32_t nB = ok ? half2_bits(neg_scale_times_pow2(sB, kK23), neg_scale_times_pow2(sB, kK23)) : 0u;
+    static_for<8>([&](auto X) {
+      constexpr int x = decltype(X)::value;
+      const uint32_t n2 = x < 4 ? nA : nB;
+      constexpr uint32_t kc = centre_pair(slot_pos(x));
+      uint4 c;
+      c.x = centre_codes(scale_codes(magic_slot<x>(wd[0], w6[0], magic), n2), n2, kc);
+      c.y = centre_codes(scale_codes(magic_slot<x>(wd[1], w6[1], magic), n2), n2, kc);
+      c.z = centre_codes(scale_codes(magic_slot<x>(wd[2], w6[2], magic), n2), n2, kc);
+      c.w = centre_codes(scale_codes(magic_slot<x>(wd[3], w6[3], magic), n2), n2, kc);
+      *reinterpret_cast<uint4*>(stg + L::KT + sw128_offset(key, 8 * (8 * w + x), kXKeys)) = c;
+    });
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      __half mh, ml;
+      centre_hi_lo(ok ? (e ? sB : sA) : 0u, kK23, mh, ml);
+      const __half mt[2] = {mh, ml};
+#pragma unroll
+      for (int tt = 0; tt < kCentreTerms<G>(); ++tt)
+        *reinterpret_cast<__half*>(stg + L::KZ + sw128_offset(key, tt * G + gA + e, kXKeys)) = mt[centre_z_term(tt)];
+    }
+  }
+  // V codes -> code * s_V * 2^(k_V + pos - 10), transposed: thread (half-word hw, keys 8kb..8kb+7)
+  if (u < (D / 8) * 8) {
+    const int hw = u % (D / 8), kb8 = u / (D / 8);
+    const int chbase = 64 * (hw % (D / 64)) + hw / (D / 64);
+    const int gA = chbase / 32;
+    uint32_t W[4], W6[4], nA[4], nB[4];
+
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      uint32_t hv[2];
+      float sa[2], sb[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = 8 * kb8 + 2 * p + e;
+        const bool ok = (base + key >= S && base + key < hist_end);
+        const uint8_t* vb = raw + (key >> pshift) * BB;
+        const int slot = key & pmask;
+        hv[e] = *reinterpret_cast<const uint16_t*>(vb + g.v_codes_off() + slot * (D / 4) + hw * 2);
+        const uint32_t* szr = reinterpret_cast<const uint32_t*>(vb + g.v_sz_off() + slot * (D / 8));
+        sa[e] = ok ? neg_scale_times_pow2(szr[gA], kV23) : 0.f;
+        sb[e] = ok ? neg_scale_times_pow2(szr[gA + 1], kV23) : 0.f;
+      }
+      W[p] = hv[0] | (hv[1] << 16);
+      W6[p] = W[p] >> 6;
+      nA[p] = half2_bits(sa[0], sa[1]);
+      nB[p] = half2_bits(sb[0], sb[1]);
+    }
+    static_for<8>([&](auto X) {
+      constexpr int s = decltype(X)::value;
+      constexpr uint32_t kc = centre_pair(slot_pos(s));
+      uint4 c;
+      c.x = centre_codes(scale_codes(magic_slot<s>(W[0], W6[0], magic), s < 4 ? nA[0] : nB[0]), s < 4 ? nA[0] : nB[0], kc);
+      c.y = centre_codes(scale_codes(magic_slot<s>(W[1], W6[1], magic), s < 4 ? nA[1] : nB[1]), s < 4 ? nA[1] : nB[1], kc);
+      c.z = centre_codes(scale_codes(magic_slot<s>(W[2], W6[2], magic), s < 4 ? nA[2] : nB[2]), s < 4 ? nA[2] : nB[2], kc);
+      c.w = centre_codes(scale_codes(magic_slot<s>(W[3], W6[3], magic), s < 4 ? nA[3] : nB[3]), s < 4 ? nA[3] : nB[3], kc);
+      *reinterpret_cast<uint4*>(stg + L::VT + sw128_offset(chbase + 8 * s, 8 * kb8, D)) = c;
+    });
+    // the centres of groups gA, gA + 1 for one key each of the 8 threads that share kb8 and
+    // gA: Zv rows g (hi) and G + g (lo), column key
+    const int ckey = 8 * kb8 + hw / (D / 64);
+    const bool cok = (base + ckey >= S && base + ckey < hist_end);
+    const uint32_t* cszr = reinterpret_cast<const uint32_t*>(raw + (ckey >> pshift) * BB + g.v_sz_off() +
+                                                             (ckey & pmask) * (D / 8));
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      __half mh, ml;
+      centre_hi_lo(cok ? cszr[gA + e] : 0u, kV23, mh, ml);
+      *reinterpret_cast<__half*>(stg + L::ZV + sw128_offset(gA + e, ckey, 16)) = mh;
+      *reinterpret_cast<__half*>(stg + L::ZV + sw128_offset(G + gA + e, ckey, 16)) = ml;
+    }
+  }
+}
+
+// Pre-pass of the unpacked-prefix form: every INT2 history tile of every (request, kv head)
+// is dequantised once per call into the workspace, as the image of an attention stage
+// (XLayout<D>::STAGE bytes, padding zero), so that the attention CTAs of all the request's
+// query tiles bulk-copy it instead of each unpacking it.  Grid (tile j, kv head, request),
+// 128 threads; tiles past a request's history exit at once.  A page outside the block table
+// or the pool is flagged as in the attention kernel.
+template <int D>
+__global__ void __launch_bounds__(128) extend_unpack_kernel(ExtendArgs a) {
+  using L = XLayout<D>;
+  extern __shared__ __align__(1024) uint8_t xu_smem_raw[];
+  uint8_t* stg = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(xu_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* raw = stg + L::STAGE;   // the tile's pages, contiguous
+  const Geom& g = a.g;
+  const int j = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int u = threadIdx.x;
+  const int n_pre = a.prefix_lens[b];
+  if (n_pre < 0 || (long long)n_pre > (long long)g.max_pages_per_req * g.P) return;   // flagged by the attention
+  const int hist_end = max(g.S, n_pre - g.W);
+  if (hist_end <= g.S) return;
+  const int u0 = g.S / 64;
+  if (j > (hist_end - 1) / 64 - u0) return;
+  const int base = 64 * (u0 + j);
+  const int pshift = __ffs(g.P) - 1, pmask = g.P - 1, nblk = kXKeys >> pshift;
+  const size_t BB = g.block_bytes();
+  const uint8_t* pool_l = a.pool + (size_t)a.layer * g.layer_pool_bytes();
+  for (int bi = 0; bi < nblk; ++bi) {
+    const int lp = (base >> pshift) + bi;
+    const int p0 = lp << pshift;
+    if (p0 + g.P <= g.S || p0 >= hist_end) continue;   // no history token in this page
+    const int page = (lp < a.bt_stride && lp < g.max_pages_per_req) ? a.block_table[(size_t)b * a.bt_stride + lp] : -1;
+    if (page < 0 || page >= g.num_pages) {
+      if (u == 0) flag_error(a.status, kDevBadPage);
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(pool_l + ((size_t)page * g.Hkv + kvh) * BB);
+    uint4* dst = reinterpret_cast<uint4*>(raw + bi * BB);
+    for (int q = u; q < (int)(BB / 16); q += 128) dst[q] = src[q];
+  }
+  for (int q = u; q < L::STAGE / 16; q += 128) reinterpret_cast<uint4*>(stg)[q] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  unpack_int2_tile<D>(raw, stg, u, base, g.S, hist_end, pshift, pmask, BB, g, a.code_magic,
+                      static_cast<uint32_t>(a.k_exp_K) << 23, static_cast<uint32_t>(a.k_exp_V) << 23);
+  __syncthreads();
+  uint4* out = reinterpret_cast<uint4*>(a.prep + (((size_t)b * g.Hkv + kvh) * a.prep_tiles + j) * L::STAGE);
+  for (int q = u; q < L::STAGE / 16; q += 128) out[q] = reinterpret_cast<const uint4*>(stg)[q];
+}
+
 template <int D>
 __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a) {
   using L = XLayout<D>;
@@ -324,6 +478,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   const int kend = min(len, i0 + tq);
   tl.nC = (kend + 63) / 64;
   const int n_tiles = tl.n();
+  // unpacked-prefix form: this request's INT2 tiles were dequantised by the pre-pass
+  const bool use_prep = a.prep != nullptr && tl.nR <= a.prep_tiles;
   int req = 0;
   if (tl.nW > 0) {
     req = a.req_slot[b];
@@ -530,103 +686,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     }
   };
   auto unpack_int2 = [&](int j, uint8_t* stg) {
-    const int base = tl.base(j);
-    const uint8_t* raw = smem + L::RAW0 + (j % L::NRAW) * L::RAW_BYTES;
-    const uint32_t magic = a.code_magic;
-    // K codes -> code * s * 2^(k_K + pos - 10); thread (key, w) writes channels [64w, 64w + 64),
-    // groups 2w and 2w + 1, and those groups' centres m = z + 1.5 s: Kz row key, column t G + g
-    // holds term centre_z_term(t) of m (the query side matches it)
-    if (u < kXKeys * (D / 64)) {
-      const int key = u / (D / 64), w = u % (D / 64);
-      const bool ok = hist_ok(base + key);
-      const uint8_t* kb = raw + (key >> pshift) * BB;
-      const int slot = key & pmask;
-      uint32_t wd[4], w6[4];
-#pragma unroll
-      for (int tg = 0; tg < 4; ++tg) {
-        wd[tg] = *reinterpret_cast<const uint32_t*>(kb + slot * (D / 4) + (tg * (D / 64) + w) * 4);
-        w6[tg] = wd[tg] >> 6;
-      }
-      uint32_t szw[G];
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg)
-        szw[gg] = *reinterpret_cast<const uint32_t*>(kb + g.k_sz_off() + slot * (D / 8) + gg * 4);
-      const int gA = 2 * w;
-      const uint32_t sA = szw[gA], sB = szw[gA + 1];
-      const uint32_t nA = ok ? half2_bits(neg_scale_times_pow2(sA, kK23), neg_scale_times_pow2(sA, kK23)) : 0u;
-      const uint32_t nB = ok ? half2_bits(neg_scale_times_pow2(sB, kK23), neg_scale_times_pow2(sB, kK23)) : 0u;
-      static_for<8>([&](auto X) {
-        constexpr int x = decltype(X)::value;
-        const uint32_t n2 = x < 4 ? nA : nB;
-        constexpr uint32_t kc = centre_pair(slot_pos(x));
-        uint4 c;
-        c.x = centre_codes(scale_codes(magic_slot<x>(wd[0], w6[0], magic), n2), n2, kc);
-        c.y = centre_codes(scale_codes(magic_slot<x>(wd[1], w6[1], magic), n2), n2, kc);
-        c.z = centre_codes(scale_codes(magic_slot<x>(wd[2], w6[2], magic), n2), n2, kc);
-        c.w = centre_codes(scale_codes(magic_slot<x>(wd[3], w6[3], magic), n2), n2, kc);
-        *reinterpret_cast<uint4*>(stg + L::KT + sw128_offset(key, 8 * (8 * w + x), kXKeys)) = c;
-      });
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        __half mh, ml;
-        centre_hi_lo(ok ? (e ? sB : sA) : 0u, kK23, mh, ml);
-        const __half mt[2] = {mh, ml};
-#pragma unroll
-        for (int tt = 0; tt < kCentreTerms<G>(); ++tt)
-          *reinterpret_cast<__half*>(stg + L::KZ + sw128_offset(key, tt * G + gA + e, kXKeys)) = mt[centre_z_term(tt)];
-      }
-    }
-    // V codes -> code * s_V * 2^(k_V + pos - 10), transposed: thread (half-word hw, keys 8kb..8kb+7)
-    if (u < (D / 8) * 8) {
-      const int hw = u % (D / 8), kb8 = u / (D / 8);
-      const int chbase = 64 * (hw % (D / 64)) + hw / (D / 64);
-      const int gA = chbase / 32;
-      uint32_t W[4], W6[4], nA[4], nB[4];
-
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        uint32_t hv[2];
-        float sa[2], sb[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int key = 8 * kb8 + 2 * p + e;
-          const bool ok = hist_ok(base + key);
-          const uint8_t* vb = raw + (key >> pshift) * BB;
-          const int slot = key & pmask;
-          hv[e] = *reinterpret_cast<const uint16_t*>(vb + g.v_codes_off() + slot * (D / 4) + hw * 2);
-          const uint32_t* szr = reinterpret_cast<const uint32_t*>(vb + g.v_sz_off() + slot * (D / 8));
-          sa[e] = ok ? neg_scale_times_pow2(szr[gA], kV23) : 0.f;
-          sb[e] = ok ? neg_scale_times_pow2(szr[gA + 1], kV23) : 0.f;
-        }
-        W[p] = hv[0] | (hv[1] << 16);
-        W6[p] = W[p] >> 6;
-        nA[p] = half2_bits(sa[0], sa[1]);
-        nB[p] = half2_bits(sb[0], sb[1]);
-      }
-      static_for<8>([&](auto X) {
-        constexpr int s = decltype(X)::value;
-        constexpr uint32_t kc = centre_pair(slot_pos(s));
-        uint4 c;
-        c.x = centre_codes(scale_codes(magic_slot<s>(W[0], W6[0], magic), s < 4 ? nA[0] : nB[0]), s < 4 ? nA[0] : nB[0], kc);
-        c.y = centre_codes(scale_codes(magic_slot<s>(W[1], W6[1], magic), s < 4 ? nA[1] : nB[1]), s < 4 ? nA[1] : nB[1], kc);
-        c.z = centre_codes(scale_codes(magic_slot<s>(W[2], W6[2], magic), s < 4 ? nA[2] : nB[2]), s < 4 ? nA[2] : nB[2], kc);
-        c.w = centre_codes(scale_codes(magic_slot<s>(W[3], W6[3], magic), s < 4 ? nA[3] : nB[3]), s < 4 ? nA[3] : nB[3], kc);
-        *reinterpret_cast<uint4*>(stg + L::VT + sw128_offset(chbase + 8 * s, 8 * kb8, D)) = c;
-      });
-      // the centres of groups gA, gA + 1 for one key each of the 8 threads that share kb8 and
-      // gA: Zv rows g (hi) and G + g (lo), column key
-      const int ckey = 8 * kb8 + hw / (D / 64);
-      const bool cok = hist_ok(base + ckey);
-      const uint32_t* cszr = reinterpret_cast<const uint32_t*>(raw + (ckey >> pshift) * BB + g.v_sz_off() +
-                                                               (ckey & pmask) * (D / 8));
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        __half mh, ml;
-        centre_hi_lo(cok ? cszr[gA + e] : 0u, kV23, mh, ml);
-        *reinterpret_cast<__half*>(stg + L::ZV + sw128_offset(gA + e, ckey, 16)) = mh;
-        *reinterpret_cast<__half*>(stg + L::ZV + sw128_offset(G + gA + e, ckey, 16)) = ml;
-      }
-    }
+    unpack_int2_tile<D>(smem + L::RAW0 + (j % L::NRAW) * L::RAW_BYTES, stg, u, tl.base(j), tl.S, tl.hist_end,
+                        pshift, pmask, BB, g, a.code_magic, kK23, kV23);
   };
   // BF16 window or chunk tile: K rows copied into the swizzled K tile, V rows transposed
   auto plain_row = [&](int kind, int base, int key, int kv) -> const uint16_t* {
@@ -897,7 +958,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     if (tl.nR > 0) write_q_rot();
     write_q_plain();
     tmem_wait_st();
-  } else if (warp == 4) {
+  } else if (warp == 4 && !use_prep) {
     // the pages of the first NRAW - 1 tiles (the loop requests tile j + NRAW - 1 at tile j)
 #pragma unroll 1
     for (int t = 0; t < L::NRAW - 1 && t < tl.nR; ++t) {
@@ -929,6 +990,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       if (lane == 0) mbar_arrive(&p_full[i & 1]);
     }
   } else if (warp < 8) {
+    int copies_issued = 0;   // unpacked form, warp 4 lane 0: INT2 tiles [0, copies_issued) requested
+    int copies_done = 0;     // tiles [0, copies_done) known to have landed (their stage was freed since)
     for (int j = 0; j < n_tiles; ++j) {
       // stage j % NST was last read by tile j - NST's MMAs
       const bool ok = j < L::NST || xwait(&kv_empty[j % L::NST], (uint32_t)(((j / L::NST) - 1) & 1), a.status);
@@ -939,7 +1002,24 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         aborted = true;
         break;
       }
-      if (warp == 4 && j + L::NRAW - 1 < tl.nR) {
+      if (j >= L::NST) copies_done = j - L::NST + 1;
+      if (use_prep && j < tl.nR) {
+        // the tile's dequantised image: one bulk copy into its stage by warp 4 lane 0, whose
+        // arrival carries the bytes; warps 5-7 arrive at once
+        if (lane == 0) {
+          uint64_t* bar = &kv_full[j % L::NST];
+          if (warp == 4) {
+            mbar_arrive_expect_tx(bar, (uint32_t)L::STAGE);
+            bulk_g2s(smem + L::ST0 + (j % L::NST) * L::STAGE,
+                     a.prep + (((size_t)b * g.Hkv + kvh) * a.prep_tiles + j) * L::STAGE, (uint32_t)L::STAGE, bar);
+            copies_issued = j + 1;
+          } else {
+            mbar_arrive(bar);
+          }
+        }
+        continue;
+      }
+      if (warp == 4 && !use_prep && j + L::NRAW - 1 < tl.nR) {
         int pg[kMaxBlk];
         tile_pages(j + L::NRAW - 1, pg);
         if (lane == 0) issue_raw(j + L::NRAW - 1, pg);
@@ -955,10 +1035,15 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       __syncwarp();
       if (lane == 0) mbar_arrive(&kv_full[j % L::NST]);
     }
-    // no bulk copy may still be writing this CTA's shared memory when it exits (bounded waits)
-    if (u == 0)
+    // no bulk copy may still be writing this CTA's shared memory when it exits (bounded waits;
+    // a stage copy not yet known to have landed is the last on its stage, so its phase parity
+    // is unambiguous)
+    if (u == 0) {
       for (int t = raw_done; t < raw_issued; ++t)
         (void)mbar_wait_bounded(&raw_full[t % L::NRAW], (uint32_t)((t / L::NRAW) & 1), nullptr);
+      for (int t = copies_done; t < copies_issued; ++t)
+        (void)mbar_wait_bounded(&kv_full[t % L::NST], (uint32_t)((t / L::NST) & 1), nullptr);
+    }
   } else if (warp == 8 && lane == 0) {
     // MMA issue: the scores of tile qk (its stage unpacked; its S buffer, which holds tile
     // qk - 2's weights, free once that tile's PV is issued: the MMAs run in issue order) and
@@ -1113,6 +1198,12 @@ int launch_extend_d(const ExtendArgs& a, void* stream) {
   const long long per = a.g.rph ? 64 / a.g.gq() : 64;
   const long long units = a.g.rph ? (long long)a.total_tokens : rows;
   const unsigned qgrid = (unsigned)((units + per - 1) / per) + 1;
+  if (a.prep) {
+    const size_t usm = XLayout<D>::STAGE + XLayout<D>::RAW_BYTES + 1024;
+    if ((e = ensure_smem_limit(extend_unpack_kernel<D>, usm)) != cudaSuccess) return (int)e;
+    extend_unpack_kernel<D><<<dim3((unsigned)a.prep_tiles, (unsigned)a.g.Hkv, (unsigned)a.batch), 128, usm, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+  }
   extend_qrot_kernel<D><<<dim3(qgrid, heads), 256, qsm, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
   e = ensure_smem_limit(extend_attn_kernel<D>, XLayout<D>::SMEM);
@@ -1134,6 +1225,13 @@ size_t extend_workspace_bytes(const Geom& g, long long total_tokens) {
 void extend_ws_offsets(const Geom& g, size_t* rvt_off, size_t* qrot_off) {
   *rvt_off = 0;
   *qrot_off = ((size_t)(g.rph ? g.Hkv : 1) * g.D * g.D * 4 + 255) & ~size_t(255);
+}
+
+size_t extend_prep_tile_bytes(int D) { return D == 128 ? XLayout<128>::STAGE : XLayout<64>::STAGE; }
+
+long long extend_prep_tiles(const Geom& g, long long max_prefix) {
+  const long long hist_end = max_prefix - g.W > g.S ? max_prefix - g.W : g.S;
+  return hist_end > g.S ? (hist_end - 1) / 64 - g.S / 64 + 1 : 0;
 }
 
 int launch_extend(const ExtendArgs& a, void* stream) {

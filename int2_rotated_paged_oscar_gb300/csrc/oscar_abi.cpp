@@ -904,6 +904,23 @@ oscar_status oscar_extend_workspace_size(const oscar_config* cfg, int32_t total_
   return OSCAR_OK;
 }
 
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+}  // namespace
+
+oscar_status oscar_extend_workspace_size_unpacked(const oscar_config* cfg, int32_t total_tokens, int32_t batch,
+                                                  int32_t max_prefix, size_t* bytes) {
+  Geom g;
+  oscar_status st = validate(cfg, &g);
+  if (st != OSCAR_OK) return st;
+  if (!bytes || total_tokens < 0 || batch < 0 || max_prefix < 0)
+    return fail(OSCAR_ERR_INVALID, "bad arguments to extend workspace size");
+  const long long tiles = oscar::extend_prep_tiles(g, max_prefix);
+  *bytes = align256(oscar::extend_workspace_bytes(g, total_tokens)) +
+           (size_t)batch * g.Hkv * (size_t)tiles * oscar::extend_prep_tile_bytes(g.D);
+  return OSCAR_OK;
+}
+
 oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, const void* K_new,
                                const void* V_new, int32_t kv_dtype, void* out, int32_t out_dtype,
                                const int32_t* cu_seqlens, const int32_t* prefix_lens, int32_t batch,
@@ -961,6 +978,23 @@ oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
   a.k_exp_K = ek;
   a.k_exp_V = ev;
   a.code_magic = oscar::kCodeMagic;
+  // unpacked-prefix form when the workspace holds at least one tile per (request, kv head)
+  // past the base: as many tiles per pair as fit, at most what the longest prefix can have
+  a.prep = nullptr;
+  a.prep_tiles = 0;
+  {
+    const size_t base = align256(need);
+    const size_t per_tile = (size_t)batch * ctx->g.Hkv * oscar::extend_prep_tile_bytes(ctx->g.D);
+    if (ws_bytes >= base + per_tile) {
+      long long tiles = (long long)((ws_bytes - base) / per_tile);
+      const long long cap = oscar::extend_prep_tiles(ctx->g, (long long)ctx->g.max_pages_per_req * ctx->g.P);
+      if (tiles > cap) tiles = cap;
+      if (tiles > 0) {
+        a.prep = a.ws + base;
+        a.prep_tiles = (int)tiles;
+      }
+    }
+  }
   LaunchScope ls(ctx, "extend", stream);
   int e = oscar::launch_extend(a, stream);
   ls.done(e);

@@ -143,8 +143,16 @@ struct ExtendArgs {
   size_t rvt_off, qrot_off;
   int k_exp_K, k_exp_V;
   unsigned code_magic;
+  // unpacked-prefix form (null: every attention CTA unpacks its INT2 tiles itself): the
+  // pre-pass writes tile j of (request b, kv head h) at prep + ((b Hkv + h) prep_tiles + j) *
+  // extend_prep_tile_bytes(D); requests with more INT2 tiles than prep_tiles unpack themselves
+  uint8_t* prep;
+  int prep_tiles;
 };
 size_t extend_workspace_bytes(const Geom& g, long long total_tokens);
+size_t extend_prep_tile_bytes(int D);
+// INT2 history tiles (64 keys) of a prefix of max_prefix tokens
+long long extend_prep_tiles(const Geom& g, long long max_prefix);
 void extend_ws_offsets(const Geom& g, size_t* rvt_off, size_t* qrot_off);
 int launch_extend(const ExtendArgs& a, void* stream);
 // Self-test of the bounded-wait failure path: waits on an mbarrier that nothing arrives on.

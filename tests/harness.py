@@ -374,15 +374,21 @@ def cache_pages_for(n: int, g: cache.Geometry) -> int:
 
 
 def run_extend(gc: GpuCache, layer, q: np.ndarray, q_dtype: str, k_new: np.ndarray, v_new: np.ndarray, cu, prefix,
-               bt: np.ndarray, req_slot, fx, out_bf16=False, max_chunk=None):
-    """oscar_extend_attn on the GPU cache; k_new / v_new BF16-valued float arrays [T, Hkv, d]."""
+               bt: np.ndarray, req_slot, fx, out_bf16=False, max_chunk=None, unpacked=False):
+    """oscar_extend_attn on the GPU cache; k_new / v_new BF16-valued float arrays [T, Hkv, d].  unpacked: a
+    workspace of the unpacked-prefix form (the prefix dequantised once by a pre-pass), sized for the longest
+    prefix (True) or for prefixes of at most that many tokens (an int: longer ones unpack their own tiles)."""
     torch = torch_mod()
     import int2_rotated_paged_oscar_gb300 as osc
     cu = np.asarray(cu, np.int32)
     total = int(cu[-1])
     b = cu.size - 1
     max_chunk = int(np.diff(cu).max()) if max_chunk is None else max_chunk
-    ws_bytes = osc.oscar_extend_workspace_size(gc.cfg, total)
+    if unpacked is not False:   # True: sized for the longest prefix; an int: for prefixes up to that length
+        cap = int(max(prefix)) if unpacked is True else int(unpacked)
+        ws_bytes = osc.oscar_extend_workspace_size_unpacked(gc.cfg, total, b, cap)
+    else:
+        ws_bytes = osc.oscar_extend_workspace_size(gc.cfg, total)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
     out = torch.empty((total, q.shape[1], q.shape[2]), dtype=torch.bfloat16 if out_bf16 else torch.float32,
                       device="cuda")

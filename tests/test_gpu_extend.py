@@ -73,6 +73,13 @@ def test_extend_parity(osc, shape, prefix, chunks, q_dtype, out_bf16, q_scale):
         cu = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
         slots = np.arange(len(prefix), dtype=np.int32)
         got = H.run_extend(gc, 0, q, q_dtype, k, v, cu, prefix, bt, slots, fx, out_bf16=out_bf16)
+        # the unpacked-prefix form (the history dequantised once per call by a pre-pass, the attention CTAs
+        # copying its tiles) runs the same operands through the same MMAs: identical outputs, also when the
+        # workspace holds the tiles of the shorter prefixes only (the longest prefix unpacks its own)
+        for form in (True, max(1, sorted(prefix)[-2] if len(prefix) > 1 else prefix[0] // 2)):
+            got_u = H.run_extend(gc, 0, q, q_dtype, k, v, cu, prefix, bt, slots, fx, out_bf16=out_bf16,
+                                 unpacked=form)
+            assert np.array_equal(got_u, got), f"unpacked form {form}: {np.abs(got_u - got).max():.3e} apart"
         want = attention.extend(_image(gc, geom), 0, q, k, v, cu, prefix, bt, slots, fx["R_K"], fx["R_V"])
         if out_bf16:
             # a BF16 store rounds each element to 2^-9 of itself: one BF16 ulp of the element plus the
@@ -119,6 +126,8 @@ def test_extend_on_a_forked_prefix(osc):
         q = syn.queries(wl, 0, total, sub=10)
         cu = np.array([0, chunks[0], total], np.int32)
         got = H.run_extend(gc, 0, q, "bf16", kc, vc, cu, [n_pre, n_pre], bt, [0, 1], fx)
+        got_u = H.run_extend(gc, 0, q, "bf16", kc, vc, cu, [n_pre, n_pre], bt, [0, 1], fx, unpacked=True)
+        assert np.array_equal(got_u, got), "the unpacked-prefix form reads the shared pages the same way"
         # oracle: both prefixes written from scratch into separate pages
         bt_o = np.stack([np.arange(ppr), ppr + np.arange(ppr)]).astype(np.int32)
         img = cache.CacheImage(H.geometry(shape, 2 * ppr, 2))
