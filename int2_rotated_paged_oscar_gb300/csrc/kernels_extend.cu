@@ -423,7 +423,9 @@ __global__ void __launch_bounds__(128) extend_unpack_kernel(ExtendArgs a) {
   for (int q = u; q < L::STAGE / 16; q += 128) out[q] = reinterpret_cast<const uint4*>(stg)[q];
 }
 
-template <int D>
+// PREP: launched with the unpacked-prefix workspace (a second instantiation, so that the form
+// without it compiles to the kernel that has no copy path at all)
+template <int D, bool PREP>
 __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a) {
   using L = XLayout<D>;
   constexpr int G = L::G;
@@ -479,7 +481,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   tl.nC = (kend + 63) / 64;
   const int n_tiles = tl.n();
   // unpacked-prefix form: this request's INT2 tiles were dequantised by the pre-pass
-  const bool use_prep = a.prep != nullptr && tl.nR <= a.prep_tiles;
+  const bool use_prep = PREP && a.prep != nullptr && tl.nR <= a.prep_tiles;
   int req = 0;
   if (tl.nW > 0) {
     req = a.req_slot[b];
@@ -1206,11 +1208,12 @@ int launch_extend_d(const ExtendArgs& a, void* stream) {
   }
   extend_qrot_kernel<D><<<dim3(qgrid, heads), 256, qsm, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
-  e = ensure_smem_limit(extend_attn_kernel<D>, XLayout<D>::SMEM);
+  auto kern = a.prep ? extend_attn_kernel<D, true> : extend_attn_kernel<D, false>;
+  e = ensure_smem_limit(kern, XLayout<D>::SMEM);
   if (e != cudaSuccess) return (int)e;
   const int tq = kXRows / a.g.gq();
   dim3 grid((unsigned)((a.max_chunk + tq - 1) / tq), (unsigned)a.g.Hkv, (unsigned)a.batch);
-  extend_attn_kernel<D><<<grid, kXThreads, XLayout<D>::SMEM, s>>>(a);
+  kern<<<grid, kXThreads, XLayout<D>::SMEM, s>>>(a);
   return (int)cudaGetLastError();
 }
 
