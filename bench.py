@@ -688,14 +688,14 @@ def extend_leg(osc, bf16_peak, reps=5, row_shift=37, configs=((4, 32768, 2048), 
 
         # the unpacked-prefix form (the history dequantised once per call, its tiles copied by every
         # query tile's CTA), and the form in which each CTA unpacks the pages itself
-        ms, kms = timed(osc.oscar_extend_workspace_size_unpacked(cfg, B * T, B, npre))
-        packed_ms = timed(osc.oscar_extend_workspace_size(cfg, B * T))[0] if npre else ms
+        ms, kms = timed(osc.oscar_extend_workspace_size_unpacked(cfg, B * T, B, npre, T))
+        packed_ms = timed(osc.oscar_extend_workspace_size(cfg, B * T))[0]
         flops = 4.0 * 128 * 32 * B * sum(npre + i + 1 for i in range(T))
         tf = flops / (ms * 1e-3) / 1e12
         rows.append({"requests": B, "prefix_tokens": npre, "chunk_tokens": T, "ms_per_call": ms,
                      "kernel_ms": kms, "algorithmic_tflops": tf, "bf16_peak_tflops": bf16_peak,
                      "frac_of_bf16_peak": tf / bf16_peak, "tokens_per_s": B * T / (ms * 1e-3),
-                     "form": "unpacked prefix" if npre else "no prefix",
+                     "form": "shared tiles formed once per call (unpacked prefix)",
                      "ms_per_call_in_cta_unpack": packed_ms})
         osc.oscar_destroy(ctx)
         del pool, slab, kd, vd, kn, vn, q, out

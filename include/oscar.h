@@ -342,25 +342,28 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
  *  workspace: device scratch of at least oscar_extend_workspace_size(cfg,
  *  total_tokens) bytes (256-byte aligned, no initialisation); it holds q R_K for
  *  every query row and R_V^T (one per kv head with rotation_per_kv_head).  With
- *  oscar_extend_workspace_size_unpacked(cfg, total_tokens, batch, max_prefix)
- *  bytes or more, the unpacked-prefix form runs: a pre-pass dequantises every
- *  INT2 history tile (64 keys) of each request once per call into the workspace
- *  (T tiles per (request, kv head), T as many as fit), and the attention CTAs
- *  of all the request's query tiles copy those tiles instead of each unpacking
- *  the pages; a request whose prefix has more than T history tiles unpacks its
- *  own.  Both forms give identical outputs.  Softmax scale 1/sqrt(d), query
+ *  oscar_extend_workspace_size_unpacked(cfg, total_tokens, batch, max_prefix,
+ *  max_chunk) bytes or more, the unpacked-prefix form runs: a pre-pass forms
+ *  every 64-key tile that the query tiles of a request share (its INT2 history
+ *  tiles, dequantised; its BF16 window tiles; its chunk's own tiles) once per
+ *  call into the workspace, and the attention CTAs of all the request's query
+ *  tiles copy those tiles instead of each forming them from the pages and rows.
+ *  The workspace holds the window and chunk tiles for this max_chunk and T INT2
+ *  tiles per (request, kv head), T as many as fit; a request with more history
+ *  tiles forms its own.  Both forms give identical outputs.  Softmax scale 1/sqrt(d), query
  *  head h reads kv head h / (n_q_heads / n_kv_heads).  Kernels on the stream:
  *  the pre-pass (unpacked form), the query rotation, then the tensor-core
  *  attention (timing name "extend"). */
 oscar_status oscar_extend_workspace_size(const oscar_config* cfg, int32_t total_tokens, size_t* bytes);
 /* Workspace of the unpacked-prefix form for batch requests whose prefixes hold at
- * most max_prefix tokens: the base size plus, per (request, kv head), one
- * dequantised operand tile (42 KB at d = 128, 26 KB at d = 64) per 64 positions
- * of the INT2 history (672 B per history token and kv head at d = 128, against
- * the cache's 96 B: a working copy for one call).  Negative arguments:
- * OSCAR_ERR_INVALID. */
+ * most max_prefix tokens and whose chunks at most max_chunk (the max_chunk given
+ * to oscar_extend_attn): the base size plus, per (request, kv head), one operand
+ * tile (42 KB at d = 128, 26 KB at d = 64) per 64 positions of the INT2 history
+ * (672 B per history token and kv head at d = 128, against the cache's 96 B: a
+ * working copy for one call), of the BF16 window and of the chunk.  Negative
+ * arguments: OSCAR_ERR_INVALID. */
 oscar_status oscar_extend_workspace_size_unpacked(const oscar_config* cfg, int32_t total_tokens, int32_t batch,
-                                                  int32_t max_prefix, size_t* bytes);
+                                                  int32_t max_prefix, int32_t max_chunk, size_t* bytes);
 oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int32_t q_dtype, const void* K_new,
                                const void* V_new, int32_t kv_dtype, void* out, int32_t out_dtype,
                                const int32_t* cu_seqlens, const int32_t* prefix_lens, int32_t batch,

@@ -84,7 +84,7 @@ _SIGS = {
     "oscar_decode_attn_noalloc": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32,
                                          _i32, _vp, _vp, _vp]),
     "oscar_extend_workspace_size": (_i32, [_cfgp, _i32, ctypes.POINTER(ctypes.c_size_t)]),
-    "oscar_extend_workspace_size_unpacked": (_i32, [_cfgp, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)]),
+    "oscar_extend_workspace_size_unpacked": (_i32, [_cfgp, _i32, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)]),
     "oscar_extend_step": (_i32, [_vp, _i32, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _vp,
                                  _i32, _vp, _vp, _vp, _f32, _f32, _vp, ctypes.c_size_t, _vp]),
     "oscar_extend_attn": (_i32, [_vp, _i32, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _vp,
@@ -290,9 +290,10 @@ def oscar_extend_workspace_size(cfg: oscar_config, total_tokens: int) -> int:
     return out.value
 
 
-def oscar_extend_workspace_size_unpacked(cfg: oscar_config, total_tokens: int, batch: int, max_prefix: int) -> int:
+def oscar_extend_workspace_size_unpacked(cfg: oscar_config, total_tokens: int, batch: int, max_prefix: int,
+                                         max_chunk: int) -> int:
     out = ctypes.c_size_t()
-    _check(load().oscar_extend_workspace_size_unpacked(ctypes.byref(cfg), total_tokens, batch, max_prefix,
+    _check(load().oscar_extend_workspace_size_unpacked(ctypes.byref(cfg), total_tokens, batch, max_prefix, max_chunk,
                                                        ctypes.byref(out)))
     return out.value
 

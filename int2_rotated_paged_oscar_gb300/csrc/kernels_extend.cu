@@ -376,12 +376,83 @@ __device__ __forceinline__ void unpack_int2_tile(const uint8_t* raw, uint8_t* st
   }
 }
 
-// Pre-pass of the unpacked-prefix form: every INT2 history tile of every (request, kv head)
-// is dequantised once per call into the workspace, as the image of an attention stage
-// (XLayout<D>::STAGE bytes, padding zero), so that the attention CTAs of all the request's
-// query tiles bulk-copy it instead of each unpacking it.  Grid (tile j, kv head, request),
-// 128 threads; tiles past a request's history exit at once.  A page outside the block table
-// or the pool is flagged as in the attention kernel.
+// Where the K / V rows of a BF16 tile come from: window tiles read the request's slab slots
+// (sink slots [0, n_sink), recent slots [S, S + n_rec)), chunk tiles the call's own K / V rows
+// (chunk keys below kend); other keys are zero.
+struct PlainSrc {
+  int kind, base;
+  int n_sink, S, n_rec, kend, c0, kvh, Hkv, window, D;
+  const uint16_t* slab_req;   // this request's and kv head's K slab (V follows after window rows)
+  const uint16_t* K_new;
+  const uint16_t* V_new;
+  __device__ const uint16_t* row(int key, int kv) const {
+    if (kind == kTileWindow) {
+      const int slot = base + key;
+      const bool ok = slot < n_sink || (slot >= S && slot < S + n_rec);
+      return ok ? slab_req + ((size_t)kv * window + slot) * D : nullptr;
+    }
+    const int kc = base + key;
+    if (kc >= kend) return nullptr;
+    return (kv ? V_new : K_new) + ((size_t)(c0 + kc) * Hkv + kvh) * D;
+  }
+};
+
+// BF16 window or chunk tile into a stage: K rows copied into the swizzled K tile, V rows
+// transposed, by 128 threads u = 0..127.  Used by the attention kernel and by the pre-pass.
+template <int D>
+__device__ __forceinline__ void unpack_plain_tile(const PlainSrc& src, uint8_t* stg, int u) {
+  using L = XLayout<D>;
+  constexpr int KI = kXKeys * (D / 8) / 128;   // 16-byte K pieces per thread
+  uint4 kv[KI];
+#pragma unroll
+  for (int m = 0; m < KI; ++m) {
+    const int item = u + 128 * m;
+    const int key = item / (D / 8), cc = item % (D / 8);
+    const uint16_t* row = src.row(key, 0);
+    kv[m] = row ? *reinterpret_cast<const uint4*>(row + 8 * cc) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  uint4 vr[8];
+  const bool vt = u < D;   // thread (channel block hw8, keys 8kb..8kb+7)
+  const int hw8 = u % (D / 8), kb8 = u / (D / 8);
+  if (vt) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint16_t* row = src.row(8 * kb8 + k, 1);
+      vr[k] = row ? *reinterpret_cast<const uint4*>(row + 8 * hw8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < KI; ++m) {
+    const int item = u + 128 * m;
+    const int key = item / (D / 8), cc = item % (D / 8);
+    *reinterpret_cast<uint4*>(stg + L::KT + sw128_offset(key, 8 * cc, kXKeys)) = kv[m];
+  }
+  if (vt) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+      uint32_t c[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint4 x = vr[2 * p], y = vr[2 * p + 1];
+        const uint32_t xs = (e >> 1) == 0 ? x.x : ((e >> 1) == 1 ? x.y : ((e >> 1) == 2 ? x.z : x.w));
+        const uint32_t ys = (e >> 1) == 0 ? y.x : ((e >> 1) == 1 ? y.y : ((e >> 1) == 2 ? y.z : y.w));
+        c[p] = prmt(xs, ys, sel);
+      }
+      *reinterpret_cast<uint4*>(stg + L::VT + sw128_offset(8 * hw8 + e, 8 * kb8, D)) =
+          make_uint4(c[0], c[1], c[2], c[3]);
+    }
+  }
+}
+
+// Pre-pass of the unpacked-prefix form: every tile that the attention CTAs of a request share
+// (its INT2 history tiles, dequantised; its BF16 window tiles; its chunk's own tiles, the V rows
+// transposed) is formed once per call into the workspace, as the image of an attention stage
+// (XLayout<D>::STAGE bytes, padding zero), so that the CTAs of all the request's query tiles
+// bulk-copy it instead of each forming it.  Per (request, kv head): prep_tiles INT2 tiles, then
+// prep_wt window tiles, then prep_ct chunk tiles.  Grid (tile, kv head, request), 128 threads;
+// tiles past a request's own exit at once.  A page outside the block table or the pool is
+// flagged as in the attention kernel.
 template <int D>
 __global__ void __launch_bounds__(128) extend_unpack_kernel(ExtendArgs a) {
   using L = XLayout<D>;
@@ -394,6 +465,46 @@ __global__ void __launch_bounds__(128) extend_unpack_kernel(ExtendArgs a) {
   const int n_pre = a.prefix_lens[b];
   if (n_pre < 0 || (long long)n_pre > (long long)g.max_pages_per_req * g.P) return;   // flagged by the attention
   const int hist_end = max(g.S, n_pre - g.W);
+  uint4* out = reinterpret_cast<uint4*>(
+      a.prep + (((size_t)b * g.Hkv + kvh) * (a.prep_tiles + a.prep_wt + a.prep_ct) + j) * L::STAGE);
+  if (j >= a.prep_tiles) {
+    // a BF16 tile: window slots of the request's slab, or the chunk's own K / V rows
+    PlainSrc ps;
+    const int c0 = a.cu_seqlens[b], len = a.cu_seqlens[b + 1] - c0;
+    ps.n_sink = min(g.S, n_pre);
+    ps.S = g.S;
+    ps.n_rec = n_pre > g.S ? n_pre - hist_end : 0;
+    ps.kend = len;
+    ps.c0 = c0;
+    ps.kvh = kvh;
+    ps.Hkv = g.Hkv;
+    ps.window = g.window();
+    ps.D = D;
+    ps.K_new = a.K_new;
+    ps.V_new = a.V_new;
+    ps.slab_req = nullptr;
+    if (j < a.prep_tiles + a.prep_wt) {
+      const int w = j - a.prep_tiles;
+      const int win_end = ps.n_rec > 0 ? g.S + ps.n_rec : ps.n_sink;
+      if (64 * w >= win_end) return;
+      const int req = a.req_slot[b];
+      if (req < 0 || req >= g.max_req) return;   // flagged by the attention
+      ps.kind = kTileWindow;
+      ps.base = 64 * w;
+      ps.slab_req = a.slab + ((size_t)a.layer * g.max_req + req) * g.slab_req_elems() + (size_t)kvh * 2 * g.window() * D;
+    } else {
+      const int c = j - a.prep_tiles - a.prep_wt;
+      if (len < 0 || c0 < 0 || c0 + len > a.total_tokens || 64 * c >= len) return;   // flagged by the attention
+      ps.kind = kTileChunk;
+      ps.base = 64 * c;
+    }
+    for (int q = u; q < L::STAGE / 16; q += 128) reinterpret_cast<uint4*>(stg)[q] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    unpack_plain_tile<D>(ps, stg, u);
+    __syncthreads();
+    for (int q = u; q < L::STAGE / 16; q += 128) out[q] = reinterpret_cast<const uint4*>(stg)[q];
+    return;
+  }
   if (hist_end <= g.S) return;
   const int u0 = g.S / 64;
   if (j > (hist_end - 1) / 64 - u0) return;
@@ -419,7 +530,6 @@ __global__ void __launch_bounds__(128) extend_unpack_kernel(ExtendArgs a) {
   unpack_int2_tile<D>(raw, stg, u, base, g.S, hist_end, pshift, pmask, BB, g, a.code_magic,
                       static_cast<uint32_t>(a.k_exp_K) << 23, static_cast<uint32_t>(a.k_exp_V) << 23);
   __syncthreads();
-  uint4* out = reinterpret_cast<uint4*>(a.prep + (((size_t)b * g.Hkv + kvh) * a.prep_tiles + j) * L::STAGE);
   for (int q = u; q < L::STAGE / 16; q += 128) out[q] = reinterpret_cast<const uint4*>(stg)[q];
 }
 
@@ -480,8 +590,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   const int kend = min(len, i0 + tq);
   tl.nC = (kend + 63) / 64;
   const int n_tiles = tl.n();
-  // unpacked-prefix form: this request's INT2 tiles were dequantised by the pre-pass
-  const bool use_prep = PREP && a.prep != nullptr && tl.nR <= a.prep_tiles;
+  // unpacked-prefix form: this request's tiles were formed by the pre-pass
+  const bool use_prep = PREP && a.prep != nullptr && tl.nR <= a.prep_tiles && tl.nW <= a.prep_wt && tl.nC <= a.prep_ct;
   int req = 0;
   if (tl.nW > 0) {
     req = a.req_slot[b];
@@ -691,62 +801,25 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     unpack_int2_tile<D>(smem + L::RAW0 + (j % L::NRAW) * L::RAW_BYTES, stg, u, tl.base(j), tl.S, tl.hist_end,
                         pshift, pmask, BB, g, a.code_magic, kK23, kV23);
   };
-  // BF16 window or chunk tile: K rows copied into the swizzled K tile, V rows transposed
-  auto plain_row = [&](int kind, int base, int key, int kv) -> const uint16_t* {
-    if (kind == kTileWindow) {
-      const int slot = base + key;
-      const bool ok = slot < tl.n_sink || (slot >= tl.S && slot < tl.S + tl.n_rec);
-      return ok ? slab_req + ((size_t)kv * g.window() + slot) * D : nullptr;
-    }
-    const int kc = base + key;
-    if (kc >= kend) return nullptr;
-    const uint16_t* src = kv ? a.V_new : a.K_new;
-    return src + ((size_t)(c0 + kc) * g.Hkv + kvh) * D;
+  auto plain_src = [&](int j) {
+    PlainSrc ps;
+    ps.kind = tl.kind(j);
+    ps.base = tl.base(j);
+    ps.n_sink = tl.n_sink;
+    ps.S = tl.S;
+    ps.n_rec = tl.n_rec;
+    ps.kend = kend;
+    ps.c0 = c0;
+    ps.kvh = kvh;
+    ps.Hkv = g.Hkv;
+    ps.window = g.window();
+    ps.D = D;
+    ps.slab_req = slab_req;
+    ps.K_new = a.K_new;
+    ps.V_new = a.V_new;
+    return ps;
   };
-  auto unpack_plain = [&](int j, uint8_t* stg) {
-    const int kind = tl.kind(j), base = tl.base(j);
-    constexpr int KI = kXKeys * (D / 8) / 128;   // 16-byte K pieces per thread
-    uint4 kv[KI];
-#pragma unroll
-    for (int m = 0; m < KI; ++m) {
-      const int item = u + 128 * m;
-      const int key = item / (D / 8), cc = item % (D / 8);
-      const uint16_t* row = plain_row(kind, base, key, 0);
-      kv[m] = row ? *reinterpret_cast<const uint4*>(row + 8 * cc) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    uint4 vr[8];
-    const bool vt = u < D;   // thread (channel block hw8, keys 8kb..8kb+7)
-    const int hw8 = u % (D / 8), kb8 = u / (D / 8);
-    if (vt) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint16_t* row = plain_row(kind, base, 8 * kb8 + k, 1);
-        vr[k] = row ? *reinterpret_cast<const uint4*>(row + 8 * hw8) : make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < KI; ++m) {
-      const int item = u + 128 * m;
-      const int key = item / (D / 8), cc = item % (D / 8);
-      *reinterpret_cast<uint4*>(stg + L::KT + sw128_offset(key, 8 * cc, kXKeys)) = kv[m];
-    }
-    if (vt) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-        uint32_t c[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const uint4 x = vr[2 * p], y = vr[2 * p + 1];
-          const uint32_t xs = (e >> 1) == 0 ? x.x : ((e >> 1) == 1 ? x.y : ((e >> 1) == 2 ? x.z : x.w));
-          const uint32_t ys = (e >> 1) == 0 ? y.x : ((e >> 1) == 1 ? y.y : ((e >> 1) == 2 ? y.z : y.w));
-          c[p] = prmt(xs, ys, sel);
-        }
-        *reinterpret_cast<uint4*>(stg + L::VT + sw128_offset(8 * hw8 + e, 8 * kb8, D)) =
-            make_uint4(c[0], c[1], c[2], c[3]);
-      }
-    }
-  };
+  auto unpack_plain = [&](int j, uint8_t* stg) { unpack_plain_tile<D>(plain_src(j), stg, u); };
   // tile j into stage j % NST; false when an INT2 tile's pages did not arrive in time (the
   // status word is flagged; the caller stops at its next barrier)
   auto unpack = [&](int j) -> bool {
@@ -992,7 +1065,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       if (lane == 0) mbar_arrive(&p_full[i & 1]);
     }
   } else if (warp < 8) {
-    int copies_issued = 0;   // unpacked form, warp 4 lane 0: INT2 tiles [0, copies_issued) requested
+    int copies_issued = 0;   // unpacked form, warp 4 lane 0: tiles [0, copies_issued) requested
     int copies_done = 0;     // tiles [0, copies_done) known to have landed (their stage was freed since)
     for (int j = 0; j < n_tiles; ++j) {
       // stage j % NST was last read by tile j - NST's MMAs
@@ -1005,15 +1078,18 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         break;
       }
       if (j >= L::NST) copies_done = j - L::NST + 1;
-      if (use_prep && j < tl.nR) {
-        // the tile's dequantised image: one bulk copy into its stage by warp 4 lane 0, whose
-        // arrival carries the bytes; warps 5-7 arrive at once
+      if (use_prep) {
+        // the tile's image: one bulk copy into its stage by warp 4 lane 0, whose arrival
+        // carries the bytes; warps 5-7 arrive at once
         if (lane == 0) {
           uint64_t* bar = &kv_full[j % L::NST];
           if (warp == 4) {
+            const int pj = j < tl.nR ? j : (j < tl.nR + tl.nW ? a.prep_tiles + (j - tl.nR)
+                                                              : a.prep_tiles + a.prep_wt + (j - tl.nR - tl.nW));
             mbar_arrive_expect_tx(bar, (uint32_t)L::STAGE);
             bulk_g2s(smem + L::ST0 + (j % L::NST) * L::STAGE,
-                     a.prep + (((size_t)b * g.Hkv + kvh) * a.prep_tiles + j) * L::STAGE, (uint32_t)L::STAGE, bar);
+                     a.prep + (((size_t)b * g.Hkv + kvh) * (a.prep_tiles + a.prep_wt + a.prep_ct) + pj) * L::STAGE,
+                     (uint32_t)L::STAGE, bar);
             copies_issued = j + 1;
           } else {
             mbar_arrive(bar);
@@ -1203,7 +1279,8 @@ int launch_extend_d(const ExtendArgs& a, void* stream) {
   if (a.prep) {
     const size_t usm = XLayout<D>::STAGE + XLayout<D>::RAW_BYTES + 1024;
     if ((e = ensure_smem_limit(extend_unpack_kernel<D>, usm)) != cudaSuccess) return (int)e;
-    extend_unpack_kernel<D><<<dim3((unsigned)a.prep_tiles, (unsigned)a.g.Hkv, (unsigned)a.batch), 128, usm, s>>>(a);
+    const unsigned tiles = (unsigned)(a.prep_tiles + a.prep_wt + a.prep_ct);
+    extend_unpack_kernel<D><<<dim3(tiles, (unsigned)a.g.Hkv, (unsigned)a.batch), 128, usm, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
   }
   extend_qrot_kernel<D><<<dim3(qgrid, heads), 256, qsm, s>>>(a);
@@ -1235,6 +1312,15 @@ size_t extend_prep_tile_bytes(int D) { return D == 128 ? XLayout<128>::STAGE : X
 long long extend_prep_tiles(const Geom& g, long long max_prefix) {
   const long long hist_end = max_prefix - g.W > g.S ? max_prefix - g.W : g.S;
   return hist_end > g.S ? (hist_end - 1) / 64 - g.S / 64 + 1 : 0;
+}
+
+int extend_prep_window_tiles(const Geom& g) { return (g.S + g.W + 63) / 64; }
+
+long long extend_prep_chunk_tiles(const Geom& g, long long max_chunk) {
+  // the attention grid covers ceil(max_chunk / tq) query tiles of tq tokens, so a chunk may hold
+  // up to that many tokens (more is flagged)
+  const long long tq = kXRows / g.gq();
+  return ((max_chunk + tq - 1) / tq * tq + 63) / 64;
 }
 
 int launch_extend(const ExtendArgs& a, void* stream) {

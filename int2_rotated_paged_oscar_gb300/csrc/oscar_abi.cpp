@@ -909,13 +909,14 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 }  // namespace
 
 oscar_status oscar_extend_workspace_size_unpacked(const oscar_config* cfg, int32_t total_tokens, int32_t batch,
-                                                  int32_t max_prefix, size_t* bytes) {
+                                                  int32_t max_prefix, int32_t max_chunk, size_t* bytes) {
   Geom g;
   oscar_status st = validate(cfg, &g);
   if (st != OSCAR_OK) return st;
-  if (!bytes || total_tokens < 0 || batch < 0 || max_prefix < 0)
+  if (!bytes || total_tokens < 0 || batch < 0 || max_prefix < 0 || max_chunk < 0)
     return fail(OSCAR_ERR_INVALID, "bad arguments to extend workspace size");
-  const long long tiles = oscar::extend_prep_tiles(g, max_prefix);
+  const long long tiles = oscar::extend_prep_tiles(g, max_prefix) + oscar::extend_prep_window_tiles(g) +
+                          oscar::extend_prep_chunk_tiles(g, max_chunk);
   *bytes = align256(oscar::extend_workspace_bytes(g, total_tokens)) +
            (size_t)batch * g.Hkv * (size_t)tiles * oscar::extend_prep_tile_bytes(g.D);
   return OSCAR_OK;
@@ -978,21 +979,23 @@ oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
   a.k_exp_K = ek;
   a.k_exp_V = ev;
   a.code_magic = oscar::kCodeMagic;
-  // unpacked-prefix form when the workspace holds at least one tile per (request, kv head)
-  // past the base: as many tiles per pair as fit, at most what the longest prefix can have
+  // unpacked-prefix form when the workspace holds, past the base, the window and chunk tiles
+  // of every (request, kv head): then as many INT2 tiles per pair as fit, at most what the
+  // longest prefix can have
   a.prep = nullptr;
-  a.prep_tiles = 0;
+  a.prep_tiles = a.prep_wt = a.prep_ct = 0;
   {
     const size_t base = align256(need);
     const size_t per_tile = (size_t)batch * ctx->g.Hkv * oscar::extend_prep_tile_bytes(ctx->g.D);
-    if (ws_bytes >= base + per_tile) {
-      long long tiles = (long long)((ws_bytes - base) / per_tile);
+    const long long fixed = oscar::extend_prep_window_tiles(ctx->g) + oscar::extend_prep_chunk_tiles(ctx->g, max_chunk);
+    if (ws_bytes >= base && (long long)((ws_bytes - base) / per_tile) >= fixed) {
+      long long tiles = (long long)((ws_bytes - base) / per_tile) - fixed;
       const long long cap = oscar::extend_prep_tiles(ctx->g, (long long)ctx->g.max_pages_per_req * ctx->g.P);
       if (tiles > cap) tiles = cap;
-      if (tiles > 0) {
-        a.prep = a.ws + base;
-        a.prep_tiles = (int)tiles;
-      }
+      a.prep = a.ws + base;
+      a.prep_tiles = (int)tiles;
+      a.prep_wt = oscar::extend_prep_window_tiles(ctx->g);
+      a.prep_ct = (int)oscar::extend_prep_chunk_tiles(ctx->g, max_chunk);
     }
   }
   LaunchScope ls(ctx, "extend", stream);

@@ -143,16 +143,20 @@ struct ExtendArgs {
   size_t rvt_off, qrot_off;
   int k_exp_K, k_exp_V;
   unsigned code_magic;
-  // unpacked-prefix form (null: every attention CTA unpacks its INT2 tiles itself): the
-  // pre-pass writes tile j of (request b, kv head h) at prep + ((b Hkv + h) prep_tiles + j) *
-  // extend_prep_tile_bytes(D); requests with more INT2 tiles than prep_tiles unpack themselves
+  // unpacked-prefix form (null: every attention CTA forms its tiles itself): per (request b,
+  // kv head h) the pre-pass writes prep_tiles INT2 tiles, prep_wt window tiles and prep_ct
+  // chunk tiles, tile j at prep + ((b Hkv + h) (prep_tiles + prep_wt + prep_ct) + j) *
+  // extend_prep_tile_bytes(D); a request with more tiles of a kind forms its own
   uint8_t* prep;
-  int prep_tiles;
+  int prep_tiles, prep_wt, prep_ct;
 };
 size_t extend_workspace_bytes(const Geom& g, long long total_tokens);
 size_t extend_prep_tile_bytes(int D);
 // INT2 history tiles (64 keys) of a prefix of max_prefix tokens
 long long extend_prep_tiles(const Geom& g, long long max_prefix);
+// BF16 window tiles of a request, and chunk tiles of a chunk of at most max_chunk tokens
+int extend_prep_window_tiles(const Geom& g);
+long long extend_prep_chunk_tiles(const Geom& g, long long max_chunk);
 void extend_ws_offsets(const Geom& g, size_t* rvt_off, size_t* qrot_off);
 int launch_extend(const ExtendArgs& a, void* stream);
 // Self-test of the bounded-wait failure path: waits on an mbarrier that nothing arrives on.

@@ -386,7 +386,7 @@ def run_extend(gc: GpuCache, layer, q: np.ndarray, q_dtype: str, k_new: np.ndarr
     max_chunk = int(np.diff(cu).max()) if max_chunk is None else max_chunk
     if unpacked is not False:   # True: sized for the longest prefix; an int: for prefixes up to that length
         cap = int(max(prefix)) if unpacked is True else int(unpacked)
-        ws_bytes = osc.oscar_extend_workspace_size_unpacked(gc.cfg, total, b, cap)
+        ws_bytes = osc.oscar_extend_workspace_size_unpacked(gc.cfg, total, b, cap, max_chunk)
     else:
         ws_bytes = osc.oscar_extend_workspace_size(gc.cfg, total)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
