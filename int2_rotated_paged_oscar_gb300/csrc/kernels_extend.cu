@@ -130,18 +130,20 @@ struct XLayout {
 
 // ------------------------------------------------------------------ query rotation
 // q' = q R_K for every (chunk token, query head) row, float32, into the workspace; the
-// last CTA writes R_V^T for the epilogues.  CTA: 64 rows x D columns, thread (row t/4,
-// column set t%4: the float4 columns 4 (t%4) + 16 m, so that the four threads of a row
-// read R from four different bank groups); q rows padded by one float (row stride D + 1
-// puts the eight rows a warp reads in different banks).
+// last CTA writes R_V^T for the epilogues.  CTA: 64 rows x D columns with R in shared
+// memory and q transposed beside it ([D][64 + 4]); thread t owns rows 4 (t / 16) .. + 3 and
+// the float4 columns (t % 16) + 16 k, so that per step i one float4 of q (four rows) and D / 64
+// float4 of R row i feed 4 x D / 16 fused multiply-adds.  Every output is the chain
+// fma(q_i, R[i][c], .) over i = 0 .. D - 1.
+constexpr int kQsPad = 4;   // q^T row stride 64 + 4 floats: 16-byte aligned rows
 template <int D>
-__host__ __device__ constexpr size_t qrot_smem_floats() { return (size_t)D * D + 64 * (D + 1); }
+__host__ __device__ constexpr size_t qrot_smem_floats() { return (size_t)D * D + (size_t)D * (64 + kQsPad); }
 
 template <int D>
 __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
   extern __shared__ __align__(16) float xq_sm[];
   float* Rs = xq_sm;              // [D][D]
-  float* qs = xq_sm + D * D;      // [64][D + 1]
+  float* qt = xq_sm + D * D;      // [D][64 + kQsPad]: q transposed
   const int t = threadIdx.x;
   const Geom& g = a.g;
   const long long rows = (long long)a.total_tokens * g.Hq;
@@ -175,33 +177,40 @@ __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
       const size_t e = (size_t)r * D + idx % D;
       v = __uint_as_float((uint32_t) static_cast<const uint16_t*>(a.q)[e] << 16);   // BF16 query
     }
-    qs[(idx / D) * (D + 1) + idx % D] = v;
+    qt[(idx % D) * (64 + kQsPad) + idx / D] = v;
   }
   __syncthreads();
-  constexpr int NM = D / 16;   // float4 columns per thread
-  const int rr = t >> 2, cq = t & 3;
-  float4 acc[NM];
+  constexpr int NC4 = D / 64;   // float4 columns per thread
+  const int rg = t >> 4, cg = t & 15;
+  float4 acc[4][NC4];
 #pragma unroll
-  for (int m = 0; m < NM; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float* qrow = qs + rr * (D + 1);
+  for (int rw = 0; rw < 4; ++rw)
+#pragma unroll
+    for (int k = 0; k < NC4; ++k) acc[rw][k] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int i = 0; i < D; ++i) {
-    const float qi = qrow[i];
-    const float4* rrow = reinterpret_cast<const float4*>(Rs + i * D + 4 * cq);
+    const float4 qv = *reinterpret_cast<const float4*>(qt + i * (64 + kQsPad) + 4 * rg);
+    const float qr[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-    for (int m = 0; m < NM; ++m) {
-      const float4 rv = rrow[4 * m];
-      acc[m].x = fmaf(qi, rv.x, acc[m].x);
-      acc[m].y = fmaf(qi, rv.y, acc[m].y);
-      acc[m].z = fmaf(qi, rv.z, acc[m].z);
-      acc[m].w = fmaf(qi, rv.w, acc[m].w);
+    for (int k = 0; k < NC4; ++k) {
+      const float4 rv = *reinterpret_cast<const float4*>(Rs + i * D + 4 * (cg + 16 * k));
+#pragma unroll
+      for (int rw = 0; rw < 4; ++rw) {
+        acc[rw][k].x = fmaf(qr[rw], rv.x, acc[rw][k].x);
+        acc[rw][k].y = fmaf(qr[rw], rv.y, acc[rw][k].y);
+        acc[rw][k].z = fmaf(qr[rw], rv.z, acc[rw][k].z);
+        acc[rw][k].w = fmaf(qr[rw], rv.w, acc[rw][k].w);
+      }
     }
   }
-  const long long r = row_of(rr);
-  if (r < rows) {
-    float4* dst = reinterpret_cast<float4*>(qrot + (size_t)r * D + 4 * cq);
 #pragma unroll
-    for (int m = 0; m < NM; ++m) dst[4 * m] = acc[m];
+  for (int rw = 0; rw < 4; ++rw) {
+    const long long r = row_of(4 * rg + rw);
+    if (r < rows) {
+      float4* dst = reinterpret_cast<float4*>(qrot + (size_t)r * D);
+#pragma unroll
+      for (int k = 0; k < NC4; ++k) dst[cg + 16 * k] = acc[rw][k];
+    }
   }
 }
 
