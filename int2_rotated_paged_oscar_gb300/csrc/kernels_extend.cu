@@ -159,12 +159,33 @@ __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
     }
     return;
   }
-  for (int idx = t; idx < D * D / 4; idx += 256)
-    reinterpret_cast<float4*>(Rs)[idx] =
-        __ldg(reinterpret_cast<const float4*>(a.R_K + (size_t)kvh * g.rot_stride()) + idx);
   // global row of local row l: one rotation per layer, rows 64 x + l of [tokens][Hq]; one per kv
   // head, the 64 / gq tokens x gq query heads of kv head kvh starting at token (64 / gq) x
   const int gq = g.gq();
+  {
+    // The attention reads q' only for requests with INT2 history tiles: a CTA whose rows all
+    // belong to requests without history (every request of a prefill from scratch) stops here.
+    const long long tok0 = g.rph ? (long long)blockIdx.x * (64 / gq) : (long long)blockIdx.x * 64 / g.Hq;
+    long long tok1 = g.rph ? tok0 + 64 / gq - 1 : ((long long)blockIdx.x * 64 + 63) / g.Hq;
+    if (tok1 >= a.total_tokens) tok1 = a.total_tokens - 1;
+    auto request_of = [&](long long tk) {   // largest b with cu_seqlens[b] <= tk
+      int lo = 0, hi = a.batch - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.cu_seqlens[mid] <= tk) lo = mid; else hi = mid - 1;
+      }
+      return lo;
+    };
+    if (tok0 <= tok1) {
+      const int b0 = request_of(tok0), b1 = request_of(tok1);
+      bool need = b1 - b0 > 64;
+      for (int bb = b0; !need && bb <= b1; ++bb) need = a.prefix_lens[bb] - g.W > g.S;
+      if (!need) return;
+    }
+  }
+  for (int idx = t; idx < D * D / 4; idx += 256)
+    reinterpret_cast<float4*>(Rs)[idx] =
+        __ldg(reinterpret_cast<const float4*>(a.R_K + (size_t)kvh * g.rot_stride()) + idx);
   auto row_of = [&](int l) -> long long {
     if (!g.rph) return (long long)blockIdx.x * 64 + l;
     const long long tok = (long long)blockIdx.x * (64 / gq) + l / gq;
@@ -1197,7 +1218,9 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   const int half = (tid >> 7) & 1;
   constexpr int NJ = D / 2;
   const int j0 = half * NJ;
-  if (warp < 8) {
+  // with no INT2 tile the rotated accumulator holds zeros, and y R_V^T is zero: out = O_plain / l
+  const bool rotated = tl.nR > 0;
+  if (warp < 8 && rotated) {
     const float4* rvt = reinterpret_cast<const float4*>(a.ws + a.rvt_off + (g.rph ? (size_t)kvh * D * D * 4 : 0));
     for (int idx = tid; idx < D * D / 4; idx += 256) reinterpret_cast<float4*>(Rt)[idx] = rvt[idx];
     if (warp < 4) linv[r] = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -1224,6 +1247,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       }
     }
   }
+  if (warp < 4 && !rotated) linv[r] = l_run > 0.f ? 1.f / l_run : 0.f;
   __syncthreads();
   if (warp < 8) {
     // the TMEM loads are warp-collective: every lane takes part, rows outside the chunk included
@@ -1238,7 +1262,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     }
     const float* yr = Y + r * L::YS;
 #pragma unroll 2
-    for (int i = 0; i < D; ++i) {
+    for (int i = 0; rotated && i < D; ++i) {
       const float yi = yr[i];
       const float4* rt = reinterpret_cast<const float4*>(Rt + i * D + j0);
 #pragma unroll
