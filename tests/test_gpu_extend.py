@@ -170,7 +170,8 @@ def test_extend_flags_host_sizes_that_miss_a_chunk(osc):
 
 def test_extend_step_equals_extend_then_write(osc):
     """oscar_extend_step = oscar_extend_attn then oscar_write_kv of the chunk: the same outputs and the same
-    cache bytes (pages and window slots), bit for bit; then a decode over the extended cache matches the oracle."""
+    cache bytes (pages and window slots), bit for bit; then a decode over the extended cache matches the oracle.
+    The step runs with the unpacked-prefix workspace, the separate calls with the base one."""
     import torch
     shape = syn.Shape(32, 8, 128, 64, 32, 4, 128, 1)
     wl = syn.Workload("xstep", shape, [0], seed=47, dtype="bf16")
@@ -186,7 +187,8 @@ def test_extend_step_equals_extend_then_write(osc):
             k, v = syn.kv_tokens(wl, 0, total, sub=11)
             q = syn.queries(wl, 0, total, sub=12)
             cu = np.array([0, chunks[0], total], np.int32)
-            ws_bytes = osc.oscar_extend_workspace_size(gc.cfg, total)
+            ws_bytes = (osc.oscar_extend_workspace_size_unpacked(gc.cfg, total, 2, max(prefix), max(chunks)) if fused
+                        else osc.oscar_extend_workspace_size(gc.cfg, total))
             ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
             out = torch.empty((total, shape.n_q_heads, shape.head_dim), dtype=torch.float32, device="cuda")
             args = (H.dev_input(q, "bf16"), osc.DTYPE_BF16, H.dev_input(k, "bf16"), H.dev_input(v, "bf16"),

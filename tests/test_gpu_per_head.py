@@ -114,6 +114,9 @@ def test_per_head_rotations_all_equal_match_the_per_layer_path_bit_for_bit(osc, 
         xa = H.run_extend(ga, 0, qx, "bf16", kc, vc, cu, cur, bt, [0, 1], fx)
         xb = H.run_extend(gb, 0, qx, "bf16", kc, vc, cu, cur, bt, [0, 1], fx8)
         assert np.array_equal(xa, xb)
+        # the unpacked-prefix form too (its pre-pass forms the same tiles in either context)
+        xb_u = H.run_extend(gb, 0, qx, "bf16", kc, vc, cu, cur, bt, [0, 1], fx8, unpacked=True)
+        assert np.array_equal(xb_u, xa)
     finally:
         ga.close()
         gb.close()
@@ -166,6 +169,8 @@ def test_per_head_rotations_parity(osc, dtype):
         qx = syn.as_input(syn.queries(wl, 0, 2 * t, sub=302), "bf16")
         cux = np.array([0, t, 2 * t], np.int32)
         got = H.run_extend(gc, 0, qx, "bf16", kc, vc, cux, cur, bt, slots, fx)
+        got_u = H.run_extend(gc, 0, qx, "bf16", kc, vc, cux, cur, bt, slots, fx, unpacked=True)
+        assert np.array_equal(got_u, got), "unpacked-prefix form with a rotation per kv head"
         want = attention.extend(gimg, 0, qx, kc, vc, cux, cur, bt, slots, fx["R_K"], fx["R_V"])
         H.assert_decode_close(got, want)
     finally:
