@@ -97,14 +97,15 @@ struct XLayout {
   static constexpr int RAW_BYTES = kXKeys * 3 * D / 4;           // 64 INT2 tokens: codes and (scale, zero) of K, V
   static constexpr int RAW0 = ST0 + NST * STAGE;
   static constexpr int BAR = RAW0 + NRAW * RAW_BYTES;
-  // s_full[2], pv_done, kv_full[NST], kv_empty[NST], p_full[2], raw_full[NRAW]; then the TMEM
-  // slot, the abort flag
-  static constexpr int NBAR = 2 + 1 + 2 * NST + 2 + NRAW;
+  // s_full[2], pv_done, kv_full[NST], kv_empty[NST], p_full[2], raw_full[NRAW], epi_copy,
+  // epi_mma; then the TMEM slot, the abort flag
+  static constexpr int NBAR = 2 + 1 + 2 * NST + 2 + NRAW + 2;
   static constexpr int BYTES = BAR + NBAR * 8 + 16;
   static constexpr int SMEM = BYTES + 1024;
-  // epilogue reuse (after the last MMA): R_V^T [D][D] f32 from 0, then y [128][D+1] f32, then 1/l [128]
-  static constexpr int YS = D + 1;
-  static constexpr int RT = 0, Y = (D * D * 4 + 1023) / 1024 * 1024, LINV = Y + kXRows * YS * 4;
+  // epilogue reuse (after the last MMA): R_V as f16 hi and lo planes (the B operand of y R_V^T,
+  // K-major, 128-byte swizzle) from 0, then 1/l [128]
+  static constexpr int RP = 0, RP_BYTES = 2 * D * D * 2;
+  static constexpr int LINV = (RP_BYTES + 1023) / 1024 * 1024;
   // TMEM columns
   // the V centre accumulator (16 columns) directly follows the rotated one: one PV MMA with
   // N = D + 16 reads the Zv rows that follow the Vt rows in shared memory
@@ -123,14 +124,15 @@ struct XLayout {
   static_assert(STAGE % 1024 == 0 && ST0 % 1024 == 0, "operand tiles 1024-aligned");
   static_assert(C_QZ + 8 <= TMEM_COLS && C_P2 + kXKeys <= TMEM_COLS, "TMEM plan");
   static_assert(ZV == VT + D * 128, "Zv rows follow the Vt rows");
-  static_assert(LINV + kXRows * 4 <= RAW0, "R_V^T, y and 1/l fit below the raw buffers");
+  static_assert(LINV + kXRows * 4 <= RAW0, "the R_V planes and 1/l fit below the raw buffers");
   static_assert(RAW0 % 16 == 0 && RAW_BYTES % 16 == 0, "bulk copy destinations 16-byte aligned");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 // ------------------------------------------------------------------ query rotation
 // q' = q R_K for every (chunk token, query head) row, float32, into the workspace; the
-// last CTA writes R_V^T for the epilogues.  CTA: 64 rows x D columns with R in shared
+// last CTA writes R_V as f16 hi and lo planes (row n = output channel n, K-major with the
+// 128-byte swizzle: the B operand of the epilogue's y R_V^T on the tensor cores).  CTA: 64 rows x D columns with R in shared
 // memory and q transposed beside it ([D][64 + 4]); thread t owns rows 4 (t / 16) .. + 3 and
 // the float4 columns (t % 16) + 16 k, so that per step i one float4 of q (four rows) and D / 64
 // float4 of R row i feed 4 x D / 16 fused multiply-adds.  Every output is the chain
@@ -151,11 +153,22 @@ __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
   // blockIdx.y: the kv head whose rotation the CTA applies (0 with one rotation per layer)
   const int kvh = blockIdx.y;
   if (blockIdx.x == gridDim.x - 1) {
-    float* rvt = reinterpret_cast<float*>(a.ws + a.rvt_off) + (size_t)kvh * D * D;
+    uint8_t* rp = a.ws + a.rvp_off + (size_t)kvh * (2 * D * D * 2);
     const float* rv = a.R_V + (size_t)kvh * g.rot_stride();
-    for (int idx = t; idx < D * D; idx += 256) {
-      const int i = idx / D, j = idx % D;   // rvt[i][j] = R_V[j][i]; coalesced writes
-      rvt[idx] = __ldg(rv + (size_t)j * D + i);
+    for (int item = t; item < D * D / 8; item += 256) {   // 8 consecutive k of row n
+      const int n = item / (D / 8), k0 = 8 * (item % (D / 8));
+      const float4 x0 = __ldg(reinterpret_cast<const float4*>(rv + (size_t)n * D + k0));
+      const float4 x1 = __ldg(reinterpret_cast<const float4*>(rv + (size_t)n * D + k0 + 4));
+      const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        hi[q] = pack_half2(v[2 * q], v[2 * q + 1]);
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[q]));
+        lo[q] = pack_half2(v[2 * q] - hf.x, v[2 * q + 1] - hf.y);
+      }
+      *reinterpret_cast<uint4*>(rp + sw128_offset(n, k0, D)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(rp + D * D * 2 + sw128_offset(n, k0, D)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     return;
   }
@@ -580,6 +593,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   // (its scores need tile j's PV issued first)
   uint64_t* p_full = kv_empty + L::NST;
   uint64_t* raw_full = p_full + 2;         // [NRAW] raw buffer j % NRAW holds INT2 tile j's pages (bulk copies)
+  uint64_t* epi_copy = raw_full + L::NRAW;  // epilogue: the R_V planes arrived
+  uint64_t* epi_mma = epi_copy + 1;          // epilogue: y R_V^T done (commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR + 8 * L::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR + 8 * L::NBAR + 4);
 
@@ -651,6 +666,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       mbar_init(&p_full[0], 4);
       mbar_init(&p_full[1], 4);
       for (int rb = 0; rb < L::NRAW; ++rb) mbar_init(&raw_full[rb], 1);
+      mbar_init(epi_copy, 1);
+      mbar_init(epi_mma, 1);
       *abort_flag = 0;
       fence_barrier_init();
     }
@@ -1206,25 +1223,30 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   }
   (void)aborted;
 
-  // ---------------- epilogue: out = (O_plain + y R_V^T) / l
+  // ---------------- epilogue: out = O_plain / l + (y / l) R_V^T.  y / l goes to TMEM as f16 hi and
+  // lo planes over the dead score columns (the A operand), R_V's planes arrive by one bulk copy
+  // (the B operand), and three MMAs per K step (hi hi, hi lo, lo hi) leave y R_V^T / l in the
+  // rotated accumulator's columns.  A CTA without INT2 tiles has a zero rotated accumulator and
+  // skips all of it.
   bool ok = true;
   if (warp < 8) {
     ok = __all_sync(0xffffffffu, xwait(pv_done, (uint32_t)((n_tiles - 1) & 1), a.status));
     tc_fence_after();
   }
-  float* Rt = reinterpret_cast<float*>(smem + L::RT);
-  float* Y = reinterpret_cast<float*>(smem + L::Y);
   float* linv = reinterpret_cast<float*>(smem + L::LINV);
   const int half = (tid >> 7) & 1;
   constexpr int NJ = D / 2;
   const int j0 = half * NJ;
-  // with no INT2 tile the rotated accumulator holds zeros, and y R_V^T is zero: out = O_plain / l
-  const bool rotated = tl.nR > 0;
-  if (warp < 8 && rotated) {
-    const float4* rvt = reinterpret_cast<const float4*>(a.ws + a.rvt_off + (g.rph ? (size_t)kvh * D * D * 4 : 0));
-    for (int idx = tid; idx < D * D / 4; idx += 256) reinterpret_cast<float4*>(Rt)[idx] = rvt[idx];
-    if (warp < 4) linv[r] = l_run > 0.f ? 1.f / l_run : 0.f;
-    // y: the rotated accumulator at value scale, this thread's half of row r
+  if (warp < 4) linv[r] = l_run > 0.f ? 1.f / l_run : 0.f;
+  // every MMA has completed (or the CTA stores nothing): the shared memory below is free
+  const bool rotated = __syncthreads_and(ok) && tl.nR > 0;
+  if (rotated && tid == 0) {
+    mbar_arrive_expect_tx(epi_copy, (uint32_t)L::RP_BYTES);
+    bulk_g2s(smem + L::RP, a.ws + a.rvp_off + (g.rph ? (size_t)kvh * L::RP_BYTES : 0), (uint32_t)L::RP_BYTES,
+             epi_copy);
+  }
+  if (rotated && warp < 8) {
+    const float li = linv[r];
     uint32_t oz[32];
     tmem_ld32_nowait(lane_base + L::C_OZ, oz);
     tmem_wait_ld();
@@ -1239,57 +1261,75 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       for (int gg = 0; gg < G; ++gg)
         zsel = gg == gidx ? __uint_as_float(oz[gg]) + __uint_as_float(oz[G + gg]) : zsel;
       const float zv = zsel * pow2f(-a.k_exp_V);
+      uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const int ch = j0 + 32 * cb + k;
-        const float fch = pow2f(10 - slot_pos((ch % 64) / 8) - a.k_exp_V);
-        Y[r * L::YS + ch] = fmaf(__uint_as_float(o[k]), fch, zv);
+      for (int q = 0; q < 16; ++q) {
+        const int ch = j0 + 32 * cb + 2 * q;
+        const float y0 = fmaf(__uint_as_float(o[2 * q]), pow2f(10 - slot_pos((ch % 64) / 8) - a.k_exp_V), zv) * li;
+        const float y1 =
+            fmaf(__uint_as_float(o[2 * q + 1]), pow2f(10 - slot_pos(((ch + 1) % 64) / 8) - a.k_exp_V), zv) * li;
+        hi[q] = half2_bits(y0, y1);
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[q]));
+        lo[q] = half2_bits(y0 - hf.x, y1 - hf.y);
       }
+      tmem_st16(lane_base + L::C_S + (uint32_t)(j0 / 2 + 16 * cb), hi);
+      tmem_st16(lane_base + L::C_S + (uint32_t)(D / 2 + j0 / 2 + 16 * cb), lo);
     }
+    tmem_wait_st();
   }
-  if (warp < 4 && !rotated) linv[r] = l_run > 0.f ? 1.f / l_run : 0.f;
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  if (rotated && warp == 8 && lane == 0) {
+    const bool okc = mbar_wait_bounded(epi_copy, 0, a.status);
+    tc_fence_after();
+    if (okc) {
+      const uint64_t dRP = smem_desc_sw128(smem_u32(smem) + L::RP);
+      const uint32_t idesc = idesc_f16_f32(kXRows, D);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t bk = (uint32_t)((kk >> 2) * D * 128 + (kk & 3) * 32);
+        const uint32_t a_hi = tmem + L::C_S + (uint32_t)(8 * kk), a_lo = a_hi + (uint32_t)(D / 2);
+        tc_mma_ts(tmem + L::C_OROT, a_hi, dadd(dRP, bk), idesc, kk ? 1u : 0u);
+        tc_mma_ts(tmem + L::C_OROT, a_hi, dadd(dRP, (uint32_t)(D * D * 2) + bk), idesc, 1u);
+        tc_mma_ts(tmem + L::C_OROT, a_lo, dadd(dRP, bk), idesc, 1u);
+      }
+    } else {
+      (void)mbar_wait_bounded(epi_copy, 0, nullptr);   // the copy lands before the CTA exits
+    }
+    tc_commit(epi_mma);
+  }
   if (warp < 8) {
-    // the TMEM loads are warp-collective: every lane takes part, rows outside the chunk included
+    bool okm = ok;
+    if (rotated) {
+      okm = __all_sync(0xffffffffu, xwait(epi_mma, 0, a.status));
+      tc_fence_after();
+    }
+    const float li = linv[r];
     float acc[NJ];
 #pragma unroll
     for (int cb = 0; cb < NJ / 32; ++cb) {
-      uint32_t o[32];
+      uint32_t o[32], y[32];
       tmem_ld32_nowait(lane_base + L::C_OPLAIN + (uint32_t)(j0 + 32 * cb), o);
+      if (rotated) tmem_ld32_nowait(lane_base + L::C_OROT + (uint32_t)(j0 + 32 * cb), y);
       tmem_wait_ld();
 #pragma unroll
-      for (int k = 0; k < 32; ++k) acc[32 * cb + k] = __uint_as_float(o[k]);
+      for (int k = 0; k < 32; ++k)
+        acc[32 * cb + k] = rotated ? fmaf(__uint_as_float(o[k]), li, __uint_as_float(y[k])) : __uint_as_float(o[k]) * li;
     }
-    const float* yr = Y + r * L::YS;
-#pragma unroll 2
-    for (int i = 0; rotated && i < D; ++i) {
-      const float yi = yr[i];
-      const float4* rt = reinterpret_cast<const float4*>(Rt + i * D + j0);
-#pragma unroll
-      for (int j4 = 0; j4 < NJ / 4; ++j4) {
-        const float4 rv = rt[j4];
-        acc[4 * j4] = fmaf(yi, rv.x, acc[4 * j4]);
-        acc[4 * j4 + 1] = fmaf(yi, rv.y, acc[4 * j4 + 1]);
-        acc[4 * j4 + 2] = fmaf(yi, rv.z, acc[4 * j4 + 2]);
-        acc[4 * j4 + 3] = fmaf(yi, rv.w, acc[4 * j4 + 3]);
-      }
-    }
-    const float li = linv[r];
-    if (!ok || !row_ok) {
+    if (!okm || !row_ok) {
       // nothing to store
     } else if (a.out_dtype == kDtypeF32) {
       float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + qrow * D + j0);
 #pragma unroll
       for (int j4 = 0; j4 < NJ / 4; ++j4)
-        dst[j4] = make_float4(acc[4 * j4] * li, acc[4 * j4 + 1] * li, acc[4 * j4 + 2] * li, acc[4 * j4 + 3] * li);
+        dst[j4] = make_float4(acc[4 * j4], acc[4 * j4 + 1], acc[4 * j4 + 2], acc[4 * j4 + 3]);
     } else {
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + qrow * D + j0);
 #pragma unroll
       for (int j8 = 0; j8 < NJ / 8; ++j8)
-        dst[j8] = make_uint4(pack_bf162(acc[8 * j8] * li, acc[8 * j8 + 1] * li),
-                             pack_bf162(acc[8 * j8 + 2] * li, acc[8 * j8 + 3] * li),
-                             pack_bf162(acc[8 * j8 + 4] * li, acc[8 * j8 + 5] * li),
-                             pack_bf162(acc[8 * j8 + 6] * li, acc[8 * j8 + 7] * li));
+        dst[j8] = make_uint4(pack_bf162(acc[8 * j8], acc[8 * j8 + 1]), pack_bf162(acc[8 * j8 + 2], acc[8 * j8 + 3]),
+                             pack_bf162(acc[8 * j8 + 4], acc[8 * j8 + 5]), pack_bf162(acc[8 * j8 + 6], acc[8 * j8 + 7]));
     }
   }
   tc_fence_before();
@@ -1329,14 +1369,15 @@ int launch_extend_d(const ExtendArgs& a, void* stream) {
 
 }  // namespace
 
-// workspace: R_V^T ([Hkv][D][D] with a rotation per kv head, else [D][D]) then q R_K per row
+// workspace: R_V's f16 hi and lo planes ([Hkv][2][D][D] with a rotation per kv head, else
+// [2][D][D]; the size of a float32 D x D per rotation), then q R_K per row
 size_t extend_workspace_bytes(const Geom& g, long long total_tokens) {
   const size_t rvt = ((size_t)(g.rph ? g.Hkv : 1) * g.D * g.D * 4 + 255) & ~size_t(255);
   return rvt + (size_t)total_tokens * g.Hq * g.D * 4;
 }
 
-void extend_ws_offsets(const Geom& g, size_t* rvt_off, size_t* qrot_off) {
-  *rvt_off = 0;
+void extend_ws_offsets(const Geom& g, size_t* rvp_off, size_t* qrot_off) {
+  *rvp_off = 0;
   *qrot_off = ((size_t)(g.rph ? g.Hkv : 1) * g.D * g.D * 4 + 255) & ~size_t(255);
 }
 

@@ -975,7 +975,7 @@ oscar_status oscar_extend_attn(oscar_ctx* ctx, int32_t layer, const void* q, int
   a.slab = ctx->slab;
   a.status = ctx->d_status;
   a.ws = static_cast<uint8_t*>(workspace);
-  oscar::extend_ws_offsets(ctx->g, &a.rvt_off, &a.qrot_off);
+  oscar::extend_ws_offsets(ctx->g, &a.rvp_off, &a.qrot_off);
   a.k_exp_K = ek;
   a.k_exp_V = ev;
   a.code_magic = oscar::kCodeMagic;

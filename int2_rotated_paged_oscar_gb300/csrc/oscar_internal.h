@@ -139,8 +139,8 @@ struct ExtendArgs {
   const uint8_t* pool;
   const uint16_t* slab;
   int* status;
-  uint8_t* ws;               // R_V^T [D][D] f32 at rvt_off, q' = q R_K [total_tokens][Hq][D] f32 at qrot_off
-  size_t rvt_off, qrot_off;
+  uint8_t* ws;               // R_V as f16 hi / lo planes at rvp_off, q' = q R_K [total_tokens][Hq][D] f32 at qrot_off
+  size_t rvp_off, qrot_off;
   int k_exp_K, k_exp_V;
   unsigned code_magic;
   // unpacked-prefix form (null: every attention CTA forms its tiles itself): per (request b,
@@ -157,7 +157,7 @@ long long extend_prep_tiles(const Geom& g, long long max_prefix);
 // BF16 window tiles of a request, and chunk tiles of a chunk of at most max_chunk tokens
 int extend_prep_window_tiles(const Geom& g);
 long long extend_prep_chunk_tiles(const Geom& g, long long max_chunk);
-void extend_ws_offsets(const Geom& g, size_t* rvt_off, size_t* qrot_off);
+void extend_ws_offsets(const Geom& g, size_t* rvp_off, size_t* qrot_off);
 int launch_extend(const ExtendArgs& a, void* stream);
 // Self-test of the bounded-wait failure path: waits on an mbarrier that nothing arrives on.
 int launch_wait_selftest(int* status, long long limit_ns, void* stream);
