@@ -341,7 +341,8 @@ oscar_status oscar_decode_attn_noalloc(oscar_ctx* ctx, int32_t layer, const void
  *  (else OSCAR_ERR_UNSUPPORTED).
  *  workspace: device scratch of at least oscar_extend_workspace_size(cfg,
  *  total_tokens) bytes (256-byte aligned, no initialisation); it holds q R_K for
- *  every query row and R_V^T (one per kv head with rotation_per_kv_head).  With
+ *  every query row and R_V as f16 hi / lo planes (one per kv head with
+ *  rotation_per_kv_head) for the epilogue's y R_V^T on the tensor cores.  With
  *  oscar_extend_workspace_size_unpacked(cfg, total_tokens, batch, max_prefix,
  *  max_chunk) bytes or more, the unpacked-prefix form runs: a pre-pass forms
  *  every 64-key tile that the query tiles of a request share (its INT2 history
