@@ -14,8 +14,7 @@
 // then the BF16 window tiles, then the chunk's own tiles.  Per tile:
 //   S = Q K^T into TMEM (two buffers, so the next tile's scores are computed while the
 //   softmax reads this tile's), softmax by the row's own thread, P back into TMEM over
-//   the tile's own scores (history tiles) or to shared memory (BF16 tiles), O += P V
-//   into TMEM.  History tiles take both A operands from TMEM (the rotated query planes,
+//   the tile's own scores, O += P V into TMEM.  History tiles take both A operands from TMEM (the rotated query planes,
 //   the weights), so the tensor core reads only the unpacked keys and values from shared
 //   memory, and their softmax waits for the previous tile's PV only to rescale.
 // History tiles run in the rotated basis with f16 operands, each dequantised value split
@@ -35,12 +34,15 @@
 // P as three BF16 terms (24 bits; the values are unbounded BF16), K and V exactly
 // as stored.  Both kinds share one running softmax reference per row; the two
 // output accumulators (rotated and plain) are rescaled together.  The epilogue forms
-// out = (O_plain + y R_V^T) / l, y the rotated accumulator put back to value scale.
+// out = O_plain / l + (y / l) R_V^T on the tensor cores, y the rotated accumulator put
+// back to value scale.
 //
-// Roles: warps 0-3 (softmax; thread r owns row r = TMEM lane r), warps 4-7 (unpack of
-// the next tile into the shared-memory operand tiles, INT2 pages staged one tile ahead
-// by cp.async), warp 8 (TMEM allocation, MMA issue).  The roles meet only at mbarriers:
-// kv_full (a stage unpacked), s_full (scores in TMEM), p_full (weights in place),
+// Roles: warps 0-3 (softmax; thread r owns row r = TMEM lane r), warps 4-7 (the next
+// tile into a shared-memory operand stage: INT2 pages bulk-copied two tiles ahead and
+// unpacked, BF16 rows copied and V transposed; or, in the unpacked-prefix form, one bulk
+// copy of the tile's image that a pre-pass formed once per call for all the request's
+// query tiles), warp 8 (TMEM allocation, MMA issue).  The roles meet only at mbarriers:
+// kv_full (a stage filled), s_full (scores in TMEM), p_full (weights in place),
 // pv_done and kv_empty (a tile's PV done, its stage free), so the scores of
 // tile j are computed while the softmax works on tile j - 1.  Every wait is bounded by
 // %globaltimer: a timeout flags the status word and the CTA drains and exits.
