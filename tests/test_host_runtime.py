@@ -186,6 +186,35 @@ def test_workspace_planning(osc):
     assert osc.oscar_bf16_decode_workspace_size(c, 1, 32768) > 0
 
 
+def test_extend_unpacked_workspace_planning(osc):
+    """The unpacked-prefix extend workspace: the base size plus, per (request, kv head), one 43,008-byte
+    operand image (d = 128) per 64 positions of INT2 history (sink 4, window 128), of the window slots
+    and of the chunk (the attention grid's query tiles of 32 tokens at GQA 4, rounded up to 64 keys)."""
+    c = _cfg(osc, num_layers=1, num_pages=600)
+    tile = 128 * 64 * 2 + 64 * 128 + 128 * 64 * 2 + 16 * 128
+    assert tile == 43008
+    base = osc.oscar_extend_workspace_size(c, 2048)
+    base256 = (base + 255) // 256 * 256
+
+    def tiles(max_prefix, max_chunk):
+        hist_end = max(4, max_prefix - 128)
+        hist = (hist_end - 1) // 64 - 4 // 64 + 1 if hist_end > 4 else 0
+        chunk = ((max_chunk + 31) // 32 * 32 + 63) // 64
+        return hist + (4 + 128 + 63) // 64 + chunk
+
+    for batch, max_prefix, max_chunk in [(1, 0, 1), (4, 32768, 2048), (3, 133, 65), (2, 132, 64), (8, 200, 0)]:
+        got = osc.oscar_extend_workspace_size_unpacked(c, 2048, batch, max_prefix, max_chunk)
+        assert got == base256 + batch * 8 * tiles(max_prefix, max_chunk) * tile, (batch, max_prefix, max_chunk)
+    # 64 more history tokens: one more tile per (request, kv head)
+    a = osc.oscar_extend_workspace_size_unpacked(c, 2048, 4, 32768, 2048)
+    b = osc.oscar_extend_workspace_size_unpacked(c, 2048, 4, 32768 + 64, 2048)
+    assert b - a == 4 * 8 * tile
+    for bad in [(-1, 100, 64), (1, -1, 64), (1, 100, -1)]:
+        with pytest.raises(osc.OscarError) as ei:
+            osc.oscar_extend_workspace_size_unpacked(c, 2048, *bad)
+        assert ei.value.status == osc.ERR_INVALID
+
+
 def test_calibration_matches_oracle_fixture():
     """The product's offline calibration and the oracle fixture are independent code; they must agree."""
     import numpy as np
