@@ -95,6 +95,41 @@ def test_extend_parity(osc, shape, prefix, chunks, q_dtype, out_bf16, q_scale):
         gc.close()
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_extend_forms_agree_on_random_requests(osc, seed):
+    """Random shapes, prefixes and chunks (seeded): the form in which every CTA forms its tiles, the
+    unpacked-prefix form with a workspace for every prefix, and one with a workspace for shorter prefixes
+    only give identical outputs (the same operands through the same MMAs)."""
+    rng = np.random.default_rng(1000 + seed)
+    gq = int(rng.choice([1, 2, 4, 8]))
+    hkv = int(rng.choice([2, 4, 8]))
+    d = int(rng.choice([64, 128]))
+    page = int(rng.choice([16, 32, 64]))
+    sink = int(rng.choice([0, 4]))
+    recent = int(rng.choice([32, 64, 128]))
+    shape = syn.Shape(gq * hkv, hkv, d, page, 32, sink, recent, 1)
+    b = int(rng.integers(1, 5))
+    prefix = [int(x) for x in rng.integers(0, 1600, size=b)]
+    chunks = [int(x) for x in rng.integers(0, 180, size=b)]
+    chunks[int(rng.integers(0, b))] = int(rng.integers(1, 180))   # at least one query token
+    wl = syn.Workload("ext_rand", shape, [0], seed=60 + seed, dtype="bf16")
+    fx = H.fixture(wl)
+    gc, geom, bt = _setup(wl, fx, prefix)
+    try:
+        total = sum(chunks)
+        k, v = syn.kv_tokens(wl, 0, total, sub=13)
+        q = syn.queries(wl, 0, total, sub=14, scale=0.5)
+        cu = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+        slots = np.arange(b, dtype=np.int32)
+        got = H.run_extend(gc, 0, q, "bf16", k, v, cu, prefix, bt, slots, fx)
+        assert np.all(np.isfinite(got))
+        for form in (True, int(rng.integers(0, max(prefix) + 1))):
+            got_u = H.run_extend(gc, 0, q, "bf16", k, v, cu, prefix, bt, slots, fx, unpacked=form)
+            assert np.array_equal(got_u, got), (shape, prefix, chunks, form)
+    finally:
+        gc.close()
+
+
 def test_extend_on_a_forked_prefix(osc):
     """Prefix caching end to end: request 0 writes a prefix, request 1 forks it (full history pages
     shared, the partial page copied, the window copied), and one extend call serves both with
