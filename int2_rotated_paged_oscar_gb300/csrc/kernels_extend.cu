@@ -132,23 +132,29 @@ struct XLayout {
 };
 
 // ------------------------------------------------------------------ query rotation
-// q' = q R_K for every (chunk token, query head) row, float32, into the workspace; the
-// last CTA writes R_V as f16 hi and lo planes (row n = output channel n, K-major with the
-// 128-byte swizzle: the B operand of the epilogue's y R_V^T on the tensor cores).  CTA: 64 rows x D columns with R in shared
-// memory and q transposed beside it ([D][64 + 4]); thread t owns rows 4 (t / 16) .. + 3 and
-// the float4 columns (t % 16) + 16 k, so that per step i one float4 of q (four rows) and D / 64
-// float4 of R row i feed 4 x D / 16 fused multiply-adds.  Every output is the chain
-// fma(q_i, R[i][c], .) over i = 0 .. D - 1.
-constexpr int kQsPad = 4;   // q^T row stride 64 + 4 floats: 16-byte aligned rows
+// q' = q R_K for every (chunk token, query head) row, float32, into the workspace, on the
+// tensor cores: a CTA takes 128 rows (the BF16 query as received, K-major with the 128-byte
+// swizzle) against R_K^T split exactly into three BF16 planes (R = R1 + R2 + R3, 3 x 8
+// significant bits covering float32's 24), built in shared memory; 3 x D/16 MMAs (the small
+// planes first) into one float32 TMEM accumulator, which thread t reads for row t.  The last
+// CTA writes R_V as f16 hi and lo planes (row n = output channel n, K-major with the 128-byte
+// swizzle: the B operand of the epilogue's y R_V^T).
 template <int D>
-__host__ __device__ constexpr size_t qrot_smem_floats() { return (size_t)D * D + (size_t)D * (64 + kQsPad); }
+struct QrPlan {
+  static constexpr int PLANE = D * D * 2;        // one BF16 plane of R_K^T
+  static constexpr int A_OFF = 3 * PLANE;        // 128 query rows, BF16
+  static constexpr int BAR = A_OFF + 128 * D * 2;
+  static constexpr int SMEM = BAR + 16 + 1024;   // slack for the 1024-byte alignment of the base
+};
 
 template <int D>
-__global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
-  extern __shared__ __align__(16) float xq_sm[];
-  float* Rs = xq_sm;              // [D][D]
-  float* qt = xq_sm + D * D;      // [D][64 + kQsPad]: q transposed
-  const int t = threadIdx.x;
+__global__ void __launch_bounds__(128, 1) extend_qrot_kernel(ExtendArgs a) {
+  using Q = QrPlan<D>;
+  extern __shared__ uint8_t xq_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(xq_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Q::BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Q::BAR + 8);
+  const int t = threadIdx.x, warp = t >> 5;
   const Geom& g = a.g;
   const long long rows = (long long)a.total_tokens * g.Hq;
   float* qrot = reinterpret_cast<float*>(a.ws + a.qrot_off);
@@ -157,7 +163,7 @@ __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
   if (blockIdx.x == gridDim.x - 1) {
     uint8_t* rp = a.ws + a.rvp_off + (size_t)kvh * (2 * D * D * 2);
     const float* rv = a.R_V + (size_t)kvh * g.rot_stride();
-    for (int item = t; item < D * D / 8; item += 256) {   // 8 consecutive k of row n
+    for (int item = t; item < D * D / 8; item += 128) {   // 8 consecutive k of row n
       const int n = item / (D / 8), k0 = 8 * (item % (D / 8));
       const float4 x0 = __ldg(reinterpret_cast<const float4*>(rv + (size_t)n * D + k0));
       const float4 x1 = __ldg(reinterpret_cast<const float4*>(rv + (size_t)n * D + k0 + 4));
@@ -174,14 +180,19 @@ __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
     }
     return;
   }
-  // global row of local row l: one rotation per layer, rows 64 x + l of [tokens][Hq]; one per kv
-  // head, the 64 / gq tokens x gq query heads of kv head kvh starting at token (64 / gq) x
+  // global row of local row l: one rotation per layer, rows 128 x + l of [tokens][Hq]; one per
+  // kv head, the 128 / gq tokens x gq query heads of kv head kvh starting at token (128 / gq) x
   const int gq = g.gq();
+  auto row_of = [&](int l) -> long long {
+    if (!g.rph) return (long long)blockIdx.x * 128 + l;
+    const long long tok = (long long)blockIdx.x * (128 / gq) + l / gq;
+    return tok < a.total_tokens ? tok * g.Hq + (long long)kvh * gq + l % gq : rows;
+  };
   {
     // The attention reads q' only for requests with INT2 history tiles: a CTA whose rows all
     // belong to requests without history (every request of a prefill from scratch) stops here.
-    const long long tok0 = g.rph ? (long long)blockIdx.x * (64 / gq) : (long long)blockIdx.x * 64 / g.Hq;
-    long long tok1 = g.rph ? tok0 + 64 / gq - 1 : ((long long)blockIdx.x * 64 + 63) / g.Hq;
+    const long long tok0 = g.rph ? (long long)blockIdx.x * (128 / gq) : (long long)blockIdx.x * 128 / g.Hq;
+    long long tok1 = g.rph ? tok0 + 128 / gq - 1 : ((long long)blockIdx.x * 128 + 127) / g.Hq;
     if (tok1 >= a.total_tokens) tok1 = a.total_tokens - 1;
     auto request_of = [&](long long tk) {   // largest b with cu_seqlens[b] <= tk
       int lo = 0, hi = a.batch - 1;
@@ -198,56 +209,87 @@ __global__ void __launch_bounds__(256) extend_qrot_kernel(ExtendArgs a) {
       if (!need) return;
     }
   }
-  for (int idx = t; idx < D * D / 4; idx += 256)
-    reinterpret_cast<float4*>(Rs)[idx] =
-        __ldg(reinterpret_cast<const float4*>(a.R_K + (size_t)kvh * g.rot_stride()) + idx);
-  auto row_of = [&](int l) -> long long {
-    if (!g.rph) return (long long)blockIdx.x * 64 + l;
-    const long long tok = (long long)blockIdx.x * (64 / gq) + l / gq;
-    return tok < a.total_tokens ? tok * g.Hq + (long long)kvh * gq + l % gq : rows;
-  };
-  for (int idx = t; idx < 64 * D; idx += 256) {
-    const long long r = row_of(idx / D);
-    float v = 0.f;
-    if (r < rows) {
-      const size_t e = (size_t)r * D + idx % D;
-      v = __uint_as_float((uint32_t) static_cast<const uint16_t*>(a.q)[e] << 16);   // BF16 query
+  // R_K^T as three BF16 planes (row n = column n of R_K); item = (n, k-octet)
+  const float* R = a.R_K + (size_t)kvh * g.rot_stride();
+  for (int item = t; item < D * D / 8; item += 128) {
+    const int n = item % D, k0 = (item / D) * 8;
+    uint32_t pk[3][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t lo[3], hi[3];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float r = __ldg(R + (size_t)(k0 + 2 * q + e) * D + n);
+        const __nv_bfloat16 p1 = __float2bfloat16_rn(r);
+        const float r1 = r - __bfloat162float(p1);
+        const __nv_bfloat16 p2 = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 p3 = __float2bfloat16_rn(r1 - __bfloat162float(p2));
+        (e ? hi : lo)[0] = *reinterpret_cast<const uint16_t*>(&p1);
+        (e ? hi : lo)[1] = *reinterpret_cast<const uint16_t*>(&p2);
+        (e ? hi : lo)[2] = *reinterpret_cast<const uint16_t*>(&p3);
+      }
+#pragma unroll
+      for (int p = 0; p < 3; ++p) pk[p][q] = lo[p] | (hi[p] << 16);
     }
-    qt[(idx % D) * (64 + kQsPad) + idx / D] = v;
+    const uint32_t off = sw128_offset(n, k0, D);
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+      *reinterpret_cast<uint4*>(sm + p * Q::PLANE + off) = make_uint4(pk[p][0], pk[p][1], pk[p][2], pk[p][3]);
   }
+  // the query rows, BF16 as received (rows past the end zero)
+  for (int idx = t; idx < 128 * D / 8; idx += 128) {
+    const int l = idx / (D / 8), c8 = idx % (D / 8);
+    const long long r = row_of(l);
+    const uint4 v = r < rows ? *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + (size_t)r * D + 8 * c8)
+                             : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(sm + Q::A_OFF + sw128_offset(l, 8 * c8, 128)) = v;
+  }
+  if (t == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, D);
+  // the planes and rows were written by ordinary stores; the MMAs read them through the async proxy
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
-  constexpr int NC4 = D / 64;   // float4 columns per thread
-  const int rg = t >> 4, cg = t & 15;
-  float4 acc[4][NC4];
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (t == 0) {
+    const uint32_t idesc = idesc_bf16_f32(128, D);
+    const uint32_t a_base = smem_u32(sm + Q::A_OFF), b_base = smem_u32(sm);
 #pragma unroll
-  for (int rw = 0; rw < 4; ++rw)
+    for (int pp = 0; pp < 3; ++pp) {
+      const int p = 2 - pp;   // the small planes first: each MMA rounds relative to the running sum
 #pragma unroll
-    for (int k = 0; k < NC4; ++k) acc[rw][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int i = 0; i < D; ++i) {
-    const float4 qv = *reinterpret_cast<const float4*>(qt + i * (64 + kQsPad) + 4 * rg);
-    const float qr[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-    for (int k = 0; k < NC4; ++k) {
-      const float4 rv = *reinterpret_cast<const float4*>(Rs + i * D + 4 * (cg + 16 * k));
-#pragma unroll
-      for (int rw = 0; rw < 4; ++rw) {
-        acc[rw][k].x = fmaf(qr[rw], rv.x, acc[rw][k].x);
-        acc[rw][k].y = fmaf(qr[rw], rv.y, acc[rw][k].y);
-        acc[rw][k].z = fmaf(qr[rw], rv.z, acc[rw][k].z);
-        acc[rw][k].w = fmaf(qr[rw], rv.w, acc[rw][k].w);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ak = (uint32_t)((kk >> 2) * 128 * 128 + (kk & 3) * 32);
+        const uint32_t bk = (uint32_t)(p * Q::PLANE + (kk >> 2) * D * 128 + (kk & 3) * 32);
+        tc_mma_bf16(tmem, smem_desc_sw128(a_base + ak), smem_desc_sw128(b_base + bk), idesc, (pp | kk) ? 1u : 0u);
       }
     }
+    tc_commit(bar);
   }
+  const bool ok = mbar_wait_bounded(bar, 0, a.status);
+  tc_fence_after();
+  // thread t reads row t (TMEM lane t)
+  const long long r = row_of(t);
+#pragma unroll 1
+  for (int cb = 0; cb < D / 32; ++cb) {
+    uint32_t v[32];
+    tmem_ld32_nowait(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(32 * cb), v);
+    tmem_wait_ld();
+    if (ok && r < rows) {
+      float4* dst = reinterpret_cast<float4*>(qrot + (size_t)r * D + 32 * cb);
 #pragma unroll
-  for (int rw = 0; rw < 4; ++rw) {
-    const long long r = row_of(4 * rg + rw);
-    if (r < rows) {
-      float4* dst = reinterpret_cast<float4*>(qrot + (size_t)r * D);
-#pragma unroll
-      for (int k = 0; k < NC4; ++k) dst[cg + 16 * k] = acc[rw][k];
+      for (int j = 0; j < 8; ++j)
+        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                             __uint_as_float(v[4 * j + 3]));
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, D);
 }
 
 // ------------------------------------------------------------------ attention
@@ -1347,12 +1389,12 @@ template <int D>
 int launch_extend_d(const ExtendArgs& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long rows = (long long)a.total_tokens * a.g.Hq;
-  const size_t qsm = qrot_smem_floats<D>() * sizeof(float);
+  const size_t qsm = QrPlan<D>::SMEM;
   cudaError_t e = ensure_smem_limit(extend_qrot_kernel<D>, qsm);
   if (e != cudaSuccess) return (int)e;
-  // one rotation per kv head: grid.y = kv heads, each CTA 64 / gq tokens of its head's query rows
+  // one rotation per kv head: grid.y = kv heads, each CTA 128 / gq tokens of its head's query rows
   const int heads = a.g.rph ? a.g.Hkv : 1;
-  const long long per = a.g.rph ? 64 / a.g.gq() : 64;
+  const long long per = a.g.rph ? 128 / a.g.gq() : 128;
   const long long units = a.g.rph ? (long long)a.total_tokens : rows;
   const unsigned qgrid = (unsigned)((units + per - 1) / per) + 1;
   if (a.prep) {
@@ -1362,7 +1404,7 @@ int launch_extend_d(const ExtendArgs& a, void* stream) {
     extend_unpack_kernel<D><<<dim3(tiles, (unsigned)a.g.Hkv, (unsigned)a.batch), 128, usm, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
   }
-  extend_qrot_kernel<D><<<dim3(qgrid, heads), 256, qsm, s>>>(a);
+  extend_qrot_kernel<D><<<dim3(qgrid, heads), 128, qsm, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
   auto kern = a.prep ? extend_attn_kernel<D, true> : extend_attn_kernel<D, false>;
   e = ensure_smem_limit(kern, XLayout<D>::SMEM);
