@@ -1420,8 +1420,8 @@ int launch_extend_d(const ExtendArgs& a, void* stream) {
 // workspace: R_V's f16 hi and lo planes ([Hkv][2][D][D] with a rotation per kv head, else
 // [2][D][D]; the size of a float32 D x D per rotation), then q R_K per row
 size_t extend_workspace_bytes(const Geom& g, long long total_tokens) {
-  const size_t rvt = ((size_t)(g.rph ? g.Hkv : 1) * g.D * g.D * 4 + 255) & ~size_t(255);
-  return rvt + (size_t)total_tokens * g.Hq * g.D * 4;
+  const size_t rvp = ((size_t)(g.rph ? g.Hkv : 1) * g.D * g.D * 4 + 255) & ~size_t(255);
+  return rvp + (size_t)total_tokens * g.Hq * g.D * 4;
 }
 
 void extend_ws_offsets(const Geom& g, size_t* rvp_off, size_t* qrot_off) {
