@@ -68,6 +68,7 @@ constexpr int kXKeys = 64;                   // keys per tile
 constexpr int kXThreads = 9 * 32;            // softmax 0-3, unpack 4-7 (warp 4 also copies pages), MMA 8
 constexpr float kXLog2e = 1.4426950408889634f;
 constexpr float kXRescaleLog2 = 8.f;         // the reference moves when a score exceeds it by more
+constexpr float kXRescaleLog2Bf16 = 24.f;    // the same on BF16 tiles, whose weights go in as BF16 terms
 constexpr float kXWeightShift = 6.f;         // weights 2^(s - m), m = reference - shift: at most 2^14
 
 enum TileKind { kTileInt2 = 0, kTileWindow = 1, kTileChunk = 2 };
@@ -986,7 +987,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
   };
 
   // ---------------- softmax of tile i (warps 0-3); false on a wait timeout
-  float m_ref = -INFINITY, thr = -INFINITY, l_run = 0.f;
+  float m_ref = -INFINITY, l_run = 0.f;
+  bool ref_set = false;   // the reference has been placed by a visible key
   auto softmax_tile = [&](int i) -> bool {
     const int kind = tl.kind(i), base = tl.base(i);
     // waits are made warp-uniform: the TMEM accesses below are warp-collective.  With the tiles
@@ -1030,11 +1032,16 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
     }
     const float mloc = mraw * F;
     float alpha = 1.f;
+    // Weights 2^(score - m_ref) stay below 2^(shift + rescale): 2^14 on INT2 tiles (f16 operands);
+    // on BF16 tiles (BF16 terms, float32 sums) the reference may lag by 24 before it moves, which
+    // spares the rescale of both accumulators on most tiles of a growing causal chunk
+    const float thr =
+        ref_set ? m_ref + kXWeightShift + (kind == kTileInt2 ? kXRescaleLog2 : kXRescaleLog2Bf16) : -INFINITY;
     if (mloc > thr) {
       const float nm = mloc - kXWeightShift;
       alpha = ex2(m_ref - nm);
       m_ref = nm;
-      thr = nm + kXWeightShift + kXRescaleLog2;
+      ref_set = true;
     }
     // The weights go over the tile's own scores in TMEM, so only a rescale of the
     // accumulators waits for the previous tile's PV.  (A tile's scores are complete only
