@@ -307,7 +307,6 @@ __device__ __forceinline__ bool unpack_bar_any(bool v) {
 }
 
 __device__ __forceinline__ uint32_t half2_bits(float lo_elem, float hi_elem) { return pack_half2(lo_elem, hi_elem); }
-__device__ __forceinline__ float bf16_round_f(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 // 2^e for e in the float32 normal range
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
 
@@ -1096,7 +1095,10 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
       }
       tmem_wait_st();
     } else {
-      // three BF16 terms of the weights (24 bits: window and chunk values are unbounded BF16)
+      // three BF16 terms of the weights (24 bits: window and chunk values are unbounded BF16):
+      // hi = p with its mantissa cut to BF16, lo = the same of p - hi, lo2 = p - hi - lo, each
+      // exactly a BF16 value (8 significant bits each) and hi + lo + lo2 = p exactly; a term's
+      // BF16 pattern is the upper half of its float32 pattern
       const uint32_t pcol = lane_base + L::C_S + (uint32_t)((i & 1) * kXKeys);
       const uint32_t p2col = lane_base + L::C_P2 + (uint32_t)((i & 1) * (kXKeys / 2));
 #pragma unroll
@@ -1106,11 +1108,14 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attn_kernel(ExtendArgs a)
         for (int q = 0; q < 4; ++q) {
           const int k0 = 8 * qt + 2 * q;
           const float p0 = ex2(fmaf(sc[k0], F, negm)), p1 = ex2(fmaf(sc[k0 + 1], F, negm));
-          const float h0 = bf16_round_f(p0), h1 = bf16_round_f(p1);
-          const float l0 = bf16_round_f(p0 - h0), l1 = bf16_round_f(p1 - h1);
-          hi[q] = pack_bf162(h0, h1);
-          lo[q] = pack_bf162(l0, l1);
-          lo2[q] = pack_bf162(p0 - h0 - l0, p1 - h1 - l1);
+          const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFF0000u);
+          const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFF0000u);
+          const float r0 = p0 - h0, r1 = p1 - h1;   // exact
+          const float l0 = __uint_as_float(__float_as_uint(r0) & 0xFFFF0000u);
+          const float l1 = __uint_as_float(__float_as_uint(r1) & 0xFFFF0000u);
+          hi[q] = prmt(__float_as_uint(h0), __float_as_uint(h1), 0x7632u);
+          lo[q] = prmt(__float_as_uint(l0), __float_as_uint(l1), 0x7632u);
+          lo2[q] = prmt(__float_as_uint(r0 - l0), __float_as_uint(r1 - l1), 0x7632u);
           lsum += p0 + p1;
         }
         tmem_st4(pcol + (uint32_t)(4 * qt), hi);
