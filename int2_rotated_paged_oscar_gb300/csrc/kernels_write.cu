@@ -547,9 +547,11 @@ __global__ void __launch_bounds__(kFwhtWarps * 32) write_fwht_kernel(WriteArgs a
       const float inv = sc > 0.f ? __frcp_rn(sc) : 0.f;  // s = 0: every code 0
       const float zinv = -z * inv;
       // code = clamp(rne((clip(y) - z) / s), 0, 3) as y * (1/s) - z/s clamped to the images of the
-      // clip range and to [0, 3], rounded by adding 1.5 * 2^23 (the code is the pattern's low bits)
+      // clip range and to [0, 3], rounded by adding 1.5 * 2^23 (the code is the pattern's low bits);
+      // the image of clip is below 0 when the BF16 zero lands above a clip that BF16 cannot
+      // represent and the group spans less than that rounding, so t_hi is kept at 0 or above
       const float t_lo = fmaxf(fmaf(-clip, inv, zinv), 0.f);
-      const float t_hi = fminf(fmaf(clip, inv, zinv), 3.f);
+      const float t_hi = fmaxf(fminf(fmaf(clip, inv, zinv), 3.f), 0.f);
       uint32_t pat[8];
 #pragma unroll
       for (int m = 0; m < 8; ++m)

@@ -109,9 +109,13 @@ __device__ __forceinline__ void quant_group(const float (&y)[32], int gi, float 
   const float inv = sc > 0.f ? __frcp_rn(sc) : 0.f;  // s = 0: every code 0
   const float zinv = -z * inv;
   // y -> y * inv - z * inv is monotonic, so clamping it to the images of -clip and
-  // clip is the same as clipping y first; then clamp to [0, 3]
+  // clip is the same as clipping y first; then clamp to [0, 3].  The image of clip is
+  // below 0 when z, the group minimum rounded to BF16, lands above a clip that BF16
+  // cannot represent and the group spans less than that rounding: every code is then
+  // 0, and t_hi must not go below 0 (a negative code would borrow from its neighbours
+  // in the packed word).  t_lo above 3 needs no care: t_hi <= 3 wins the clamp.
   const float t_lo = fmaxf(fmaf(-clip, inv, zinv), 0.f);
-  const float t_hi = fminf(fmaf(clip, inv, zinv), 3.f);
+  const float t_hi = fmaxf(fminf(fmaf(clip, inv, zinv), 3.f), 0.f);
   // the code argument and the rounding add in float32 pairs (two IEEE operations each,
   // the same results as the scalar forms)
   const float2 inv2 = make_float2(inv, inv), zinv2 = make_float2(zinv, zinv);

@@ -105,6 +105,61 @@ def test_naive_int2_identity_rotation(osc):
         gc.close()
 
 
+@pytest.mark.parametrize("path", ["dense_bf16", "dense_f32", "hadamard_f32"])
+def test_write_group_zero_rounded_past_the_clip(osc, path):
+    """Groups held within a BF16 ulp of a clip that BF16 cannot represent (c = 1 + 0.75 * 2^-7): the zero
+    rounds past the clip, (clip - z) / s is about -6, and every code is 0 (3 for the mirrored groups below
+    -c) on both sides ([summary §2.2 B]: clip, then min/max INT2 with codes clamped to the four levels).
+    The rotated rows are alpha (1.0 x16, 1.0078125 x16) and their negatives, alpha = 1 + 2^-8 + 2^-10: dense
+    R = alpha I on BF16 rows (tensor cores) and on float32 rows, and the Hadamard-only write of float32 rows
+    whose Hadamard rotation is that row (x = y R^T).  Even tokens carry the edge rows in K, odd tokens in V,
+    and the other rows are the seeded workload."""
+    shape = syn.Shape(32, 8, 128, 64, 32, 4, 128, 1)
+    dtype = "bf16" if path == "dense_bf16" else "f32"
+    wl = syn.Workload("clip_edge", shape, [0], seed=23, dtype=dtype)
+    c = 1 + 0.75 * 2.0 ** -7
+    alpha = 1 + 2.0 ** -8 + 2.0 ** -10
+    row = np.repeat([1.0, 1.0078125], 16)
+    edge = np.concatenate([row, row, -row, -row])
+    if path == "hadamard_f32":
+        had = H.fixture(wl, u_identity=True)
+        r_k, r_v = had["R_K"], had["R_V"]
+        xk, xv = (alpha * edge) @ np.asarray(r_k, np.float64).T, (alpha * edge) @ np.asarray(r_v, np.float64).T
+    else:
+        r_k = r_v = (alpha * np.eye(128)).astype(np.float32)
+        xk = xv = edge
+    fx = {"R_K": r_k, "R_V": r_v, "clip_K": c, "clip_V": c}
+    n = 300
+    k, v = syn.kv_tokens(wl, 0, n)
+    k, v = np.array(k, np.float64), np.array(v, np.float64)
+    k[0::2] = xk
+    v[1::2] = xv
+    k, v = k.astype(np.float32), v.astype(np.float32)
+    ppr = syn.pages_for(n, shape.page_size) + 1
+    bt = _contiguous_bt(1, ppr)
+    geom = H.geometry(shape, ppr, 1)
+    img = cache.CacheImage(geom)
+    gc = H.make_gpu_cache(geom, shape.n_q_heads, ppr)
+    cu, sp, slots = np.array([0, n], np.int32), np.zeros(1, np.int32), np.zeros(1, np.int32)
+    try:
+        diag = cache.write_kv(img, 0, k, v, cu, sp, r_k, r_v, c, c, bt, slots)
+        for kv in ("k", "v"):
+            z = diag[kv]["zero"]
+            assert np.any(z == 1.0078125) and np.any(z == -1.0078125)
+        if path == "hadamard_f32":
+            osc.oscar_write_kv_hadamard(gc.ctx, 0, H.dev_input(k, dtype), H.dev_input(v, dtype), H.dtype_code(dtype),
+                                        H.dev(cu), H.dev(sp), 1, n, c, c, H.dev(bt), ppr, H.dev(slots))
+        else:
+            osc.oscar_write_kv(gc.ctx, 0, H.dev_input(k, dtype), H.dev_input(v, dtype), H.dtype_code(dtype), H.dev(cu),
+                               H.dev(sp), 1, n, H.dev(r_k), H.dev(r_v), c, c, H.dev(bt), ppr, H.dev(slots))
+        assert osc.oscar_check_status(gc.ctx) == 0
+        res = H.compare_history(gc.pool_np(), geom, 0, diag, exact_ties=(path == "dense_bf16"))
+        assert res["elements"] > 0
+        H.compare_window(gc.slab_np(), img.slab, 0, range(1))
+    finally:
+        gc.close()
+
+
 def _hadamard_case(osc, shape, dtype, rph):
     """Data-oblivious rotation R = H P (U = I), written by oscar_write_kv_hadamard (BF16 rows: one exact
     +-1 plane on the tensor cores; float32 rows: the fast Walsh-Hadamard transform) against the oracle's

@@ -219,6 +219,26 @@ def test_quantizer_constant_group():
     assert zero[0, 0] == quant.bf16_round(1.2345)
 
 
+def test_quantizer_zero_rounded_past_the_clip():
+    """A group held within a BF16 ulp of a clip that BF16 cannot represent.  R = alpha I with
+    alpha = 1 + 2^-8 + 2^-10 maps 1.0 to 1.0048828125 (inside the ulp below c = 1 + 0.75 * 2^-7) and
+    1.0078125 above c.  The zero rounds to 1.0078125, past the clip, and the scale is BF16 of
+    2^-10 / 3 = 1.3359375 * 2^-12 (1/3 = 1.0101010...b * 2^-2 rounds up at 7 bits), so every
+    (clip(y) - z) / s is at most -6: all codes are 0.  The mirrored group sits below -c: the zero
+    rounds to -1.0078125 and every code is 3."""
+    alpha = 1 + 2.0 ** -8 + 2.0 ** -10
+    c = 1 + 0.75 * 2.0 ** -7
+    row = np.repeat([1.0, 1.0078125], 16)
+    x = np.concatenate([row, row, -row, -row])[None, None, :]
+    q = cache.quantize_rows(x, alpha * np.eye(128), c, 32)
+    s_hand = 1.3359375 * 2.0 ** -12
+    assert np.array_equal(q["zero"][0, 0], [1.0078125, 1.0078125, -1.0078125, -1.0078125])
+    assert np.array_equal(q["scale"][0, 0], [s_hand] * 4)
+    assert np.all(q["codes"][0, 0, :64] == 0) and np.all(q["codes"][0, 0, 64:] == 3)
+    # the image of the clip under (y - z) / s is about -6, not within [0, 3]
+    assert (c - 1.0078125) / s_hand < -5.5
+
+
 def test_quantize_with_matches_quantize_groups():
     rng = np.random.default_rng(14)
     y = rng.standard_normal((50, 128))
