@@ -318,7 +318,7 @@ extern "C" {
 
 const char* oscar_last_error(void) { return g_last_error.c_str(); }
 
-const char* oscar_version(void) { return "oscar-gb300 0.9 (sm_103a)"; }
+const char* oscar_version(void) { return "oscar-gb300 0.10 (sm_103a)"; }
 
 size_t oscar_int2_pool_bytes(const oscar_config* cfg) {
   Geom g;
