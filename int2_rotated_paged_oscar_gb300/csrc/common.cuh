@@ -20,7 +20,7 @@ namespace oscar {
 // first launch on a device), so that later launches, including ones recorded
 // into a CUDA graph, issue nothing but the launch itself.  max_carveout: also ask
 // for the largest shared-memory share of the SM's L1/shared storage, for kernels
-// whose resident CTAs per SM need it (the driver's default split may leave room
+// whose resident CTAs per SM need it (the CUDA runtime's default carveout may leave room
 // for fewer).
 inline cudaError_t ensure_smem_limit_ptr(const void* kern, size_t bytes, bool max_carveout = false) {
   struct Entry { const void* k; int dev; size_t bytes; };
