@@ -425,6 +425,44 @@ def test_decode_gq1_gq2_d64(osc):
         H.assert_decode_close(got, want)
 
 
+@pytest.mark.parametrize("seed", range(10))
+def test_decode_random_requests(osc, seed):
+    """Random shapes (GQA 1-8, d = 64 / 128, pages 16-64, with and without sink, windows 32-128) and 1-6
+    requests of random lengths up to 5,000 tokens, written by the GPU and decoded with q x 1 or x 0.25:
+    within the decode tolerance of the oracle attending over the GPU's own cache image."""
+    rng = np.random.default_rng(9000 + seed)
+    gq, hkv = int(rng.choice([1, 2, 4, 8])), int(rng.choice([2, 4, 8]))
+    d, page = int(rng.choice([64, 128])), int(rng.choice([16, 32, 64]))
+    sink, recent = int(rng.choice([0, 4])), int(rng.choice([32, 64, 128]))
+    shape = syn.Shape(gq * hkv, hkv, d, page, 32, sink, recent, 1)
+    b = int(rng.integers(1, 7))
+    lens = [int(x) for x in rng.integers(1, 5000, size=b)]
+    q_scale = float(rng.choice([1.0, 0.25]))
+    wl = syn.Workload("dec_rand", shape, [0], seed=800 + seed, dtype="bf16")
+    fx = H.fixture(wl)
+    ppr = max(syn.pages_for(n, page) for n in lens) + 1
+    bt = _contiguous_bt(b, ppr)
+    geom = H.geometry(shape, b * ppr, b)
+    gc = H.make_gpu_cache(geom, shape.n_q_heads, ppr)
+    try:
+        ks, vs = zip(*[syn.kv_tokens(wl, 0, n, sub=i) for i, n in enumerate(lens)])
+        k, v = np.concatenate(ks), np.concatenate(vs)
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        slots = np.arange(b, dtype=np.int32)
+        osc.oscar_write_kv(gc.ctx, 0, H.dev_input(k, "bf16"), H.dev_input(v, "bf16"), osc.DTYPE_BF16, H.dev(cu),
+                           H.dev(np.zeros(b, np.int32)), b, int(cu[-1]), H.dev(fx["R_K"]), H.dev(fx["R_V"]),
+                           fx["clip_K"], fx["clip_V"], H.dev(bt), ppr, H.dev(slots))
+        assert osc.oscar_check_status(gc.ctx) == 0
+        q = syn.queries(wl, 0, b, sub=31, scale=q_scale)
+        got = H.run_decode(gc, 0, q, "bf16", bt, lens, list(range(b)), fx)
+        gimg = cache.CacheImage(geom)
+        gimg.pool, gimg.slab = gc.pool_np(), gc.slab_np()
+        want = attention.decode(gimg, 0, q, bt, lens, list(range(b)), fx["R_K"], fx["R_V"])
+        H.assert_decode_close(got, want)
+    finally:
+        gc.close()
+
+
 def test_decode_independent_of_split_count(osc):
     """A larger max_seq changes the split plan but not the result (beyond summation order)."""
     wl = syn.Workload("split", syn.Shape(32, 8, 128, 64, 32, 4, 128, 1), [0], seed=5)
