@@ -77,6 +77,56 @@ def test_write_parity(osc, wl, lens):
         gc.close()
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_write_random_requests(osc, seed):
+    """Random shapes (d = 64 / 128, pages 16-64, 2-8 kv heads, with and without sink, windows 32-128), BF16
+    or float32 rows, the dense or the Hadamard-only rotation, 1-4 requests on pages handed out in reverse
+    order: a prefill of random lengths, then an extend chunk of each request after its prefix (ring tokens
+    evicted into history).  Codes, scales and zeros against the oracle under the near-boundary rule, window
+    slots bit-exact."""
+    rng = np.random.default_rng(7000 + seed)
+    gq, hkv = int(rng.choice([1, 4])), int(rng.choice([2, 4, 8]))
+    d, page = int(rng.choice([64, 128])), int(rng.choice([16, 32, 64]))
+    sink, recent = int(rng.choice([0, 4])), int(rng.choice([32, 64, 128]))
+    dtype = str(rng.choice(["bf16", "f32"]))
+    had = bool(rng.integers(0, 2))
+    shape = syn.Shape(gq * hkv, hkv, d, page, 32, sink, recent, 1)
+    b = int(rng.integers(1, 5))
+    lens = [int(x) for x in rng.integers(0, 1500, size=b)]
+    lens[int(rng.integers(0, b))] = int(rng.integers(1, 1500))
+    chunk = [int(x) for x in rng.integers(0, 300, size=b)]
+    wl = syn.Workload("wr_rand", shape, [0], seed=900 + seed, dtype=dtype)
+    fx = H.fixture(wl, u_identity=had)
+    ppr = max(syn.pages_for(n + c + 1, page) for n, c in zip(lens, chunk)) + 1
+    bt = np.arange(b * ppr, dtype=np.int32)[::-1].copy().reshape(b, ppr)
+    geom = H.geometry(shape, b * ppr, b)
+    img = cache.CacheImage(geom)
+    gc = H.make_gpu_cache(geom, shape.n_q_heads, ppr)
+    slots = np.arange(b, dtype=np.int32)
+    try:
+        for now, start, sub0 in ((lens, [0] * b, 0), (chunk, lens, 10)):
+            k = np.concatenate([syn.kv_tokens(wl, 0, n, sub=sub0 + i)[0] for i, n in enumerate(now)])
+            v = np.concatenate([syn.kv_tokens(wl, 0, n, sub=sub0 + i)[1] for i, n in enumerate(now)])
+            cu = np.concatenate([[0], np.cumsum(now)]).astype(np.int32)
+            sp = np.asarray(start, np.int32)
+            diag = cache.write_kv(img, 0, k, v, cu, sp, fx["R_K"], fx["R_V"], fx["clip_K"], fx["clip_V"], bt, slots)
+            if int(cu[-1]) == 0:
+                continue
+            if had:
+                osc.oscar_write_kv_hadamard(gc.ctx, 0, H.dev_input(k, dtype), H.dev_input(v, dtype),
+                                            H.dtype_code(dtype), H.dev(cu), H.dev(sp), b, int(cu[-1]), fx["clip_K"],
+                                            fx["clip_V"], H.dev(bt), ppr, H.dev(slots))
+            else:
+                osc.oscar_write_kv(gc.ctx, 0, H.dev_input(k, dtype), H.dev_input(v, dtype), H.dtype_code(dtype),
+                                   H.dev(cu), H.dev(sp), b, int(cu[-1]), H.dev(fx["R_K"]), H.dev(fx["R_V"]),
+                                   fx["clip_K"], fx["clip_V"], H.dev(bt), ppr, H.dev(slots))
+            assert osc.oscar_check_status(gc.ctx) == 0
+            H.compare_history(gc.pool_np(), geom, 0, diag)
+            H.compare_window(gc.slab_np(), img.slab, 0, range(b))
+    finally:
+        gc.close()
+
+
 def test_naive_int2_identity_rotation(osc):
     """The pages' naive INT2 baseline (no rotation, R_K = R_V = I; clip from the unrotated calibration values)
     runs on the same kernels: write codes against the oracle, and decode against the oracle on the GPU's cache."""
