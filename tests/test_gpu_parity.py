@@ -375,6 +375,60 @@ def test_fused_decode_step_equals_append_then_decode(osc, shape, ppr, lens0, ste
         gb.close()
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_fused_decode_step_random_requests(osc, seed):
+    """Random shapes (GQA 1-8, d = 64 / 128, pages 16-64, with and without sink, windows 32-128), 1-5
+    requests and 5-30 fused decode steps in a random decode form: after every step the appended rows
+    against the oracle's append under the near-boundary rule, and every seventh step's output within the
+    decode tolerance of the oracle decoding the GPU's own cache (the tolerance is stated for identical
+    caches); window slots bit-exact at the end."""
+    import torch
+    rng = np.random.default_rng(11000 + seed)
+    gq, hkv = int(rng.choice([1, 2, 4, 8])), int(rng.choice([2, 4, 8]))
+    d, page = int(rng.choice([64, 128])), int(rng.choice([16, 32, 64]))
+    sink, recent = int(rng.choice([0, 4])), int(rng.choice([32, 64, 128]))
+    shape = syn.Shape(gq * hkv, hkv, d, page, 32, sink, recent, 1)
+    b = int(rng.integers(1, 6))
+    lens = [int(x) for x in rng.integers(1, 1500, size=b)]
+    steps = int(rng.integers(5, 31))
+    one = bool(rng.integers(0, 2))
+    wl = syn.Workload("step_rand", shape, [0], seed=1200 + seed)
+    fx = H.fixture(wl)
+    ppr = max(syn.pages_for(n + steps + 1, page) for n in lens) + 1
+    bt = _contiguous_bt(b, ppr)
+    gc, img, _, _, _ = _prefill_both(osc, wl, fx, lens, bt, b * ppr)
+    osc.oscar_set_decode_form(gc.ctx, osc.DECODE_ONE_LAUNCH if one else osc.DECODE_THREE_KERNELS)
+    try:
+        slots = np.arange(b, dtype=np.int32)
+        max_seq = page * ppr
+        ws_bytes = osc.oscar_decode_workspace_size(gc.cfg, b, max_seq)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        rk, rv, btd, sld = H.dev(fx["R_K"]), H.dev(fx["R_V"]), H.dev(bt), H.dev(slots)
+        appended = []   # exemptions are budgeted over all steps' appended rows
+        for step in range(steps):
+            kn, vn = syn.kv_tokens(wl, 0, b, sub=300 + step)
+            q = syn.queries(wl, 0, b, sub=300 + step, scale=0.5)
+            out = torch.empty((b, shape.n_q_heads, d), dtype=torch.float32, device="cuda")
+            osc.oscar_decode_step(gc.ctx, 0, H.dev_input(kn, "bf16"), H.dev_input(vn, "bf16"), osc.DTYPE_BF16,
+                                  H.dev_input(q, "bf16"), osc.DTYPE_BF16, out, osc.DTYPE_F32, btd, ppr,
+                                  H.dev(np.array(lens, np.int32) + 1), sld, b, max_seq, sink, recent, rk, rv,
+                                  fx["clip_K"], fx["clip_V"], ws, ws_bytes)
+            assert osc.oscar_check_status(gc.ctx) == 0
+            diag = cache.append_step(img, 0, kn, vn, np.array(lens, np.int32), fx["R_K"], fx["R_V"], fx["clip_K"],
+                                     fx["clip_V"], bt, slots)
+            appended.append(H.compare_history(gc.pool_np(), img.g, 0, diag, enforce_budget=False))
+            lens = [n + 1 for n in lens]
+            if step % 7 == 6 or step == steps - 1:
+                gimg = cache.CacheImage(img.g)
+                gimg.pool, gimg.slab = gc.pool_np(), gc.slab_np()
+                want = attention.decode(gimg, 0, q, bt, lens, slots, fx["R_K"], fx["R_V"])
+                H.assert_decode_close(out.cpu().numpy().astype(np.float64), want)
+        H.check_budget(H.merge_results(appended))
+        H.compare_window(gc.slab_np(), img.slab, 0, range(b))
+    finally:
+        gc.close()
+
+
 def test_prefill_plus_appends_matches_direct_prefill_on_gpu(osc):
     wl = syn.Workload("chain", syn.Shape(16, 8, 128, 64, 32, 4, 128, 1), [0], seed=9)
     fx = H.fixture(wl)
