@@ -175,3 +175,51 @@ def test_per_head_rotations_parity(osc, dtype):
         H.assert_decode_close(got, want)
     finally:
         gc.close()
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_per_head_random_requests(osc, seed):
+    """Random shapes (GQA 1-8, d = 64 / 128, pages 16-64, with and without sink, windows 32-128), BF16 or
+    float32 rows, 1-4 requests with distinct per-kv-head rotations: the write against the oracle under the
+    near-boundary rule (window bit-exact), then decode and extend (the unpacked-prefix form) within the
+    decode tolerance of the oracle over the GPU's cache; queries and chunk rows are BF16 values."""
+    rng = np.random.default_rng(13000 + seed)
+    gq, hkv = int(rng.choice([1, 2, 4, 8])), int(rng.choice([2, 4, 8]))
+    d, page = int(rng.choice([64, 128])), int(rng.choice([16, 32, 64]))
+    sink, recent = int(rng.choice([0, 4])), int(rng.choice([32, 64, 128]))
+    dtype = str(rng.choice(["bf16", "f32"]))
+    shape = syn.Shape(gq * hkv, hkv, d, page, 32, sink, recent, 1)
+    b = int(rng.integers(1, 5))
+    lens = [int(x) for x in rng.integers(1, 1500, size=b)]
+    chunks = [int(x) for x in rng.integers(0, 150, size=b)]
+    chunks[int(rng.integers(0, b))] = int(rng.integers(1, 150))
+    wl = syn.Workload("ph_rand", shape, [0], seed=1400 + seed, dtype=dtype)
+    fx = _head_fixture(wl)
+    ppr = max(syn.pages_for(n + c + 1, page) for n, c in zip(lens, chunks)) + 1
+    bt = np.arange(b * ppr, dtype=np.int32).reshape(b, ppr)
+    geom = H.geometry(shape, b * ppr, b)
+    img = cache.CacheImage(geom)
+    gc = H.make_gpu_cache(geom, shape.n_q_heads, ppr, rotation_per_kv_head=1)
+    slots = np.arange(b, dtype=np.int32)
+    try:
+        k, v = _inputs(wl, lens)
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        diag = cache.write_kv(img, 0, k, v, cu, np.zeros(b, np.int32), fx["R_K"], fx["R_V"], fx["clip_K"],
+                              fx["clip_V"], bt, slots)
+        _write(osc, gc, fx, k, v, dtype, lens, [0] * b, bt)
+        H.compare_history(gc.pool_np(), geom, 0, diag)
+        H.compare_window(gc.slab_np(), img.slab, 0, range(b))
+        gimg = cache.CacheImage(geom)
+        gimg.pool, gimg.slab = gc.pool_np(), gc.slab_np()
+        bf = lambda x: syn.as_input(x, "bf16")
+        q = bf(syn.queries(wl, 0, b, sub=41, scale=0.5))
+        got = H.run_decode(gc, 0, q, "bf16", bt, lens, list(range(b)), fx)
+        H.assert_decode_close(got, attention.decode(gimg, 0, q, bt, lens, list(range(b)), fx["R_K"], fx["R_V"]))
+        total = sum(chunks)
+        kx, vx = (bf(x) for x in syn.kv_tokens(wl, 0, total, sub=42))
+        qx = bf(syn.queries(wl, 0, total, sub=43, scale=0.5))
+        cux = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+        gx = H.run_extend(gc, 0, qx, "bf16", kx, vx, cux, lens, bt, slots, fx, unpacked=True)
+        H.assert_decode_close(gx, attention.extend(gimg, 0, qx, kx, vx, cux, lens, bt, slots, fx["R_K"], fx["R_V"]))
+    finally:
+        gc.close()
